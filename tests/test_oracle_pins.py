@@ -1,0 +1,335 @@
+"""Pins for the CPU oracle: checks against what the pages and mathematics fix.
+
+None of these re-types the oracle's own formula: each compares it with a
+library routine (scipy lfilter, torch SDPA / softplus), an unrolled closed
+form, a special case with a known answer, an invariant the pages state
+(rejected drafts never enter the memory; drafting does not change it), or a
+figure the pages print (tests/golden/sizing.json).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import hyflash_oracle as O
+from workload import CONFIGS, make_layer_weights, make_ssm_core_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+TINY = CONFIGS["tiny_fp32"]
+
+
+def small_cfg(**kw):
+    base = dict(d_model=32, n_q_heads=4, n_kv_heads=2, head_dim=8, window=6,
+                ssm_heads=2, ssm_headdim=4, d_state=3, n_layers=1, batch=2,
+                prefix=10, rounds=3, chunk=4)
+    base.update(kw)
+    return TINY.replace(name="pin_small", **base)
+
+
+def ssm_case(T=37, Hm=3, P=4, N=5, seed=0):
+    x, B, dt_raw, A_log = make_ssm_core_inputs(T, Hm, P, N, seed)
+    x, B = x.numpy(), B.numpy()
+    dt = O.softplus(dt_raw.numpy())
+    A = -np.exp(A_log.numpy())
+    return x, B, dt, A
+
+
+def rel(a, b):
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+# ---------------------------------------------------------------- softplus
+
+def test_softplus_closed_values():
+    assert O.softplus(0.0) == pytest.approx(math.log(2.0), rel=1e-15)
+    assert O.softplus(50.0) == pytest.approx(50.0, rel=1e-15)
+    assert O.softplus(-50.0) == pytest.approx(math.exp(-50.0), rel=1e-12)
+    xs = np.linspace(-30, 30, 1001)
+    ref = torch.nn.functional.softplus(torch.tensor(xs, dtype=torch.float64),
+                                       threshold=1e6).numpy()
+    assert np.max(np.abs(O.softplus(xs) - ref)) < 1e-14
+
+
+# ---------------------------------------------------------------- the fold
+
+@pytest.mark.parametrize("chunk", [1, 3, 8, 16, 37, 64, 100])
+def test_chunked_fold_equals_recurrence(chunk):
+    x, B, dt, A = ssm_case(T=37)
+    h0 = np.random.default_rng(1).standard_normal((3, 4, 5))
+    r = O.ssm_fold_recurrent(h0, x, B, dt, A)
+    c = O.ssm_fold_chunked(h0, x, B, dt, A, chunk)
+    assert rel(c, r) < 1e-12
+
+
+def test_fold_unrolled_product_closed_form():
+    # h_T = prod_t a_t h_0 + sum_t dt_t (prod_{s>t} exp(dt_s A)) x_t (x) B_t,
+    # written with explicit scalar loops on a tiny case.
+    x, B, dt, A = ssm_case(T=6, Hm=2, P=3, N=2, seed=3)
+    h0 = np.random.default_rng(2).standard_normal((2, 3, 2))
+    want = np.zeros((2, 3, 2))
+    for hd in range(2):
+        for p in range(3):
+            for n in range(2):
+                total = h0[hd, p, n]
+                for s in range(6):
+                    total *= math.exp(dt[s, hd] * A[hd])
+                for t in range(6):
+                    w = dt[t, hd]
+                    for s in range(t + 1, 6):
+                        w *= math.exp(dt[s, hd] * A[hd])
+                    total += w * x[t, hd, p] * B[t, n]
+                want[hd, p, n] = total
+    got = O.ssm_fold_recurrent(h0, x, B, dt, A)
+    assert rel(got, want) < 1e-13
+
+
+def test_fold_constant_decay_matches_lfilter():
+    signal = pytest.importorskip("scipy.signal")
+    x, B, _, A = ssm_case(T=50, Hm=2, P=3, N=4, seed=5)
+    dt = np.full((50, 2), 0.37)
+    got = O.ssm_fold_recurrent(np.zeros((2, 3, 4)), x, B, dt, A)
+    for hd in range(2):
+        a = math.exp(0.37 * A[hd])
+        for p in range(3):
+            for n in range(4):
+                u = dt[:, hd] * x[:, hd, p] * B[:, n]
+                y = signal.lfilter([1.0], [1.0, -a], u)
+                assert abs(got[hd, p, n] - y[-1]) < 1e-12 * max(1.0, abs(y[-1]))
+
+
+def test_fold_zero_decay_is_plain_sum():
+    x, B, dt, _ = ssm_case(T=20, seed=7)
+    A = np.zeros(3)
+    got = O.ssm_fold_recurrent(np.zeros((3, 4, 5)), x, B, dt, A)
+    want = np.zeros((3, 4, 5))
+    for t in range(20):
+        want += dt[t][:, None, None] * np.multiply.outer(x[t], B[t]).reshape(3, 4, 5)
+    assert rel(got, want) < 1e-13
+
+
+def test_fold_huge_decay_keeps_last_token_only():
+    x, B, dt, _ = ssm_case(T=9, seed=8)
+    A = np.full(3, -1e9)
+    got = O.ssm_fold_recurrent(np.ones((3, 4, 5)), x, B, dt, A)
+    want = dt[-1][:, None, None] * x[-1][:, :, None] * B[-1][None, None, :]
+    assert rel(got, want) < 1e-15
+
+
+def test_fold_dt_zero_leaves_state_bit_identical():
+    x, B, _, A = ssm_case(T=11, seed=9)
+    h0 = np.random.default_rng(4).standard_normal((3, 4, 5))
+    got = O.ssm_fold_recurrent(h0, x, B, np.zeros((11, 3)), A)
+    assert np.array_equal(got, h0)
+
+
+def test_outer_product_orientation_and_read():
+    # one token, h0 = 0, x = e_p0, B = e_n0 -> only h[:, p0, n0] = dt
+    x = np.zeros((1, 2, 4)); x[0, :, 1] = 1.0
+    B = np.zeros((1, 5)); B[0, 3] = 1.0
+    dt = np.array([[0.5, 0.25]])
+    h = O.ssm_fold_recurrent(np.zeros((2, 4, 5)), x, B, dt, np.array([-1.0, -2.0]))
+    want = np.zeros((2, 4, 5)); want[0, 1, 3] = 0.5; want[1, 1, 3] = 0.25
+    assert np.array_equal(h, want)
+    # read: one-hot C selects column n0 of every head's state
+    hr = np.random.default_rng(0).standard_normal((2, 4, 5))
+    C = np.zeros((2, 5)); C[0, 3] = 1.0; C[1, 0] = 2.0
+    y = O.ssm_read(hr, C)
+    assert np.array_equal(y[0], hr[:, :, 3]) and np.array_equal(y[1], 2.0 * hr[:, :, 0])
+
+
+def test_ssm_inputs_use_softplus_and_bias():
+    cfg = small_cfg()
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    f = np.random.default_rng(3).standard_normal((5, cfg.d_model))
+    x, B, dt = O.ssm_inputs(lw, cfg, f)
+    tf = torch.tensor(f)
+    ref_dt = torch.nn.functional.softplus(tf @ torch.tensor(lw.w_dt) + torch.tensor(lw.dt_bias),
+                                          threshold=1e6).numpy()
+    assert rel(dt, ref_dt) < 1e-14
+    assert x.shape == (5, cfg.ssm_heads, cfg.ssm_headdim) and B.shape == (5, cfg.d_state)
+    assert np.all(lw.A < 0)
+
+
+# ---------------------------------------------------------------- ring
+
+def test_ring_matches_bruteforce_last_window():
+    cfg = small_cfg(window=5)
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(11)
+    history = []  # every committed feature row, in order
+    feats0 = rng.standard_normal((3, cfg.d_model))
+    ctx = O.prefill_layer(lw, cfg, feats0)
+    history += list(feats0)
+    for _ in range(12):
+        rows = rng.standard_normal((8, cfg.d_model))
+        n = int(rng.integers(0, 9))
+        ctx = O.commit_layer(lw, cfg, ctx, rows, n)
+        history += list(rows[:n])
+        T = len(history)
+        assert ctx.pos == T
+        last = list(range(max(0, T - cfg.window), T))
+        for s in range(cfg.window):
+            holders = [p for p in last if p % cfg.window == s]
+            if holders:
+                p = holders[0]
+                assert ctx.tag[s] == p
+                k, _ = O.kv_of(lw, cfg, np.asarray(history[p])[None])
+                assert np.allclose(ctx.ring_k[:, s, :], k[0], rtol=0, atol=1e-13)
+            else:
+                assert ctx.tag[s] == -1
+
+
+# ---------------------------------------------------------------- commit invariants
+
+def test_commit_zero_and_rejected_rows():
+    cfg = small_cfg()
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(12)
+    ctx = O.prefill_layer(lw, cfg, rng.standard_normal((9, cfg.d_model)))
+    rows = rng.standard_normal((8, cfg.d_model))
+    z = O.commit_layer(lw, cfg, ctx, rows, 0)
+    assert np.array_equal(z.h, ctx.h) and np.array_equal(z.ring_k, ctx.ring_k) and z.pos == ctx.pos
+    for n in range(1, 9):
+        a = O.commit_layer(lw, cfg, ctx, rows, n)
+        rows2 = rows.copy()
+        rows2[n:] = rng.standard_normal((8 - n, cfg.d_model)) * 100.0
+        b = O.commit_layer(lw, cfg, ctx, rows2, n)
+        assert np.array_equal(a.h, b.h) and np.array_equal(a.ring_k, b.ring_k)
+        assert np.array_equal(a.ring_v, b.ring_v) and a.pos == b.pos
+
+
+def test_split_commit_equals_single_and_prefill():
+    cfg = small_cfg(window=4)
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(13)
+    pre = rng.standard_normal((7, cfg.d_model))
+    rows = rng.standard_normal((8, cfg.d_model))
+    base = O.prefill_layer(lw, cfg, pre, method="recurrent")
+    one = O.commit_layer(lw, cfg, base, rows, 7)
+    two = O.commit_layer(lw, cfg, O.commit_layer(lw, cfg, base, rows[:3], 3), rows[3:], 4)
+    assert rel(two.h, one.h) < 1e-13 and np.array_equal(two.tag, one.tag)
+    assert np.array_equal(two.ring_k, one.ring_k)
+    full = O.prefill_layer(lw, cfg, np.concatenate([pre, rows[:7]]), method="chunked", chunk=3)
+    assert rel(full.h, one.h) < 1e-12 and np.array_equal(full.tag, one.tag)
+    assert np.allclose(full.ring_v, one.ring_v, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- attention
+
+def test_window_covering_prefix_equals_full_attention_sdpa():
+    cfg = small_cfg(window=64)
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(14)
+    pre = rng.standard_normal((23, cfg.d_model))
+    ctx = O.prefill_layer(lw, cfg, pre)
+    X = rng.standard_normal((7, cfg.d_model))
+    _, parts = O.draft_layer(lw, cfg, ctx, X, return_parts=True)
+    kp, vp = O.kv_of(lw, cfg, pre)
+    keys = np.concatenate([kp, parts["Ks"]], 0)       # [L+7, Hkv, dh]
+    vals = np.concatenate([vp, parts["Vs"]], 0)
+    q = torch.tensor(parts["Q"]).permute(1, 0, 2)[None]   # [1, Hq, 7, dh]
+    k = torch.tensor(keys).permute(1, 0, 2)[None]
+    v = torch.tensor(vals).permute(1, 0, 2)[None]
+    G = cfg.n_q_heads // cfg.n_kv_heads
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q, k.repeat_interleave(G, dim=1), v.repeat_interleave(G, dim=1))
+    ref = ref[0].permute(1, 0, 2).numpy()
+    assert rel(parts["O"], ref) < 1e-13
+
+
+def test_equal_keys_give_mean_of_values():
+    cfg = small_cfg(window=8)
+    ctx = O.Context.empty(cfg)
+    rng = np.random.default_rng(15)
+    k = np.tile(rng.standard_normal((1, cfg.n_kv_heads, cfg.head_dim)), (5, 1, 1))
+    v = rng.standard_normal((5, cfg.n_kv_heads, cfg.head_dim))
+    O.ring_append(ctx, cfg, k, v, 0)
+    ctx.pos = 5
+    Q = rng.standard_normal((7, cfg.n_q_heads, cfg.head_dim))
+    Ks = np.tile(k[:1], (7, 1, 1))
+    Vs = rng.standard_normal((7, cfg.n_kv_heads, cfg.head_dim))
+    out = O.window_block_attention(cfg, ctx, Q, Ks, Vs)
+    G = cfg.n_q_heads // cfg.n_kv_heads
+    for hq in range(cfg.n_q_heads):
+        mean = np.concatenate([v[:, hq // G], Vs[:, hq // G]]).mean(0)
+        assert np.allclose(out[:, hq], mean[None], rtol=0, atol=1e-14)
+
+
+def test_empty_window_attends_slots_only():
+    cfg = small_cfg()
+    ctx = O.Context.empty(cfg)
+    ctx.ring_k[:] = 1e3  # garbage in unused slots must not be read
+    rng = np.random.default_rng(16)
+    Q = rng.standard_normal((7, cfg.n_q_heads, cfg.head_dim))
+    Ks = rng.standard_normal((7, cfg.n_kv_heads, cfg.head_dim))
+    Vs = rng.standard_normal((7, cfg.n_kv_heads, cfg.head_dim))
+    out = O.window_block_attention(cfg, ctx, Q, Ks, Vs)
+    q = torch.tensor(Q).permute(1, 0, 2)[None]
+    G = cfg.n_q_heads // cfg.n_kv_heads
+    k = torch.tensor(Ks).permute(1, 0, 2)[None].repeat_interleave(G, dim=1)
+    v = torch.tensor(Vs).permute(1, 0, 2)[None].repeat_interleave(G, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v)[0].permute(1, 0, 2).numpy()
+    assert rel(out, ref) < 1e-13
+
+
+# ---------------------------------------------------------------- layer output
+
+def test_layer_output_composition():
+    cfg = small_cfg()
+    w = make_layer_weights(cfg, 0)
+    lw = O.Weights64.from_any(w)
+    rng = np.random.default_rng(17)
+    ctx = O.prefill_layer(lw, cfg, rng.standard_normal((9, cfg.d_model)))
+    X = rng.standard_normal((7, cfg.d_model))
+    # zero output projections: the layer is the identity on the residual
+    lz = O.Weights64(**{**lw.__dict__, "w_o": np.zeros_like(lw.w_o), "w_mo": np.zeros_like(lw.w_mo)})
+    assert np.array_equal(O.draft_layer(lz, cfg, ctx, X), X)
+    # only the memory branch: out - X = y W_mo with y the one-hot-checked read
+    lm = O.Weights64(**{**lw.__dict__, "w_o": np.zeros_like(lw.w_o)})
+    out = O.draft_layer(lm, cfg, ctx, X)
+    y = torch.einsum("hpn,sn->shp", torch.tensor(ctx.h), torch.tensor(X) @ torch.tensor(lw.w_C))
+    ref = (y.reshape(7, -1) @ torch.tensor(lw.w_mo)).numpy()
+    assert rel(out - X, ref) < 1e-10  # out - X cancels against |X| ~ 1
+
+
+def test_draft_leaves_context_unchanged():
+    cfg = small_cfg()
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(18)
+    ctx = O.prefill_layer(lw, cfg, rng.standard_normal((9, cfg.d_model)))
+    before = ctx.clone()
+    O.draft_layer(lw, cfg, ctx, rng.standard_normal((7, cfg.d_model)))
+    assert np.array_equal(before.h, ctx.h) and np.array_equal(before.ring_k, ctx.ring_k)
+    assert np.array_equal(before.tag, ctx.tag) and before.pos == ctx.pos
+
+
+def test_batched_drafter_invalid_count_is_noop_and_flagged():
+    cfg = small_cfg()
+    w = [make_layer_weights(cfg, 0)]
+    d = O.OracleDrafter(cfg, w, 3)
+    rng = np.random.default_rng(19)
+    d.prefill([5, 0, 12], rng.standard_normal((17, cfg.d_model)))
+    snap = [c[0].clone() for c in d.ctx]
+    offs, err = d.commit(rng.standard_normal((3, 8, cfg.d_model)), [3, 9, 8])
+    assert err and list(offs) == [0, 3, 3, 11]
+    assert np.array_equal(d.ctx[1][0].h, snap[1].h) and d.ctx[1][0].pos == 0
+    assert d.ctx[0][0].pos == 8 and d.ctx[2][0].pos == 20
+
+
+# ---------------------------------------------------------------- sizing (pages' figures)
+
+def test_sizing_matches_printed_figures():
+    g = json.load(open(os.path.join(GOLDEN, "sizing.json")))
+    t = g["target_kv_32k"]
+    assert O.target_kv_bytes(t["n_layers"], t["n_kv_heads"], t["head_dim"], t["seq"],
+                             t["elem_bytes"]) == t["bytes"] == int(6.25 * 2**30)
+    k = g["drafter_window_kv"]
+    kv = O.window_kv_bytes(k["n_layers"], k["n_kv_heads"], k["head_dim"], k["window"], k["elem_bytes"])
+    assert kv == k["bytes"] == int(2.5 * 2**20)
+    s = g["drafter_state"]
+    st = O.state_bytes(s["n_layers"], s["d_inner"], s["d_state"], s["elem_bytes"])
+    assert st == s["bytes"] == int(2.5 * 2**20)
+    assert kv + st == g["drafter_context_total"]["bytes"]

@@ -1,0 +1,211 @@
+"""Synthetic workloads shaped like the HyFlash drafter configurations.
+
+Sources for the shapes and laws (HyFlash: A Prefix-Memory Prior for On-Device
+Speculative Decoding, and the learnaivisually explainer of it, "That is
+HyFlash" and "Where it earns its keep" sections):
+  * one drafter layer = local attention over the most recent committed target
+    features plus the 7 draft slots, and a Mamba-2 recurrent memory;
+  * block of 7 draft positions; accepted counts per round 1..8 (7 drafts plus
+    the target's bonus token).
+
+Distributions (stated with the workloads): features and slot embeddings
+~N(0,1); projection weights ~N(0, 0.02); dt = softplus(N(0,1) - 2) obtained
+through W_dt with std 1/sqrt(D) and dt_bias = -2; A = -exp(U(0,1)) through
+A_log ~ U(0,1); B, C ~ N(0, 1/16) (1/16 read as a standard deviation) through
+W_B, W_C with std (1/16)/sqrt(D).
+
+Everything is drawn with torch's CPU generator so that the exact same bytes can
+be handed to the GPU path and to the oracle. bf16 configurations round once
+to bfloat16 here; both sides then consume those rounded values.
+"""
+from __future__ import annotations
+
+import dataclasses
+import hashlib
+import math
+from typing import Optional, Sequence
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class DrafterShape:
+    name: str
+    d_model: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    window: int
+    block: int
+    ssm_heads: int
+    ssm_headdim: int
+    d_state: int
+    n_layers: int
+    batch: int
+    prefix: int            # prefix length for batch configs with a single length
+    rounds: int
+    dtype: str             # "f32" or "bf16"
+    chunk: int = 128
+    n_groups: int = 1
+    prefix_lo: int = 0     # log-uniform prefix range (serving batch)
+    prefix_hi: int = 0
+
+    @property
+    def d_inner(self) -> int:
+        return self.ssm_heads * self.ssm_headdim
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def replace(self, **kw) -> "DrafterShape":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads, in the order they are listed with the baseline metric.
+CONFIGS = {
+    "tiny_fp32": DrafterShape(
+        name="tiny_fp32", d_model=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+        window=64, block=7, ssm_heads=4, ssm_headdim=64, d_state=16,
+        n_layers=1, batch=1, prefix=512, rounds=20, dtype="f32"),
+    "qwen3_4b_bf16": DrafterShape(
+        name="qwen3_4b_bf16", d_model=2560, n_q_heads=32, n_kv_heads=8,
+        head_dim=128, window=512, block=7, ssm_heads=80, ssm_headdim=64,
+        d_state=128, n_layers=1, batch=1, prefix=8192, rounds=200,
+        dtype="bf16"),
+    "phi4_bf16": DrafterShape(
+        name="phi4_bf16", d_model=5120, n_q_heads=40, n_kv_heads=10,
+        head_dim=128, window=512, block=7, ssm_heads=160, ssm_headdim=64,
+        d_state=128, n_layers=1, batch=1, prefix=32768, rounds=200,
+        dtype="bf16"),
+    "serving_qwen3_4b_b64": DrafterShape(
+        name="serving_qwen3_4b_b64", d_model=2560, n_q_heads=32, n_kv_heads=8,
+        head_dim=128, window=512, block=7, ssm_heads=80, ssm_headdim=64,
+        d_state=128, n_layers=3, batch=64, prefix=0, rounds=500,
+        dtype="bf16", prefix_lo=2048, prefix_hi=32768),
+    "prefill_phi4_sweep": DrafterShape(
+        name="prefill_phi4_sweep", d_model=5120, n_q_heads=40, n_kv_heads=10,
+        head_dim=128, window=512, block=7, ssm_heads=160, ssm_headdim=64,
+        d_state=128, n_layers=1, batch=8, prefix=4096, rounds=0,
+        dtype="bf16", chunk=128),
+}
+CONFIG_ORDER = list(CONFIGS)
+
+
+def rng(*key) -> torch.Generator:
+    """A CPU generator seeded from a stable hash of ``key``."""
+    h = hashlib.sha256(repr(key).encode()).digest()
+    return torch.Generator().manual_seed(int.from_bytes(h[:8], "little") & ((1 << 63) - 1))
+
+
+def _round(t: torch.Tensor, cfg: DrafterShape) -> torch.Tensor:
+    return t.to(cfg.torch_dtype).contiguous()
+
+
+@dataclasses.dataclass
+class LayerWeightsT:
+    """Per-layer weights, row-major [in, out]; dt_bias and A_log stay fp32."""
+    w_q: torch.Tensor
+    w_k: torch.Tensor
+    w_v: torch.Tensor
+    w_o: torch.Tensor
+    w_x: torch.Tensor
+    w_B: torch.Tensor
+    w_C: torch.Tensor
+    w_dt: torch.Tensor
+    w_mo: torch.Tensor
+    dt_bias: torch.Tensor
+    A_log: torch.Tensor
+
+    FIELDS = ("w_q", "w_k", "w_v", "w_o", "w_x", "w_B", "w_C", "w_dt", "w_mo",
+              "dt_bias", "A_log")
+
+
+def make_layer_weights(cfg: DrafterShape, layer: int, seed: int = 0) -> LayerWeightsT:
+    g = rng("weights", cfg.name, seed, layer)
+    D, hq, hkv, dh = cfg.d_model, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    din, N, Hm = cfg.d_inner, cfg.d_state, cfg.ssm_heads
+
+    def n(shape, std):
+        return _round(torch.randn(shape, generator=g) * std, cfg)
+
+    return LayerWeightsT(
+        w_q=n((D, hq * dh), 0.02),
+        w_k=n((D, hkv * dh), 0.02),
+        w_v=n((D, hkv * dh), 0.02),
+        w_o=n((hq * dh, D), 0.02),
+        w_x=n((D, din), 0.02),
+        w_B=n((D, N), (1.0 / 16.0) / math.sqrt(D)),
+        w_C=n((D, N), (1.0 / 16.0) / math.sqrt(D)),
+        w_dt=n((D, Hm), 1.0 / math.sqrt(D)),
+        w_mo=n((din, D), 0.02),
+        dt_bias=torch.full((Hm,), -2.0, dtype=torch.float32),
+        A_log=torch.rand((Hm,), generator=g, dtype=torch.float32),
+    )
+
+
+def make_prefix_lens(cfg: DrafterShape, seed: int = 0) -> list:
+    """Per-request prefix lengths: fixed, or log-uniform in [lo, hi]."""
+    if cfg.prefix_lo:
+        g = rng("lens", cfg.name, seed)
+        u = torch.rand((cfg.batch,), generator=g, dtype=torch.float64)
+        lo, hi = math.log(cfg.prefix_lo), math.log(cfg.prefix_hi)
+        return [int(math.floor(math.exp(lo + (hi - lo) * float(x)))) for x in u]
+    return [cfg.prefix] * cfg.batch
+
+
+def make_prefix_feats(cfg: DrafterShape, lens: Sequence[int], seed: int = 0,
+                      request_offset: int = 0) -> torch.Tensor:
+    """Packed committed target features [sum(lens), D] ~ N(0,1).
+
+    Each request draws from its own stream, so a subset of requests can be
+    regenerated on its own (``request_offset`` names the first request).
+    """
+    parts = []
+    for i, L in enumerate(lens):
+        g = rng("prefix", cfg.name, seed, request_offset + i)
+        parts.append(torch.randn((L, cfg.d_model), generator=g))
+    if not parts:
+        return torch.zeros((0, cfg.d_model), dtype=cfg.torch_dtype)
+    return _round(torch.cat(parts, 0), cfg)
+
+
+def make_round_inputs(cfg: DrafterShape, rnd: int, batch: Optional[int] = None,
+                      seed: int = 0):
+    """Slot embeddings [B, 7, D] and commit features [B, 8, D] for one round.
+
+    All 8 commit rows are filled; rows at or beyond the accepted count stand for
+    rejected drafts and must never influence anything.
+    """
+    B = cfg.batch if batch is None else batch
+    g = rng("round", cfg.name, seed, rnd)
+    slot = torch.randn((B, cfg.block, cfg.d_model), generator=g)
+    feats = torch.randn((B, cfg.block + 1, cfg.d_model), generator=g)
+    return _round(slot, cfg), _round(feats, cfg)
+
+
+def make_accepted(cfg: DrafterShape, rnd: int, batch: Optional[int] = None,
+                  seed: int = 0) -> torch.Tensor:
+    """Accepted counts per request, uniform integers in 1..block+1 (int32)."""
+    B = cfg.batch if batch is None else batch
+    g = rng("accepted", cfg.name, seed, rnd)
+    return torch.randint(1, cfg.block + 2, (B,), generator=g, dtype=torch.int32)
+
+
+def make_ssm_core_inputs(T: int, Hm: int, P: int, N: int, seed: int = 0):
+    """Direct SSM inputs with the workload laws: x ~ N(0,1), B ~ N(0,1/16),
+    dt = softplus(N(0,1) - 2) drawn as its pre-activation, A_log ~ U(0,1).
+
+    Returns (x [T,Hm,P], B [T,N], dt_raw [T,Hm], A_log [Hm]) as float64 tensors;
+    the caller applies softplus (the method's arithmetic) itself.
+    """
+    g = rng("ssm_core", T, Hm, P, N, seed)
+    x = torch.randn((T, Hm, P), generator=g, dtype=torch.float64)
+    B = torch.randn((T, N), generator=g, dtype=torch.float64) / 16.0
+    dt_raw = torch.randn((T, Hm), generator=g, dtype=torch.float64) - 2.0
+    A_log = torch.rand((Hm,), generator=g, dtype=torch.float64)
+    return x, B, dt_raw, A_log
