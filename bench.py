@@ -1,0 +1,465 @@
+"""Benchmark of the HyFlash drafter hot path on one GB300 (or N replicas).
+
+A step is one speculative round on device-resident inputs: hf_draft (all
+layers: slot projections, window+block attention, memory read, output
+projections) followed by hf_commit (count check, projections, ring append,
+sequential memory update) for every request of the batch. The prefix is
+folded once beforehand with hf_prefill, which is timed on its own and
+reported under "prefill".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--impl hyflash|reference]
+
+Multi-GPU (torchrun, one rank per GPU): each rank runs an independent replica
+with its own requests (weak scaling, no collective on the data path); the
+barrier/max-over-ranks timing is the only communication.
+
+--impl reference times the float64 CPU oracle (plain NumPy, as it stands) on
+the host cores for the same metric: there is no other implementation of this
+method to run.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "drafter draft-steps/s and committed tokens/s at 1 GB300; % of HBM/tensor roofline"
+UNIT = "draft-steps/s"
+DEFAULT_CONFIG = "qwen3_4b_bf16"
+
+
+# ------------------------------------------------------------------ distributed helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ algorithmic sizes
+
+def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float):
+    """Bytes and flops each step must move/do at minimum (weights, window,
+    state and slot I/O read or written once)."""
+    e = cfg.elem_bytes
+    D, hq, hkv, dh, W = cfg.d_model, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.window
+    din, N, Hm, P, S, L = cfg.d_inner, cfg.d_state, cfg.ssm_heads, cfg.ssm_headdim, cfg.block, cfg.n_layers
+    Nd = hq * dh + 2 * hkv * dh + N
+    Nz = hq * dh + din
+    Nc = 2 * hkv * dh + din + N + Hm
+    R = batch * S
+    nv = window_fill  # valid ring entries per request
+    fam = {}
+    # per launch (one layer) of each kernel family
+    fam["draft_proj"] = e * Nd * D + e * R * D + 4 * R * Nd
+    fam["out_proj"] = e * D * Nz + e * R * Nz + 2 * e * R * D
+    fam["attn_mem"] = (batch * (nv * 2 * hkv * dh * e + Hm * P * N * 4)
+                       + 4 * R * Nd + e * R * Nz)
+    rows = batch * mean_accept
+    fam["commit_proj"] = (e * L * Nc * D + e * rows * D
+                          + L * rows * (2 * hkv * dh * e + (din + N + Hm) * 4))
+    fam["commit_state"] = L * (batch * Hm * P * N * 8 + rows * (din + N + Hm) * 4)
+    draft = L * (fam["draft_proj"] + fam["out_proj"] + fam["attn_mem"])
+    commit = fam["commit_proj"] + fam["commit_state"]
+    flops = L * 2 * R * D * (Nd + Nz) + 2 * rows * D * L * Nc
+    return {"per_launch": fam, "draft_bytes": draft, "commit_bytes": commit,
+            "step_bytes": draft + commit, "step_flops": flops}
+
+
+def prefill_flops(cfg, total_tokens: int, ring_rows: int) -> float:
+    D, din, N, Hm, P = cfg.d_model, cfg.d_inner, cfg.d_state, cfg.ssm_heads, cfg.ssm_headdim
+    kvd = cfg.n_kv_heads * cfg.head_dim
+    per_tok = 2 * D * (din + N + Hm) + 2 * Hm * P * N
+    return cfg.n_layers * (total_tokens * per_tok + ring_rows * 2 * D * 2 * kvd)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_rounds(cfg, batch: int, steps: int, warmup: int, budget_s: float, seed: int = 0):
+    """Time the float64 oracle on host cores: prefill untimed, then rounds of
+    draft + commit; stops early after budget_s seconds of timed work."""
+    from oracle import hyflash_oracle as O
+    from workload import (make_accepted, make_layer_weights, make_prefix_feats,
+                          make_prefix_lens, make_round_inputs)
+    weights = [make_layer_weights(cfg, l) for l in range(cfg.n_layers)]
+    orc = O.OracleDrafter(cfg, weights, batch)
+    lens = make_prefix_lens(cfg)[:batch]
+    orc.prefill(lens, make_prefix_feats(cfg, lens, seed=seed))
+    for r in range(warmup):
+        slot, feats = make_round_inputs(cfg, r, batch, seed=seed)
+        orc.draft(slot)
+        orc.commit(feats, make_accepted(cfg, r, batch, seed=seed).numpy())
+    done, accepted, t_total = 0, 0, 0.0
+    for r in range(warmup, warmup + steps):
+        slot, feats = make_round_inputs(cfg, r, batch, seed=seed)
+        n = make_accepted(cfg, r, batch, seed=seed).numpy()
+        t0 = time.perf_counter()
+        orc.draft(slot)
+        orc.commit(feats, n)
+        t_total += time.perf_counter() - t0
+        done += 1
+        accepted += int(n.sum())
+        if t_total > budget_s:
+            break
+    return done, accepted, t_total
+
+
+def run_reference(args, cfg):
+    ws, rank = dist_init("gloo")
+    if rank != 0:
+        return 0
+    batch = cfg.batch
+    budget = float(os.environ.get("HF_REF_BUDGET_S", "120"))
+    done, acc, t = oracle_rounds(cfg, batch, args.steps, args.warmup, budget)
+    v = done / t if t > 0 else 0.0
+    sample = (f"{done} of {args.steps} requested rounds (draft+commit) of {cfg.name}, batch {batch}, "
+              f"after an untimed oracle prefill and {args.warmup} untimed warm-up rounds")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * t / max(done, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "committed_tokens_per_s": acc / t if t > 0 else 0.0,
+        "config": {"workload": cfg.name, "batch": batch, "prefix": cfg.prefix,
+                   "layers": cfg.n_layers, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_hyflash(args, cfg):
+    import torch
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+
+    from speculative_decoding_drafter_hf_gb300 import build as _b
+    _b.build()
+    import speculative_decoding_drafter_hf_gb300 as hf
+    from workload import (make_accepted, make_layer_weights, make_prefix_feats, make_prefix_lens,
+                          make_round_inputs)
+
+    batch = cfg.batch
+    seed = rank  # each replica drafts for its own requests
+    drafter = hf.Drafter(cfg, batch, device=local)
+    for l in range(cfg.n_layers):
+        drafter.set_weights(l, make_layer_weights(cfg, l))
+    lens = make_prefix_lens(cfg, seed=0)[:batch]
+    total = sum(lens)
+    feats = make_prefix_feats(cfg, lens, seed=seed).to(dev)
+    stream = torch.cuda.current_stream()
+
+    # ---- prefill (one warm-up, then timed)
+    drafter.prefill(feats, lens)
+    drafter.sync()
+    pf_times = []
+    for _ in range(2):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        drafter.prefill(feats, lens)
+        b.record(stream)
+        b.synchronize()
+        pf_times.append(a.elapsed_time(b))
+    drafter.sync()
+    pf_ms = min(pf_times)
+    ring_rows = sum(min(L, cfg.window) for L in lens)
+    pf_flops = prefill_flops(cfg, total, ring_rows)
+    del feats
+
+    # ---- per-round inputs, resident on the device
+    nsteps = args.warmup + args.steps
+    slots, commits, counts = [], [], []
+    for r in range(nsteps):
+        s, f = make_round_inputs(cfg, r, batch, seed=seed)
+        slots.append(s)
+        commits.append(f)
+        counts.append(make_accepted(cfg, r, batch, seed=seed))
+    d_slot = torch.stack(slots).to(dev)
+    d_feat = torch.stack(commits).to(dev)
+    d_cnt = torch.stack(counts).to(dev)
+    out = torch.empty((batch, cfg.block, cfg.d_model), dtype=drafter.torch_dtype, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    def step(r):
+        drafter.draft(d_slot[r], out)
+        drafter.commit(d_feat[r], d_cnt[r])
+
+    for r in range(args.warmup):
+        step(r)
+    drafter.sync()
+
+    # ---- timed region: per-step events, L2 flushed between steps (untimed)
+    drafter.profile(True)
+    for fam in hf.Family:
+        drafter.profile_read(fam, reset=True)
+    launches0 = drafter.launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step(args.warmup + i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    drafter.sync()
+    launches = drafter.launch_count() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    fam_ms = {}
+    for fam in hf.Family:
+        ms, n = drafter.profile_read(fam, reset=True)
+        fam_ms[fam.name.lower()] = (ms, n)
+    drafter.profile(False)
+    accepted = int(d_cnt[args.warmup:].sum().item())
+    total_ms_max = max_over_ranks(total_ms, dev)
+    all_steps = sum_over_ranks(args.steps, dev)
+    all_acc = sum_over_ranks(accepted, dev)
+    value = all_steps / (total_ms_max / 1e3)
+
+    # ---- e2e: the same rounds from pinned host buffers, copies inside the timed region
+    h_slot = d_slot.cpu().pin_memory()
+    h_feat = d_feat.cpu().pin_memory()
+    h_cnt = d_cnt.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    b_slot = torch.empty_like(d_slot[0])
+    b_feat = torch.empty_like(d_feat[0])
+    b_cnt = torch.empty_like(d_cnt[0])
+    e2e_ev = []
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        r = args.warmup + i
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        b_slot.copy_(h_slot[r], non_blocking=True)
+        b_feat.copy_(h_feat[r], non_blocking=True)
+        b_cnt.copy_(h_cnt[r], non_blocking=True)
+        drafter.draft(b_slot, out)
+        drafter.commit(b_feat, b_cnt)
+        h_out.copy_(out, non_blocking=True)
+        b.record(stream)
+        e2e_ev.append((a, b))
+    torch.cuda.synchronize()
+    barrier()
+    drafter.sync()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), dev)
+    e2e_value = all_steps / (e2e_ms / 1e3)
+    es = drafter.np_elem
+    h2d = (h_slot[0].numel() + h_feat[0].numel()) * es + h_cnt[0].numel() * 4
+    d2h = h_out.numel() * es
+
+    # ---- roofline of the dominant kernel family
+    import json as _json
+    peaks = {}
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        peaks = _json.load(open(pp))
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    tc_peak = float(peaks.get("bf16_tflops", 1900.0))
+    peak_src = "measured" if peaks else "fallback"
+    fill = min(cfg.prefix, cfg.window)
+    alg = algorithmic(cfg, batch, fill, (cfg.block + 2) / 2.0)
+    fam_bytes = {"draft_proj": alg["per_launch"]["draft_proj"],
+                 "out_proj": alg["per_launch"]["out_proj"],
+                 "attn_mem": alg["per_launch"]["attn_mem"],
+                 "commit_proj": alg["per_launch"]["commit_proj"],
+                 "commit_state": alg["per_launch"]["commit_state"]}
+    top = max(fam_bytes, key=lambda k: fam_ms.get(k, (0, 0))[0])
+    ms_top, n_top = fam_ms[top]
+    # one profiled scope per layer (draft families) or per call (commit families)
+    scopes = args.steps * (cfg.n_layers if top in ("draft_proj", "out_proj", "attn_mem") else 1)
+    avg_ms = ms_top / max(scopes, 1)
+    achieved = fam_bytes[top] / (avg_ms / 1e3) / 1e9 if avg_ms > 0 else 0.0
+    roofline = {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": hbm_peak,
+                "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": fam_bytes[top], "avg_launch_ms": avg_ms}
+
+    # ---- CPU oracle beside it (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        budget = float(os.environ.get("HF_CPU_BUDGET_S", "20"))
+        done, acc, t = oracle_rounds(cfg, batch, args.steps, 1, budget)
+        cpu = {"value": done / t if t > 0 else 0.0, "unit": UNIT, "cores": cpu_cores(),
+               "kind": "oracle",
+               "sample": f"{done} rounds (draft+commit) of {cfg.name}, batch {batch}, float64 NumPy, "
+                         f"after an untimed oracle prefill and 1 warm-up round"}
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.dtype, "data": "synthetic",
+            "config": {"workload": cfg.name, "batch_per_gpu": batch, "prefix": cfg.prefix,
+                       "layers": cfg.n_layers, "window": cfg.window, "block": cfg.block,
+                       "l2": f"flushed between steps ({2 * l2 >> 20} MiB write, untimed)",
+                       "parallelism": f"replicas x{ws}"},
+            "committed_tokens_per_s": all_acc / (total_ms_max / 1e3),
+            "step_ms_median": statistics.median(step_ms),
+            "algorithmic": {"step_bytes": alg["step_bytes"], "draft_bytes": alg["draft_bytes"],
+                            "commit_bytes": alg["commit_bytes"],
+                            "step_hbm_frac": alg["step_bytes"] / (total_ms / args.steps / 1e3) / 1e9 / hbm_peak},
+            "kernels_ms_per_step": {k: v[0] / args.steps for k, v in fam_ms.items() if v[1]},
+            "roofline": roofline,
+            "prefill": {"tokens": total, "ms": pf_ms, "tokens_per_s": total / (pf_ms / 1e3),
+                        "tflops": pf_flops / (pf_ms / 1e3) / 1e12,
+                        "tensor_frac": pf_flops / (pf_ms / 1e3) / 1e12 / tc_peak},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": int(launches),
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    drafter.close()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="hyflash", choices=["hyflash", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from workload import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_hyflash(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

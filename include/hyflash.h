@@ -1,0 +1,228 @@
+/*
+ * hyflash.h -- C ABI of the HyFlash drafter-layer library (GB300, sm_103a).
+ *
+ * What the library computes ("HyFlash: A Prefix-Memory Prior for On-Device
+ * Speculative Decoding", abstract; learnaivisually explainer "HyFlash lifts
+ * on-device speculative decoding 16.2%", paragraph "That is HyFlash" and FAQ
+ * "Why does the memory update only from committed features?"):
+ *
+ *   Each drafter layer has two branches. Local attention lets the 7 draft-slot
+ *   queries attend, in both directions, over a sliding window of the most
+ *   recent committed target features and over all draft slots. A Mamba-2
+ *   recurrent memory folds committed target features into a fixed-size state
+ *     h_t = exp(dt_t * A) * h_{t-1} + dt_t * x_t (outer) B_t,   y = C . h
+ *   (dt = softplus(f W_dt + dt_bias), A = -exp(A_log)); drafting only reads
+ *   it, and only features the target committed ever write it.
+ *
+ *   prefill : fold a committed prefix into the memory, fill the window.
+ *   commit  : append the accepted features of one verification round to the
+ *             window ring and advance the memory over them, in order.
+ *   draft   : run the layers for the 7 slot embeddings; read-only.
+ *
+ * Readings where the pages are silent (the oracle states the same ones):
+ * out = X + O W_o + y W_mo (two branches summed into the residual, no norms,
+ * RoPE, MLP, conv1d, gate or skip); the draft-time memory query is
+ * C_s = X_s W_C; window K/V and memory inputs are projections of the
+ * committed target features by the layer's own weights; one SSM group;
+ * softmax scale 1/sqrt(head_dim); a slot attends to its own key too; GQA
+ * maps query head h to KV head h / (n_q_heads / n_kv_heads); committed
+ * position t lives in ring slot t mod window.
+ *
+ * Conventions for every call below:
+ *   - "device" pointers are CUDA global-memory addresses on the handle's
+ *     device, "host" pointers are ordinary CPU memory. The caller owns every
+ *     buffer it passes; the library owns the window rings, recurrent states,
+ *     positions, weights and its scratch.
+ *   - Matrices are row-major. Element type of features, slot embeddings,
+ *     outputs and weights is the handle's dtype (fp32 or bf16);
+ *     dt_bias and A_log are always fp32; the recurrent state is always fp32.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued asynchronously; nothing here synchronises the
+ *     host unless its comment says so.
+ *   - Errors found on the host return at once and change nothing. Errors
+ *     found on the device (an accepted count outside 0..block+1) leave that
+ *     request untouched, set the handle's device error word, and surface at
+ *     the next hf_sync(). hf_last_error() gives a message for the last
+ *     non-OK status.
+ *   - A handle is not thread-safe; calls on one handle must be ordered.
+ */
+#ifndef HYFLASH_H
+#define HYFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct hf_handle hf_handle;
+
+typedef enum {
+  HF_OK = 0,
+  HF_EINVAL = 1,   /* bad argument or configuration */
+  HF_ENOMEM = 2,   /* device allocation failed (nothing leaked) */
+  HF_ECUDA = 3,    /* CUDA runtime error (no device, launch failure, ...) */
+  HF_ETIMEOUT = 4, /* a bounded device-side wait gave up */
+  HF_EDEVICE = 5   /* a device-side argument check failed (see hf_last_error) */
+} hf_status;
+
+typedef enum { HF_F32 = 0, HF_BF16 = 1 } hf_dtype;
+
+/* Shape of the drafter. Block is the number of draft slots (7 on the pages:
+ * "In the paper the block is 7 positions"); commits take up to block+1 rows
+ * (7 drafts plus the target's bonus token). */
+typedef struct {
+  int32_t d_model;      /* D */
+  int32_t n_q_heads;    /* Hq */
+  int32_t n_kv_heads;   /* Hkv, divides Hq */
+  int32_t head_dim;     /* dh, multiple of 4, <= 256 */
+  int32_t window;       /* W >= block+1: sliding-window ring length */
+  int32_t block;        /* S = 7 draft slots (1..16 accepted) */
+  int32_t ssm_heads;    /* Hm */
+  int32_t ssm_headdim;  /* P */
+  int32_t d_state;      /* N, multiple of 4 */
+  int32_t n_groups;     /* must be 1 */
+  int32_t n_layers;     /* drafter depth */
+  int32_t max_batch;    /* requests held by the handle */
+  int32_t chunk;        /* prefill scan chunk length: 64, 128 or 256 */
+  int32_t dtype;        /* hf_dtype */
+  int64_t prefill_tokens_max; /* tokens per internal prefill pass; 0 = 32768 */
+} hf_config;
+
+/* One layer's weights, HOST pointers, row-major [in, out] in the handle's
+ * dtype (dt_bias, A_log: fp32 [ssm_heads]). Shapes:
+ *   w_q [D, Hq*dh]  w_k, w_v [D, Hkv*dh]  w_o [Hq*dh, D]
+ *   w_x [D, Hm*P]   w_B, w_C [D, N]       w_dt [D, Hm]   w_mo [Hm*P, D] */
+typedef struct {
+  const void* w_q;
+  const void* w_k;
+  const void* w_v;
+  const void* w_o;
+  const void* w_x;
+  const void* w_B;
+  const void* w_C;
+  const void* w_dt;
+  const void* w_mo;
+  const float* dt_bias;
+  const float* A_log;
+} hf_layer_weights;
+
+/* Create a handle on CUDA device `device`: validates cfg (HF_EINVAL before
+ * touching CUDA), allocates and zeroes rings, states, positions, weights and
+ * scratch (HF_ENOMEM on failure, everything freed). Synchronises. */
+hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out);
+
+/* Free everything the handle owns. Synchronises the device. NULL is a no-op. */
+void hf_destroy(hf_handle* h);
+
+/* Copy one layer's weights in from HOST memory (re-laid-out for the kernels:
+ * transposed to [out, in] and concatenated per call site). Synchronises;
+ * the caller may free its buffers afterwards. */
+hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w);
+
+/* Prefill (fold the committed prefix). feats: DEVICE [sum(lens), D] packed
+ * in request order; lens: HOST int32 [n_req], each >= 0; requests: HOST int32
+ * [n_req] distinct request slots in 0..max_batch-1, or NULL for 0..n_req-1.
+ * Each named request is reset, its memory becomes the fold of all its
+ * features from h = 0 (chunked scan, chunk = cfg.chunk), its window holds the
+ * last min(L, W) features' K/V at slot pos mod W, and pos = L. Other
+ * requests are untouched. */
+hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens,
+                     const int32_t* requests, int32_t n_req, void* stream);
+
+/* Commit one verification round for requests 0..batch-1. feats: DEVICE
+ * [batch, block+1, D]; n_accepted: DEVICE int32 [batch]. For request b the
+ * rows t < n_b are appended in order (ring slot (pos_b + t) mod W, memory
+ * update token by token) and pos_b += n_b. Rows t >= n_b are never read.
+ * n_b = 0 is a no-op. n_b outside 0..block+1 leaves request b untouched and
+ * raises HF_EDEVICE at the next hf_sync. Packed row offsets (exclusive scan
+ * of the valid counts) are kept for inspection (HF_T_OFFSETS). */
+hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted,
+                    int32_t batch, void* stream);
+
+/* Draft for requests 0..batch-1: slot_emb DEVICE [batch, block, D] ->
+ * out DEVICE [batch, block, D] (may not alias slot_emb). Runs every layer;
+ * layer l+1's slot input is layer l's output. Never writes rings, states or
+ * positions. */
+hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
+                   void* stream);
+
+/* Synchronise `stream`, then read and clear the device error word. Returns
+ * HF_EDEVICE if a device-side check failed since the last hf_sync, HF_ECUDA
+ * on an asynchronous CUDA error, HF_OK otherwise. */
+hf_status hf_sync(hf_handle* h, void* stream);
+
+/* Message for the last non-OK status of this handle ("" if none); the
+ * pointer stays valid until the next call on the handle. h may be NULL
+ * (then the message of the last failed hf_create in this thread). */
+const char* hf_last_error(const hf_handle* h);
+
+/* Static name of a status code. */
+const char* hf_status_string(hf_status s);
+
+/* ---- inspection (tests, checkpoints) ---------------------------------- */
+
+typedef enum {
+  HF_T_STATE = 0,     /* fp32 [L, max_batch, Hm, P, N] */
+  HF_T_RING_K = 1,    /* dtype [L, max_batch, Hkv, W, dh] */
+  HF_T_RING_V = 2,    /* dtype [L, max_batch, Hkv, W, dh] */
+  HF_T_RING_TAG = 3,  /* int32 [max_batch, W]: committed position held by
+                         each slot, -1 if empty */
+  HF_T_POS = 4,       /* int64 [max_batch]: committed tokens per request */
+  HF_T_OFFSETS = 5,   /* int32 [max_batch + 1]: packed row offsets of the
+                         last commit (entries past its batch are stale) */
+  HF_T_DRAFT_PROJ = 6,/* fp32 [max_batch*block, Hq*dh + 2*Hkv*dh + N]: last
+                         layer's slot projections Q|K_s|V_s|C_s, last draft */
+  HF_T_DRAFT_MIX = 7  /* dtype [max_batch*block, Hq*dh + Hm*P]: last layer's
+                         attention output | memory read y, last draft */
+} hf_tensor_id;
+
+/* Size in bytes of an inspectable tensor. */
+hf_status hf_tensor_bytes(const hf_handle* h, int32_t which, size_t* bytes);
+
+/* Copy a whole inspectable tensor to HOST memory (bytes must equal
+ * hf_tensor_bytes). Synchronises the device. */
+hf_status hf_read_tensor(hf_handle* h, int32_t which, void* host_out, size_t bytes);
+
+/* Bytes of the complete drafter context (states, rings, tags, positions):
+ * the fixed-size draft-side memory of all requests and layers. */
+size_t hf_context_bytes(const hf_handle* h);
+
+/* Copy the complete context to / from HOST memory (checkpoint, or byte
+ * comparison of before/after). Synchronise the device. */
+hf_status hf_export_context(hf_handle* h, void* host_out, size_t bytes);
+hf_status hf_import_context(hf_handle* h, const void* host_in, size_t bytes);
+
+/* ---- measurement ------------------------------------------------------ */
+
+/* Kernel families timed by the profiler and counted by hf_launch_count. */
+typedef enum {
+  HF_K_DRAFT_PROJ = 0,   /* draft input projections (Q|K_s|V_s|C_s) */
+  HF_K_ATTN_MEM = 1,     /* window+block attention and memory read */
+  HF_K_OUT_PROJ = 2,     /* output projections + residual */
+  HF_K_COMMIT_PREP = 3,  /* count check, offsets, row gather */
+  HF_K_COMMIT_PROJ = 4,  /* commit projections + ring append */
+  HF_K_COMMIT_STATE = 5, /* sequential memory update */
+  HF_K_PREFILL = 6,      /* every prefill kernel */
+  HF_K_OTHER = 7,        /* split-K combine and helpers */
+  HF_K_COUNT = 8
+} hf_kernel_family;
+
+/* Turn per-kernel CUDA-event timing on/off (events recorded on the launch
+ * stream around every launch; results are read with hf_profile_read). */
+hf_status hf_profile_enable(hf_handle* h, int32_t on);
+
+/* Synchronises, then returns total milliseconds and launches of a family
+ * since the last reset, and resets that family if reset != 0. */
+hf_status hf_profile_read(hf_handle* h, int32_t family, double* total_ms,
+                          int64_t* launches, int32_t reset);
+
+/* Number of kernels this handle has launched since creation. */
+int64_t hf_launch_count(const hf_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYFLASH_H */

@@ -1,0 +1,160 @@
+// Shared device helpers and the internal (non-ABI) interface between the
+// runtime (hyflash.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "hyflash.h"
+
+namespace hf {
+
+// ---------------------------------------------------------------- dtype glue
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Stable softplus in fp32: max(x,0) + log1p(exp(-|x|)).
+__device__ __forceinline__ float softplus_f(float x) {
+  return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+}
+
+// Device error word bits.
+enum : int32_t { ERR_BAD_ACCEPTED = 1, ERR_TIMEOUT = 2 };
+
+// ---------------------------------------------------------------- dims
+// All derived sizes of a handle, passed by value to kernels.
+struct Dims {
+  int D, Hq, Hkv, dh, W, S, Hm, P, N, L, Bmax;
+  int G;       // Hq / Hkv
+  int QD;      // Hq*dh
+  int KVD;     // Hkv*dh
+  int dinner;  // Hm*P
+  int Nd;      // draft projection columns: QD + 2*KVD + N
+  int Nc;      // commit projection columns per layer: 2*KVD + dinner + N + Hm
+  int NS;      // memory-input columns: dinner + N + Hm
+  int Nz;      // output-projection inputs: QD + dinner
+  int esize;   // element bytes of the model dtype
+};
+
+// ---------------------------------------------------------------- GEMM epilogues
+enum EpiKind : int { EPI_F32 = 0, EPI_RESID = 1, EPI_SSM_KV = 2 };
+
+struct Epi {
+  int kind;
+  // EPI_F32: out[r*ld + c] = v
+  float* out;
+  int ld;
+  // EPI_RESID: out_t[r*ld + c] = resid[r*ld + c] + v  (model dtype)
+  const void* resid;
+  void* out_t;
+  // EPI_SSM_KV: column c -> layer = layer0 + c / cols_per_layer,
+  // local column cl = c % cols_per_layer + col_off in the per-layer
+  // [K | V | x | B | dt] block. K/V go to the ring slot of the row's
+  // committed position; x, B and softplus(dt + bias) go to xbd (fp32).
+  int layer0, cols_per_layer, col_off;
+  const int32_t* row_req;   // request of each packed row
+  const int64_t* row_pos;   // committed position of each packed row
+  const int32_t* n_rows;    // device count of valid rows (NULL: all)
+  void* ring_k;
+  void* ring_v;
+  float* xbd;
+  long long xbd_layer_stride;  // elements between layers in xbd
+  const float* dt_bias;        // [L][Hm]
+  Dims d;
+};
+
+template <typename T>
+__device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
+  if (e.kind == EPI_F32) {
+    e.out[(size_t)r * e.ld + c] = v;
+  } else if (e.kind == EPI_RESID) {
+    size_t i = (size_t)r * e.ld + c;
+    float x = to_f(((const T*)e.resid)[i]);
+    ((T*)e.out_t)[i] = from_f<T>(x + v);
+  } else {
+    if (e.n_rows && r >= *e.n_rows) return;
+    const Dims& d = e.d;
+    int layer = e.layer0 + c / e.cols_per_layer;
+    int cl = c % e.cols_per_layer + e.col_off;
+    if (cl < 2 * d.KVD) {
+      int which = cl >= d.KVD;
+      int cc = cl - which * d.KVD;
+      int kvh = cc / d.dh, dd = cc % d.dh;
+      int b = e.row_req[r];
+      int slot = (int)(e.row_pos[r] % d.W);
+      size_t idx = ((((size_t)layer * d.Bmax + b) * d.Hkv + kvh) * d.W + slot) * d.dh + dd;
+      ((T*)(which ? e.ring_v : e.ring_k))[idx] = from_f<T>(v);
+    } else {
+      int j = cl - 2 * d.KVD;
+      float o = v;
+      if (j >= d.dinner + d.N) o = softplus_f(v + e.dt_bias[layer * d.Hm + (j - d.dinner - d.N)]);
+      e.xbd[(size_t)layer * e.xbd_layer_stride + (size_t)r * d.NS + j] = o;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+// Every launcher enqueues on `st` and returns cudaGetLastError().
+
+// Y[r, c] = sum_k X[r, k] * Wt[c, k] for r < R, c < C; epilogue per element.
+// X row stride ldx, Wt row stride ldw (both in elements). part: split-K
+// scratch of at least splits*R*C floats (unused when splits == 1).
+cudaError_t launch_gemm_fma(int dtype, const void* X, int ldx, const void* Wt, int ldw,
+                            int R, int C, int K, int splits, float* part,
+                            const Epi& epi, cudaStream_t st, int* launches);
+
+// Window+block attention and memory read for one layer, batch B.
+// proj [B*S, Nd] fp32 (Q|K_s|V_s|C_s); ring_k/v of this layer; pos [Bmax];
+// state of this layer; mix [B*S, Nz] model dtype (O | y).
+cudaError_t launch_attn_mem(int dtype, const Dims& d, int B, const float* proj,
+                            const void* ring_k, const void* ring_v, const int64_t* pos,
+                            const float* state, void* mix, float* part_o, float* part_ml,
+                            int nsplit, cudaStream_t st, int* launches_attn,
+                            int* launches_other);
+
+// Commit prep: validate counts, offsets, row map, tags, gather rows.
+cudaError_t launch_commit_prep(int dtype, const Dims& d, int B, const void* feats,
+                               const int32_t* n_acc, const int64_t* pos, int32_t* offsets,
+                               int32_t* row_req, int64_t* row_pos, int32_t* tags,
+                               void* packed, int32_t* err, cudaStream_t st);
+
+// Sequential memory update over the accepted rows, all layers; pos += n.
+cudaError_t launch_commit_state(const Dims& d, int B, const int32_t* offsets,
+                                const float* xbd, long long xbd_layer_stride,
+                                const float* A_log, float* state, int64_t* pos,
+                                cudaStream_t st);
+
+// Prefill helpers (lens/reqs/cu are device int32 arrays of n_req entries).
+cudaError_t launch_prefill_reset(const Dims& d, int n_req, const int32_t* reqs,
+                                 float* state, int32_t* tags, int64_t* pos, cudaStream_t st);
+cudaError_t launch_prefill_ring_prep(int dtype, const Dims& d, int n_req, int n_rows,
+                                     const int32_t* lens, const int32_t* reqs,
+                                     const void* feats, int32_t* row_req, int64_t* row_pos,
+                                     int32_t* tags, void* packed, cudaStream_t st);
+cudaError_t launch_prefill_scan(const Dims& d, int layer, int n_req, const int32_t* lens,
+                                const int32_t* reqs, long long seg0, long long seg1,
+                                const float* xbd, const float* A_log, float* state,
+                                cudaStream_t st);
+cudaError_t launch_prefill_finish(int n_req, const int32_t* lens, const int32_t* reqs,
+                                  int64_t* pos, cudaStream_t st);
+
+}  // namespace hf

@@ -1,0 +1,684 @@
+// Host runtime and C ABI of the HyFlash drafter-layer library.
+//
+// The handle owns, per layer, the window rings and recurrent states of all
+// requests, the re-laid-out weights, and the scratch the kernels need. Every
+// call enqueues kernels on the caller's stream; host work is argument
+// checking, pointer arithmetic and grid sizing only.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+using hf::Dims;
+using hf::Epi;
+
+struct ProfRec {
+  cudaEvent_t a, b;
+  int fam;
+};
+
+struct hf_handle {
+  hf_config cfg{};
+  int device = 0;
+  Dims d{};
+  size_t esz = 4;
+  std::vector<void*> allocs;
+
+  void* w_draft = nullptr;   // [L][Nd][D]
+  void* w_commit = nullptr;  // [L][Nc][D]
+  void* w_out = nullptr;     // [L][D][Nz]
+  float* dt_bias = nullptr;  // [L][Hm]
+  float* A_log = nullptr;    // [L][Hm]
+
+  void* ring_k = nullptr;    // [L][Bmax][Hkv][W][dh]
+  void* ring_v = nullptr;
+  int32_t* tags = nullptr;   // [Bmax][W]
+  int64_t* pos = nullptr;    // [Bmax]
+  float* state = nullptr;    // [L][Bmax][Hm][P][N]
+
+  int32_t* offsets = nullptr;  // [Bmax+1]
+  int32_t* row_req = nullptr;  // [Rmax]
+  int64_t* row_pos = nullptr;  // [Rmax]
+  void* packed = nullptr;      // [Rmax][D]
+  long long rmax = 0;
+  float* xbd = nullptr;        // [L][(S+1)*Bmax][NS]
+  long long xbd_ls = 0;
+
+  float* proj = nullptr;       // [Bmax*S][Nd]
+  void* mix = nullptr;         // [Bmax*S][Nz]
+  void* xbuf[2] = {nullptr, nullptr};
+  float* attn_o = nullptr;
+  float* attn_ml = nullptr;
+  int nsplit = 1;
+  float* part = nullptr;
+  size_t part_elems = 0;
+
+  float* pf_xbd = nullptr;     // [Tseg][NS]
+  long long pf_tokens = 0;
+  int32_t* pf_lens = nullptr;  // [Bmax]
+  int32_t* pf_reqs = nullptr;  // [Bmax]
+
+  int32_t* err = nullptr;
+
+  bool prof = false;
+  std::vector<ProfRec> pending;
+  std::vector<cudaEvent_t> pool;
+  double tot_ms[HF_K_COUNT] = {};
+  int64_t nl[HF_K_COUNT] = {};
+  int64_t launches = 0;
+  std::string msg;
+};
+
+namespace {
+
+thread_local std::string g_create_error;
+
+hf_status fail(hf_handle* h, hf_status s, const std::string& m) {
+  if (h) h->msg = m;
+  else g_create_error = m;
+  return s;
+}
+
+hf_status cuda_fail(hf_handle* h, cudaError_t e, const char* where) {
+  return fail(h, HF_ECUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+#define HF_CUDA(h, call)                                  \
+  do {                                                    \
+    cudaError_t _e = (call);                              \
+    if (_e != cudaSuccess) return cuda_fail(h, _e, #call); \
+  } while (0)
+
+long long round_up(long long a, long long b) { return (a + b - 1) / b * b; }
+
+hf_status validate(const hf_config* c, std::string* why) {
+  auto bad = [&](const char* m) { *why = m; return HF_EINVAL; };
+  if (!c) return bad("config is NULL");
+  if (c->d_model <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+      c->window <= 0 || c->block <= 0 || c->ssm_heads <= 0 || c->ssm_headdim <= 0 ||
+      c->d_state <= 0 || c->n_layers <= 0 || c->max_batch <= 0)
+    return bad("every dimension must be positive");
+  if (c->n_groups != 1) return bad("n_groups must be 1");
+  if (c->n_q_heads % c->n_kv_heads) return bad("n_kv_heads must divide n_q_heads");
+  if (c->head_dim % 4 || c->head_dim > 256) return bad("head_dim must be a multiple of 4, <= 256");
+  if (c->d_state % 4 || c->d_state > 256) return bad("d_state must be a multiple of 4, <= 256");
+  if (c->ssm_headdim % 4) return bad("ssm_headdim must be a multiple of 4");
+  if ((long long)c->ssm_headdim * c->d_state > 8192) return bad("ssm_headdim * d_state must be <= 8192");
+  if (c->block > 16) return bad("block must be <= 16");
+  if (c->window < c->block + 1) return bad("window must be >= block + 1");
+  if ((c->n_q_heads / c->n_kv_heads) * c->block > 64) return bad("(n_q_heads/n_kv_heads)*block must be <= 64");
+  if (c->chunk != 64 && c->chunk != 128 && c->chunk != 256) return bad("chunk must be 64, 128 or 256");
+  if (c->dtype != HF_F32 && c->dtype != HF_BF16) return bad("dtype must be HF_F32 or HF_BF16");
+  if (c->d_model % 8) return bad("d_model must be a multiple of 8");
+  if (c->prefill_tokens_max < 0) return bad("prefill_tokens_max must be >= 0");
+  if (c->max_batch > 65535) return bad("max_batch must be <= 65535");
+  return HF_OK;
+}
+
+Dims make_dims(const hf_config& c) {
+  Dims d{};
+  d.D = c.d_model; d.Hq = c.n_q_heads; d.Hkv = c.n_kv_heads; d.dh = c.head_dim;
+  d.W = c.window; d.S = c.block; d.Hm = c.ssm_heads; d.P = c.ssm_headdim; d.N = c.d_state;
+  d.L = c.n_layers; d.Bmax = c.max_batch;
+  d.G = d.Hq / d.Hkv;
+  d.QD = d.Hq * d.dh;
+  d.KVD = d.Hkv * d.dh;
+  d.dinner = d.Hm * d.P;
+  d.Nd = d.QD + 2 * d.KVD + d.N;
+  d.Nc = 2 * d.KVD + d.dinner + d.N + d.Hm;
+  d.NS = (int)round_up(d.dinner + d.N + d.Hm, 4);
+  d.Nz = d.QD + d.dinner;
+  d.esize = c.dtype == HF_F32 ? 4 : 2;
+  return d;
+}
+
+hf_status dev_alloc(hf_handle* h, void** p, size_t bytes) {
+  *p = nullptr;
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return fail(h, HF_ENOMEM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed: " +
+                                  cudaGetErrorString(e));
+  }
+  h->allocs.push_back(*p);
+  e = cudaMemset(*p, 0, bytes);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemset");
+  return HF_OK;
+}
+
+void free_all(hf_handle* h) {
+  for (auto& r : h->pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : h->pool) cudaEventDestroy(e);
+  h->pending.clear();
+  h->pool.clear();
+  for (void* p : h->allocs) cudaFree(p);
+  h->allocs.clear();
+}
+
+// ---- profiling: events around launches of one family
+cudaEvent_t get_event(hf_handle* h) {
+  if (!h->pool.empty()) {
+    cudaEvent_t e = h->pool.back();
+    h->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct Scope {
+  hf_handle* h;
+  int fam;
+  cudaStream_t st;
+  ProfRec rec{};
+  int before;
+  int count = 0;  // launches made inside the scope
+  Scope(hf_handle* h_, int fam_, cudaStream_t st_) : h(h_), fam(fam_), st(st_) {
+    if (h->prof) {
+      rec.a = get_event(h);
+      rec.b = get_event(h);
+      rec.fam = fam;
+      cudaEventRecord(rec.a, st);
+    }
+  }
+  ~Scope() {
+    h->launches += count;
+    if (h->prof) {
+      cudaEventRecord(rec.b, st);
+      h->pending.push_back(rec);
+      h->nl[fam] += count;
+    }
+  }
+};
+
+hf_status drain_profile(hf_handle* h) {
+  if (h->pending.empty()) return HF_OK;
+  HF_CUDA(h, cudaEventSynchronize(h->pending.back().b));
+  for (auto& r : h->pending) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) h->tot_ms[r.fam] += ms;
+    h->pool.push_back(r.a);
+    h->pool.push_back(r.b);
+  }
+  h->pending.clear();
+  return HF_OK;
+}
+
+int pick_splits(const hf_handle* h, long long R, long long C, long long K, int tile_r, int tile_c) {
+  long long tiles = ((R + tile_r - 1) / tile_r) * ((C + tile_c - 1) / tile_c);
+  int s = (int)std::max<long long>(1, (2 * 152 + tiles - 1) / tiles);
+  s = (int)std::min<long long>(s, std::max<long long>(1, K / 256));
+  s = std::min(s, 16);
+  while (s > 1 && (size_t)s * R * C > h->part_elems) --s;
+  return s;
+}
+
+hf_status gemm(hf_handle* h, int fam, const void* X, int ldx, const void* Wt, int ldw, int R,
+               int C, int K, const Epi& epi, cudaStream_t st) {
+  if (R <= 0 || C <= 0) return HF_OK;
+  int splits = pick_splits(h, R, C, K, 64, 64);
+  Scope sc(h, fam, st);
+  cudaError_t e = hf::launch_gemm_fma(h->cfg.dtype, X, ldx, Wt, ldw, R, C, K, splits, h->part,
+                                      epi, st, &sc.count);
+  if (e != cudaSuccess) return cuda_fail(h, e, "gemm launch");
+  return HF_OK;
+}
+
+Epi epi_base(const hf_handle* h) {
+  Epi e{};
+  e.d = h->d;
+  e.dt_bias = h->dt_bias;
+  e.ring_k = h->ring_k;
+  e.ring_v = h->ring_v;
+  return e;
+}
+
+char* bptr(void* p, size_t off) { return static_cast<char*>(p) + off; }
+const char* bptr(const void* p, size_t off) { return static_cast<const char*>(p) + off; }
+
+}  // namespace
+
+extern "C" {
+
+const char* hf_status_string(hf_status s) {
+  switch (s) {
+    case HF_OK: return "HF_OK";
+    case HF_EINVAL: return "HF_EINVAL";
+    case HF_ENOMEM: return "HF_ENOMEM";
+    case HF_ECUDA: return "HF_ECUDA";
+    case HF_ETIMEOUT: return "HF_ETIMEOUT";
+    case HF_EDEVICE: return "HF_EDEVICE";
+  }
+  return "HF_UNKNOWN";
+}
+
+const char* hf_last_error(const hf_handle* h) {
+  return h ? h->msg.c_str() : g_create_error.c_str();
+}
+
+hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
+  if (!out) return fail(nullptr, HF_EINVAL, "out is NULL");
+  *out = nullptr;
+  std::string why;
+  if (validate(cfg, &why) != HF_OK) return fail(nullptr, HF_EINVAL, why);
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    return fail(nullptr, HF_ECUDA, std::string("no CUDA device: ") + cudaGetErrorString(e));
+  }
+  if (device < 0 || device >= ndev) return fail(nullptr, HF_EINVAL, "device index out of range");
+  e = cudaSetDevice(device);
+  if (e != cudaSuccess) return fail(nullptr, HF_ECUDA, cudaGetErrorString(e));
+
+  hf_handle* h = new hf_handle();
+  h->cfg = *cfg;
+  if (h->cfg.prefill_tokens_max == 0) h->cfg.prefill_tokens_max = 16384;
+  h->device = device;
+  h->d = make_dims(h->cfg);
+  const Dims& d = h->d;
+  h->esz = d.esize;
+  const size_t es = h->esz;
+  const size_t L = d.L, Bm = d.Bmax;
+  h->rmax = std::max<long long>((long long)(d.S + 1) * Bm, (long long)Bm * d.W);
+  h->xbd_ls = (long long)(d.S + 1) * Bm * d.NS;
+  h->nsplit = (d.W + 31) / 32;
+  h->pf_tokens = h->cfg.prefill_tokens_max;
+  h->part_elems = (size_t)16 << 20;
+  const size_t R = (size_t)d.G * d.S;
+
+  hf_status s = HF_OK;
+  auto A = [&](void** p, size_t bytes) {
+    if (s == HF_OK) s = dev_alloc(h, p, bytes);
+  };
+  A(&h->w_draft, L * d.Nd * d.D * es);
+  A(&h->w_commit, L * d.Nc * d.D * es);
+  A(&h->w_out, L * d.D * d.Nz * es);
+  A((void**)&h->dt_bias, L * d.Hm * 4);
+  A((void**)&h->A_log, L * d.Hm * 4);
+  A(&h->ring_k, L * Bm * d.Hkv * d.W * d.dh * es);
+  A(&h->ring_v, L * Bm * d.Hkv * d.W * d.dh * es);
+  A((void**)&h->tags, Bm * d.W * 4);
+  A((void**)&h->pos, Bm * 8);
+  A((void**)&h->state, L * Bm * d.Hm * d.P * d.N * 4);
+  A((void**)&h->offsets, (Bm + 1) * 4);
+  A((void**)&h->row_req, h->rmax * 4);
+  A((void**)&h->row_pos, h->rmax * 8);
+  A(&h->packed, h->rmax * d.D * es);
+  A((void**)&h->xbd, L * h->xbd_ls * 4);
+  A((void**)&h->proj, Bm * d.S * d.Nd * 4);
+  A(&h->mix, Bm * d.S * d.Nz * es);
+  A(&h->xbuf[0], Bm * d.S * d.D * es);
+  A(&h->xbuf[1], Bm * d.S * d.D * es);
+  A((void**)&h->attn_o, Bm * d.Hkv * h->nsplit * R * d.dh * 4);
+  A((void**)&h->attn_ml, Bm * d.Hkv * h->nsplit * R * 2 * 4);
+  A((void**)&h->part, h->part_elems * 4);
+  A((void**)&h->pf_xbd, (size_t)h->pf_tokens * d.NS * 4);
+  A((void**)&h->pf_lens, Bm * 4);
+  A((void**)&h->pf_reqs, Bm * 4);
+  A((void**)&h->err, 16);
+  if (s == HF_OK) {
+    // Empty ring slots carry tag -1.
+    e = cudaMemset(h->tags, 0xff, Bm * d.W * 4);
+    if (e != cudaSuccess) s = cuda_fail(h, e, "cudaMemset(tags)");
+  }
+  if (s == HF_OK) {
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) s = cuda_fail(h, e, "cudaDeviceSynchronize");
+  }
+  if (s != HF_OK) {
+    g_create_error = h->msg;
+    free_all(h);
+    delete h;
+    return s;
+  }
+  *out = h;
+  return HF_OK;
+}
+
+void hf_destroy(hf_handle* h) {
+  if (!h) return;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+}
+
+hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w) {
+  if (!h) return HF_EINVAL;
+  if (!w || layer < 0 || layer >= h->d.L) return fail(h, HF_EINVAL, "bad layer or weights");
+  const void* ptrs[] = {w->w_q, w->w_k, w->w_v, w->w_o, w->w_x, w->w_B, w->w_C, w->w_dt, w->w_mo,
+                        w->dt_bias, w->A_log};
+  for (const void* p : ptrs)
+    if (!p) return fail(h, HF_EINVAL, "a weight pointer is NULL");
+  HF_CUDA(h, cudaSetDevice(h->device));
+  const Dims& d = h->d;
+  const size_t es = h->esz, D = d.D;
+  // Transpose a host [in, out] matrix into rows [out][in] of dst (row length ld).
+  auto put_t = [&](std::vector<char>& dst, size_t row0, size_t ld, const void* src, size_t in,
+                   size_t outn) {
+    const char* s = static_cast<const char*>(src);
+    for (size_t i = 0; i < in; ++i)
+      for (size_t o = 0; o < outn; ++o)
+        std::memcpy(&dst[((row0 + o) * ld + i) * es], s + (i * outn + o) * es, es);
+  };
+  std::vector<char> wd((size_t)d.Nd * D * es), wc((size_t)d.Nc * D * es), wo((size_t)D * d.Nz * es);
+  put_t(wd, 0, D, w->w_q, D, d.QD);
+  put_t(wd, d.QD, D, w->w_k, D, d.KVD);
+  put_t(wd, d.QD + d.KVD, D, w->w_v, D, d.KVD);
+  put_t(wd, d.QD + 2 * d.KVD, D, w->w_C, D, d.N);
+  put_t(wc, 0, D, w->w_k, D, d.KVD);
+  put_t(wc, d.KVD, D, w->w_v, D, d.KVD);
+  put_t(wc, 2 * d.KVD, D, w->w_x, D, d.dinner);
+  put_t(wc, 2 * d.KVD + d.dinner, D, w->w_B, D, d.N);
+  put_t(wc, 2 * d.KVD + d.dinner + d.N, D, w->w_dt, D, d.Hm);
+  // W_out^T: row c = [W_o[:, c] | W_mo[:, c]]
+  {
+    const char* so = static_cast<const char*>(w->w_o);
+    const char* sm = static_cast<const char*>(w->w_mo);
+    for (size_t k = 0; k < (size_t)d.QD; ++k)
+      for (size_t c = 0; c < D; ++c) std::memcpy(&wo[(c * d.Nz + k) * es], so + (k * D + c) * es, es);
+    for (size_t k = 0; k < (size_t)d.dinner; ++k)
+      for (size_t c = 0; c < D; ++c)
+        std::memcpy(&wo[(c * d.Nz + d.QD + k) * es], sm + (k * D + c) * es, es);
+  }
+  HF_CUDA(h, cudaMemcpy(bptr(h->w_draft, (size_t)layer * wd.size()), wd.data(), wd.size(), cudaMemcpyHostToDevice));
+  HF_CUDA(h, cudaMemcpy(bptr(h->w_commit, (size_t)layer * wc.size()), wc.data(), wc.size(), cudaMemcpyHostToDevice));
+  HF_CUDA(h, cudaMemcpy(bptr(h->w_out, (size_t)layer * wo.size()), wo.data(), wo.size(), cudaMemcpyHostToDevice));
+  HF_CUDA(h, cudaMemcpy(h->dt_bias + (size_t)layer * d.Hm, w->dt_bias, d.Hm * 4, cudaMemcpyHostToDevice));
+  HF_CUDA(h, cudaMemcpy(h->A_log + (size_t)layer * d.Hm, w->A_log, d.Hm * 4, cudaMemcpyHostToDevice));
+  HF_CUDA(h, cudaDeviceSynchronize());
+  return HF_OK;
+}
+
+hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch, void* stream) {
+  if (!h) return HF_EINVAL;
+  if (!slot_emb || !out) return fail(h, HF_EINVAL, "NULL buffer");
+  if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
+  if (slot_emb == out) return fail(h, HF_EINVAL, "out may not alias slot_emb");
+  if (batch == 0) return HF_OK;
+  HF_CUDA(h, cudaSetDevice(h->device));
+  cudaStream_t st = (cudaStream_t)stream;
+  const Dims& d = h->d;
+  const size_t es = h->esz;
+  const int R = batch * d.S;
+  const size_t ring_ls = (size_t)d.Bmax * d.Hkv * d.W * d.dh * es;
+  const size_t state_ls = (size_t)d.Bmax * d.Hm * d.P * d.N;
+  for (int l = 0; l < d.L; ++l) {
+    const void* X = l == 0 ? slot_emb : h->xbuf[(l - 1) % 2];
+    void* Y = l == d.L - 1 ? out : h->xbuf[l % 2];
+    Epi e1 = epi_base(h);
+    e1.kind = hf::EPI_F32;
+    e1.out = h->proj;
+    e1.ld = d.Nd;
+    hf_status s = gemm(h, HF_K_DRAFT_PROJ, X, d.D, bptr(h->w_draft, (size_t)l * d.Nd * d.D * es),
+                       d.D, R, d.Nd, d.D, e1, st);
+    if (s != HF_OK) return s;
+    {
+      Scope sc(h, HF_K_ATTN_MEM, st);
+      int other = 0;
+      cudaError_t e = hf::launch_attn_mem(h->cfg.dtype, d, batch, h->proj,
+                                          bptr(h->ring_k, l * ring_ls), bptr(h->ring_v, l * ring_ls),
+                                          h->pos, h->state + l * state_ls, h->mix, h->attn_o,
+                                          h->attn_ml, h->nsplit, st, &sc.count, &other);
+      sc.count += other;
+      if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
+    }
+    Epi e2 = epi_base(h);
+    e2.kind = hf::EPI_RESID;
+    e2.resid = X;
+    e2.out_t = Y;
+    e2.ld = d.D;
+    s = gemm(h, HF_K_OUT_PROJ, h->mix, d.Nz, bptr(h->w_out, (size_t)l * d.D * d.Nz * es), d.Nz, R,
+             d.D, d.Nz, e2, st);
+    if (s != HF_OK) return s;
+  }
+  return HF_OK;
+}
+
+hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, int32_t batch,
+                    void* stream) {
+  if (!h) return HF_EINVAL;
+  if (!feats || !n_accepted) return fail(h, HF_EINVAL, "NULL buffer");
+  if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
+  if (batch == 0) return HF_OK;
+  HF_CUDA(h, cudaSetDevice(h->device));
+  cudaStream_t st = (cudaStream_t)stream;
+  const Dims& d = h->d;
+  {
+    Scope sc(h, HF_K_COMMIT_PREP, st);
+    cudaError_t e = hf::launch_commit_prep(h->cfg.dtype, d, batch, feats, n_accepted, h->pos,
+                                           h->offsets, h->row_req, h->row_pos, h->tags, h->packed,
+                                           h->err, st);
+    sc.count = 1;
+    if (e != cudaSuccess) return cuda_fail(h, e, "commit prep launch");
+  }
+  Epi ep = epi_base(h);
+  ep.kind = hf::EPI_SSM_KV;
+  ep.layer0 = 0;
+  ep.cols_per_layer = d.Nc;
+  ep.col_off = 0;
+  ep.row_req = h->row_req;
+  ep.row_pos = h->row_pos;
+  ep.n_rows = h->offsets + batch;
+  ep.xbd = h->xbd;
+  ep.xbd_layer_stride = h->xbd_ls;
+  hf_status s = gemm(h, HF_K_COMMIT_PROJ, h->packed, d.D, h->w_commit, d.D, batch * (d.S + 1),
+                     d.L * d.Nc, d.D, ep, st);
+  if (s != HF_OK) return s;
+  {
+    Scope sc(h, HF_K_COMMIT_STATE, st);
+    cudaError_t e = hf::launch_commit_state(d, batch, h->offsets, h->xbd, h->xbd_ls, h->A_log,
+                                            h->state, h->pos, st);
+    sc.count = 1;
+    if (e != cudaSuccess) return cuda_fail(h, e, "commit state launch");
+  }
+  return HF_OK;
+}
+
+hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const int32_t* requests,
+                     int32_t n_req, void* stream) {
+  if (!h) return HF_EINVAL;
+  const Dims& d = h->d;
+  if (n_req < 0 || n_req > d.Bmax) return fail(h, HF_EINVAL, "n_req out of range");
+  if (n_req == 0) return HF_OK;
+  if (!lens) return fail(h, HF_EINVAL, "lens is NULL");
+  std::vector<int32_t> reqs(n_req);
+  std::vector<char> seen(d.Bmax, 0);
+  long long total = 0, ring_rows = 0;
+  for (int i = 0; i < n_req; ++i) {
+    reqs[i] = requests ? requests[i] : i;
+    if (reqs[i] < 0 || reqs[i] >= d.Bmax) return fail(h, HF_EINVAL, "request index out of range");
+    if (seen[reqs[i]]) return fail(h, HF_EINVAL, "request named twice");
+    seen[reqs[i]] = 1;
+    if (lens[i] < 0) return fail(h, HF_EINVAL, "negative prefix length");
+    total += lens[i];
+    ring_rows += std::min<long long>(lens[i], d.W);
+  }
+  if (total > 0 && !feats) return fail(h, HF_EINVAL, "feats is NULL");
+  if (total > (long long)INT32_MAX) return fail(h, HF_EINVAL, "prefix too long");
+  HF_CUDA(h, cudaSetDevice(h->device));
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t es = h->esz;
+  HF_CUDA(h, cudaMemcpyAsync(h->pf_lens, lens, n_req * 4, cudaMemcpyHostToDevice, st));
+  HF_CUDA(h, cudaMemcpyAsync(h->pf_reqs, reqs.data(), n_req * 4, cudaMemcpyHostToDevice, st));
+  Scope sc(h, HF_K_PREFILL, st);
+  cudaError_t e = hf::launch_prefill_reset(d, n_req, h->pf_reqs, h->state, h->tags, h->pos, st);
+  sc.count++;
+  if (e != cudaSuccess) return cuda_fail(h, e, "prefill reset");
+  if (ring_rows > 0) {
+    e = hf::launch_prefill_ring_prep(h->cfg.dtype, d, n_req, (int)ring_rows, h->pf_lens,
+                                     h->pf_reqs, feats, h->row_req, h->row_pos, h->tags,
+                                     h->packed, st);
+    sc.count++;
+    if (e != cudaSuccess) return cuda_fail(h, e, "prefill ring prep");
+  }
+  for (int l = 0; l < d.L; ++l) {
+    const char* wl = bptr(h->w_commit, (size_t)l * d.Nc * d.D * es);
+    if (ring_rows > 0) {
+      Epi ek = epi_base(h);
+      ek.kind = hf::EPI_SSM_KV;
+      ek.layer0 = l;
+      ek.cols_per_layer = 2 * d.KVD;
+      ek.col_off = 0;
+      ek.row_req = h->row_req;
+      ek.row_pos = h->row_pos;
+      int splits = pick_splits(h, ring_rows, 2 * d.KVD, d.D, 64, 64);
+      e = hf::launch_gemm_fma(h->cfg.dtype, h->packed, d.D, wl, d.D, (int)ring_rows, 2 * d.KVD, d.D,
+                              splits, h->part, ek, st, &sc.count);
+      if (e != cudaSuccess) return cuda_fail(h, e, "prefill kv gemm");
+    }
+    for (long long s0 = 0; s0 < total; s0 += h->pf_tokens) {
+      const long long s1 = std::min(total, s0 + h->pf_tokens);
+      Epi ex = epi_base(h);
+      ex.kind = hf::EPI_SSM_KV;
+      ex.layer0 = l;
+      ex.cols_per_layer = d.dinner + d.N + d.Hm;
+      ex.col_off = 2 * d.KVD;
+      ex.xbd = h->pf_xbd;
+      ex.xbd_layer_stride = 0;
+      e = hf::launch_gemm_fma(h->cfg.dtype, bptr(feats, (size_t)s0 * d.D * es), d.D,
+                              wl + (size_t)2 * d.KVD * d.D * es, d.D, (int)(s1 - s0),
+                              d.dinner + d.N + d.Hm, d.D, 1, h->part, ex, st, &sc.count);
+      if (e != cudaSuccess) return cuda_fail(h, e, "prefill ssm gemm");
+      e = hf::launch_prefill_scan(d, l, n_req, h->pf_lens, h->pf_reqs, s0, s1, h->pf_xbd, h->A_log,
+                                  h->state, st);
+      sc.count++;
+      if (e != cudaSuccess) return cuda_fail(h, e, "prefill scan");
+    }
+  }
+  e = hf::launch_prefill_finish(n_req, h->pf_lens, h->pf_reqs, h->pos, st);
+  sc.count++;
+  if (e != cudaSuccess) return cuda_fail(h, e, "prefill finish");
+  return HF_OK;
+}
+
+hf_status hf_sync(hf_handle* h, void* stream) {
+  if (!h) return HF_EINVAL;
+  HF_CUDA(h, cudaSetDevice(h->device));
+  HF_CUDA(h, cudaStreamSynchronize((cudaStream_t)stream));
+  HF_CUDA(h, cudaGetLastError());
+  int32_t word = 0;
+  HF_CUDA(h, cudaMemcpy(&word, h->err, 4, cudaMemcpyDeviceToHost));
+  if (word) {
+    HF_CUDA(h, cudaMemset(h->err, 0, 4));
+    std::string m;
+    if (word & hf::ERR_BAD_ACCEPTED) m += "accepted count outside 0..block+1 (request left unchanged); ";
+    if (word & hf::ERR_TIMEOUT) m += "a bounded device wait gave up; ";
+    return fail(h, (word & hf::ERR_TIMEOUT) ? HF_ETIMEOUT : HF_EDEVICE, m);
+  }
+  return HF_OK;
+}
+
+hf_status hf_tensor_bytes(const hf_handle* h, int32_t which, size_t* bytes) {
+  if (!h || !bytes) return HF_EINVAL;
+  const Dims& d = h->d;
+  const size_t L = d.L, Bm = d.Bmax;
+  switch (which) {
+    case HF_T_STATE: *bytes = L * Bm * d.Hm * d.P * d.N * 4; break;
+    case HF_T_RING_K:
+    case HF_T_RING_V: *bytes = L * Bm * d.Hkv * d.W * d.dh * h->esz; break;
+    case HF_T_RING_TAG: *bytes = Bm * d.W * 4; break;
+    case HF_T_POS: *bytes = Bm * 8; break;
+    case HF_T_OFFSETS: *bytes = (Bm + 1) * 4; break;
+    case HF_T_DRAFT_PROJ: *bytes = Bm * d.S * d.Nd * 4; break;
+    case HF_T_DRAFT_MIX: *bytes = Bm * d.S * d.Nz * h->esz; break;
+    default: return HF_EINVAL;
+  }
+  return HF_OK;
+}
+
+static const void* tensor_ptr(const hf_handle* h, int which) {
+  switch (which) {
+    case HF_T_STATE: return h->state;
+    case HF_T_RING_K: return h->ring_k;
+    case HF_T_RING_V: return h->ring_v;
+    case HF_T_RING_TAG: return h->tags;
+    case HF_T_POS: return h->pos;
+    case HF_T_OFFSETS: return h->offsets;
+    case HF_T_DRAFT_PROJ: return h->proj;
+    case HF_T_DRAFT_MIX: return h->mix;
+  }
+  return nullptr;
+}
+
+hf_status hf_read_tensor(hf_handle* h, int32_t which, void* host_out, size_t bytes) {
+  if (!h) return HF_EINVAL;
+  size_t want = 0;
+  if (hf_tensor_bytes(h, which, &want) != HF_OK) return fail(h, HF_EINVAL, "unknown tensor id");
+  if (!host_out || bytes != want) return fail(h, HF_EINVAL, "host buffer size mismatch");
+  HF_CUDA(h, cudaSetDevice(h->device));
+  HF_CUDA(h, cudaDeviceSynchronize());
+  HF_CUDA(h, cudaMemcpy(host_out, tensor_ptr(h, which), bytes, cudaMemcpyDeviceToHost));
+  return HF_OK;
+}
+
+size_t hf_context_bytes(const hf_handle* h) {
+  if (!h) return 0;
+  size_t total = 0, b = 0;
+  for (int w : {HF_T_STATE, HF_T_RING_K, HF_T_RING_V, HF_T_RING_TAG, HF_T_POS}) {
+    hf_tensor_bytes(h, w, &b);
+    total += b;
+  }
+  return total;
+}
+
+static hf_status copy_context(hf_handle* h, void* host, size_t bytes, bool out) {
+  if (!h) return HF_EINVAL;
+  if (!host || bytes != hf_context_bytes(h)) return fail(h, HF_EINVAL, "context size mismatch");
+  HF_CUDA(h, cudaSetDevice(h->device));
+  HF_CUDA(h, cudaDeviceSynchronize());
+  size_t off = 0, b = 0;
+  for (int w : {HF_T_STATE, HF_T_RING_K, HF_T_RING_V, HF_T_RING_TAG, HF_T_POS}) {
+    hf_tensor_bytes(h, w, &b);
+    void* dev = const_cast<void*>(tensor_ptr(h, w));
+    if (out)
+      HF_CUDA(h, cudaMemcpy(bptr(host, off), dev, b, cudaMemcpyDeviceToHost));
+    else
+      HF_CUDA(h, cudaMemcpy(dev, bptr(host, off), b, cudaMemcpyHostToDevice));
+    off += b;
+  }
+  return HF_OK;
+}
+
+hf_status hf_export_context(hf_handle* h, void* host_out, size_t bytes) {
+  return copy_context(h, host_out, bytes, true);
+}
+
+hf_status hf_import_context(hf_handle* h, const void* host_in, size_t bytes) {
+  return copy_context(h, const_cast<void*>(host_in), bytes, false);
+}
+
+hf_status hf_profile_enable(hf_handle* h, int32_t on) {
+  if (!h) return HF_EINVAL;
+  h->prof = on != 0;
+  return HF_OK;
+}
+
+hf_status hf_profile_read(hf_handle* h, int32_t family, double* total_ms, int64_t* launches,
+                          int32_t reset) {
+  if (!h || family < 0 || family >= HF_K_COUNT) return HF_EINVAL;
+  HF_CUDA(h, cudaSetDevice(h->device));
+  hf_status s = drain_profile(h);
+  if (s != HF_OK) return s;
+  if (total_ms) *total_ms = h->tot_ms[family];
+  if (launches) *launches = h->nl[family];
+  if (reset) {
+    h->tot_ms[family] = 0;
+    h->nl[family] = 0;
+  }
+  return HF_OK;
+}
+
+int64_t hf_launch_count(const hf_handle* h) { return h ? h->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+"""Shared driver for parity tests: one library handle and one oracle fed the
+same seeded inputs (from the workload module), compared element by element."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import hyflash_oracle as O
+from workload import make_layer_weights
+
+# Tolerances: max-normalised error |g - r|_inf / |r|_inf per compared tensor.
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def maxnorm_err(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = float(np.max(np.abs(ref))) if ref.size else 0.0
+    num = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    if den == 0.0:
+        return num
+    return num / den
+
+
+class Pair:
+    """A GPU handle and an oracle over the same weights and inputs."""
+
+    def __init__(self, cfg, batch=None, prefill_tokens_max=0, seed=0, oracle=True):
+        import speculative_decoding_drafter_hf_gb300 as hf
+        self.cfg = cfg
+        self.B = cfg.batch if batch is None else batch
+        self.weights = [make_layer_weights(cfg, l, seed) for l in range(cfg.n_layers)]
+        self.gpu = hf.Drafter(cfg, self.B, prefill_tokens_max=prefill_tokens_max)
+        for l, w in enumerate(self.weights):
+            self.gpu.set_weights(l, w)
+        self.orc = O.OracleDrafter(cfg, self.weights, self.B) if oracle else None
+        self.tol = TOL[cfg.dtype]
+
+    def close(self):
+        self.gpu.close()
+
+    def prefill(self, lens, feats, requests=None):
+        self.gpu.prefill(feats.cuda(), lens, requests)
+        if self.orc is not None:
+            self.orc.prefill(lens, feats, requests=requests)
+
+    def commit(self, feats, n):
+        self.gpu.commit(feats.cuda(), n.to(torch.int32).cuda())
+        if self.orc is not None:
+            return self.orc.commit(feats, n.numpy())
+        return None
+
+    def draft(self, slot):
+        out = self.gpu.draft(slot.cuda())
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy().astype(np.float64)
+        ref = self.orc.draft(slot) if self.orc is not None else None
+        return got, ref
+
+    def check_context(self, requests=None, what=""):
+        """State, ring (valid slots), tags and positions against the oracle."""
+        cfg, g = self.cfg, self.gpu
+        import speculative_decoding_drafter_hf_gb300 as hf
+        state = g.read(hf.Tensor.STATE)
+        rk = g.read(hf.Tensor.RING_K)
+        rv = g.read(hf.Tensor.RING_V)
+        tags = g.read(hf.Tensor.RING_TAG)
+        pos = g.read(hf.Tensor.POS)
+        reqs = range(self.B) if requests is None else requests
+        worst = 0.0
+        for b in reqs:
+            for l in range(cfg.n_layers):
+                c = self.orc.ctx[b][l]
+                assert pos[b] == c.pos, f"{what}: pos of request {b}: {pos[b]} != {c.pos}"
+                assert np.array_equal(tags[b], c.tag.astype(np.int32)), f"{what}: ring tags of request {b}"
+                e = maxnorm_err(state[l, b], c.h)
+                assert e <= self.tol, f"{what}: state err {e:.3e} (layer {l}, request {b})"
+                worst = max(worst, e)
+                valid = c.tag >= 0
+                if valid.any():
+                    for name, gr, orr in (("K", rk, c.ring_k), ("V", rv, c.ring_v)):
+                        e = maxnorm_err(gr[l, b][:, valid, :], orr[:, valid, :])
+                        assert e <= self.tol, f"{what}: ring {name} err {e:.3e} (layer {l}, request {b})"
+                        worst = max(worst, e)
+        return worst

@@ -1,0 +1,83 @@
+"""The C-ABI library loads here (no GPU) and exports every declared symbol;
+host-side argument checks answer without touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hyflash.h")
+
+
+def _ensure_built():
+    from speculative_decoding_drafter_hf_gb300 import build
+    return build.build()
+
+
+@pytest.fixture(scope="module")
+def hf():
+    _ensure_built()
+    import speculative_decoding_drafter_hf_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hf_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(hf):
+    lib = ctypes.CDLL(hf.LIB_PATH)
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in hyflash.h but not exported"
+    assert set(names) == set(hf.EXPORTED)
+
+
+def test_config_struct_layout(hf):
+    assert ctypes.sizeof(hf.HfConfig) == 64
+    assert ctypes.sizeof(hf.HfLayerWeights) == 11 * ctypes.sizeof(ctypes.c_void_p)
+
+
+def _cfg(hf, **kw):
+    from workload import CONFIGS
+    c = hf.make_config(CONFIGS["tiny_fp32"], 2)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value", [
+    ("n_groups", 2), ("n_kv_heads", 3), ("head_dim", 66), ("window", 7), ("chunk", 100),
+    ("dtype", 5), ("d_model", 250), ("block", 17), ("d_state", 18), ("max_batch", 0),
+    ("prefill_tokens_max", -1), ("ssm_headdim", 130)])
+def test_invalid_config_is_einval_without_cuda(hf, field, value):
+    from speculative_decoding_drafter_hf_gb300 import _binding as B
+    h = ctypes.c_void_p()
+    s = B.hf_create(ctypes.byref(_cfg(hf, **{field: value})), 0, ctypes.byref(h))
+    assert s == hf.Status.EINVAL and not h.value
+    assert B.hf_last_error(None).decode()
+
+
+def test_null_handle_calls_are_einval(hf):
+    from speculative_decoding_drafter_hf_gb300 import _binding as B
+    assert B.hf_draft(None, None, None, 1, None) == hf.Status.EINVAL
+    assert B.hf_commit(None, None, None, 1, None) == hf.Status.EINVAL
+    assert B.hf_sync(None, None) == hf.Status.EINVAL
+    assert B.hf_context_bytes(None) == 0
+    assert B.hf_launch_count(None) == 0
+    B.hf_destroy(None)
+    assert B.hf_status_string(5) == b"HF_EDEVICE"
+
+
+def test_valid_config_without_gpu_is_ecuda(hf):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from speculative_decoding_drafter_hf_gb300 import _binding as B
+    h = ctypes.c_void_p()
+    s = B.hf_create(ctypes.byref(_cfg(hf)), 0, ctypes.byref(h))
+    assert s == hf.Status.ECUDA and not h.value

@@ -1,0 +1,156 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Bars: ring tags, positions and commit offsets bit-exact; floating point
+within max-normalised 1e-4 (fp32 mode) or 2e-2 (bf16 mode) per tensor.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _harness import Pair, maxnorm_err
+from speculative_decoding_drafter_hf_gb300 import Tensor
+from workload import (CONFIGS, make_accepted, make_prefix_feats, make_prefix_lens,
+                      make_round_inputs)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from speculative_decoding_drafter_hf_gb300 import build
+    build.build()
+
+
+def run_rounds(p: Pair, rounds: int, check_every: int = 1, n_override=None):
+    cfg = p.cfg
+    worst = 0.0
+    for r in range(rounds):
+        slot, feats = make_round_inputs(cfg, r, p.B)
+        got, ref = p.draft(slot)
+        e = maxnorm_err(got, ref)
+        assert e <= p.tol, f"round {r}: draft err {e:.3e}"
+        worst = max(worst, e)
+        n = make_accepted(cfg, r, p.B) if n_override is None else n_override(r)
+        offs, _ = p.commit(feats, n)
+        got_offs = p.gpu.read(Tensor.OFFSETS)
+        assert np.array_equal(got_offs[:p.B + 1], offs.astype(np.int32)), f"round {r}: offsets"
+        if (r + 1) % check_every == 0 or r == rounds - 1:
+            worst = max(worst, p.check_context(what=f"round {r}"))
+    return worst
+
+
+def test_tiny_fp32_all_rounds():
+    cfg = CONFIGS["tiny_fp32"]
+    p = Pair(cfg)
+    lens = make_prefix_lens(cfg)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="prefill")
+    run_rounds(p, cfg.rounds)
+    p.close()
+
+
+def test_tiny_fp32_batch_ragged_multilayer_segments():
+    # several requests, prefixes empty / shorter than W / longer than W and not
+    # a multiple of the prefill pass, three layers, tiny prefill passes
+    cfg = CONFIGS["tiny_fp32"].replace(n_layers=3, batch=5)
+    p = Pair(cfg, prefill_tokens_max=50)
+    lens = [0, 13, 64, 65, 301]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="prefill")
+    run_rounds(p, 6)
+    p.close()
+
+
+def test_prefill_subset_of_requests_leaves_others():
+    cfg = CONFIGS["tiny_fp32"].replace(batch=4)
+    p = Pair(cfg)
+    lens = [100, 7, 70, 0]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    run_rounds(p, 2)
+    lens2 = [33, 129]
+    p.prefill(lens2, make_prefix_feats(cfg, lens2, seed=5), requests=[2, 0])
+    p.check_context(what="re-prefill")
+    run_rounds(p, 2)
+    p.close()
+
+
+def test_draft_is_read_only_bytewise():
+    cfg = CONFIGS["tiny_fp32"].replace(batch=2)
+    p = Pair(cfg, oracle=False)
+    lens = [80, 20]
+    p.gpu.prefill(make_prefix_feats(cfg, lens).cuda(), lens)
+    before = p.gpu.export_context()
+    slot, _ = make_round_inputs(cfg, 0, 2)
+    p.gpu.draft(slot.cuda())
+    torch.cuda.synchronize()
+    assert p.gpu.export_context() == before
+    p.close()
+
+
+def test_rejected_rows_and_zero_counts_never_change_anything():
+    cfg = CONFIGS["tiny_fp32"].replace(batch=3)
+    p = Pair(cfg, oracle=False)
+    lens = [70, 5, 0]
+    p.gpu.prefill(make_prefix_feats(cfg, lens).cuda(), lens)
+    start = p.gpu.export_context()
+    _, feats = make_round_inputs(cfg, 1, 3)
+    n = torch.tensor([3, 0, 8], dtype=torch.int32)
+    p.gpu.commit(feats.cuda(), n.cuda())
+    after_a = p.gpu.export_context()
+    p.gpu.import_context(start)
+    feats2 = feats.clone()
+    feats2[0, 3:] = torch.randn(5, cfg.d_model) * 50
+    feats2[1, :] = torch.randn(8, cfg.d_model) * 50
+    p.gpu.commit(feats2.cuda(), n.cuda())
+    assert p.gpu.export_context() == after_a
+    p.gpu.import_context(start)
+    p.gpu.commit(feats2.cuda(), torch.zeros(3, dtype=torch.int32).cuda())
+    assert p.gpu.export_context() == start
+    p.gpu.sync()
+    p.close()
+
+
+def test_invalid_accepted_count_is_flagged_and_skipped():
+    cfg = CONFIGS["tiny_fp32"].replace(batch=3)
+    p = Pair(cfg)
+    lens = [40, 40, 40]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    _, feats = make_round_inputs(cfg, 2, 3)
+    n = torch.tensor([2, 9, 5], dtype=torch.int32)
+    offs, err = p.commit(feats, n)
+    assert err
+    import speculative_decoding_drafter_hf_gb300 as hf
+    st, msg = p.gpu.sync_status()
+    assert st == hf.Status.EDEVICE and "accepted" in msg
+    assert p.gpu.sync_status()[0] == hf.Status.OK  # the word is cleared
+    assert np.array_equal(p.gpu.read(hf.Tensor.OFFSETS)[:4], offs.astype(np.int32))
+    p.check_context(what="after invalid count")
+    n = torch.tensor([-1, 1, 1], dtype=torch.int32)
+    p.commit(feats, n)
+    assert p.gpu.sync_status()[0] == hf.Status.EDEVICE
+    p.check_context(what="after negative count")
+    p.close()
+
+
+def test_qwen3_4b_shape_bf16():
+    cfg = CONFIGS["qwen3_4b_bf16"]
+    p = Pair(cfg)
+    lens = make_prefix_lens(cfg)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="prefill")
+    run_rounds(p, 8, check_every=4)
+    p.close()
+
+
+def test_serving_shape_bf16_subset():
+    # serving-batch shape (3 layers, Qwen3-4B widths) with 6 requests of
+    # log-uniform prefixes; requests are independent, so a subset is exact.
+    cfg = CONFIGS["serving_qwen3_4b_b64"].replace(batch=6, prefix_lo=600, prefix_hi=3000)
+    p = Pair(cfg)
+    lens = make_prefix_lens(cfg)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="prefill")
+    run_rounds(p, 4, check_every=2)
+    p.close()
