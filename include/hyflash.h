@@ -87,7 +87,7 @@ typedef struct {
   int32_t max_batch;    /* requests held by the handle */
   int32_t chunk;        /* prefill scan chunk length: 64, 128 or 256 */
   int32_t dtype;        /* hf_dtype */
-  int64_t prefill_tokens_max; /* tokens per internal prefill pass; 0 = 32768 */
+  int64_t prefill_tokens_max; /* tokens per internal prefill pass; 0 = 16384 */
 } hf_config;
 
 /* One layer's weights, HOST pointers, row-major [in, out] in the handle's
@@ -155,7 +155,8 @@ hf_status hf_sync(hf_handle* h, void* stream);
 
 /* Message for the last non-OK status of this handle ("" if none); the
  * pointer stays valid until the next call on the handle. h may be NULL
- * (then the message of the last failed hf_create in this thread). */
+ * (then the message of the last failed call without a handle -- hf_create
+ * or hf_attention_noalloc -- in this thread). */
 const char* hf_last_error(const hf_handle* h);
 
 /* Static name of a status code. */
@@ -220,6 +221,49 @@ hf_status hf_profile_read(hf_handle* h, int32_t family, double* total_ms,
 
 /* Number of kernels this handle has launched since creation. */
 int64_t hf_launch_count(const hf_handle* h);
+
+/* ---- allocation-free window attention --------------------------------
+ *
+ * The pages have no counterpart to this call. It runs the same window+block
+ * attention kernels as hf_draft (split over the window, then combined), but
+ * it keeps the split partials in one fixed array compiled into the
+ * library's device image instead of in memory a handle allocated. It is for
+ * callers that cannot allocate device memory when they run the op: a host
+ * that gives all of the GPU's memory to its own arena, a serving loop whose
+ * memory was sized once at start-up, or code that must not cause the
+ * device-wide synchronisation cudaMalloc/cudaFree can bring. This call
+ * makes no cudaMalloc, cudaFree or other allocating call.
+ *
+ * The fixed array holds 4,194,304 floats (16 MiB) and exists on every GPU
+ * that loads the library until the process exits. A call needs
+ *   batch * n_kv_heads * ceil(window / 32) * (n_q_heads / n_kv_heads)
+ *         * block * (head_dim + 2)
+ * floats of it; a larger call returns HF_EINVAL and launches nothing.
+ * All calls share the one array: calls that can overlap on the GPU (other
+ * streams, other host threads) race and must be ordered by the caller. Each
+ * call rewrites every partial it later reads, so nothing needs clearing.
+ * The first call on each device looks up the array's device address (once,
+ * with that device current); make that first call before any stream
+ * capture.
+ *
+ * Arguments (all buffers DEVICE memory on the current device, caller-owned):
+ *   dtype     HF_F32 or HF_BF16: element type of ring_k, ring_v and out.
+ *   proj      fp32 [batch*block, proj_ld]: row b*block+s holds slot s of
+ *             request b: query head h at columns [h*dh, (h+1)*dh), slot key
+ *             of KV head g at Hq*dh + g*dh, slot value at Hq*dh + Hkv*dh + g*dh
+ *             (proj_ld >= Hq*dh + 2*Hkv*dh; the draft projection layout).
+ *   ring_k/v  [batch, Hkv, window, dh]: window entries; the first
+ *             min(pos_b, window) slots of request b are attended.
+ *   pos       int64 [batch]: committed tokens per request.
+ *   out       [batch*block, out_ld]: attention output of head h written to
+ *             columns [h*dh, (h+1)*dh) (out_ld >= Hq*dh); other columns kept.
+ * Errors: HF_EINVAL for bad sizes or pointers (message in
+ * hf_last_error(NULL)), HF_ECUDA for a failed launch. */
+hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t n_q_heads,
+                               int32_t n_kv_heads, int32_t head_dim, int32_t window,
+                               int32_t block, const float* proj, int32_t proj_ld,
+                               const void* ring_k, const void* ring_v, const int64_t* pos,
+                               void* out, int32_t out_ld, void* stream);
 
 #ifdef __cplusplus
 }

@@ -104,11 +104,13 @@ hf_profile_enable = _sig("hf_profile_enable", _st, _h, _i32)
 hf_profile_read = _sig("hf_profile_read", _st, _h, _i32, ctypes.POINTER(ctypes.c_double),
                        ctypes.POINTER(ctypes.c_int64), _i32)
 hf_launch_count = _sig("hf_launch_count", ctypes.c_int64, _h)
+hf_attention_noalloc = _sig("hf_attention_noalloc", _st, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                            _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp)
 
 EXPORTED = ("hf_create", "hf_destroy", "hf_set_weights", "hf_prefill", "hf_commit", "hf_draft",
             "hf_sync", "hf_last_error", "hf_status_string", "hf_tensor_bytes", "hf_read_tensor",
             "hf_context_bytes", "hf_export_context", "hf_import_context", "hf_profile_enable",
-            "hf_profile_read", "hf_launch_count")
+            "hf_profile_read", "hf_launch_count", "hf_attention_noalloc")
 
 
 class HyflashError(RuntimeError):

@@ -10,6 +10,9 @@
 //
 // Memory read: y[s, h, p] = sum_n state[h, p, n] * C_s[s, n], with C_s the
 // slot projection through W_C; the state is only read.
+#include <cstdio>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace hf {
@@ -204,3 +207,126 @@ cudaError_t launch_attn_mem(int dtype, const Dims& d, int B, const float* proj,
 }
 
 }  // namespace hf
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the window+block attention.
+//
+// Some callers cannot allocate device memory at the moment they need this
+// op: code running under an arena that owns all of the GPU's memory, a
+// serving loop whose memory was sized once at start-up, or a host that must
+// not trigger the device-wide synchronisation cudaMalloc/cudaFree can cause.
+// For them the split partials live in one fixed array in the library's own
+// device image instead of in a handle's scratch. The array exists on every
+// GPU that loads the library, from load until the process exits.
+namespace hf {
+namespace {
+
+constexpr size_t kNoAllocFloats = (size_t)4 << 20;  // 16 MiB of fp32 partials
+static __device__ __align__(256) float g_noalloc_attn_scratch[kNoAllocFloats];
+
+constexpr int kMaxDevices = 64;
+float* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// The symbol's device address on the current device, looked up once per
+// device (host code must not use the array's name as a device pointer).
+cudaError_t noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_attn_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t run_noalloc(const Dims& d, int B, const float* proj, const void* ring_k,
+                        const void* ring_v, const int64_t* pos, void* out, int nsplit,
+                        float* scratch, cudaStream_t st) {
+  const int R = d.G * d.S, dhp = d.dh + 4, JK = JT + d.S;
+  const size_t n_o = (size_t)B * d.Hkv * nsplit * R * d.dh;
+  float* part_o = scratch;
+  float* part_ml = scratch + n_o;
+  size_t smem = (size_t)(R * dhp + 2 * JK * dhp + R * JK) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const float qscale = 1.4426950408889634f / sqrtf((float)d.dh);
+  attn_partial_kernel<T><<<dim3(nsplit, d.Hkv, B), 128, smem, st>>>(
+      d, proj, (const T*)ring_k, (const T*)ring_v, pos, part_o, part_ml, nsplit, qscale);
+  attn_combine_kernel<T><<<dim3(d.Hkv, B), 256, 0, st>>>(d, part_o, part_ml, nsplit, (T*)out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace hf
+
+extern "C" hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t n_q_heads,
+                                          int32_t n_kv_heads, int32_t head_dim, int32_t window,
+                                          int32_t block, const float* proj, int32_t proj_ld,
+                                          const void* ring_k, const void* ring_v,
+                                          const int64_t* pos, void* out, int32_t out_ld,
+                                          void* stream) {
+  using namespace hf;
+  auto bad = [](const char* m) {
+    set_thread_error(m);
+    return HF_EINVAL;
+  };
+  if (dtype != HF_F32 && dtype != HF_BF16) return bad("dtype must be HF_F32 or HF_BF16");
+  if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || window <= 0 || block <= 0)
+    return bad("dimensions must be positive (batch >= 0)");
+  if (n_q_heads % n_kv_heads) return bad("n_kv_heads must divide n_q_heads");
+  if (head_dim % 4 || head_dim > 256) return bad("head_dim must be a multiple of 4, <= 256");
+  if (block > MAXS || (n_q_heads / n_kv_heads) * block > 64)
+    return bad("block must be <= 16 and (n_q_heads/n_kv_heads)*block <= 64");
+  const long long qd = (long long)n_q_heads * head_dim, kvd = (long long)n_kv_heads * head_dim;
+  if (proj_ld < qd + 2 * kvd) return bad("proj_ld must be >= Hq*dh + 2*Hkv*dh");
+  if (out_ld < qd) return bad("out_ld must be >= Hq*dh");
+  if (batch == 0) return HF_OK;
+  if (!proj || !ring_k || !ring_v || !pos || !out) return bad("NULL buffer");
+  const int nsplit = (window + JT - 1) / JT;
+  const long long R = (long long)(n_q_heads / n_kv_heads) * block;
+  const long long need = (long long)batch * n_kv_heads * nsplit * R * (head_dim + 2);
+  if (need > (long long)kNoAllocFloats) {
+    char m[200];
+    snprintf(m, sizeof m,
+             "hf_attention_noalloc: needs %lld floats of scratch, the fixed array holds %zu "
+             "(batch * n_kv_heads * ceil(window/32) * (Hq/Hkv) * block * (head_dim + 2))",
+             need, kNoAllocFloats);
+    set_thread_error(m);
+    return HF_EINVAL;
+  }
+  float* scratch = nullptr;
+  cudaError_t e = noalloc_scratch(&scratch);
+  if (e == cudaSuccess) {
+    Dims d{};
+    d.Hq = n_q_heads;
+    d.Hkv = n_kv_heads;
+    d.dh = head_dim;
+    d.W = window;
+    d.S = block;
+    d.G = n_q_heads / n_kv_heads;
+    d.QD = (int)qd;
+    d.KVD = (int)kvd;
+    d.Nd = proj_ld;
+    d.Nz = out_ld;
+    d.esize = dtype == HF_F32 ? 4 : 2;
+    cudaStream_t st = (cudaStream_t)stream;
+    e = dtype == HF_F32
+            ? run_noalloc<float>(d, batch, proj, ring_k, ring_v, pos, out, nsplit, scratch, st)
+            : run_noalloc<__nv_bfloat16>(d, batch, proj, ring_k, ring_v, pos, out, nsplit, scratch,
+                                         st);
+  }
+  if (e != cudaSuccess) {
+    set_thread_error(cudaGetErrorString(e));
+    return HF_ECUDA;
+  }
+  return HF_OK;
+}

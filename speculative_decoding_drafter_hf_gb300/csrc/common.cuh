@@ -154,6 +154,9 @@ cudaError_t launch_prefill_scan(const Dims& d, int layer, int n_req, const int32
                                 const int32_t* reqs, long long seg0, long long seg1,
                                 const float* xbd, const float* A_log, float* state,
                                 cudaStream_t st);
+// Message reported by hf_last_error(NULL) for calls that have no handle.
+void set_thread_error(const char* msg);
+
 cudaError_t launch_prefill_finish(int n_req, const int32_t* lens, const int32_t* reqs,
                                   int64_t* pos, cudaStream_t st);
 

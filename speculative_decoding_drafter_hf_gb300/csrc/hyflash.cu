@@ -247,6 +247,10 @@ const char* bptr(const void* p, size_t off) { return static_cast<const char*>(p)
 
 }  // namespace
 
+namespace hf {
+void set_thread_error(const char* msg) { g_create_error = msg ? msg : ""; }
+}  // namespace hf
+
 extern "C" {
 
 const char* hf_status_string(hf_status s) {
