@@ -122,6 +122,15 @@ cudaError_t launch_gemm_fma(int dtype, const void* X, int ldx, const void* Wt, i
                             int R, int C, int K, int splits, float* part,
                             const Epi& epi, cudaStream_t st, int* launches);
 
+// bf16 tensor-core GEMM: D[m, n] = sum_k A[m, k] * B[n, k], A [M, K] with row
+// stride lda, B [N, K] with row stride ldb (elements, multiples of 8). With
+// swap = 1 the epilogue sees (row n, column m), else (row m, column n).
+// ws / counters: split-K partial tiles and per-tile tickets (kept at zero).
+cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb,
+                           int N, int K, int swap, int splits, float* ws, size_t ws_elems,
+                           int* counters, int n_counters, int32_t* err, const Epi& epi,
+                           cudaStream_t st, int* launches);
+
 // Window+block attention and memory read for one layer, batch B.
 // proj [B*S, Nd] fp32 (Q|K_s|V_s|C_s); ring_k/v of this layer; pos [Bmax];
 // state of this layer; mix [B*S, Nz] model dtype (O | y).

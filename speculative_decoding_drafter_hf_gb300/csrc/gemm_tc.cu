@@ -1,0 +1,402 @@
+// bf16 GEMM on the 5th-generation tensor cores: D[m, n] = sum_k A[m, k] * B[n, k].
+//
+// A and B are K-major bf16 matrices in global memory. TMA copies 64-wide
+// K slices of both into 128-byte-swizzled shared memory (a ring of STAGES
+// slots guarded by mbarriers), one elected thread issues tcgen05.mma
+// (M = 128, N = BN, K = 16 per instruction) into an fp32 accumulator in
+// tensor memory, and all four warps read the accumulator back with
+// tcgen05.ld for the epilogue.
+//
+// Two uses:
+//  * skinny (draft / commit): A = weights [out features, K], B = the few
+//    activation rows (7 slots per request, or the accepted rows), so the
+//    weights stream through the tensor core exactly once; the epilogue maps
+//    D[m, n] to output row n, column m ("swap"). Split-K over CTAs keeps
+//    every SM streaming; partial tiles are summed by the last CTA to finish
+//    a tile, in split order (deterministic, no atomics on data, no waiting).
+//  * prefill: A = the prefix features [tokens, K], B = weight rows; output
+//    row m, column n.
+//
+// Every mbarrier wait is bounded (clock-based); on expiry the CTA raises
+// ERR_TIMEOUT in the device error word, drains the copies it issued (again
+// bounded), frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace hf {
+namespace {
+
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile whose rows are 128 bytes
+// (64 bf16) with the 128-byte swizzle; 8-row groups are 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(const void* p) {
+  const uint64_t a = smem_u32(p);
+  uint64_t d = (a >> 4) & 0x3FFFull;   // start address
+  d |= 1ull << 16;                     // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset: 8 rows x 128 B
+  d |= 1ull << 46;                     // descriptor version
+  d |= 2ull << 61;                     // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulate, both
+// operands K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct TcArgs {
+  int M, N, K;        // D is M x N
+  int kblocks;        // ceil(K / 64)
+  int splits;         // split-K factor (grid.z)
+  int swap;           // 1: output row = n, column = m; 0: row = m, column = n
+  float* ws;          // split-K partial tiles
+  int* counters;      // one ticket counter per output tile, left at zero
+  int32_t* err;       // device error word
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(128, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+               TcArgs a, Epi epi) {
+  constexpr int A_BYTES = 128 * 128;
+  constexpr int B_BYTES = BN * 128;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t NCOLS = BN < 32 ? 32 : BN;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* done = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] issued, [2] consumed, [3] last
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int m_tile = blockIdx.x, n_tile = blockIdx.y, split = blockIdx.z;
+  const int kb0 = (int)((long long)split * a.kblocks / a.splits);
+  const int kb1 = (int)((long long)(split + 1) * a.kblocks / a.splits);
+  const int nkb = kb1 - kb0;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    flags[0] = flags[1] = flags[2] = flags[3] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(NCOLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    int i = 0;
+    for (; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      if (i >= STAGES && !mbar_wait(&empty[s], ph ^ 1u)) {
+        atomicExch(&flags[0], 1);
+        break;
+      }
+      if (*(volatile int*)&flags[0]) break;
+      mbar_expect_tx(&full[s], STAGE_BYTES);
+      tma_load_2d(sA + s * A_BYTES, &ta, &full[s], (kb0 + i) * 64, m_tile * 128);
+      tma_load_2d(sB + s * B_BYTES, &tb, &full[s], (kb0 + i) * 64, n_tile * BN);
+    }
+    flags[1] = i;
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(BN < 16 ? 16 : BN);
+    int i = 0;
+    for (; i < nkb; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
+      if (!mbar_wait(&full[s], ph)) {
+        atomicExch(&flags[0], 1);
+        break;
+      }
+      tc_fence_after();
+      const uint64_t da = sdesc_sw128(sA + s * A_BYTES);
+      const uint64_t db = sdesc_sw128(sB + s * B_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem, da + 2ull * kk, db + 2ull * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&empty[s]);
+    }
+    flags[2] = i;
+    umma_commit(done);
+  }
+  __syncwarp();
+
+  const bool ok = mbar_wait(done, 0);
+  if (__syncthreads_or(!ok || flags[0])) {
+    // Timed out somewhere: report, drain issued copies (bounded), free TMEM.
+    if (tid == 0) {
+      atomicOr(a.err, ERR_TIMEOUT);
+      for (int i = flags[2]; i < flags[1]; ++i)
+        mbar_wait(&full[i % STAGES], (uint32_t)(i / STAGES) & 1u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOLS));
+    return;
+  }
+  tc_fence_after();
+
+  const int m_local = warp * 32 + lane;
+  const int m = m_tile * 128 + m_local;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  float v[16];
+  if (a.splits == 1) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      tmem_ld16(trow + c0, v);
+      if (m < a.M) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int n = n_tile * BN + c0 + j;
+          if (n < a.N) {
+            if (a.swap)
+              epi_apply<__nv_bfloat16>(epi, n, m, v[j]);
+            else
+              epi_apply<__nv_bfloat16>(epi, m, n, v[j]);
+          }
+        }
+      }
+    }
+  } else {
+    const int tile = m_tile * gridDim.y + n_tile;
+    const size_t tile_elems = (size_t)BN * 128;
+    float* part = a.ws + ((size_t)tile * a.splits + split) * tile_elems;
+    const int n_here = min(BN, a.N - n_tile * BN);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      tmem_ld16(trow + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < n_here) part[(size_t)(c0 + j) * 128 + m_local] = v[j];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const int t = atomicAdd(&a.counters[tile], 1);
+      flags[3] = (t == a.splits - 1);
+    }
+    __syncthreads();
+    if (flags[3]) {
+      __threadfence();
+      const float* base = a.ws + (size_t)tile * a.splits * tile_elems;
+      for (int nl = 0; nl < n_here; ++nl) {
+        float s = 0.f;
+        for (int sp = 0; sp < a.splits; ++sp)
+          s += __ldcg(&base[(size_t)sp * tile_elems + (size_t)nl * 128 + m_local]);
+        if (m < a.M) {
+          const int n = n_tile * BN + nl;
+          if (a.swap)
+            epi_apply<__nv_bfloat16>(epi, n, m, s);
+          else
+            epi_apply<__nv_bfloat16>(epi, m, n, s);
+        }
+      }
+      if (tid == 0) a.counters[tile] = 0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOLS));
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      g_encode_err = e != cudaSuccess ? e : cudaErrorNotSupported;
+    else
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode_err;
+}
+
+// 2-D bf16 tensor map over rows x K (row stride ld elements), box 64 x box_rows.
+cudaError_t make_map(CUtensorMap* map, const void* base, long long rows, long long K, long long ld,
+                     int box_rows) {
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& a,
+                      const Epi& epi, dim3 grid, cudaStream_t st) {
+  constexpr size_t smem = 1024 + (size_t)STAGES * (128 * 128 + BN * 128) + (2 * STAGES + 1) * 8 + 32;
+  static bool configured = false;  // per instantiation; attribute is per-device-global
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  tc_gemm_kernel<BN, STAGES><<<grid, 128, smem, st>>>(ma, mb, a, epi);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb, int N,
+                           int K, int swap, int splits, float* ws, size_t ws_elems, int* counters,
+                           int n_counters, int32_t* err, const Epi& epi, cudaStream_t st,
+                           int* launches) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  int bn = 16;
+  while (bn < N && bn < 256) bn *= 2;
+  const int m_tiles = (M + 127) / 128;
+  const int n_tiles = (N + bn - 1) / bn;
+  TcArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.kblocks = (K + 63) / 64;
+  a.swap = swap;
+  a.err = err;
+  a.counters = counters;
+  a.ws = ws;
+  splits = std::max(1, std::min(splits, a.kblocks));
+  const size_t tile_elems = (size_t)bn * 128;
+  while (splits > 1 && (size_t)m_tiles * n_tiles * splits * tile_elems > ws_elems) --splits;
+  if (splits > 1 && m_tiles * n_tiles > n_counters) splits = 1;
+  a.splits = splits;
+  CUtensorMap ma, mb;
+  cudaError_t e = make_map(&ma, A, M, K, lda, 128);
+  if (e != cudaSuccess) return e;
+  e = make_map(&mb, B, N, K, ldb, bn);
+  if (e != cudaSuccess) return e;
+  dim3 grid(m_tiles, n_tiles, splits);
+  ++*launches;
+  switch (bn) {
+    case 16: return launch_tc<16, 6>(ma, mb, a, epi, grid, st);
+    case 32: return launch_tc<32, 6>(ma, mb, a, epi, grid, st);
+    case 64: return launch_tc<64, 5>(ma, mb, a, epi, grid, st);
+    case 128: return launch_tc<128, 4>(ma, mb, a, epi, grid, st);
+    default: return launch_tc<256, 4>(ma, mb, a, epi, grid, st);
+  }
+}
+
+}  // namespace hf

@@ -55,6 +55,8 @@ struct hf_handle {
   int nsplit = 1;
   float* part = nullptr;
   size_t part_elems = 0;
+  int* counters = nullptr;     // split-K tickets of the tensor-core GEMM
+  int n_counters = 0;
 
   float* pf_xbd = nullptr;     // [Tseg][NS]
   long long pf_tokens = 0;
@@ -115,6 +117,8 @@ hf_status validate(const hf_config* c, std::string* why) {
   if (c->d_model % 8) return bad("d_model must be a multiple of 8");
   if (c->prefill_tokens_max < 0) return bad("prefill_tokens_max must be >= 0");
   if (c->max_batch > 65535) return bad("max_batch must be <= 65535");
+  if (c->dtype == HF_BF16 && (c->head_dim % 8 || ((long long)c->ssm_heads * c->ssm_headdim) % 8))
+    return bad("bf16 needs head_dim and ssm_heads*ssm_headdim multiples of 8");
   return HF_OK;
 }
 
@@ -222,13 +226,33 @@ int pick_splits(const hf_handle* h, long long R, long long C, long long K, int t
   return s;
 }
 
+// Y[r, c] = sum_k X[r, k] Wt[c, k] with epilogue. fp32 handles use the
+// CUDA-core kernel; bf16 handles use the tensor-core kernel with the weights
+// as the 128-row operand (they stream once) and the activation rows as N.
+cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, int ldw, int R,
+                        int C, int K, const Epi& epi, cudaStream_t st, int* count) {
+  if (R <= 0 || C <= 0) return cudaSuccess;
+  if (h->cfg.dtype == HF_F32) {
+    int splits = pick_splits(h, R, C, K, 64, 64);
+    return hf::launch_gemm_fma(h->cfg.dtype, X, ldx, Wt, ldw, R, C, K, splits, h->part, epi, st,
+                               count);
+  }
+  int bn = 16;
+  while (bn < R && bn < 256) bn *= 2;
+  const long long tiles = (long long)((C + 127) / 128) * ((R + bn - 1) / bn);
+  const int kblocks = (K + 63) / 64;
+  const int target = bn <= 16 ? 2 * 152 : 152;
+  int splits = (int)std::max<long long>(1, (target + tiles - 1) / tiles);
+  splits = std::min(splits, std::max(1, kblocks / 2));
+  return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->part, h->part_elems,
+                            h->counters, h->n_counters, h->err, epi, st, count);
+}
+
 hf_status gemm(hf_handle* h, int fam, const void* X, int ldx, const void* Wt, int ldw, int R,
                int C, int K, const Epi& epi, cudaStream_t st) {
   if (R <= 0 || C <= 0) return HF_OK;
-  int splits = pick_splits(h, R, C, K, 64, 64);
   Scope sc(h, fam, st);
-  cudaError_t e = hf::launch_gemm_fma(h->cfg.dtype, X, ldx, Wt, ldw, R, C, K, splits, h->part,
-                                      epi, st, &sc.count);
+  cudaError_t e = gemm_launch(h, X, ldx, Wt, ldw, R, C, K, epi, st, &sc.count);
   if (e != cudaSuccess) return cuda_fail(h, e, "gemm launch");
   return HF_OK;
 }
@@ -326,6 +350,8 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   A((void**)&h->attn_o, Bm * d.Hkv * h->nsplit * R * d.dh * 4);
   A((void**)&h->attn_ml, Bm * d.Hkv * h->nsplit * R * 2 * 4);
   A((void**)&h->part, h->part_elems * 4);
+  h->n_counters = 1 << 16;
+  A((void**)&h->counters, (size_t)h->n_counters * 4);
   A((void**)&h->pf_xbd, (size_t)h->pf_tokens * d.NS * 4);
   A((void**)&h->pf_lens, Bm * 4);
   A((void**)&h->pf_reqs, Bm * 4);
@@ -536,9 +562,8 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
       ek.col_off = 0;
       ek.row_req = h->row_req;
       ek.row_pos = h->row_pos;
-      int splits = pick_splits(h, ring_rows, 2 * d.KVD, d.D, 64, 64);
-      e = hf::launch_gemm_fma(h->cfg.dtype, h->packed, d.D, wl, d.D, (int)ring_rows, 2 * d.KVD, d.D,
-                              splits, h->part, ek, st, &sc.count);
+      e = gemm_launch(h, h->packed, d.D, wl, d.D, (int)ring_rows, 2 * d.KVD, d.D, ek, st,
+                      &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "prefill kv gemm");
     }
     for (long long s0 = 0; s0 < total; s0 += h->pf_tokens) {
@@ -550,9 +575,16 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
       ex.col_off = 2 * d.KVD;
       ex.xbd = h->pf_xbd;
       ex.xbd_layer_stride = 0;
-      e = hf::launch_gemm_fma(h->cfg.dtype, bptr(feats, (size_t)s0 * d.D * es), d.D,
-                              wl + (size_t)2 * d.KVD * d.D * es, d.D, (int)(s1 - s0),
-                              d.dinner + d.N + d.Hm, d.D, 1, h->part, ex, st, &sc.count);
+      const void* fseg = bptr(feats, (size_t)s0 * d.D * es);
+      const void* wseg = wl + (size_t)2 * d.KVD * d.D * es;
+      const int nx = d.dinner + d.N + d.Hm;
+      if (h->cfg.dtype == HF_F32)
+        e = hf::launch_gemm_fma(h->cfg.dtype, fseg, d.D, wseg, d.D, (int)(s1 - s0), nx, d.D, 1,
+                                h->part, ex, st, &sc.count);
+      else  // tokens as the 128-row operand, features as N
+        e = hf::launch_gemm_tc(fseg, d.D, (int)(s1 - s0), wseg, d.D, nx, d.D, 0, 1, h->part,
+                               h->part_elems, h->counters, h->n_counters, h->err, ex, st,
+                               &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "prefill ssm gemm");
       e = hf::launch_prefill_scan(d, l, n_req, h->pf_lens, h->pf_reqs, s0, s1, h->pf_xbd, h->A_log,
                                   h->state, st);

@@ -154,3 +154,36 @@ def test_serving_shape_bf16_subset():
     p.check_context(what="prefill")
     run_rounds(p, 4, check_every=2)
     p.close()
+
+
+@pytest.mark.parametrize("name,lens", [("tiny_fp32", [300, 20]), ("qwen3_4b_bf16", [1500, 300])])
+def test_draft_steps_individually(name, lens):
+    """Rows a4 (slot projections), a5 (attention) and a6 (memory read) on
+    their own, read back from the handle after one draft."""
+    from oracle import hyflash_oracle as O
+    cfg = CONFIGS[name].replace(batch=len(lens))
+    p = Pair(cfg)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    slot, _ = make_round_inputs(cfg, 3, p.B)
+    got, ref = p.draft(slot)
+    S, QD, KVD = cfg.block, cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    proj = p.gpu.read(Tensor.DRAFT_PROJ)
+    mix = p.gpu.read(Tensor.DRAFT_MIX)
+    lw = p.orc.layers[0]
+    X = O.to64(slot)
+    for b in range(p.B):
+        _, parts = O.draft_layer(lw, cfg, p.orc.ctx[b][0], X[b], return_parts=True)
+        rows = slice(b * S, (b + 1) * S)
+        checks = [
+            ("Q", proj[rows, :QD], parts["Q"].reshape(S, -1)),
+            ("K_s", proj[rows, QD:QD + KVD], parts["Ks"].reshape(S, -1)),
+            ("V_s", proj[rows, QD + KVD:QD + 2 * KVD], parts["Vs"].reshape(S, -1)),
+            ("C_s", proj[rows, QD + 2 * KVD:], parts["Cs"]),
+            ("attention", mix[rows, :QD], parts["O"].reshape(S, -1)),
+            ("memory read", mix[rows, QD:], parts["y"].reshape(S, -1)),
+        ]
+        for what, g, r in checks:
+            e = maxnorm_err(g, r)
+            assert e <= p.tol, f"request {b}: {what} err {e:.3e}"
+    assert maxnorm_err(got, ref) <= p.tol
+    p.close()
