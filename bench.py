@@ -3,9 +3,11 @@
 A step is one speculative round on device-resident inputs: hf_draft (all
 layers: slot projections, window+block attention, memory read, output
 projections) followed by hf_commit (count check, projections, ring append,
-sequential memory update) for every request of the batch. The prefix is
-folded once beforehand with hf_prefill, which is timed on its own and
-reported under "prefill".
+sequential memory update) for every request of the batch. The two calls are
+captured once into a CUDA graph that reads fixed staging buffers; each step
+stages its round's inputs and replays the graph (how a serving loop would
+run it, without per-kernel host launch cost). The prefix is folded once
+beforehand with hf_prefill, which is timed on its own under "prefill".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
                     [--impl hyflash|reference]
@@ -301,54 +303,80 @@ def run_hyflash(args, cfg):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
 
-    def step(r):
-        drafter.draft(d_slot[r], out)
-        drafter.commit(d_feat[r], d_cnt[r])
+    # Fixed staging buffers: one round (draft + commit) is captured into a
+    # CUDA graph reading from them; each step stages its round's inputs
+    # (device to device, outside the timed events) and replays the graph.
+    st_slot = torch.empty_like(d_slot[0])
+    st_feat = torch.empty_like(d_feat[0])
+    st_cnt = torch.empty_like(d_cnt[0])
+
+    def stage(r):
+        st_slot.copy_(d_slot[r])
+        st_feat.copy_(d_feat[r])
+        st_cnt.copy_(d_cnt[r])
+
+    def round_calls():
+        drafter.draft(st_slot, out)
+        drafter.commit(st_feat, st_cnt)
 
     for r in range(args.warmup):
-        step(r)
+        stage(r)
+        round_calls()
     drafter.sync()
 
-    # ---- timed region: per-step events, L2 flushed between steps (untimed)
-    drafter.profile(True)
+    drafter.profile(2)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    n0 = drafter.launch_count()
+    with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
+        round_calls()
+    launches_per_step = drafter.launch_count() - n0
+    torch.cuda.current_stream().wait_stream(side)
+    for r in range(args.warmup):
+        stage(r)
+        graph.replay()
+    torch.cuda.synchronize()
+    drafter.profile_collect()
     for fam in hf.Family:
         drafter.profile_read(fam, reset=True)
-    launches0 = drafter.launch_count()
+
+    # ---- timed region: per-step events around the graph replay, L2 flushed
+    # between steps (untimed); per-family times from the library's events
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
+            stage(args.warmup + i)
             flush.zero_()
             ev[i][0].record(stream)
-            step(args.warmup + i)
+            graph.replay()
             ev[i][1].record(stream)
+            drafter.profile_collect()
         torch.cuda.synchronize()
     barrier()
     drafter.sync()
-    launches = drafter.launch_count() - launches0
+    launches = launches_per_step * args.steps
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
     fam_ms = {}
     for fam in hf.Family:
         ms, n = drafter.profile_read(fam, reset=True)
         fam_ms[fam.name.lower()] = (ms, n)
-    drafter.profile(False)
     accepted = int(d_cnt[args.warmup:].sum().item())
     total_ms_max = max_over_ranks(total_ms, dev)
     all_steps = sum_over_ranks(args.steps, dev)
     all_acc = sum_over_ranks(accepted, dev)
     value = all_steps / (total_ms_max / 1e3)
 
-    # ---- e2e: the same rounds from pinned host buffers, copies inside the timed region
+    # ---- e2e: the same rounds from pinned host buffers, the copies inside the
+    # timed region: host -> staging buffers, the captured round, output -> host
     h_slot = d_slot.cpu().pin_memory()
     h_feat = d_feat.cpu().pin_memory()
     h_cnt = d_cnt.cpu().pin_memory()
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    b_slot = torch.empty_like(d_slot[0])
-    b_feat = torch.empty_like(d_feat[0])
-    b_cnt = torch.empty_like(d_cnt[0])
     e2e_ev = []
     barrier()
     torch.cuda.synchronize()
@@ -357,17 +385,18 @@ def run_hyflash(args, cfg):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        b_slot.copy_(h_slot[r], non_blocking=True)
-        b_feat.copy_(h_feat[r], non_blocking=True)
-        b_cnt.copy_(h_cnt[r], non_blocking=True)
-        drafter.draft(b_slot, out)
-        drafter.commit(b_feat, b_cnt)
+        st_slot.copy_(h_slot[r], non_blocking=True)
+        st_feat.copy_(h_feat[r], non_blocking=True)
+        st_cnt.copy_(h_cnt[r], non_blocking=True)
+        graph.replay()
         h_out.copy_(out, non_blocking=True)
         b.record(stream)
         e2e_ev.append((a, b))
     torch.cuda.synchronize()
     barrier()
     drafter.sync()
+    del graph
+    drafter.profile(0)
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), dev)
     e2e_value = all_steps / (e2e_ms / 1e3)
     es = drafter.np_elem
@@ -421,6 +450,7 @@ def run_hyflash(args, cfg):
             "config": {"workload": cfg.name, "batch_per_gpu": batch, "prefix": cfg.prefix,
                        "layers": cfg.n_layers, "window": cfg.window, "block": cfg.block,
                        "l2": f"flushed between steps ({2 * l2 >> 20} MiB write, untimed)",
+                       "timing": "CUDA graph of one round replayed per step; CUDA events",
                        "parallelism": f"replicas x{ws}"},
             "committed_tokens_per_s": all_acc / (total_ms_max / 1e3),
             "step_ms_median": statistics.median(step_ms),

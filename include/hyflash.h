@@ -210,12 +210,22 @@ typedef enum {
   HF_K_COUNT = 8
 } hf_kernel_family;
 
-/* Turn per-kernel CUDA-event timing on/off (events recorded on the launch
- * stream around every launch; results are read with hf_profile_read). */
-hf_status hf_profile_enable(hf_handle* h, int32_t on);
+/* Per-kernel-family timing with CUDA events recorded on the launch stream
+ * around each family's launches. mode 0: off. mode 1: every call records
+ * fresh events, read once by hf_profile_collect. mode 2 (for CUDA graphs):
+ * events are recorded as external event nodes (cudaEventRecordExternal), so
+ * calls captured into a graph re-record them on every replay; the records
+ * are kept, and each hf_profile_collect adds the latest replay's times.
+ * Changing the mode synchronises the device and drops kept records: do it
+ * only when no graph holding them will be replayed again. */
+hf_status hf_profile_enable(hf_handle* h, int32_t mode);
 
-/* Synchronises, then returns total milliseconds and launches of a family
- * since the last reset, and resets that family if reset != 0. */
+/* Synchronise on the recorded events and add their elapsed times and
+ * launch counts to the per-family totals. */
+hf_status hf_profile_collect(hf_handle* h);
+
+/* Per-family totals (milliseconds, launches) accumulated by
+ * hf_profile_collect; reset != 0 zeroes that family afterwards. */
 hf_status hf_profile_read(hf_handle* h, int32_t family, double* total_ms,
                           int64_t* launches, int32_t reset);
 

@@ -101,6 +101,7 @@ hf_context_bytes = _sig("hf_context_bytes", ctypes.c_size_t, _h)
 hf_export_context = _sig("hf_export_context", _st, _h, _vp, ctypes.c_size_t)
 hf_import_context = _sig("hf_import_context", _st, _h, _vp, ctypes.c_size_t)
 hf_profile_enable = _sig("hf_profile_enable", _st, _h, _i32)
+hf_profile_collect = _sig("hf_profile_collect", _st, _h)
 hf_profile_read = _sig("hf_profile_read", _st, _h, _i32, ctypes.POINTER(ctypes.c_double),
                        ctypes.POINTER(ctypes.c_int64), _i32)
 hf_launch_count = _sig("hf_launch_count", ctypes.c_int64, _h)
@@ -110,7 +111,7 @@ hf_attention_noalloc = _sig("hf_attention_noalloc", _st, _i32, _i32, _i32, _i32,
 EXPORTED = ("hf_create", "hf_destroy", "hf_set_weights", "hf_prefill", "hf_commit", "hf_draft",
             "hf_sync", "hf_last_error", "hf_status_string", "hf_tensor_bytes", "hf_read_tensor",
             "hf_context_bytes", "hf_export_context", "hf_import_context", "hf_profile_enable",
-            "hf_profile_read", "hf_launch_count", "hf_attention_noalloc")
+            "hf_profile_collect", "hf_profile_read", "hf_launch_count", "hf_attention_noalloc")
 
 
 class HyflashError(RuntimeError):
@@ -286,8 +287,12 @@ class Drafter:
         self._check(hf_import_context(self._h, buf.ctypes.data, buf.size))
 
     # -- measurement
-    def profile(self, on: bool):
-        self._check(hf_profile_enable(self._h, 1 if on else 0))
+    def profile(self, mode):
+        """0 off, 1 (or True) per-call records, 2 records kept for graph replays."""
+        self._check(hf_profile_enable(self._h, int(mode)))
+
+    def profile_collect(self):
+        self._check(hf_profile_collect(self._h))
 
     def profile_read(self, family: int, reset: bool = False):
         ms = ctypes.c_double()

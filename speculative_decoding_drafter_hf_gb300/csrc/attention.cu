@@ -179,9 +179,6 @@ cudaError_t run(const Dims& d, int B, const float* proj, const void* ring_k, con
   if (B <= 0) return cudaSuccess;
   const int R = d.G * d.S, dhp = d.dh + 4, JK = JT + d.S;
   size_t smem = (size_t)(R * dhp + 2 * JK * dhp + R * JK) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   const float qscale = 1.4426950408889634f / sqrtf((float)d.dh);
   attn_partial_kernel<T><<<dim3(nsplit, d.Hkv, B), 128, smem, st>>>(
       d, proj, (const T*)ring_k, (const T*)ring_v, pos, part_o, part_ml, nsplit, qscale);
@@ -194,6 +191,24 @@ cudaError_t run(const Dims& d, int B, const float* proj, const void* ring_k, con
 }
 
 }  // namespace
+
+// Dynamic shared memory of the attention kernel is raised once per process
+// (at handle creation), so launches stay legal inside stream capture.
+cudaError_t configure_attn(const Dims& d) {
+  const int R = d.G * d.S, dhp = d.dh + 4, JK = JT + d.S;
+  const int smem = (int)((size_t)(R * dhp + 2 * JK * dhp + R * JK) * sizeof(float));
+  static int configured = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (smem <= configured) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<float>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_partial_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) configured = smem;
+  return e;
+}
 
 cudaError_t launch_attn_mem(int dtype, const Dims& d, int B, const float* proj,
                             const void* ring_k, const void* ring_v, const int64_t* pos,

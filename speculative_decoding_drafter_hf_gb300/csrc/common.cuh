@@ -131,6 +131,11 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
                            int* counters, int n_counters, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches);
 
+// One-time kernel attribute set-up (dynamic shared memory limits, driver
+// entry points), done at handle creation.
+cudaError_t configure_tc();
+cudaError_t configure_attn(const Dims& d);
+
 // Window+block attention and memory read for one layer, batch B.
 // proj [B*S, Nd] fp32 (Q|K_s|V_s|C_s); ring_k/v of this layer; pos [Bmax];
 // state of this layer; mix [B*S, Nz] model dtype (O | y).

@@ -344,21 +344,37 @@ cudaError_t make_map(CUtensorMap* map, const void* base, long long rows, long lo
 }
 
 template <int BN, int STAGES>
+constexpr size_t tc_smem() {
+  return 1024 + (size_t)STAGES * (128 * 128 + BN * 128) + (2 * STAGES + 1) * 8 + 32;
+}
+
+template <int BN, int STAGES>
+cudaError_t configure_one() {
+  return cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)tc_smem<BN, STAGES>());
+}
+
+template <int BN, int STAGES>
 cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& a,
                       const Epi& epi, dim3 grid, cudaStream_t st) {
-  constexpr size_t smem = 1024 + (size_t)STAGES * (128 * 128 + BN * 128) + (2 * STAGES + 1) * 8 + 32;
-  static bool configured = false;  // per instantiation; attribute is per-device-global
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  tc_gemm_kernel<BN, STAGES><<<grid, 128, smem, st>>>(ma, mb, a, epi);
+  tc_gemm_kernel<BN, STAGES><<<grid, 128, tc_smem<BN, STAGES>(), st>>>(ma, mb, a, epi);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+// Shared-memory limits of every instantiation, set at handle creation so
+// that launches stay legal inside stream capture.
+cudaError_t configure_tc() {
+  cudaError_t e = get_encoder();
+  if (e == cudaSuccess) e = configure_one<16, 6>();
+  if (e == cudaSuccess) e = configure_one<32, 6>();
+  if (e == cudaSuccess) e = configure_one<64, 5>();
+  if (e == cudaSuccess) e = configure_one<128, 4>();
+  if (e == cudaSuccess) e = configure_one<256, 4>();
+  return e;
+}
 
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb, int N,
                            int K, int swap, int splits, float* ws, size_t ws_elems, int* counters,

@@ -18,6 +18,7 @@ using hf::Epi;
 struct ProfRec {
   cudaEvent_t a, b;
   int fam;
+  int count;
 };
 
 struct hf_handle {
@@ -65,8 +66,9 @@ struct hf_handle {
 
   int32_t* err = nullptr;
 
-  bool prof = false;
-  std::vector<ProfRec> pending;
+  int prof = 0;                 // 0 off, 1 records read once, 2 records kept (graphs)
+  std::vector<ProfRec> pending;  // mode 1
+  std::vector<ProfRec> kept;     // mode 2
   std::vector<cudaEvent_t> pool;
   double tot_ms[HF_K_COUNT] = {};
   int64_t nl[HF_K_COUNT] = {};
@@ -156,10 +158,12 @@ hf_status dev_alloc(hf_handle* h, void** p, size_t bytes) {
 }
 
 void free_all(hf_handle* h) {
-  for (auto& r : h->pending) {
-    cudaEventDestroy(r.a);
-    cudaEventDestroy(r.b);
-  }
+  for (auto* v : {&h->pending, &h->kept})
+    for (auto& r : *v) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+  h->kept.clear();
   for (auto e : h->pool) cudaEventDestroy(e);
   h->pending.clear();
   h->pool.clear();
@@ -186,35 +190,62 @@ struct Scope {
   ProfRec rec{};
   int before;
   int count = 0;  // launches made inside the scope
+  // Mode 2 records with cudaEventRecordExternal so that, inside stream
+  // capture, the records become graph nodes that re-record on every replay.
+  unsigned flags() const { return h->prof == 2 ? cudaEventRecordExternal : cudaEventRecordDefault; }
   Scope(hf_handle* h_, int fam_, cudaStream_t st_) : h(h_), fam(fam_), st(st_) {
     if (h->prof) {
       rec.a = get_event(h);
       rec.b = get_event(h);
       rec.fam = fam;
-      cudaEventRecord(rec.a, st);
+      cudaEventRecordWithFlags(rec.a, st, flags());
     }
   }
   ~Scope() {
     h->launches += count;
     if (h->prof) {
-      cudaEventRecord(rec.b, st);
-      h->pending.push_back(rec);
-      h->nl[fam] += count;
+      cudaEventRecordWithFlags(rec.b, st, flags());
+      rec.count = count;
+      (h->prof == 2 ? h->kept : h->pending).push_back(rec);
     }
   }
 };
 
-hf_status drain_profile(hf_handle* h) {
-  if (h->pending.empty()) return HF_OK;
-  HF_CUDA(h, cudaEventSynchronize(h->pending.back().b));
+// Add the elapsed time of every finished record to the family totals. Mode-1
+// records are released; mode-2 records stay (their events are re-recorded by
+// each replay of the graph they were captured into).
+hf_status collect_profile(hf_handle* h) {
+  for (auto* v : {&h->pending, &h->kept}) {
+    if (v->empty()) continue;
+    cudaError_t e = cudaEventSynchronize(v->back().b);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      continue;  // never recorded yet (a captured graph not replayed)
+    }
+    for (auto& r : *v) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+        h->tot_ms[r.fam] += ms;
+        h->nl[r.fam] += r.count;
+      } else {
+        cudaGetLastError();
+      }
+    }
+  }
   for (auto& r : h->pending) {
-    float ms = 0.f;
-    if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) h->tot_ms[r.fam] += ms;
     h->pool.push_back(r.a);
     h->pool.push_back(r.b);
   }
   h->pending.clear();
   return HF_OK;
+}
+
+// Current device switch only when needed (cheap, and legal during capture).
+cudaError_t ensure_device(const hf_handle* h) {
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return e;
+  return cur == h->device ? cudaSuccess : cudaSetDevice(h->device);
 }
 
 int pick_splits(const hf_handle* h, long long R, long long C, long long K, int tile_r, int tile_c) {
@@ -362,6 +393,11 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     if (e != cudaSuccess) s = cuda_fail(h, e, "cudaMemset(tags)");
   }
   if (s == HF_OK) {
+    e = hf::configure_attn(h->d);
+    if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc();
+    if (e != cudaSuccess) s = cuda_fail(h, e, "kernel set-up");
+  }
+  if (s == HF_OK) {
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) s = cuda_fail(h, e, "cudaDeviceSynchronize");
   }
@@ -436,7 +472,7 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
   if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
   if (slot_emb == out) return fail(h, HF_EINVAL, "out may not alias slot_emb");
   if (batch == 0) return HF_OK;
-  HF_CUDA(h, cudaSetDevice(h->device));
+  HF_CUDA(h, ensure_device(h));
   cudaStream_t st = (cudaStream_t)stream;
   const Dims& d = h->d;
   const size_t es = h->esz;
@@ -481,7 +517,7 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, 
   if (!feats || !n_accepted) return fail(h, HF_EINVAL, "NULL buffer");
   if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
   if (batch == 0) return HF_OK;
-  HF_CUDA(h, cudaSetDevice(h->device));
+  HF_CUDA(h, ensure_device(h));
   cudaStream_t st = (cudaStream_t)stream;
   const Dims& d = h->d;
   {
@@ -536,7 +572,7 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
   }
   if (total > 0 && !feats) return fail(h, HF_EINVAL, "feats is NULL");
   if (total > (long long)INT32_MAX) return fail(h, HF_EINVAL, "prefix too long");
-  HF_CUDA(h, cudaSetDevice(h->device));
+  HF_CUDA(h, ensure_device(h));
   cudaStream_t st = (cudaStream_t)stream;
   const size_t es = h->esz;
   HF_CUDA(h, cudaMemcpyAsync(h->pf_lens, lens, n_req * 4, cudaMemcpyHostToDevice, st));
@@ -694,18 +730,38 @@ hf_status hf_import_context(hf_handle* h, const void* host_in, size_t bytes) {
   return copy_context(h, const_cast<void*>(host_in), bytes, false);
 }
 
-hf_status hf_profile_enable(hf_handle* h, int32_t on) {
+hf_status hf_profile_enable(hf_handle* h, int32_t mode) {
   if (!h) return HF_EINVAL;
-  h->prof = on != 0;
+  if (mode < 0 || mode > 2) return fail(h, HF_EINVAL, "profile mode must be 0, 1 or 2");
+  HF_CUDA(h, ensure_device(h));
+  if (!h->kept.empty()) {
+    HF_CUDA(h, cudaDeviceSynchronize());
+    for (auto& r : h->kept) {
+      h->pool.push_back(r.a);
+      h->pool.push_back(r.b);
+    }
+    h->kept.clear();
+  }
+  h->prof = mode;
+  // Pre-create events so that recording under stream capture needs no
+  // event creation.
+  while (mode && h->pool.size() < 256) {
+    cudaEvent_t e;
+    HF_CUDA(h, cudaEventCreate(&e));
+    h->pool.push_back(e);
+  }
   return HF_OK;
+}
+
+hf_status hf_profile_collect(hf_handle* h) {
+  if (!h) return HF_EINVAL;
+  HF_CUDA(h, ensure_device(h));
+  return collect_profile(h);
 }
 
 hf_status hf_profile_read(hf_handle* h, int32_t family, double* total_ms, int64_t* launches,
                           int32_t reset) {
   if (!h || family < 0 || family >= HF_K_COUNT) return HF_EINVAL;
-  HF_CUDA(h, cudaSetDevice(h->device));
-  hf_status s = drain_profile(h);
-  if (s != HF_OK) return s;
   if (total_ms) *total_ms = h->tot_ms[family];
   if (launches) *launches = h->nl[family];
   if (reset) {

@@ -187,3 +187,44 @@ def test_draft_steps_individually(name, lens):
             assert e <= p.tol, f"request {b}: {what} err {e:.3e}"
     assert maxnorm_err(got, ref) <= p.tol
     p.close()
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_4b_bf16"])
+def test_rounds_captured_in_cuda_graph(name):
+    """draft + commit captured once into a CUDA graph and replayed per round
+    (with the profiler recording inside the graph) match the oracle."""
+    cfg = CONFIGS[name].replace(batch=2)
+    p = Pair(cfg)
+    lens = [700, 90]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    st_slot = torch.empty((2, cfg.block, cfg.d_model), dtype=p.gpu.torch_dtype, device="cuda")
+    st_feat = torch.empty((2, cfg.block + 1, cfg.d_model), dtype=p.gpu.torch_dtype, device="cuda")
+    st_cnt = torch.empty((2,), dtype=torch.int32, device="cuda")
+    out = torch.empty_like(st_slot)
+    p.gpu.profile(2)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+        p.gpu.draft(st_slot, out)
+        p.gpu.commit(st_feat, st_cnt)
+    torch.cuda.current_stream().wait_stream(side)
+    for r in range(3):
+        slot, feats = make_round_inputs(cfg, r, 2)
+        n = make_accepted(cfg, r, 2)
+        st_slot.copy_(slot.cuda())
+        st_feat.copy_(feats.cuda())
+        st_cnt.copy_(n.cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        p.gpu.profile_collect()
+        ref = p.orc.draft(slot)
+        p.orc.commit(feats, n.numpy())
+        e = maxnorm_err(out.float().cpu().numpy(), ref)
+        assert e <= p.tol, f"round {r}: draft err {e:.3e}"
+        p.check_context(what=f"graph round {r}")
+    ms, launches = p.gpu.profile_read(0)
+    assert ms > 0 and launches >= 3
+    del g
+    p.gpu.profile(0)
+    p.close()
