@@ -36,6 +36,12 @@
  *   - Matrices are row-major. Element type of features, slot embeddings,
  *     outputs and weights is the handle's dtype (fp32 or bf16);
  *     dt_bias and A_log are always fp32; the recurrent state is always fp32.
+ *     Device buffers passed to prefill, commit and draft must be 16-byte
+ *     aligned (HF_EINVAL otherwise); d_model must be a multiple of 8.
+ *   - Kernels are launched with programmatic dependent launch: each kernel
+ *     of a call may start while the previous one finishes, and waits for
+ *     it before touching its data. Calls may be captured into CUDA graphs
+ *     (nothing in prefill/commit/draft allocates or synchronises).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream). Work is enqueued asynchronously; nothing here synchronises the
  *     host unless its comment says so.
@@ -76,12 +82,12 @@ typedef struct {
   int32_t d_model;      /* D */
   int32_t n_q_heads;    /* Hq */
   int32_t n_kv_heads;   /* Hkv, divides Hq */
-  int32_t head_dim;     /* dh, multiple of 4, <= 256 */
+  int32_t head_dim;     /* dh, multiple of 4 (of 8 for bf16), <= 256 */
   int32_t window;       /* W >= block+1: sliding-window ring length */
   int32_t block;        /* S = 7 draft slots (1..16 accepted) */
   int32_t ssm_heads;    /* Hm */
-  int32_t ssm_headdim;  /* P */
-  int32_t d_state;      /* N, multiple of 4 */
+  int32_t ssm_headdim;  /* P, multiple of 4; P*N a multiple of 128, <= 8192 */
+  int32_t d_state;      /* N, a power of two in 4..128 */
   int32_t n_groups;     /* must be 1 */
   int32_t n_layers;     /* drafter depth */
   int32_t max_batch;    /* requests held by the handle */

@@ -1,15 +1,21 @@
-// Window + block attention and the draft-time memory read for one layer.
+// Window + block attention and the draft-time memory read for one layer, in
+// one launch.
 //
 // Attention (learnaivisually explainer, "That is HyFlash"): the 7 slot
 // queries of a request attend, bidirectionally and with no mask, over the
-// valid entries of that request's window ring and over the 7 slot keys. One
-// CTA takes one (request, KV head, window split) and all G = Hq/Hkv query
-// heads that share the KV head (G*7 query rows), so each K/V tile is read
-// from HBM once. Splits combine with the usual max/sum rescaling, in a fixed
-// order, in a second kernel.
+// valid entries of that request's window ring and over the 7 slot keys.
+// CTA (request b, KV head g, split j) takes ring slots [32 j, 32 j + 32) of
+// (b, g) and all G = Hq/Hkv query heads sharing g (G*7 query rows), so each
+// K/V tile crosses HBM once: one bulk copy (TMA) per tile into shared
+// memory, converted to padded fp32 rows. Scores, an exp2-based softmax and
+// the P.V product run in fp32; the split writes (max, sum, partial O). The
+// last split of (b, g) to finish -- a ticket counter, no waiting -- combines
+// all splits in split order (deterministic) and writes O.
 //
-// Memory read: y[s, h, p] = sum_n state[h, p, n] * C_s[s, n], with C_s the
-// slot projection through W_C; the state is only read.
+// Memory read (same launch, the CTAs after the attention ones): y[s, h, p] =
+// sum_n state[h, p, n] * C_s[s, n]. The state block of (b, h) is read with
+// 16-byte loads, all in flight at once, and reduced across the lanes that
+// share a state row. The state is never written here.
 #include <cstdio>
 #include <mutex>
 
@@ -18,210 +24,346 @@
 namespace hf {
 namespace {
 
-constexpr int JT = 32;      // ring keys per split
-constexpr int MAXS = 16;    // max block slots
+constexpr int JT = 32;       // ring keys per split
+constexpr int MAXS = 16;     // max block slots
+constexpr int THREADS = 256;
+constexpr int MEM_QPT = 8;   // float4 state elements per thread (P*N <= 8192)
+
+struct AttnArgs {
+  Dims d;
+  int B;          // requests
+  int nsplit;     // ring splits per (request, KV head)
+  int n_attn;     // attention CTAs: B * Hkv * nsplit; memory-read CTAs follow
+  float qscale;   // log2(e) / sqrt(dh)
+  const float* proj;    // [B*S, Nd] fp32: Q | K_s | V_s | C_s
+  const void* ring_k;   // [B][Hkv][W][dh] of this layer
+  const void* ring_v;
+  const int64_t* pos;   // [B]
+  const float* state;   // [B][Hm][P][N] of this layer (unused without memory CTAs)
+  void* mix;            // [B*S, Nz]: O at columns [0, Hq*dh), y at [Hq*dh, Nz)
+  float* part_o;        // [B*Hkv*nsplit][R][dh]
+  float* part_ml;       // [B*Hkv*nsplit][R][2]
+  int* tickets;         // [B*Hkv], left at zero
+  int32_t* err;
+};
+
+struct AttnSmem {
+  size_t bar, stage_k, stage_v, q, k, v, s, w, flag, total;
+};
+
+__host__ __device__ inline AttnSmem attn_smem(const Dims& d, int esize, int nsplit) {
+  AttnSmem m{};
+  size_t off = 0;
+  const int R = d.G * d.S, dhp = d.dh + 4, JK = JT + d.S;
+  m.bar = off;
+  off += 16;
+  const size_t tile = (size_t)JT * d.dh * esize;
+  m.stage_k = off;
+  off += tile;
+  m.stage_v = off;
+  off += tile;
+  m.q = off;
+  off += (size_t)R * dhp * 4;
+  m.k = off;
+  off += (size_t)JK * dhp * 4;
+  m.v = off;
+  off += (size_t)JK * dhp * 4;
+  m.s = off;
+  off += (size_t)R * JK * 4;
+  m.w = off;
+  off += (size_t)nsplit * R * 4;
+  off = (off + 15) & ~(size_t)15;
+  m.flag = off;
+  off += 16;
+  const size_t mem_need = (size_t)d.S * d.N * 4;
+  m.total = off > mem_need ? off : mem_need;
+  return m;
+}
 
 template <typename T>
-__global__ void __launch_bounds__(128)
-attn_partial_kernel(Dims d, const float* __restrict__ proj, const T* __restrict__ ring_k,
-                    const T* __restrict__ ring_v, const int64_t* __restrict__ pos,
-                    float* __restrict__ part_o, float* __restrict__ part_ml, int nsplit,
-                    float qscale) {
-  extern __shared__ __align__(16) float sm[];
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+__device__ __forceinline__ void attn_cta(const AttnArgs& a, uint8_t* sm, int idx) {
+  const Dims& d = a.d;
+  const int split = idx % a.nsplit, rest = idx / a.nsplit;
+  const int kvh = rest % d.Hkv, b = rest / d.Hkv;
   const int S = d.S, G = d.G, R = G * S, dh = d.dh, dhp = dh + 4, JK = JT + S;
-  float* q = sm;
-  float* k = q + R * dhp;
-  float* v = k + JK * dhp;
-  float* s = v + JK * dhp;
+  const AttnSmem L = attn_smem(d, (int)sizeof(T), a.nsplit);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar);
+  T* stk = reinterpret_cast<T*>(sm + L.stage_k);
+  T* stv = reinterpret_cast<T*>(sm + L.stage_v);
+  float* q = reinterpret_cast<float*>(sm + L.q);
+  float* k = reinterpret_cast<float*>(sm + L.k);
+  float* v = reinterpret_cast<float*>(sm + L.v);
+  float* s = reinterpret_cast<float*>(sm + L.s);
+  float* w = reinterpret_cast<float*>(sm + L.w);
+  int* flag = reinterpret_cast<int*>(sm + L.flag);
   const int tid = threadIdx.x, nthr = blockDim.x;
 
-  const long long p = pos[b];
+  pdl_wait();
+  const long long p = __ldcg(&a.pos[b]);
   const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);
   const int j0 = split * JT;
   const int nring = max(0, min(nv, j0 + JT) - j0);
   const int nslot = split == 0 ? S : 0;
-  const int nk = nring + nslot;
+  int nk = nring + nslot;
   const size_t rowbase = (size_t)b * S;
-
-  for (int i = tid; i < R * dh; i += nthr) {
-    int r = i / dh, dd = i % dh, g = r / S, sl = r % S;
-    q[r * dhp + dd] = proj[(rowbase + sl) * d.Nd + (size_t)(kvh * G + g) * dh + dd] * qscale;
-  }
   const size_t rb = ((size_t)b * d.Hkv + kvh) * d.W * dh;
-  for (int i = tid; i < nring * dh; i += nthr) {
-    int j = i / dh, dd = i % dh;
-    k[j * dhp + dd] = to_f(ring_k[rb + (size_t)(j0 + j) * dh + dd]);
-    v[j * dhp + dd] = to_f(ring_v[rb + (size_t)(j0 + j) * dh + dd]);
+
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (nring > 0) {
+      const uint32_t bytes = (uint32_t)(nring * dh * sizeof(T));
+      mbar_expect_tx(bar, 2 * bytes);
+      bulk_g2s(stk, static_cast<const T*>(a.ring_k) + rb + (size_t)j0 * dh, bytes, bar);
+      bulk_g2s(stv, static_cast<const T*>(a.ring_v) + rb + (size_t)j0 * dh, bytes, bar);
+    }
   }
-  for (int i = tid; i < nslot * dh; i += nthr) {
-    int j = i / dh, dd = i % dh;
-    const float* row = proj + (rowbase + j) * d.Nd;
-    k[(nring + j) * dhp + dd] = row[d.QD + kvh * dh + dd];
-    v[(nring + j) * dhp + dd] = row[d.QD + d.KVD + kvh * dh + dd];
+  // Query rows (pre-scaled) and the slot keys/values, 16-byte loads.
+  const int c4n = dh / 4;
+  for (int i = tid; i < R * c4n; i += nthr) {
+    const int r = i / c4n, c = (i % c4n) * 4, g = r / S, sl = r % S;
+    float4 x = __ldcg(reinterpret_cast<const float4*>(
+        a.proj + (rowbase + sl) * d.Nd + (size_t)(kvh * G + g) * dh + c));
+    x.x *= a.qscale;
+    x.y *= a.qscale;
+    x.z *= a.qscale;
+    x.w *= a.qscale;
+    *reinterpret_cast<float4*>(&q[r * dhp + c]) = x;
+  }
+  for (int i = tid; i < nslot * c4n; i += nthr) {
+    const int j = i / c4n, c = (i % c4n) * 4;
+    const float* row = a.proj + (rowbase + j) * d.Nd;
+    *reinterpret_cast<float4*>(&k[(nring + j) * dhp + c]) =
+        __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
+    *reinterpret_cast<float4*>(&v[(nring + j) * dhp + c]) =
+        __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
+  }
+  __syncthreads();  // barrier initialised before anyone waits on it
+  bool ok = true;
+  if (nring > 0) ok = mbar_wait(bar, 0);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) {
+      atomicOr(a.err, ERR_TIMEOUT);
+      mbar_wait(bar, 0);  // bounded: let the copies land before leaving
+    }
+    nk = 0;  // contribute an empty split, keep the ticket count consistent
+  } else if (nring > 0) {
+    constexpr int VE = 16 / (int)sizeof(T);
+    for (int i = tid; i < nring * dh / VE; i += nthr) {
+      const int e0 = i * VE, j = e0 / dh, c = e0 % dh;
+      const uint4 rk = *reinterpret_cast<const uint4*>(&stk[e0]);
+      const uint4 rv = *reinterpret_cast<const uint4*>(&stv[e0]);
+      const T* tk = reinterpret_cast<const T*>(&rk);
+      const T* tv = reinterpret_cast<const T*>(&rv);
+#pragma unroll
+      for (int u = 0; u < VE; ++u) {
+        k[j * dhp + c + u] = to_f(tk[u]);
+        v[j * dhp + c + u] = to_f(tv[u]);
+      }
+    }
   }
   __syncthreads();
 
   for (int i = tid; i < R * nk; i += nthr) {
-    int r = i / nk, j = i % nk;
+    const int r = i / nk, j = i % nk;
     float acc = 0.f;
     for (int dd = 0; dd < dh; dd += 4) {
-      float4 a = *reinterpret_cast<const float4*>(&q[r * dhp + dd]);
-      float4 c = *reinterpret_cast<const float4*>(&k[j * dhp + dd]);
-      acc = fmaf(a.x, c.x, fmaf(a.y, c.y, fmaf(a.z, c.z, fmaf(a.w, c.w, acc))));
+      const float4 x = *reinterpret_cast<const float4*>(&q[r * dhp + dd]);
+      const float4 y = *reinterpret_cast<const float4*>(&k[j * dhp + dd]);
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
     }
     s[r * JK + j] = acc;
   }
   __syncthreads();
 
   const int warp = tid / 32, lane = tid % 32, nw = nthr / 32;
-  const size_t pbase = ((size_t)(b * d.Hkv + kvh) * nsplit + split) * R;
+  const size_t pbase = ((size_t)(b * d.Hkv + kvh) * a.nsplit + split) * R;
   for (int r = warp; r < R; r += nw) {
     float m = -INFINITY;
     for (int j = lane; j < nk; j += 32) m = fmaxf(m, s[r * JK + j]);
     m = warp_max(m);
     float l = 0.f;
     for (int j = lane; j < nk; j += 32) {
-      float e = exp2f(s[r * JK + j] - m);
+      const float e = exp2f(s[r * JK + j] - m);
       s[r * JK + j] = e;
       l += e;
     }
     l = warp_sum(l);
     if (lane == 0) {
-      part_ml[(pbase + r) * 2 + 0] = m;
-      part_ml[(pbase + r) * 2 + 1] = l;
+      a.part_ml[(pbase + r) * 2 + 0] = m;
+      a.part_ml[(pbase + r) * 2 + 1] = l;
     }
   }
   __syncthreads();
 
-  const int d4n = dh / 4;
-  for (int i = tid; i < R * d4n; i += nthr) {
-    int r = i / d4n, d4 = (i % d4n) * 4;
+  for (int i = tid; i < R * c4n; i += nthr) {
+    const int r = i / c4n, c = (i % c4n) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < nk; ++j) {
-      float pj = s[r * JK + j];
-      float4 vv = *reinterpret_cast<const float4*>(&v[j * dhp + d4]);
-      acc.x = fmaf(pj, vv.x, acc.x);
-      acc.y = fmaf(pj, vv.y, acc.y);
-      acc.z = fmaf(pj, vv.z, acc.z);
-      acc.w = fmaf(pj, vv.w, acc.w);
+      const float pj = s[r * JK + j];
+      const float4 y = *reinterpret_cast<const float4*>(&v[j * dhp + c]);
+      acc.x = fmaf(pj, y.x, acc.x);
+      acc.y = fmaf(pj, y.y, acc.y);
+      acc.z = fmaf(pj, y.z, acc.z);
+      acc.w = fmaf(pj, y.w, acc.w);
     }
-    *reinterpret_cast<float4*>(&part_o[(pbase + r) * dh + d4]) = acc;
+    *reinterpret_cast<float4*>(&a.part_o[(pbase + r) * dh + c]) = acc;
   }
-}
 
-template <typename T>
-__global__ void attn_combine_kernel(Dims d, const float* __restrict__ part_o,
-                                    const float* __restrict__ part_ml, int nsplit,
-                                    T* __restrict__ mix) {
-  const int kvh = blockIdx.x, b = blockIdx.y;
-  const int S = d.S, G = d.G, R = G * S, dh = d.dh;
-  const size_t base = (size_t)(b * d.Hkv + kvh) * nsplit * R;
-  for (int i = threadIdx.x; i < R * dh; i += blockDim.x) {
-    int r = i / dh, dd = i % dh;
+  // Ticket: the last split of (b, g) to finish combines.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) *flag = atomicAdd(&a.tickets[b * d.Hkv + kvh], 1) == a.nsplit - 1;
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();
+  const size_t base = (size_t)(b * d.Hkv + kvh) * a.nsplit * R;
+  for (int r = tid; r < R; r += nthr) {
     float M = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, part_ml[(base + (size_t)sp * R + r) * 2]);
-    float L = 0.f, acc = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      size_t e = base + (size_t)sp * R + r;
-      float ls = part_ml[e * 2 + 1];
-      if (ls > 0.f) {
-        float w = exp2f(part_ml[e * 2] - M);
-        L = fmaf(ls, w, L);
-        acc = fmaf(part_o[e * dh + dd], w, acc);
-      }
+    for (int sp = 0; sp < a.nsplit; ++sp)
+      M = fmaxf(M, __ldcg(&a.part_ml[(base + (size_t)sp * R + r) * 2]));
+    float Lsum = 0.f;
+    for (int sp = 0; sp < a.nsplit; ++sp) {
+      const size_t e = base + (size_t)sp * R + r;
+      const float ls = __ldcg(&a.part_ml[e * 2 + 1]);
+      const float wt = ls > 0.f ? exp2f(__ldcg(&a.part_ml[e * 2]) - M) : 0.f;
+      w[sp * R + r] = wt;
+      Lsum = fmaf(ls, wt, Lsum);
     }
-    int g = r / S, sl = r % S;
-    mix[((size_t)b * S + sl) * d.Nz + (size_t)(kvh * G + g) * dh + dd] = from_f<T>(acc / L);
-  }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(256)
-memread_kernel(Dims d, const float* __restrict__ proj, const float* __restrict__ state,
-               T* __restrict__ mix) {
-  __shared__ float cs[MAXS * 256];
-  const int hd = blockIdx.x, b = blockIdx.y;
-  const int S = d.S, N = d.N, P = d.P;
-  const int cC = d.QD + 2 * d.KVD;
-  for (int i = threadIdx.x; i < S * N; i += blockDim.x) {
-    int sl = i / N, n = i % N;
-    cs[sl * N + n] = proj[((size_t)b * S + sl) * d.Nd + cC + n];
+    const float inv = 1.f / Lsum;
+    for (int sp = 0; sp < a.nsplit; ++sp) w[sp * R + r] *= inv;
   }
   __syncthreads();
-  const float* h = state + (((size_t)b * d.Hm + hd) * P) * N;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
-  for (int p = warp; p < P; p += nw) {
-    float acc[MAXS];
-#pragma unroll
-    for (int sl = 0; sl < MAXS; ++sl) acc[sl] = 0.f;
-    for (int n = lane; n < N; n += 32) {
-      float hv = h[(size_t)p * N + n];
-#pragma unroll
-      for (int sl = 0; sl < MAXS; ++sl)
-        if (sl < S) acc[sl] = fmaf(hv, cs[sl * N + n], acc[sl]);
+  T* mix = static_cast<T*>(a.mix);
+  for (int i = tid; i < R * c4n; i += nthr) {
+    const int r = i / c4n, c = (i % c4n) * 4, g = r / S, sl = r % S;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int sp = 0; sp < a.nsplit; ++sp) {
+      const float wt = w[sp * R + r];
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(
+          &a.part_o[(base + (size_t)sp * R + r) * dh + c]));
+      acc.x = fmaf(wt, o.x, acc.x);
+      acc.y = fmaf(wt, o.y, acc.y);
+      acc.z = fmaf(wt, o.z, acc.z);
+      acc.w = fmaf(wt, o.w, acc.w);
     }
+    T* dst = mix + ((size_t)b * S + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
+    dst[0] = from_f<T>(acc.x);
+    dst[1] = from_f<T>(acc.y);
+    dst[2] = from_f<T>(acc.z);
+    dst[3] = from_f<T>(acc.w);
+  }
+  if (tid == 0) a.tickets[b * d.Hkv + kvh] = 0;
+}
+
+template <typename T>
+__device__ __forceinline__ void mem_cta(const AttnArgs& a, uint8_t* sm, int idx) {
+  const Dims& d = a.d;
+  const int b = idx / d.Hm, hd = idx % d.Hm;
+  const int S = d.S, N = d.N, P = d.P;
+  float* cs = reinterpret_cast<float*>(sm);
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  pdl_wait();
+  const float4* h = reinterpret_cast<const float4*>(a.state + (((size_t)b * d.Hm + hd) * P) * N);
+  const int nq = P * N / 4;
+  float4 hv[MEM_QPT];
+#pragma unroll
+  for (int u = 0; u < MEM_QPT; ++u) {
+    const int qi = tid + u * nthr;
+    hv[u] = qi < nq ? __ldcg(&h[qi]) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int cC = d.QD + 2 * d.KVD;
+  for (int i = tid; i < S * N / 4; i += nthr) {
+    const int sl = (i * 4) / N, n = (i * 4) % N;
+    *reinterpret_cast<float4*>(&cs[sl * N + n]) =
+        __ldcg(reinterpret_cast<const float4*>(a.proj + ((size_t)b * S + sl) * d.Nd + cC + n));
+  }
+  __syncthreads();
+  const int gsz = N / 4;  // lanes sharing one state row (power of two <= 32)
+  T* mix = static_cast<T*>(a.mix);
+#pragma unroll
+  for (int u = 0; u < MEM_QPT; ++u) {
+    if (u * nthr >= nq) break;  // uniform across the CTA
+    const int qi = tid + u * nthr;
+    const int pr = (qi * 4) / N, n = (qi * 4) % N;
 #pragma unroll
     for (int sl = 0; sl < MAXS; ++sl) {
-      if (sl < S) {
-        float v = warp_sum(acc[sl]);
-        if (lane == 0)
-          mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)hd * P + p] = from_f<T>(v);
-      }
+      if (sl >= S) break;
+      const float4 c = *reinterpret_cast<const float4*>(&cs[sl * N + n]);
+      float acc = hv[u].x * c.x + hv[u].y * c.y + hv[u].z * c.z + hv[u].w * c.w;
+      for (int o = gsz / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if ((qi & (gsz - 1)) == 0 && qi < nq)
+        mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)hd * P + pr] = from_f<T>(acc);
     }
   }
 }
 
 template <typename T>
-cudaError_t run(const Dims& d, int B, const float* proj, const void* ring_k, const void* ring_v,
-                const int64_t* pos, const float* state, void* mix, float* part_o,
-                float* part_ml, int nsplit, cudaStream_t st, int* la, int* lo) {
-  if (B <= 0) return cudaSuccess;
-  const int R = d.G * d.S, dhp = d.dh + 4, JK = JT + d.S;
-  size_t smem = (size_t)(R * dhp + 2 * JK * dhp + R * JK) * sizeof(float);
-  const float qscale = 1.4426950408889634f / sqrtf((float)d.dh);
-  attn_partial_kernel<T><<<dim3(nsplit, d.Hkv, B), 128, smem, st>>>(
-      d, proj, (const T*)ring_k, (const T*)ring_v, pos, part_o, part_ml, nsplit, qscale);
-  ++*la;
-  memread_kernel<T><<<dim3(d.Hm, B), 256, 0, st>>>(d, proj, state, (T*)mix);
-  ++*la;
-  attn_combine_kernel<T><<<dim3(d.Hkv, B), 256, 0, st>>>(d, part_o, part_ml, nsplit, (T*)mix);
-  ++*lo;
-  return cudaGetLastError();
+__global__ void __launch_bounds__(THREADS) attn_mem_kernel(AttnArgs a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  pdl_trigger();
+  if ((int)blockIdx.x < a.n_attn)
+    attn_cta<T>(a, sm, blockIdx.x);
+  else
+    mem_cta<T>(a, sm, blockIdx.x - a.n_attn);
+}
+
+int g_configured_smem = 0;
+std::mutex g_config_mu;
+
+cudaError_t ensure_smem(size_t smem) {
+  std::lock_guard<std::mutex> lock(g_config_mu);
+  if ((int)smem <= g_configured_smem) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_mem_kernel<float>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_mem_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) g_configured_smem = (int)smem;
+  return e;
+}
+
+cudaError_t launch(int dtype, const AttnArgs& a, int n_mem, cudaStream_t st) {
+  const AttnSmem L = attn_smem(a.d, dtype == HF_F32 ? 4 : 2, a.nsplit);
+  const dim3 grid(a.n_attn + n_mem);
+  if (dtype == HF_F32) return launch_pdl(attn_mem_kernel<float>, grid, dim3(THREADS), L.total, st, a);
+  return launch_pdl(attn_mem_kernel<__nv_bfloat16>, grid, dim3(THREADS), L.total, st, a);
 }
 
 }  // namespace
 
+int attn_splits(const Dims& d) { return (d.W + JT - 1) / JT; }
+
 // Dynamic shared memory of the attention kernel is raised once per process
 // (at handle creation), so launches stay legal inside stream capture.
-cudaError_t configure_attn(const Dims& d) {
-  const int R = d.G * d.S, dhp = d.dh + 4, JK = JT + d.S;
-  const int smem = (int)((size_t)(R * dhp + 2 * JK * dhp + R * JK) * sizeof(float));
-  static int configured = 0;
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  if (smem <= configured) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<float>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_partial_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess) configured = smem;
-  return e;
-}
+cudaError_t configure_attn(const Dims& d) { return ensure_smem(attn_smem(d, 4, attn_splits(d)).total); }
 
-cudaError_t launch_attn_mem(int dtype, const Dims& d, int B, const float* proj,
-                            const void* ring_k, const void* ring_v, const int64_t* pos,
-                            const float* state, void* mix, float* part_o, float* part_ml,
-                            int nsplit, cudaStream_t st, int* la, int* lo) {
-  if (dtype == HF_F32)
-    return run<float>(d, B, proj, ring_k, ring_v, pos, state, mix, part_o, part_ml, nsplit, st,
-                      la, lo);
-  return run<__nv_bfloat16>(d, B, proj, ring_k, ring_v, pos, state, mix, part_o, part_ml, nsplit,
-                            st, la, lo);
+cudaError_t launch_attn_mem(int dtype, const Dims& d, int B, const float* proj, const void* ring_k,
+                            const void* ring_v, const int64_t* pos, const float* state, void* mix,
+                            float* part_o, float* part_ml, int* tickets, int32_t* err,
+                            cudaStream_t st, int* launches) {
+  if (B <= 0) return cudaSuccess;
+  AttnArgs a{};
+  a.d = d;
+  a.B = B;
+  a.nsplit = attn_splits(d);
+  a.n_attn = B * d.Hkv * a.nsplit;
+  a.qscale = 1.4426950408889634f / sqrtf((float)d.dh);
+  a.proj = proj;
+  a.ring_k = ring_k;
+  a.ring_v = ring_v;
+  a.pos = pos;
+  a.state = state;
+  a.mix = mix;
+  a.part_o = part_o;
+  a.part_ml = part_ml;
+  a.tickets = tickets;
+  a.err = err;
+  ++*launches;
+  return launch(dtype, a, B * d.Hm, st);
 }
-
-}  // namespace hf
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the window+block attention.
@@ -230,54 +372,46 @@ cudaError_t launch_attn_mem(int dtype, const Dims& d, int B, const float* proj,
 // op: code running under an arena that owns all of the GPU's memory, a
 // serving loop whose memory was sized once at start-up, or a host that must
 // not trigger the device-wide synchronisation cudaMalloc/cudaFree can cause.
-// For them the split partials live in one fixed array in the library's own
-// device image instead of in a handle's scratch. The array exists on every
-// GPU that loads the library, from load until the process exits.
-namespace hf {
+// For them the split partials and split tickets live in fixed arrays in the
+// library's own device image instead of in a handle's scratch. The arrays
+// exist on every GPU that loads the library, from load until the process
+// exits. Tickets start at zero (static storage) and every call leaves them
+// at zero.
 namespace {
 
 constexpr size_t kNoAllocFloats = (size_t)4 << 20;  // 16 MiB of fp32 partials
+constexpr int kNoAllocTickets = 1 << 14;            // (request, KV head) pairs
 static __device__ __align__(256) float g_noalloc_attn_scratch[kNoAllocFloats];
+static __device__ __align__(256) int g_noalloc_attn_tickets[kNoAllocTickets];
+static __device__ int g_noalloc_attn_err;  // bounded-wait expiries (not reported)
 
 constexpr int kMaxDevices = 64;
-float* g_noalloc_ptr[kMaxDevices] = {};
+struct NoAllocPtrs {
+  float* scratch;
+  int* tickets;
+  int* err;
+};
+NoAllocPtrs g_noalloc[kMaxDevices] = {};
 std::mutex g_noalloc_mu;
 
-// The symbol's device address on the current device, looked up once per
-// device (host code must not use the array's name as a device pointer).
-cudaError_t noalloc_scratch(float** out) {
+// The arrays' device addresses on the current device, looked up once per
+// device (host code must not use the arrays' names as device pointers).
+cudaError_t noalloc_scratch(NoAllocPtrs* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
+  if (!g_noalloc[dev].scratch) {
+    void *p = nullptr, *t = nullptr, *r = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_attn_scratch);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&t, g_noalloc_attn_tickets);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&r, g_noalloc_attn_err);
     if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
+    g_noalloc[dev] = {static_cast<float*>(p), static_cast<int*>(t), static_cast<int*>(r)};
   }
-  *out = g_noalloc_ptr[dev];
+  *out = g_noalloc[dev];
   return cudaSuccess;
-}
-
-template <typename T>
-cudaError_t run_noalloc(const Dims& d, int B, const float* proj, const void* ring_k,
-                        const void* ring_v, const int64_t* pos, void* out, int nsplit,
-                        float* scratch, cudaStream_t st) {
-  const int R = d.G * d.S, dhp = d.dh + 4, JK = JT + d.S;
-  const size_t n_o = (size_t)B * d.Hkv * nsplit * R * d.dh;
-  float* part_o = scratch;
-  float* part_ml = scratch + n_o;
-  size_t smem = (size_t)(R * dhp + 2 * JK * dhp + R * JK) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<T>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const float qscale = 1.4426950408889634f / sqrtf((float)d.dh);
-  attn_partial_kernel<T><<<dim3(nsplit, d.Hkv, B), 128, smem, st>>>(
-      d, proj, (const T*)ring_k, (const T*)ring_v, pos, part_o, part_ml, nsplit, qscale);
-  attn_combine_kernel<T><<<dim3(d.Hkv, B), 256, 0, st>>>(d, part_o, part_ml, nsplit, (T*)out);
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -298,28 +432,33 @@ extern "C" hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t 
   if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || window <= 0 || block <= 0)
     return bad("dimensions must be positive (batch >= 0)");
   if (n_q_heads % n_kv_heads) return bad("n_kv_heads must divide n_q_heads");
-  if (head_dim % 4 || head_dim > 256) return bad("head_dim must be a multiple of 4, <= 256");
+  if (head_dim % 8 || head_dim > 256) return bad("head_dim must be a multiple of 8, <= 256");
   if (block > MAXS || (n_q_heads / n_kv_heads) * block > 64)
     return bad("block must be <= 16 and (n_q_heads/n_kv_heads)*block <= 64");
   const long long qd = (long long)n_q_heads * head_dim, kvd = (long long)n_kv_heads * head_dim;
-  if (proj_ld < qd + 2 * kvd) return bad("proj_ld must be >= Hq*dh + 2*Hkv*dh");
+  if (proj_ld < qd + 2 * kvd || proj_ld % 4)
+    return bad("proj_ld must be a multiple of 4 and >= Hq*dh + 2*Hkv*dh");
   if (out_ld < qd) return bad("out_ld must be >= Hq*dh");
   if (batch == 0) return HF_OK;
   if (!proj || !ring_k || !ring_v || !pos || !out) return bad("NULL buffer");
+  if (reinterpret_cast<uintptr_t>(proj) % 16 || reinterpret_cast<uintptr_t>(ring_k) % 16 ||
+      reinterpret_cast<uintptr_t>(ring_v) % 16)
+    return bad("proj, ring_k and ring_v must be 16-byte aligned");
   const int nsplit = (window + JT - 1) / JT;
   const long long R = (long long)(n_q_heads / n_kv_heads) * block;
   const long long need = (long long)batch * n_kv_heads * nsplit * R * (head_dim + 2);
-  if (need > (long long)kNoAllocFloats) {
-    char m[200];
+  if (need > (long long)kNoAllocFloats || (long long)batch * n_kv_heads > kNoAllocTickets) {
+    char m[240];
     snprintf(m, sizeof m,
              "hf_attention_noalloc: needs %lld floats of scratch, the fixed array holds %zu "
-             "(batch * n_kv_heads * ceil(window/32) * (Hq/Hkv) * block * (head_dim + 2))",
-             need, kNoAllocFloats);
+             "(batch * n_kv_heads * ceil(window/32) * (Hq/Hkv) * block * (head_dim + 2)); "
+             "batch * n_kv_heads must be <= %d",
+             need, kNoAllocFloats, kNoAllocTickets);
     set_thread_error(m);
     return HF_EINVAL;
   }
-  float* scratch = nullptr;
-  cudaError_t e = noalloc_scratch(&scratch);
+  NoAllocPtrs ptrs{};
+  cudaError_t e = noalloc_scratch(&ptrs);
   if (e == cudaSuccess) {
     Dims d{};
     d.Hq = n_q_heads;
@@ -332,12 +471,30 @@ extern "C" hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t 
     d.KVD = (int)kvd;
     d.Nd = proj_ld;
     d.Nz = out_ld;
+    d.Hm = 1;
+    d.P = 4;
+    d.N = 4;
     d.esize = dtype == HF_F32 ? 4 : 2;
-    cudaStream_t st = (cudaStream_t)stream;
-    e = dtype == HF_F32
-            ? run_noalloc<float>(d, batch, proj, ring_k, ring_v, pos, out, nsplit, scratch, st)
-            : run_noalloc<__nv_bfloat16>(d, batch, proj, ring_k, ring_v, pos, out, nsplit, scratch,
-                                         st);
+    const AttnSmem L = attn_smem(d, d.esize, nsplit);
+    e = ensure_smem(L.total);
+    if (e == cudaSuccess) {
+      AttnArgs a{};
+      a.d = d;
+      a.B = batch;
+      a.nsplit = nsplit;
+      a.n_attn = batch * n_kv_heads * nsplit;
+      a.qscale = 1.4426950408889634f / sqrtf((float)head_dim);
+      a.proj = proj;
+      a.ring_k = ring_k;
+      a.ring_v = ring_v;
+      a.pos = pos;
+      a.mix = out;
+      a.part_o = ptrs.scratch;
+      a.part_ml = ptrs.scratch + (size_t)a.n_attn * R * head_dim;
+      a.tickets = ptrs.tickets;
+      a.err = ptrs.err;
+      e = launch(dtype, a, 0, (cudaStream_t)stream);
+    }
   }
   if (e != cudaSuccess) {
     set_thread_error(cudaGetErrorString(e));

@@ -12,76 +12,133 @@
 namespace hf {
 namespace {
 
+constexpr int QPT = 8;  // float4 state elements per thread (P*N <= 8192)
+
 // grid (B, S+1): CTA (b, t) owns accepted row t of request b.
 template <typename T>
-__global__ void commit_prep_kernel(Dims d, int B, const T* __restrict__ feats,
-                                   const int32_t* __restrict__ n_acc,
-                                   const int64_t* __restrict__ pos, int32_t* __restrict__ offsets,
-                                   int32_t* __restrict__ row_req, int64_t* __restrict__ row_pos,
-                                   int32_t* __restrict__ tags, T* __restrict__ packed,
-                                   int32_t* __restrict__ err) {
+__global__ void __launch_bounds__(128)
+commit_prep_kernel(Dims d, int B, const T* __restrict__ feats, const int32_t* __restrict__ n_acc,
+                   const int64_t* __restrict__ pos, int32_t* __restrict__ offsets,
+                   int32_t* __restrict__ row_req, int64_t* __restrict__ row_pos,
+                   int32_t* __restrict__ tags, T* __restrict__ packed, int32_t* __restrict__ err) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x, t = blockIdx.y;
   const int lim = d.S + 1;
   __shared__ int s_off, s_n;
-  if (threadIdx.x == 0) {
-    int off = 0;
-    for (int i = 0; i < b; ++i) {
-      int n = n_acc[i];
-      off += (n >= 0 && n <= lim) ? n : 0;
+  if (threadIdx.x < 32) {
+    // offset of request b = sum of the valid counts before it (warp-parallel)
+    int part = 0;
+    for (int i = threadIdx.x; i < b; i += 32) {
+      const int n = n_acc[i];
+      part += (n >= 0 && n <= lim) ? n : 0;
     }
-    int n = n_acc[b];
-    bool ok = n >= 0 && n <= lim;
-    if (!ok && t == 0) atomicOr(err, ERR_BAD_ACCEPTED);
-    s_off = off;
-    s_n = ok ? n : 0;
-    if (t == 0) {
-      offsets[b] = off;
-      if (b == B - 1) offsets[B] = off + s_n;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (threadIdx.x == 0) {
+      const int n = n_acc[b];
+      const bool ok = n >= 0 && n <= lim;
+      if (!ok && t == 0) atomicOr(err, ERR_BAD_ACCEPTED);
+      s_off = part;
+      s_n = ok ? n : 0;
+      if (t == 0) {
+        offsets[b] = part;
+        if (b == B - 1) offsets[B] = part + s_n;
+      }
     }
   }
   __syncthreads();
   if (t >= s_n) return;
   const int r = s_off + t;
-  const long long p = pos[b] + t;
+  const long long p = __ldcg(&pos[b]) + t;
   if (threadIdx.x == 0) {
     row_req[r] = b;
     row_pos[r] = p;
     tags[(size_t)b * d.W + (int)(p % d.W)] = (int32_t)p;
   }
-  const T* src = feats + ((size_t)b * lim + t) * d.D;
-  T* dst = packed + (size_t)r * d.D;
-  for (int i = threadIdx.x; i < d.D; i += blockDim.x) dst[i] = src[i];
+  // gather the row: 16-byte chunks, loads batched ahead of the stores
+  const uint4* src = reinterpret_cast<const uint4*>(feats + ((size_t)b * lim + t) * d.D);
+  uint4* dst = reinterpret_cast<uint4*>(packed + (size_t)r * d.D);
+  const int nchunk = d.D * (int)sizeof(T) / 16;
+  for (int i0 = threadIdx.x; i0 < nchunk; i0 += 4 * blockDim.x) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < nchunk) v[u] = __ldg(&src[i]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < nchunk) dst[i] = v[u];
+    }
+  }
 }
 
-// grid (Hm, B, L): the state of one (layer, request, head) is read once,
-// advanced over the request's accepted rows in order, and written once.
+// grid (Hm, B, L): the state of one (layer, request, head) is read once (all
+// loads in flight together), advanced over the request's accepted rows in
+// order, and written once.
 __global__ void __launch_bounds__(256)
 commit_state_kernel(Dims d, const int32_t* __restrict__ offsets, const float* __restrict__ xbd,
                     long long xls, const float* __restrict__ A_log, float* __restrict__ state,
                     int64_t* __restrict__ pos) {
+  extern __shared__ __align__(16) float sm[];
+  pdl_trigger();
+  pdl_wait();
   const int hd = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
-  const int off = offsets[b], n = offsets[b + 1] - off;
+  const int off = __ldcg(&offsets[b]), n = __ldcg(&offsets[b + 1]) - off;
   if (n <= 0) return;
   if (l == 0 && hd == 0 && threadIdx.x == 0) pos[b] += n;
-  const float A = -expf(A_log[l * d.Hm + hd]);
-  float4* h = reinterpret_cast<float4*>(state + ((((size_t)l * d.Bmax + b) * d.Hm + hd) * d.P) * d.N);
+  const int P = d.P, N = d.N;
+  float4* h = reinterpret_cast<float4*>(state + ((((size_t)l * d.Bmax + b) * d.Hm + hd) * P) * N);
+  const int nq = P * N / 4;
+  float4 hv[QPT];
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {
+    const int q = threadIdx.x + u * blockDim.x;
+    hv[u] = q < nq ? __ldcg(&h[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // stage x (this head), B and dt of the n accepted rows
+  const int rows = d.S + 1;       // n <= block + 1
+  float* sx = sm;                 // [rows][P]
+  float* sb = sx + rows * P;      // [rows][N]
+  float* sd = sb + rows * N;      // [rows]
   const float* xb = xbd + (size_t)l * xls;
-  const int nq = d.P * d.N / 4;
-  for (int q = threadIdx.x; q < nq; q += blockDim.x) {
-    const int e = q * 4, p = e / d.N, nn = e % d.N;
-    float4 hv = h[q];
-    for (int t = 0; t < n; ++t) {
-      const float* row = xb + (size_t)(off + t) * d.NS;
-      const float dt = row[d.dinner + d.N + hd];
-      const float dec = expf(dt * A);
-      const float xv = dt * row[hd * d.P + p];
-      const float4 Bv = *reinterpret_cast<const float4*>(row + d.dinner + nn);
-      hv.x = fmaf(dec, hv.x, xv * Bv.x);
-      hv.y = fmaf(dec, hv.y, xv * Bv.y);
-      hv.z = fmaf(dec, hv.z, xv * Bv.z);
-      hv.w = fmaf(dec, hv.w, xv * Bv.w);
+  for (int i = threadIdx.x; i < n * (P / 4); i += blockDim.x) {
+    const int t = i / (P / 4), c = (i % (P / 4)) * 4;
+    *reinterpret_cast<float4*>(&sx[t * P + c]) =
+        __ldcg(reinterpret_cast<const float4*>(xb + (size_t)(off + t) * d.NS + hd * P + c));
+  }
+  for (int i = threadIdx.x; i < n * (N / 4); i += blockDim.x) {
+    const int t = i / (N / 4), c = (i % (N / 4)) * 4;
+    *reinterpret_cast<float4*>(&sb[t * N + c]) =
+        __ldcg(reinterpret_cast<const float4*>(xb + (size_t)(off + t) * d.NS + d.dinner + c));
+  }
+  for (int t = threadIdx.x; t < n; t += blockDim.x)
+    sd[t] = __ldcg(&xb[(size_t)(off + t) * d.NS + d.dinner + N + hd]);
+  __syncthreads();
+  const float A = -expf(A_log[l * d.Hm + hd]);
+  for (int t = 0; t < n; ++t) {
+    const float dt = sd[t];
+    const float dec = expf(dt * A);
+#pragma unroll
+    for (int u = 0; u < QPT; ++u) {
+      const int q = threadIdx.x + u * blockDim.x;
+      if (q < nq) {
+        const int e = q * 4, p = e / N, c = e % N;
+        const float xv = dt * sx[t * P + p];
+        const float4 Bv = *reinterpret_cast<const float4*>(&sb[t * N + c]);
+        hv[u].x = fmaf(dec, hv[u].x, xv * Bv.x);
+        hv[u].y = fmaf(dec, hv[u].y, xv * Bv.y);
+        hv[u].z = fmaf(dec, hv[u].z, xv * Bv.z);
+        hv[u].w = fmaf(dec, hv[u].w, xv * Bv.w);
+      }
     }
-    h[q] = hv;
+  }
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {
+    const int q = threadIdx.x + u * blockDim.x;
+    if (q < nq) h[q] = hv[u];
   }
 }
 
@@ -91,24 +148,23 @@ cudaError_t launch_commit_prep(int dtype, const Dims& d, int B, const void* feat
                                const int32_t* n_acc, const int64_t* pos, int32_t* offsets,
                                int32_t* row_req, int64_t* row_pos, int32_t* tags, void* packed,
                                int32_t* err, cudaStream_t st) {
-  dim3 grid(B, d.S + 1);
+  const dim3 grid(B, d.S + 1);
   if (dtype == HF_F32)
-    commit_prep_kernel<float><<<grid, 128, 0, st>>>(d, B, (const float*)feats, n_acc, pos,
-                                                    offsets, row_req, row_pos, tags,
-                                                    (float*)packed, err);
-  else
-    commit_prep_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(
-        d, B, (const __nv_bfloat16*)feats, n_acc, pos, offsets, row_req, row_pos, tags,
-        (__nv_bfloat16*)packed, err);
-  return cudaGetLastError();
+    return launch_pdl(commit_prep_kernel<float>, grid, dim3(128), 0, st, d, B,
+                      (const float*)feats, n_acc, pos, offsets, row_req, row_pos, tags,
+                      (float*)packed, err);
+  return launch_pdl(commit_prep_kernel<__nv_bfloat16>, grid, dim3(128), 0, st, d, B,
+                    (const __nv_bfloat16*)feats, n_acc, pos, offsets, row_req, row_pos, tags,
+                    (__nv_bfloat16*)packed, err);
 }
 
 cudaError_t launch_commit_state(const Dims& d, int B, const int32_t* offsets, const float* xbd,
                                 long long xls, const float* A_log, float* state, int64_t* pos,
                                 cudaStream_t st) {
-  commit_state_kernel<<<dim3(d.Hm, B, d.L), 256, 0, st>>>(d, offsets, xbd, xls, A_log, state,
-                                                         pos);
-  return cudaGetLastError();
+  // staging for block+1 rows of x (P values), B (N values) and dt
+  const size_t smem = (size_t)(d.S + 1) * (d.P + d.N + 1) * sizeof(float);
+  return launch_pdl(commit_state_kernel, dim3(d.Hm, B, d.L), dim3(256), smem, st, d, offsets, xbd,
+                    xls, A_log, state, pos);
 }
 
 }  // namespace hf

@@ -37,6 +37,82 @@ __device__ __forceinline__ float softplus_f(float x) {
   return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch: every kernel of a round lets the next one
+// start as soon as all of its CTAs are running (launch_dependents), and waits
+// for the previous kernel's completion and memory (wait) before it reads or
+// writes anything that kernel may touch. Every kernel calls pdl_wait before it
+// finishes, so completion stays transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with the programmatic-stream-serialization attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// ---------------------------------------------------------------- mbarrier / bulk copy
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz: bound of every wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+
+// 1-D bulk copy global -> shared (addresses 16-byte aligned, bytes % 16 == 0),
+// completing `bytes` of transaction on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Device error word bits.
 enum : int32_t { ERR_BAD_ACCEPTED = 1, ERR_TIMEOUT = 2 };
 
@@ -88,10 +164,10 @@ __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
     e.out[(size_t)r * e.ld + c] = v;
   } else if (e.kind == EPI_RESID) {
     size_t i = (size_t)r * e.ld + c;
-    float x = to_f(((const T*)e.resid)[i]);
+    float x = to_f(__ldcg(&((const T*)e.resid)[i]));
     ((T*)e.out_t)[i] = from_f<T>(x + v);
   } else {
-    if (e.n_rows && r >= *e.n_rows) return;
+    if (e.n_rows && r >= __ldcg(e.n_rows)) return;
     const Dims& d = e.d;
     int layer = e.layer0 + c / e.cols_per_layer;
     int cl = c % e.cols_per_layer + e.col_off;
@@ -99,8 +175,8 @@ __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
       int which = cl >= d.KVD;
       int cc = cl - which * d.KVD;
       int kvh = cc / d.dh, dd = cc % d.dh;
-      int b = e.row_req[r];
-      int slot = (int)(e.row_pos[r] % d.W);
+      int b = __ldcg(&e.row_req[r]);
+      int slot = (int)(__ldcg(&e.row_pos[r]) % d.W);
       size_t idx = ((((size_t)layer * d.Bmax + b) * d.Hkv + kvh) * d.W + slot) * d.dh + dd;
       ((T*)(which ? e.ring_v : e.ring_k))[idx] = from_f<T>(v);
     } else {
@@ -136,14 +212,15 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
 cudaError_t configure_tc();
 cudaError_t configure_attn(const Dims& d);
 
-// Window+block attention and memory read for one layer, batch B.
+// Window+block attention and memory read for one layer, batch B, one launch.
 // proj [B*S, Nd] fp32 (Q|K_s|V_s|C_s); ring_k/v of this layer; pos [Bmax];
-// state of this layer; mix [B*S, Nz] model dtype (O | y).
+// state of this layer; mix [B*S, Nz] model dtype (O | y); part_o/part_ml:
+// split partials; tickets [B*Hkv] (kept at zero).
+int attn_splits(const Dims& d);
 cudaError_t launch_attn_mem(int dtype, const Dims& d, int B, const float* proj,
                             const void* ring_k, const void* ring_v, const int64_t* pos,
                             const float* state, void* mix, float* part_o, float* part_ml,
-                            int nsplit, cudaStream_t st, int* launches_attn,
-                            int* launches_other);
+                            int* tickets, int32_t* err, cudaStream_t st, int* launches);
 
 // Commit prep: validate counts, offsets, row map, tags, gather rows.
 cudaError_t launch_commit_prep(int dtype, const Dims& d, int B, const void* feats,

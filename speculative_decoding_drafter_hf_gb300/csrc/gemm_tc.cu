@@ -30,43 +30,6 @@
 namespace hf {
 namespace {
 
-constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `parity` to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
-  return true;
-}
-
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y) {
   asm volatile(
@@ -136,6 +99,8 @@ struct TcArgs {
   int kblocks;        // ceil(K / 64)
   int splits;         // split-K factor (grid.z)
   int swap;           // 1: output row = n, column = m; 0: row = m, column = n
+  int prefetch_a;     // 1: A does not depend on earlier kernels (weights): load it
+                      //    before waiting on the previous kernel
   float* ws;          // split-K partial tiles
   int* counters;      // one ticket counter per output tile, left at zero
   int32_t* err;       // device error word
@@ -166,6 +131,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const int kb0 = (int)((long long)split * a.kblocks / a.splits);
   const int kb1 = (int)((long long)(split + 1) * a.kblocks / a.splits);
   const int nkb = kb1 - kb0;
+  pdl_trigger();
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -188,8 +154,27 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // TMA producer
-    int i = 0;
+    // TMA producer. The first ring of stages is filled up front; with
+    // prefetch_a the A tiles (weights) are requested before waiting for the
+    // previous kernel, so their HBM read overlaps that kernel's tail.
+    const int pre = nkb < STAGES ? nkb : STAGES;
+    if (a.prefetch_a) {
+      for (int j = 0; j < pre; ++j) {
+        mbar_expect_tx(&full[j], STAGE_BYTES);
+        tma_load_2d(sA + j * A_BYTES, &ta, &full[j], (kb0 + j) * 64, m_tile * 128);
+      }
+      pdl_wait();
+      for (int j = 0; j < pre; ++j)
+        tma_load_2d(sB + j * B_BYTES, &tb, &full[j], (kb0 + j) * 64, n_tile * BN);
+    } else {
+      pdl_wait();
+      for (int j = 0; j < pre; ++j) {
+        mbar_expect_tx(&full[j], STAGE_BYTES);
+        tma_load_2d(sA + j * A_BYTES, &ta, &full[j], (kb0 + j) * 64, m_tile * 128);
+        tma_load_2d(sB + j * B_BYTES, &tb, &full[j], (kb0 + j) * 64, n_tile * BN);
+      }
+    }
+    int i = pre;
     for (; i < nkb; ++i) {
       const int s = i % STAGES;
       const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
@@ -226,6 +211,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     umma_commit(done);
   }
   __syncwarp();
+  pdl_wait();  // the epilogue writes memory earlier kernels may still read
 
   const bool ok = mbar_wait(done, 0);
   if (__syncthreads_or(!ok || flags[0])) {
@@ -358,8 +344,8 @@ cudaError_t configure_one() {
 template <int BN, int STAGES>
 cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& a,
                       const Epi& epi, dim3 grid, cudaStream_t st) {
-  tc_gemm_kernel<BN, STAGES><<<grid, 128, tc_smem<BN, STAGES>(), st>>>(ma, mb, a, epi);
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<BN, STAGES>, grid, dim3(128), tc_smem<BN, STAGES>(), st, ma,
+                    mb, a, epi);
 }
 
 }  // namespace
@@ -391,6 +377,7 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   a.K = K;
   a.kblocks = (K + 63) / 64;
   a.swap = swap;
+  a.prefetch_a = swap;
   a.err = err;
   a.counters = counters;
   a.ws = ws;

@@ -58,6 +58,8 @@ struct hf_handle {
   size_t part_elems = 0;
   int* counters = nullptr;     // split-K tickets of the tensor-core GEMM
   int n_counters = 0;
+  int* attn_cnt = nullptr;     // split-combine tickets of the attention kernel
+  int num_sms = 152;
 
   float* pf_xbd = nullptr;     // [Tseg][NS]
   long long pf_tokens = 0;
@@ -108,9 +110,11 @@ hf_status validate(const hf_config* c, std::string* why) {
   if (c->n_groups != 1) return bad("n_groups must be 1");
   if (c->n_q_heads % c->n_kv_heads) return bad("n_kv_heads must divide n_q_heads");
   if (c->head_dim % 4 || c->head_dim > 256) return bad("head_dim must be a multiple of 4, <= 256");
-  if (c->d_state % 4 || c->d_state > 256) return bad("d_state must be a multiple of 4, <= 256");
+  if (c->d_state < 4 || c->d_state > 128 || (c->d_state & (c->d_state - 1)))
+    return bad("d_state must be a power of two in 4..128");
   if (c->ssm_headdim % 4) return bad("ssm_headdim must be a multiple of 4");
-  if ((long long)c->ssm_headdim * c->d_state > 8192) return bad("ssm_headdim * d_state must be <= 8192");
+  if ((long long)c->ssm_headdim * c->d_state > 8192 || ((long long)c->ssm_headdim * c->d_state) % 128)
+    return bad("ssm_headdim * d_state must be a multiple of 128, <= 8192");
   if (c->block > 16) return bad("block must be <= 16");
   if (c->window < c->block + 1) return bad("window must be >= block + 1");
   if ((c->n_q_heads / c->n_kv_heads) * c->block > 64) return bad("(n_q_heads/n_kv_heads)*block must be <= 64");
@@ -272,8 +276,10 @@ cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, in
   while (bn < R && bn < 256) bn *= 2;
   const long long tiles = (long long)((C + 127) / 128) * ((R + bn - 1) / bn);
   const int kblocks = (K + 63) / 64;
-  const int target = bn <= 16 ? 2 * 152 : 152;
-  int splits = (int)std::max<long long>(1, (target + tiles - 1) / tiles);
+  // Split K so that the grid fills the resident CTA slots in one wave
+  // (two CTAs per SM fit at N = 16, one otherwise).
+  const int slots = (bn <= 16 ? 2 : 1) * h->num_sms;
+  int splits = (int)std::max<long long>(1, slots / tiles);
   splits = std::min(splits, std::max(1, kblocks / 2));
   return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->part, h->part_elems,
                             h->counters, h->n_counters, h->err, epi, st, count);
@@ -350,7 +356,7 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   const size_t L = d.L, Bm = d.Bmax;
   h->rmax = std::max<long long>((long long)(d.S + 1) * Bm, (long long)Bm * d.W);
   h->xbd_ls = (long long)(d.S + 1) * Bm * d.NS;
-  h->nsplit = (d.W + 31) / 32;
+  h->nsplit = hf::attn_splits(d);
   h->pf_tokens = h->cfg.prefill_tokens_max;
   h->part_elems = (size_t)16 << 20;
   const size_t R = (size_t)d.G * d.S;
@@ -383,6 +389,12 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   A((void**)&h->part, h->part_elems * 4);
   h->n_counters = 1 << 16;
   A((void**)&h->counters, (size_t)h->n_counters * 4);
+  A((void**)&h->attn_cnt, Bm * d.Hkv * 4);
+  if (s == HF_OK) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess && sms > 0)
+      h->num_sms = sms;
+  }
   A((void**)&h->pf_xbd, (size_t)h->pf_tokens * d.NS * 4);
   A((void**)&h->pf_lens, Bm * 4);
   A((void**)&h->pf_reqs, Bm * 4);
@@ -471,6 +483,8 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
   if (!slot_emb || !out) return fail(h, HF_EINVAL, "NULL buffer");
   if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
   if (slot_emb == out) return fail(h, HF_EINVAL, "out may not alias slot_emb");
+  if (reinterpret_cast<uintptr_t>(slot_emb) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(h, HF_EINVAL, "slot_emb and out must be 16-byte aligned");
   if (batch == 0) return HF_OK;
   HF_CUDA(h, ensure_device(h));
   cudaStream_t st = (cudaStream_t)stream;
@@ -491,12 +505,10 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
     if (s != HF_OK) return s;
     {
       Scope sc(h, HF_K_ATTN_MEM, st);
-      int other = 0;
       cudaError_t e = hf::launch_attn_mem(h->cfg.dtype, d, batch, h->proj,
                                           bptr(h->ring_k, l * ring_ls), bptr(h->ring_v, l * ring_ls),
                                           h->pos, h->state + l * state_ls, h->mix, h->attn_o,
-                                          h->attn_ml, h->nsplit, st, &sc.count, &other);
-      sc.count += other;
+                                          h->attn_ml, h->attn_cnt, h->err, st, &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
     }
     Epi e2 = epi_base(h);
@@ -515,6 +527,7 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, 
                     void* stream) {
   if (!h) return HF_EINVAL;
   if (!feats || !n_accepted) return fail(h, HF_EINVAL, "NULL buffer");
+  if (reinterpret_cast<uintptr_t>(feats) % 16) return fail(h, HF_EINVAL, "feats must be 16-byte aligned");
   if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
   if (batch == 0) return HF_OK;
   HF_CUDA(h, ensure_device(h));
@@ -571,6 +584,7 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
     ring_rows += std::min<long long>(lens[i], d.W);
   }
   if (total > 0 && !feats) return fail(h, HF_EINVAL, "feats is NULL");
+  if (reinterpret_cast<uintptr_t>(feats) % 16) return fail(h, HF_EINVAL, "feats must be 16-byte aligned");
   if (total > (long long)INT32_MAX) return fail(h, HF_EINVAL, "prefix too long");
   HF_CUDA(h, ensure_device(h));
   cudaStream_t st = (cudaStream_t)stream;
