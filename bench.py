@@ -324,25 +324,35 @@ def run_hyflash(args, cfg):
         round_calls()
     drafter.sync()
 
+    def capture():
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        n0 = drafter.launch_count()
+        with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+            round_calls()
+        torch.cuda.current_stream().wait_stream(side)
+        return g, drafter.launch_count() - n0
+
+    # Two captures of the same round: a clean one (timed for `value`, kernels
+    # chained by programmatic dependent launch) and one with the library's
+    # event nodes around each kernel family (they serialise the kernels; it
+    # gives the per-family device times used for the roofline).
+    drafter.profile(0)
+    graph, launches_per_step = capture()
     drafter.profile(2)
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    graph = torch.cuda.CUDAGraph()
-    n0 = drafter.launch_count()
-    with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
-        round_calls()
-    launches_per_step = drafter.launch_count() - n0
-    torch.cuda.current_stream().wait_stream(side)
+    graph_prof, _ = capture()
     for r in range(args.warmup):
         stage(r)
         graph.replay()
+        graph_prof.replay()
     torch.cuda.synchronize()
     drafter.profile_collect()
     for fam in hf.Family:
         drafter.profile_read(fam, reset=True)
 
     # ---- timed region: per-step events around the graph replay, L2 flushed
-    # between steps (untimed); per-family times from the library's events
+    # between steps (untimed)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier()
@@ -354,13 +364,20 @@ def run_hyflash(args, cfg):
             ev[i][0].record(stream)
             graph.replay()
             ev[i][1].record(stream)
-            drafter.profile_collect()
         torch.cuda.synchronize()
     barrier()
     drafter.sync()
     launches = launches_per_step * args.steps
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
+
+    # ---- per-family device times: the same rounds through the profiled graph
+    for i in range(args.steps):
+        stage(args.warmup + i)
+        flush.zero_()
+        graph_prof.replay()
+        drafter.profile_collect()
+    torch.cuda.synchronize()
     fam_ms = {}
     for fam in hf.Family:
         ms, n = drafter.profile_read(fam, reset=True)
@@ -395,7 +412,7 @@ def run_hyflash(args, cfg):
     torch.cuda.synchronize()
     barrier()
     drafter.sync()
-    del graph
+    del graph, graph_prof
     drafter.profile(0)
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), dev)
     e2e_value = all_steps / (e2e_ms / 1e3)
@@ -450,7 +467,8 @@ def run_hyflash(args, cfg):
             "config": {"workload": cfg.name, "batch_per_gpu": batch, "prefix": cfg.prefix,
                        "layers": cfg.n_layers, "window": cfg.window, "block": cfg.block,
                        "l2": f"flushed between steps ({2 * l2 >> 20} MiB write, untimed)",
-                       "timing": "CUDA graph of one round replayed per step; CUDA events",
+                       "timing": "CUDA graph of one round replayed per step; CUDA events; "
+                                 "kernel-family times from a second pass with event nodes",
                        "parallelism": f"replicas x{ws}"},
             "committed_tokens_per_s": all_acc / (total_ms_max / 1e3),
             "step_ms_median": statistics.median(step_ms),

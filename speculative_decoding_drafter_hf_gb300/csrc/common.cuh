@@ -201,11 +201,12 @@ cudaError_t launch_gemm_fma(int dtype, const void* X, int ldx, const void* Wt, i
 // bf16 tensor-core GEMM: D[m, n] = sum_k A[m, k] * B[n, k], A [M, K] with row
 // stride lda, B [N, K] with row stride ldb (elements, multiples of 8). With
 // swap = 1 the epilogue sees (row n, column m), else (row m, column n).
-// ws / counters: split-K partial tiles and per-tile tickets (kept at zero).
+// Split-K partner CTAs (splits <= 8) form a thread-block cluster and sum
+// their partial tiles through distributed shared memory.
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb,
-                           int N, int K, int swap, int splits, float* ws, size_t ws_elems,
-                           int* counters, int n_counters, int32_t* err, const Epi& epi,
+                           int N, int K, int swap, int splits, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches);
+int tc_pick_splits(int M, int N, int K);
 
 // One-time kernel attribute set-up (dynamic shared memory limits, driver
 // entry points), done at handle creation.

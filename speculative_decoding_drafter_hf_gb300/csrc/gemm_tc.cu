@@ -94,15 +94,34 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Thread-block-cluster helpers (split-K partner CTAs of one output tile form
+// a cluster along grid z; partial tiles are summed through distributed
+// shared memory).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 struct TcArgs {
   int M, N, K;        // D is M x N
   int kblocks;        // ceil(K / 64)
-  int splits;         // split-K factor (grid.z)
+  int splits;         // split-K factor (grid.z = cluster size along z; <= 8)
   int swap;           // 1: output row = n, column = m; 0: row = m, column = n
   int prefetch_a;     // 1: A does not depend on earlier kernels (weights): load it
                       //    before waiting on the previous kernel
-  float* ws;          // split-K partial tiles
-  int* counters;      // one ticket counter per output tile, left at zero
   int32_t* err;       // device error word
 };
 
@@ -223,6 +242,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     }
     tc_fence_before();
     __syncthreads();
+    if (a.splits > 1) {  // keep the cluster's barrier sequence matched
+      cluster_sync_all();
+      cluster_sync_all();
+    }
     if (warp == 1)
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOLS));
     return;
@@ -251,41 +274,37 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       }
     }
   } else {
-    const int tile = m_tile * gridDim.y + n_tile;
-    const size_t tile_elems = (size_t)BN * 128;
-    float* part = a.ws + ((size_t)tile * a.splits + split) * tile_elems;
+    // Split-K: this CTA's partial tile goes to its own shared memory (the
+    // drained stage buffers); after a cluster barrier, rank r sums rows
+    // r, r + splits, ... over all partners in rank order (deterministic).
+    float* red = reinterpret_cast<float*>(smem);
     const int n_here = min(BN, a.N - n_tile * BN);
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
       tmem_ld16(trow + c0, v);
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if (c0 + j < n_here) part[(size_t)(c0 + j) * 128 + m_local] = v[j];
+        if (c0 + j < n_here) red[(c0 + j) * 128 + m_local] = v[j];
     }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const int t = atomicAdd(&a.counters[tile], 1);
-      flags[3] = (t == a.splits - 1);
-    }
-    __syncthreads();
-    if (flags[3]) {
-      __threadfence();
-      const float* base = a.ws + (size_t)tile * a.splits * tile_elems;
-      for (int nl = 0; nl < n_here; ++nl) {
-        float s = 0.f;
-        for (int sp = 0; sp < a.splits; ++sp)
-          s += __ldcg(&base[(size_t)sp * tile_elems + (size_t)nl * 128 + m_local]);
-        if (m < a.M) {
-          const int n = n_tile * BN + nl;
-          if (a.swap)
-            epi_apply<__nv_bfloat16>(epi, n, m, s);
-          else
-            epi_apply<__nv_bfloat16>(epi, m, n, s);
-        }
+    cluster_sync_all();
+    const int rank = (int)cluster_rank();
+    for (int nl = rank; nl < n_here; nl += a.splits) {
+      float part[8];
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp)
+        part[sp] = sp < a.splits ? ld_peer(&red[nl * 128 + m_local], (uint32_t)sp) : 0.f;
+      float sum = 0.f;
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp) sum += part[sp];
+      if (m < a.M) {
+        const int n = n_tile * BN + nl;
+        if (a.swap)
+          epi_apply<__nv_bfloat16>(epi, n, m, sum);
+        else
+          epi_apply<__nv_bfloat16>(epi, m, n, sum);
       }
-      if (tid == 0) a.counters[tile] = 0;
     }
+    cluster_sync_all();  // partners keep their shared memory until all reads are done
   }
   tc_fence_before();
   __syncthreads();
@@ -342,11 +361,47 @@ cudaError_t configure_one() {
 }
 
 template <int BN, int STAGES>
+cudaLaunchConfig_t tc_config(dim3 grid, int cz, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = tc_smem<BN, STAGES>();
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = cz;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+template <int BN, int STAGES>
 cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& a,
                       const Epi& epi, dim3 grid, cudaStream_t st) {
-  return launch_pdl(tc_gemm_kernel<BN, STAGES>, grid, dim3(128), tc_smem<BN, STAGES>(), st, ma,
-                    mb, a, epi);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = tc_config<BN, STAGES>(grid, a.splits, st, attr);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES>, ma, mb, a, epi);
 }
+
+// How many clusters of cz CTAs of this instantiation are resident at once.
+template <int BN, int STAGES>
+int max_clusters(int cz) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = tc_config<BN, STAGES>(dim3(1, 1, cz), cz, nullptr, attr);
+  cfg.attrs = attr + 1;  // occupancy query: cluster shape only
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, STAGES>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int g_max_clusters[5][9] = {};  // [log2(BN/16)][cz]
 
 }  // namespace
 
@@ -359,13 +414,37 @@ cudaError_t configure_tc() {
   if (e == cudaSuccess) e = configure_one<64, 5>();
   if (e == cudaSuccess) e = configure_one<128, 4>();
   if (e == cudaSuccess) e = configure_one<256, 4>();
-  return e;
+  if (e != cudaSuccess) return e;
+  for (int cz = 1; cz <= 8; ++cz) {
+    g_max_clusters[0][cz] = max_clusters<16, 6>(cz);
+    g_max_clusters[1][cz] = max_clusters<32, 6>(cz);
+    g_max_clusters[2][cz] = max_clusters<64, 5>(cz);
+    g_max_clusters[3][cz] = max_clusters<128, 4>(cz);
+    g_max_clusters[4][cz] = max_clusters<256, 4>(cz);
+  }
+  return cudaSuccess;
+}
+
+// Split-K factor for an M x N x K product: the largest cluster size (<= 8,
+// <= kblocks / 2) whose clusters, one per output tile, are all resident in a
+// single wave; 1 when the tiles alone fill the GPU.
+int tc_pick_splits(int M, int N, int K) {
+  int bn = 16, lg = 0;
+  while (bn < N && bn < 256) {
+    bn *= 2;
+    ++lg;
+  }
+  const long long tiles = (long long)((M + 127) / 128) * ((N + bn - 1) / bn);
+  const int kblocks = (K + 63) / 64;
+  int best = 1;
+  for (int cz = 2; cz <= 8 && cz <= kblocks / 2; ++cz)
+    if (tiles <= g_max_clusters[lg][cz]) best = cz;
+  return best;
 }
 
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb, int N,
-                           int K, int swap, int splits, float* ws, size_t ws_elems, int* counters,
-                           int n_counters, int32_t* err, const Epi& epi, cudaStream_t st,
-                           int* launches) {
+                           int K, int swap, int splits, int32_t* err, const Epi& epi,
+                           cudaStream_t st, int* launches) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   int bn = 16;
   while (bn < N && bn < 256) bn *= 2;
@@ -379,19 +458,13 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   a.swap = swap;
   a.prefetch_a = swap;
   a.err = err;
-  a.counters = counters;
-  a.ws = ws;
-  splits = std::max(1, std::min(splits, a.kblocks));
-  const size_t tile_elems = (size_t)bn * 128;
-  while (splits > 1 && (size_t)m_tiles * n_tiles * splits * tile_elems > ws_elems) --splits;
-  if (splits > 1 && m_tiles * n_tiles > n_counters) splits = 1;
-  a.splits = splits;
+  a.splits = std::max(1, std::min(std::min(splits, 8), a.kblocks));
   CUtensorMap ma, mb;
   cudaError_t e = make_map(&ma, A, M, K, lda, 128);
   if (e != cudaSuccess) return e;
   e = make_map(&mb, B, N, K, ldb, bn);
   if (e != cudaSuccess) return e;
-  dim3 grid(m_tiles, n_tiles, splits);
+  dim3 grid(m_tiles, n_tiles, a.splits);
   ++*launches;
   switch (bn) {
     case 16: return launch_tc<16, 6>(ma, mb, a, epi, grid, st);

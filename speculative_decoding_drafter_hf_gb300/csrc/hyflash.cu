@@ -272,17 +272,8 @@ cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, in
     return hf::launch_gemm_fma(h->cfg.dtype, X, ldx, Wt, ldw, R, C, K, splits, h->part, epi, st,
                                count);
   }
-  int bn = 16;
-  while (bn < R && bn < 256) bn *= 2;
-  const long long tiles = (long long)((C + 127) / 128) * ((R + bn - 1) / bn);
-  const int kblocks = (K + 63) / 64;
-  // Split K so that the grid fills the resident CTA slots in one wave
-  // (two CTAs per SM fit at N = 16, one otherwise).
-  const int slots = (bn <= 16 ? 2 : 1) * h->num_sms;
-  int splits = (int)std::max<long long>(1, slots / tiles);
-  splits = std::min(splits, std::max(1, kblocks / 2));
-  return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->part, h->part_elems,
-                            h->counters, h->n_counters, h->err, epi, st, count);
+  const int splits = hf::tc_pick_splits(C, R, K);
+  return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->err, epi, st, count);
 }
 
 hf_status gemm(hf_handle* h, int fam, const void* X, int ldx, const void* Wt, int ldw, int R,
@@ -632,9 +623,8 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
         e = hf::launch_gemm_fma(h->cfg.dtype, fseg, d.D, wseg, d.D, (int)(s1 - s0), nx, d.D, 1,
                                 h->part, ex, st, &sc.count);
       else  // tokens as the 128-row operand, features as N
-        e = hf::launch_gemm_tc(fseg, d.D, (int)(s1 - s0), wseg, d.D, nx, d.D, 0, 1, h->part,
-                               h->part_elems, h->counters, h->n_counters, h->err, ex, st,
-                               &sc.count);
+        e = hf::launch_gemm_tc(fseg, d.D, (int)(s1 - s0), wseg, d.D, nx, d.D, 0, 1, h->err, ex,
+                               st, &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "prefill ssm gemm");
       e = hf::launch_prefill_scan(d, l, n_req, h->pf_lens, h->pf_reqs, s0, s1, h->pf_xbd, h->A_log,
                                   h->state, st);
