@@ -1,21 +1,18 @@
-// Window + block attention and the draft-time memory read for one layer, in
-// one launch.
+// Window + block attention, split over the window with the splits combined
+// through global memory: the variant behind hf_attention_noalloc.
 //
 // Attention (learnaivisually explainer, "That is HyFlash"): the 7 slot
 // queries of a request attend, bidirectionally and with no mask, over the
 // valid entries of that request's window ring and over the 7 slot keys.
 // CTA (request b, KV head g, split j) takes ring slots [32 j, 32 j + 32) of
-// (b, g) and all G = Hq/Hkv query heads sharing g (G*7 query rows), so each
-// K/V tile crosses HBM once: one bulk copy (TMA) per tile into shared
-// memory, converted to padded fp32 rows. Scores, an exp2-based softmax and
-// the P.V product run in fp32; the split writes (max, sum, partial O). The
-// last split of (b, g) to finish -- a ticket counter, no waiting -- combines
-// all splits in split order (deterministic) and writes O.
-//
-// Memory read (same launch, the CTAs after the attention ones): y[s, h, p] =
-// sum_n state[h, p, n] * C_s[s, n]. The state block of (b, h) is read with
-// 16-byte loads, all in flight at once, and reduced across the lanes that
-// share a state row. The state is never written here.
+// (b, g) and all G = Hq/Hkv query heads sharing g (G*7 query rows): one bulk
+// copy (TMA) per K/V tile into shared memory, converted to padded fp32 rows;
+// scores, an exp2-based softmax and the P.V product in fp32. Each split
+// writes (max, sum, partial O) to scratch memory; the last split of (b, g)
+// to finish -- a ticket counter, no waiting -- combines all splits in split
+// order (deterministic) and writes O. The scratch and tickets live in fixed
+// device arrays (see the end of this file). hf_draft uses the cluster
+// variant in attention_cluster.cu, which keeps the partials on chip.
 #include <cstdio>
 #include <mutex>
 
@@ -27,20 +24,18 @@ namespace {
 constexpr int JT = 32;       // ring keys per split
 constexpr int MAXS = 16;     // max block slots
 constexpr int THREADS = 256;
-constexpr int MEM_QPT = 8;   // float4 state elements per thread (P*N <= 8192)
 
 struct AttnArgs {
   Dims d;
   int B;          // requests
   int nsplit;     // ring splits per (request, KV head)
-  int n_attn;     // attention CTAs: B * Hkv * nsplit; memory-read CTAs follow
+  int n_attn;     // CTAs: B * Hkv * nsplit
   float qscale;   // log2(e) / sqrt(dh)
   const float* proj;    // [B*S, Nd] fp32: Q | K_s | V_s | C_s
   const void* ring_k;   // [B][Hkv][W][dh] of this layer
   const void* ring_v;
   const int64_t* pos;   // [B]
-  const float* state;   // [B][Hm][P][N] of this layer (unused without memory CTAs)
-  void* mix;            // [B*S, Nz]: O at columns [0, Hq*dh), y at [Hq*dh, Nz)
+  void* mix;            // [B*S, Nz]: O at columns [0, Hq*dh)
   float* part_o;        // [B*Hkv*nsplit][R][dh]
   float* part_ml;       // [B*Hkv*nsplit][R][2]
   int* tickets;         // [B*Hkv], left at zero
@@ -75,8 +70,7 @@ __host__ __device__ inline AttnSmem attn_smem(const Dims& d, int esize, int nspl
   off = (off + 15) & ~(size_t)15;
   m.flag = off;
   off += 16;
-  const size_t mem_need = (size_t)d.S * d.N * 4;
-  m.total = off > mem_need ? off : mem_need;
+  m.total = off;
   return m;
 }
 
@@ -259,55 +253,10 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, uint8_t* sm, int idx
 }
 
 template <typename T>
-__device__ __forceinline__ void mem_cta(const AttnArgs& a, uint8_t* sm, int idx) {
-  const Dims& d = a.d;
-  const int b = idx / d.Hm, hd = idx % d.Hm;
-  const int S = d.S, N = d.N, P = d.P;
-  float* cs = reinterpret_cast<float*>(sm);
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  pdl_wait();
-  const float4* h = reinterpret_cast<const float4*>(a.state + (((size_t)b * d.Hm + hd) * P) * N);
-  const int nq = P * N / 4;
-  float4 hv[MEM_QPT];
-#pragma unroll
-  for (int u = 0; u < MEM_QPT; ++u) {
-    const int qi = tid + u * nthr;
-    hv[u] = qi < nq ? __ldcg(&h[qi]) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  const int cC = d.QD + 2 * d.KVD;
-  for (int i = tid; i < S * N / 4; i += nthr) {
-    const int sl = (i * 4) / N, n = (i * 4) % N;
-    *reinterpret_cast<float4*>(&cs[sl * N + n]) =
-        __ldcg(reinterpret_cast<const float4*>(a.proj + ((size_t)b * S + sl) * d.Nd + cC + n));
-  }
-  __syncthreads();
-  const int gsz = N / 4;  // lanes sharing one state row (power of two <= 32)
-  T* mix = static_cast<T*>(a.mix);
-#pragma unroll
-  for (int u = 0; u < MEM_QPT; ++u) {
-    if (u * nthr >= nq) break;  // uniform across the CTA
-    const int qi = tid + u * nthr;
-    const int pr = (qi * 4) / N, n = (qi * 4) % N;
-#pragma unroll
-    for (int sl = 0; sl < MAXS; ++sl) {
-      if (sl >= S) break;
-      const float4 c = *reinterpret_cast<const float4*>(&cs[sl * N + n]);
-      float acc = hv[u].x * c.x + hv[u].y * c.y + hv[u].z * c.z + hv[u].w * c.w;
-      for (int o = gsz / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if ((qi & (gsz - 1)) == 0 && qi < nq)
-        mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)hd * P + pr] = from_f<T>(acc);
-    }
-  }
-}
-
-template <typename T>
 __global__ void __launch_bounds__(THREADS) attn_mem_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   pdl_trigger();
-  if ((int)blockIdx.x < a.n_attn)
-    attn_cta<T>(a, sm, blockIdx.x);
-  else
-    mem_cta<T>(a, sm, blockIdx.x - a.n_attn);
+  attn_cta<T>(a, sm, blockIdx.x);
 }
 
 int g_configured_smem = 0;
@@ -325,45 +274,14 @@ cudaError_t ensure_smem(size_t smem) {
   return e;
 }
 
-cudaError_t launch(int dtype, const AttnArgs& a, int n_mem, cudaStream_t st) {
+cudaError_t launch(int dtype, const AttnArgs& a, cudaStream_t st) {
   const AttnSmem L = attn_smem(a.d, dtype == HF_F32 ? 4 : 2, a.nsplit);
-  const dim3 grid(a.n_attn + n_mem);
+  const dim3 grid(a.n_attn);
   if (dtype == HF_F32) return launch_pdl(attn_mem_kernel<float>, grid, dim3(THREADS), L.total, st, a);
   return launch_pdl(attn_mem_kernel<__nv_bfloat16>, grid, dim3(THREADS), L.total, st, a);
 }
 
 }  // namespace
-
-int attn_splits(const Dims& d) { return (d.W + JT - 1) / JT; }
-
-// Dynamic shared memory of the attention kernel is raised once per process
-// (at handle creation), so launches stay legal inside stream capture.
-cudaError_t configure_attn(const Dims& d) { return ensure_smem(attn_smem(d, 4, attn_splits(d)).total); }
-
-cudaError_t launch_attn_mem(int dtype, const Dims& d, int B, const float* proj, const void* ring_k,
-                            const void* ring_v, const int64_t* pos, const float* state, void* mix,
-                            float* part_o, float* part_ml, int* tickets, int32_t* err,
-                            cudaStream_t st, int* launches) {
-  if (B <= 0) return cudaSuccess;
-  AttnArgs a{};
-  a.d = d;
-  a.B = B;
-  a.nsplit = attn_splits(d);
-  a.n_attn = B * d.Hkv * a.nsplit;
-  a.qscale = 1.4426950408889634f / sqrtf((float)d.dh);
-  a.proj = proj;
-  a.ring_k = ring_k;
-  a.ring_v = ring_v;
-  a.pos = pos;
-  a.state = state;
-  a.mix = mix;
-  a.part_o = part_o;
-  a.part_ml = part_ml;
-  a.tickets = tickets;
-  a.err = err;
-  ++*launches;
-  return launch(dtype, a, B * d.Hm, st);
-}
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the window+block attention.
@@ -493,7 +411,7 @@ extern "C" hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t 
       a.part_ml = ptrs.scratch + (size_t)a.n_attn * R * head_dim;
       a.tickets = ptrs.tickets;
       a.err = ptrs.err;
-      e = launch(dtype, a, 0, (cudaStream_t)stream);
+      e = launch(dtype, a, (cudaStream_t)stream);
     }
   }
   if (e != cudaSuccess) {

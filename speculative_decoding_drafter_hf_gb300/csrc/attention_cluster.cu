@@ -1,0 +1,477 @@
+// Window + block attention and the draft-time memory read for one layer, in
+// one launch; the path hf_draft takes.
+//
+// Attention (learnaivisually explainer, "That is HyFlash"): the 7 slot
+// queries of a request attend, bidirectionally and with no mask, over the
+// valid entries of that request's window ring and over the 7 slot keys.
+//
+// Work split: the window of (request b, KV head g) is cut into `nsplit` <= 8
+// tiles of JT keys; the nsplit CTAs of (b, g) form one thread-block cluster.
+// Each CTA takes all G = Hq/Hkv query heads sharing g (G*7 query rows), so a
+// K/V tile crosses HBM once: one bulk copy (TMA) per tile into shared memory,
+// used in place in the ring's own element type. The slot keys join the
+// tile of rank 0. Scores and P.V are register-blocked over 4 / 2 query rows;
+// each lane walks its key's 16-byte chunks in a lane-rotated order so that
+// the 8 lanes of a quarter-warp touch distinct banks. Softmax is exp2-based
+// in fp32. The partial (max, sum, O) of every CTA stays in its shared memory;
+// after a cluster barrier, rank r combines rows r, r + nsplit, ... by reading
+// all partners' partials through distributed shared memory in rank order
+// (deterministic, no global round trip, no atomics).
+//
+// Memory read (same launch, the CTAs after the attention clusters):
+// y[s, h, p] = sum_n state[h, p, n] * C_s[s, n]. The state block of (b, h)
+// is read with 16-byte loads, all in flight at once, and reduced across the
+// lanes that share a state row. The state is never written here.
+#include "common.cuh"
+
+namespace hf {
+namespace {
+
+constexpr int MAXS = 16;     // max block slots
+constexpr int THREADS = 256;
+constexpr int MEM_QPT = 8;   // float4 state elements per thread (P*N <= 8192)
+constexpr int MAX_SPLIT = 8; // portable cluster size
+
+struct Plan {
+  int nsplit;  // CTAs (cluster size) per (request, KV head)
+  int jt;      // ring keys per CTA, multiple of 32
+};
+
+__host__ __device__ inline Plan make_plan(int W) {
+  Plan p;
+  p.nsplit = (W + 63) / 64;
+  if (p.nsplit > MAX_SPLIT) p.nsplit = MAX_SPLIT;
+  if (p.nsplit < 1) p.nsplit = 1;
+  int per = (W + p.nsplit - 1) / p.nsplit;
+  p.jt = (per + 31) / 32 * 32;
+  return p;
+}
+
+struct Args {
+  Dims d;
+  Plan plan;
+  int n_attn;     // attention CTAs = B * Hkv * nsplit
+  int n_mem;      // memory-read CTAs = B * Hm
+  float qscale;   // log2(e) / sqrt(dh)
+  const float* proj;    // [B*S, Nd] fp32: Q | K_s | V_s | C_s
+  const void* ring_k;   // [B][Hkv][W][dh] of this layer
+  const void* ring_v;
+  const int64_t* pos;   // [B]
+  const float* state;   // [B][Hm][P][N] of this layer
+  void* mix;            // [B*S, Nz]: O at columns [0, Hq*dh), y at [Hq*dh, Nz)
+  int32_t* err;
+};
+
+struct Layout {
+  size_t bar, kt, vt, q, s, ml, total;
+};
+
+__host__ __device__ inline Layout make_layout(const Dims& d, const Plan& p, int esize) {
+  Layout m{};
+  size_t off = 0;
+  const int R = d.G * d.S, JK = p.jt + d.S;
+  m.bar = off;
+  off += 16;
+  m.kt = off;
+  off += (size_t)JK * d.dh * esize;
+  m.vt = off;
+  off += (size_t)JK * d.dh * esize;
+  m.q = off;  // query rows, later the partial O
+  off += (size_t)R * (d.dh + 4) * 4;
+  m.s = off;
+  off += (size_t)R * JK * 4;
+  m.ml = off;
+  off += (size_t)R * 2 * 4;
+  off = (off + 15) & ~(size_t)15;
+  const size_t mem_need = (size_t)d.S * d.N * 4;
+  m.total = off > mem_need ? off : mem_need;
+  return m;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ float ld_peer_f(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// 16 bytes of T as floats.
+template <typename T> struct Chunk;
+template <> struct Chunk<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(const __nv_bfloat16* p, float* f) {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __bfloat1622float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+};
+template <> struct Chunk<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const float* p, float* f) {
+    const float4 r = *reinterpret_cast<const float4*>(p);
+    f[0] = r.x;
+    f[1] = r.y;
+    f[2] = r.z;
+    f[3] = r.w;
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ void attn_cta(const Args& a, uint8_t* sm, int idx) {
+  const Dims& d = a.d;
+  const int nsplit = a.plan.nsplit, JT = a.plan.jt;
+  const int rank = nsplit > 1 ? (int)cluster_rank() : 0;
+  const int pair = idx / nsplit;
+  const int kvh = pair % d.Hkv, b = pair / d.Hkv;
+  const int S = d.S, G = d.G, R = G * S, dh = d.dh, dhp = dh + 4, JK = JT + S;
+  constexpr int VE = Chunk<T>::N;
+  const int nch = dh / VE;  // 16-byte chunks per key row
+  const Layout L = make_layout(d, a.plan, (int)sizeof(T));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar);
+  T* kt = reinterpret_cast<T*>(sm + L.kt);
+  T* vt = reinterpret_cast<T*>(sm + L.vt);
+  float* q = reinterpret_cast<float*>(sm + L.q);
+  float* s = reinterpret_cast<float*>(sm + L.s);
+  float* ml = reinterpret_cast<float*>(sm + L.ml);
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid / 32, lane = tid % 32, nw = nthr / 32;
+
+  pdl_wait();
+  const long long p = __ldcg(&a.pos[b]);
+  const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);
+  const int j0 = rank * JT;
+  int nring = max(0, min(nv, j0 + JT) - j0);
+  const int nslot = rank == 0 ? S : 0;
+  const size_t rowbase = (size_t)b * S;
+  const size_t rb = ((size_t)b * d.Hkv + kvh) * d.W * dh;
+
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (nring > 0) {
+      const uint32_t bytes = (uint32_t)(nring * dh * sizeof(T));
+      mbar_expect_tx(bar, 2 * bytes);
+      bulk_g2s(kt, static_cast<const T*>(a.ring_k) + rb + (size_t)j0 * dh, bytes, bar);
+      bulk_g2s(vt, static_cast<const T*>(a.ring_v) + rb + (size_t)j0 * dh, bytes, bar);
+    }
+  }
+  // Query rows (pre-scaled, fp32) and, on rank 0, the slot keys/values
+  // appended after the ring tile in the ring's element type.
+  const int c4n = dh / 4;
+  for (int i = tid; i < R * c4n; i += nthr) {
+    const int r = i / c4n, c = (i % c4n) * 4, g = r / S, sl = r % S;
+    float4 x = __ldcg(reinterpret_cast<const float4*>(
+        a.proj + (rowbase + sl) * d.Nd + (size_t)(kvh * G + g) * dh + c));
+    x.x *= a.qscale;
+    x.y *= a.qscale;
+    x.z *= a.qscale;
+    x.w *= a.qscale;
+    *reinterpret_cast<float4*>(&q[r * dhp + c]) = x;
+  }
+  __syncthreads();  // barrier initialised before anyone waits on it
+  bool ok = true;
+  if (nring > 0) ok = mbar_wait(bar, 0);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) {
+      atomicOr(a.err, ERR_TIMEOUT);
+      mbar_wait(bar, 0);  // bounded: let the copies land before the buffers are reused
+    }
+    nring = 0;  // drop the ring tile; the cluster sequence below stays matched
+  }
+  // slot keys/values go after the (possibly dropped) ring rows
+  for (int i = tid; i < nslot * c4n; i += nthr) {
+    const int j = i / c4n, c = (i % c4n) * 4;
+    const float* row = a.proj + (rowbase + j) * d.Nd;
+    const float4 kx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
+    const float4 vx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
+    T* kd = kt + (size_t)(nring + j) * dh + c;
+    T* vd = vt + (size_t)(nring + j) * dh + c;
+    kd[0] = from_f<T>(kx.x); kd[1] = from_f<T>(kx.y); kd[2] = from_f<T>(kx.z); kd[3] = from_f<T>(kx.w);
+    vd[0] = from_f<T>(vx.x); vd[1] = from_f<T>(vx.y); vd[2] = from_f<T>(vx.z); vd[3] = from_f<T>(vx.w);
+  }
+  const int nk = nring + nslot;
+  __syncthreads();
+
+  // Scores: lane = key (32-key groups), 4 query rows per item.
+  {
+    const int kgroups = (nk + 31) / 32, rblocks = (R + 3) / 4;
+    for (int it = warp; it < kgroups * rblocks; it += nw) {
+      const int kg = it / rblocks, r0 = (it % rblocks) * 4;
+      const int j = kg * 32 + lane;
+      const bool jv = j < nk;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const T* krow = kt + (size_t)(jv ? j : 0) * dh;
+      for (int c = 0; c < nch; ++c) {
+        const int cc = (c + lane) % nch;
+        float kf[VE];
+        Chunk<T>::load(krow + cc * VE, kf);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int r = min(r0 + rr, R - 1);
+          const float* qr = q + r * dhp + cc * VE;
+#pragma unroll
+          for (int e4 = 0; e4 < VE; e4 += 4) {
+            const float4 qv = *reinterpret_cast<const float4*>(qr + e4);
+            acc[rr] = fmaf(qv.x, kf[e4], fmaf(qv.y, kf[e4 + 1],
+                      fmaf(qv.z, kf[e4 + 2], fmaf(qv.w, kf[e4 + 3], acc[rr]))));
+          }
+        }
+      }
+      if (jv) {
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+          if (r0 + rr < R) s[(r0 + rr) * JK + j] = acc[rr];
+      }
+    }
+  }
+  __syncthreads();
+
+  // Softmax (unnormalised): one warp per row.
+  for (int r = warp; r < R; r += nw) {
+    float m = -INFINITY;
+    for (int j = lane; j < nk; j += 32) m = fmaxf(m, s[r * JK + j]);
+    m = warp_max(m);
+    float l = 0.f;
+    for (int j = lane; j < nk; j += 32) {
+      const float e = exp2f(s[r * JK + j] - m);
+      s[r * JK + j] = e;
+      l += e;
+    }
+    l = warp_sum(l);
+    if (lane == 0) {
+      ml[r * 2 + 0] = m;
+      ml[r * 2 + 1] = l;
+    }
+  }
+  __syncthreads();
+
+  // P.V: item = (2 query rows, one 16-byte chunk of dh); the partial O
+  // overwrites the query rows (no longer needed).
+  {
+    const int rblocks = (R + 1) / 2;
+    float* o = q;
+    for (int it = tid; it < rblocks * nch; it += nthr) {
+      const int r0 = (it / nch) * 2, cc = it % nch;
+      const int r1 = min(r0 + 1, R - 1);
+      float acc0[VE], acc1[VE];
+#pragma unroll
+      for (int e = 0; e < VE; ++e) acc0[e] = acc1[e] = 0.f;
+      for (int j = 0; j < nk; ++j) {
+        float vf[VE];
+        Chunk<T>::load(vt + (size_t)j * dh + cc * VE, vf);
+        const float p0 = s[r0 * JK + j], p1 = s[r1 * JK + j];
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          acc0[e] = fmaf(p0, vf[e], acc0[e]);
+          acc1[e] = fmaf(p1, vf[e], acc1[e]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < VE; e += 4) {
+        *reinterpret_cast<float4*>(&o[r0 * dhp + cc * VE + e]) =
+            make_float4(acc0[e], acc0[e + 1], acc0[e + 2], acc0[e + 3]);
+        if (r0 + 1 < R)
+          *reinterpret_cast<float4*>(&o[(r0 + 1) * dhp + cc * VE + e]) =
+              make_float4(acc1[e], acc1[e + 1], acc1[e + 2], acc1[e + 3]);
+      }
+    }
+  }
+
+  T* mix = static_cast<T*>(a.mix);
+  if (nsplit == 1) {
+    __syncthreads();
+    for (int i = tid; i < R * c4n; i += nthr) {
+      const int r = i / c4n, c = (i % c4n) * 4, g = r / S, sl = r % S;
+      const float inv = 1.f / ml[r * 2 + 1];
+      const float4 x = *reinterpret_cast<const float4*>(&q[r * dhp + c]);
+      T* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
+      dst[0] = from_f<T>(x.x * inv);
+      dst[1] = from_f<T>(x.y * inv);
+      dst[2] = from_f<T>(x.z * inv);
+      dst[3] = from_f<T>(x.w * inv);
+    }
+    return;
+  }
+
+  // Combine through distributed shared memory: rank r owns rows r, r+nsplit, ...
+  cluster_sync_all();
+  const int my_rows = (R - rank + nsplit - 1) / nsplit;
+  for (int i = tid; i < my_rows * c4n; i += nthr) {
+    const int r = rank + (i / c4n) * nsplit, c = (i % c4n) * 4, g = r / S, sl = r % S;
+    float mp[MAX_SPLIT], lp[MAX_SPLIT];
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < MAX_SPLIT; ++sp) {
+      if (sp < nsplit) {
+        const uint32_t ad = peer_addr(&ml[r * 2], (uint32_t)sp);
+        mp[sp] = ld_peer_f(ad);
+        lp[sp] = ld_peer_f(ad + 4);
+        M = fmaxf(M, mp[sp]);
+      }
+    }
+    float Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sp = 0; sp < MAX_SPLIT; ++sp) {
+      if (sp < nsplit) {
+        const float wt = lp[sp] > 0.f ? exp2f(mp[sp] - M) : 0.f;
+        const float4 ov = ld_peer_f4(peer_addr(&q[r * dhp + c], (uint32_t)sp));
+        Lsum = fmaf(lp[sp], wt, Lsum);
+        acc.x = fmaf(wt, ov.x, acc.x);
+        acc.y = fmaf(wt, ov.y, acc.y);
+        acc.z = fmaf(wt, ov.z, acc.z);
+        acc.w = fmaf(wt, ov.w, acc.w);
+      }
+    }
+    const float inv = 1.f / Lsum;
+    T* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
+    dst[0] = from_f<T>(acc.x * inv);
+    dst[1] = from_f<T>(acc.y * inv);
+    dst[2] = from_f<T>(acc.z * inv);
+    dst[3] = from_f<T>(acc.w * inv);
+  }
+  cluster_sync_all();  // partners keep their shared memory until every read is done
+}
+
+template <typename T>
+__device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
+  const Dims& d = a.d;
+  const int b = idx / d.Hm, hd = idx % d.Hm;
+  const int S = d.S, N = d.N, P = d.P;
+  float* cs = reinterpret_cast<float*>(sm);
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  pdl_wait();
+  const float4* h = reinterpret_cast<const float4*>(a.state + (((size_t)b * d.Hm + hd) * P) * N);
+  const int nq = P * N / 4;
+  float4 hv[MEM_QPT];
+#pragma unroll
+  for (int u = 0; u < MEM_QPT; ++u) {
+    const int qi = tid + u * nthr;
+    hv[u] = qi < nq ? __ldcg(&h[qi]) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int cC = d.QD + 2 * d.KVD;
+  for (int i = tid; i < S * N / 4; i += nthr) {
+    const int sl = (i * 4) / N, n = (i * 4) % N;
+    *reinterpret_cast<float4*>(&cs[sl * N + n]) =
+        __ldcg(reinterpret_cast<const float4*>(a.proj + ((size_t)b * S + sl) * d.Nd + cC + n));
+  }
+  __syncthreads();
+  const int gsz = N / 4;  // lanes sharing one state row (power of two <= 32)
+  T* mix = static_cast<T*>(a.mix);
+#pragma unroll
+  for (int u = 0; u < MEM_QPT; ++u) {
+    if (u * nthr >= nq) break;  // uniform across the CTA
+    const int qi = tid + u * nthr;
+    const int pr = (qi * 4) / N, n = (qi * 4) % N;
+#pragma unroll
+    for (int sl = 0; sl < MAXS; ++sl) {
+      if (sl >= S) break;
+      const float4 c = *reinterpret_cast<const float4*>(&cs[sl * N + n]);
+      float acc = hv[u].x * c.x + hv[u].y * c.y + hv[u].z * c.z + hv[u].w * c.w;
+      for (int o = gsz / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if ((qi & (gsz - 1)) == 0 && qi < nq)
+        mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)hd * P + pr] = from_f<T>(acc);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(THREADS) attn_cluster_kernel(Args a) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  pdl_trigger();
+  const int idx = blockIdx.x;
+  if (idx < a.n_attn)
+    attn_cta<T>(a, sm, idx);
+  else if (idx < a.n_attn + a.n_mem)
+    mem_cta<T>(a, sm, idx - a.n_attn);
+  else
+    pdl_wait();  // cluster padding
+}
+
+}  // namespace
+
+size_t attn_cluster_smem(const Dims& d, int esize) {
+  return make_layout(d, make_plan(d.W), esize).total;
+}
+
+cudaError_t configure_attn_cluster(const Dims& d) {
+  static int configured = 0;
+  const int smem = (int)attn_cluster_smem(d, 4);
+  if (smem <= configured) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<float>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_cluster_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) configured = smem;
+  return e;
+}
+
+cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
+                                const void* ring_k, const void* ring_v, const int64_t* pos,
+                                const float* state, void* mix, int32_t* err, cudaStream_t st,
+                                int* launches) {
+  if (B <= 0) return cudaSuccess;
+  Args a{};
+  a.d = d;
+  a.plan = make_plan(d.W);
+  a.n_attn = B * d.Hkv * a.plan.nsplit;
+  a.n_mem = B * d.Hm;
+  a.qscale = 1.4426950408889634f / sqrtf((float)d.dh);
+  a.proj = proj;
+  a.ring_k = ring_k;
+  a.ring_v = ring_v;
+  a.pos = pos;
+  a.state = state;
+  a.mix = mix;
+  a.err = err;
+  const int cz = a.plan.nsplit;
+  const int total = (a.n_attn + a.n_mem + cz - 1) / cz * cz;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(total);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = make_layout(d, a.plan, dtype == HF_F32 ? 4 : 2).total;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cz;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  ++*launches;
+  if (dtype == HF_F32) return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<float>, a);
+  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<__nv_bfloat16>, a);
+}
+
+}  // namespace hf

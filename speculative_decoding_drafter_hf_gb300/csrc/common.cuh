@@ -209,19 +209,18 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
 int tc_pick_splits(int M, int N, int K);
 
 // One-time kernel attribute set-up (dynamic shared memory limits, driver
-// entry points), done at handle creation.
+// entry points, cluster occupancy), done at handle creation.
 cudaError_t configure_tc();
-cudaError_t configure_attn(const Dims& d);
+cudaError_t configure_attn_cluster(const Dims& d);
 
-// Window+block attention and memory read for one layer, batch B, one launch.
-// proj [B*S, Nd] fp32 (Q|K_s|V_s|C_s); ring_k/v of this layer; pos [Bmax];
-// state of this layer; mix [B*S, Nz] model dtype (O | y); part_o/part_ml:
-// split partials; tickets [B*Hkv] (kept at zero).
-int attn_splits(const Dims& d);
-cudaError_t launch_attn_mem(int dtype, const Dims& d, int B, const float* proj,
-                            const void* ring_k, const void* ring_v, const int64_t* pos,
-                            const float* state, void* mix, float* part_o, float* part_ml,
-                            int* tickets, int32_t* err, cudaStream_t st, int* launches);
+// Window+block attention and memory read for one layer, batch B, one launch
+// (attention_cluster.cu). proj [B*S, Nd] fp32 (Q|K_s|V_s|C_s); ring_k/v and
+// state of this layer; pos [Bmax]; mix [B*S, Nz] model dtype (O | y).
+size_t attn_cluster_smem(const Dims& d, int esize);
+cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
+                                const void* ring_k, const void* ring_v, const int64_t* pos,
+                                const float* state, void* mix, int32_t* err, cudaStream_t st,
+                                int* launches);
 
 // Commit prep: validate counts, offsets, row map, tags, gather rows.
 cudaError_t launch_commit_prep(int dtype, const Dims& d, int B, const void* feats,

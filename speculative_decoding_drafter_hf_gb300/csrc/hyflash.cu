@@ -51,14 +51,10 @@ struct hf_handle {
   float* proj = nullptr;       // [Bmax*S][Nd]
   void* mix = nullptr;         // [Bmax*S][Nz]
   void* xbuf[2] = {nullptr, nullptr};
-  float* attn_o = nullptr;
-  float* attn_ml = nullptr;
-  int nsplit = 1;
   float* part = nullptr;
   size_t part_elems = 0;
   int* counters = nullptr;     // split-K tickets of the tensor-core GEMM
   int n_counters = 0;
-  int* attn_cnt = nullptr;     // split-combine tickets of the attention kernel
   int num_sms = 152;
 
   float* pf_xbd = nullptr;     // [Tseg][NS]
@@ -100,6 +96,23 @@ hf_status cuda_fail(hf_handle* h, cudaError_t e, const char* where) {
 
 long long round_up(long long a, long long b) { return (a + b - 1) / b * b; }
 
+Dims make_dims(const hf_config& c) {
+  Dims d{};
+  d.D = c.d_model; d.Hq = c.n_q_heads; d.Hkv = c.n_kv_heads; d.dh = c.head_dim;
+  d.W = c.window; d.S = c.block; d.Hm = c.ssm_heads; d.P = c.ssm_headdim; d.N = c.d_state;
+  d.L = c.n_layers; d.Bmax = c.max_batch;
+  d.G = d.Hq / d.Hkv;
+  d.QD = d.Hq * d.dh;
+  d.KVD = d.Hkv * d.dh;
+  d.dinner = d.Hm * d.P;
+  d.Nd = d.QD + 2 * d.KVD + d.N;
+  d.Nc = 2 * d.KVD + d.dinner + d.N + d.Hm;
+  d.NS = (int)round_up(d.dinner + d.N + d.Hm, 4);
+  d.Nz = d.QD + d.dinner;
+  d.esize = c.dtype == HF_F32 ? 4 : 2;
+  return d;
+}
+
 hf_status validate(const hf_config* c, std::string* why) {
   auto bad = [&](const char* m) { *why = m; return HF_EINVAL; };
   if (!c) return bad("config is NULL");
@@ -125,24 +138,12 @@ hf_status validate(const hf_config* c, std::string* why) {
   if (c->max_batch > 65535) return bad("max_batch must be <= 65535");
   if (c->dtype == HF_BF16 && (c->head_dim % 8 || ((long long)c->ssm_heads * c->ssm_headdim) % 8))
     return bad("bf16 needs head_dim and ssm_heads*ssm_headdim multiples of 8");
+  {
+    const Dims d = make_dims(*c);
+    if (hf::attn_cluster_smem(d, d.esize) > 232448)
+      return bad("window too long for the attention tile (shared memory per CTA > 227 KB)");
+  }
   return HF_OK;
-}
-
-Dims make_dims(const hf_config& c) {
-  Dims d{};
-  d.D = c.d_model; d.Hq = c.n_q_heads; d.Hkv = c.n_kv_heads; d.dh = c.head_dim;
-  d.W = c.window; d.S = c.block; d.Hm = c.ssm_heads; d.P = c.ssm_headdim; d.N = c.d_state;
-  d.L = c.n_layers; d.Bmax = c.max_batch;
-  d.G = d.Hq / d.Hkv;
-  d.QD = d.Hq * d.dh;
-  d.KVD = d.Hkv * d.dh;
-  d.dinner = d.Hm * d.P;
-  d.Nd = d.QD + 2 * d.KVD + d.N;
-  d.Nc = 2 * d.KVD + d.dinner + d.N + d.Hm;
-  d.NS = (int)round_up(d.dinner + d.N + d.Hm, 4);
-  d.Nz = d.QD + d.dinner;
-  d.esize = c.dtype == HF_F32 ? 4 : 2;
-  return d;
 }
 
 hf_status dev_alloc(hf_handle* h, void** p, size_t bytes) {
@@ -347,10 +348,8 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   const size_t L = d.L, Bm = d.Bmax;
   h->rmax = std::max<long long>((long long)(d.S + 1) * Bm, (long long)Bm * d.W);
   h->xbd_ls = (long long)(d.S + 1) * Bm * d.NS;
-  h->nsplit = hf::attn_splits(d);
   h->pf_tokens = h->cfg.prefill_tokens_max;
   h->part_elems = (size_t)16 << 20;
-  const size_t R = (size_t)d.G * d.S;
 
   hf_status s = HF_OK;
   auto A = [&](void** p, size_t bytes) {
@@ -375,12 +374,9 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   A(&h->mix, Bm * d.S * d.Nz * es);
   A(&h->xbuf[0], Bm * d.S * d.D * es);
   A(&h->xbuf[1], Bm * d.S * d.D * es);
-  A((void**)&h->attn_o, Bm * d.Hkv * h->nsplit * R * d.dh * 4);
-  A((void**)&h->attn_ml, Bm * d.Hkv * h->nsplit * R * 2 * 4);
   A((void**)&h->part, h->part_elems * 4);
   h->n_counters = 1 << 16;
   A((void**)&h->counters, (size_t)h->n_counters * 4);
-  A((void**)&h->attn_cnt, Bm * d.Hkv * 4);
   if (s == HF_OK) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess && sms > 0)
@@ -396,7 +392,7 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     if (e != cudaSuccess) s = cuda_fail(h, e, "cudaMemset(tags)");
   }
   if (s == HF_OK) {
-    e = hf::configure_attn(h->d);
+    e = hf::configure_attn_cluster(h->d);
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc();
     if (e != cudaSuccess) s = cuda_fail(h, e, "kernel set-up");
   }
@@ -496,10 +492,11 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
     if (s != HF_OK) return s;
     {
       Scope sc(h, HF_K_ATTN_MEM, st);
-      cudaError_t e = hf::launch_attn_mem(h->cfg.dtype, d, batch, h->proj,
-                                          bptr(h->ring_k, l * ring_ls), bptr(h->ring_v, l * ring_ls),
-                                          h->pos, h->state + l * state_ls, h->mix, h->attn_o,
-                                          h->attn_ml, h->attn_cnt, h->err, st, &sc.count);
+      cudaError_t e = hf::launch_attn_cluster(h->cfg.dtype, d, batch, h->proj,
+                                              bptr(h->ring_k, l * ring_ls),
+                                              bptr(h->ring_v, l * ring_ls), h->pos,
+                                              h->state + l * state_ls, h->mix, h->err, st,
+                                              &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
     }
     Epi e2 = epi_base(h);
