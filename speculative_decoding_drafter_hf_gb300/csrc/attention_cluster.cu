@@ -220,35 +220,55 @@ __device__ __forceinline__ void attn_cta(const Args& a, uint8_t* sm, int idx) {
   const int nk = nring + nslot;
   __syncthreads();
 
-  // Scores: lane = key (32-key groups), 4 query rows per item.
+  // Scores: a half-warp takes one key, each of its 16 lanes a contiguous
+  // slice of dh/16 elements (conflict-free); a warp owns 4 query rows whose
+  // matching slices it keeps in registers across all keys. Partial dots are
+  // summed over the 16 lanes of the half with shuffles.
   {
-    const int kgroups = (nk + 31) / 32, rblocks = (R + 3) / 4;
-    for (int it = warp; it < kgroups * rblocks; it += nw) {
-      const int kg = it / rblocks, r0 = (it % rblocks) * 4;
-      const int j = kg * 32 + lane;
-      const bool jv = j < nk;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const T* krow = kt + (size_t)(jv ? j : 0) * dh;
-      for (int c = 0; c < nch; ++c) {
-        const int cc = (c + lane) % nch;
-        float kf[VE];
-        Chunk<T>::load(krow + cc * VE, kf);
+    const int half = lane / 16, hl = lane % 16;
+    const int E = dh / 16;  // elements per lane, 1..16
+    const int rblocks = (R + 3) / 4;
+    for (int rbk = warp; rbk < rblocks; rbk += nw) {
+      const int r0 = rbk * 4;
+      float qf[4][16];
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const int r = min(r0 + rr, R - 1);
-          const float* qr = q + r * dhp + cc * VE;
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = min(r0 + rr, R - 1);
 #pragma unroll
-          for (int e4 = 0; e4 < VE; e4 += 4) {
-            const float4 qv = *reinterpret_cast<const float4*>(qr + e4);
-            acc[rr] = fmaf(qv.x, kf[e4], fmaf(qv.y, kf[e4 + 1],
-                      fmaf(qv.z, kf[e4 + 2], fmaf(qv.w, kf[e4 + 3], acc[rr]))));
+        for (int e = 0; e < 16; ++e) qf[rr][e] = e < E ? q[r * dhp + hl * E + e] : 0.f;
+      }
+      for (int jp = 0; jp < nk; jp += 2) {
+        const int j = jp + half;
+        float kf[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) kf[e] = 0.f;
+        if (j < nk) {
+          const T* kp = kt + (size_t)j * dh + hl * E;
+          if (E == VE) {
+            Chunk<T>::load(kp, kf);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (e < E) kf[e] = to_f(kp[e]);
           }
         }
-      }
-      if (jv) {
+        float acc[4];
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr)
-          if (r0 + rr < R) s[(r0 + rr) * JK + j] = acc[rr];
+        for (int rr = 0; rr < 4; ++rr) {
+          float a2 = 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) a2 = fmaf(qf[rr][e], kf[e], a2);
+          acc[rr] = a2;
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], o);
+        if (hl == 0 && j < nk) {
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr)
+            if (r0 + rr < R) s[(r0 + rr) * JK + j] = acc[rr];
+        }
       }
     }
   }
@@ -431,6 +451,13 @@ cudaError_t configure_attn_cluster(const Dims& d) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(attn_cluster_kernel<__nv_bfloat16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_cluster_kernel<float>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_cluster_kernel<__nv_bfloat16>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) configured = smem;
   return e;
 }

@@ -355,9 +355,14 @@ constexpr size_t tc_smem() {
 
 template <int BN, int STAGES>
 cudaError_t configure_one() {
-  return cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)tc_smem<BN, STAGES>());
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)tc_smem<BN, STAGES>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
 template <int BN, int STAGES>
