@@ -82,7 +82,7 @@ typedef struct {
   int32_t d_model;      /* D */
   int32_t n_q_heads;    /* Hq */
   int32_t n_kv_heads;   /* Hkv, divides Hq */
-  int32_t head_dim;     /* dh, multiple of 16, <= 256 */
+  int32_t head_dim;     /* dh: 32, 64, 128 or 256 */
   int32_t window;       /* W >= block+1: sliding-window ring length */
   int32_t block;        /* S = 7 draft slots (1..16 accepted) */
   int32_t ssm_heads;    /* Hm */

@@ -143,7 +143,7 @@ template <> struct Chunk<float> {
   }
 };
 
-template <typename T>
+template <typename T, int E>
 __device__ __forceinline__ void attn_cta(const Args& a, uint8_t* sm, int idx) {
   const Dims& d = a.d;
   const int nsplit = a.plan.nsplit, JT = a.plan.jt;
@@ -225,39 +225,38 @@ __device__ __forceinline__ void attn_cta(const Args& a, uint8_t* sm, int idx) {
   // matching slices it keeps in registers across all keys. Partial dots are
   // summed over the 16 lanes of the half with shuffles.
   {
-    const int half = lane / 16, hl = lane % 16;
-    const int E = dh / 16;  // elements per lane, 1..16
+    const int half = lane / 16, hl = lane % 16;  // E = dh / 16 elements per lane
     const int rblocks = (R + 3) / 4;
     for (int rbk = warp; rbk < rblocks; rbk += nw) {
       const int r0 = rbk * 4;
-      float qf[4][16];
+      float qf[4][E];
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
         const int r = min(r0 + rr, R - 1);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) qf[rr][e] = e < E ? q[r * dhp + hl * E + e] : 0.f;
+        for (int e = 0; e < E; ++e) qf[rr][e] = q[r * dhp + hl * E + e];
       }
       for (int jp = 0; jp < nk; jp += 2) {
         const int j = jp + half;
-        float kf[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) kf[e] = 0.f;
+        float kf[E];
         if (j < nk) {
           const T* kp = kt + (size_t)j * dh + hl * E;
-          if (E == VE) {
+          if constexpr (E == VE) {
             Chunk<T>::load(kp, kf);
           } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              if (e < E) kf[e] = to_f(kp[e]);
+            for (int e = 0; e < E; ++e) kf[e] = to_f(kp[e]);
           }
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) kf[e] = 0.f;
         }
         float acc[4];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
           float a2 = 0.f;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) a2 = fmaf(qf[rr][e], kf[e], a2);
+          for (int e = 0; e < E; ++e) a2 = fmaf(qf[rr][e], kf[e], a2);
           acc[rr] = a2;
         }
 #pragma unroll
@@ -423,13 +422,14 @@ __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
   }
 }
 
-template <typename T>
+// E = head_dim / 16: the slice of a key each lane of a half-warp holds.
+template <typename T, int E>
 __global__ void __launch_bounds__(THREADS) attn_cluster_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t sm[];
   pdl_trigger();
   const int idx = blockIdx.x;
   if (idx < a.n_attn)
-    attn_cta<T>(a, sm, idx);
+    attn_cta<T, E>(a, sm, idx);
   else if (idx < a.n_attn + a.n_mem)
     mem_cta<T>(a, sm, idx - a.n_attn);
   else
@@ -442,24 +442,45 @@ size_t attn_cluster_smem(const Dims& d, int esize) {
   return make_layout(d, make_plan(d.W), esize).total;
 }
 
+template <typename T, int E>
+cudaError_t configure_one(int smem) {
+  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<T, E>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_cluster_kernel<T, E>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
+template <typename T>
+cudaError_t configure_dtype(int smem) {
+  cudaError_t e = configure_one<T, 2>(smem);
+  if (e == cudaSuccess) e = configure_one<T, 4>(smem);
+  if (e == cudaSuccess) e = configure_one<T, 8>(smem);
+  if (e == cudaSuccess) e = configure_one<T, 16>(smem);
+  return e;
+}
+
 cudaError_t configure_attn_cluster(const Dims& d) {
   static int configured = 0;
   const int smem = (int)attn_cluster_smem(d, 4);
   if (smem <= configured) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<float>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_cluster_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_cluster_kernel<float>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_cluster_kernel<__nv_bfloat16>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = configure_dtype<float>(smem);
+  if (e == cudaSuccess) e = configure_dtype<__nv_bfloat16>(smem);
   if (e == cudaSuccess) configured = smem;
   return e;
+}
+
+template <typename T>
+cudaError_t launch_typed(const cudaLaunchConfig_t& cfg, const Args& a) {
+  switch (a.d.dh) {
+    case 32: return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<T, 2>, a);
+    case 64: return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<T, 4>, a);
+    case 128: return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<T, 8>, a);
+    case 256: return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<T, 16>, a);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
@@ -497,8 +518,8 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   ++*launches;
-  if (dtype == HF_F32) return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<float>, a);
-  return cudaLaunchKernelEx(&cfg, attn_cluster_kernel<__nv_bfloat16>, a);
+  if (dtype == HF_F32) return launch_typed<float>(cfg, a);
+  return launch_typed<__nv_bfloat16>(cfg, a);
 }
 
 }  // namespace hf

@@ -12,7 +12,7 @@
 namespace hf {
 namespace {
 
-constexpr int QPT = 8;  // float4 state elements per thread (P*N <= 8192)
+constexpr int QPT = 2;  // float4 state elements per thread of the state update
 
 // grid (B, S+1): CTA (b, t) owns accepted row t of request b.
 template <typename T>
@@ -75,28 +75,34 @@ commit_prep_kernel(Dims d, int B, const T* __restrict__ feats, const int32_t* __
   }
 }
 
-// grid (Hm, B, L): the state of one (layer, request, head) is read once (all
-// loads in flight together), advanced over the request's accepted rows in
-// order, and written once.
+// grid (Hm * qsplit, B, L): CTA (h, q) takes 1/qsplit of the state of one
+// (layer, request, head), reads it once (all loads in flight together),
+// advances it over the request's accepted rows in order, and writes it once.
 __global__ void __launch_bounds__(256)
-commit_state_kernel(Dims d, const int32_t* __restrict__ offsets, const float* __restrict__ xbd,
-                    long long xls, const float* __restrict__ A_log, float* __restrict__ state,
+commit_state_kernel(Dims d, int qsplit, const int32_t* __restrict__ offsets,
+                    const float* __restrict__ xbd, long long xls,
+                    const float* __restrict__ A_log, float* __restrict__ state,
                     int64_t* __restrict__ pos) {
   extern __shared__ __align__(16) float sm[];
   pdl_trigger();
   pdl_wait();
-  const int hd = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
+  const int hd = blockIdx.x / qsplit, qs = blockIdx.x % qsplit;
+  const int b = blockIdx.y, l = blockIdx.z;
   const int off = __ldcg(&offsets[b]), n = __ldcg(&offsets[b + 1]) - off;
   if (n <= 0) return;
-  if (l == 0 && hd == 0 && threadIdx.x == 0) pos[b] += n;
+  if (l == 0 && hd == 0 && qs == 0 && threadIdx.x == 0) pos[b] += n;
   const int P = d.P, N = d.N;
   float4* h = reinterpret_cast<float4*>(state + ((((size_t)l * d.Bmax + b) * d.Hm + hd) * P) * N);
   const int nq = P * N / 4;
+  const int q0 = qs * (QPT * (int)blockDim.x);
   float4 hv[QPT];
+  int pi[QPT], ci[QPT];
 #pragma unroll
   for (int u = 0; u < QPT; ++u) {
-    const int q = threadIdx.x + u * blockDim.x;
+    const int q = q0 + threadIdx.x + u * blockDim.x;
     hv[u] = q < nq ? __ldcg(&h[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    pi[u] = (q * 4) / N;
+    ci[u] = (q * 4) % N;
   }
   // stage x (this head), B and dt of the n accepted rows
   const int rows = d.S + 1;       // n <= block + 1
@@ -117,27 +123,23 @@ commit_state_kernel(Dims d, const int32_t* __restrict__ offsets, const float* __
   for (int t = threadIdx.x; t < n; t += blockDim.x)
     sd[t] = __ldcg(&xb[(size_t)(off + t) * d.NS + d.dinner + N + hd]);
   __syncthreads();
-  const float A = -expf(A_log[l * d.Hm + hd]);
+  const float A = -expf(__ldcg(&A_log[l * d.Hm + hd]));
   for (int t = 0; t < n; ++t) {
     const float dt = sd[t];
     const float dec = expf(dt * A);
 #pragma unroll
     for (int u = 0; u < QPT; ++u) {
-      const int q = threadIdx.x + u * blockDim.x;
-      if (q < nq) {
-        const int e = q * 4, p = e / N, c = e % N;
-        const float xv = dt * sx[t * P + p];
-        const float4 Bv = *reinterpret_cast<const float4*>(&sb[t * N + c]);
-        hv[u].x = fmaf(dec, hv[u].x, xv * Bv.x);
-        hv[u].y = fmaf(dec, hv[u].y, xv * Bv.y);
-        hv[u].z = fmaf(dec, hv[u].z, xv * Bv.z);
-        hv[u].w = fmaf(dec, hv[u].w, xv * Bv.w);
-      }
+      const float xv = dt * sx[t * P + pi[u]];
+      const float4 Bv = *reinterpret_cast<const float4*>(&sb[t * N + ci[u]]);
+      hv[u].x = fmaf(dec, hv[u].x, xv * Bv.x);
+      hv[u].y = fmaf(dec, hv[u].y, xv * Bv.y);
+      hv[u].z = fmaf(dec, hv[u].z, xv * Bv.z);
+      hv[u].w = fmaf(dec, hv[u].w, xv * Bv.w);
     }
   }
 #pragma unroll
   for (int u = 0; u < QPT; ++u) {
-    const int q = threadIdx.x + u * blockDim.x;
+    const int q = q0 + threadIdx.x + u * blockDim.x;
     if (q < nq) h[q] = hv[u];
   }
 }
@@ -163,8 +165,10 @@ cudaError_t launch_commit_state(const Dims& d, int B, const int32_t* offsets, co
                                 cudaStream_t st) {
   // staging for block+1 rows of x (P values), B (N values) and dt
   const size_t smem = (size_t)(d.S + 1) * (d.P + d.N + 1) * sizeof(float);
-  return launch_pdl(commit_state_kernel, dim3(d.Hm, B, d.L), dim3(256), smem, st, d, offsets, xbd,
-                    xls, A_log, state, pos);
+  const int nq = d.P * d.N / 4;
+  const int qsplit = (nq + QPT * 256 - 1) / (QPT * 256);
+  return launch_pdl(commit_state_kernel, dim3(d.Hm * qsplit, B, d.L), dim3(256), smem, st, d,
+                    qsplit, offsets, xbd, xls, A_log, state, pos);
 }
 
 }  // namespace hf

@@ -118,7 +118,7 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
 struct TcArgs {
   int M, N, K;        // D is M x N
   int kblocks;        // ceil(K / 64)
-  int splits;         // split-K factor (grid.z = cluster size along z; <= 8)
+  int splits;         // split-K factor (grid.x = cluster size along x; <= 8)
   int swap;           // 1: output row = n, column = m; 0: row = m, column = n
   int prefetch_a;     // 1: A does not depend on earlier kernels (weights): load it
                       //    before waiting on the previous kernel
@@ -146,7 +146,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] issued, [2] consumed, [3] last
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int m_tile = blockIdx.x, n_tile = blockIdx.y, split = blockIdx.z;
+  // grid (splits, m_tiles, n_tiles); the splits of one tile form a cluster along x
+  const int split = blockIdx.x, m_tile = blockIdx.y, n_tile = blockIdx.z;
   const int kb0 = (int)((long long)split * a.kblocks / a.splits);
   const int kb1 = (int)((long long)(split + 1) * a.kblocks / a.splits);
   const int nkb = kb1 - kb0;
@@ -375,9 +376,9 @@ cudaLaunchConfig_t tc_config(dim3 grid, int cz, cudaStream_t st, cudaLaunchAttri
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.x = cz;
   attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = cz;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cfg;
@@ -395,7 +396,7 @@ cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs
 template <int BN, int STAGES>
 int max_clusters(int cz) {
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = tc_config<BN, STAGES>(dim3(1, 1, cz), cz, nullptr, attr);
+  cudaLaunchConfig_t cfg = tc_config<BN, STAGES>(dim3(cz, 1, 1), cz, nullptr, attr);
   cfg.attrs = attr + 1;  // occupancy query: cluster shape only
   cfg.numAttrs = 1;
   int n = 0;
@@ -469,7 +470,8 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   if (e != cudaSuccess) return e;
   e = make_map(&mb, B, N, K, ldb, bn);
   if (e != cudaSuccess) return e;
-  dim3 grid(m_tiles, n_tiles, a.splits);
+  if (m_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
+  dim3 grid(a.splits, m_tiles, n_tiles);
   ++*launches;
   switch (bn) {
     case 16: return launch_tc<16, 6>(ma, mb, a, epi, grid, st);

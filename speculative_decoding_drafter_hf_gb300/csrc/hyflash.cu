@@ -122,7 +122,8 @@ hf_status validate(const hf_config* c, std::string* why) {
     return bad("every dimension must be positive");
   if (c->n_groups != 1) return bad("n_groups must be 1");
   if (c->n_q_heads % c->n_kv_heads) return bad("n_kv_heads must divide n_q_heads");
-  if (c->head_dim % 16 || c->head_dim > 256) return bad("head_dim must be a multiple of 16, <= 256");
+  if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256)
+    return bad("head_dim must be 32, 64, 128 or 256");
   if (c->d_state < 4 || c->d_state > 128 || (c->d_state & (c->d_state - 1)))
     return bad("d_state must be a power of two in 4..128");
   if (c->ssm_headdim % 4) return bad("ssm_headdim must be a multiple of 4");
