@@ -422,6 +422,305 @@ __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core variant (bf16 rings, head_dim a multiple of 64).
+//
+// Ring K/V tiles arrive by 2-D TMA in 128-byte-swizzled sub-tiles of 64
+// columns (16-byte chunk c of row r stored at chunk c ^ (r & 7)), so the
+// 8 rows an ldmatrix phase reads fall in distinct banks. Q (pre-scaled) and
+// the probabilities P are written by threads in the same layout. Q.K^T and
+// P.V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate): the tiles are
+// G*7 <= 64 query rows by <= 80 keys, below the 64/128-row minimum of the
+// tcgen05 path. Softmax is fp32; P is rounded to bf16 for the P.V product
+// and the row sums use the rounded values.
+
+struct TcLayout {
+  size_t k, v, q, p, s, o, ml, bar, total;
+  int krows, qrows, ksub;
+};
+
+__host__ __device__ inline TcLayout make_tc_layout(const Dims& d, const Plan& pl) {
+  TcLayout m{};
+  m.krows = (pl.jt + d.S + 15) / 16 * 16;
+  m.qrows = (d.G * d.S + 15) / 16 * 16;
+  m.ksub = (m.krows + 63) / 64;
+  const int dsub = d.dh / 64;
+  size_t off = 0;  // sub-tiles: rows multiple of 16 -> sizes multiple of 2048 B
+  m.k = off;
+  off += (size_t)dsub * m.krows * 128;
+  m.v = off;
+  off += (size_t)dsub * m.krows * 128;
+  m.q = off;
+  off += (size_t)dsub * m.qrows * 128;
+  m.p = off;
+  off += (size_t)m.ksub * m.qrows * 128;
+  m.s = off;
+  off += (size_t)m.qrows * (m.krows + 4) * 4;
+  m.o = off;
+  off += (size_t)m.qrows * (d.dh + 4) * 4;
+  m.ml = off;
+  off += (size_t)m.qrows * 2 * 4;
+  m.bar = off;
+  off += 16;
+  const size_t mem_need = (size_t)d.S * d.N * 4;
+  m.total = (off > mem_need ? off : mem_need) + 1024;  // + slack to 1024-align the base
+  return m;
+}
+
+// Byte offset of 16-byte chunk c of row r in a swizzled tile of `rows` rows.
+__device__ __forceinline__ uint32_t sw_chunk(int rows, int r, int c) {
+  return (uint32_t)((c >> 3) * rows * 128 + r * 128 + ((((c & 7) ^ (r & 7))) << 4));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t a, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(a));
+}
+__device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk,
+                                            const CUtensorMap* mv, uint8_t* sm_raw, int idx) {
+  const Dims& d = a.d;
+  const int nsplit = a.plan.nsplit, JT = a.plan.jt;
+  const int rank = nsplit > 1 ? (int)cluster_rank() : 0;
+  const int pair = idx / nsplit;
+  const int kvh = pair % d.Hkv, b = pair / d.Hkv;
+  const int S = d.S, G = d.G, R = G * S, dh = d.dh, dsub = dh / 64;
+  const TcLayout L = make_tc_layout(d, a.plan);
+  const int KR = L.krows, QR = L.qrows;
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* kt = sm + L.k;
+  uint8_t* vt = sm + L.v;
+  uint8_t* qt = sm + L.q;
+  uint8_t* pt = sm + L.p;
+  float* s = reinterpret_cast<float*>(sm + L.s);
+  float* o = reinterpret_cast<float*>(sm + L.o);
+  float* ml = reinterpret_cast<float*>(sm + L.ml);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar);
+  const int SLD = KR + 4, OLD = dh + 4;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid / 32, lane = tid % 32, nw = nthr / 32;
+
+  pdl_wait();
+  const long long p = __ldcg(&a.pos[b]);
+  const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);
+  const int j0 = rank * JT;
+  int nring = max(0, min(nv, j0 + JT) - j0);
+  const int nslot = rank == 0 ? S : 0;
+  const size_t rowbase = (size_t)b * S;
+
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (nring > 0) {
+      const int y0 = (b * d.Hkv + kvh) * d.W + j0;
+      mbar_expect_tx(bar, (uint32_t)(2 * dsub * JT * 128));
+      for (int u = 0; u < dsub; ++u) {
+        tma_load_2d(kt + (size_t)u * KR * 128, mk, bar, u * 64, y0);
+        tma_load_2d(vt + (size_t)u * KR * 128, mv, bar, u * 64, y0);
+      }
+    }
+  }
+  // Q rows (pre-scaled) as bf16; rows R..QR-1 zero.
+  const int c4n = dh / 4;
+  for (int i = tid; i < QR * c4n; i += nthr) {
+    const int r = i / c4n, c = (i % c4n) * 4;
+    uint2 w = make_uint2(0u, 0u);
+    if (r < R) {
+      const int g = r / S, sl = r % S;
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(
+          a.proj + (rowbase + sl) * d.Nd + (size_t)(kvh * G + g) * dh + c));
+      w = make_uint2(pack_bf16x2(x.x * a.qscale, x.y * a.qscale),
+                     pack_bf16x2(x.z * a.qscale, x.w * a.qscale));
+    }
+    *reinterpret_cast<uint2*>(qt + sw_chunk(QR, r, c >> 3) + (c & 7) * 2) = w;
+  }
+  __syncthreads();  // barrier initialised before anyone waits on it
+  bool ok = true;
+  if (nring > 0) ok = mbar_wait(bar, 0);
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) {
+      atomicOr(a.err, ERR_TIMEOUT);
+      mbar_wait(bar, 0);  // bounded: let the copies land before the buffers are reused
+    }
+    nring = 0;
+  }
+  const int nk = nring + nslot;
+  // slot keys/values after the ring rows; rows nk..KR-1 zero (finite V for P.V)
+  for (int i = tid; i < (KR - nring) * c4n; i += nthr) {
+    const int j = nring + i / c4n, c = (i % c4n) * 4;
+    uint2 kw = make_uint2(0u, 0u), vw = make_uint2(0u, 0u);
+    if (j < nk) {
+      const float* row = a.proj + (rowbase + (j - nring)) * d.Nd;
+      const float4 kx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
+      const float4 vx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
+      kw = make_uint2(pack_bf16x2(kx.x, kx.y), pack_bf16x2(kx.z, kx.w));
+      vw = make_uint2(pack_bf16x2(vx.x, vx.y), pack_bf16x2(vx.z, vx.w));
+    }
+    const uint32_t off = sw_chunk(KR, j, c >> 3) + (c & 7) * 2;
+    *reinterpret_cast<uint2*>(kt + off) = kw;
+    *reinterpret_cast<uint2*>(vt + off) = vw;
+  }
+  __syncthreads();
+
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const uint32_t kb = smem_u32(kt), vb = smem_u32(vt), qb = smem_u32(qt), pb = smem_u32(pt);
+  // S = Q K^T
+  {
+    const int MT = QR / 16, NT = KR / 8, KS = dh / 16;
+    for (int t = warp; t < MT * NT; t += nw) {
+      const int mt = t / NT, nt = t % NT;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3, b0, b1;
+        ldsm_x4(qb + sw_chunk(QR, mt * 16 + (lane & 15), ks * 2 + (lane >> 4)), a0, a1, a2, a3);
+        ldsm_x2(kb + sw_chunk(KR, nt * 8 + (lane & 7), ks * 2 + ((lane >> 3) & 1)), b0, b1);
+        mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+      }
+      const int r = mt * 16 + g8, col = nt * 8 + 2 * t4;
+      s[r * SLD + col] = c[0];
+      s[r * SLD + col + 1] = c[1];
+      s[(r + 8) * SLD + col] = c[2];
+      s[(r + 8) * SLD + col + 1] = c[3];
+    }
+  }
+  __syncthreads();
+  // softmax rows -> P (bf16, keys >= nk and rows >= R zero), (max, sum) per row
+  for (int r = warp; r < QR; r += nw) {
+    float m = -INFINITY;
+    if (r < R)
+      for (int j = lane; j < nk; j += 32) m = fmaxf(m, s[r * SLD + j]);
+    m = warp_max(m);
+    float l = 0.f;
+    for (int j0p = 0; j0p < KR; j0p += 64) {
+      const int j = j0p + 2 * lane;  // two keys per lane per step
+      if (j < KR) {
+        float e0 = 0.f, e1 = 0.f;
+        if (r < R && j < nk) e0 = exp2f(s[r * SLD + j] - m);
+        if (r < R && j + 1 < nk) e1 = exp2f(s[r * SLD + j + 1] - m);
+        const uint32_t w = pack_bf16x2(e0, e1);
+        const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&w);
+        const float2 back = __bfloat1622float2(h2);
+        l += back.x + back.y;
+        *reinterpret_cast<uint32_t*>(pt + sw_chunk(QR, r, j >> 3) + (j & 7) * 2) = w;
+      }
+    }
+    l = warp_sum(l);
+    if (lane == 0) {
+      ml[r * 2 + 0] = m;
+      ml[r * 2 + 1] = l;
+    }
+  }
+  __syncthreads();
+  // O = P V
+  {
+    const int MT = QR / 16, NT = dh / 8, KS = KR / 16;
+    for (int t = warp; t < MT * NT; t += nw) {
+      const int mt = t / NT, nt = t % NT;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3, b0, b1;
+        ldsm_x4(pb + sw_chunk(QR, mt * 16 + (lane & 15), ks * 2 + (lane >> 4)), a0, a1, a2, a3);
+        ldsm_x2_t(vb + sw_chunk(KR, ks * 16 + (lane & 15), nt), b0, b1);
+        mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+      }
+      const int r = mt * 16 + g8, col = nt * 8 + 2 * t4;
+      o[r * OLD + col] = c[0];
+      o[r * OLD + col + 1] = c[1];
+      o[(r + 8) * OLD + col] = c[2];
+      o[(r + 8) * OLD + col + 1] = c[3];
+    }
+  }
+
+  __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
+  if (nsplit == 1) {
+    __syncthreads();
+    for (int i = tid; i < R * c4n; i += nthr) {
+      const int r = i / c4n, c = (i % c4n) * 4, g = r / S, sl = r % S;
+      const float inv = 1.f / ml[r * 2 + 1];
+      const float4 x = *reinterpret_cast<const float4*>(&o[r * OLD + c]);
+      __nv_bfloat16* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16x2(x.x * inv, x.y * inv), pack_bf16x2(x.z * inv, x.w * inv));
+    }
+    return;
+  }
+  cluster_sync_all();
+  const int my_rows = (R - rank + nsplit - 1) / nsplit;
+  for (int i = tid; i < my_rows * c4n; i += nthr) {
+    const int r = rank + (i / c4n) * nsplit, c = (i % c4n) * 4, g = r / S, sl = r % S;
+    float mp[MAX_SPLIT], lp[MAX_SPLIT];
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < MAX_SPLIT; ++sp) {
+      if (sp < nsplit) {
+        const uint32_t ad = peer_addr(&ml[r * 2], (uint32_t)sp);
+        mp[sp] = ld_peer_f(ad);
+        lp[sp] = ld_peer_f(ad + 4);
+        M = fmaxf(M, mp[sp]);
+      }
+    }
+    float Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sp = 0; sp < MAX_SPLIT; ++sp) {
+      if (sp < nsplit) {
+        const float wt = lp[sp] > 0.f ? exp2f(mp[sp] - M) : 0.f;
+        const float4 ov = ld_peer_f4(peer_addr(&o[r * OLD + c], (uint32_t)sp));
+        Lsum = fmaf(lp[sp], wt, Lsum);
+        acc.x = fmaf(wt, ov.x, acc.x);
+        acc.y = fmaf(wt, ov.y, acc.y);
+        acc.z = fmaf(wt, ov.z, acc.z);
+        acc.w = fmaf(wt, ov.w, acc.w);
+      }
+    }
+    const float inv = 1.f / Lsum;
+    __nv_bfloat16* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  }
+  cluster_sync_all();  // partners keep their shared memory until every read is done
+}
+
+__global__ void __launch_bounds__(THREADS)
+attn_tc_kernel(Args a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  pdl_trigger();
+  const int idx = blockIdx.x;
+  if (idx < a.n_attn)
+    attn_tc_cta(a, &mk, &mv, sm, idx);
+  else if (idx < a.n_attn + a.n_mem)
+    mem_cta<__nv_bfloat16>(a, sm, idx - a.n_attn);
+  else
+    pdl_wait();  // cluster padding
+}
+
 // E = head_dim / 16: the slice of a key each lane of a half-warp holds.
 template <typename T, int E>
 __global__ void __launch_bounds__(THREADS) attn_cluster_kernel(Args a) {
@@ -438,8 +737,17 @@ __global__ void __launch_bounds__(THREADS) attn_cluster_kernel(Args a) {
 
 }  // namespace
 
+bool attn_uses_tc(const Dims& d, int dtype) { return dtype == HF_BF16 && d.dh % 64 == 0; }
+
+int attn_tile_rows(const Dims& d) { return make_plan(d.W).jt; }
+
 size_t attn_cluster_smem(const Dims& d, int esize) {
-  return make_layout(d, make_plan(d.W), esize).total;
+  const size_t cuda_core = make_layout(d, make_plan(d.W), esize).total;
+  if (esize == 2 && d.dh % 64 == 0) {
+    const size_t tc = make_tc_layout(d, make_plan(d.W)).total;
+    return tc > cuda_core ? tc : cuda_core;
+  }
+  return cuda_core;
 }
 
 template <typename T, int E>
@@ -464,10 +772,17 @@ cudaError_t configure_dtype(int smem) {
 
 cudaError_t configure_attn_cluster(const Dims& d) {
   static int configured = 0;
-  const int smem = (int)attn_cluster_smem(d, 4);
+  int smem = (int)attn_cluster_smem(d, 4);
+  const int smem_bf16 = (int)attn_cluster_smem(d, 2);
+  if (smem_bf16 > smem) smem = smem_bf16;
   if (smem <= configured) return cudaSuccess;
   cudaError_t e = configure_dtype<float>(smem);
   if (e == cudaSuccess) e = configure_dtype<__nv_bfloat16>(smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) configured = smem;
   return e;
 }
@@ -485,7 +800,8 @@ cudaError_t launch_typed(const cudaLaunchConfig_t& cfg, const Args& a) {
 
 cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
-                                const float* state, void* mix, int32_t* err, cudaStream_t st,
+                                const float* state, void* mix, const CUtensorMap* mk,
+                                const CUtensorMap* mv, int32_t* err, cudaStream_t st,
                                 int* launches) {
   if (B <= 0) return cudaSuccess;
   Args a{};
@@ -506,7 +822,9 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(total);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = make_layout(d, a.plan, dtype == HF_F32 ? 4 : 2).total;
+  const bool tc = attn_uses_tc(d, dtype) && mk && mv;
+  cfg.dynamicSmemBytes = tc ? make_tc_layout(d, a.plan).total
+                            : make_layout(d, a.plan, dtype == HF_F32 ? 4 : 2).total;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -518,6 +836,7 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   ++*launches;
+  if (tc) return cudaLaunchKernelEx(&cfg, attn_tc_kernel, a, *mk, *mv);
   if (dtype == HF_F32) return launch_typed<float>(cfg, a);
   return launch_typed<__nv_bfloat16>(cfg, a);
 }

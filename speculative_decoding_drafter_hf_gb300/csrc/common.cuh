@@ -2,6 +2,7 @@
 // runtime (hyflash.cu) and the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -113,6 +114,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 2-D tiled TMA load (tensor map in param/const/global space) completing on bar.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Device error word bits.
 enum : int32_t { ERR_BAD_ACCEPTED = 1, ERR_TIMEOUT = 2 };
 
@@ -208,6 +219,11 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
                            cudaStream_t st, int* launches);
 int tc_pick_splits(int M, int N, int K);
 
+// 2-D bf16 tensor map over rows x K (row stride ld elements), box 64 x
+// box_rows, 128-byte swizzle (gemm_tc.cu).
+cudaError_t make_map(CUtensorMap* map, const void* base, long long rows, long long K, long long ld,
+                     int box_rows);
+
 // One-time kernel attribute set-up (dynamic shared memory limits, driver
 // entry points, cluster occupancy), done at handle creation.
 cudaError_t configure_tc();
@@ -216,10 +232,16 @@ cudaError_t configure_attn_cluster(const Dims& d);
 // Window+block attention and memory read for one layer, batch B, one launch
 // (attention_cluster.cu). proj [B*S, Nd] fp32 (Q|K_s|V_s|C_s); ring_k/v and
 // state of this layer; pos [Bmax]; mix [B*S, Nz] model dtype (O | y).
+// bf16 handles with head_dim % 64 == 0 run the tensor-core variant, which
+// loads ring tiles through the per-layer tensor maps mk / mv (rows =
+// Bmax*Hkv*W, box attn_tile_rows(d) rows); other handles pass NULL maps.
 size_t attn_cluster_smem(const Dims& d, int esize);
+int attn_tile_rows(const Dims& d);
+bool attn_uses_tc(const Dims& d, int dtype);
 cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
-                                const float* state, void* mix, int32_t* err, cudaStream_t st,
+                                const float* state, void* mix, const CUtensorMap* mk,
+                                const CUtensorMap* mv, int32_t* err, cudaStream_t st,
                                 int* launches);
 
 // Commit prep: validate counts, offsets, row map, tags, gather rows.

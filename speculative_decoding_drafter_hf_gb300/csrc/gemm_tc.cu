@@ -30,15 +30,6 @@
 namespace hf {
 namespace {
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
@@ -333,7 +324,10 @@ cudaError_t get_encoder() {
   return g_encode_err;
 }
 
-// 2-D bf16 tensor map over rows x K (row stride ld elements), box 64 x box_rows.
+}  // namespace
+
+// 2-D bf16 tensor map over rows x K (row stride ld elements), box 64 x box_rows,
+// 128-byte swizzle.
 cudaError_t make_map(CUtensorMap* map, const void* base, long long rows, long long K, long long ld,
                      int box_rows) {
   cudaError_t e = get_encoder();
@@ -348,6 +342,8 @@ cudaError_t make_map(CUtensorMap* map, const void* base, long long rows, long lo
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+namespace {
 
 template <int BN, int STAGES>
 constexpr size_t tc_smem() {
@@ -392,15 +388,33 @@ cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES>, ma, mb, a, epi);
 }
 
-// How many clusters of cz CTAs of this instantiation are resident at once.
+// Resource twin of tc_gemm_kernel for cluster occupancy queries: same block
+// size, launch bounds and dynamic shared memory, no tensor-memory use (the
+// occupancy query on the tcgen05 kernel itself reports one CTA per SM, while
+// two fit by shared memory and run concurrently).
+__global__ void __launch_bounds__(128, 1) tc_occupancy_twin() {}
+
 template <int BN, int STAGES>
 int max_clusters(int cz) {
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = tc_config<BN, STAGES>(dim3(cz, 1, 1), cz, nullptr, attr);
-  cfg.attrs = attr + 1;  // occupancy query: cluster shape only
+  const int smem = (int)tc_smem<BN, STAGES>();
+  if (cudaFuncSetAttribute(tc_occupancy_twin, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cz, 1, 1);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cz;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, STAGES>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_occupancy_twin, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }

@@ -53,6 +53,7 @@ struct hf_handle {
   void* xbuf[2] = {nullptr, nullptr};
   float* part = nullptr;
   size_t part_elems = 0;
+  std::vector<CUtensorMap> ring_maps;  // per layer: K, V tile maps (tensor-core attention)
   int* counters = nullptr;     // split-K tickets of the tensor-core GEMM
   int n_counters = 0;
   int num_sms = 152;
@@ -392,6 +393,20 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     e = cudaMemset(h->tags, 0xff, Bm * d.W * 4);
     if (e != cudaSuccess) s = cuda_fail(h, e, "cudaMemset(tags)");
   }
+  if (s == HF_OK && hf::attn_uses_tc(d, h->cfg.dtype)) {
+    // 2-D maps over each layer's rings: rows = Bmax*Hkv*W, box = one attention tile
+    h->ring_maps.resize(2 * L);
+    const size_t layer_bytes = Bm * d.Hkv * d.W * d.dh * es;
+    const long long rows = (long long)Bm * d.Hkv * d.W;
+    for (size_t l = 0; l < L && s == HF_OK; ++l) {
+      e = hf::make_map(&h->ring_maps[2 * l], bptr(h->ring_k, l * layer_bytes), rows, d.dh, d.dh,
+                       hf::attn_tile_rows(d));
+      if (e == cudaSuccess)
+        e = hf::make_map(&h->ring_maps[2 * l + 1], bptr(h->ring_v, l * layer_bytes), rows, d.dh,
+                         d.dh, hf::attn_tile_rows(d));
+      if (e != cudaSuccess) s = cuda_fail(h, e, "ring tensor maps");
+    }
+  }
   if (s == HF_OK) {
     e = hf::configure_attn_cluster(h->d);
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc();
@@ -493,10 +508,12 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
     if (s != HF_OK) return s;
     {
       Scope sc(h, HF_K_ATTN_MEM, st);
+      const CUtensorMap* mk = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l];
+      const CUtensorMap* mv = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l + 1];
       cudaError_t e = hf::launch_attn_cluster(h->cfg.dtype, d, batch, h->proj,
                                               bptr(h->ring_k, l * ring_ls),
                                               bptr(h->ring_v, l * ring_ls), h->pos,
-                                              h->state + l * state_ls, h->mix, h->err, st,
+                                              h->state + l * state_ls, h->mix, mk, mv, h->err, st,
                                               &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
     }
