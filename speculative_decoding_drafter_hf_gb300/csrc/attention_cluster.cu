@@ -380,6 +380,22 @@ __device__ __forceinline__ void attn_cta(const Args& a, uint8_t* sm, int idx) {
   cluster_sync_all();  // partners keep their shared memory until every read is done
 }
 
+// Sum over the 32 lanes of each of 32 values: after the butterfly each lane
+// l holds the total of value l (31 shuffles instead of 32 x 5).
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool upper = (lane & half) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+    }
+  }
+  return v[0];
+}
+
 template <typename T>
 __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
   const Dims& d = a.d;
@@ -387,8 +403,42 @@ __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
   const int S = d.S, N = d.N, P = d.P;
   float* cs = reinterpret_cast<float*>(sm);
   const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid / 32, lane = tid % 32, nw = nthr / 32;
   pdl_wait();
-  const float4* h = reinterpret_cast<const float4*>(a.state + (((size_t)b * d.Hm + hd) * P) * N);
+  const float* hb = a.state + (((size_t)b * d.Hm + hd) * P) * N;
+  T* mix = static_cast<T*>(a.mix);
+  const int cC = d.QD + 2 * d.KVD;
+  if (N == 128 && S <= 8) {
+    // lane l owns state columns 4l..4l+3; a warp takes 4 state rows at a time
+    // and all slots: 4 x 8 partial dots per lane, one reduce-scatter.
+    float4 c4[8];
+#pragma unroll
+    for (int sl = 0; sl < 8; ++sl)
+      c4[sl] = sl < S ? __ldcg(reinterpret_cast<const float4*>(
+                            a.proj + ((size_t)b * S + sl) * d.Nd + cC + 4 * lane))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = warp * 4; p0 < P; p0 += nw * 4) {
+      float4 hv[4];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr)
+        hv[rr] = p0 + rr < P ? __ldcg(reinterpret_cast<const float4*>(hb + (size_t)(p0 + rr) * N) + lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      float v[32];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+        for (int sl = 0; sl < 8; ++sl)
+          v[rr * 8 + sl] = hv[rr].x * c4[sl].x + hv[rr].y * c4[sl].y + hv[rr].z * c4[sl].z +
+                           hv[rr].w * c4[sl].w;
+      const float tot = reduce_scatter32(v, lane);
+      const int rr = lane / 8, sl = lane % 8, pr = p0 + rr;
+      if (sl < S && pr < P)
+        mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)hd * P + pr] = from_f<T>(tot);
+    }
+    return;
+  }
+  // general shapes: flat float4 walk, reduction across the lanes of a row
+  const float4* h = reinterpret_cast<const float4*>(hb);
   const int nq = P * N / 4;
   float4 hv[MEM_QPT];
 #pragma unroll
@@ -396,7 +446,6 @@ __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
     const int qi = tid + u * nthr;
     hv[u] = qi < nq ? __ldcg(&h[qi]) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  const int cC = d.QD + 2 * d.KVD;
   for (int i = tid; i < S * N / 4; i += nthr) {
     const int sl = (i * 4) / N, n = (i * 4) % N;
     *reinterpret_cast<float4*>(&cs[sl * N + n]) =
@@ -404,7 +453,6 @@ __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
   }
   __syncthreads();
   const int gsz = N / 4;  // lanes sharing one state row (power of two <= 32)
-  T* mix = static_cast<T*>(a.mix);
 #pragma unroll
   for (int u = 0; u < MEM_QPT; ++u) {
     if (u * nthr >= nq) break;  // uniform across the CTA

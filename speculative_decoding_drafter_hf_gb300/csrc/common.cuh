@@ -158,6 +158,7 @@ struct Epi {
   // [K | V | x | B | dt] block. K/V go to the ring slot of the row's
   // committed position; x, B and softplus(dt + bias) go to xbd (fp32).
   int layer0, cols_per_layer, col_off;
+  int cols_valid;           // > 0: per-layer columns at or past this are padding (skipped)
   const int32_t* row_req;   // request of each packed row
   const int64_t* row_pos;   // committed position of each packed row
   const int32_t* n_rows;    // device count of valid rows (NULL: all)
@@ -182,6 +183,7 @@ __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
     const Dims& d = e.d;
     int layer = e.layer0 + c / e.cols_per_layer;
     int cl = c % e.cols_per_layer + e.col_off;
+    if (e.cols_valid > 0 && cl >= e.cols_valid) return;
     if (cl < 2 * d.KVD) {
       int which = cl >= d.KVD;
       int cc = cl - which * d.KVD;
@@ -214,9 +216,12 @@ cudaError_t launch_gemm_fma(int dtype, const void* X, int ldx, const void* Wt, i
 // swap = 1 the epilogue sees (row n, column m), else (row m, column n).
 // Split-K partner CTAs (splits <= 8) form a thread-block cluster and sum
 // their partial tiles through distributed shared memory.
+// a_tiles (optional): A pre-tiled by tile_weights, read with bulk copies.
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb,
                            int N, int K, int swap, int splits, int32_t* err, const Epi& epi,
-                           cudaStream_t st, int* launches);
+                           cudaStream_t st, int* launches, const void* a_tiles = nullptr);
+void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst);
+size_t tiled_bytes(long long M, long long K);
 int tc_pick_splits(int M, int N, int K);
 
 // 2-D bf16 tensor map over rows x K (row stride ld elements), box 64 x

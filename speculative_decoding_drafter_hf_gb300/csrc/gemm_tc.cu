@@ -113,6 +113,9 @@ struct TcArgs {
   int swap;           // 1: output row = n, column = m; 0: row = m, column = n
   int prefetch_a;     // 1: A does not depend on earlier kernels (weights): load it
                       //    before waiting on the previous kernel
+  const uint8_t* a_tiles;  // non-NULL: A stored pre-tiled (see tile_weights); each
+                           // (m_tile, k_block) is one 16 KB swizzled tile, read by
+                           // one bulk copy; NULL: A read through the tensor map
   int32_t* err;       // device error word
 };
 
@@ -169,10 +172,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     // prefetch_a the A tiles (weights) are requested before waiting for the
     // previous kernel, so their HBM read overlaps that kernel's tail.
     const int pre = nkb < STAGES ? nkb : STAGES;
+    // A tile of local k-block i into stage st
+    auto load_a = [&](int st, int i) {
+      if (a.a_tiles)
+        bulk_g2s(sA + st * A_BYTES,
+                 a.a_tiles + ((size_t)m_tile * a.kblocks + (kb0 + i)) * (size_t)A_BYTES, A_BYTES,
+                 &full[st]);
+      else
+        tma_load_2d(sA + st * A_BYTES, &ta, &full[st], (kb0 + i) * 64, m_tile * 128);
+    };
     if (a.prefetch_a) {
       for (int j = 0; j < pre; ++j) {
         mbar_expect_tx(&full[j], STAGE_BYTES);
-        tma_load_2d(sA + j * A_BYTES, &ta, &full[j], (kb0 + j) * 64, m_tile * 128);
+        load_a(j, j);
       }
       pdl_wait();
       for (int j = 0; j < pre; ++j)
@@ -181,7 +193,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       pdl_wait();
       for (int j = 0; j < pre; ++j) {
         mbar_expect_tx(&full[j], STAGE_BYTES);
-        tma_load_2d(sA + j * A_BYTES, &ta, &full[j], (kb0 + j) * 64, m_tile * 128);
+        load_a(j, j);
         tma_load_2d(sB + j * B_BYTES, &tb, &full[j], (kb0 + j) * 64, n_tile * BN);
       }
     }
@@ -195,7 +207,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       }
       if (*(volatile int*)&flags[0]) break;
       mbar_expect_tx(&full[s], STAGE_BYTES);
-      tma_load_2d(sA + s * A_BYTES, &ta, &full[s], (kb0 + i) * 64, m_tile * 128);
+      load_a(s, i);
       tma_load_2d(sB + s * B_BYTES, &tb, &full[s], (kb0 + i) * 64, n_tile * BN);
     }
     flags[1] = i;
@@ -388,33 +400,16 @@ cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs
   return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES>, ma, mb, a, epi);
 }
 
-// Resource twin of tc_gemm_kernel for cluster occupancy queries: same block
-// size, launch bounds and dynamic shared memory, no tensor-memory use (the
-// occupancy query on the tcgen05 kernel itself reports one CTA per SM, while
-// two fit by shared memory and run concurrently).
-__global__ void __launch_bounds__(128, 1) tc_occupancy_twin() {}
-
+// How many clusters of cz CTAs of this instantiation are resident at once
+// (the driver's answer for the tcgen05 kernel itself: one CTA per SM).
 template <int BN, int STAGES>
 int max_clusters(int cz) {
-  const int smem = (int)tc_smem<BN, STAGES>();
-  if (cudaFuncSetAttribute(tc_occupancy_twin, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cz, 1, 1);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cz;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = tc_config<BN, STAGES>(dim3(cz, 1, 1), cz, nullptr, attr);
+  cfg.attrs = attr + 1;  // occupancy query: cluster shape only
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_occupancy_twin, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, STAGES>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -429,14 +424,14 @@ int g_max_clusters[5][9] = {};  // [log2(BN/16)][cz]
 // that launches stay legal inside stream capture.
 cudaError_t configure_tc() {
   cudaError_t e = get_encoder();
-  if (e == cudaSuccess) e = configure_one<16, 6>();
+  if (e == cudaSuccess) e = configure_one<16, 7>();
   if (e == cudaSuccess) e = configure_one<32, 6>();
   if (e == cudaSuccess) e = configure_one<64, 5>();
   if (e == cudaSuccess) e = configure_one<128, 4>();
   if (e == cudaSuccess) e = configure_one<256, 4>();
   if (e != cudaSuccess) return e;
   for (int cz = 1; cz <= 8; ++cz) {
-    g_max_clusters[0][cz] = max_clusters<16, 6>(cz);
+    g_max_clusters[0][cz] = max_clusters<16, 7>(cz);
     g_max_clusters[1][cz] = max_clusters<32, 6>(cz);
     g_max_clusters[2][cz] = max_clusters<64, 5>(cz);
     g_max_clusters[3][cz] = max_clusters<128, 4>(cz);
@@ -464,7 +459,7 @@ int tc_pick_splits(int M, int N, int K) {
 
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb, int N,
                            int K, int swap, int splits, int32_t* err, const Epi& epi,
-                           cudaStream_t st, int* launches) {
+                           cudaStream_t st, int* launches, const void* a_tiles) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   int bn = 16;
   while (bn < N && bn < 256) bn *= 2;
@@ -479,21 +474,47 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   a.prefetch_a = swap;
   a.err = err;
   a.splits = std::max(1, std::min(std::min(splits, 8), a.kblocks));
+  a.a_tiles = static_cast<const uint8_t*>(a_tiles);
   CUtensorMap ma, mb;
-  cudaError_t e = make_map(&ma, A, M, K, lda, 128);
+  cudaError_t e = make_map(&mb, B, N, K, ldb, bn);
   if (e != cudaSuccess) return e;
-  e = make_map(&mb, B, N, K, ldb, bn);
-  if (e != cudaSuccess) return e;
+  if (a_tiles)
+    ma = mb;  // unused by the kernel
+  else if ((e = make_map(&ma, A, M, K, lda, 128)) != cudaSuccess)
+    return e;
   if (m_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
   dim3 grid(a.splits, m_tiles, n_tiles);
   ++*launches;
   switch (bn) {
-    case 16: return launch_tc<16, 6>(ma, mb, a, epi, grid, st);
+    case 16: return launch_tc<16, 7>(ma, mb, a, epi, grid, st);
     case 32: return launch_tc<32, 6>(ma, mb, a, epi, grid, st);
     case 64: return launch_tc<64, 5>(ma, mb, a, epi, grid, st);
     case 128: return launch_tc<128, 4>(ma, mb, a, epi, grid, st);
     default: return launch_tc<256, 4>(ma, mb, a, epi, grid, st);
   }
+}
+
+// Re-lay a row-major bf16 matrix [M][K] (host) as 128 x 64 tiles in the
+// shared-memory image the kernel's tensor-core descriptors expect (rows of
+// 128 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7)), ordered
+// [m_tile][k_block]; rows past M and columns past K are zero. Each CTA then
+// streams a contiguous run of its m-tile's k-blocks.
+void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst) {
+  const long long mt = (M + 127) / 128, kb = (K + 63) / 64;
+  for (long long t = 0; t < mt; ++t)
+    for (long long b = 0; b < kb; ++b) {
+      uint16_t* tile = dst + (t * kb + b) * 128 * 64;
+      for (int r = 0; r < 128; ++r)
+        for (int c = 0; c < 64; ++c) {
+          const long long gr = t * 128 + r, gc = b * 64 + c;
+          const uint16_t v = (gr < M && gc < K) ? src[gr * K + gc] : 0;
+          tile[r * 64 + ((((c >> 3) ^ (r & 7))) << 3) + (c & 7)] = v;
+        }
+    }
+}
+
+size_t tiled_bytes(long long M, long long K) {
+  return (size_t)((M + 127) / 128) * ((K + 63) / 64) * 128 * 64 * 2;
 }
 
 }  // namespace hf

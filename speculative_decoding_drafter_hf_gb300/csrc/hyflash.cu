@@ -31,6 +31,13 @@ struct hf_handle {
   void* w_draft = nullptr;   // [L][Nd][D]
   void* w_commit = nullptr;  // [L][Nc][D]
   void* w_out = nullptr;     // [L][D][Nz]
+  // bf16: the same three weights pre-tiled for the tensor-core GEMM
+  // (tile_weights; commit weights padded per layer to a multiple of 128 rows)
+  void* wt_draft = nullptr;
+  void* wt_commit = nullptr;
+  void* wt_out = nullptr;
+  size_t wt_draft_l = 0, wt_commit_l = 0, wt_out_l = 0;  // bytes per layer
+  int nc_pad = 0;                                         // padded commit rows per layer
   float* dt_bias = nullptr;  // [L][Hm]
   float* A_log = nullptr;    // [L][Hm]
 
@@ -268,7 +275,8 @@ int pick_splits(const hf_handle* h, long long R, long long C, long long K, int t
 // CUDA-core kernel; bf16 handles use the tensor-core kernel with the weights
 // as the 128-row operand (they stream once) and the activation rows as N.
 cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, int ldw, int R,
-                        int C, int K, const Epi& epi, cudaStream_t st, int* count) {
+                        int C, int K, const Epi& epi, cudaStream_t st, int* count,
+                        const void* tiles = nullptr) {
   if (R <= 0 || C <= 0) return cudaSuccess;
   if (h->cfg.dtype == HF_F32) {
     int splits = pick_splits(h, R, C, K, 64, 64);
@@ -276,14 +284,14 @@ cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, in
                                count);
   }
   const int splits = hf::tc_pick_splits(C, R, K);
-  return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->err, epi, st, count);
+  return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->err, epi, st, count, tiles);
 }
 
 hf_status gemm(hf_handle* h, int fam, const void* X, int ldx, const void* Wt, int ldw, int R,
-               int C, int K, const Epi& epi, cudaStream_t st) {
+               int C, int K, const Epi& epi, cudaStream_t st, const void* tiles = nullptr) {
   if (R <= 0 || C <= 0) return HF_OK;
   Scope sc(h, fam, st);
-  cudaError_t e = gemm_launch(h, X, ldx, Wt, ldw, R, C, K, epi, st, &sc.count);
+  cudaError_t e = gemm_launch(h, X, ldx, Wt, ldw, R, C, K, epi, st, &sc.count, tiles);
   if (e != cudaSuccess) return cuda_fail(h, e, "gemm launch");
   return HF_OK;
 }
@@ -360,6 +368,15 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   A(&h->w_draft, L * d.Nd * d.D * es);
   A(&h->w_commit, L * d.Nc * d.D * es);
   A(&h->w_out, L * d.D * d.Nz * es);
+  if (h->cfg.dtype == HF_BF16) {
+    h->nc_pad = (d.Nc + 127) / 128 * 128;
+    h->wt_draft_l = hf::tiled_bytes(d.Nd, d.D);
+    h->wt_commit_l = hf::tiled_bytes(h->nc_pad, d.D);
+    h->wt_out_l = hf::tiled_bytes(d.D, d.Nz);
+    A(&h->wt_draft, L * h->wt_draft_l);
+    A(&h->wt_commit, L * h->wt_commit_l);
+    A(&h->wt_out, L * h->wt_out_l);
+  }
   A((void**)&h->dt_bias, L * d.Hm * 4);
   A((void**)&h->A_log, L * d.Hm * 4);
   A(&h->ring_k, L * Bm * d.Hkv * d.W * d.dh * es);
@@ -475,6 +492,18 @@ hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w)
   HF_CUDA(h, cudaMemcpy(bptr(h->w_draft, (size_t)layer * wd.size()), wd.data(), wd.size(), cudaMemcpyHostToDevice));
   HF_CUDA(h, cudaMemcpy(bptr(h->w_commit, (size_t)layer * wc.size()), wc.data(), wc.size(), cudaMemcpyHostToDevice));
   HF_CUDA(h, cudaMemcpy(bptr(h->w_out, (size_t)layer * wo.size()), wo.data(), wo.size(), cudaMemcpyHostToDevice));
+  if (h->cfg.dtype == HF_BF16) {
+    std::vector<uint16_t> t(std::max({h->wt_draft_l, h->wt_commit_l, h->wt_out_l}) / 2);
+    hf::tile_weights(reinterpret_cast<const uint16_t*>(wd.data()), d.Nd, D, t.data());
+    HF_CUDA(h, cudaMemcpy(bptr(h->wt_draft, (size_t)layer * h->wt_draft_l), t.data(), h->wt_draft_l,
+                          cudaMemcpyHostToDevice));
+    hf::tile_weights(reinterpret_cast<const uint16_t*>(wc.data()), d.Nc, D, t.data());
+    HF_CUDA(h, cudaMemcpy(bptr(h->wt_commit, (size_t)layer * h->wt_commit_l), t.data(),
+                          h->wt_commit_l, cudaMemcpyHostToDevice));
+    hf::tile_weights(reinterpret_cast<const uint16_t*>(wo.data()), D, d.Nz, t.data());
+    HF_CUDA(h, cudaMemcpy(bptr(h->wt_out, (size_t)layer * h->wt_out_l), t.data(), h->wt_out_l,
+                          cudaMemcpyHostToDevice));
+  }
   HF_CUDA(h, cudaMemcpy(h->dt_bias + (size_t)layer * d.Hm, w->dt_bias, d.Hm * 4, cudaMemcpyHostToDevice));
   HF_CUDA(h, cudaMemcpy(h->A_log + (size_t)layer * d.Hm, w->A_log, d.Hm * 4, cudaMemcpyHostToDevice));
   HF_CUDA(h, cudaDeviceSynchronize());
@@ -504,7 +533,8 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
     e1.out = h->proj;
     e1.ld = d.Nd;
     hf_status s = gemm(h, HF_K_DRAFT_PROJ, X, d.D, bptr(h->w_draft, (size_t)l * d.Nd * d.D * es),
-                       d.D, R, d.Nd, d.D, e1, st);
+                       d.D, R, d.Nd, d.D, e1, st,
+                       h->wt_draft ? bptr(h->wt_draft, (size_t)l * h->wt_draft_l) : nullptr);
     if (s != HF_OK) return s;
     {
       Scope sc(h, HF_K_ATTN_MEM, st);
@@ -523,7 +553,7 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
     e2.out_t = Y;
     e2.ld = d.D;
     s = gemm(h, HF_K_OUT_PROJ, h->mix, d.Nz, bptr(h->w_out, (size_t)l * d.D * d.Nz * es), d.Nz, R,
-             d.D, d.Nz, e2, st);
+             d.D, d.Nz, e2, st, h->wt_out ? bptr(h->wt_out, (size_t)l * h->wt_out_l) : nullptr);
     if (s != HF_OK) return s;
   }
   return HF_OK;
@@ -557,8 +587,16 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, 
   ep.n_rows = h->offsets + batch;
   ep.xbd = h->xbd;
   ep.xbd_layer_stride = h->xbd_ls;
-  hf_status s = gemm(h, HF_K_COMMIT_PROJ, h->packed, d.D, h->w_commit, d.D, batch * (d.S + 1),
-                     d.L * d.Nc, d.D, ep, st);
+  hf_status s;
+  if (h->wt_commit) {  // pre-tiled: rows padded per layer to nc_pad, padding skipped
+    ep.cols_per_layer = h->nc_pad;
+    ep.cols_valid = d.Nc;
+    s = gemm(h, HF_K_COMMIT_PROJ, h->packed, d.D, h->w_commit, d.D, batch * (d.S + 1),
+             d.L * h->nc_pad, d.D, ep, st, h->wt_commit);
+  } else {
+    s = gemm(h, HF_K_COMMIT_PROJ, h->packed, d.D, h->w_commit, d.D, batch * (d.S + 1), d.L * d.Nc,
+             d.D, ep, st);
+  }
   if (s != HF_OK) return s;
   {
     Scope sc(h, HF_K_COMMIT_STATE, st);
