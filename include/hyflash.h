@@ -140,8 +140,9 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens,
 /* Commit one verification round for requests 0..batch-1. feats: DEVICE
  * [batch, block+1, D]; n_accepted: DEVICE int32 [batch]. For request b the
  * rows t < n_b are appended in order (ring slot (pos_b + t) mod W, memory
- * update token by token) and pos_b += n_b. Rows t >= n_b are never read.
- * n_b = 0 is a no-op. n_b outside 0..block+1 leaves request b untouched and
+ * update token by token) and pos_b += n_b. Rows t >= n_b (the rejected
+ * drafts) pass through the batched projection but are discarded: they never
+ * reach the window, the memory or the positions. n_b = 0 is a no-op. n_b outside 0..block+1 leaves request b untouched and
  * raises HF_EDEVICE at the next hf_sync. Packed row offsets (exclusive scan
  * of the valid counts) are kept for inspection (HF_T_OFFSETS). */
 hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted,

@@ -159,9 +159,16 @@ struct Epi {
   // committed position; x, B and softplus(dt + bias) go to xbd (fp32).
   int layer0, cols_per_layer, col_off;
   int cols_valid;           // > 0: per-layer columns at or past this are padding (skipped)
-  const int32_t* row_req;   // request of each packed row
-  const int64_t* row_pos;   // committed position of each packed row
-  const int32_t* n_rows;    // device count of valid rows (NULL: all)
+  // Row source of EPI_SSM_KV (one of):
+  //  * commit rows (n_acc != NULL): row r = b*(S+1) + t of the caller's
+  //    [B, S+1, D] features; valid iff 0 <= n_acc[b] <= S+1 and t < n_acc[b];
+  //    committed position pos[b] + t (pos before this commit);
+  //  * mapped rows (row_req != NULL): request and position per packed row;
+  //  * neither: every row valid, no ring columns (x/B/dt of prefill tokens).
+  const int32_t* n_acc;
+  const int64_t* pos;
+  const int32_t* row_req;
+  const int64_t* row_pos;
   void* ring_k;
   void* ring_v;
   float* xbd;
@@ -169,6 +176,45 @@ struct Epi {
   const float* dt_bias;        // [L][Hm]
   Dims d;
 };
+
+// Request and committed position of an EPI_SSM_KV row; position < 0: skip.
+__device__ __forceinline__ void epi_row(const Epi& e, int r, int& b, long long& p) {
+  if (e.n_acc) {
+    const int lim = e.d.S + 1;
+    b = r / lim;
+    const int t = r % lim;
+    const int n = __ldcg(&e.n_acc[b]);
+    p = (n >= 0 && n <= lim && t < n) ? __ldcg(&e.pos[b]) + t : -1;
+  } else if (e.row_req) {
+    b = __ldcg(&e.row_req[r]);
+    p = __ldcg(&e.row_pos[r]);
+  } else {
+    b = 0;
+    p = 0;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void epi_ssm(const Epi& e, int r, int c, float v, int b, long long p) {
+  if (p < 0) return;
+  const Dims& d = e.d;
+  const int layer = e.layer0 + c / e.cols_per_layer;
+  const int cl = c % e.cols_per_layer + e.col_off;
+  if (e.cols_valid > 0 && cl >= e.cols_valid) return;
+  if (cl < 2 * d.KVD) {
+    const int which = cl >= d.KVD;
+    const int cc = cl - which * d.KVD;
+    const int kvh = cc / d.dh, dd = cc % d.dh;
+    const int slot = (int)(p % d.W);
+    const size_t idx = ((((size_t)layer * d.Bmax + b) * d.Hkv + kvh) * d.W + slot) * d.dh + dd;
+    ((T*)(which ? e.ring_v : e.ring_k))[idx] = from_f<T>(v);
+  } else {
+    const int j = cl - 2 * d.KVD;
+    float o = v;
+    if (j >= d.dinner + d.N) o = softplus_f(v + __ldg(&e.dt_bias[layer * d.Hm + (j - d.dinner - d.N)]));
+    e.xbd[(size_t)layer * e.xbd_layer_stride + (size_t)r * d.NS + j] = o;
+  }
+}
 
 template <typename T>
 __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
@@ -179,25 +225,10 @@ __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
     float x = to_f(__ldcg(&((const T*)e.resid)[i]));
     ((T*)e.out_t)[i] = from_f<T>(x + v);
   } else {
-    if (e.n_rows && r >= __ldcg(e.n_rows)) return;
-    const Dims& d = e.d;
-    int layer = e.layer0 + c / e.cols_per_layer;
-    int cl = c % e.cols_per_layer + e.col_off;
-    if (e.cols_valid > 0 && cl >= e.cols_valid) return;
-    if (cl < 2 * d.KVD) {
-      int which = cl >= d.KVD;
-      int cc = cl - which * d.KVD;
-      int kvh = cc / d.dh, dd = cc % d.dh;
-      int b = __ldcg(&e.row_req[r]);
-      int slot = (int)(__ldcg(&e.row_pos[r]) % d.W);
-      size_t idx = ((((size_t)layer * d.Bmax + b) * d.Hkv + kvh) * d.W + slot) * d.dh + dd;
-      ((T*)(which ? e.ring_v : e.ring_k))[idx] = from_f<T>(v);
-    } else {
-      int j = cl - 2 * d.KVD;
-      float o = v;
-      if (j >= d.dinner + d.N) o = softplus_f(v + e.dt_bias[layer * d.Hm + (j - d.dinner - d.N)]);
-      e.xbd[(size_t)layer * e.xbd_layer_stride + (size_t)r * d.NS + j] = o;
-    }
+    int b;
+    long long p;
+    epi_row(e, r, b, p);
+    epi_ssm<T>(e, r, c, v, b, p);
   }
 }
 
@@ -249,16 +280,13 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
                                 const CUtensorMap* mv, int32_t* err, cudaStream_t st,
                                 int* launches);
 
-// Commit prep: validate counts, offsets, row map, tags, gather rows.
-cudaError_t launch_commit_prep(int dtype, const Dims& d, int B, const void* feats,
-                               const int32_t* n_acc, const int64_t* pos, int32_t* offsets,
-                               int32_t* row_req, int64_t* row_pos, int32_t* tags,
-                               void* packed, int32_t* err, cudaStream_t st);
-
-// Sequential memory update over the accepted rows, all layers; pos += n.
-cudaError_t launch_commit_state(const Dims& d, int B, const int32_t* offsets,
-                                const float* xbd, long long xbd_layer_stride,
-                                const float* A_log, float* state, int64_t* pos,
+// Commit state step, all layers: validates the accepted counts (error word),
+// writes the packed offsets (exclusive scan of the valid counts) and the ring
+// tags of the appended positions, advances the memory over rows
+// b*(S+1) + t < b*(S+1) + n_b of xbd in order, then pos += n.
+cudaError_t launch_commit_state(const Dims& d, int B, const int32_t* n_acc, const float* xbd,
+                                long long xbd_layer_stride, const float* A_log, float* state,
+                                int64_t* pos, int32_t* offsets, int32_t* tags, int32_t* err,
                                 cudaStream_t st);
 
 // Prefill helpers (lens/reqs/cu are device int32 arrays of n_req entries).

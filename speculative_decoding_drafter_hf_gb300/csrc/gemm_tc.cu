@@ -119,6 +119,16 @@ struct TcArgs {
   int32_t* err;       // device error word
 };
 
+// Epilogue cache (shared memory after the barriers): per output row of the
+// tile its request and committed position (ring rows), and for small tiles
+// the residual inputs; filled during the main loop by the otherwise idle
+// warps 2-3, so the epilogue issues no dependent global loads.
+template <int BN>
+struct EpiCache {
+  static constexpr int RES_ROWS = BN <= 32 ? BN : 0;
+  static constexpr size_t bytes = BN * 8 + BN * 4 + RES_ROWS * 128 * 4;
+};
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(128, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
@@ -127,6 +137,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   constexpr int B_BYTES = BN * 128;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t NCOLS = BN < 32 ? 32 : BN;
+  constexpr int RES_ROWS = EpiCache<BN>::RES_ROWS;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -138,6 +149,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   uint64_t* done = empty + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] issued, [2] consumed, [3] last
+  // epilogue cache after the 32 bytes of TMEM slot and flags (8-byte aligned)
+  long long* ep_p = reinterpret_cast<long long*>(reinterpret_cast<uint8_t*>(done) + 8 + 32);
+  int* ep_b = reinterpret_cast<int*>(ep_p + BN);
+  float* ep_res = reinterpret_cast<float*>(ep_b + BN);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   // grid (splits, m_tiles, n_tiles); the splits of one tile form a cluster along x
@@ -235,6 +250,25 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   }
   __syncwarp();
   pdl_wait();  // the epilogue writes memory earlier kernels may still read
+  const int n_here = min(BN, a.N - n_tile * BN);
+  if (warp >= 2 && a.swap) {  // idle during the main loop: fetch the epilogue inputs
+    const int t2 = tid - 64;
+    if (epi.kind == EPI_SSM_KV) {
+      for (int nl = t2; nl < n_here; nl += 64) {
+        int bq;
+        long long pq;
+        epi_row(epi, n_tile * BN + nl, bq, pq);
+        ep_b[nl] = bq;
+        ep_p[nl] = pq;
+      }
+    } else if (epi.kind == EPI_RESID && RES_ROWS > 0) {
+      const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(epi.resid);
+      for (int i = t2; i < n_here * 128; i += 64) {
+        const int nl = i >> 7, mq = m_tile * 128 + (i & 127);
+        ep_res[i] = mq < a.M ? to_f(__ldcg(&res[(size_t)(n_tile * BN + nl) * epi.ld + mq])) : 0.f;
+      }
+    }
+  }
 
   const bool ok = mbar_wait(done, 0);
   if (__syncthreads_or(!ok || flags[0])) {
@@ -260,21 +294,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const int m = m_tile * 128 + m_local;
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
   float v[16];
+  // Output of tile row nl (activation row n) and this thread's column m.
+  auto emit = [&](int nl, float val) {
+    const int n = n_tile * BN + nl;
+    if (!a.swap) {
+      epi_apply<__nv_bfloat16>(epi, m, n, val);
+    } else if (epi.kind == EPI_F32) {
+      epi.out[(size_t)n * epi.ld + m] = val;
+    } else if (epi.kind == EPI_RESID) {
+      const size_t i = (size_t)n * epi.ld + m;
+      const float x = RES_ROWS > 0 ? ep_res[nl * 128 + m_local]
+                                   : to_f(__ldcg(&static_cast<const __nv_bfloat16*>(epi.resid)[i]));
+      static_cast<__nv_bfloat16*>(epi.out_t)[i] = __float2bfloat16_rn(x + val);
+    } else {
+      epi_ssm<__nv_bfloat16>(epi, n, m, val, ep_b[nl], ep_p[nl]);
+    }
+  };
   if (a.splits == 1) {
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
       tmem_ld16(trow + c0, v);
       if (m < a.M) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = n_tile * BN + c0 + j;
-          if (n < a.N) {
-            if (a.swap)
-              epi_apply<__nv_bfloat16>(epi, n, m, v[j]);
-            else
-              epi_apply<__nv_bfloat16>(epi, m, n, v[j]);
-          }
-        }
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < n_here) emit(c0 + j, v[j]);
       }
     }
   } else {
@@ -282,7 +325,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     // drained stage buffers); after a cluster barrier, rank r sums rows
     // r, r + splits, ... over all partners in rank order (deterministic).
     float* red = reinterpret_cast<float*>(smem);
-    const int n_here = min(BN, a.N - n_tile * BN);
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
       tmem_ld16(trow + c0, v);
@@ -300,13 +342,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       float sum = 0.f;
 #pragma unroll
       for (int sp = 0; sp < 8; ++sp) sum += part[sp];
-      if (m < a.M) {
-        const int n = n_tile * BN + nl;
-        if (a.swap)
-          epi_apply<__nv_bfloat16>(epi, n, m, sum);
-        else
-          epi_apply<__nv_bfloat16>(epi, m, n, sum);
-      }
+      if (m < a.M) emit(nl, sum);
     }
     cluster_sync_all();  // partners keep their shared memory until all reads are done
   }
@@ -359,7 +395,9 @@ namespace {
 
 template <int BN, int STAGES>
 constexpr size_t tc_smem() {
-  return 1024 + (size_t)STAGES * (128 * 128 + BN * 128) + (2 * STAGES + 1) * 8 + 32;
+  // 1 KB alignment slack, stages, barriers, TMEM slot + flags (28 B), epilogue cache
+  return 1024 + (size_t)STAGES * (128 * 128 + BN * 128) + (2 * STAGES + 1) * 8 + 32 +
+         EpiCache<BN>::bytes;
 }
 
 template <int BN, int STAGES>

@@ -569,39 +569,32 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, 
   HF_CUDA(h, ensure_device(h));
   cudaStream_t st = (cudaStream_t)stream;
   const Dims& d = h->d;
-  {
-    Scope sc(h, HF_K_COMMIT_PREP, st);
-    cudaError_t e = hf::launch_commit_prep(h->cfg.dtype, d, batch, feats, n_accepted, h->pos,
-                                           h->offsets, h->row_req, h->row_pos, h->tags, h->packed,
-                                           h->err, st);
-    sc.count = 1;
-    if (e != cudaSuccess) return cuda_fail(h, e, "commit prep launch");
-  }
+  // Projections of all batch*(S+1) rows of all layers in one GEMM; the
+  // epilogue keeps only rows t < n_b (ring append at pos_b + t; x, B, dt).
   Epi ep = epi_base(h);
   ep.kind = hf::EPI_SSM_KV;
   ep.layer0 = 0;
   ep.cols_per_layer = d.Nc;
   ep.col_off = 0;
-  ep.row_req = h->row_req;
-  ep.row_pos = h->row_pos;
-  ep.n_rows = h->offsets + batch;
+  ep.n_acc = n_accepted;
+  ep.pos = h->pos;
   ep.xbd = h->xbd;
   ep.xbd_layer_stride = h->xbd_ls;
+  const int rows = batch * (d.S + 1);
   hf_status s;
   if (h->wt_commit) {  // pre-tiled: rows padded per layer to nc_pad, padding skipped
     ep.cols_per_layer = h->nc_pad;
     ep.cols_valid = d.Nc;
-    s = gemm(h, HF_K_COMMIT_PROJ, h->packed, d.D, h->w_commit, d.D, batch * (d.S + 1),
-             d.L * h->nc_pad, d.D, ep, st, h->wt_commit);
+    s = gemm(h, HF_K_COMMIT_PROJ, feats, d.D, h->w_commit, d.D, rows, d.L * h->nc_pad, d.D, ep, st,
+             h->wt_commit);
   } else {
-    s = gemm(h, HF_K_COMMIT_PROJ, h->packed, d.D, h->w_commit, d.D, batch * (d.S + 1), d.L * d.Nc,
-             d.D, ep, st);
+    s = gemm(h, HF_K_COMMIT_PROJ, feats, d.D, h->w_commit, d.D, rows, d.L * d.Nc, d.D, ep, st);
   }
   if (s != HF_OK) return s;
   {
     Scope sc(h, HF_K_COMMIT_STATE, st);
-    cudaError_t e = hf::launch_commit_state(d, batch, h->offsets, h->xbd, h->xbd_ls, h->A_log,
-                                            h->state, h->pos, st);
+    cudaError_t e = hf::launch_commit_state(d, batch, n_accepted, h->xbd, h->xbd_ls, h->A_log,
+                                            h->state, h->pos, h->offsets, h->tags, h->err, st);
     sc.count = 1;
     if (e != cudaSuccess) return cuda_fail(h, e, "commit state launch");
   }
