@@ -143,7 +143,14 @@ struct Dims {
 };
 
 // ---------------------------------------------------------------- GEMM epilogues
-enum EpiKind : int { EPI_F32 = 0, EPI_RESID = 1, EPI_SSM_KV = 2 };
+enum EpiKind : int {
+  EPI_F32 = 0,    // plain fp32 store
+  EPI_RESID = 1,  // residual add, model dtype
+  EPI_SSM_KV = 2, // ring append / memory inputs (commit, prefill window)
+  EPI_DT = 3,     // prefill: dt of token r, head c, stored transposed (fp32)
+  EPI_XB = 4,     // prefill: w-scaled x and B of token r, stored transposed (model dtype)
+  EPI_STATE = 5   // prefill: state row r = (head, p), column n: decay * state + v
+};
 
 struct Epi {
   int kind;
@@ -174,6 +181,17 @@ struct Epi {
   float* xbd;
   long long xbd_layer_stride;  // elements between layers in xbd
   const float* dt_bias;        // [L][Hm]
+  // Prefill chunked-scan epilogues (one request, one segment of T tokens):
+  //  EPI_DT    dtw[c*ldt + r] = softplus(v + dt_bias[layer0][c])
+  //  EPI_XB    c <  dinner: xsT[c*ldt + r] = dtw[(c/P)*ldt + r] * v   (dtw holds w)
+  //            c >= dinner: bT[(c-dinner)*ldt + r] = v
+  //  EPI_STATE st[r*N + c] = seg_decay[r/P] * st[r*N + c] + v
+  float* dtw;
+  int ldt;
+  void* xsT;
+  void* bT;
+  float* st;
+  const float* seg_decay;
   Dims d;
 };
 
@@ -224,11 +242,23 @@ __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
     size_t i = (size_t)r * e.ld + c;
     float x = to_f(__ldcg(&((const T*)e.resid)[i]));
     ((T*)e.out_t)[i] = from_f<T>(x + v);
-  } else {
+  } else if (e.kind == EPI_SSM_KV) {
     int b;
     long long p;
     epi_row(e, r, b, p);
     epi_ssm<T>(e, r, c, v, b, p);
+  } else if (e.kind == EPI_DT) {
+    e.dtw[(size_t)c * e.ldt + r] = softplus_f(v + __ldg(&e.dt_bias[e.layer0 * e.d.Hm + c]));
+  } else if (e.kind == EPI_XB) {
+    if (c < e.d.dinner) {
+      const float w = __ldcg(&e.dtw[(size_t)(c / e.d.P) * e.ldt + r]);
+      static_cast<T*>(e.xsT)[(size_t)c * e.ldt + r] = from_f<T>(w * v);
+    } else {
+      static_cast<T*>(e.bT)[(size_t)(c - e.d.dinner) * e.ldt + r] = from_f<T>(v);
+    }
+  } else {  // EPI_STATE
+    const size_t i = (size_t)r * e.d.N + c;
+    e.st[i] = fmaf(__ldcg(&e.seg_decay[r / e.d.P]), __ldcg(&e.st[i]), v);
   }
 }
 
@@ -296,10 +326,13 @@ cudaError_t launch_prefill_ring_prep(int dtype, const Dims& d, int n_req, int n_
                                      const int32_t* lens, const int32_t* reqs,
                                      const void* feats, int32_t* row_req, int64_t* row_pos,
                                      int32_t* tags, void* packed, cudaStream_t st);
-cudaError_t launch_prefill_scan(const Dims& d, int layer, int n_req, const int32_t* lens,
-                                const int32_t* reqs, long long seg0, long long seg1,
-                                const float* xbd, const float* A_log, float* state,
-                                cudaStream_t st);
+// Chunked decay scan of one prefill segment of T tokens, per head h (grid Hm):
+// dtw[h][t] holds dt_t on entry and w_t = dt_t * exp(A_h * sum_{s>t} dt_s)
+// on exit; seg_decay[h] = exp(A_h * sum_t dt_t). Chunks of `chunk` tokens
+// are scanned within a warp; chunk and warp totals combine with shuffles
+// and a CTA-level suffix pass.
+cudaError_t launch_prefill_decay(const Dims& d, int layer, int T, int ldt, int chunk, float* dtw,
+                                 const float* A_log, float* seg_decay, cudaStream_t st);
 // Message reported by hf_last_error(NULL) for calls that have no handle.
 void set_thread_error(const char* msg);
 

@@ -65,7 +65,11 @@ struct hf_handle {
   int n_counters = 0;
   int num_sms = 152;
 
-  float* pf_xbd = nullptr;     // [Tseg][NS]
+  // prefill segment scratch (Tseg = pf_tokens tokens, transposed layouts)
+  float* pf_dtw = nullptr;     // [Hm][Tseg] fp32: dt, then decay weights w
+  float* pf_decay = nullptr;   // [Hm] fp32: decay of the whole segment
+  void* pf_xsT = nullptr;      // [Hm*P][Tseg] model dtype: w * x
+  void* pf_bT = nullptr;       // [N][Tseg] model dtype: B
   long long pf_tokens = 0;
   int32_t* pf_lens = nullptr;  // [Bmax]
   int32_t* pf_reqs = nullptr;  // [Bmax]
@@ -296,6 +300,16 @@ hf_status gemm(hf_handle* h, int fam, const void* X, int ldx, const void* Wt, in
   return HF_OK;
 }
 
+// Y[t, c] = sum_k F[t, k] W[c, k] over the T tokens of a prefill segment,
+// tokens as the 128-row operand (no split: T is large), epilogue per element.
+cudaError_t tokens_gemm(hf_handle* h, const void* F, int T, const void* W, int C, const Epi& epi,
+                        cudaStream_t st, int* count) {
+  const Dims& d = h->d;
+  if (h->cfg.dtype == HF_F32)
+    return hf::launch_gemm_fma(h->cfg.dtype, F, d.D, W, d.D, T, C, d.D, 1, h->part, epi, st, count);
+  return hf::launch_gemm_tc(F, d.D, T, W, d.D, C, d.D, 0, 1, h->err, epi, st, count);
+}
+
 Epi epi_base(const hf_handle* h) {
   Epi e{};
   e.d = h->d;
@@ -358,7 +372,7 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   const size_t L = d.L, Bm = d.Bmax;
   h->rmax = std::max<long long>((long long)(d.S + 1) * Bm, (long long)Bm * d.W);
   h->xbd_ls = (long long)(d.S + 1) * Bm * d.NS;
-  h->pf_tokens = h->cfg.prefill_tokens_max;
+  h->pf_tokens = round_up(h->cfg.prefill_tokens_max, 64);
   h->part_elems = (size_t)16 << 20;
 
   hf_status s = HF_OK;
@@ -401,7 +415,10 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess && sms > 0)
       h->num_sms = sms;
   }
-  A((void**)&h->pf_xbd, (size_t)h->pf_tokens * d.NS * 4);
+  A((void**)&h->pf_dtw, (size_t)d.Hm * h->pf_tokens * 4);
+  A((void**)&h->pf_decay, (size_t)d.Hm * 4);
+  A(&h->pf_xsT, (size_t)d.dinner * h->pf_tokens * es);
+  A(&h->pf_bT, (size_t)d.N * h->pf_tokens * es);
   A((void**)&h->pf_lens, Bm * 4);
   A((void**)&h->pf_reqs, Bm * 4);
   A((void**)&h->err, 16);
@@ -653,29 +670,55 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
                       &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "prefill kv gemm");
     }
-    for (long long s0 = 0; s0 < total; s0 += h->pf_tokens) {
-      const long long s1 = std::min(total, s0 + h->pf_tokens);
-      Epi ex = epi_base(h);
-      ex.kind = hf::EPI_SSM_KV;
-      ex.layer0 = l;
-      ex.cols_per_layer = d.dinner + d.N + d.Hm;
-      ex.col_off = 2 * d.KVD;
-      ex.xbd = h->pf_xbd;
-      ex.xbd_layer_stride = 0;
-      const void* fseg = bptr(feats, (size_t)s0 * d.D * es);
-      const void* wseg = wl + (size_t)2 * d.KVD * d.D * es;
-      const int nx = d.dinner + d.N + d.Hm;
-      if (h->cfg.dtype == HF_F32)
-        e = hf::launch_gemm_fma(h->cfg.dtype, fseg, d.D, wseg, d.D, (int)(s1 - s0), nx, d.D, 1,
-                                h->part, ex, st, &sc.count);
-      else  // tokens as the 128-row operand, features as N
-        e = hf::launch_gemm_tc(fseg, d.D, (int)(s1 - s0), wseg, d.D, nx, d.D, 0, 1, h->err, ex,
-                               st, &sc.count);
-      if (e != cudaSuccess) return cuda_fail(h, e, "prefill ssm gemm");
-      e = hf::launch_prefill_scan(d, l, n_req, h->pf_lens, h->pf_reqs, s0, s1, h->pf_xbd, h->A_log,
-                                  h->state, st);
-      sc.count++;
-      if (e != cudaSuccess) return cuda_fail(h, e, "prefill scan");
+    // Memory fold, per request and segment of at most Tseg tokens:
+    //   dt (transposed) -> chunked decay scan -> w*x, B (transposed, bf16/fp32)
+    //   -> state = decay_seg * state + (w*x)^T B   (contraction over tokens)
+    const long long Tseg = h->pf_tokens;
+    const int nx = d.dinner + d.N;
+    const char* w_xb = wl + (size_t)2 * d.KVD * d.D * es;
+    const char* w_dt = wl + (size_t)(2 * d.KVD + d.dinner + d.N) * d.D * es;
+    long long cu = 0;
+    for (int i = 0; i < n_req; ++i) {
+      const long long Li = lens[i];
+      float* st_b = h->state + (((size_t)l * d.Bmax + reqs[i]) * d.Hm * d.P) * d.N;
+      for (long long s0 = 0; s0 < Li; s0 += Tseg) {
+        const int T = (int)std::min(Tseg, Li - s0);
+        const void* fseg = bptr(feats, (size_t)(cu + s0) * d.D * es);
+        Epi e1 = epi_base(h);
+        e1.kind = hf::EPI_DT;
+        e1.layer0 = l;
+        e1.dtw = h->pf_dtw;
+        e1.ldt = (int)Tseg;
+        e = tokens_gemm(h, fseg, T, w_dt, d.Hm, e1, st, &sc.count);
+        if (e != cudaSuccess) return cuda_fail(h, e, "prefill dt gemm");
+        e = hf::launch_prefill_decay(d, l, T, (int)Tseg, h->cfg.chunk, h->pf_dtw, h->A_log,
+                                     h->pf_decay, st);
+        sc.count++;
+        if (e != cudaSuccess) return cuda_fail(h, e, "prefill decay scan");
+        Epi e2 = epi_base(h);
+        e2.kind = hf::EPI_XB;
+        e2.dtw = h->pf_dtw;
+        e2.ldt = (int)Tseg;
+        e2.xsT = h->pf_xsT;
+        e2.bT = h->pf_bT;
+        e = tokens_gemm(h, fseg, T, w_xb, nx, e2, st, &sc.count);
+        if (e != cudaSuccess) return cuda_fail(h, e, "prefill x/B gemm");
+        Epi e3 = epi_base(h);
+        e3.kind = hf::EPI_STATE;
+        e3.st = st_b;
+        e3.seg_decay = h->pf_decay;
+        if (h->cfg.dtype == HF_F32) {
+          const int splits = pick_splits(h, d.dinner, d.N, T, 64, 64);
+          e = hf::launch_gemm_fma(h->cfg.dtype, h->pf_xsT, (int)Tseg, h->pf_bT, (int)Tseg, d.dinner,
+                                  d.N, T, splits, h->part, e3, st, &sc.count);
+        } else {
+          const int splits = hf::tc_pick_splits(d.dinner, d.N, T);
+          e = hf::launch_gemm_tc(h->pf_xsT, Tseg, d.dinner, h->pf_bT, Tseg, d.N, T, 0, splits,
+                                 h->err, e3, st, &sc.count);
+        }
+        if (e != cudaSuccess) return cuda_fail(h, e, "prefill contraction gemm");
+      }
+      cu += Li;
     }
   }
   e = hf::launch_prefill_finish(n_req, h->pf_lens, h->pf_reqs, h->pos, st);

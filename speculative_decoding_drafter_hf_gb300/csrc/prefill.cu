@@ -1,5 +1,6 @@
 // Prefill helpers: reset a request, fill its window from the last W prefix
-// features, fold the prefix into its memory, set its position.
+// features, the chunked decay scan of the memory fold, set its position.
+// (The fold's contractions run on the tensor-core GEMM: gemm_tc.cu.)
 //
 // Source: HyFlash abstract ("recurrent memory compresses historical target
 // features into fixed-size states") and the explainer's "That is HyFlash":
@@ -63,77 +64,66 @@ __global__ void prefill_ring_prep_kernel(Dims d, int n_req, const int32_t* __res
   for (int i = threadIdx.x; i < d.D; i += blockDim.x) dst[i] = src[i];
 }
 
-// grid (Hm, n_req): token-by-token fold of the rows [seg0, seg1) of the packed
-// prefix that belong to request i, starting from the state in memory.
-constexpr int SCAN_TC = 32;   // tokens staged per step
-constexpr int SCAN_QPT = 8;   // float4 state elements per thread (P*N <= 8192)
+// grid (Hm), 32 warps: chunked suffix scan of a_t = dt_t * A_h over one
+// segment. Warp w owns a contiguous range of whole chunks; pass 1 sums each
+// range, a CTA-level suffix over the 32 range totals gives every warp the
+// decay carried in from later tokens; pass 2 walks the warp's chunks from the
+// last one back, with an inclusive suffix scan across lanes (shuffles) inside
+// each chunk, and turns dt_t into w_t = dt_t * exp(sum_{s>t} a_s).
+constexpr int DECAY_MAX_E = 8;  // tokens per lane per chunk (chunk <= 256)
 
-__global__ void __launch_bounds__(256)
-prefill_scan_kernel(Dims d, int layer, const int32_t* __restrict__ lens,
-                    const int32_t* __restrict__ reqs, long long seg0, long long seg1,
-                    const float* __restrict__ xbd, const float* __restrict__ A_log,
-                    float* __restrict__ state) {
-  extern __shared__ __align__(16) float sm[];
-  const int hd = blockIdx.x, i = blockIdx.y;
-  long long cu = 0;
-  for (int k = 0; k < i; ++k) cu += lens[k];
-  const long long t0 = cu > seg0 ? cu : seg0;
-  const long long tend = cu + lens[i];
-  const long long t1 = tend < seg1 ? tend : seg1;
-  if (t0 >= t1) return;
-  const int b = reqs[i];
-  const int P = d.P, N = d.N;
-  const float A = -expf(A_log[layer * d.Hm + hd]);
-  float4* h = reinterpret_cast<float4*>(state + ((((size_t)layer * d.Bmax + b) * d.Hm + hd) * P) * N);
-  const int nq = P * N / 4;
-
-  float4 hv[SCAN_QPT];
-  int qp[SCAN_QPT], qn[SCAN_QPT];
-#pragma unroll
-  for (int u = 0; u < SCAN_QPT; ++u) {
-    int q = threadIdx.x + u * blockDim.x;
-    qp[u] = (q * 4) / N;
-    qn[u] = (q * 4) % N;
-    hv[u] = q < nq ? h[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+__global__ void __launch_bounds__(1024)
+prefill_decay_kernel(Dims d, int layer, int T, int ldt, int chunk, float* __restrict__ dtw,
+                     const float* __restrict__ A_log, float* __restrict__ seg_decay) {
+  __shared__ float wsum[32];
+  const int h = blockIdx.x, warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const float A = -expf(A_log[layer * d.Hm + h]);
+  float* row = dtw + (size_t)h * ldt;
+  const int per = (T + 31) / 32;
+  const int R = (per + chunk - 1) / chunk * chunk;  // tokens per warp, whole chunks
+  const int w0 = warp * R, w1 = min(T, w0 + R);
+  float acc = 0.f;
+  for (int t = w0 + lane; t < w1; t += 32) acc += row[t] * A;
+  acc = warp_sum(acc);
+  if (lane == 0) wsum[warp] = acc;
+  __syncthreads();
+  float carry = 0.f;  // sum over all tokens after this warp's range
+  for (int w2 = 31; w2 > warp; --w2) carry += wsum[w2];
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int w2 = 31; w2 >= 0; --w2) tot += wsum[w2];
+    seg_decay[h] = expf(tot);
   }
-  float* xs = sm;                       // [TC][P]
-  float* bs = xs + SCAN_TC * P;         // [TC][N]
-  float* ds = bs + SCAN_TC * N;         // [TC]
-  for (long long c0 = t0; c0 < t1; c0 += SCAN_TC) {
-    const int nt = (int)((t1 - c0) < SCAN_TC ? (t1 - c0) : SCAN_TC);
-    __syncthreads();
-    for (int k = threadIdx.x; k < nt * P; k += blockDim.x) {
-      int t = k / P, p = k % P;
-      xs[t * P + p] = xbd[(size_t)(c0 - seg0 + t) * d.NS + hd * P + p];
-    }
-    for (int k = threadIdx.x; k < nt * N; k += blockDim.x) {
-      int t = k / N, n = k % N;
-      bs[t * N + n] = xbd[(size_t)(c0 - seg0 + t) * d.NS + d.dinner + n];
-    }
-    for (int k = threadIdx.x; k < nt; k += blockDim.x)
-      ds[k] = xbd[(size_t)(c0 - seg0 + k) * d.NS + d.dinner + d.N + hd];
-    __syncthreads();
-    for (int t = 0; t < nt; ++t) {
-      const float dt = ds[t];
-      const float dec = expf(dt * A);
+  const int E = chunk / 32;
+  for (int k = R / chunk - 1; k >= 0; --k) {
+    const int cs = w0 + k * chunk;
+    if (cs >= w1) continue;
+    float a[DECAY_MAX_E], dv[DECAY_MAX_E];
+    float lane_tot = 0.f;
 #pragma unroll
-      for (int u = 0; u < SCAN_QPT; ++u) {
-        int q = threadIdx.x + u * blockDim.x;
-        if (q < nq) {
-          const float xv = dt * xs[t * P + qp[u]];
-          const float4 Bv = *reinterpret_cast<const float4*>(&bs[t * N + qn[u]]);
-          hv[u].x = fmaf(dec, hv[u].x, xv * Bv.x);
-          hv[u].y = fmaf(dec, hv[u].y, xv * Bv.y);
-          hv[u].z = fmaf(dec, hv[u].z, xv * Bv.z);
-          hv[u].w = fmaf(dec, hv[u].w, xv * Bv.w);
-        }
-      }
+    for (int e = 0; e < DECAY_MAX_E; ++e) {
+      const int t = cs + lane * E + e;
+      dv[e] = (e < E && t < w1) ? row[t] : 0.f;
+      a[e] = dv[e] * A;
+      lane_tot += a[e];
     }
-  }
+    float incl = lane_tot;  // sum over this lane and all later lanes of the chunk
 #pragma unroll
-  for (int u = 0; u < SCAN_QPT; ++u) {
-    int q = threadIdx.x + u * blockDim.x;
-    if (q < nq) h[q] = hv[u];
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    float excl = __shfl_down_sync(0xffffffffu, incl, 1);  // later lanes only
+    if (lane == 31) excl = 0.f;
+    const float chunk_tot = __shfl_sync(0xffffffffu, incl, 0);
+    float run = carry + excl;
+#pragma unroll
+    for (int e = DECAY_MAX_E - 1; e >= 0; --e) {
+      const int t = cs + lane * E + e;
+      if (e < E && t < w1) row[t] = dv[e] * expf(run);
+      run += a[e];
+    }
+    carry += chunk_tot;
   }
 }
 
@@ -167,14 +157,11 @@ cudaError_t launch_prefill_ring_prep(int dtype, const Dims& d, int n_req, int n_
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_scan(const Dims& d, int layer, int n_req, const int32_t* lens,
-                                const int32_t* reqs, long long seg0, long long seg1,
-                                const float* xbd, const float* A_log, float* state,
-                                cudaStream_t st) {
-  if (n_req <= 0 || seg1 <= seg0) return cudaSuccess;
-  size_t smem = (size_t)SCAN_TC * (d.P + d.N + 1) * sizeof(float);
-  prefill_scan_kernel<<<dim3(d.Hm, n_req), 256, smem, st>>>(d, layer, lens, reqs, seg0, seg1, xbd,
-                                                            A_log, state);
+cudaError_t launch_prefill_decay(const Dims& d, int layer, int T, int ldt, int chunk, float* dtw,
+                                 const float* A_log, float* seg_decay, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (chunk < 32 || chunk > 32 * DECAY_MAX_E || chunk % 32) return cudaErrorInvalidValue;
+  prefill_decay_kernel<<<d.Hm, 1024, 0, st>>>(d, layer, T, ldt, chunk, dtw, A_log, seg_decay);
   return cudaGetLastError();
 }
 

@@ -228,3 +228,18 @@ def test_rounds_captured_in_cuda_graph(name):
     del g
     p.gpu.profile(0)
     p.close()
+
+
+@pytest.mark.parametrize("chunk,tokens_max", [(64, 1000), (128, 4096), (256, 700)])
+def test_prefill_chunked_scan_segments_bf16(chunk, tokens_max):
+    """The prefill fold (dt projection, chunked decay scan, w-scaled x/B
+    projection, contraction over tokens) with several chunk sizes and with
+    prefixes split into segments at non-multiples of the chunk; three
+    requests of different lengths (one empty)."""
+    cfg = CONFIGS["qwen3_4b_bf16"].replace(batch=3, chunk=chunk)
+    p = Pair(cfg, prefill_tokens_max=tokens_max)
+    lens = [2500, 0, 333]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what=f"prefill chunk {chunk}")
+    run_rounds(p, 2)
+    p.close()
