@@ -119,6 +119,35 @@ struct TcArgs {
   int32_t* err;       // device error word
 };
 
+// Token-major epilogue (swap = 0: output row m = this thread's accumulator
+// lane, 16 consecutive output columns n0..n0+15): loads that depend only on
+// the row (decay weight of the column's head, segment decay of the row's
+// head) are made once per chunk and the state update is vectorised, so the
+// epilogue issues no per-element dependent loads.
+__device__ __forceinline__ void epi_chunk16(const Epi& e, int m, int n0, int ncols, const float* v) {
+  const Dims& d = e.d;
+  if (e.kind == EPI_XB && n0 + 16 <= d.dinner && d.P % 16 == 0) {
+    const float w = __ldcg(&e.dtw[(size_t)(n0 / d.P) * e.ldt + m]);
+    __nv_bfloat16* x = static_cast<__nv_bfloat16*>(e.xsT);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[(size_t)(n0 + j) * e.ldt + m] = __float2bfloat16_rn(w * v[j]);
+    return;
+  }
+  if (e.kind == EPI_STATE && ncols == 16 && d.N % 16 == 0) {
+    const float dec = __ldcg(&e.seg_decay[m / d.P]);
+    float4* st = reinterpret_cast<float4*>(e.st + (size_t)m * d.N + n0);
+    float4 old[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) old[q] = __ldcg(&st[q]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      st[q] = make_float4(fmaf(dec, old[q].x, v[4 * q]), fmaf(dec, old[q].y, v[4 * q + 1]),
+                          fmaf(dec, old[q].z, v[4 * q + 2]), fmaf(dec, old[q].w, v[4 * q + 3]));
+    return;
+  }
+  for (int j = 0; j < ncols; ++j) epi_apply<__nv_bfloat16>(e, m, n0 + j, v[j]);
+}
+
 // Epilogue cache (shared memory after the barriers): per output row of the
 // tile its request and committed position (ring rows), and for small tiles
 // the residual inputs; filled during the main loop by the otherwise idle
@@ -314,12 +343,44 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
       tmem_ld16(trow + c0, v);
-      if (m < a.M) {
+      if (m < a.M && c0 < n_here) {
+        if (!a.swap) {
+          epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (c0 + j < n_here) emit(c0 + j, v[j]);
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < n_here) emit(c0 + j, v[j]);
+        }
       }
     }
+  } else if (!a.swap) {
+    // Split-K, token-major: partial tiles meet in distributed shared memory;
+    // rank r owns the 16-column chunks r, r + splits, ... of the tile and sums
+    // them over all partners in rank order (deterministic).
+    float* red = reinterpret_cast<float*>(smem);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      tmem_ld16(trow + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + m_local] = v[j];
+    }
+    cluster_sync_all();
+    const int rank = (int)cluster_rank();
+    for (int c0 = rank * 16; c0 < n_here; c0 += a.splits * 16) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float part[8];
+#pragma unroll
+        for (int sp = 0; sp < 8; ++sp)
+          part[sp] = sp < a.splits ? ld_peer(&red[(c0 + j) * 128 + m_local], (uint32_t)sp) : 0.f;
+        float sum = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < 8; ++sp) sum += part[sp];
+        v[j] = sum;
+      }
+      if (m < a.M) epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
+    }
+    cluster_sync_all();  // partners keep their shared memory until all reads are done
   } else {
     // Split-K: this CTA's partial tile goes to its own shared memory (the
     // drained stage buffers); after a cluster barrier, rank r sums rows

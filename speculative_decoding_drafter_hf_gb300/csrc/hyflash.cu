@@ -149,8 +149,8 @@ hf_status validate(const hf_config* c, std::string* why) {
   if (c->d_model % 8) return bad("d_model must be a multiple of 8");
   if (c->prefill_tokens_max < 0) return bad("prefill_tokens_max must be >= 0");
   if (c->max_batch > 65535) return bad("max_batch must be <= 65535");
-  if (c->dtype == HF_BF16 && (c->head_dim % 8 || ((long long)c->ssm_heads * c->ssm_headdim) % 8))
-    return bad("bf16 needs head_dim and ssm_heads*ssm_headdim multiples of 8");
+  if (c->dtype == HF_BF16 && c->ssm_headdim % 16)
+    return bad("bf16 needs ssm_headdim a multiple of 16");
   {
     const Dims d = make_dims(*c);
     if (hf::attn_cluster_smem(d, d.esize) > 232448)
