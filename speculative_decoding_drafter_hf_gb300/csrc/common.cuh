@@ -282,6 +282,14 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
                            int N, int K, int swap, int splits, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches, const void* a_tiles = nullptr);
 void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst);
+
+// Persistent warp-specialised bf16 GEMM for large token-major products
+// (gemm_persistent.cu): output row m of A's rows, column n of B's rows;
+// epilogue through epi_chunk16. One CTA per SM (num_sms).
+cudaError_t configure_tc_persistent(int num_sms);
+cudaError_t launch_gemm_persistent(const void* A, long long lda, int M, const void* B,
+                                   long long ldb, int N, int K, int32_t* err, const Epi& epi,
+                                   int num_sms, cudaStream_t st, int* launches);
 size_t tiled_bytes(long long M, long long K);
 int tc_pick_splits(int M, int N, int K);
 

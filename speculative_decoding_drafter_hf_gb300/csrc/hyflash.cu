@@ -307,6 +307,8 @@ cudaError_t tokens_gemm(hf_handle* h, const void* F, int T, const void* W, int C
   const Dims& d = h->d;
   if (h->cfg.dtype == HF_F32)
     return hf::launch_gemm_fma(h->cfg.dtype, F, d.D, W, d.D, T, C, d.D, 1, h->part, epi, st, count);
+  if (C >= 256 && (long long)((T + 127) / 128) * ((C + 255) / 256) >= h->num_sms)
+    return hf::launch_gemm_persistent(F, d.D, T, W, d.D, C, d.D, h->err, epi, h->num_sms, st, count);
   return hf::launch_gemm_tc(F, d.D, T, W, d.D, C, d.D, 0, 1, h->err, epi, st, count);
 }
 
@@ -444,6 +446,7 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   if (s == HF_OK) {
     e = hf::configure_attn_cluster(h->d);
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc();
+    if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc_persistent(h->num_sms);
     if (e != cudaSuccess) s = cuda_fail(h, e, "kernel set-up");
   }
   if (s == HF_OK) {

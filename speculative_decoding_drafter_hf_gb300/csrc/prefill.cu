@@ -11,17 +11,21 @@
 namespace hf {
 namespace {
 
+// grid (blocks, n_req, L): zero the request's state (all layers), clear its
+// ring tags and position.
 __global__ void prefill_reset_kernel(Dims d, const int32_t* __restrict__ reqs,
                                      float* __restrict__ state, int32_t* __restrict__ tags,
                                      int64_t* __restrict__ pos) {
-  const int b = reqs[blockIdx.x];
-  const size_t per = (size_t)d.Hm * d.P * d.N;
-  for (int l = 0; l < d.L; ++l) {
-    float4* h = reinterpret_cast<float4*>(state + ((size_t)l * d.Bmax + b) * per);
-    for (size_t i = threadIdx.x; i < per / 4; i += blockDim.x) h[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int b = reqs[blockIdx.y], l = blockIdx.z;
+  const size_t per4 = (size_t)d.Hm * d.P * d.N / 4;
+  float4* h = reinterpret_cast<float4*>(state + ((size_t)l * d.Bmax + b) * per4 * 4);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < per4;
+       i += (size_t)gridDim.x * blockDim.x)
+    h[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (blockIdx.x == 0 && l == 0) {
+    for (int i = threadIdx.x; i < d.W; i += blockDim.x) tags[(size_t)b * d.W + i] = -1;
+    if (threadIdx.x == 0) pos[b] = 0;
   }
-  for (int i = threadIdx.x; i < d.W; i += blockDim.x) tags[(size_t)b * d.W + i] = -1;
-  if (threadIdx.x == 0) pos[b] = 0;
 }
 
 // grid (n_rows): packed ring row j -> request i, its position, gathered row.
@@ -59,9 +63,10 @@ __global__ void prefill_ring_prep_kernel(Dims d, int n_req, const int32_t* __res
   }
   __syncthreads();
   if (!s_found) return;
-  const T* src = feats + (size_t)s_src * d.D;
-  T* dst = packed + (size_t)j * d.D;
-  for (int i = threadIdx.x; i < d.D; i += blockDim.x) dst[i] = src[i];
+  // D * sizeof(T) is a multiple of 16 and both rows are 16-byte aligned
+  const uint4* src = reinterpret_cast<const uint4*>(feats + (size_t)s_src * d.D);
+  uint4* dst = reinterpret_cast<uint4*>(packed + (size_t)j * d.D);
+  for (int i = threadIdx.x; i < d.D * (int)sizeof(T) / 16; i += blockDim.x) dst[i] = src[i];
 }
 
 // grid (Hm), 32 warps: chunked suffix scan of a_t = dt_t * A_h over one
@@ -138,7 +143,9 @@ __global__ void prefill_finish_kernel(int n_req, const int32_t* __restrict__ len
 cudaError_t launch_prefill_reset(const Dims& d, int n_req, const int32_t* reqs, float* state,
                                  int32_t* tags, int64_t* pos, cudaStream_t st) {
   if (n_req <= 0) return cudaSuccess;
-  prefill_reset_kernel<<<n_req, 256, 0, st>>>(d, reqs, state, tags, pos);
+  const size_t per4 = (size_t)d.Hm * d.P * d.N / 4;
+  const int blocks = (int)std::min<size_t>((per4 + 1023) / 1024, 64);
+  prefill_reset_kernel<<<dim3(blocks, n_req, d.L), 256, 0, st>>>(d, reqs, state, tags, pos);
   return cudaGetLastError();
 }
 
