@@ -192,15 +192,22 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+ORACLE_PREFIX_CAP = 8192    # oracle prefill length cap (a round's cost does not depend on it)
+ORACLE_BATCH_CAP = 2        # requests the oracle drafts for in its timed sample
+
+
 def oracle_rounds(cfg, batch: int, steps: int, warmup: int, budget_s: float, seed: int = 0):
     """Time the float64 oracle on host cores: prefill untimed, then rounds of
-    draft + commit; stops early after budget_s seconds of timed work."""
+    draft + commit; stops early after budget_s seconds of timed work. Large
+    workloads run on a bounded sample: at most ORACLE_BATCH_CAP requests whose
+    prefixes are capped at ORACLE_PREFIX_CAP tokens (the window and memory
+    are full either way, so a round costs the same)."""
     from oracle import hyflash_oracle as O
     from workload import (make_accepted, make_layer_weights, make_prefix_feats,
                           make_prefix_lens, make_round_inputs)
     weights = [make_layer_weights(cfg, l) for l in range(cfg.n_layers)]
     orc = O.OracleDrafter(cfg, weights, batch)
-    lens = make_prefix_lens(cfg)[:batch]
+    lens = [min(L, ORACLE_PREFIX_CAP) for L in make_prefix_lens(cfg)[:batch]]
     orc.prefill(lens, make_prefix_feats(cfg, lens, seed=seed))
     for r in range(warmup):
         slot, feats = make_round_inputs(cfg, r, batch, seed=seed)
@@ -221,21 +228,35 @@ def oracle_rounds(cfg, batch: int, steps: int, warmup: int, budget_s: float, see
     return done, accepted, t_total
 
 
+def cpu_sample(cfg, steps: int, warmup: int, budget: float):
+    """Oracle draft-steps/s for the whole batch, from a bounded sample."""
+    sb = min(cfg.batch, ORACLE_BATCH_CAP)
+    done, acc, t = oracle_rounds(cfg, sb, steps, warmup, budget)
+    scale = sb / cfg.batch  # a step drafts and commits for every request of the batch
+    v = done / t * scale if t > 0 else 0.0
+    sample = (f"{done} rounds (draft+commit) of {cfg.name} for {sb} of {cfg.batch} requests "
+              f"(rate scaled by {sb}/{cfg.batch}), prefixes capped at {ORACLE_PREFIX_CAP} tokens, "
+              f"float64 NumPy, after an untimed oracle prefill and {warmup} warm-up rounds")
+    return v, acc / t * (1 / scale) if t > 0 else 0.0, done, t, sample
+
+
 def run_reference(args, cfg):
     ws, rank = dist_init("gloo")
     if rank != 0:
         return 0
-    batch = cfg.batch
+    if cfg.rounds == 0:
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "prefill sweep: the float64 oracle folds 4K-128K-token prefixes at "
+                          "batch 8 far beyond a bounded run"}), flush=True)
+        return 0
     budget = float(os.environ.get("HF_REF_BUDGET_S", "120"))
-    done, acc, t = oracle_rounds(cfg, batch, args.steps, args.warmup, budget)
-    v = done / t if t > 0 else 0.0
-    sample = (f"{done} of {args.steps} requested rounds (draft+commit) of {cfg.name}, batch {batch}, "
-              f"after an untimed oracle prefill and {args.warmup} untimed warm-up rounds")
+    v, tok_rate, done, t, sample = cpu_sample(cfg, args.steps, args.warmup, budget)
+    batch = cfg.batch
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
         "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * t / max(done, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "committed_tokens_per_s": acc / t if t > 0 else 0.0,
+        "data": "synthetic", "committed_tokens_per_s": tok_rate,
         "config": {"workload": cfg.name, "batch": batch, "prefix": cfg.prefix,
                    "layers": cfg.n_layers, "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
@@ -247,6 +268,94 @@ def run_reference(args, cfg):
 
 
 # ------------------------------------------------------------------ GPU arm
+
+def prefix_features(cfg, lens, seed, dev):
+    """Seeded prefix features ~N(0,1) on the device. Up to 2^26 values they
+    come from the shared CPU generator (the bytes the oracle sees); larger
+    prefixes are drawn directly on the GPU (a seeded CUDA generator)."""
+    import torch
+    from workload import make_prefix_feats
+    total = sum(lens)
+    if total * cfg.d_model <= (1 << 26):
+        return make_prefix_feats(cfg, lens, seed=seed).to(dev)
+    g = torch.Generator(device=dev).manual_seed(7919 + seed)
+    return torch.randn((total, cfg.d_model), generator=g, device=dev).to(cfg.torch_dtype)
+
+
+def run_prefill_sweep(args, cfg):
+    """Prefill throughput: each step folds a batch of prefixes (all layers)."""
+    import torch
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    from speculative_decoding_drafter_hf_gb300 import build as _b
+    _b.build()
+    import speculative_decoding_drafter_hf_gb300 as hf
+    from workload import make_layer_weights
+    cfg = cfg.replace(chunk=args.chunk, n_layers=args.layers,
+                      prefix=args.prefix if args.prefix else cfg.prefix)
+    batch = cfg.batch
+    lens = [cfg.prefix] * batch
+    tseg = max(4096, min(cfg.prefix, 16384))
+    drafter = hf.Drafter(cfg, batch, device=local, prefill_tokens_max=tseg)
+    for l in range(cfg.n_layers):
+        drafter.set_weights(l, make_layer_weights(cfg, l))
+    feats = prefix_features(cfg, lens, rank, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        drafter.prefill(feats, lens)
+    drafter.sync()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    n0 = drafter.launch_count()
+    ev = []
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            drafter.prefill(feats, lens)
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+    barrier()
+    drafter.sync()
+    launches = drafter.launch_count() - n0
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dev)
+    tokens = sum(lens)
+    all_tok = sum_over_ranks(tokens * args.steps, dev)
+    value = all_tok / (total_ms / 1e3)
+    ring_rows = sum(min(L, cfg.window) for L in lens)
+    flops = prefill_flops(cfg, tokens, ring_rows)
+    peaks = {}
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        peaks = json.load(open(pp))
+    tc_peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    achieved = flops * args.steps / (total_ms / 1e3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "prefill tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "batch_per_gpu": batch, "prefix": cfg.prefix,
+                       "layers": cfg.n_layers, "chunk": cfg.chunk,
+                       "l2": f"flushed between steps ({2 * l2 >> 20} MiB write, untimed)",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": "tensor", "kernel": "whole prefill", "achieved": achieved,
+                         "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                         "traffic": None,
+                         "peak_source": "measured (sustained)" if peaks else "fallback",
+                         "algorithmic_flops_per_step": flops},
+            "gpu_launches": int(launches), "cpu_baseline": None,
+            "e2e": None, "clocks": clk.summary()}), flush=True)
+    drafter.close()
+    return 0
+
 
 def run_hyflash(args, cfg):
     import torch
@@ -268,7 +377,7 @@ def run_hyflash(args, cfg):
         drafter.set_weights(l, make_layer_weights(cfg, l))
     lens = make_prefix_lens(cfg, seed=0)[:batch]
     total = sum(lens)
-    feats = make_prefix_feats(cfg, lens, seed=seed).to(dev)
+    feats = prefix_features(cfg, lens, seed, dev)
     stream = torch.cuda.current_stream()
 
     # ---- prefill (one warm-up, then timed)
@@ -451,11 +560,9 @@ def run_hyflash(args, cfg):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         budget = float(os.environ.get("HF_CPU_BUDGET_S", "20"))
-        done, acc, t = oracle_rounds(cfg, batch, args.steps, 1, budget)
-        cpu = {"value": done / t if t > 0 else 0.0, "unit": UNIT, "cores": cpu_cores(),
-               "kind": "oracle",
-               "sample": f"{done} rounds (draft+commit) of {cfg.name}, batch {batch}, float64 NumPy, "
-                         f"after an untimed oracle prefill and 1 warm-up round"}
+        v_cpu, _, _, _, sample = cpu_sample(cfg, args.steps, 1, budget)
+        cpu = {"value": v_cpu, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": sample}
 
     clocks = clk.summary()
     if rank == 0:
@@ -499,6 +606,9 @@ def main(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="hyflash", choices=["hyflash", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--prefix", type=int, default=0, help="prefill sweep: prefix length")
+    ap.add_argument("--chunk", type=int, default=128, help="prefill sweep: scan chunk")
+    ap.add_argument("--layers", type=int, default=1, help="prefill sweep: drafter depth")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -506,6 +616,8 @@ def main(argv=None):
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if cfg.rounds == 0:
+        return run_prefill_sweep(args, cfg)
     return run_hyflash(args, cfg)
 
 

@@ -1,0 +1,148 @@
+"""Parity at the full workload shapes (Phi-4-shaped drafter, serving batch,
+long-prefix prefill sweep), compared on outputs the oracle can afford:
+sampled memory heads of long prefixes, every window entry, ring tags and
+positions exactly, and full round parity on a subset of independent requests.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _harness import TOL, Pair, maxnorm_err
+from oracle import hyflash_oracle as O
+from speculative_decoding_drafter_hf_gb300 import Tensor
+from workload import (CONFIGS, make_accepted, make_layer_weights, make_prefix_feats,
+                      make_prefix_lens, make_round_inputs)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from speculative_decoding_drafter_hf_gb300 import build
+    build.build()
+
+
+def sampled_state(lw, cfg, feats64, heads, chunk):
+    """Oracle fold of the listed memory heads only (heads are independent)."""
+    P = cfg.ssm_headdim
+    cols = np.concatenate([np.arange(h * P, (h + 1) * P) for h in heads])
+    T = feats64.shape[0]
+    x = (feats64 @ lw.w_x[:, cols]).reshape(T, len(heads), P)
+    B = feats64 @ lw.w_B
+    dt = O.softplus(feats64 @ lw.w_dt[:, heads] + lw.dt_bias[heads][None, :])
+    h0 = np.zeros((len(heads), P, cfg.d_state))
+    return O.ssm_fold_chunked(h0, x, B, dt, lw.A[heads], chunk)
+
+
+def check_long_prefill(cfg, lens, heads, tokens_max=16384):
+    import speculative_decoding_drafter_hf_gb300 as hf
+    w = make_layer_weights(cfg, 0)
+    lw = O.Weights64.from_any(w)
+    d = hf.Drafter(cfg, len(lens), prefill_tokens_max=tokens_max)
+    d.set_weights(0, w)
+    feats = make_prefix_feats(cfg, lens)
+    d.prefill(feats.cuda(), lens)
+    d.sync()
+    state = d.read(Tensor.STATE)
+    rk = d.read(Tensor.RING_K)
+    tags = d.read(Tensor.RING_TAG)
+    pos = d.read(Tensor.POS)
+    tol = TOL[cfg.dtype]
+    off = 0
+    for b, L in enumerate(lens):
+        f64 = O.to64(feats[off:off + L])
+        off += L
+        assert pos[b] == L
+        ref = O.Context.empty(cfg)
+        first = max(0, L - cfg.window)
+        k, v = O.kv_of(lw, cfg, f64[first:])
+        O.ring_append(ref, cfg, k, v, first)
+        assert np.array_equal(tags[b], ref.tag.astype(np.int32)), f"request {b}: ring tags"
+        valid = ref.tag >= 0
+        e = maxnorm_err(rk[0, b][:, valid, :], ref.ring_k[:, valid, :])
+        assert e <= tol, f"request {b}: ring K err {e:.3e}"
+        if b < 2:  # memory: sampled heads of the first two requests
+            want = sampled_state(lw, cfg, f64, heads, cfg.chunk)
+            for i, hd in enumerate(heads):
+                e = maxnorm_err(state[0, b, hd], want[i])
+                assert e <= tol, f"request {b} head {hd}: state err {e:.3e}"
+    d.close()
+
+
+def test_phi4_full_prefix_32k_sampled_heads():
+    cfg = CONFIGS["phi4_bf16"]
+    check_long_prefill(cfg, [cfg.prefix], heads=[0, 57, 159])
+
+
+def test_phi4_shape_rounds_full_parity():
+    # the Phi-4 widths at a prefix that keeps the oracle cheap (the window is
+    # full, so the round kernels see the same shapes as at 32K)
+    cfg = CONFIGS["phi4_bf16"].replace(prefix=1100)
+    p = Pair(cfg)
+    lens = make_prefix_lens(cfg)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="prefill")
+    for r in range(3):
+        slot, feats = make_round_inputs(cfg, r, p.B)
+        got, ref = p.draft(slot)
+        assert maxnorm_err(got, ref) <= p.tol
+        p.commit(feats, make_accepted(cfg, r, p.B))
+        p.check_context(what=f"round {r}")
+    p.close()
+
+
+@pytest.mark.parametrize("chunk", [64, 256])
+def test_prefill_sweep_batch8_4k(chunk):
+    cfg = CONFIGS["prefill_phi4_sweep"].replace(chunk=chunk)
+    check_long_prefill(cfg, [4096] * 8, heads=[3, 80, 150], tokens_max=4096)
+
+
+def test_prefill_sweep_64k_sampled_heads():
+    cfg = CONFIGS["prefill_phi4_sweep"].replace(batch=1)
+    check_long_prefill(cfg, [65536], heads=[1, 100])
+
+
+def test_serving_batch64_three_layers_subset():
+    """All 64 requests and 3 layers on the GPU; the oracle follows requests
+    0, 31 and 63 (requests are independent, so the subset is exact)."""
+    import speculative_decoding_drafter_hf_gb300 as hf
+    cfg = CONFIGS["serving_qwen3_4b_b64"].replace(prefix_lo=520, prefix_hi=1500)
+    B = cfg.batch
+    weights = [make_layer_weights(cfg, l) for l in range(cfg.n_layers)]
+    d = hf.Drafter(cfg, B)
+    for l, w in enumerate(weights):
+        d.set_weights(l, w)
+    lens = make_prefix_lens(cfg)
+    feats = make_prefix_feats(cfg, lens)
+    d.prefill(feats.cuda(), lens)
+    subset = [0, 31, 63]
+    orc = O.OracleDrafter(cfg, weights, len(subset))
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    sub_feats = torch.cat([feats[starts[b]:starts[b + 1]] for b in subset])
+    orc.prefill([lens[b] for b in subset], sub_feats)
+    tol = TOL[cfg.dtype]
+    for r in range(2):
+        slot, cf = make_round_inputs(cfg, r, B)
+        n = make_accepted(cfg, r, B)
+        out = d.draft(slot.cuda()).float().cpu().numpy()
+        ref = orc.draft(slot[subset])
+        for i, b in enumerate(subset):
+            e = maxnorm_err(out[b], ref[i])
+            assert e <= tol, f"round {r} request {b}: draft err {e:.3e}"
+        d.commit(cf.cuda(), n.cuda())
+        orc.commit(cf[subset], n[subset].numpy())
+        offs = d.read(Tensor.OFFSETS)
+        want = np.concatenate([[0], np.cumsum(n.numpy())]).astype(np.int32)
+        assert np.array_equal(offs[:B + 1], want)
+        state = d.read(Tensor.STATE)
+        pos = d.read(Tensor.POS)
+        tags = d.read(Tensor.RING_TAG)
+        for i, b in enumerate(subset):
+            assert pos[b] == orc.ctx[i][0].pos
+            assert np.array_equal(tags[b], orc.ctx[i][0].tag.astype(np.int32))
+            for l in range(cfg.n_layers):
+                e = maxnorm_err(state[l, b], orc.ctx[i][l].h)
+                assert e <= tol, f"round {r} request {b} layer {l}: state err {e:.3e}"
+    d.close()
