@@ -1,0 +1,73 @@
+"""Host-side logic of bench.py on CPU: the replica (weak-scaling) reduction
+over two gloo ranks, the algorithmic byte counts, and the clock summary."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import torch.distributed as dist
+    ws, r = bench.dist_init("gloo")
+    bench.barrier()
+    # each replica timed a different number of ms and did 10 steps
+    t = bench.max_over_ranks(100.0 + 50.0 * rank)
+    n = bench.sum_over_ranks(10)
+    q.put((r, ws, t, n))
+    dist.destroy_process_group()
+
+
+def test_replica_reduction_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[0] for r in res] == [0, 1]
+    for _, ws, t, n in res:
+        assert ws == 2 and t == 150.0 and n == 20.0  # max time, summed units
+
+
+def test_single_process_reduction_is_identity():
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.sum_over_ranks(7) == 7.0
+
+
+def test_algorithmic_bytes_qwen_shape():
+    from workload import CONFIGS
+    cfg = CONFIGS["qwen3_4b_bf16"]
+    a = bench.algorithmic(cfg, 1, 512, 4.5)
+    # draft weights alone: (Hq*dh + 2*Hkv*dh + N) * D + D * (Hq*dh + Hm*P), bf16
+    w = ((4096 + 2048 + 128) * 2560 + 2560 * (4096 + 5120)) * 2
+    assert w < a["draft_bytes"] < w * 1.1
+    assert a["step_bytes"] == a["draft_bytes"] + a["commit_bytes"]
+
+
+def test_clock_summary_parses_samples(tmp_path):
+    c = bench.ClockSampler(0)
+    c.path = str(tmp_path / "clk.csv")
+    with open(c.path, "w") as f:
+        f.write("0, 1900, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Active\n")
+        f.write("0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active\n")
+    c.proc = object()
+    s = c.summary()
+    assert s["sm_mhz"] == pytest.approx(1985.0) and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
