@@ -51,7 +51,9 @@ struct Args {
   Dims d;
   Plan plan;
   int n_attn;     // attention CTAs = B * Hkv * nsplit
-  int n_mem;      // memory-read CTAs = B * Hm
+  int n_mem;      // memory-read CTAs = B * ceil(Hm / hpc)
+  int hpc;        // memory heads per memory-read CTA
+  int ntile;      // tensor-core path: 64-key window tiles per CTA
   float qscale;   // log2(e) / sqrt(dh)
   const float* proj;    // [B*S, Nd] fp32: Q | K_s | V_s | C_s
   const void* ring_k;   // [B][Hkv][W][dh] of this layer
@@ -397,9 +399,8 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 }
 
 template <typename T>
-__device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
+__device__ __forceinline__ void mem_head(const Args& a, uint8_t* sm, int b, int hd) {
   const Dims& d = a.d;
-  const int b = idx / d.Hm, hd = idx % d.Hm;
   const int S = d.S, N = d.N, P = d.P;
   float* cs = reinterpret_cast<float*>(sm);
   const int tid = threadIdx.x, nthr = blockDim.x;
@@ -440,6 +441,7 @@ __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
   // general shapes: flat float4 walk, reduction across the lanes of a row
   const float4* h = reinterpret_cast<const float4*>(hb);
   const int nq = P * N / 4;
+  __syncthreads();  // cs of the previous head fully consumed
   float4 hv[MEM_QPT];
 #pragma unroll
   for (int u = 0; u < MEM_QPT; ++u) {
@@ -470,46 +472,70 @@ __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
   }
 }
 
+template <typename T>
+__device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
+  const Dims& d = a.d;
+  const int nhb = (d.Hm + a.hpc - 1) / a.hpc;
+  const int b = idx / nhb, hd0 = (idx % nhb) * a.hpc;
+  const int hd1 = min(d.Hm, hd0 + a.hpc);
+  for (int hd = hd0; hd < hd1; ++hd) mem_head<T>(a, sm, b, hd);
+}
+
+
 // ---------------------------------------------------------------------------
-// Tensor-core variant (bf16 rings, head_dim a multiple of 64).
+// Tensor-core variant (bf16 rings, head_dim a multiple of 64): flash decoding.
 //
-// Ring K/V tiles arrive by 2-D TMA in 128-byte-swizzled sub-tiles of 64
-// columns (16-byte chunk c of row r stored at chunk c ^ (r & 7)), so the
-// 8 rows an ldmatrix phase reads fall in distinct banks. Q (pre-scaled) and
-// the probabilities P are written by threads in the same layout. Q.K^T and
-// P.V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate): the tiles are
-// G*7 <= 64 query rows by <= 80 keys, below the 64/128-row minimum of the
-// tcgen05 path. Softmax is fp32; P is rounded to bf16 for the P.V product
-// and the row sums use the rounded values.
+// The valid part of the window of (request b, KV head g) is cut into tiles of
+// KT = 64 keys; the nsplit CTAs of (b, g) (one cluster) take `ntile`
+// consecutive tiles each, and rank 0 also takes the 7 slot keys: every tile
+// buffer holds 64 ring rows (written by TMA) and 16 slot rows (written once
+// by the threads), and rank 0's last tile covers all 80. The split count
+// follows the batch: enough CTAs to fill the GPU at batch 1 (8
+// per cluster), one CTA per (b, g) walking the whole window at large batch.
+// Ring tiles arrive by 2-D TMA through a TC_STAGES-deep ring of shared-memory
+// buffers, in 128-byte-swizzled sub-tiles of 64 columns (16-byte chunk c of
+// row r stored at chunk c ^ (r & 7)); Q (pre-scaled by log2(e)/sqrt(dh)) and
+// the probabilities P are written by threads in the same layout, so every
+// ldmatrix phase reads 8 distinct banks. Per tile: S = Q.K^T on mma.sync
+// m16n8k16 (bf16 in, fp32 accumulate; the tiles are G*7 <= 64 query rows,
+// below the 128-row minimum of the tcgen05 path), an online-softmax update of
+// the running row max m and sum l (fp32, exp2), P rounded to bf16 (the row
+// sums use the rounded values) and O = scale * O + P.V with O held in
+// registers across tiles. One CTA writes O / l; a cluster combines its
+// ranks' (m, l, O) through distributed shared memory in rank order.
+
+constexpr int KT = 64;         // keys per window tile
+constexpr int KTS = KT + 16;   // rows of a tile buffer: window tile + slot rows
+constexpr int TC_STAGES = 2;   // window tiles in flight per CTA
+constexpr int OT_MAX = 8;      // 16x8 O fragments per warp (QR * dh <= 8192)
 
 struct TcLayout {
-  size_t k, v, q, p, s, o, ml, bar, total;
-  int krows, qrows, ksub;
+  size_t kv, q, p, s, ml, bar, total;
+  int qrows, stage;
 };
 
-__host__ __device__ inline TcLayout make_tc_layout(const Dims& d, const Plan& pl) {
+__host__ __device__ inline TcLayout make_tc_layout(const Dims& d) {
   TcLayout m{};
-  m.krows = (pl.jt + d.S + 15) / 16 * 16;
   m.qrows = (d.G * d.S + 15) / 16 * 16;
-  m.ksub = (m.krows + 63) / 64;
   const int dsub = d.dh / 64;
-  size_t off = 0;  // sub-tiles: rows multiple of 16 -> sizes multiple of 2048 B
-  m.k = off;
-  off += (size_t)dsub * m.krows * 128;
-  m.v = off;
-  off += (size_t)dsub * m.krows * 128;
+  m.stage = dsub * KTS * 128;  // one K (or V) tile buffer, multiple of 1024 B
+  size_t off = 0;
+  m.kv = off;  // [stage][K | V]; after the last tile, the partial O for the cluster combine
+  size_t kv = (size_t)TC_STAGES * 2 * m.stage;
+  const size_t o = (size_t)m.qrows * (d.dh + 4) * 4;
+  if (o > kv) kv = (o + 1023) & ~(size_t)1023;
+  off += kv;
   m.q = off;
   off += (size_t)dsub * m.qrows * 128;
-  m.p = off;
-  off += (size_t)m.ksub * m.qrows * 128;
+  m.p = off;  // two 64-column sub-tiles (80 keys)
+  off += (size_t)m.qrows * 2 * 128;
   m.s = off;
-  off += (size_t)m.qrows * (m.krows + 4) * 4;
-  m.o = off;
-  off += (size_t)m.qrows * (d.dh + 4) * 4;
-  m.ml = off;
-  off += (size_t)m.qrows * 2 * 4;
+  off += (size_t)m.qrows * (KTS + 4) * 4;
+  m.ml = off;  // per row: running max, running sum, rescale factor of this tile
+  off += (size_t)m.qrows * 3 * 4;
+  off = (off + 7) & ~(size_t)7;
   m.bar = off;
-  off += 16;
+  off += TC_STAGES * 8;
   const size_t mem_need = (size_t)d.S * d.N * 4;
   m.total = (off > mem_need ? off : mem_need) + 1024;  // + slack to 1024-align the base
   return m;
@@ -553,47 +579,50 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk,
                                             const CUtensorMap* mv, uint8_t* sm_raw, int idx) {
   const Dims& d = a.d;
-  const int nsplit = a.plan.nsplit, JT = a.plan.jt;
+  const int nsplit = a.plan.nsplit;
   const int rank = nsplit > 1 ? (int)cluster_rank() : 0;
   const int pair = idx / nsplit;
   const int kvh = pair % d.Hkv, b = pair / d.Hkv;
   const int S = d.S, G = d.G, R = G * S, dh = d.dh, dsub = dh / 64;
-  const TcLayout L = make_tc_layout(d, a.plan);
-  const int KR = L.krows, QR = L.qrows;
+  const TcLayout L = make_tc_layout(d);
+  const int QR = L.qrows;
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint8_t* kt = sm + L.k;
-  uint8_t* vt = sm + L.v;
+  uint8_t* kv = sm + L.kv;
   uint8_t* qt = sm + L.q;
   uint8_t* pt = sm + L.p;
   float* s = reinterpret_cast<float*>(sm + L.s);
-  float* o = reinterpret_cast<float*>(sm + L.o);
   float* ml = reinterpret_cast<float*>(sm + L.ml);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar);
-  const int SLD = KR + 4, OLD = dh + 4;
+  constexpr int SLD = KTS + 4;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid / 32, lane = tid % 32, nw = nthr / 32;
 
   pdl_wait();
   const long long p = __ldcg(&a.pos[b]);
-  const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);
-  const int j0 = rank * JT;
-  int nring = max(0, min(nv, j0 + JT) - j0);
-  const int nslot = rank == 0 ? S : 0;
+  const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);  // valid ring rows 0..nv-1
+  const int t0 = rank * a.ntile;
+  const int nwt = max(0, min(a.ntile, (nv + KT - 1) / KT - t0));  // ring tiles of this CTA
+  const bool slots = rank == 0;
+  const int nsteps = max(nwt, slots ? 1 : 0);
   const size_t rowbase = (size_t)b * S;
+  const int y_head = (b * d.Hkv + kvh) * d.W;
 
+  auto issue = [&](int i) {  // ring tile i of this CTA into its stage
+    uint64_t* br = &bar[i % TC_STAGES];
+    uint8_t* kd = kv + (size_t)(i % TC_STAGES) * 2 * L.stage;
+    const int y0 = y_head + (t0 + i) * KT;
+    mbar_expect_tx(br, (uint32_t)(2 * dsub * KT * 128));  // K and V, KT rows each
+    for (int u = 0; u < dsub; ++u) {
+      tma_load_2d(kd + (size_t)u * KTS * 128, mk, br, u * 64, y0);
+      tma_load_2d(kd + L.stage + (size_t)u * KTS * 128, mv, br, u * 64, y0);
+    }
+  };
   if (tid == 0) {
-    mbar_init(bar, 1);
+    for (int i = 0; i < TC_STAGES; ++i) mbar_init(&bar[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    if (nring > 0) {
-      const int y0 = (b * d.Hkv + kvh) * d.W + j0;
-      mbar_expect_tx(bar, (uint32_t)(2 * dsub * JT * 128));
-      for (int u = 0; u < dsub; ++u) {
-        tma_load_2d(kt + (size_t)u * KR * 128, mk, bar, u * 64, y0);
-        tma_load_2d(vt + (size_t)u * KR * 128, mv, bar, u * 64, y0);
-      }
-    }
+    for (int i = 0; i < TC_STAGES && i < nwt; ++i) issue(i);
   }
   // Q rows (pre-scaled) as bf16; rows R..QR-1 zero.
   const int c4n = dh / 4;
@@ -609,126 +638,219 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     }
     *reinterpret_cast<uint2*>(qt + sw_chunk(QR, r, c >> 3) + (c & 7) * 2) = w;
   }
-  __syncthreads();  // barrier initialised before anyone waits on it
-  bool ok = true;
-  if (nring > 0) ok = mbar_wait(bar, 0);
-  if (!__syncthreads_and(ok)) {
-    if (tid == 0) {
-      atomicOr(a.err, ERR_TIMEOUT);
-      mbar_wait(bar, 0);  // bounded: let the copies land before the buffers are reused
+  // slot keys / values (rank 0) into rows KT..KT+15 of every tile buffer
+  // (the copies write rows 0..KT-1 only); rows past S zero (finite V for P.V)
+  if (slots)
+    for (int i = tid; i < TC_STAGES * 16 * c4n; i += nthr) {
+      const int stg = i / (16 * c4n), j = (i / c4n) % 16, c = (i % c4n) * 4;
+      uint2 kw = make_uint2(0u, 0u), vw = make_uint2(0u, 0u);
+      if (j < S) {
+        const float* row = a.proj + (rowbase + j) * d.Nd;
+        const float4 kx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
+        const float4 vx =
+            __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
+        kw = make_uint2(pack_bf16x2(kx.x, kx.y), pack_bf16x2(kx.z, kx.w));
+        vw = make_uint2(pack_bf16x2(vx.x, vx.y), pack_bf16x2(vx.z, vx.w));
+      }
+      uint8_t* kd = kv + (size_t)stg * 2 * L.stage;
+      const uint32_t off = sw_chunk(KTS, KT + j, c >> 3) + (c & 7) * 2;
+      *reinterpret_cast<uint2*>(kd + off) = kw;
+      *reinterpret_cast<uint2*>(kd + L.stage + off) = vw;
     }
-    nring = 0;
+  for (int r = tid; r < QR; r += nthr) {
+    ml[r * 3 + 0] = -INFINITY;
+    ml[r * 3 + 1] = 0.f;
+    ml[r * 3 + 2] = 0.f;
   }
-  const int nk = nring + nslot;
-  // slot keys/values after the ring rows; rows nk..KR-1 zero (finite V for P.V)
-  for (int i = tid; i < (KR - nring) * c4n; i += nthr) {
-    const int j = nring + i / c4n, c = (i % c4n) * 4;
-    uint2 kw = make_uint2(0u, 0u), vw = make_uint2(0u, 0u);
-    if (j < nk) {
-      const float* row = a.proj + (rowbase + (j - nring)) * d.Nd;
-      const float4 kx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
-      const float4 vx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
-      kw = make_uint2(pack_bf16x2(kx.x, kx.y), pack_bf16x2(kx.z, kx.w));
-      vw = make_uint2(pack_bf16x2(vx.x, vx.y), pack_bf16x2(vx.z, vx.w));
-    }
-    const uint32_t off = sw_chunk(KR, j, c >> 3) + (c & 7) * 2;
-    *reinterpret_cast<uint2*>(kt + off) = kw;
-    *reinterpret_cast<uint2*>(vt + off) = vw;
-  }
-  __syncthreads();
 
   const int g8 = lane >> 2, t4 = lane & 3;
-  const uint32_t kb = smem_u32(kt), vb = smem_u32(vt), qb = smem_u32(qt), pb = smem_u32(pt);
-  // S = Q K^T
-  {
-    const int MT = QR / 16, NT = KR / 8, KS = dh / 16;
-    for (int t = warp; t < MT * NT; t += nw) {
-      const int mt = t / NT, nt = t % NT;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a0, a1, a2, a3, b0, b1;
-        ldsm_x4(qb + sw_chunk(QR, mt * 16 + (lane & 15), ks * 2 + (lane >> 4)), a0, a1, a2, a3);
-        ldsm_x2(kb + sw_chunk(KR, nt * 8 + (lane & 7), ks * 2 + ((lane >> 3) & 1)), b0, b1);
-        mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+  const int MT = QR / 16, NTD = dh / 8;
+  const int n_ot = MT * NTD;  // O fragments, warp w owns w, w + nw, ...
+  float oacc[OT_MAX][4];
+#pragma unroll
+  for (int k = 0; k < OT_MAX; ++k) oacc[k][0] = oacc[k][1] = oacc[k][2] = oacc[k][3] = 0.f;
+  const uint32_t qb = smem_u32(qt), pb = smem_u32(pt);
+  int done = 0;  // ring tiles consumed
+  bool aborted = false;
+  __syncthreads();  // barriers initialised, Q / slot rows / row state written
+
+  for (int i = 0; i < nsteps; ++i) {
+    const bool ring = i < nwt;                    // a window tile arrives in stage i % STAGES
+    const bool with_slots = slots && i == nsteps - 1;
+    const int kr0 = ring ? 0 : KT;                // first key row of the step
+    const int rows = (ring ? KT : 0) + (with_slots ? 16 : 0);
+    const int nvr = ring ? min(KT, nv - (t0 + i) * KT) : 0;  // valid window rows
+    const int nsk = with_slots ? S : 0;                       // valid slot rows
+    uint8_t* kt = kv + (size_t)(ring ? i % TC_STAGES : 0) * 2 * L.stage;
+    uint8_t* vt = kt + L.stage;
+    if (ring) {
+      const bool ok = mbar_wait(&bar[i % TC_STAGES], (uint32_t)((i / TC_STAGES) & 1));
+      if (!__syncthreads_and(ok)) {
+        aborted = true;
+        break;
       }
-      const int r = mt * 16 + g8, col = nt * 8 + 2 * t4;
-      s[r * SLD + col] = c[0];
-      s[r * SLD + col + 1] = c[1];
-      s[(r + 8) * SLD + col] = c[2];
-      s[(r + 8) * SLD + col + 1] = c[3];
+      // window rows past the valid ones: V zeroed (P is zero there, V must be finite)
+      if (nvr < KT)
+        for (int e = tid; e < (KT - nvr) * c4n; e += nthr) {
+          const int j = nvr + e / c4n, c = (e % c4n) * 4;
+          *reinterpret_cast<uint2*>(vt + sw_chunk(KTS, j, c >> 3) + (c & 7) * 2) =
+              make_uint2(0u, 0u);
+        }
+      done = i + 1;
     }
-  }
-  __syncthreads();
-  // softmax rows -> P (bf16, keys >= nk and rows >= R zero), (max, sum) per row
-  for (int r = warp; r < QR; r += nw) {
-    float m = -INFINITY;
-    if (r < R)
-      for (int j = lane; j < nk; j += 32) m = fmaxf(m, s[r * SLD + j]);
-    m = warp_max(m);
-    float l = 0.f;
-    for (int j0p = 0; j0p < KR; j0p += 64) {
-      const int j = j0p + 2 * lane;  // two keys per lane per step
-      if (j < KR) {
-        float e0 = 0.f, e1 = 0.f;
-        if (r < R && j < nk) e0 = exp2f(s[r * SLD + j] - m);
-        if (r < R && j + 1 < nk) e1 = exp2f(s[r * SLD + j + 1] - m);
-        const uint32_t w = pack_bf16x2(e0, e1);
-        const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&w);
-        const float2 back = __bfloat1622float2(h2);
-        l += back.x + back.y;
-        *reinterpret_cast<uint32_t*>(pt + sw_chunk(QR, r, j >> 3) + (j & 7) * 2) = w;
+    // S = Q K^T over this tile
+    {
+      const uint32_t kb = smem_u32(kt);
+      const int NTK = rows / 8, KS = dh / 16;
+      for (int t = warp; t < MT * NTK; t += nw) {
+        const int mt = t / NTK, nt = t % NTK;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3, b0, b1;
+          ldsm_x4(qb + sw_chunk(QR, mt * 16 + (lane & 15), ks * 2 + (lane >> 4)), a0, a1, a2, a3);
+          ldsm_x2(kb + sw_chunk(KTS, kr0 + nt * 8 + (lane & 7), ks * 2 + ((lane >> 3) & 1)), b0,
+                  b1);
+          mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+        }
+        const int r = mt * 16 + g8, col = nt * 8 + 2 * t4;
+        *reinterpret_cast<float2*>(&s[r * SLD + col]) = make_float2(c[0], c[1]);
+        *reinterpret_cast<float2*>(&s[(r + 8) * SLD + col]) = make_float2(c[2], c[3]);
       }
     }
-    l = warp_sum(l);
-    if (lane == 0) {
-      ml[r * 2 + 0] = m;
-      ml[r * 2 + 1] = l;
+    __syncthreads();  // scores complete; P.V of the previous step done everywhere
+    if (tid == 0 && ring && i >= 1 && i + TC_STAGES - 1 < nwt) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(i + TC_STAGES - 1);  // into the stage of tile i - 1, free now
     }
-  }
-  __syncthreads();
-  // O = P V
-  {
-    const int MT = QR / 16, NT = dh / 8, KS = KR / 16;
-    for (int t = warp; t < MT * NT; t += nw) {
-      const int mt = t / NT, nt = t % NT;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a0, a1, a2, a3, b0, b1;
-        ldsm_x4(pb + sw_chunk(QR, mt * 16 + (lane & 15), ks * 2 + (lane >> 4)), a0, a1, a2, a3);
-        ldsm_x2_t(vb + sw_chunk(KR, ks * 16 + (lane & 15), nt), b0, b1);
-        mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+    // online softmax: new max, rescale factor, P (bf16), running sum.
+    // Column c of the step is key row kr0 + c of the tile buffer.
+    for (int r = warp; r < QR; r += nw) {
+      float x[4];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int c = 64 * h + 2 * lane + q, j = kr0 + c;
+          const bool valid = r < R && c < rows && (j < nvr || (j >= KT && j < KT + nsk));
+          x[2 * h + q] = valid ? s[r * SLD + c] : -INFINITY;
+          mt = fmaxf(mt, x[2 * h + q]);
+        }
       }
-      const int r = mt * 16 + g8, col = nt * 8 + 2 * t4;
-      o[r * OLD + col] = c[0];
-      o[r * OLD + col + 1] = c[1];
-      o[(r + 8) * OLD + col] = c[2];
-      o[(r + 8) * OLD + col + 1] = c[3];
+      const float m_old = ml[r * 3 + 0];
+      const float m_new = fmaxf(m_old, warp_max(mt));
+      const float sc = (r < R && m_old != -INFINITY) ? exp2f(m_old - m_new) : 0.f;
+      float lsum = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = 64 * h + 2 * lane;
+        if (c < rows) {
+          const float e0 = x[2 * h] == -INFINITY ? 0.f : exp2f(x[2 * h] - m_new);
+          const float e1 = x[2 * h + 1] == -INFINITY ? 0.f : exp2f(x[2 * h + 1] - m_new);
+          const uint32_t w = pack_bf16x2(e0, e1);
+          const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+          lsum += back.x + back.y;
+          *reinterpret_cast<uint32_t*>(pt + sw_chunk(QR, r, c >> 3) + (c & 7) * 2) = w;
+        }
+      }
+      lsum = warp_sum(lsum);
+      if (lane == 0) {
+        ml[r * 3 + 0] = r < R ? m_new : -INFINITY;
+        ml[r * 3 + 1] = ml[r * 3 + 1] * sc + lsum;
+        ml[r * 3 + 2] = sc;
+      }
+    }
+    __syncthreads();
+    // O = scale * O + P V
+    {
+      const uint32_t vb = smem_u32(vt);
+      const int KS = rows / 16;
+#pragma unroll
+      for (int k = 0; k < OT_MAX; ++k) {
+        const int t = warp + k * nw;
+        if (t < n_ot) {
+          const int mt = t / NTD, nt = t % NTD;
+          const int r0 = mt * 16 + g8;
+          const float sc0 = ml[r0 * 3 + 2], sc1 = ml[(r0 + 8) * 3 + 2];
+          float* c = oacc[k];
+          c[0] *= sc0;
+          c[1] *= sc0;
+          c[2] *= sc1;
+          c[3] *= sc1;
+          for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a0, a1, a2, a3, b0, b1;
+            ldsm_x4(pb + sw_chunk(QR, mt * 16 + (lane & 15), ks * 2 + (lane >> 4)), a0, a1, a2,
+                    a3);
+            ldsm_x2_t(vb + sw_chunk(KTS, kr0 + ks * 16 + (lane & 15), nt), b0, b1);
+            mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
+          }
+        }
+      }
     }
   }
 
-  __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
-  if (nsplit == 1) {
-    __syncthreads();
-    for (int i = tid; i < R * c4n; i += nthr) {
-      const int r = i / c4n, c = (i % c4n) * 4, g = r / S, sl = r % S;
-      const float inv = 1.f / ml[r * 2 + 1];
-      const float4 x = *reinterpret_cast<const float4*>(&o[r * OLD + c]);
-      __nv_bfloat16* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
-      *reinterpret_cast<uint2*>(dst) =
-          make_uint2(pack_bf16x2(x.x * inv, x.y * inv), pack_bf16x2(x.z * inv, x.w * inv));
+  if (aborted) {
+    // a tile copy never completed: report, let the copies in flight land
+    // (bounded) before the shared memory is released, write nothing
+    if (tid == 0) {
+      atomicOr(a.err, ERR_TIMEOUT);
+      const int issued = min(nwt, max(TC_STAGES, done + TC_STAGES - 1));
+      for (int i = done; i < issued; ++i)
+        mbar_wait(&bar[i % TC_STAGES], (uint32_t)((i / TC_STAGES) & 1));
+    }
+    if (nsplit > 1) {
+      cluster_sync_all();  // matches the two cluster barriers of the combine
+      cluster_sync_all();
     }
     return;
   }
+
+  __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
+  __syncthreads();  // last row sums visible; every read of the tile buffers done
+  if (nsplit == 1) {
+#pragma unroll
+    for (int k = 0; k < OT_MAX; ++k) {
+      const int t = warp + k * nw;
+      if (t < n_ot) {
+        const int mt = t / NTD, nt = t % NTD, col = nt * 8 + 2 * t4;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int r = mt * 16 + g8 + 8 * h2;
+          if (r < R) {
+            const int g = r / S, sl = r % S;
+            const float inv = 1.f / ml[r * 3 + 1];
+            __nv_bfloat16* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + col;
+            *reinterpret_cast<uint32_t*>(dst) =
+                pack_bf16x2(oacc[k][2 * h2] * inv, oacc[k][2 * h2 + 1] * inv);
+          }
+        }
+      }
+    }
+    return;
+  }
+  // partial O (unnormalised) into the tile buffers, then the cluster combine
+  float* o = reinterpret_cast<float*>(kv);
+  const int OLD = dh + 4;
+#pragma unroll
+  for (int k = 0; k < OT_MAX; ++k) {
+    const int t = warp + k * nw;
+    if (t < n_ot) {
+      const int mt = t / NTD, nt = t % NTD, col = nt * 8 + 2 * t4;
+      const int r = mt * 16 + g8;
+      *reinterpret_cast<float2*>(&o[r * OLD + col]) = make_float2(oacc[k][0], oacc[k][1]);
+      *reinterpret_cast<float2*>(&o[(r + 8) * OLD + col]) = make_float2(oacc[k][2], oacc[k][3]);
+    }
+  }
   cluster_sync_all();
   const int my_rows = (R - rank + nsplit - 1) / nsplit;
-  for (int i = tid; i < my_rows * c4n; i += nthr) {
-    const int r = rank + (i / c4n) * nsplit, c = (i % c4n) * 4, g = r / S, sl = r % S;
+  for (int e = tid; e < my_rows * c4n; e += nthr) {
+    const int r = rank + (e / c4n) * nsplit, c = (e % c4n) * 4, g = r / S, sl = r % S;
     float mp[MAX_SPLIT], lp[MAX_SPLIT];
     float M = -INFINITY;
 #pragma unroll
     for (int sp = 0; sp < MAX_SPLIT; ++sp) {
       if (sp < nsplit) {
-        const uint32_t ad = peer_addr(&ml[r * 2], (uint32_t)sp);
+        const uint32_t ad = peer_addr(&ml[r * 3], (uint32_t)sp);
         mp[sp] = ld_peer_f(ad);
         lp[sp] = ld_peer_f(ad + 4);
         M = fmaxf(M, mp[sp]);
@@ -785,53 +907,47 @@ __global__ void __launch_bounds__(THREADS) attn_cluster_kernel(Args a) {
 
 }  // namespace
 
-bool attn_uses_tc(const Dims& d, int dtype) { return dtype == HF_BF16 && d.dh % 64 == 0; }
-
-int attn_tile_rows(const Dims& d) { return make_plan(d.W).jt; }
-
-size_t attn_cluster_smem(const Dims& d, int esize) {
-  const size_t cuda_core = make_layout(d, make_plan(d.W), esize).total;
-  if (esize == 2 && d.dh % 64 == 0) {
-    const size_t tc = make_tc_layout(d, make_plan(d.W)).total;
-    return tc > cuda_core ? tc : cuda_core;
-  }
-  return cuda_core;
+bool attn_uses_tc(const Dims& d, int dtype) {
+  const int qrows = (d.G * d.S + 15) / 16 * 16;
+  return dtype == HF_BF16 && d.dh % 64 == 0 && qrows * d.dh <= OT_MAX * 8 * 128;
 }
 
-template <typename T, int E>
-cudaError_t configure_one(int smem) {
-  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<T, E>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+int attn_tile_rows(const Dims&) { return KT; }
+
+size_t attn_cluster_smem(const Dims& d, int esize) {
+  if (esize == 2 && attn_uses_tc(d, HF_BF16)) return make_tc_layout(d).total;
+  return make_layout(d, make_plan(d.W), esize).total;
+}
+
+constexpr int kMaxSmem = 232448;  // opt-in shared memory per CTA
+
+template <typename K>
+cudaError_t configure_kernel(K kernel) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_cluster_kernel<T, E>,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
 template <typename T>
-cudaError_t configure_dtype(int smem) {
-  cudaError_t e = configure_one<T, 2>(smem);
-  if (e == cudaSuccess) e = configure_one<T, 4>(smem);
-  if (e == cudaSuccess) e = configure_one<T, 8>(smem);
-  if (e == cudaSuccess) e = configure_one<T, 16>(smem);
+cudaError_t configure_dtype() {
+  cudaError_t e = configure_kernel(attn_cluster_kernel<T, 2>);
+  if (e == cudaSuccess) e = configure_kernel(attn_cluster_kernel<T, 4>);
+  if (e == cudaSuccess) e = configure_kernel(attn_cluster_kernel<T, 8>);
+  if (e == cudaSuccess) e = configure_kernel(attn_cluster_kernel<T, 16>);
   return e;
 }
 
-cudaError_t configure_attn_cluster(const Dims& d) {
-  static int configured = 0;
-  int smem = (int)attn_cluster_smem(d, 4);
-  const int smem_bf16 = (int)attn_cluster_smem(d, 2);
-  if (smem_bf16 > smem) smem = smem_bf16;
-  if (smem <= configured) return cudaSuccess;
-  cudaError_t e = configure_dtype<float>(smem);
-  if (e == cudaSuccess) e = configure_dtype<__nv_bfloat16>(smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess) configured = smem;
+// Every variant may use up to the opt-in maximum; the launch passes the
+// layout's own size, which sets the occupancy.
+cudaError_t configure_attn_cluster(const Dims&) {
+  static bool configured = false;
+  if (configured) return cudaSuccess;
+  cudaError_t e = configure_dtype<float>();
+  if (e == cudaSuccess) e = configure_dtype<__nv_bfloat16>();
+  if (e == cudaSuccess) e = configure_kernel(attn_tc_kernel);
+  if (e == cudaSuccess) configured = true;
   return e;
 }
 
@@ -846,17 +962,40 @@ cudaError_t launch_typed(const cudaLaunchConfig_t& cfg, const Args& a) {
   return cudaErrorInvalidValue;
 }
 
+// Split of the tensor-core path: about two CTAs per SM over the batch's
+// (request, KV head) pairs, at most 8 (one cluster) and no more than the
+// window has tiles; every rank gets the same number of tiles.
+static Plan make_tc_plan(const Dims& d, int B, int num_sms, int* ntile) {
+  const int nwin = (d.W + KT - 1) / KT;
+  const int pairs = B * d.Hkv;
+  int ns = (2 * num_sms + pairs - 1) / pairs;
+  ns = ns < 1 ? 1 : (ns > MAX_SPLIT ? MAX_SPLIT : ns);
+  if (ns > nwin) ns = nwin;
+  *ntile = (nwin + ns - 1) / ns;
+  Plan p;
+  p.nsplit = (nwin + *ntile - 1) / *ntile;
+  p.jt = *ntile * KT;
+  return p;
+}
+
 cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
                                 const float* state, void* mix, const CUtensorMap* mk,
-                                const CUtensorMap* mv, int32_t* err, cudaStream_t st,
+                                const CUtensorMap* mv, int32_t* err, int num_sms, cudaStream_t st,
                                 int* launches) {
   if (B <= 0) return cudaSuccess;
+  const bool tc = attn_uses_tc(d, dtype) && mk && mv;
   Args a{};
   a.d = d;
-  a.plan = make_plan(d.W);
+  if (tc)
+    a.plan = make_tc_plan(d, B, num_sms, &a.ntile);
+  else
+    a.plan = make_plan(d.W);
   a.n_attn = B * d.Hkv * a.plan.nsplit;
-  a.n_mem = B * d.Hm;
+  // memory-read CTAs: one head each up to ~8 CTAs per SM, then several
+  a.hpc = (B * d.Hm + 8 * num_sms - 1) / (8 * num_sms);
+  if (a.hpc < 1) a.hpc = 1;
+  a.n_mem = B * ((d.Hm + a.hpc - 1) / a.hpc);
   a.qscale = 1.4426950408889634f / sqrtf((float)d.dh);
   a.proj = proj;
   a.ring_k = ring_k;
@@ -870,8 +1009,7 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(total);
   cfg.blockDim = dim3(THREADS);
-  const bool tc = attn_uses_tc(d, dtype) && mk && mv;
-  cfg.dynamicSmemBytes = tc ? make_tc_layout(d, a.plan).total
+  cfg.dynamicSmemBytes = tc ? make_tc_layout(d).total
                             : make_layout(d, a.plan, dtype == HF_F32 ? 4 : 2).total;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];

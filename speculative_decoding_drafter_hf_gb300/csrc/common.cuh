@@ -315,8 +315,8 @@ bool attn_uses_tc(const Dims& d, int dtype);
 cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
                                 const float* state, void* mix, const CUtensorMap* mk,
-                                const CUtensorMap* mv, int32_t* err, cudaStream_t st,
-                                int* launches);
+                                const CUtensorMap* mv, int32_t* err, int num_sms,
+                                cudaStream_t st, int* launches);
 
 // Commit state step, all layers: validates the accepted counts (error word),
 // writes the packed offsets (exclusive scan of the valid counts) and the ring

@@ -563,8 +563,8 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
       cudaError_t e = hf::launch_attn_cluster(h->cfg.dtype, d, batch, h->proj,
                                               bptr(h->ring_k, l * ring_ls),
                                               bptr(h->ring_v, l * ring_ls), h->pos,
-                                              h->state + l * state_ls, h->mix, mk, mv, h->err, st,
-                                              &sc.count);
+                                              h->state + l * state_ls, h->mix, mk, mv, h->err,
+                                              h->num_sms, st, &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
     }
     Epi e2 = epi_base(h);

@@ -160,11 +160,17 @@ def test_serving_shape_bf16_subset():
 def test_draft_steps_individually(name, lens):
     """Rows a4 (slot projections), a5 (attention) and a6 (memory read) on
     their own, read back from the handle after one draft."""
-    from oracle import hyflash_oracle as O
     cfg = CONFIGS[name].replace(batch=len(lens))
     p = Pair(cfg)
     p.prefill(lens, make_prefix_feats(cfg, lens))
-    slot, _ = make_round_inputs(cfg, 3, p.B)
+    check_draft_parts(p, 3)
+    p.close()
+
+
+def check_draft_parts(p: Pair, round_: int):
+    from oracle import hyflash_oracle as O
+    cfg = p.cfg
+    slot, _ = make_round_inputs(cfg, round_, p.B)
     got, ref = p.draft(slot)
     S, QD, KVD = cfg.block, cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
     proj = p.gpu.read(Tensor.DRAFT_PROJ)
@@ -186,6 +192,36 @@ def test_draft_steps_individually(name, lens):
             e = maxnorm_err(g, r)
             assert e <= p.tol, f"request {b}: {what} err {e:.3e}"
     assert maxnorm_err(got, ref) <= p.tol
+
+
+# bf16 attention shapes away from the headline ones: windows that are not a
+# multiple of the 64-key tile, 1..8 query heads per KV head, head_dim 64 /
+# 128 / 256, empty / partial / wrapped windows, and batches that give one CTA
+# per (request, KV head) walking several tiles as well as multi-CTA clusters.
+ATTN_SHAPES = {
+    "w100_dh64_g4": (dict(d_model=512, n_q_heads=8, n_kv_heads=2, head_dim=64, window=100,
+                          ssm_heads=8, ssm_headdim=64, d_state=64), [0, 37, 100, 250]),
+    "w200_dh128_g8": (dict(d_model=1024, n_q_heads=16, n_kv_heads=2, head_dim=128, window=200,
+                           ssm_heads=8, ssm_headdim=64, d_state=64), [150, 1000]),
+    "w70_dh256_g2": (dict(d_model=512, n_q_heads=4, n_kv_heads=2, head_dim=256, window=70,
+                          ssm_heads=4, ssm_headdim=32, d_state=64), [69, 71, 500]),
+    "w300_b80_one_cta": (dict(d_model=256, n_q_heads=8, n_kv_heads=4, head_dim=64, window=300,
+                              ssm_heads=4, ssm_headdim=32, d_state=32),
+                         [(37 * i) % 420 for i in range(80)]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ATTN_SHAPES))
+def test_attention_shapes_bf16(name):
+    dims, lens = ATTN_SHAPES[name]
+    cfg = CONFIGS["qwen3_4b_bf16"].replace(batch=len(lens), **dims)
+    p = Pair(cfg)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    check_draft_parts(p, 1)
+    n = make_accepted(cfg, 1, p.B)
+    _, feats = make_round_inputs(cfg, 1, p.B)
+    p.commit(feats, n)
+    check_draft_parts(p, 2)
     p.close()
 
 
