@@ -376,6 +376,8 @@ def run_hyflash(args, cfg):
     for l in range(cfg.n_layers):
         drafter.set_weights(l, make_layer_weights(cfg, l))
     lens = make_prefix_lens(cfg, seed=0)[:batch]
+    if args.prefix_max:  # smaller prefill (e.g. for profiling); rounds unchanged once windows fill
+        lens = [min(L, args.prefix_max) for L in lens]
     total = sum(lens)
     feats = prefix_features(cfg, lens, seed, dev)
     stream = torch.cuda.current_stream()
@@ -428,9 +430,17 @@ def run_hyflash(args, cfg):
         drafter.draft(st_slot, out)
         drafter.commit(st_feat, st_cnt)
 
+    # eager warm-up rounds, marked with NVTX ranges ("draft", "commit") so a
+    # profiler can select one round's launches by range
+    nvtx = torch.cuda.nvtx
     for r in range(args.warmup):
         stage(r)
-        round_calls()
+        nvtx.range_push("draft")
+        drafter.draft(st_slot, out)
+        nvtx.range_pop()
+        nvtx.range_push("commit")
+        drafter.commit(st_feat, st_cnt)
+        nvtx.range_pop()
     drafter.sync()
 
     def capture():
@@ -571,7 +581,10 @@ def run_hyflash(args, cfg):
             "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic",
-            "config": {"workload": cfg.name, "batch_per_gpu": batch, "prefix": cfg.prefix,
+            "config": {"workload": cfg.name, "batch_per_gpu": batch,
+                       "prefix": (f"log-uniform [{cfg.prefix_lo}, {cfg.prefix_hi}]"
+                                  if cfg.prefix_lo else cfg.prefix),
+                       "prefix_cap": args.prefix_max or None,
                        "layers": cfg.n_layers, "window": cfg.window, "block": cfg.block,
                        "l2": f"flushed between steps ({2 * l2 >> 20} MiB write, untimed)",
                        "timing": "CUDA graph of one round replayed per step; CUDA events; "
@@ -607,6 +620,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="hyflash", choices=["hyflash", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--prefix", type=int, default=0, help="prefill sweep: prefix length")
+    ap.add_argument("--prefix-max", type=int, default=0,
+                    help="round configs: cap every request's prefix (0: the workload's own)")
     ap.add_argument("--chunk", type=int, default=128, help="prefill sweep: scan chunk")
     ap.add_argument("--layers", type=int, default=1, help="prefill sweep: drafter depth")
     args = ap.parse_args(argv)

@@ -53,6 +53,7 @@ struct Args {
   int n_attn;     // attention CTAs = B * Hkv * nsplit
   int n_mem;      // memory-read CTAs = B * ceil(Hm / hpc)
   int hpc;        // memory heads per memory-read CTA
+  int mem_tc;     // 1: memory read on the tensor cores (tf32 mma.sync)
   int ntile;      // tensor-core path: 64-key window tiles per CTA
   float qscale;   // log2(e) / sqrt(dh)
   const float* proj;    // [B*S, Nd] fp32: Q | K_s | V_s | C_s
@@ -62,6 +63,9 @@ struct Args {
   const float* state;   // [B][Hm][P][N] of this layer
   void* mix;            // [B*S, Nz]: O at columns [0, Hq*dh), y at [Hq*dh, Nz)
   int32_t* err;
+  int early;      // 1: ring, positions and state are final at launch (the previous
+                  // launch signalled its dependents after its own dependency wait):
+                  // read them before waiting; only the projections need the wait
 };
 
 struct Layout {
@@ -490,53 +494,108 @@ __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
 // consecutive tiles each, and rank 0 also takes the 7 slot keys: every tile
 // buffer holds 64 ring rows (written by TMA) and 16 slot rows (written once
 // by the threads), and rank 0's last tile covers all 80. The split count
-// follows the batch: enough CTAs to fill the GPU at batch 1 (8
-// per cluster), one CTA per (b, g) walking the whole window at large batch.
-// Ring tiles arrive by 2-D TMA through a TC_STAGES-deep ring of shared-memory
-// buffers, in 128-byte-swizzled sub-tiles of 64 columns (16-byte chunk c of
-// row r stored at chunk c ^ (r & 7)); Q (pre-scaled by log2(e)/sqrt(dh)) and
-// the probabilities P are written by threads in the same layout, so every
-// ldmatrix phase reads 8 distinct banks. Per tile: S = Q.K^T on mma.sync
-// m16n8k16 (bf16 in, fp32 accumulate; the tiles are G*7 <= 64 query rows,
-// below the 128-row minimum of the tcgen05 path), an online-softmax update of
-// the running row max m and sum l (fp32, exp2), P rounded to bf16 (the row
-// sums use the rounded values) and O = scale * O + P.V with O held in
-// registers across tiles. One CTA writes O / l; a cluster combines its
-// ranks' (m, l, O) through distributed shared memory in rank order.
+// follows the batch: enough CTAs to fill the GPU at batch 1 (8 per cluster),
+// one CTA per (b, g) walking the whole window at large batch. Ring tiles
+// arrive by 2-D TMA through a TC_STAGES-deep ring of shared-memory buffers,
+// in 128-byte-swizzled sub-tiles of 64 columns (16-byte chunk c of row r at
+// chunk c ^ (r & 7)); Q (pre-scaled by log2(e)/sqrt(dh)) is written by the
+// threads in the same layout, so every ldmatrix phase reads 8 distinct banks.
+//
+// Warp (m, k, h) owns query rows 16m..16m+15, the k-th group of KW keys of
+// every tile and the h-th part of the head dimension of O. It runs its own
+// flash-decoding loop: S = Q.K^T on mma.sync m16n8k16 (bf16 in, fp32
+// accumulate; G*7 <= 64 query rows are below the 128-row minimum of the
+// tcgen05 path), an online-softmax update of its row max m and sum l in
+// registers (fp32, exp2), P rounded to bf16 and reused in registers as the
+// A operand of O = scale * O + P.V (the row sums use the rounded values).
+// Warps never wait on each other inside the loop; at the end the key groups
+// are merged through shared memory, and a cluster merges its ranks' (m, l, O)
+// through distributed shared memory in rank order.
 
 constexpr int KT = 64;         // keys per window tile
 constexpr int KTS = KT + 16;   // rows of a tile buffer: window tile + slot rows
 constexpr int TC_STAGES = 2;   // window tiles in flight per CTA
-constexpr int OT_MAX = 8;      // 16x8 O fragments per warp (QR * dh <= 8192)
+constexpr int OW_MAX = 16;     // 16x8 O fragments per warp (head-dim part <= 128)
+
+// Warp roles of the tensor-core attention for a shape.
+struct TcWarps {
+  int mt, dp, kg, kw, dw;  // m-tiles, head-dim parts, key groups, keys / group, O columns / warp
+};
+__host__ __device__ inline TcWarps tc_warps(const Dims& d) {
+  TcWarps w;
+  w.mt = (d.G * d.S + 15) / 16;
+  w.dp = d.dh > 128 ? d.dh / 128 : 1;
+  w.kg = 8 / (w.mt * w.dp);
+  if (w.kg > 4) w.kg = 4;
+  if (w.kg < 1) w.kg = 1;
+  w.kw = KT / w.kg;
+  w.dw = d.dh / w.dp;
+  return w;
+}
+
+// Memory read on the tensor cores: y[s, p] = sum_n h[p, n] C[s, n] per
+// (request, memory head) as a [P x N] x [N x 8] product on mma.sync
+// m16n8k8 tf32 (fp32 accumulate; h and C rounded to tf32 with
+// round-to-nearest, relative error 2^-11, below the bf16 rounding of the
+// output). Warp (m-tile, k-part) loads its 16 state rows x (N / parts)
+// columns straight into registers as 16-byte loads (every 32-byte sector
+// fully used), the whole head in flight at once; the next head's loads are
+// issued as soon as the current head's fragments are consumed. Within each
+// group of 16 state columns lane t holds columns 4t..4t+3 and serves two
+// k-steps (columns 4t, 4t+1 as logical k = t, t + 4, then 4t+2, 4t+3): the
+// same permutation on both operands, so the sum is unchanged.
+constexpr int MEM_G16 = 8;  // 16-column groups per warp (N <= 128)
+
+__host__ __device__ inline bool mem_tc_ok(const Dims& d) {
+  return d.P % 16 == 0 && d.P <= 128 && d.N % 16 == 0 && d.N <= 128 && d.S <= 8;
+}
+__host__ __device__ inline int mem_ksplit(const Dims& d) {
+  const int mt = d.P / 16;
+  int ks = mt >= 8 ? 1 : 8 / mt;
+  while (ks > 1 && (d.N / 16) % ks) --ks;
+  return ks;
+}
+__host__ __device__ inline size_t mem_tc_bytes(const Dims& d) {
+  return (size_t)mem_ksplit(d) * d.P * 8 * 4;
+}
 
 struct TcLayout {
-  size_t kv, q, p, s, ml, bar, total;
+  size_t kv, okg, o, q, ml, mlk, bar, total;
   int qrows, stage;
 };
 
 __host__ __device__ inline TcLayout make_tc_layout(const Dims& d) {
   TcLayout m{};
-  m.qrows = (d.G * d.S + 15) / 16 * 16;
+  const TcWarps w = tc_warps(d);
+  m.qrows = w.mt * 16;
   const int dsub = d.dh / 64;
   m.stage = dsub * KTS * 128;  // one K (or V) tile buffer, multiple of 1024 B
   size_t off = 0;
-  m.kv = off;  // [stage][K | V]; after the last tile, the partial O for the cluster combine
-  size_t kv = (size_t)TC_STAGES * 2 * m.stage;
+  // [stage][K | V]; after the last tile: the key groups' partial O, then the
+  // CTA's partial O for the cluster combine
+  m.kv = off;
+  const size_t og = (size_t)w.kg * m.qrows * (d.dh + 4) * 4;
   const size_t o = (size_t)m.qrows * (d.dh + 4) * 4;
-  if (o > kv) kv = (o + 1023) & ~(size_t)1023;
+  size_t kv = (size_t)TC_STAGES * 2 * m.stage;
+  if (og + o > kv) kv = og + o;
+  kv = (kv + 1023) & ~(size_t)1023;
+  m.okg = off;
+  m.o = off + og;
   off += kv;
   m.q = off;
   off += (size_t)dsub * m.qrows * 128;
-  m.p = off;  // two 64-column sub-tiles (80 keys)
-  off += (size_t)m.qrows * 2 * 128;
-  m.s = off;
-  off += (size_t)m.qrows * (KTS + 4) * 4;
-  m.ml = off;  // per row: running max, running sum, rescale factor of this tile
-  off += (size_t)m.qrows * 3 * 4;
+  m.ml = off;  // per row: the CTA's max and sum (cluster combine)
+  off += (size_t)m.qrows * 2 * 4;
+  m.mlk = off;  // per key group and row: max and sum
+  off += (size_t)w.kg * m.qrows * 2 * 4;
   off = (off + 7) & ~(size_t)7;
   m.bar = off;
   off += TC_STAGES * 8;
-  const size_t mem_need = (size_t)d.S * d.N * 4;
+  size_t mem_need = (size_t)d.S * d.N * 4;
+  if (mem_tc_ok(d)) {
+    const size_t t = mem_tc_bytes(d);
+    if (t > mem_need) mem_need = t;
+  }
   m.total = (off > mem_need ? off : mem_need) + 1024;  // + slack to 1024-align the base
   return m;
 }
@@ -550,16 +609,6 @@ __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, 
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(a));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r0), "=r"(r1)
-               : "r"(a));
-}
-__device__ __forceinline__ void ldsm_x2_t(uint32_t a, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r0), "=r"(r1)
                : "r"(a));
 }
 __device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
@@ -576,6 +625,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a));
+}
+
 __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk,
                                             const CUtensorMap* mv, uint8_t* sm_raw, int idx) {
   const Dims& d = a.d;
@@ -585,20 +641,20 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   const int kvh = pair % d.Hkv, b = pair / d.Hkv;
   const int S = d.S, G = d.G, R = G * S, dh = d.dh, dsub = dh / 64;
   const TcLayout L = make_tc_layout(d);
+  const TcWarps W = tc_warps(d);
   const int QR = L.qrows;
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   uint8_t* kv = sm + L.kv;
   uint8_t* qt = sm + L.q;
-  uint8_t* pt = sm + L.p;
-  float* s = reinterpret_cast<float*>(sm + L.s);
   float* ml = reinterpret_cast<float*>(sm + L.ml);
+  float* mlk = reinterpret_cast<float*>(sm + L.mlk);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L.bar);
-  constexpr int SLD = KTS + 4;
   const int tid = threadIdx.x, nthr = blockDim.x;
-  const int warp = tid / 32, lane = tid % 32, nw = nthr / 32;
+  const int warp = tid / 32, lane = tid % 32;
+  const int g8 = lane >> 2, t4 = lane & 3;
 
-  pdl_wait();
+  if (!a.early) pdl_wait();
   const long long p = __ldcg(&a.pos[b]);
   const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);  // valid ring rows 0..nv-1
   const int t0 = rank * a.ntile;
@@ -624,6 +680,7 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     for (int i = 0; i < TC_STAGES && i < nwt; ++i) issue(i);
   }
+  if (a.early) pdl_wait();  // the projections below come from the previous launch
   // Q rows (pre-scaled) as bf16; rows R..QR-1 zero.
   const int c4n = dh / 4;
   for (int i = tid; i < QR * c4n; i += nthr) {
@@ -657,30 +714,108 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
       *reinterpret_cast<uint2*>(kd + off) = kw;
       *reinterpret_cast<uint2*>(kd + L.stage + off) = vw;
     }
-  for (int r = tid; r < QR; r += nthr) {
-    ml[r * 3 + 0] = -INFINITY;
-    ml[r * 3 + 1] = 0.f;
-    ml[r * 3 + 2] = 0.f;
-  }
+  __syncthreads();  // barriers initialised, Q and slot rows written
 
-  const int g8 = lane >> 2, t4 = lane & 3;
-  const int MT = QR / 16, NTD = dh / 8;
-  const int n_ot = MT * NTD;  // O fragments, warp w owns w, w + nw, ...
-  float oacc[OT_MAX][4];
+  // this warp's role
+  const int nact = W.mt * W.kg * W.dp;
+  const bool active = warp < nact;
+  const int wdp = warp % W.dp, wkg = (warp / W.dp) % W.kg, wmt = warp / (W.dp * W.kg);
+  const int NTO = W.dw / 8;  // O fragments of this warp
+  float o[OW_MAX][4];
 #pragma unroll
-  for (int k = 0; k < OT_MAX; ++k) oacc[k][0] = oacc[k][1] = oacc[k][2] = oacc[k][3] = 0.f;
-  const uint32_t qb = smem_u32(qt), pb = smem_u32(pt);
+  for (int k = 0; k < OW_MAX; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY;  // running max of rows g8, g8 + 8 of the m-tile
+  float l0 = 0.f, l1 = 0.f;              // this lane's part of the running sums
+  const uint32_t qb = smem_u32(qt);
+  const int qrow = wmt * 16 + (lane & 15);
+
+  // One online-softmax update over the 16 keys at tile rows kr..kr+15 of
+  // the K/V buffers kb/vb; key row j is valid when j < nvr or KT <= j < KT + nsk.
+  auto update = [&](uint32_t kb, uint32_t vb, int kr, int nvr, int nsk) {
+    float sc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+    // S = Q K^T: per k-step one Q fragment and one K fragment pair
+    const uint32_t krow = kb + (uint32_t)(kr + (lane & 7) + ((lane >> 4) << 3)) * 128;
+    const int kx = lane & 7;  // row phase of the swizzle (kr is a multiple of 8)
+    for (int ks = 0; ks < dh / 16; ++ks) {
+      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+      ldsm_x4(qb + sw_chunk(QR, qrow, ks * 2 + (lane >> 4)), a0, a1, a2, a3);
+      const int c = ks * 2 + ((lane >> 3) & 1);
+      ldsm_x4(krow + (uint32_t)((c >> 3) * KTS * 128 + (((c & 7) ^ kx) << 4)), b0, b1, b2, b3);
+      mma_bf16_16816(sc[0], a0, a1, a2, a3, b0, b1);
+      mma_bf16_16816(sc[1], a0, a1, a2, a3, b2, b3);
+    }
+    // masked row maxima over this warp's keys (quad of lanes per row)
+    float x0 = -INFINITY, x1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        const int j = kr + n * 8 + 2 * t4;
+        const bool v0 = j < nvr || (j >= KT && j < KT + nsk);
+        const bool v1 = j + 1 < nvr || (j + 1 >= KT && j + 1 < KT + nsk);
+        if (!v0) sc[n][0] = sc[n][2] = -INFINITY;
+        if (!v1) sc[n][1] = sc[n][3] = -INFINITY;
+        x0 = fmaxf(x0, fmaxf(sc[n][0], sc[n][1]));
+        x1 = fmaxf(x1, fmaxf(sc[n][2], sc[n][3]));
+      }
+    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
+    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
+    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    const float s0 = m0 == -INFINITY ? 0.f : exp2f(m0 - n0);
+    const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    l0 *= s0;
+    l1 *= s1;
+#pragma unroll
+    for (int k = 0; k < OW_MAX; ++k)
+      if (k < NTO) {
+        o[k][0] *= s0;
+        o[k][1] *= s0;
+        o[k][2] *= s1;
+        o[k][3] *= s1;
+      }
+    // P = exp2(S - m) rounded to bf16, packed as the A operand of P.V
+    uint32_t pa[2][2];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        const float e0 = sc[n][0] == -INFINITY ? 0.f : exp2f(sc[n][0] - n0);
+        const float e1 = sc[n][1] == -INFINITY ? 0.f : exp2f(sc[n][1] - n0);
+        const float e2 = sc[n][2] == -INFINITY ? 0.f : exp2f(sc[n][2] - n1);
+        const float e3 = sc[n][3] == -INFINITY ? 0.f : exp2f(sc[n][3] - n1);
+        pa[n][0] = pack_bf16x2(e0, e1);
+        pa[n][1] = pack_bf16x2(e2, e3);
+        const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[n][0]));
+        const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[n][1]));
+        l0 += r0.x + r0.y;
+        l1 += r1.x + r1.y;
+      }
+    // O += P V over this warp's head-dim part, two 8-column fragments per load
+    {
+      const int key = kr + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const uint32_t vrow = vb + (uint32_t)key * 128;
+      const int c0 = wdp * (W.dw / 8) + (lane >> 4);
+#pragma unroll
+      for (int k = 0; k < OW_MAX; k += 2)
+        if (k < NTO) {
+          uint32_t b0, b1, b2, b3;
+          const int c = c0 + k;
+          ldsm_x4_t(vrow + (uint32_t)((c >> 3) * KTS * 128 + (((c & 7) ^ (key & 7)) << 4)), b0, b1,
+                    b2, b3);
+          mma_bf16_16816(o[k], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b0, b1);
+          mma_bf16_16816(o[k + 1], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b2, b3);
+        }
+    }
+  };
+
   int done = 0;  // ring tiles consumed
   bool aborted = false;
-  __syncthreads();  // barriers initialised, Q / slot rows / row state written
-
   for (int i = 0; i < nsteps; ++i) {
-    const bool ring = i < nwt;                    // a window tile arrives in stage i % STAGES
+    const bool ring = i < nwt;  // a window tile arrives in stage i % STAGES
     const bool with_slots = slots && i == nsteps - 1;
-    const int kr0 = ring ? 0 : KT;                // first key row of the step
-    const int rows = (ring ? KT : 0) + (with_slots ? 16 : 0);
     const int nvr = ring ? min(KT, nv - (t0 + i) * KT) : 0;  // valid window rows
-    const int nsk = with_slots ? S : 0;                       // valid slot rows
     uint8_t* kt = kv + (size_t)(ring ? i % TC_STAGES : 0) * 2 * L.stage;
     uint8_t* vt = kt + L.stage;
     if (ring) {
@@ -690,101 +825,27 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
         break;
       }
       // window rows past the valid ones: V zeroed (P is zero there, V must be finite)
-      if (nvr < KT)
+      if (nvr < KT) {
         for (int e = tid; e < (KT - nvr) * c4n; e += nthr) {
           const int j = nvr + e / c4n, c = (e % c4n) * 4;
           *reinterpret_cast<uint2*>(vt + sw_chunk(KTS, j, c >> 3) + (c & 7) * 2) =
               make_uint2(0u, 0u);
         }
+        __syncthreads();
+      }
       done = i + 1;
+      if (active)
+        for (int q = 0; q < W.kw; q += 16)
+          if (wkg * W.kw + q < nvr) update(smem_u32(kt), smem_u32(vt), wkg * W.kw + q, nvr, 0);
     }
-    // S = Q K^T over this tile
-    {
-      const uint32_t kb = smem_u32(kt);
-      const int NTK = rows / 8, KS = dh / 16;
-      for (int t = warp; t < MT * NTK; t += nw) {
-        const int mt = t / NTK, nt = t % NTK;
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t a0, a1, a2, a3, b0, b1;
-          ldsm_x4(qb + sw_chunk(QR, mt * 16 + (lane & 15), ks * 2 + (lane >> 4)), a0, a1, a2, a3);
-          ldsm_x2(kb + sw_chunk(KTS, kr0 + nt * 8 + (lane & 7), ks * 2 + ((lane >> 3) & 1)), b0,
-                  b1);
-          mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
-        }
-        const int r = mt * 16 + g8, col = nt * 8 + 2 * t4;
-        *reinterpret_cast<float2*>(&s[r * SLD + col]) = make_float2(c[0], c[1]);
-        *reinterpret_cast<float2*>(&s[(r + 8) * SLD + col]) = make_float2(c[2], c[3]);
-      }
-    }
-    __syncthreads();  // scores complete; P.V of the previous step done everywhere
-    if (tid == 0 && ring && i >= 1 && i + TC_STAGES - 1 < nwt) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(i + TC_STAGES - 1);  // into the stage of tile i - 1, free now
-    }
-    // online softmax: new max, rescale factor, P (bf16), running sum.
-    // Column c of the step is key row kr0 + c of the tile buffer.
-    for (int r = warp; r < QR; r += nw) {
-      float x[4];
-      float mt = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int c = 64 * h + 2 * lane + q, j = kr0 + c;
-          const bool valid = r < R && c < rows && (j < nvr || (j >= KT && j < KT + nsk));
-          x[2 * h + q] = valid ? s[r * SLD + c] : -INFINITY;
-          mt = fmaxf(mt, x[2 * h + q]);
-        }
-      }
-      const float m_old = ml[r * 3 + 0];
-      const float m_new = fmaxf(m_old, warp_max(mt));
-      const float sc = (r < R && m_old != -INFINITY) ? exp2f(m_old - m_new) : 0.f;
-      float lsum = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = 64 * h + 2 * lane;
-        if (c < rows) {
-          const float e0 = x[2 * h] == -INFINITY ? 0.f : exp2f(x[2 * h] - m_new);
-          const float e1 = x[2 * h + 1] == -INFINITY ? 0.f : exp2f(x[2 * h + 1] - m_new);
-          const uint32_t w = pack_bf16x2(e0, e1);
-          const float2 back = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-          lsum += back.x + back.y;
-          *reinterpret_cast<uint32_t*>(pt + sw_chunk(QR, r, c >> 3) + (c & 7) * 2) = w;
-        }
-      }
-      lsum = warp_sum(lsum);
-      if (lane == 0) {
-        ml[r * 3 + 0] = r < R ? m_new : -INFINITY;
-        ml[r * 3 + 1] = ml[r * 3 + 1] * sc + lsum;
-        ml[r * 3 + 2] = sc;
-      }
-    }
-    __syncthreads();
-    // O = scale * O + P V
-    {
-      const uint32_t vb = smem_u32(vt);
-      const int KS = rows / 16;
-#pragma unroll
-      for (int k = 0; k < OT_MAX; ++k) {
-        const int t = warp + k * nw;
-        if (t < n_ot) {
-          const int mt = t / NTD, nt = t % NTD;
-          const int r0 = mt * 16 + g8;
-          const float sc0 = ml[r0 * 3 + 2], sc1 = ml[(r0 + 8) * 3 + 2];
-          float* c = oacc[k];
-          c[0] *= sc0;
-          c[1] *= sc0;
-          c[2] *= sc1;
-          c[3] *= sc1;
-          for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a0, a1, a2, a3, b0, b1;
-            ldsm_x4(pb + sw_chunk(QR, mt * 16 + (lane & 15), ks * 2 + (lane >> 4)), a0, a1, a2,
-                    a3);
-            ldsm_x2_t(vb + sw_chunk(KTS, kr0 + ks * 16 + (lane & 15), nt), b0, b1);
-            mma_bf16_16816(c, a0, a1, a2, a3, b0, b1);
-          }
-        }
+    // the slot keys (rows KT..KT+15) go to the last key group
+    if (with_slots && active && wkg == W.kg - 1)
+      update(smem_u32(kt), smem_u32(vt), KT, 0, S);
+    if (ring) {
+      __syncthreads();  // every warp done with this stage
+      if (tid == 0 && i + TC_STAGES < nwt) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(i + TC_STAGES);
       }
     }
   }
@@ -794,7 +855,7 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     // (bounded) before the shared memory is released, write nothing
     if (tid == 0) {
       atomicOr(a.err, ERR_TIMEOUT);
-      const int issued = min(nwt, max(TC_STAGES, done + TC_STAGES - 1));
+      const int issued = min(nwt, done + TC_STAGES);
       for (int i = done; i < issued; ++i)
         mbar_wait(&bar[i % TC_STAGES], (uint32_t)((i / TC_STAGES) & 1));
     }
@@ -805,43 +866,68 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     return;
   }
 
+  // key groups -> shared memory (the tile buffers are free now)
+  __syncthreads();
+  float* okg = reinterpret_cast<float*>(sm + L.okg);  // [kg][QR][dh + 4]
+  float* octa = reinterpret_cast<float*>(sm + L.o);   // [QR][dh + 4]
+  const int OLD = dh + 4;
+  if (active) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const int r = wmt * 16 + g8;
+    float* ob = okg + ((size_t)wkg * QR + r) * OLD + wdp * W.dw + 2 * t4;
+#pragma unroll
+    for (int k = 0; k < OW_MAX; ++k)
+      if (k < NTO) {
+        *reinterpret_cast<float2*>(ob + k * 8) = make_float2(o[k][0], o[k][1]);
+        *reinterpret_cast<float2*>(ob + 8 * OLD + k * 8) = make_float2(o[k][2], o[k][3]);
+      }
+    if (t4 == 0 && wdp == 0) {
+      float* mb = mlk + ((size_t)wkg * QR + r) * 2;
+      mb[0] = m0;
+      mb[1] = l0;
+      mb[16] = m1;
+      mb[17] = l1;
+    }
+  }
+  __syncthreads();
+  // merge the key groups per row: M = max m_k, L = sum w_k l_k, O = sum w_k O_k
   __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
-  __syncthreads();  // last row sums visible; every read of the tile buffers done
-  if (nsplit == 1) {
-#pragma unroll
-    for (int k = 0; k < OT_MAX; ++k) {
-      const int t = warp + k * nw;
-      if (t < n_ot) {
-        const int mt = t / NTD, nt = t % NTD, col = nt * 8 + 2 * t4;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int r = mt * 16 + g8 + 8 * h2;
-          if (r < R) {
-            const int g = r / S, sl = r % S;
-            const float inv = 1.f / ml[r * 3 + 1];
-            __nv_bfloat16* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + col;
-            *reinterpret_cast<uint32_t*>(dst) =
-                pack_bf16x2(oacc[k][2 * h2] * inv, oacc[k][2 * h2 + 1] * inv);
-          }
-        }
+  for (int e = tid; e < R * c4n; e += nthr) {
+    const int r = e / c4n, c = (e % c4n) * 4;
+    float M = -INFINITY;
+    for (int k = 0; k < W.kg; ++k) M = fmaxf(M, mlk[((size_t)k * QR + r) * 2]);
+    float Ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < W.kg; ++k) {
+      const float lk = mlk[((size_t)k * QR + r) * 2 + 1];
+      const float wt = lk > 0.f ? exp2f(mlk[((size_t)k * QR + r) * 2] - M) : 0.f;
+      const float4 ov = *reinterpret_cast<const float4*>(okg + ((size_t)k * QR + r) * OLD + c);
+      Ls = fmaf(wt, lk, Ls);
+      acc.x = fmaf(wt, ov.x, acc.x);
+      acc.y = fmaf(wt, ov.y, acc.y);
+      acc.z = fmaf(wt, ov.z, acc.z);
+      acc.w = fmaf(wt, ov.w, acc.w);
+    }
+    if (nsplit == 1) {
+      const int g = r / S, sl = r % S;
+      const float inv = 1.f / Ls;
+      __nv_bfloat16* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    } else {
+      *reinterpret_cast<float4*>(octa + (size_t)r * OLD + c) = acc;
+      if (c == 0) {
+        ml[r * 2] = M;
+        ml[r * 2 + 1] = Ls;
       }
     }
-    return;
   }
-  // partial O (unnormalised) into the tile buffers, then the cluster combine
-  float* o = reinterpret_cast<float*>(kv);
-  const int OLD = dh + 4;
-#pragma unroll
-  for (int k = 0; k < OT_MAX; ++k) {
-    const int t = warp + k * nw;
-    if (t < n_ot) {
-      const int mt = t / NTD, nt = t % NTD, col = nt * 8 + 2 * t4;
-      const int r = mt * 16 + g8;
-      *reinterpret_cast<float2*>(&o[r * OLD + col]) = make_float2(oacc[k][0], oacc[k][1]);
-      *reinterpret_cast<float2*>(&o[(r + 8) * OLD + col]) = make_float2(oacc[k][2], oacc[k][3]);
-    }
-  }
+  if (nsplit == 1) return;
   cluster_sync_all();
+  // rank `rank` combines rows rank, rank + nsplit, ... over all ranks
   const int my_rows = (R - rank + nsplit - 1) / nsplit;
   for (int e = tid; e < my_rows * c4n; e += nthr) {
     const int r = rank + (e / c4n) * nsplit, c = (e % c4n) * 4, g = r / S, sl = r % S;
@@ -850,7 +936,7 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
 #pragma unroll
     for (int sp = 0; sp < MAX_SPLIT; ++sp) {
       if (sp < nsplit) {
-        const uint32_t ad = peer_addr(&ml[r * 3], (uint32_t)sp);
+        const uint32_t ad = peer_addr(&ml[r * 2], (uint32_t)sp);
         mp[sp] = ld_peer_f(ad);
         lp[sp] = ld_peer_f(ad + 4);
         M = fmaxf(M, mp[sp]);
@@ -862,7 +948,7 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     for (int sp = 0; sp < MAX_SPLIT; ++sp) {
       if (sp < nsplit) {
         const float wt = lp[sp] > 0.f ? exp2f(mp[sp] - M) : 0.f;
-        const float4 ov = ld_peer_f4(peer_addr(&o[r * OLD + c], (uint32_t)sp));
+        const float4 ov = ld_peer_f4(peer_addr(octa + (size_t)r * OLD + c, (uint32_t)sp));
         Lsum = fmaf(lp[sp], wt, Lsum);
         acc.x = fmaf(wt, ov.x, acc.x);
         acc.y = fmaf(wt, ov.y, acc.y);
@@ -878,15 +964,105 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   cluster_sync_all();  // partners keep their shared memory until every read is done
 }
 
-__global__ void __launch_bounds__(THREADS)
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ void mma_tf32_1688(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int idx) {
+  const Dims& d = a.d;
+  const int nhb = (d.Hm + a.hpc - 1) / a.hpc;
+  const int b = idx / nhb, hd0 = (idx % nhb) * a.hpc;
+  const int nh = min(d.Hm, hd0 + a.hpc) - hd0;
+  const int P = d.P, N = d.N, S = d.S;
+  const int MT = P / 16, KSPL = mem_ksplit(d), G16 = N / 16 / KSPL;
+  float* red = reinterpret_cast<float*>(sm_raw);  // [KSPL][P][8]
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int mt = warp % MT, kp = warp / MT;
+  const bool active = kp < KSPL;
+  const int r0 = mt * 16 + g8;
+  const int col0 = kp * G16 * 16 + 4 * t4;  // this lane's first column
+  if (!a.early) pdl_wait();
+  const float* hb0 = a.state + ((size_t)b * d.Hm + hd0) * P * N;
+  float4 hv[2][MEM_G16];
+  auto load = [&](int i) {
+    const float* hb = hb0 + (size_t)i * P * N;
+#pragma unroll
+    for (int j = 0; j < MEM_G16; ++j)
+      if (j < G16) {
+        hv[0][j] = __ldcg(reinterpret_cast<const float4*>(hb + (size_t)r0 * N + col0 + j * 16));
+        hv[1][j] = __ldcg(reinterpret_cast<const float4*>(hb + (size_t)(r0 + 8) * N + col0 + j * 16));
+      }
+  };
+  if (active && nh > 0) load(0);
+  if (a.early) pdl_wait();  // C comes from the previous launch
+  // B fragments (C of this request, slot g8), held for all heads
+  uint32_t bf[MEM_G16][4];
+  {
+    const float* crow = a.proj + ((size_t)b * S + g8) * d.Nd + d.QD + 2 * d.KVD + col0;
+#pragma unroll
+    for (int j = 0; j < MEM_G16; ++j) {
+      float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (active && j < G16 && g8 < S) c = __ldcg(reinterpret_cast<const float4*>(crow + j * 16));
+      bf[j][0] = to_tf32(c.x);
+      bf[j][1] = to_tf32(c.y);
+      bf[j][2] = to_tf32(c.z);
+      bf[j][3] = to_tf32(c.w);
+    }
+  }
+  __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
+  for (int i = 0; i < nh; ++i) {
+    if (active) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < MEM_G16; ++j)
+        if (j < G16) {
+          mma_tf32_1688(c, to_tf32(hv[0][j].x), to_tf32(hv[1][j].x), to_tf32(hv[0][j].y),
+                        to_tf32(hv[1][j].y), bf[j][0], bf[j][1]);
+          mma_tf32_1688(c, to_tf32(hv[0][j].z), to_tf32(hv[1][j].z), to_tf32(hv[0][j].w),
+                        to_tf32(hv[1][j].w), bf[j][2], bf[j][3]);
+        }
+      if (i + 1 < nh) load(i + 1);  // next head in flight during the reduction
+      // c: (row r0, slots 2t4, 2t4+1), (row r0 + 8, same slots)
+      float* rp = red + ((size_t)kp * P + r0) * 8 + 2 * t4;
+      *reinterpret_cast<float2*>(rp) = make_float2(c[0], c[1]);
+      *reinterpret_cast<float2*>(rp + 64) = make_float2(c[2], c[3]);
+    }
+    __syncthreads();
+    for (int e = tid; e < S * P; e += blockDim.x) {
+      const int sl = e / P, p = e % P;
+      float y = 0.f;
+      for (int q = 0; q < KSPL; ++q) y += red[((size_t)q * P + p) * 8 + sl];
+      mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)(hd0 + i) * P + p] = __float2bfloat16_rn(y);
+    }
+    __syncthreads();  // partial sums read before the next head overwrites them
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 2)
 attn_tc_kernel(Args a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
   extern __shared__ __align__(128) uint8_t sm[];
   pdl_trigger();
   const int idx = blockIdx.x;
   if (idx < a.n_attn)
     attn_tc_cta(a, &mk, &mv, sm, idx);
-  else if (idx < a.n_attn + a.n_mem)
-    mem_cta<__nv_bfloat16>(a, sm, idx - a.n_attn);
+  else if (idx < a.n_attn + a.n_mem) {
+    if (a.mem_tc)
+      mem_tc_cta(a, sm, idx - a.n_attn);
+    else
+      mem_cta<__nv_bfloat16>(a, sm, idx - a.n_attn);
+  }
   else
     pdl_wait();  // cluster padding
 }
@@ -909,7 +1085,8 @@ __global__ void __launch_bounds__(THREADS) attn_cluster_kernel(Args a) {
 
 bool attn_uses_tc(const Dims& d, int dtype) {
   const int qrows = (d.G * d.S + 15) / 16 * 16;
-  return dtype == HF_BF16 && d.dh % 64 == 0 && qrows * d.dh <= OT_MAX * 8 * 128;
+  // the warp roles need m-tiles x head-dim parts <= 4 (at least two key groups)
+  return dtype == HF_BF16 && d.dh % 64 == 0 && qrows * d.dh <= 8192;
 }
 
 int attn_tile_rows(const Dims&) { return KT; }
@@ -981,8 +1158,8 @@ static Plan make_tc_plan(const Dims& d, int B, int num_sms, int* ntile) {
 cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
                                 const float* state, void* mix, const CUtensorMap* mk,
-                                const CUtensorMap* mv, int32_t* err, int num_sms, cudaStream_t st,
-                                int* launches) {
+                                const CUtensorMap* mv, int32_t* err, int num_sms, int early,
+                                cudaStream_t st, int* launches) {
   if (B <= 0) return cudaSuccess;
   const bool tc = attn_uses_tc(d, dtype) && mk && mv;
   Args a{};
@@ -996,6 +1173,7 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   a.hpc = (B * d.Hm + 8 * num_sms - 1) / (8 * num_sms);
   if (a.hpc < 1) a.hpc = 1;
   a.n_mem = B * ((d.Hm + a.hpc - 1) / a.hpc);
+  a.mem_tc = tc && mem_tc_ok(d) ? 1 : 0;
   a.qscale = 1.4426950408889634f / sqrtf((float)d.dh);
   a.proj = proj;
   a.ring_k = ring_k;
@@ -1004,6 +1182,7 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   a.state = state;
   a.mix = mix;
   a.err = err;
+  a.early = early && tc;
   const int cz = a.plan.nsplit;
   const int total = (a.n_attn + a.n_mem + cz - 1) / cz * cz;
   cudaLaunchConfig_t cfg = {};

@@ -234,6 +234,56 @@ __device__ __forceinline__ void epi_ssm(const Epi& e, int r, int c, float v, int
   }
 }
 
+// The same epilogue split into a per-column part (fixed for a thread that
+// owns one output column) and a per-row part (the ring-row offset of a
+// committed row, -1 when the row is skipped), so that a tile's inner loop is
+// one store per element.
+struct SsmCol {
+  int kind;      // 0: skip, 1: ring K/V, 2: x or B, 3: dt (softplus with bias)
+  void* ring;    // ring_k or ring_v (kind 1)
+  size_t base;   // element offset of (layer, head, dim) in the ring, or of (layer, column) in xbd
+  float bias;    // dt bias (kind 3)
+};
+
+__device__ __forceinline__ SsmCol ssm_col(const Epi& e, int c) {
+  const Dims& d = e.d;
+  SsmCol k{0, nullptr, 0, 0.f};
+  const int layer = e.layer0 + c / e.cols_per_layer;
+  const int cl = c % e.cols_per_layer + e.col_off;
+  if (e.cols_valid > 0 && cl >= e.cols_valid) return k;
+  if (cl < 2 * d.KVD) {
+    const int which = cl >= d.KVD;
+    const int cc = cl - which * d.KVD;
+    k.kind = 1;
+    k.ring = which ? e.ring_v : e.ring_k;
+    k.base = (((size_t)layer * d.Bmax * d.Hkv + cc / d.dh) * d.W) * d.dh + cc % d.dh;
+  } else {
+    const int j = cl - 2 * d.KVD;
+    k.base = (size_t)layer * e.xbd_layer_stride + j;
+    k.kind = 2;
+    if (j >= d.dinner + d.N) {
+      k.kind = 3;
+      k.bias = __ldg(&e.dt_bias[layer * d.Hm + (j - d.dinner - d.N)]);
+    }
+  }
+  return k;
+}
+
+// Ring-row offset of row r (request b, position p), or -1 when p < 0.
+__device__ __forceinline__ long long ssm_row_off(const Dims& d, int b, long long p) {
+  return p < 0 ? -1 : ((long long)b * d.Hkv * d.W + p % d.W) * d.dh;
+}
+
+template <typename T>
+__device__ __forceinline__ void ssm_store(const Epi& e, const SsmCol& k, int r, long long ro,
+                                          float v) {
+  if (ro < 0 || k.kind == 0) return;
+  if (k.kind == 1)
+    static_cast<T*>(k.ring)[k.base + ro] = from_f<T>(v);
+  else
+    e.xbd[k.base + (size_t)r * e.d.NS] = k.kind == 3 ? softplus_f(v + k.bias) : v;
+}
+
 template <typename T>
 __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
   if (e.kind == EPI_F32) {
@@ -278,9 +328,13 @@ cudaError_t launch_gemm_fma(int dtype, const void* X, int ldx, const void* Wt, i
 // Split-K partner CTAs (splits <= 8) form a thread-block cluster and sum
 // their partial tiles through distributed shared memory.
 // a_tiles (optional): A pre-tiled by tile_weights, read with bulk copies.
+// late_trigger: the CTAs signal programmatic completion only after their own
+// dependency wait, so that the next launch may read, before its own wait,
+// anything that the launches before this one wrote.
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb,
                            int N, int K, int swap, int splits, int32_t* err, const Epi& epi,
-                           cudaStream_t st, int* launches, const void* a_tiles = nullptr);
+                           cudaStream_t st, int* launches, const void* a_tiles = nullptr,
+                           int late_trigger = 0);
 void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst);
 
 // Persistent warp-specialised bf16 GEMM for large token-major products
@@ -315,7 +369,7 @@ bool attn_uses_tc(const Dims& d, int dtype);
 cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
                                 const float* state, void* mix, const CUtensorMap* mk,
-                                const CUtensorMap* mv, int32_t* err, int num_sms,
+                                const CUtensorMap* mv, int32_t* err, int num_sms, int early,
                                 cudaStream_t st, int* launches);
 
 // Commit state step, all layers: validates the accepted counts (error word),

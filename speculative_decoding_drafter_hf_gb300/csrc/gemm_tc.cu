@@ -63,6 +63,7 @@ struct TcArgs {
                            // (m_tile, k_block) is one 16 KB swizzled tile, read by
                            // one bulk copy; NULL: A read through the tensor map
   int32_t* err;       // device error word
+  int late_trigger;   // 1: signal dependents only after the dependency wait
 };
 
 // Epilogue cache (shared memory after the barriers): per output row of the
@@ -106,7 +107,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const int kb0 = (int)((long long)split * a.kblocks / a.splits);
   const int kb1 = (int)((long long)(split + 1) * a.kblocks / a.splits);
   const int nkb = kb1 - kb0;
-  pdl_trigger();
+  if (!a.late_trigger) pdl_trigger();
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -148,10 +149,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         load_a(j, j);
       }
       pdl_wait();
+      if (a.late_trigger) pdl_trigger();
       for (int j = 0; j < pre; ++j)
         tma_load_2d(sB + j * B_BYTES, &tb, &full[j], (kb0 + j) * 64, n_tile * BN);
     } else {
       pdl_wait();
+      if (a.late_trigger) pdl_trigger();
       for (int j = 0; j < pre; ++j) {
         mbar_expect_tx(&full[j], STAGE_BYTES);
         load_a(j, j);
@@ -172,7 +175,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       tma_load_2d(sB + s * B_BYTES, &tb, &full[s], (kb0 + i) * 64, n_tile * BN);
     }
     flags[1] = i;
-  } else if (warp == 1 && lane == 0) {
+  } else if (a.late_trigger) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  if (warp == 1 && lane == 0) {
     // MMA issuer
     constexpr uint32_t idesc = idesc_bf16(BN < 16 ? 16 : BN);
     int i = 0;
@@ -205,7 +212,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         long long pq;
         epi_row(epi, n_tile * BN + nl, bq, pq);
         ep_b[nl] = bq;
-        ep_p[nl] = pq;
+        ep_p[nl] = ssm_row_off(epi.d, bq, pq);
       }
     } else if (epi.kind == EPI_RESID && RES_ROWS > 0) {
       const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(epi.resid);
@@ -240,6 +247,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const int m = m_tile * 128 + m_local;
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
   float v[16];
+  // this thread's output column of the commit projection (swap only)
+  const SsmCol scol = (a.swap && epi.kind == EPI_SSM_KV && m < a.M) ? ssm_col(epi, m)
+                                                                      : SsmCol{0, nullptr, 0, 0.f};
   // Output of tile row nl (activation row n) and this thread's column m.
   auto emit = [&](int nl, float val) {
     const int n = n_tile * BN + nl;
@@ -253,7 +263,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
                                    : to_f(__ldcg(&static_cast<const __nv_bfloat16*>(epi.resid)[i]));
       static_cast<__nv_bfloat16*>(epi.out_t)[i] = __float2bfloat16_rn(x + val);
     } else {
-      epi_ssm<__nv_bfloat16>(epi, n, m, val, ep_b[nl], ep_p[nl]);
+      ssm_store<__nv_bfloat16>(epi, scol, n, ep_p[nl], val);
     }
   };
   if (a.splits == 1) {
@@ -263,6 +273,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       if (m < a.M && c0 < n_here) {
         if (!a.swap) {
           epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
+        } else if (epi.kind == EPI_RESID && RES_ROWS == 0) {
+          // 16 independent residual loads in flight, then the stores
+          const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(epi.resid);
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(epi.out_t);
+          const size_t base = (size_t)(n_tile * BN + c0) * epi.ld + m;
+          float x[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            x[j] = c0 + j < n_here ? to_f(__ldcg(&res[base + (size_t)j * epi.ld])) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < n_here) out[base + (size_t)j * epi.ld] = __float2bfloat16_rn(x[j] + v[j]);
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
@@ -475,7 +497,8 @@ int tc_pick_splits(int M, int N, int K) {
 
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb, int N,
                            int K, int swap, int splits, int32_t* err, const Epi& epi,
-                           cudaStream_t st, int* launches, const void* a_tiles) {
+                           cudaStream_t st, int* launches, const void* a_tiles,
+                           int late_trigger) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   int bn = 16;
   while (bn < N && bn < 256) bn *= 2;
@@ -491,6 +514,7 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   a.err = err;
   a.splits = std::max(1, std::min(std::min(splits, 8), a.kblocks));
   a.a_tiles = static_cast<const uint8_t*>(a_tiles);
+  a.late_trigger = late_trigger;
   CUtensorMap ma, mb;
   cudaError_t e = make_map(&mb, B, N, K, ldb, bn);
   if (e != cudaSuccess) return e;

@@ -280,7 +280,7 @@ int pick_splits(const hf_handle* h, long long R, long long C, long long K, int t
 // as the 128-row operand (they stream once) and the activation rows as N.
 cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, int ldw, int R,
                         int C, int K, const Epi& epi, cudaStream_t st, int* count,
-                        const void* tiles = nullptr) {
+                        const void* tiles = nullptr, int late_trigger = 0) {
   if (R <= 0 || C <= 0) return cudaSuccess;
   if (h->cfg.dtype == HF_F32) {
     int splits = pick_splits(h, R, C, K, 64, 64);
@@ -288,14 +288,16 @@ cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, in
                                count);
   }
   const int splits = hf::tc_pick_splits(C, R, K);
-  return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->err, epi, st, count, tiles);
+  return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->err, epi, st, count, tiles,
+                            late_trigger);
 }
 
 hf_status gemm(hf_handle* h, int fam, const void* X, int ldx, const void* Wt, int ldw, int R,
-               int C, int K, const Epi& epi, cudaStream_t st, const void* tiles = nullptr) {
+               int C, int K, const Epi& epi, cudaStream_t st, const void* tiles = nullptr,
+               int late_trigger = 0) {
   if (R <= 0 || C <= 0) return HF_OK;
   Scope sc(h, fam, st);
-  cudaError_t e = gemm_launch(h, X, ldx, Wt, ldw, R, C, K, epi, st, &sc.count, tiles);
+  cudaError_t e = gemm_launch(h, X, ldx, Wt, ldw, R, C, K, epi, st, &sc.count, tiles, late_trigger);
   if (e != cudaSuccess) return cuda_fail(h, e, "gemm launch");
   return HF_OK;
 }
@@ -552,9 +554,13 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
     e1.kind = hf::EPI_F32;
     e1.out = h->proj;
     e1.ld = d.Nd;
+    // With the tensor-core attention, the slot projection signals its
+    // dependents only after its own dependency wait: the attention launch may
+    // then read the ring, positions and state (final by then) before its wait.
+    const int early = h->ring_maps.empty() ? 0 : 1;
     hf_status s = gemm(h, HF_K_DRAFT_PROJ, X, d.D, bptr(h->w_draft, (size_t)l * d.Nd * d.D * es),
                        d.D, R, d.Nd, d.D, e1, st,
-                       h->wt_draft ? bptr(h->wt_draft, (size_t)l * h->wt_draft_l) : nullptr);
+                       h->wt_draft ? bptr(h->wt_draft, (size_t)l * h->wt_draft_l) : nullptr, early);
     if (s != HF_OK) return s;
     {
       Scope sc(h, HF_K_ATTN_MEM, st);
@@ -564,7 +570,7 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
                                               bptr(h->ring_k, l * ring_ls),
                                               bptr(h->ring_v, l * ring_ls), h->pos,
                                               h->state + l * state_ls, h->mix, mk, mv, h->err,
-                                              h->num_sms, st, &sc.count);
+                                              h->num_sms, early, st, &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
     }
     Epi e2 = epi_base(h);

@@ -98,6 +98,15 @@ __device__ __forceinline__ void epi_chunk16(const Epi& e, int m, int n0, int nco
                           fmaf(dec, old[q].z, v[4 * q + 2]), fmaf(dec, old[q].w, v[4 * q + 3]));
     return;
   }
+  if (e.kind == EPI_SSM_KV) {  // the row's request and position once per chunk
+    int b;
+    long long p;
+    epi_row(e, m, b, p);
+    const long long ro = ssm_row_off(d, b, p);
+    if (ro < 0) return;
+    for (int j = 0; j < ncols; ++j) ssm_store<__nv_bfloat16>(e, ssm_col(e, n0 + j), m, ro, v[j]);
+    return;
+  }
   for (int j = 0; j < ncols; ++j) epi_apply<__nv_bfloat16>(e, m, n0 + j, v[j]);
 }
 
