@@ -88,32 +88,56 @@ def sum_over_ranks(x: float, device=None) -> float:
 
 # ------------------------------------------------------------------ algorithmic sizes
 
-def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float):
-    """Bytes and flops each step must move/do at minimum (weights, window,
-    state and slot I/O read or written once)."""
+def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: bool):
+    """Bytes each step must move at minimum (weights, window, state and the
+    slot / feature I/O read or written once), per kernel family of the path
+    that runs: {family: (bytes per step, launches per step)}.
+
+    fused (hf_round): the commit projection and the first layer's slot
+    projection share one launch, and the first layer's memory read is made
+    on the updated state inside the state update, so that state is read once
+    per step; later layers read their state again at draft time (their C
+    depends on the layer below, which needs the updated state first).
+    step_bytes is the fused figure: the least traffic any schedule of a
+    step needs."""
     e = cfg.elem_bytes
     D, hq, hkv, dh, W = cfg.d_model, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.window
     din, N, Hm, P, S, L = cfg.d_inner, cfg.d_state, cfg.ssm_heads, cfg.ssm_headdim, cfg.block, cfg.n_layers
-    Nd = hq * dh + 2 * hkv * dh + N
-    Nz = hq * dh + din
+    QD = hq * dh
+    Nd = QD + 2 * hkv * dh + N
+    Nz = QD + din
     Nc = 2 * hkv * dh + din + N + Hm
     R = batch * S
-    nv = window_fill  # valid ring entries per request
-    fam = {}
-    # per launch (one layer) of each kernel family
-    fam["draft_proj"] = e * Nd * D + e * R * D + 4 * R * Nd
-    fam["out_proj"] = e * D * Nz + e * R * Nz + 2 * e * R * D
-    fam["attn_mem"] = (batch * (nv * 2 * hkv * dh * e + Hm * P * N * 4)
-                       + 4 * R * Nd + e * R * Nz)
     rows = batch * mean_accept
-    fam["commit_proj"] = (e * L * Nc * D + e * rows * D
-                          + L * rows * (2 * hkv * dh * e + (din + N + Hm) * 4))
-    fam["commit_state"] = L * (batch * Hm * P * N * 8 + rows * (din + N + Hm) * 4)
-    draft = L * (fam["draft_proj"] + fam["out_proj"] + fam["attn_mem"])
-    commit = fam["commit_proj"] + fam["commit_state"]
+    w_draft, w_out, w_commit = e * Nd * D, e * D * Nz, e * L * Nc * D
+    io_draft = e * R * D + 4 * R * Nd                 # slot rows in, projections out
+    io_out = e * R * Nz + 2 * e * R * D                # mix in, residual in, output out
+    window = batch * window_fill * 2 * hkv * dh * e    # one layer's valid K and V
+    state = batch * Hm * P * N * 4                     # one layer's states, read once
+    io_attn = 4 * R * Nd + e * R * QD                  # projections in, attention out
+    io_mem = 4 * R * N + e * R * din                   # C in, memory read out
+    commit_io = e * rows * D + L * rows * (2 * hkv * dh * e + (din + N + Hm) * 4)
+    state_io = L * rows * (din + N + Hm) * 4
+
+    def fused_fams():
+        return {
+            "round_proj": (w_commit + commit_io + w_draft + io_draft, 1),
+            "draft_proj": ((L - 1) * (w_draft + io_draft), L - 1),
+            "commit_state": (L * 2 * state + state_io + io_mem, 1),
+            "attn_mem": (L * (window + io_attn) + (L - 1) * (state + io_mem), L),
+            "out_proj": (L * (w_out + io_out), L),
+        }
+
+    fam = fused_fams() if fused else {
+        "draft_proj": (L * (w_draft + io_draft), L),
+        "attn_mem": (L * (window + state + io_attn + io_mem), L),
+        "out_proj": (L * (w_out + io_out), L),
+        "commit_proj": (w_commit + commit_io, 1),
+        "commit_state": (L * 2 * state + state_io, 1),
+    }
+    step = sum(b for b, _ in fused_fams().values())
     flops = L * 2 * R * D * (Nd + Nz) + 2 * rows * D * L * Nc
-    return {"per_launch": fam, "draft_bytes": draft, "commit_bytes": commit,
-            "step_bytes": draft + commit, "step_flops": flops}
+    return {"families": fam, "step_bytes": step, "step_flops": flops}
 
 
 def prefill_flops(cfg, total_tokens: int, ring_rows: int) -> float:
@@ -426,21 +450,31 @@ def run_hyflash(args, cfg):
         st_feat.copy_(d_feat[r])
         st_cnt.copy_(d_cnt[r])
 
-    def round_calls():
-        drafter.draft(st_slot, out)
-        drafter.commit(st_feat, st_cnt)
+    fused = args.api == "round"
 
-    # eager warm-up rounds, marked with NVTX ranges ("draft", "commit") so a
-    # profiler can select one round's launches by range
+    def round_calls():
+        if fused:  # one serving iteration: commit the verified round, draft the next
+            drafter.round(st_feat, st_cnt, st_slot, out)
+        else:
+            drafter.draft(st_slot, out)
+            drafter.commit(st_feat, st_cnt)
+
+    # eager warm-up rounds, marked with NVTX ranges ("round", or "draft" and
+    # "commit") so a profiler can select one round's launches by range
     nvtx = torch.cuda.nvtx
     for r in range(args.warmup):
         stage(r)
-        nvtx.range_push("draft")
-        drafter.draft(st_slot, out)
-        nvtx.range_pop()
-        nvtx.range_push("commit")
-        drafter.commit(st_feat, st_cnt)
-        nvtx.range_pop()
+        if fused:
+            nvtx.range_push("round")
+            drafter.round(st_feat, st_cnt, st_slot, out)
+            nvtx.range_pop()
+        else:
+            nvtx.range_push("draft")
+            drafter.draft(st_slot, out)
+            nvtx.range_pop()
+            nvtx.range_push("commit")
+            drafter.commit(st_feat, st_cnt)
+            nvtx.range_pop()
     drafter.sync()
 
     def capture():
@@ -548,23 +582,19 @@ def run_hyflash(args, cfg):
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     tc_peak = float(peaks.get("bf16_tflops", 1900.0))
     peak_src = "measured" if peaks else "fallback"
-    fill = min(cfg.prefix, cfg.window)
-    alg = algorithmic(cfg, batch, fill, (cfg.block + 2) / 2.0)
-    fam_bytes = {"draft_proj": alg["per_launch"]["draft_proj"],
-                 "out_proj": alg["per_launch"]["out_proj"],
-                 "attn_mem": alg["per_launch"]["attn_mem"],
-                 "commit_proj": alg["per_launch"]["commit_proj"],
-                 "commit_state": alg["per_launch"]["commit_state"]}
-    top = max(fam_bytes, key=lambda k: fam_ms.get(k, (0, 0))[0])
-    ms_top, n_top = fam_ms[top]
-    # one profiled scope per layer (draft families) or per call (commit families)
-    scopes = args.steps * (cfg.n_layers if top in ("draft_proj", "out_proj", "attn_mem") else 1)
-    avg_ms = ms_top / max(scopes, 1)
-    achieved = fam_bytes[top] / (avg_ms / 1e3) / 1e9 if avg_ms > 0 else 0.0
+    fill = sum(min(L, cfg.window) for L in lens) / max(len(lens), 1)  # valid window rows
+    alg = algorithmic(cfg, batch, fill, (cfg.block + 2) / 2.0, fused)
+    fams = {k: v for k, v in alg["families"].items() if v[1] > 0}
+    top = max(fams, key=lambda k: fam_ms.get(k, (0, 0))[0])
+    ms_top, _ = fam_ms[top]
+    step_bytes_top, launches_top = fams[top]
+    avg_ms = ms_top / max(args.steps * launches_top, 1)  # one profiled scope per launch
+    per_launch = step_bytes_top / launches_top
+    achieved = per_launch / (avg_ms / 1e3) / 1e9 if avg_ms > 0 else 0.0
     roofline = {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": hbm_peak,
                 "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
                 "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": fam_bytes[top], "avg_launch_ms": avg_ms}
+                "algorithmic_bytes_per_launch": per_launch, "avg_launch_ms": avg_ms}
 
     # ---- CPU oracle beside it (rank 0, N=1 only)
     cpu = None
@@ -585,6 +615,8 @@ def run_hyflash(args, cfg):
                        "prefix": (f"log-uniform [{cfg.prefix_lo}, {cfg.prefix_hi}]"
                                   if cfg.prefix_lo else cfg.prefix),
                        "prefix_cap": args.prefix_max or None,
+                       "api": "hf_round (commit, then draft the next block)" if fused
+                              else "hf_draft then hf_commit",
                        "layers": cfg.n_layers, "window": cfg.window, "block": cfg.block,
                        "l2": f"flushed between steps ({2 * l2 >> 20} MiB write, untimed)",
                        "timing": "CUDA graph of one round replayed per step; CUDA events; "
@@ -592,8 +624,9 @@ def run_hyflash(args, cfg):
                        "parallelism": f"replicas x{ws}"},
             "committed_tokens_per_s": all_acc / (total_ms_max / 1e3),
             "step_ms_median": statistics.median(step_ms),
-            "algorithmic": {"step_bytes": alg["step_bytes"], "draft_bytes": alg["draft_bytes"],
-                            "commit_bytes": alg["commit_bytes"],
+            "algorithmic": {"step_bytes": alg["step_bytes"],
+                            "families": {k: {"bytes_per_step": b, "launches_per_step": n}
+                                         for k, (b, n) in fams.items()},
                             "step_hbm_frac": alg["step_bytes"] / (total_ms / args.steps / 1e3) / 1e9 / hbm_peak},
             "kernels_ms_per_step": {k: v[0] / args.steps for k, v in fam_ms.items() if v[1]},
             "roofline": roofline,
@@ -620,6 +653,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="hyflash", choices=["hyflash", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--prefix", type=int, default=0, help="prefill sweep: prefix length")
+    ap.add_argument("--api", default="round", choices=["round", "separate"],
+                    help="round: hf_round per step (commit, then draft the next block); "
+                         "separate: hf_draft then hf_commit")
     ap.add_argument("--prefix-max", type=int, default=0,
                     help="round configs: cap every request's prefix (0: the workload's own)")
     ap.add_argument("--chunk", type=int, default=128, help="prefill sweep: scan chunk")

@@ -155,6 +155,19 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted,
 hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
                    void* stream);
 
+/* One serving iteration: commit the verified round (feats, n_accepted as in
+ * hf_commit), then draft the next block (slot_emb, out as in hf_draft). The
+ * result -- context and out -- is exactly that of hf_commit followed by
+ * hf_draft (the HyFlash explainer, "That is HyFlash": the memory and the
+ * window take the newly committed features, then the parallel block is
+ * drafted against them). bf16 handles run it as one pipeline: the commit
+ * projection and the first layer's slot projection stream their weights in
+ * one grouped launch, and the first layer's memory read is computed on the
+ * updated state inside the state update (the state is read once per
+ * round). Other handles call the two entry points in turn. */
+hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
+                   const void* slot_emb, void* out, int32_t batch, void* stream);
+
 /* Synchronise `stream`, then read and clear the device error word. Returns
  * HF_EDEVICE if a device-side check failed since the last hf_sync, HF_ECUDA
  * on an asynchronous CUDA error, HF_OK otherwise. */
@@ -209,7 +222,7 @@ typedef enum {
   HF_K_DRAFT_PROJ = 0,   /* draft input projections (Q|K_s|V_s|C_s) */
   HF_K_ATTN_MEM = 1,     /* window+block attention and memory read */
   HF_K_OUT_PROJ = 2,     /* output projections + residual */
-  HF_K_COMMIT_PREP = 3,  /* count check, offsets, row gather */
+  HF_K_ROUND_PROJ = 3,   /* hf_round: grouped commit + first slot projection */
   HF_K_COMMIT_PROJ = 4,  /* commit projections + ring append */
   HF_K_COMMIT_STATE = 5, /* sequential memory update */
   HF_K_PREFILL = 6,      /* every prefill kernel */

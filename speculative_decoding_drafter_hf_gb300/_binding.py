@@ -48,7 +48,7 @@ class Family(enum.IntEnum):
     DRAFT_PROJ = 0
     ATTN_MEM = 1
     OUT_PROJ = 2
-    COMMIT_PREP = 3
+    ROUND_PROJ = 3
     COMMIT_PROJ = 4
     COMMIT_STATE = 5
     PREFILL = 6
@@ -92,6 +92,7 @@ hf_set_weights = _sig("hf_set_weights", _st, _h, _i32, ctypes.POINTER(HfLayerWei
 hf_prefill = _sig("hf_prefill", _st, _h, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32, _vp)
 hf_commit = _sig("hf_commit", _st, _h, _vp, _vp, _i32, _vp)
 hf_draft = _sig("hf_draft", _st, _h, _vp, _vp, _i32, _vp)
+hf_round = _sig("hf_round", _st, _h, _vp, _vp, _vp, _vp, _i32, _vp)
 hf_sync = _sig("hf_sync", _st, _h, _vp)
 hf_last_error = _sig("hf_last_error", ctypes.c_char_p, _h)
 hf_status_string = _sig("hf_status_string", ctypes.c_char_p, _st)
@@ -109,7 +110,7 @@ hf_attention_noalloc = _sig("hf_attention_noalloc", _st, _i32, _i32, _i32, _i32,
                             _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp)
 
 EXPORTED = ("hf_create", "hf_destroy", "hf_set_weights", "hf_prefill", "hf_commit", "hf_draft",
-            "hf_sync", "hf_last_error", "hf_status_string", "hf_tensor_bytes", "hf_read_tensor",
+            "hf_round", "hf_sync", "hf_last_error", "hf_status_string", "hf_tensor_bytes", "hf_read_tensor",
             "hf_context_bytes", "hf_export_context", "hf_import_context", "hf_profile_enable",
             "hf_profile_collect", "hf_profile_read", "hf_launch_count", "hf_attention_noalloc")
 
@@ -229,6 +230,22 @@ class Drafter:
             out = torch.empty(shp, dtype=self.torch_dtype, device=slot_emb.device)
         op = _dev_ptr(out, self.torch_dtype, shp, "out")
         self._check(hf_draft(self._h, sp, op, B, _stream_ptr(stream)))
+        return out
+
+    def round(self, feats, n_accepted, slot_emb, out=None, stream=None):
+        """hf_round: commit (feats, n_accepted), then draft slot_emb -> out."""
+        import torch
+        B = int(n_accepted.shape[0])
+        if int(slot_emb.shape[0]) != B:
+            raise ValueError("feats, n_accepted and slot_emb must have the same batch")
+        fp = _dev_ptr(feats, self.torch_dtype, (B, self.shape.block + 1, self.shape.d_model), "feats")
+        npp = _dev_ptr(n_accepted, torch.int32, (B,), "n_accepted")
+        shp = (B, self.shape.block, self.shape.d_model)
+        sp = _dev_ptr(slot_emb, self.torch_dtype, shp, "slot_emb")
+        if out is None:
+            out = torch.empty(shp, dtype=self.torch_dtype, device=slot_emb.device)
+        op = _dev_ptr(out, self.torch_dtype, shp, "out")
+        self._check(hf_round(self._h, fp, npp, sp, op, B, _stream_ptr(stream)))
         return out
 
     def sync(self, stream=None):

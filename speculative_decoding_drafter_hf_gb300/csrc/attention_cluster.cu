@@ -63,10 +63,13 @@ struct Args {
   const float* state;   // [B][Hm][P][N] of this layer
   void* mix;            // [B*S, Nz]: O at columns [0, Hq*dh), y at [Hq*dh, Nz)
   int32_t* err;
-  int early;      // 1: ring, positions and state are final at launch (the previous
-                  // launch signalled its dependents after its own dependency wait):
-                  // read them before waiting; only the projections need the wait
+  int early;      // what is final at launch (the previous launch signalled its
+                  // dependents after its own dependency wait) and may be read before
+                  // this launch's wait: EARLY_RING (ring K/V), EARLY_STATE (positions,
+                  // states); the projections always need the wait
 };
+
+constexpr int EARLY_RING = 1, EARLY_STATE = 2;
 
 struct Layout {
   size_t bar, kt, vt, q, s, ml, total;
@@ -533,32 +536,6 @@ __host__ __device__ inline TcWarps tc_warps(const Dims& d) {
   return w;
 }
 
-// Memory read on the tensor cores: y[s, p] = sum_n h[p, n] C[s, n] per
-// (request, memory head) as a [P x N] x [N x 8] product on mma.sync
-// m16n8k8 tf32 (fp32 accumulate; h and C rounded to tf32 with
-// round-to-nearest, relative error 2^-11, below the bf16 rounding of the
-// output). Warp (m-tile, k-part) loads its 16 state rows x (N / parts)
-// columns straight into registers as 16-byte loads (every 32-byte sector
-// fully used), the whole head in flight at once; the next head's loads are
-// issued as soon as the current head's fragments are consumed. Within each
-// group of 16 state columns lane t holds columns 4t..4t+3 and serves two
-// k-steps (columns 4t, 4t+1 as logical k = t, t + 4, then 4t+2, 4t+3): the
-// same permutation on both operands, so the sum is unchanged.
-constexpr int MEM_G16 = 8;  // 16-column groups per warp (N <= 128)
-
-__host__ __device__ inline bool mem_tc_ok(const Dims& d) {
-  return d.P % 16 == 0 && d.P <= 128 && d.N % 16 == 0 && d.N <= 128 && d.S <= 8;
-}
-__host__ __device__ inline int mem_ksplit(const Dims& d) {
-  const int mt = d.P / 16;
-  int ks = mt >= 8 ? 1 : 8 / mt;
-  while (ks > 1 && (d.N / 16) % ks) --ks;
-  return ks;
-}
-__host__ __device__ inline size_t mem_tc_bytes(const Dims& d) {
-  return (size_t)mem_ksplit(d) * d.P * 8 * 4;
-}
-
 struct TcLayout {
   size_t kv, okg, o, q, ml, mlk, bar, total;
   int qrows, stage;
@@ -654,13 +631,9 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   const int warp = tid / 32, lane = tid % 32;
   const int g8 = lane >> 2, t4 = lane & 3;
 
-  if (!a.early) pdl_wait();
-  const long long p = __ldcg(&a.pos[b]);
-  const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);  // valid ring rows 0..nv-1
+  const bool ring_early = (a.early & EARLY_RING) != 0;
+  const bool state_early = (a.early & EARLY_STATE) != 0;
   const int t0 = rank * a.ntile;
-  const int nwt = max(0, min(a.ntile, (nv + KT - 1) / KT - t0));  // ring tiles of this CTA
-  const bool slots = rank == 0;
-  const int nsteps = max(nwt, slots ? 1 : 0);
   const size_t rowbase = (size_t)b * S;
   const int y_head = (b * d.Hkv + kvh) * d.W;
 
@@ -674,13 +647,38 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
       tma_load_2d(kd + L.stage + (size_t)u * KTS * 128, mv, br, u * 64, y0);
     }
   };
-  if (tid == 0) {
+  auto init_bars = [&]() {
     for (int i = 0; i < TC_STAGES; ++i) mbar_init(&bar[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    for (int i = 0; i < TC_STAGES && i < nwt; ++i) issue(i);
+  };
+  // Ring tiles requested before the valid count is known (ring final, the
+  // positions not yet): the CTA's first tiles inside the window; those past
+  // the valid rows are drained at the end.
+  int nissue = 0;
+  if (ring_early && !state_early) {
+    nissue = min(TC_STAGES, min(a.ntile, (d.W + KT - 1) / KT - t0));
+    if (tid == 0) {
+      init_bars();
+      for (int i = 0; i < nissue; ++i) issue(i);
+    }
+    pdl_wait();
+  } else if (!state_early) {
+    pdl_wait();
   }
-  if (a.early) pdl_wait();  // the projections below come from the previous launch
+  const long long p = __ldcg(&a.pos[b]);
+  const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);  // valid ring rows 0..nv-1
+  const int nwt = max(0, min(a.ntile, (nv + KT - 1) / KT - t0));  // ring tiles of this CTA
+  const bool slots = rank == 0;
+  const int nsteps = max(nwt, slots ? 1 : 0);
+  if (!(ring_early && !state_early)) {
+    nissue = min(TC_STAGES, nwt);
+    if (tid == 0) {
+      init_bars();
+      for (int i = 0; i < nissue; ++i) issue(i);
+    }
+    if (state_early) pdl_wait();  // the projections below come from the previous launch
+  }
   // Q rows (pre-scaled) as bf16; rows R..QR-1 zero.
   const int c4n = dh / 4;
   for (int i = tid; i < QR * c4n; i += nthr) {
@@ -855,7 +853,7 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     // (bounded) before the shared memory is released, write nothing
     if (tid == 0) {
       atomicOr(a.err, ERR_TIMEOUT);
-      const int issued = min(nwt, done + TC_STAGES);
+      const int issued = max(nissue, min(nwt, done + TC_STAGES));
       for (int i = done; i < issued; ++i)
         mbar_wait(&bar[i % TC_STAGES], (uint32_t)((i / TC_STAGES) & 1));
     }
@@ -866,6 +864,9 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     return;
   }
 
+  // tiles requested past the valid rows: let their copies land first
+  if (tid == 0)
+    for (int i = nwt; i < nissue; ++i) mbar_wait(&bar[i % TC_STAGES], (uint32_t)((i / TC_STAGES) & 1));
   // key groups -> shared memory (the tile buffers are free now)
   __syncthreads();
   float* okg = reinterpret_cast<float*>(sm + L.okg);  // [kg][QR][dh + 4]
@@ -964,21 +965,11 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   cluster_sync_all();  // partners keep their shared memory until every read is done
 }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-
-__device__ __forceinline__ void mma_tf32_1688(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
-                                              uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
+// Memory read CTA (tensor-core form, see common.cuh): warp (m-tile, k-part)
+// loads its 16 state rows x (N / parts) columns straight into registers as
+// 16-byte loads (every 32-byte sector fully used), the whole head in flight
+// at once; the next head's loads are issued as soon as the current head's
+// fragments are consumed.
 __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int idx) {
   const Dims& d = a.d;
   const int nhb = (d.Hm + a.hpc - 1) / a.hpc;
@@ -993,7 +984,8 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
   const bool active = kp < KSPL;
   const int r0 = mt * 16 + g8;
   const int col0 = kp * G16 * 16 + 4 * t4;  // this lane's first column
-  if (!a.early) pdl_wait();
+  const bool state_early = (a.early & EARLY_STATE) != 0;
+  if (!state_early) pdl_wait();
   const float* hb0 = a.state + ((size_t)b * d.Hm + hd0) * P * N;
   float4 hv[2][MEM_G16];
   auto load = [&](int i) {
@@ -1006,7 +998,7 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
       }
   };
   if (active && nh > 0) load(0);
-  if (a.early) pdl_wait();  // C comes from the previous launch
+  if (state_early) pdl_wait();  // C comes from the previous launch
   // B fragments (C of this request, slot g8), held for all heads
   uint32_t bf[MEM_G16][4];
   {
@@ -1159,7 +1151,7 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
                                 const float* state, void* mix, const CUtensorMap* mk,
                                 const CUtensorMap* mv, int32_t* err, int num_sms, int early,
-                                cudaStream_t st, int* launches) {
+                                int with_mem, cudaStream_t st, int* launches) {
   if (B <= 0) return cudaSuccess;
   const bool tc = attn_uses_tc(d, dtype) && mk && mv;
   Args a{};
@@ -1172,7 +1164,7 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   // memory-read CTAs: one head each up to ~8 CTAs per SM, then several
   a.hpc = (B * d.Hm + 8 * num_sms - 1) / (8 * num_sms);
   if (a.hpc < 1) a.hpc = 1;
-  a.n_mem = B * ((d.Hm + a.hpc - 1) / a.hpc);
+  a.n_mem = with_mem ? B * ((d.Hm + a.hpc - 1) / a.hpc) : 0;
   a.mem_tc = tc && mem_tc_ok(d) ? 1 : 0;
   a.qscale = 1.4426950408889634f / sqrtf((float)d.dh);
   a.proj = proj;
@@ -1182,7 +1174,7 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   a.state = state;
   a.mix = mix;
   a.err = err;
-  a.early = early && tc;
+  a.early = tc ? early : 0;
   const int cz = a.plan.nsplit;
   const int total = (a.n_attn + a.n_mem + cz - 1) / cz * cz;
   cudaLaunchConfig_t cfg = {};

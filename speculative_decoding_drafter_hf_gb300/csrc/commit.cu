@@ -13,29 +13,93 @@
 namespace hf {
 namespace {
 
-constexpr int QPT = 2;  // float4 state elements per thread of the state update
+constexpr int THREADS_CS = 256;
+constexpr int QPT_HEAD = 8;  // float4 elements per thread when one CTA holds a whole head (P*N <= 8192)
 
-// grid (Hm * qsplit, B, L): CTA (h, q) takes 1/qsplit of the state of one
-// (layer, request, head), reads it once (all loads in flight together),
+// Shared memory of the state-update kernel: staged x / B / dt rows (and C
+// when the memory read is fused), then the padded copy of the new state and
+// the k-part sums of the memory read.
+struct CsLayout {
+  size_t sx, sb, sd, rows, red, total;  // float offsets
+};
+__host__ __device__ inline CsLayout cs_layout(const Dims& d, bool read) {
+  CsLayout m{};
+  const int lim = d.S + 1;
+  m.sx = 0;
+  m.sb = m.sx + (size_t)lim * d.P;
+  m.sd = m.sb + (size_t)lim * d.N;
+  m.rows = m.sd + ((lim + 3) & ~3);
+  m.red = m.rows + (read ? (size_t)d.P * (d.N + 8) : 0);
+  m.total = m.red + (read ? (size_t)mem_ksplit(d) * d.P * 8 : 0);
+  return m;
+}
+
+// grid (Hm * qsplit, B, L): CTA (h * qsplit + q, b, l) takes the q-th of
+// qsplit slices (QPT float4 per thread, whole state rows) of the state of
+// one (layer, request, head), reads it once (all loads in flight together),
 // advances it over the request's accepted rows in order, and writes it once.
-// CTA (0, b, 0) also checks n_b, writes offsets[b] (and offsets[B]), the ring
-// tags of the appended positions, and pos[b] += n_b.
-__global__ void __launch_bounds__(256)
-commit_state_kernel(Dims d, int B, int qsplit, const int32_t* __restrict__ n_acc,
+// Small batches split a head over several CTAs (more loads in flight);
+// large batches, and the fused memory read, take a whole head per CTA.
+// CTA (0, b, 0) also checks n_b, writes offsets[b] (and offsets[B]), the
+// ring tags of the appended positions, and pos[b] += n_b.
+//
+// early: the previous launch signalled its dependents after its own wait, so
+// the state, positions and counts are final at launch: they are read before
+// this launch's wait (only the staged projections come from that launch).
+// late: signal dependents only after this launch's own wait, so that the
+// next launch may read what the launches before this one wrote.
+//
+// With memC set, the layer-0 CTAs also make the next draft's memory read on
+// the state they hold, once it is final: y[s, p] = sum_n h[p, n] C[s, n]
+// (C: the slot projections of that draft, rows b*S + s with stride Nd) on
+// the tensor cores from a padded shared-memory copy of the new state, into
+// mix[b*S + s][QD + h*P + p] -- the values the draft-time read would
+// produce, without reading the state a second time.
+template <typename T, int QPT>
+__global__ void __launch_bounds__(THREADS_CS)
+commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
+                    const int32_t* __restrict__ n_acc,
                     const float* __restrict__ xbd, long long xls,
                     const float* __restrict__ A_log, float* __restrict__ state,
                     int64_t* __restrict__ pos, int32_t* __restrict__ offsets,
-                    int32_t* __restrict__ tags, int32_t* __restrict__ err) {
+                    int32_t* __restrict__ tags, int32_t* __restrict__ err,
+                    const float* __restrict__ memC, T* __restrict__ mix) {
   extern __shared__ __align__(16) float sm[];
-  pdl_trigger();
-  pdl_wait();
-  const int hd = blockIdx.x / qsplit, qs = blockIdx.x % qsplit;
-  const int b = blockIdx.y, l = blockIdx.z;
+  if (!late) pdl_trigger();
+  if (!early) {
+    pdl_wait();
+    if (late) pdl_trigger();
+  }
+  const int hd = blockIdx.x / qsplit, qs = blockIdx.x % qsplit, b = blockIdx.y, l = blockIdx.z;
   const int lim = d.S + 1;
   const int n_raw = __ldcg(&n_acc[b]);
   const bool valid = n_raw >= 0 && n_raw <= lim;
   const int n = valid ? n_raw : 0;
-  if (blockIdx.x == 0 && l == 0) {
+  const bool read = memC != nullptr && l == 0;  // (then qsplit == 1)
+  const bool bookkeeper = blockIdx.x == 0 && l == 0;
+  if (n == 0 && !read && !bookkeeper) return;
+  const int P = d.P, N = d.N;
+  float4* h = reinterpret_cast<float4*>(state + ((((size_t)l * d.Bmax + b) * d.Hm + hd) * P) * N);
+  const int nq = P * N / 4;
+  const int q0 = qs * QPT * THREADS_CS;
+  const bool work = n > 0 || read;
+  float4 hv[QPT];
+  int pi[QPT], ci[QPT];
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {  // elements past the head: index 0 (in bounds), never stored
+    const int q = q0 + threadIdx.x + u * THREADS_CS;
+    const bool in = work && q < nq;
+    hv[u] = in ? __ldcg(&h[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    pi[u] = in ? (q * 4) / N : 0;
+    ci[u] = in ? (q * 4) % N : 0;
+  }
+  // The previous launch (the commit projection) reads the positions in its
+  // epilogue and writes the staged rows: wait before touching either.
+  if (early) {
+    pdl_wait();
+    if (late) pdl_trigger();
+  }
+  if (bookkeeper) {
     __shared__ long long s_pos;
     if (threadIdx.x < 32) {
       int part = 0;
@@ -58,24 +122,12 @@ commit_state_kernel(Dims d, int B, int qsplit, const int32_t* __restrict__ n_acc
       tags[(size_t)b * d.W + (int)((p0 + t) % d.W)] = (int32_t)(p0 + t);
     if (threadIdx.x == 0) pos[b] = p0 + n;
   }
-  if (n == 0) return;
-  const int P = d.P, N = d.N;
-  float4* h = reinterpret_cast<float4*>(state + ((((size_t)l * d.Bmax + b) * d.Hm + hd) * P) * N);
-  const int nq = P * N / 4;
-  const int q0 = qs * (QPT * (int)blockDim.x);
-  float4 hv[QPT];
-  int pi[QPT], ci[QPT];
-#pragma unroll
-  for (int u = 0; u < QPT; ++u) {
-    const int q = q0 + threadIdx.x + u * blockDim.x;
-    hv[u] = q < nq ? __ldcg(&h[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
-    pi[u] = (q * 4) / N;
-    ci[u] = (q * 4) % N;
-  }
+  if (!work) return;
   // stage x (this head), B and dt of the n accepted rows b*(S+1) + t
-  float* sx = sm;             // [lim][P]
-  float* sb = sx + lim * P;   // [lim][N]
-  float* sd = sb + lim * N;   // [lim]
+  const CsLayout L = cs_layout(d, read);
+  float* sx = sm + L.sx;  // [lim][P]
+  float* sb = sm + L.sb;  // [lim][N]
+  float* sd = sm + L.sd;  // [lim]
   const float* xb = xbd + (size_t)l * xls + (size_t)b * lim * d.NS;
   for (int i = threadIdx.x; i < n * (P / 4); i += blockDim.x) {
     const int t = i / (P / 4), c = (i % (P / 4)) * 4;
@@ -104,24 +156,117 @@ commit_state_kernel(Dims d, int B, int qsplit, const int32_t* __restrict__ n_acc
       hv[u].w = fmaf(dec, hv[u].w, xv * Bv.w);
     }
   }
+  if (n > 0) {
+#pragma unroll
+    for (int u = 0; u < QPT; ++u) {
+      const int q = q0 + threadIdx.x + u * THREADS_CS;
+      if (q < nq) h[q] = hv[u];
+    }
+  }
+  if (!read) return;
+
+  // ---- memory read of the new state (tensor cores; see common.cuh)
+  const int RS = N + 8;  // padded row stride (floats): A-fragment loads conflict-free
+  float* rows = sm + L.rows;
+  float* red = sm + L.red;
 #pragma unroll
   for (int u = 0; u < QPT; ++u) {
-    const int q = q0 + threadIdx.x + u * blockDim.x;
-    if (q < nq) h[q] = hv[u];
+    const int q = q0 + threadIdx.x + u * THREADS_CS;
+    if (q < nq) *reinterpret_cast<float4*>(&rows[pi[u] * RS + ci[u]]) = hv[u];
+  }
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int MT = P / 16, KSPL = mem_ksplit(d), G16 = N / 16 / KSPL;
+  const int mt = warp % MT, kp = warp / MT;
+  const bool active = kp < KSPL;
+  const int r0 = mt * 16 + g8;
+  const int col0 = kp * G16 * 16 + 4 * t4;
+  uint32_t bf[MEM_G16][4];
+  {
+    const float* crow = memC + ((size_t)b * d.S + g8) * d.Nd + col0;
+#pragma unroll
+    for (int j = 0; j < MEM_G16; ++j) {
+      float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (active && j < G16 && g8 < d.S) c = __ldcg(reinterpret_cast<const float4*>(crow + j * 16));
+      bf[j][0] = to_tf32(c.x);
+      bf[j][1] = to_tf32(c.y);
+      bf[j][2] = to_tf32(c.z);
+      bf[j][3] = to_tf32(c.w);
+    }
+  }
+  __syncthreads();  // the new state is in shared memory
+  if (active) {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < MEM_G16; ++j)
+      if (j < G16) {
+        const float4 x0 = *reinterpret_cast<const float4*>(&rows[r0 * RS + col0 + j * 16]);
+        const float4 x1 = *reinterpret_cast<const float4*>(&rows[(r0 + 8) * RS + col0 + j * 16]);
+        mma_tf32_1688(c, to_tf32(x0.x), to_tf32(x1.x), to_tf32(x0.y), to_tf32(x1.y), bf[j][0],
+                      bf[j][1]);
+        mma_tf32_1688(c, to_tf32(x0.z), to_tf32(x1.z), to_tf32(x0.w), to_tf32(x1.w), bf[j][2],
+                      bf[j][3]);
+      }
+    float* rp = red + ((size_t)kp * P + r0) * 8 + 2 * t4;
+    *reinterpret_cast<float2*>(rp) = make_float2(c[0], c[1]);
+    *reinterpret_cast<float2*>(rp + 64) = make_float2(c[2], c[3]);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < d.S * P; e += blockDim.x) {
+    const int sl = e / P, p = e % P;
+    float y = 0.f;
+    for (int q = 0; q < KSPL; ++q) y += red[((size_t)q * P + p) * 8 + sl];
+    mix[((size_t)b * d.S + sl) * d.Nz + d.QD + (size_t)hd * P + p] = from_f<T>(y);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_commit_state(const Dims& d, int B, const int32_t* n_acc, const float* xbd,
-                                long long xls, const float* A_log, float* state, int64_t* pos,
-                                int32_t* offsets, int32_t* tags, int32_t* err, cudaStream_t st) {
-  // staging for block+1 rows of x (P values), B (N values) and dt
-  const size_t smem = (size_t)(d.S + 1) * (d.P + d.N + 1) * sizeof(float);
+size_t commit_state_smem(const Dims& d, bool read) { return cs_layout(d, read).total * sizeof(float); }
+
+namespace {
+template <typename K>
+cudaError_t set_smem(K kernel, int smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+}  // namespace
+
+cudaError_t configure_commit_state(const Dims& d) {
+  static int configured = 0;  // attribute of the kernel: keep the largest need
+  const int smem = (int)commit_state_smem(d, mem_tc_ok(d));
+  if (smem <= configured) return cudaSuccess;
+  cudaError_t e = set_smem(commit_state_kernel<float, 2>, smem);
+  if (e == cudaSuccess) e = set_smem(commit_state_kernel<float, QPT_HEAD>, smem);
+  if (e == cudaSuccess) e = set_smem(commit_state_kernel<__nv_bfloat16, 2>, smem);
+  if (e == cudaSuccess) e = set_smem(commit_state_kernel<__nv_bfloat16, QPT_HEAD>, smem);
+  if (e == cudaSuccess) configured = smem;
+  return e;
+}
+
+cudaError_t launch_commit_state(int dtype, const Dims& d, int B, const int32_t* n_acc,
+                                const float* xbd, long long xls, const float* A_log, float* state,
+                                int64_t* pos, int32_t* offsets, int32_t* tags, int32_t* err,
+                                const float* memC, void* mix, int early, int late,
+                                int num_sms, cudaStream_t st) {
+  if (memC && (dtype != HF_BF16 || !mem_tc_ok(d))) return cudaErrorInvalidValue;
   const int nq = d.P * d.N / 4;
-  const int qsplit = (nq + QPT * 256 - 1) / (QPT * 256);
-  return launch_pdl(commit_state_kernel, dim3(d.Hm * qsplit, B, d.L), dim3(256), smem, st, d, B,
-                    qsplit, n_acc, xbd, xls, A_log, state, pos, offsets, tags, err);
+  if (nq > QPT_HEAD * THREADS_CS) return cudaErrorInvalidValue;
+  // whole heads per CTA when fused or when they alone give ~4 CTAs per SM
+  const bool whole = memC != nullptr || (long long)B * d.Hm * d.L >= 4LL * num_sms;
+  const int qpt = whole ? QPT_HEAD : 2;
+  const int qsplit = (nq + qpt * THREADS_CS - 1) / (qpt * THREADS_CS);
+  const size_t smem = commit_state_smem(d, memC != nullptr);
+  const dim3 grid(d.Hm * qsplit, B, d.L);
+  const dim3 blk(THREADS_CS);
+  if (dtype == HF_F32) {
+    auto k = whole ? commit_state_kernel<float, QPT_HEAD> : commit_state_kernel<float, 2>;
+    return launch_pdl(k, grid, blk, smem, st, d, B, qsplit, early, late, n_acc, xbd, xls, A_log,
+                      state, pos, offsets, tags, err, memC, (float*)mix);
+  }
+  auto k = whole ? commit_state_kernel<__nv_bfloat16, QPT_HEAD>
+                 : commit_state_kernel<__nv_bfloat16, 2>;
+  return launch_pdl(k, grid, blk, smem, st, d, B, qsplit, early, late, n_acc, xbd, xls, A_log,
+                    state, pos, offsets, tags, err, memC, (__nv_bfloat16*)mix);
 }
 
 }  // namespace hf

@@ -312,6 +312,45 @@ __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
   }
 }
 
+// ------------------------------------------------- memory read, tensor cores
+// y[s, p] = sum_n h[p, n] C[s, n] of one (request, memory head) as a
+// [P x N] x [N x 8] product on mma.sync m16n8k8 tf32 (fp32 accumulate; h
+// and C rounded to tf32 with round-to-nearest, relative error 2^-11, below
+// the bf16 rounding of the output). Warp (m-tile, k-part) takes 16 state
+// rows and N / parts columns; within each group of 16 columns lane t holds
+// columns 4t..4t+3 and serves two k-steps (columns 4t, 4t+1 as logical
+// k = t, t + 4, then 4t+2, 4t+3): the same permutation on both operands,
+// so the sum is unchanged.
+constexpr int MEM_G16 = 8;  // 16-column groups per warp (N <= 128)
+
+__host__ __device__ inline bool mem_tc_ok(const Dims& d) {
+  return d.P % 16 == 0 && d.P <= 128 && d.N % 16 == 0 && d.N <= 128 && d.S <= 8;
+}
+__host__ __device__ inline int mem_ksplit(const Dims& d) {
+  const int mt = d.P / 16;
+  int ks = mt >= 8 ? 1 : 8 / mt;
+  while (ks > 1 && (d.N / 16) % ks) --ks;
+  return ks;
+}
+__host__ __device__ inline size_t mem_tc_bytes(const Dims& d) {
+  return (size_t)mem_ksplit(d) * d.P * 8 * 4;
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ void mma_tf32_1688(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // ---------------------------------------------------------------- launchers
 // Every launcher enqueues on `st` and returns cudaGetLastError().
 
@@ -335,6 +374,13 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
                            int N, int K, int swap, int splits, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches, const void* a_tiles = nullptr,
                            int late_trigger = 0);
+// Two swapped products with the same K in one launch (both A operands
+// pre-tiled): D0 = A0 B0^T with epilogue epi0, D1 = A1 B1^T with epi1.
+cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, const void* B0, long long ldb0,
+                                   int N0, const Epi& epi0, const void* a_tiles1, int M1,
+                                   const void* B1, long long ldb1, int N1, const Epi& epi1, int K,
+                                   int splits, int32_t* err, cudaStream_t st, int* launches,
+                                   int late_trigger = 0);
 void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst);
 
 // Persistent warp-specialised bf16 GEMM for large token-major products
@@ -363,6 +409,10 @@ cudaError_t configure_attn_cluster(const Dims& d);
 // bf16 handles with head_dim % 64 == 0 run the tensor-core variant, which
 // loads ring tiles through the per-layer tensor maps mk / mv (rows =
 // Bmax*Hkv*W, box attn_tile_rows(d) rows); other handles pass NULL maps.
+// early: what the previous launch (which signalled its dependents after its
+// own wait) leaves final at launch, read before this launch's wait:
+// bit 0 the ring K/V, bit 1 the positions and states.
+// with_mem = 0: attention only (the memory read was done elsewhere).
 size_t attn_cluster_smem(const Dims& d, int esize);
 int attn_tile_rows(const Dims& d);
 bool attn_uses_tc(const Dims& d, int dtype);
@@ -370,16 +420,22 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
                                 const float* state, void* mix, const CUtensorMap* mk,
                                 const CUtensorMap* mv, int32_t* err, int num_sms, int early,
-                                cudaStream_t st, int* launches);
+                                int with_mem, cudaStream_t st, int* launches);
 
 // Commit state step, all layers: validates the accepted counts (error word),
 // writes the packed offsets (exclusive scan of the valid counts) and the ring
 // tags of the appended positions, advances the memory over rows
-// b*(S+1) + t < b*(S+1) + n_b of xbd in order, then pos += n.
-cudaError_t launch_commit_state(const Dims& d, int B, const int32_t* n_acc, const float* xbd,
-                                long long xbd_layer_stride, const float* A_log, float* state,
-                                int64_t* pos, int32_t* offsets, int32_t* tags, int32_t* err,
-                                cudaStream_t st);
+// b*(S+1) + t < b*(S+1) + n_b of xbd in order, then pos += n. memC (or
+// NULL): C columns of the next draft's layer-0 slot projections (row
+// stride Nd); the layer-0 memory read of that draft is then done here, on
+// the new state, into the memory columns of mix (model dtype).
+size_t commit_state_smem(const Dims& d, bool read);
+cudaError_t configure_commit_state(const Dims& d);  // at handle creation
+cudaError_t launch_commit_state(int dtype, const Dims& d, int B, const int32_t* n_acc,
+                                const float* xbd, long long xbd_layer_stride, const float* A_log,
+                                float* state, int64_t* pos, int32_t* offsets, int32_t* tags,
+                                int32_t* err, const float* memC, void* mix, int early,
+                                int late, int num_sms, cudaStream_t st);
 
 // Prefill helpers (lens/reqs/cu are device int32 arrays of n_req entries).
 cudaError_t launch_prefill_reset(const Dims& d, int n_req, const int32_t* reqs,

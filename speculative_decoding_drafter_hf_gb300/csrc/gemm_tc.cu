@@ -64,6 +64,12 @@ struct TcArgs {
                            // one bulk copy; NULL: A read through the tensor map
   int32_t* err;       // device error word
   int late_trigger;   // 1: signal dependents only after the dependency wait
+  // Grouped launch: m-tiles [mt0, ...) belong to a second product with the
+  // same K (its own A tiles, B map, N and epilogue). mt0 = all m-tiles when
+  // there is one product.
+  int mt0;
+  int M1, N1;
+  const uint8_t* a_tiles1;
 };
 
 // Epilogue cache (shared memory after the barriers): per output row of the
@@ -78,8 +84,9 @@ struct EpiCache {
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(128, 1)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-               TcArgs a, Epi epi) {
+tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb0,
+               const __grid_constant__ CUtensorMap tb1, TcArgs a, const __grid_constant__ Epi epi0,
+               const __grid_constant__ Epi epi1) {
   constexpr int A_BYTES = 128 * 128;
   constexpr int B_BYTES = BN * 128;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -103,7 +110,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   // grid (splits, m_tiles, n_tiles); the splits of one tile form a cluster along x
-  const int split = blockIdx.x, m_tile = blockIdx.y, n_tile = blockIdx.z;
+  const int split = blockIdx.x, n_tile = blockIdx.z;
+  const bool second = (int)blockIdx.y >= a.mt0;  // tile of the second product
+  const int m_tile = second ? (int)blockIdx.y - a.mt0 : (int)blockIdx.y;
+  const int M = second ? a.M1 : a.M, N = second ? a.N1 : a.N;
+  const uint8_t* a_tiles = second ? a.a_tiles1 : a.a_tiles;
+  const CUtensorMap* tb = second ? &tb1 : &tb0;
+  const Epi& epi = second ? epi1 : epi0;
+  if (n_tile * BN >= N) return;  // the other product has more n-tiles (whole cluster)
   const int kb0 = (int)((long long)split * a.kblocks / a.splits);
   const int kb1 = (int)((long long)(split + 1) * a.kblocks / a.splits);
   const int nkb = kb1 - kb0;
@@ -136,9 +150,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     const int pre = nkb < STAGES ? nkb : STAGES;
     // A tile of local k-block i into stage st
     auto load_a = [&](int st, int i) {
-      if (a.a_tiles)
+      if (a_tiles)
         bulk_g2s(sA + st * A_BYTES,
-                 a.a_tiles + ((size_t)m_tile * a.kblocks + (kb0 + i)) * (size_t)A_BYTES, A_BYTES,
+                 a_tiles + ((size_t)m_tile * a.kblocks + (kb0 + i)) * (size_t)A_BYTES, A_BYTES,
                  &full[st]);
       else
         tma_load_2d(sA + st * A_BYTES, &ta, &full[st], (kb0 + i) * 64, m_tile * 128);
@@ -151,14 +165,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       pdl_wait();
       if (a.late_trigger) pdl_trigger();
       for (int j = 0; j < pre; ++j)
-        tma_load_2d(sB + j * B_BYTES, &tb, &full[j], (kb0 + j) * 64, n_tile * BN);
+        tma_load_2d(sB + j * B_BYTES, tb, &full[j], (kb0 + j) * 64, n_tile * BN);
     } else {
       pdl_wait();
       if (a.late_trigger) pdl_trigger();
       for (int j = 0; j < pre; ++j) {
         mbar_expect_tx(&full[j], STAGE_BYTES);
         load_a(j, j);
-        tma_load_2d(sB + j * B_BYTES, &tb, &full[j], (kb0 + j) * 64, n_tile * BN);
+        tma_load_2d(sB + j * B_BYTES, tb, &full[j], (kb0 + j) * 64, n_tile * BN);
       }
     }
     int i = pre;
@@ -172,7 +186,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       if (*(volatile int*)&flags[0]) break;
       mbar_expect_tx(&full[s], STAGE_BYTES);
       load_a(s, i);
-      tma_load_2d(sB + s * B_BYTES, &tb, &full[s], (kb0 + i) * 64, n_tile * BN);
+      tma_load_2d(sB + s * B_BYTES, tb, &full[s], (kb0 + i) * 64, n_tile * BN);
     }
     flags[1] = i;
   } else if (a.late_trigger) {
@@ -203,7 +217,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   }
   __syncwarp();
   pdl_wait();  // the epilogue writes memory earlier kernels may still read
-  const int n_here = min(BN, a.N - n_tile * BN);
+  const int n_here = min(BN, N - n_tile * BN);
   if (warp >= 2 && a.swap) {  // idle during the main loop: fetch the epilogue inputs
     const int t2 = tid - 64;
     if (epi.kind == EPI_SSM_KV) {
@@ -218,7 +232,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(epi.resid);
       for (int i = t2; i < n_here * 128; i += 64) {
         const int nl = i >> 7, mq = m_tile * 128 + (i & 127);
-        ep_res[i] = mq < a.M ? to_f(__ldcg(&res[(size_t)(n_tile * BN + nl) * epi.ld + mq])) : 0.f;
+        ep_res[i] = mq < M ? to_f(__ldcg(&res[(size_t)(n_tile * BN + nl) * epi.ld + mq])) : 0.f;
       }
     }
   }
@@ -248,7 +262,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
   float v[16];
   // this thread's output column of the commit projection (swap only)
-  const SsmCol scol = (a.swap && epi.kind == EPI_SSM_KV && m < a.M) ? ssm_col(epi, m)
+  const SsmCol scol = (a.swap && epi.kind == EPI_SSM_KV && m < M) ? ssm_col(epi, m)
                                                                       : SsmCol{0, nullptr, 0, 0.f};
   // Output of tile row nl (activation row n) and this thread's column m.
   auto emit = [&](int nl, float val) {
@@ -270,7 +284,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 16) {
       tmem_ld16(trow + c0, v);
-      if (m < a.M && c0 < n_here) {
+      if (m < M && c0 < n_here) {
         if (!a.swap) {
           epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
         } else if (epi.kind == EPI_RESID && RES_ROWS == 0) {
@@ -317,7 +331,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
         for (int sp = 0; sp < 8; ++sp) sum += part[sp];
         v[j] = sum;
       }
-      if (m < a.M) epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
+      if (m < M) epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
     }
     cluster_sync_all();  // partners keep their shared memory until all reads are done
   } else {
@@ -342,7 +356,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       float sum = 0.f;
 #pragma unroll
       for (int sp = 0; sp < 8; ++sp) sum += part[sp];
-      if (m < a.M) emit(nl, sum);
+      if (m < M) emit(nl, sum);
     }
     cluster_sync_all();  // partners keep their shared memory until all reads are done
   }
@@ -393,6 +407,11 @@ cudaError_t make_map(CUtensorMap* map, const void* base, long long rows, long lo
 
 namespace {
 
+// Pipeline depth of the narrow tiles (skinny products at small batch): a
+// deep ring (one CTA per SM, ~130 KB in flight); 5 / 4 stages (two CTAs per
+// SM) measured slower at batch 1.
+constexpr int kStages16 = 7, kStages32 = 6;
+
 template <int BN, int STAGES>
 constexpr size_t tc_smem() {
   // 1 KB alignment slack, stages, barriers, TMEM slot + flags (28 B), epilogue cache
@@ -431,11 +450,23 @@ cudaLaunchConfig_t tc_config(dim3 grid, int cz, cudaStream_t st, cudaLaunchAttri
 }
 
 template <int BN, int STAGES>
-cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& a,
-                      const Epi& epi, dim3 grid, cudaStream_t st) {
+cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1,
+                      const TcArgs& a, const Epi& epi0, const Epi& epi1, dim3 grid,
+                      cudaStream_t st) {
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = tc_config<BN, STAGES>(grid, a.splits, st, attr);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES>, ma, mb, a, epi);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES>, ma, mb0, mb1, a, epi0, epi1);
+}
+
+template <typename... X>
+cudaError_t launch_bn(int bn, X&&... x) {
+  switch (bn) {
+    case 16: return launch_tc<16, kStages16>(x...);
+    case 32: return launch_tc<32, kStages32>(x...);
+    case 64: return launch_tc<64, 5>(x...);
+    case 128: return launch_tc<128, 4>(x...);
+    default: return launch_tc<256, 4>(x...);
+  }
 }
 
 // How many clusters of cz CTAs of this instantiation are resident at once
@@ -462,15 +493,15 @@ int g_max_clusters[5][9] = {};  // [log2(BN/16)][cz]
 // that launches stay legal inside stream capture.
 cudaError_t configure_tc() {
   cudaError_t e = get_encoder();
-  if (e == cudaSuccess) e = configure_one<16, 7>();
-  if (e == cudaSuccess) e = configure_one<32, 6>();
+  if (e == cudaSuccess) e = configure_one<16, kStages16>();
+  if (e == cudaSuccess) e = configure_one<32, kStages32>();
   if (e == cudaSuccess) e = configure_one<64, 5>();
   if (e == cudaSuccess) e = configure_one<128, 4>();
   if (e == cudaSuccess) e = configure_one<256, 4>();
   if (e != cudaSuccess) return e;
   for (int cz = 1; cz <= 8; ++cz) {
-    g_max_clusters[0][cz] = max_clusters<16, 7>(cz);
-    g_max_clusters[1][cz] = max_clusters<32, 6>(cz);
+    g_max_clusters[0][cz] = max_clusters<16, kStages16>(cz);
+    g_max_clusters[1][cz] = max_clusters<32, kStages32>(cz);
     g_max_clusters[2][cz] = max_clusters<64, 5>(cz);
     g_max_clusters[3][cz] = max_clusters<128, 4>(cz);
     g_max_clusters[4][cz] = max_clusters<256, 4>(cz);
@@ -515,6 +546,7 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   a.splits = std::max(1, std::min(std::min(splits, 8), a.kblocks));
   a.a_tiles = static_cast<const uint8_t*>(a_tiles);
   a.late_trigger = late_trigger;
+  a.mt0 = m_tiles;
   CUtensorMap ma, mb;
   cudaError_t e = make_map(&mb, B, N, K, ldb, bn);
   if (e != cudaSuccess) return e;
@@ -525,13 +557,44 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   if (m_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
   dim3 grid(a.splits, m_tiles, n_tiles);
   ++*launches;
-  switch (bn) {
-    case 16: return launch_tc<16, 7>(ma, mb, a, epi, grid, st);
-    case 32: return launch_tc<32, 6>(ma, mb, a, epi, grid, st);
-    case 64: return launch_tc<64, 5>(ma, mb, a, epi, grid, st);
-    case 128: return launch_tc<128, 4>(ma, mb, a, epi, grid, st);
-    default: return launch_tc<256, 4>(ma, mb, a, epi, grid, st);
-  }
+  return launch_bn(bn, ma, mb, mb, a, epi, epi, grid, st);
+}
+
+cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, const void* B0, long long ldb0,
+                                   int N0, const Epi& epi0, const void* a_tiles1, int M1,
+                                   const void* B1, long long ldb1, int N1, const Epi& epi1, int K,
+                                   int splits, int32_t* err, cudaStream_t st, int* launches,
+                                   int late_trigger) {
+  if (M0 <= 0 || N0 <= 0 || M1 <= 0 || N1 <= 0 || !a_tiles0 || !a_tiles1)
+    return cudaErrorInvalidValue;
+  const int nmax = N0 > N1 ? N0 : N1;
+  int bn = 16;
+  while (bn < nmax && bn < 256) bn *= 2;
+  const int mt0 = (M0 + 127) / 128, mt1 = (M1 + 127) / 128;
+  const int n_tiles = (nmax + bn - 1) / bn;
+  TcArgs a{};
+  a.M = M0;
+  a.N = N0;
+  a.K = K;
+  a.kblocks = (K + 63) / 64;
+  a.swap = 1;
+  a.prefetch_a = 1;
+  a.err = err;
+  a.splits = std::max(1, std::min(std::min(splits, 8), a.kblocks));
+  a.a_tiles = static_cast<const uint8_t*>(a_tiles0);
+  a.late_trigger = late_trigger;
+  a.mt0 = mt0;
+  a.M1 = M1;
+  a.N1 = N1;
+  a.a_tiles1 = static_cast<const uint8_t*>(a_tiles1);
+  CUtensorMap mb0, mb1;
+  cudaError_t e = make_map(&mb0, B0, N0, K, ldb0, bn);
+  if (e == cudaSuccess) e = make_map(&mb1, B1, N1, K, ldb1, bn);
+  if (e != cudaSuccess) return e;
+  if (mt0 + mt1 > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
+  dim3 grid(a.splits, mt0 + mt1, n_tiles);
+  ++*launches;
+  return launch_bn(bn, mb0, mb0, mb1, a, epi0, epi1, grid, st);
 }
 
 // Re-lay a row-major bf16 matrix [M][K] (host) as 128 x 64 tiles in the

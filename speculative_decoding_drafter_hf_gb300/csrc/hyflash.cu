@@ -449,6 +449,7 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     e = hf::configure_attn_cluster(h->d);
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc();
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc_persistent(h->num_sms);
+    if (e == cudaSuccess) e = hf::configure_commit_state(h->d);
     if (e != cudaSuccess) s = cuda_fail(h, e, "kernel set-up");
   }
   if (s == HF_OK) {
@@ -532,71 +533,63 @@ hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w)
   return HF_OK;
 }
 
-hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch, void* stream) {
-  if (!h) return HF_EINVAL;
-  if (!slot_emb || !out) return fail(h, HF_EINVAL, "NULL buffer");
-  if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
-  if (slot_emb == out) return fail(h, HF_EINVAL, "out may not alias slot_emb");
-  if (reinterpret_cast<uintptr_t>(slot_emb) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
-    return fail(h, HF_EINVAL, "slot_emb and out must be 16-byte aligned");
-  if (batch == 0) return HF_OK;
-  HF_CUDA(h, ensure_device(h));
-  cudaStream_t st = (cudaStream_t)stream;
+namespace {
+
+constexpr int kEarlyRing = 1, kEarlyAll = 3;  // attention launch: what it may read before waiting
+// hf_round folds the first layer's memory read into the state update once a
+// layer's states are at least this large (below, the read runs beside the
+// attention, off the round's critical path).
+constexpr size_t kFuseMemBytes = 16u << 20;
+
+// Slot projections of draft layer l (rows of X) into h->proj. With the
+// tensor-core attention the GEMM signals its dependents only after its own
+// dependency wait, so that the attention launch may read the ring, positions
+// and state (final by then) before its wait.
+hf_status draft_proj(hf_handle* h, int l, const void* X, int batch, int late, cudaStream_t st) {
   const Dims& d = h->d;
-  const size_t es = h->esz;
-  const int R = batch * d.S;
-  const size_t ring_ls = (size_t)d.Bmax * d.Hkv * d.W * d.dh * es;
-  const size_t state_ls = (size_t)d.Bmax * d.Hm * d.P * d.N;
-  for (int l = 0; l < d.L; ++l) {
-    const void* X = l == 0 ? slot_emb : h->xbuf[(l - 1) % 2];
-    void* Y = l == d.L - 1 ? out : h->xbuf[l % 2];
-    Epi e1 = epi_base(h);
-    e1.kind = hf::EPI_F32;
-    e1.out = h->proj;
-    e1.ld = d.Nd;
-    // With the tensor-core attention, the slot projection signals its
-    // dependents only after its own dependency wait: the attention launch may
-    // then read the ring, positions and state (final by then) before its wait.
-    const int early = h->ring_maps.empty() ? 0 : 1;
-    hf_status s = gemm(h, HF_K_DRAFT_PROJ, X, d.D, bptr(h->w_draft, (size_t)l * d.Nd * d.D * es),
-                       d.D, R, d.Nd, d.D, e1, st,
-                       h->wt_draft ? bptr(h->wt_draft, (size_t)l * h->wt_draft_l) : nullptr, early);
-    if (s != HF_OK) return s;
-    {
-      Scope sc(h, HF_K_ATTN_MEM, st);
-      const CUtensorMap* mk = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l];
-      const CUtensorMap* mv = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l + 1];
-      cudaError_t e = hf::launch_attn_cluster(h->cfg.dtype, d, batch, h->proj,
-                                              bptr(h->ring_k, l * ring_ls),
-                                              bptr(h->ring_v, l * ring_ls), h->pos,
-                                              h->state + l * state_ls, h->mix, mk, mv, h->err,
-                                              h->num_sms, early, st, &sc.count);
-      if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
-    }
-    Epi e2 = epi_base(h);
-    e2.kind = hf::EPI_RESID;
-    e2.resid = X;
-    e2.out_t = Y;
-    e2.ld = d.D;
-    s = gemm(h, HF_K_OUT_PROJ, h->mix, d.Nz, bptr(h->w_out, (size_t)l * d.D * d.Nz * es), d.Nz, R,
-             d.D, d.Nz, e2, st, h->wt_out ? bptr(h->wt_out, (size_t)l * h->wt_out_l) : nullptr);
-    if (s != HF_OK) return s;
-  }
-  return HF_OK;
+  Epi e1 = epi_base(h);
+  e1.kind = hf::EPI_F32;
+  e1.out = h->proj;
+  e1.ld = d.Nd;
+  return gemm(h, HF_K_DRAFT_PROJ, X, d.D, bptr(h->w_draft, (size_t)l * d.Nd * d.D * h->esz), d.D,
+              batch * d.S, d.Nd, d.D, e1, st,
+              h->wt_draft ? bptr(h->wt_draft, (size_t)l * h->wt_draft_l) : nullptr, late);
 }
 
-hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, int32_t batch,
-                    void* stream) {
-  if (!h) return HF_EINVAL;
-  if (!feats || !n_accepted) return fail(h, HF_EINVAL, "NULL buffer");
-  if (reinterpret_cast<uintptr_t>(feats) % 16) return fail(h, HF_EINVAL, "feats must be 16-byte aligned");
-  if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
-  if (batch == 0) return HF_OK;
-  HF_CUDA(h, ensure_device(h));
-  cudaStream_t st = (cudaStream_t)stream;
+// The rest of draft layer l once its slot projections are in h->proj:
+// attention (+ memory read unless with_mem = 0) into h->mix, then the
+// output projection with the residual X into Y.
+hf_status draft_rest(hf_handle* h, int l, const void* X, void* Y, int batch, int early,
+                     int with_mem, cudaStream_t st) {
   const Dims& d = h->d;
-  // Projections of all batch*(S+1) rows of all layers in one GEMM; the
-  // epilogue keeps only rows t < n_b (ring append at pos_b + t; x, B, dt).
+  const size_t es = h->esz;
+  const size_t ring_ls = (size_t)d.Bmax * d.Hkv * d.W * d.dh * es;
+  const size_t state_ls = (size_t)d.Bmax * d.Hm * d.P * d.N;
+  {
+    Scope sc(h, HF_K_ATTN_MEM, st);
+    const CUtensorMap* mk = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l];
+    const CUtensorMap* mv = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l + 1];
+    cudaError_t e = hf::launch_attn_cluster(h->cfg.dtype, d, batch, h->proj,
+                                            bptr(h->ring_k, l * ring_ls),
+                                            bptr(h->ring_v, l * ring_ls), h->pos,
+                                            h->state + l * state_ls, h->mix, mk, mv, h->err,
+                                            h->num_sms, early, with_mem, st, &sc.count);
+    if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
+  }
+  Epi e2 = epi_base(h);
+  e2.kind = hf::EPI_RESID;
+  e2.resid = X;
+  e2.out_t = Y;
+  e2.ld = d.D;
+  return gemm(h, HF_K_OUT_PROJ, h->mix, d.Nz, bptr(h->w_out, (size_t)l * d.D * d.Nz * es), d.Nz,
+              batch * d.S, d.D, d.Nz, e2, st,
+              h->wt_out ? bptr(h->wt_out, (size_t)l * h->wt_out_l) : nullptr);
+}
+
+// Commit-projection epilogue: of the batch*(S+1) rows of every layer only
+// rows t < n_b are kept (ring append at pos_b + t; x, B, dt into xbd).
+Epi commit_epi(const hf_handle* h, const int32_t* n_accepted) {
+  const Dims& d = h->d;
   Epi ep = epi_base(h);
   ep.kind = hf::EPI_SSM_KV;
   ep.layer0 = 0;
@@ -606,23 +599,129 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, 
   ep.pos = h->pos;
   ep.xbd = h->xbd;
   ep.xbd_layer_stride = h->xbd_ls;
-  const int rows = batch * (d.S + 1);
-  hf_status s;
   if (h->wt_commit) {  // pre-tiled: rows padded per layer to nc_pad, padding skipped
     ep.cols_per_layer = h->nc_pad;
     ep.cols_valid = d.Nc;
-    s = gemm(h, HF_K_COMMIT_PROJ, feats, d.D, h->w_commit, d.D, rows, d.L * h->nc_pad, d.D, ep, st,
-             h->wt_commit);
-  } else {
-    s = gemm(h, HF_K_COMMIT_PROJ, feats, d.D, h->w_commit, d.D, rows, d.L * d.Nc, d.D, ep, st);
   }
+  return ep;
+}
+
+// early: the commit projection signalled its dependents after its wait;
+// late: the next launch reads the ring before its own wait.
+hf_status commit_state(hf_handle* h, const int32_t* n_accepted, int batch, const float* memC,
+                       int early, int late, cudaStream_t st) {
+  const Dims& d = h->d;
+  Scope sc(h, HF_K_COMMIT_STATE, st);
+  cudaError_t e = hf::launch_commit_state(h->cfg.dtype, d, batch, n_accepted, h->xbd, h->xbd_ls,
+                                          h->A_log, h->state, h->pos, h->offsets, h->tags, h->err,
+                                          memC, h->mix, early, late, h->num_sms, st);
+  sc.count = 1;
+  if (e != cudaSuccess) return cuda_fail(h, e, "commit state launch");
+  return HF_OK;
+}
+
+hf_status check_draft_args(hf_handle* h, const void* slot_emb, void* out, int32_t batch) {
+  if (!slot_emb || !out) return fail(h, HF_EINVAL, "NULL buffer");
+  if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
+  if (slot_emb == out) return fail(h, HF_EINVAL, "out may not alias slot_emb");
+  if (reinterpret_cast<uintptr_t>(slot_emb) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(h, HF_EINVAL, "slot_emb and out must be 16-byte aligned");
+  return HF_OK;
+}
+
+hf_status check_commit_args(hf_handle* h, const void* feats, const int32_t* n_accepted,
+                            int32_t batch) {
+  if (!feats || !n_accepted) return fail(h, HF_EINVAL, "NULL buffer");
+  if (reinterpret_cast<uintptr_t>(feats) % 16) return fail(h, HF_EINVAL, "feats must be 16-byte aligned");
+  if (batch < 0 || batch > h->d.Bmax) return fail(h, HF_EINVAL, "batch out of range");
+  return HF_OK;
+}
+
+}  // namespace
+
+hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch, void* stream) {
+  if (!h) return HF_EINVAL;
+  hf_status s = check_draft_args(h, slot_emb, out, batch);
+  if (s != HF_OK || batch == 0) return s;
+  HF_CUDA(h, ensure_device(h));
+  cudaStream_t st = (cudaStream_t)stream;
+  const Dims& d = h->d;
+  const bool tc = !h->ring_maps.empty();
+  for (int l = 0; l < d.L; ++l) {
+    const void* X = l == 0 ? slot_emb : h->xbuf[(l - 1) % 2];
+    void* Y = l == d.L - 1 ? out : h->xbuf[l % 2];
+    if ((s = draft_proj(h, l, X, batch, tc, st)) != HF_OK) return s;
+    if ((s = draft_rest(h, l, X, Y, batch, tc ? kEarlyAll : 0, 1, st)) != HF_OK) return s;
+  }
+  return HF_OK;
+}
+
+hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, int32_t batch,
+                    void* stream) {
+  if (!h) return HF_EINVAL;
+  hf_status s = check_commit_args(h, feats, n_accepted, batch);
+  if (s != HF_OK || batch == 0) return s;
+  HF_CUDA(h, ensure_device(h));
+  cudaStream_t st = (cudaStream_t)stream;
+  const Dims& d = h->d;
+  // Projections of all batch*(S+1) rows of all layers in one GEMM.
+  const Epi ep = commit_epi(h, n_accepted);
+  const int rows = batch * (d.S + 1);
+  const int late = h->cfg.dtype == HF_BF16 ? 1 : 0;  // the tensor-core GEMM can signal late
+  s = gemm(h, HF_K_COMMIT_PROJ, feats, d.D, h->w_commit, d.D, rows,
+           d.L * (h->wt_commit ? h->nc_pad : d.Nc), d.D, ep, st, h->wt_commit, late);
   if (s != HF_OK) return s;
+  return commit_state(h, n_accepted, batch, nullptr, late, 0, st);
+}
+
+hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
+                   const void* slot_emb, void* out, int32_t batch, void* stream) {
+  if (!h) return HF_EINVAL;
+  hf_status s = check_commit_args(h, feats, n_accepted, batch);
+  if (s == HF_OK) s = check_draft_args(h, slot_emb, out, batch);
+  if (s != HF_OK || batch == 0) return s;
+  const bool fused = h->cfg.dtype == HF_BF16 && h->wt_commit && h->wt_draft && !h->ring_maps.empty();
+  if (!fused) {
+    s = hf_commit(h, feats, n_accepted, batch, stream);
+    return s != HF_OK ? s : hf_draft(h, slot_emb, out, batch, stream);
+  }
+  HF_CUDA(h, ensure_device(h));
+  cudaStream_t st = (cudaStream_t)stream;
+  const Dims& d = h->d;
+  // 1. commit projection (all layers) and the layer-0 slot projection in one
+  //    grouped launch: both stream their weights at once
   {
-    Scope sc(h, HF_K_COMMIT_STATE, st);
-    cudaError_t e = hf::launch_commit_state(d, batch, n_accepted, h->xbd, h->xbd_ls, h->A_log,
-                                            h->state, h->pos, h->offsets, h->tags, h->err, st);
-    sc.count = 1;
-    if (e != cudaSuccess) return cuda_fail(h, e, "commit state launch");
+    const Epi ec = commit_epi(h, n_accepted);
+    Epi e1 = epi_base(h);
+    e1.kind = hf::EPI_F32;
+    e1.out = h->proj;
+    e1.ld = d.Nd;
+    const int M0 = d.L * h->nc_pad, N0 = batch * (d.S + 1), N1 = batch * d.S;
+    const int splits =
+        hf::tc_pick_splits((M0 + 127) / 128 * 128 + d.Nd, std::max(N0, N1), d.D);
+    Scope sc(h, HF_K_ROUND_PROJ, st);
+    cudaError_t e = hf::launch_gemm_tc_grouped(h->wt_commit, M0, feats, d.D, N0, ec, h->wt_draft,
+                                               d.Nd, slot_emb, d.D, N1, e1, d.D, splits, h->err,
+                                               st, &sc.count, /*late_trigger=*/1);
+    if (e != cudaSuccess) return cuda_fail(h, e, "grouped projection launch");
+  }
+  // 2. state update; at large batch also the layer-0 memory read of the new
+  //    state (the state is then read once per round); it starts early (the
+  //    grouped projection signals late) and signals late itself, so that the
+  //    attention may request its ring tiles before waiting
+  const size_t state_layer_bytes = (size_t)batch * d.Hm * d.P * d.N * 4;
+  const bool fuse_mem = hf::mem_tc_ok(d) && state_layer_bytes >= kFuseMemBytes;
+  s = commit_state(h, n_accepted, batch, fuse_mem ? h->proj + d.QD + 2 * d.KVD : nullptr, 1, 1,
+                   st);
+  if (s != HF_OK) return s;
+  // 3. layer 0: attention and output projection; later layers as in hf_draft
+  for (int l = 0; l < d.L; ++l) {
+    const void* X = l == 0 ? slot_emb : h->xbuf[(l - 1) % 2];
+    void* Y = l == d.L - 1 ? out : h->xbuf[l % 2];
+    if (l > 0 && (s = draft_proj(h, l, X, batch, 1, st)) != HF_OK) return s;
+    const int with_mem = l > 0 || !fuse_mem;
+    if ((s = draft_rest(h, l, X, Y, batch, l > 0 ? kEarlyAll : kEarlyRing, with_mem, st)) != HF_OK)
+      return s;
   }
   return HF_OK;
 }

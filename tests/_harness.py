@@ -57,6 +57,17 @@ class Pair:
         ref = self.orc.draft(slot) if self.orc is not None else None
         return got, ref
 
+    def round(self, feats, n, slot):
+        """hf_round on the GPU; the oracle commits, then drafts."""
+        out = self.gpu.round(feats.cuda(), n.to(torch.int32).cuda(), slot.cuda())
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy().astype(np.float64)
+        offs = ref = None
+        if self.orc is not None:
+            offs, _ = self.orc.commit(feats, n.numpy())
+            ref = self.orc.draft(slot)
+        return got, ref, offs
+
     def check_context(self, requests=None, what=""):
         """State, ring (valid slots), tags and positions against the oracle."""
         cfg, g = self.cfg, self.gpu

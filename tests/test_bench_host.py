@@ -54,11 +54,21 @@ def test_single_process_reduction_is_identity():
 def test_algorithmic_bytes_qwen_shape():
     from workload import CONFIGS
     cfg = CONFIGS["qwen3_4b_bf16"]
-    a = bench.algorithmic(cfg, 1, 512, 4.5)
-    # draft weights alone: (Hq*dh + 2*Hkv*dh + N) * D + D * (Hq*dh + Hm*P), bf16
-    w = ((4096 + 2048 + 128) * 2560 + 2560 * (4096 + 5120)) * 2
-    assert w < a["draft_bytes"] < w * 1.1
-    assert a["step_bytes"] == a["draft_bytes"] + a["commit_bytes"]
+    fused = bench.algorithmic(cfg, 1, 512, 4.5, True)
+    sep = bench.algorithmic(cfg, 1, 512, 4.5, False)
+    # weights: draft (Hq*dh + 2*Hkv*dh + N) * D + D * (Hq*dh + Hm*P), commit
+    # (2*Hkv*dh + Hm*P + N + Hm) * D, bf16
+    w = ((4096 + 2048 + 128) * 2560 + 2560 * (4096 + 5120) + (2048 + 5120 + 128 + 80) * 2560) * 2
+    assert w < fused["step_bytes"] < w * 1.1
+    # the separate path moves the same bytes plus one more read of the state
+    state = 80 * 64 * 128 * 4
+    tot = lambda a: sum(b for b, _ in a["families"].values())
+    assert tot(fused) == fused["step_bytes"]
+    assert tot(sep) - tot(fused) == pytest.approx(state)
+    # one layer: every family of the fused path launches once, except the
+    # later-layer slot projections (none)
+    assert fused["families"]["draft_proj"] == (0, 0)
+    assert all(n == 1 for k, (_, n) in fused["families"].items() if k != "draft_proj")
 
 
 def test_clock_summary_parses_samples(tmp_path):

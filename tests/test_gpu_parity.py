@@ -279,3 +279,95 @@ def test_prefill_chunked_scan_segments_bf16(chunk, tokens_max):
     p.check_context(what=f"prefill chunk {chunk}")
     run_rounds(p, 2)
     p.close()
+
+
+def run_round_api(p: Pair, rounds: int, check_every: int = 1):
+    cfg = p.cfg
+    for r in range(rounds):
+        slot, feats = make_round_inputs(cfg, r, p.B)
+        n = make_accepted(cfg, r, p.B)
+        got, ref, offs = p.round(feats, n, slot)
+        e = maxnorm_err(got, ref)
+        assert e <= p.tol, f"round {r}: draft err {e:.3e}"
+        got_offs = p.gpu.read(Tensor.OFFSETS)
+        assert np.array_equal(got_offs[:p.B + 1], offs.astype(np.int32)), f"round {r}: offsets"
+        if (r + 1) % check_every == 0 or r == rounds - 1:
+            p.check_context(what=f"round {r}")
+
+
+@pytest.mark.parametrize("name,batch,rounds", [
+    ("tiny_fp32", 3, 6),              # two entry points in turn
+    ("qwen3_4b_bf16", 2, 5),          # grouped projection, memory read in the state update
+    ("serving_qwen3_4b_b64", 5, 3),   # three layers: later layers draft as in hf_draft
+])
+def test_round_api(name, batch, rounds):
+    """hf_round = hf_commit then hf_draft, against the oracle's commit then draft."""
+    cfg = CONFIGS[name].replace(batch=batch, prefix_lo=300, prefix_hi=900) \
+        if name.startswith("serving") else CONFIGS[name].replace(batch=batch)
+    p = Pair(cfg)
+    lens = make_prefix_lens(cfg)
+    lens = [min(L, 1200) for L in lens]
+    lens[0] = 0  # one empty window: attention over the slots only
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    run_round_api(p, rounds, check_every=2)
+    p.close()
+
+
+def test_round_api_rejected_and_invalid_counts():
+    """Zero, full and invalid accepted counts through hf_round: invalid ones
+    leave the request untouched, raise EDEVICE, and the draft still reads the
+    (unchanged) state."""
+    import speculative_decoding_drafter_hf_gb300 as hf
+    cfg = CONFIGS["qwen3_4b_bf16"].replace(batch=3)
+    p = Pair(cfg)
+    lens = [700, 40, 1500]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    slot, feats = make_round_inputs(cfg, 0, p.B)
+    n = torch.tensor([0, cfg.block + 1, 3], dtype=torch.int32)
+    got, ref, _ = p.round(feats, n, slot)
+    assert maxnorm_err(got, ref) <= p.tol
+    p.check_context(what="zero / full counts")
+    slot, feats = make_round_inputs(cfg, 1, p.B)
+    bad = torch.tensor([2, -1, cfg.block + 2], dtype=torch.int32)
+    out = p.gpu.round(feats.cuda(), bad.cuda(), slot.cuda())
+    assert p.gpu.sync_status()[0] == hf.Status.EDEVICE
+    p.orc.commit(feats, np.array([2, 0, 0]))  # invalid counts: requests 1, 2 untouched
+    ref = p.orc.draft(slot)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert maxnorm_err(got, ref) <= p.tol
+    p.check_context(what="after invalid counts")
+    p.close()
+
+
+def test_round_api_in_cuda_graph():
+    """hf_round captured once and replayed per round (the benchmark's form)."""
+    cfg = CONFIGS["qwen3_4b_bf16"].replace(batch=2)
+    p = Pair(cfg)
+    lens = [900, 130]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    dt = p.gpu.torch_dtype
+    st_slot = torch.empty((2, cfg.block, cfg.d_model), dtype=dt, device="cuda")
+    st_feat = torch.empty((2, cfg.block + 1, cfg.d_model), dtype=dt, device="cuda")
+    st_cnt = torch.empty((2,), dtype=torch.int32, device="cuda")
+    out = torch.empty_like(st_slot)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+        p.gpu.round(st_feat, st_cnt, st_slot, out)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for r in range(4):
+        slot, feats = make_round_inputs(cfg, r, 2)
+        n = make_accepted(cfg, r, 2)
+        st_slot.copy_(slot)
+        st_feat.copy_(feats)
+        st_cnt.copy_(n.to(torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        p.orc.commit(feats, n.numpy())
+        ref = p.orc.draft(slot)
+        got = out.float().cpu().numpy().astype(np.float64)
+        assert maxnorm_err(got, ref) <= p.tol, f"round {r}"
+    p.check_context(what="graph rounds")
+    p.close()
