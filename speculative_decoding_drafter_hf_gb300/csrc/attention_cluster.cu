@@ -66,10 +66,10 @@ struct Args {
   int early;      // what is final at launch (the previous launch signalled its
                   // dependents after its own dependency wait) and may be read before
                   // this launch's wait: EARLY_RING (ring K/V), EARLY_STATE (positions,
-                  // states); the projections always need the wait
+                  // states), EARLY_PROJ (the slot projections)
 };
 
-constexpr int EARLY_RING = 1, EARLY_STATE = 2;
+constexpr int EARLY_RING = 1, EARLY_STATE = 2, EARLY_PROJ = 4;
 
 struct Layout {
   size_t bar, kt, vt, q, s, ml, total;
@@ -655,63 +655,75 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   // Ring tiles requested before the valid count is known (ring final, the
   // positions not yet): the CTA's first tiles inside the window; those past
   // the valid rows are drained at the end.
+  const bool proj_early = (a.early & EARLY_PROJ) != 0;
+  const bool blind = ring_early && !state_early;
+  const bool slots = rank == 0;
+  bool waited = false;
+  auto wait_once = [&]() {
+    if (!waited) pdl_wait();
+    waited = true;
+  };
+  const int c4n = dh / 4;
+  auto stage = [&]() {
+    // Q rows (pre-scaled) as bf16; rows R..QR-1 zero.
+    for (int i = tid; i < QR * c4n; i += nthr) {
+      const int r = i / c4n, c = (i % c4n) * 4;
+      uint2 w = make_uint2(0u, 0u);
+      if (r < R) {
+        const int g = r / S, sl = r % S;
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(
+            a.proj + (rowbase + sl) * d.Nd + (size_t)(kvh * G + g) * dh + c));
+        w = make_uint2(pack_bf16x2(x.x * a.qscale, x.y * a.qscale),
+                       pack_bf16x2(x.z * a.qscale, x.w * a.qscale));
+      }
+      *reinterpret_cast<uint2*>(qt + sw_chunk(QR, r, c >> 3) + (c & 7) * 2) = w;
+    }
+    // slot keys / values (rank 0) into rows KT..KT+15 of every tile buffer
+    // (the copies write rows 0..KT-1 only); rows past S zero (finite V for P.V)
+    if (slots)
+      for (int i = tid; i < TC_STAGES * 16 * c4n; i += nthr) {
+        const int stg = i / (16 * c4n), j = (i / c4n) % 16, c = (i % c4n) * 4;
+        uint2 kw = make_uint2(0u, 0u), vw = make_uint2(0u, 0u);
+        if (j < S) {
+          const float* row = a.proj + (rowbase + j) * d.Nd;
+          const float4 kx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
+          const float4 vx =
+              __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
+          kw = make_uint2(pack_bf16x2(kx.x, kx.y), pack_bf16x2(kx.z, kx.w));
+          vw = make_uint2(pack_bf16x2(vx.x, vx.y), pack_bf16x2(vx.z, vx.w));
+        }
+        uint8_t* kd = kv + (size_t)stg * 2 * L.stage;
+        const uint32_t off = sw_chunk(KTS, KT + j, c >> 3) + (c & 7) * 2;
+        *reinterpret_cast<uint2*>(kd + off) = kw;
+        *reinterpret_cast<uint2*>(kd + L.stage + off) = vw;
+      }
+  };
   int nissue = 0;
-  if (ring_early && !state_early) {
+  if (blind) {
     nissue = min(TC_STAGES, min(a.ntile, (d.W + KT - 1) / KT - t0));
     if (tid == 0) {
       init_bars();
       for (int i = 0; i < nissue; ++i) issue(i);
     }
-    pdl_wait();
-  } else if (!state_early) {
-    pdl_wait();
   }
+  if (proj_early) stage();
+  if (!state_early) wait_once();
   const long long p = __ldcg(&a.pos[b]);
   const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);  // valid ring rows 0..nv-1
   const int nwt = max(0, min(a.ntile, (nv + KT - 1) / KT - t0));  // ring tiles of this CTA
-  const bool slots = rank == 0;
   const int nsteps = max(nwt, slots ? 1 : 0);
-  if (!(ring_early && !state_early)) {
+  if (!blind) {
+    if (!ring_early) wait_once();
     nissue = min(TC_STAGES, nwt);
     if (tid == 0) {
       init_bars();
       for (int i = 0; i < nissue; ++i) issue(i);
     }
-    if (state_early) pdl_wait();  // the projections below come from the previous launch
   }
-  // Q rows (pre-scaled) as bf16; rows R..QR-1 zero.
-  const int c4n = dh / 4;
-  for (int i = tid; i < QR * c4n; i += nthr) {
-    const int r = i / c4n, c = (i % c4n) * 4;
-    uint2 w = make_uint2(0u, 0u);
-    if (r < R) {
-      const int g = r / S, sl = r % S;
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(
-          a.proj + (rowbase + sl) * d.Nd + (size_t)(kvh * G + g) * dh + c));
-      w = make_uint2(pack_bf16x2(x.x * a.qscale, x.y * a.qscale),
-                     pack_bf16x2(x.z * a.qscale, x.w * a.qscale));
-    }
-    *reinterpret_cast<uint2*>(qt + sw_chunk(QR, r, c >> 3) + (c & 7) * 2) = w;
+  if (!proj_early) {
+    wait_once();  // the projections come from the previous launch
+    stage();
   }
-  // slot keys / values (rank 0) into rows KT..KT+15 of every tile buffer
-  // (the copies write rows 0..KT-1 only); rows past S zero (finite V for P.V)
-  if (slots)
-    for (int i = tid; i < TC_STAGES * 16 * c4n; i += nthr) {
-      const int stg = i / (16 * c4n), j = (i / c4n) % 16, c = (i % c4n) * 4;
-      uint2 kw = make_uint2(0u, 0u), vw = make_uint2(0u, 0u);
-      if (j < S) {
-        const float* row = a.proj + (rowbase + j) * d.Nd;
-        const float4 kx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
-        const float4 vx =
-            __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
-        kw = make_uint2(pack_bf16x2(kx.x, kx.y), pack_bf16x2(kx.z, kx.w));
-        vw = make_uint2(pack_bf16x2(vx.x, vx.y), pack_bf16x2(vx.z, vx.w));
-      }
-      uint8_t* kd = kv + (size_t)stg * 2 * L.stage;
-      const uint32_t off = sw_chunk(KTS, KT + j, c >> 3) + (c & 7) * 2;
-      *reinterpret_cast<uint2*>(kd + off) = kw;
-      *reinterpret_cast<uint2*>(kd + L.stage + off) = vw;
-    }
   __syncthreads();  // barriers initialised, Q and slot rows written
 
   // this warp's role
@@ -727,6 +739,8 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   const uint32_t qb = smem_u32(qt);
   const int qrow = wmt * 16 + (lane & 15);
 
+  // One online-softmax update over the 16 keys at tile rows kr..kr+15 of
+  // the K/V buffers kb/vb; key row j is valid when j < nvr or KT <= j < KT + nsk.
   // One online-softmax update over the 16 keys at tile rows kr..kr+15 of
   // the K/V buffers kb/vb; key row j is valid when j < nvr or KT <= j < KT + nsk.
   auto update = [&](uint32_t kb, uint32_t vb, int kr, int nvr, int nsk) {
@@ -832,10 +846,10 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
         __syncthreads();
       }
       done = i + 1;
-      if (active)
-        for (int q = 0; q < W.kw; q += 16)
-          if (wkg * W.kw + q < nvr) update(smem_u32(kt), smem_u32(vt), wkg * W.kw + q, nvr, 0);
     }
+    if (active && ring)
+      for (int q = 0; q < W.kw; q += 16)
+        if (wkg * W.kw + q < nvr) update(smem_u32(kt), smem_u32(vt), wkg * W.kw + q, nvr, 0);
     // the slot keys (rows KT..KT+15) go to the last key group
     if (with_slots && active && wkg == W.kg - 1)
       update(smem_u32(kt), smem_u32(vt), KT, 0, S);

@@ -370,16 +370,19 @@ cudaError_t launch_gemm_fma(int dtype, const void* X, int ldx, const void* Wt, i
 // late_trigger: the CTAs signal programmatic completion only after their own
 // dependency wait, so that the next launch may read, before its own wait,
 // anything that the launches before this one wrote.
+// a_group_mtiles: a_tiles holds consecutive groups of that many m-tiles,
+// each tiled on its own by tile_weights (one matrix per layer, stacked);
+// 0: one matrix.
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb,
                            int N, int K, int swap, int splits, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches, const void* a_tiles = nullptr,
-                           int late_trigger = 0);
+                           int late_trigger = 0, int a_group_mtiles = 0);
 // Two swapped products with the same K in one launch (both A operands
 // pre-tiled): D0 = A0 B0^T with epilogue epi0, D1 = A1 B1^T with epi1.
-cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, const void* B0, long long ldb0,
-                                   int N0, const Epi& epi0, const void* a_tiles1, int M1,
-                                   const void* B1, long long ldb1, int N1, const Epi& epi1, int K,
-                                   int splits, int32_t* err, cudaStream_t st, int* launches,
+cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, int gm0, const void* B0,
+                                   long long ldb0, int N0, const Epi& epi0, const void* a_tiles1,
+                                   int M1, const void* B1, long long ldb1, int N1, const Epi& epi1,
+                                   int K, int splits, int32_t* err, cudaStream_t st, int* launches,
                                    int late_trigger = 0);
 void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst);
 
@@ -411,7 +414,8 @@ cudaError_t configure_attn_cluster(const Dims& d);
 // Bmax*Hkv*W, box attn_tile_rows(d) rows); other handles pass NULL maps.
 // early: what the previous launch (which signalled its dependents after its
 // own wait) leaves final at launch, read before this launch's wait:
-// bit 0 the ring K/V, bit 1 the positions and states.
+// bit 0 the ring K/V, bit 1 the positions and states, bit 2 the slot
+// projections (memory-read CTAs use bit 1 for state and C alike).
 // with_mem = 0: attention only (the memory read was done elsewhere).
 size_t attn_cluster_smem(const Dims& d, int esize);
 int attn_tile_rows(const Dims& d);

@@ -70,6 +70,9 @@ struct TcArgs {
   int mt0;
   int M1, N1;
   const uint8_t* a_tiles1;
+  // Tiled A stored as consecutive groups of this many m-tiles (one matrix
+  // tiled per layer, stacked), each group [k_block][m_tile]; per product.
+  int a_gm0, a_gm1;
 };
 
 // Epilogue cache (shared memory after the barriers): per output row of the
@@ -115,6 +118,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const int m_tile = second ? (int)blockIdx.y - a.mt0 : (int)blockIdx.y;
   const int M = second ? a.M1 : a.M, N = second ? a.N1 : a.N;
   const uint8_t* a_tiles = second ? a.a_tiles1 : a.a_tiles;
+  const int a_gm = second ? a.a_gm1 : a.a_gm0;  // m-tiles per stored group
+  const size_t a_tile_idx0 = ((size_t)(m_tile / a_gm) * a.kblocks) * a_gm + m_tile % a_gm;
   const CUtensorMap* tb = second ? &tb1 : &tb0;
   const Epi& epi = second ? epi1 : epi0;
   if (n_tile * BN >= N) return;  // the other product has more n-tiles (whole cluster)
@@ -152,7 +157,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     auto load_a = [&](int st, int i) {
       if (a_tiles)
         bulk_g2s(sA + st * A_BYTES,
-                 a_tiles + ((size_t)m_tile * a.kblocks + (kb0 + i)) * (size_t)A_BYTES, A_BYTES,
+                 a_tiles + (a_tile_idx0 + (size_t)(kb0 + i) * a_gm) * (size_t)A_BYTES, A_BYTES,
                  &full[st]);
       else
         tma_load_2d(sA + st * A_BYTES, &ta, &full[st], (kb0 + i) * 64, m_tile * 128);
@@ -529,7 +534,7 @@ int tc_pick_splits(int M, int N, int K) {
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb, int N,
                            int K, int swap, int splits, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches, const void* a_tiles,
-                           int late_trigger) {
+                           int late_trigger, int a_group_mtiles) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   int bn = 16;
   while (bn < N && bn < 256) bn *= 2;
@@ -547,6 +552,7 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   a.a_tiles = static_cast<const uint8_t*>(a_tiles);
   a.late_trigger = late_trigger;
   a.mt0 = m_tiles;
+  a.a_gm0 = a.a_gm1 = a_group_mtiles > 0 ? a_group_mtiles : m_tiles;
   CUtensorMap ma, mb;
   cudaError_t e = make_map(&mb, B, N, K, ldb, bn);
   if (e != cudaSuccess) return e;
@@ -560,10 +566,10 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   return launch_bn(bn, ma, mb, mb, a, epi, epi, grid, st);
 }
 
-cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, const void* B0, long long ldb0,
-                                   int N0, const Epi& epi0, const void* a_tiles1, int M1,
-                                   const void* B1, long long ldb1, int N1, const Epi& epi1, int K,
-                                   int splits, int32_t* err, cudaStream_t st, int* launches,
+cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, int gm0, const void* B0,
+                                   long long ldb0, int N0, const Epi& epi0, const void* a_tiles1,
+                                   int M1, const void* B1, long long ldb1, int N1, const Epi& epi1,
+                                   int K, int splits, int32_t* err, cudaStream_t st, int* launches,
                                    int late_trigger) {
   if (M0 <= 0 || N0 <= 0 || M1 <= 0 || N1 <= 0 || !a_tiles0 || !a_tiles1)
     return cudaErrorInvalidValue;
@@ -587,6 +593,8 @@ cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, const void* B0,
   a.M1 = M1;
   a.N1 = N1;
   a.a_tiles1 = static_cast<const uint8_t*>(a_tiles1);
+  a.a_gm0 = gm0 > 0 ? gm0 : mt0;
+  a.a_gm1 = mt1;
   CUtensorMap mb0, mb1;
   cudaError_t e = make_map(&mb0, B0, N0, K, ldb0, bn);
   if (e == cudaSuccess) e = make_map(&mb1, B1, N1, K, ldb1, bn);
@@ -600,13 +608,14 @@ cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, const void* B0,
 // Re-lay a row-major bf16 matrix [M][K] (host) as 128 x 64 tiles in the
 // shared-memory image the kernel's tensor-core descriptors expect (rows of
 // 128 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7)), ordered
-// [m_tile][k_block]; rows past M and columns past K are zero. Each CTA then
-// streams a contiguous run of its m-tile's k-blocks.
+// [k_block][m_tile]; rows past M and columns past K are zero. CTAs walk their
+// k-blocks in step, so at any moment the CTAs of a launch read one
+// contiguous run of tiles (one k-block of every m-tile).
 void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst) {
   const long long mt = (M + 127) / 128, kb = (K + 63) / 64;
   for (long long t = 0; t < mt; ++t)
     for (long long b = 0; b < kb; ++b) {
-      uint16_t* tile = dst + (t * kb + b) * 128 * 64;
+      uint16_t* tile = dst + (b * mt + t) * 128 * 64;
       for (int r = 0; r < 128; ++r)
         for (int c = 0; c < 64; ++c) {
           const long long gr = t * 128 + r, gc = b * 64 + c;

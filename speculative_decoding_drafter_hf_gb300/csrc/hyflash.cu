@@ -280,7 +280,7 @@ int pick_splits(const hf_handle* h, long long R, long long C, long long K, int t
 // as the 128-row operand (they stream once) and the activation rows as N.
 cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, int ldw, int R,
                         int C, int K, const Epi& epi, cudaStream_t st, int* count,
-                        const void* tiles = nullptr, int late_trigger = 0) {
+                        const void* tiles = nullptr, int late_trigger = 0, int tile_group = 0) {
   if (R <= 0 || C <= 0) return cudaSuccess;
   if (h->cfg.dtype == HF_F32) {
     int splits = pick_splits(h, R, C, K, 64, 64);
@@ -289,15 +289,16 @@ cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, in
   }
   const int splits = hf::tc_pick_splits(C, R, K);
   return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->err, epi, st, count, tiles,
-                            late_trigger);
+                            late_trigger, tile_group);
 }
 
 hf_status gemm(hf_handle* h, int fam, const void* X, int ldx, const void* Wt, int ldw, int R,
                int C, int K, const Epi& epi, cudaStream_t st, const void* tiles = nullptr,
-               int late_trigger = 0) {
+               int late_trigger = 0, int tile_group = 0) {
   if (R <= 0 || C <= 0) return HF_OK;
   Scope sc(h, fam, st);
-  cudaError_t e = gemm_launch(h, X, ldx, Wt, ldw, R, C, K, epi, st, &sc.count, tiles, late_trigger);
+  cudaError_t e =
+      gemm_launch(h, X, ldx, Wt, ldw, R, C, K, epi, st, &sc.count, tiles, late_trigger, tile_group);
   if (e != cudaSuccess) return cuda_fail(h, e, "gemm launch");
   return HF_OK;
 }
@@ -535,7 +536,9 @@ hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w)
 
 namespace {
 
-constexpr int kEarlyRing = 1, kEarlyAll = 3;  // attention launch: what it may read before waiting
+// Attention launch: what it may read before its dependency wait (ring K/V,
+// positions and states, slot projections).
+constexpr int kEarlyRing = 1, kEarlyState = 2, kEarlyProj = 4;
 // hf_round folds the first layer's memory read into the state update once a
 // layer's states are at least this large (below, the read runs beside the
 // attention, off the round's critical path).
@@ -651,7 +654,8 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
     const void* X = l == 0 ? slot_emb : h->xbuf[(l - 1) % 2];
     void* Y = l == d.L - 1 ? out : h->xbuf[l % 2];
     if ((s = draft_proj(h, l, X, batch, tc, st)) != HF_OK) return s;
-    if ((s = draft_rest(h, l, X, Y, batch, tc ? kEarlyAll : 0, 1, st)) != HF_OK) return s;
+    if ((s = draft_rest(h, l, X, Y, batch, tc ? kEarlyRing | kEarlyState : 0, 1, st)) != HF_OK)
+      return s;
   }
   return HF_OK;
 }
@@ -668,8 +672,10 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, 
   const Epi ep = commit_epi(h, n_accepted);
   const int rows = batch * (d.S + 1);
   const int late = h->cfg.dtype == HF_BF16 ? 1 : 0;  // the tensor-core GEMM can signal late
+  // the tiled commit weights are one matrix per layer, stacked
   s = gemm(h, HF_K_COMMIT_PROJ, feats, d.D, h->w_commit, d.D, rows,
-           d.L * (h->wt_commit ? h->nc_pad : d.Nc), d.D, ep, st, h->wt_commit, late);
+           d.L * (h->wt_commit ? h->nc_pad : d.Nc), d.D, ep, st, h->wt_commit, late,
+           h->nc_pad / 128);
   if (s != HF_OK) return s;
   return commit_state(h, n_accepted, batch, nullptr, late, 0, st);
 }
@@ -700,9 +706,9 @@ hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
     const int splits =
         hf::tc_pick_splits((M0 + 127) / 128 * 128 + d.Nd, std::max(N0, N1), d.D);
     Scope sc(h, HF_K_ROUND_PROJ, st);
-    cudaError_t e = hf::launch_gemm_tc_grouped(h->wt_commit, M0, feats, d.D, N0, ec, h->wt_draft,
-                                               d.Nd, slot_emb, d.D, N1, e1, d.D, splits, h->err,
-                                               st, &sc.count, /*late_trigger=*/1);
+    cudaError_t e = hf::launch_gemm_tc_grouped(h->wt_commit, M0, h->nc_pad / 128, feats, d.D, N0,
+                                               ec, h->wt_draft, d.Nd, slot_emb, d.D, N1, e1, d.D,
+                                               splits, h->err, st, &sc.count, /*late_trigger=*/1);
     if (e != cudaSuccess) return cuda_fail(h, e, "grouped projection launch");
   }
   // 2. state update; at large batch also the layer-0 memory read of the new
@@ -720,8 +726,10 @@ hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
     void* Y = l == d.L - 1 ? out : h->xbuf[l % 2];
     if (l > 0 && (s = draft_proj(h, l, X, batch, 1, st)) != HF_OK) return s;
     const int with_mem = l > 0 || !fuse_mem;
-    if ((s = draft_rest(h, l, X, Y, batch, l > 0 ? kEarlyAll : kEarlyRing, with_mem, st)) != HF_OK)
-      return s;
+    // layer 0 follows the state update, which signals late: the ring and the
+    // slot projections (grouped launch) are final, the positions are not
+    const int early = l > 0 ? kEarlyRing | kEarlyState : kEarlyRing | kEarlyProj;
+    if ((s = draft_rest(h, l, X, Y, batch, early, with_mem, st)) != HF_OK) return s;
   }
   return HF_OK;
 }
