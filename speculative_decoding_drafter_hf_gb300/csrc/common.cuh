@@ -386,6 +386,20 @@ cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, int gm0, const 
                                    int late_trigger = 0);
 void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst);
 
+// Stream-K variant for the skinny swapped products (gemm_streamk.cu): one or
+// two products with pre-tiled A (a_tiles1 = NULL: one), at most 32 activation
+// rows each, the (m-tile, k-block) units split evenly over min(num_sms,
+// units) CTAs; split tiles are summed through ws (floats) with one ticket
+// per tile (tickets zero between launches, restored by every launch).
+cudaError_t configure_gemm_sk();
+// Workspace floats a launch of these shapes needs (tiles, slots per tile out).
+size_t gemm_sk_workspace(int M0, int M1, int K, int num_sms, int* tiles, int* nslot);
+cudaError_t launch_gemm_sk(const void* a_tiles0, int M0, int gm0, const void* B0, long long ldb0,
+                           int N0, const Epi& epi0, const void* a_tiles1, int M1, const void* B1,
+                           long long ldb1, int N1, const Epi& epi1, int K, int num_sms, float* ws,
+                           size_t ws_floats, int* tickets, int n_tickets, int32_t* err,
+                           int late_trigger, cudaStream_t st, int* launches);
+
 // Persistent warp-specialised bf16 GEMM for large token-major products
 // (gemm_persistent.cu): output row m of A's rows, column n of B's rows;
 // epilogue through epi_chunk16. One CTA per SM (num_sms).

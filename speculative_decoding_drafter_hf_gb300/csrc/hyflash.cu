@@ -61,8 +61,10 @@ struct hf_handle {
   float* part = nullptr;
   size_t part_elems = 0;
   std::vector<CUtensorMap> ring_maps;  // per layer: K, V tile maps (tensor-core attention)
-  int* counters = nullptr;     // split-K tickets of the tensor-core GEMM
+  int* counters = nullptr;     // tile tickets of the stream-K GEMM (zero between launches)
   int n_counters = 0;
+  float* skws = nullptr;       // stream-K partial tiles
+  size_t skws_floats = 0;
   int num_sms = 152;
 
   // prefill segment scratch (Tseg = pf_tokens tokens, transposed layouts)
@@ -287,6 +289,12 @@ cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, in
     return hf::launch_gemm_fma(h->cfg.dtype, X, ldx, Wt, ldw, R, C, K, splits, h->part, epi, st,
                                count);
   }
+  // skinny and more weight tiles than SMs: stream-K (no partial last wave);
+  // otherwise one CTA or split-K cluster per tile (measured faster there)
+  if (tiles && R <= 32 && (C + 127) / 128 > h->num_sms)
+    return hf::launch_gemm_sk(tiles, C, tile_group, X, ldx, R, epi, nullptr, 0, nullptr, 0, 0, epi,
+                              K, h->num_sms, h->skws, h->skws_floats, h->counters, h->n_counters,
+                              h->err, late_trigger, st, count);
   const int splits = hf::tc_pick_splits(C, R, K);
   return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->err, epi, st, count, tiles,
                             late_trigger, tile_group);
@@ -420,6 +428,17 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) == cudaSuccess && sms > 0)
       h->num_sms = sms;
   }
+  if (h->cfg.dtype == HF_BF16) {
+    // stream-K workspace for the largest skinny product: slot projections,
+    // output projections, commit projections (alone or grouped with the
+    // first slot projection)
+    int tiles = 0, nslot = 0;
+    size_t need = hf::gemm_sk_workspace(d.Nd, 0, d.D, h->num_sms, &tiles, &nslot);
+    need = std::max(need, hf::gemm_sk_workspace(d.D, 0, d.Nz, h->num_sms, &tiles, &nslot));
+    need = std::max(need, hf::gemm_sk_workspace(d.L * h->nc_pad, d.Nd, d.D, h->num_sms, &tiles, &nslot));
+    h->skws_floats = need;
+    A((void**)&h->skws, need * 4);
+  }
   A((void**)&h->pf_dtw, (size_t)d.Hm * h->pf_tokens * 4);
   A((void**)&h->pf_decay, (size_t)d.Hm * 4);
   A(&h->pf_xsT, (size_t)d.dinner * h->pf_tokens * es);
@@ -450,6 +469,7 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     e = hf::configure_attn_cluster(h->d);
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc();
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc_persistent(h->num_sms);
+    if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_gemm_sk();
     if (e == cudaSuccess) e = hf::configure_commit_state(h->d);
     if (e != cudaSuccess) s = cuda_fail(h, e, "kernel set-up");
   }
@@ -706,9 +726,15 @@ hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
     const int splits =
         hf::tc_pick_splits((M0 + 127) / 128 * 128 + d.Nd, std::max(N0, N1), d.D);
     Scope sc(h, HF_K_ROUND_PROJ, st);
-    cudaError_t e = hf::launch_gemm_tc_grouped(h->wt_commit, M0, h->nc_pad / 128, feats, d.D, N0,
-                                               ec, h->wt_draft, d.Nd, slot_emb, d.D, N1, e1, d.D,
-                                               splits, h->err, st, &sc.count, /*late_trigger=*/1);
+    const bool sk = std::max(N0, N1) <= 32 && (M0 + 127) / 128 + (d.Nd + 127) / 128 > h->num_sms;
+    cudaError_t e =
+        sk  ? hf::launch_gemm_sk(h->wt_commit, M0, h->nc_pad / 128, feats, d.D, N0, ec, h->wt_draft,
+                                 d.Nd, slot_emb, d.D, N1, e1, d.D, h->num_sms, h->skws,
+                                 h->skws_floats, h->counters, h->n_counters, h->err,
+                                 /*late_trigger=*/1, st, &sc.count)
+            : hf::launch_gemm_tc_grouped(h->wt_commit, M0, h->nc_pad / 128, feats, d.D, N0, ec,
+                                         h->wt_draft, d.Nd, slot_emb, d.D, N1, e1, d.D, splits,
+                                         h->err, st, &sc.count, /*late_trigger=*/1);
     if (e != cudaSuccess) return cuda_fail(h, e, "grouped projection launch");
   }
   // 2. state update; at large batch also the layer-0 memory read of the new
@@ -854,7 +880,11 @@ hf_status hf_sync(hf_handle* h, void* stream) {
     HF_CUDA(h, cudaMemset(h->err, 0, 4));
     std::string m;
     if (word & hf::ERR_BAD_ACCEPTED) m += "accepted count outside 0..block+1 (request left unchanged); ";
-    if (word & hf::ERR_TIMEOUT) m += "a bounded device wait gave up; ";
+    if (word & hf::ERR_TIMEOUT) {
+      m += "a bounded device wait gave up; ";
+      // a launch that gave up may have left stream-K tickets raised
+      HF_CUDA(h, cudaMemset(h->counters, 0, (size_t)h->n_counters * 4));
+    }
     return fail(h, (word & hf::ERR_TIMEOUT) ? HF_ETIMEOUT : HF_EDEVICE, m);
   }
   return HF_OK;

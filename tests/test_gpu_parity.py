@@ -371,3 +371,23 @@ def test_round_api_in_cuda_graph():
         assert maxnorm_err(got, ref) <= p.tol, f"round {r}"
     p.check_context(what="graph rounds")
     p.close()
+
+
+@pytest.mark.parametrize("name,batch,api", [
+    ("serving_qwen3_4b_b64", 4, "separate"),  # commit projection alone, 32 rows, 174 tiles
+    ("serving_qwen3_4b_b64", 2, "round"),     # grouped with the slot projection, 16 rows
+    ("phi4_bf16", 1, "round"),                # Phi-4 widths: 164 tiles
+])
+def test_stream_k_products(name, batch, api):
+    """Skinny products with more weight tiles than SMs run stream-K (equal
+    shares of (tile, k-block) units per SM, split tiles summed in k order)."""
+    cfg = CONFIGS[name].replace(batch=batch, prefix=700, prefix_lo=300, prefix_hi=900) \
+        if name.startswith("serving") else CONFIGS[name].replace(batch=batch, prefix=700)
+    p = Pair(cfg)
+    lens = make_prefix_lens(cfg)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    if api == "round":
+        run_round_api(p, 2, check_every=1)
+    else:
+        run_rounds(p, 2, check_every=1)
+    p.close()
