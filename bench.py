@@ -140,6 +140,35 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
     return {"families": fam, "step_bytes": step, "step_flops": flops}
 
 
+def kernel_sources_digest() -> str:
+    """sha256 over the CUDA sources (names and bytes, sorted by name)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_drafter_hf_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, family: str):
+    """DRAM bytes per launch of a kernel family from the committed ncu
+    captures (profiles/traffic.json), or None when none was taken for this
+    workload or the kernels changed since."""
+    import json as _json
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            t = _json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_sources_sha256") != kernel_sources_digest():
+        return None
+    return t.get("per_launch_bytes", {}).get(workload, {}).get(family)
+
+
 def prefill_flops(cfg, total_tokens: int, ring_rows: int) -> float:
     D, din, N, Hm, P = cfg.d_model, cfg.d_inner, cfg.d_state, cfg.ssm_heads, cfg.ssm_headdim
     kvd = cfg.n_kv_heads * cfg.head_dim
@@ -592,7 +621,8 @@ def run_hyflash(args, cfg):
     per_launch = step_bytes_top / launches_top
     achieved = per_launch / (avg_ms / 1e3) / 1e9 if avg_ms > 0 else 0.0
     roofline = {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": hbm_peak,
-                "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                "unit": "GB/s", "frac": achieved / hbm_peak,
+                "traffic": measured_traffic(cfg.name, top) if fused else None,
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": per_launch, "avg_launch_ms": avg_ms}
 

@@ -81,3 +81,16 @@ def test_clock_summary_parses_samples(tmp_path):
     s = c.summary()
     assert s["sm_mhz"] == pytest.approx(1985.0) and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_traffic_only_for_unchanged_kernels(tmp_path, monkeypatch):
+    import json
+    (tmp_path / "profiles").mkdir()
+    real = bench.kernel_sources_digest()
+    for digest, want in ((real, 123), ("0" * 64, None)):
+        (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+            {"kernel_sources_sha256": digest, "per_launch_bytes": {"w": {"round_proj": 123}}}))
+        monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+        monkeypatch.setattr(bench, "kernel_sources_digest", lambda: real)
+        assert bench.measured_traffic("w", "round_proj") == want
+        assert bench.measured_traffic("w", "out_proj") is None
