@@ -908,10 +908,11 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     }
   }
   __syncthreads();
-  // merge the key groups per row: M = max m_k, L = sum w_k l_k, O = sum w_k O_k
+  // merge the key groups per row: M = max m_k, L = sum w_k l_k, O = sum w_k O_k.
+  // Thread tid owns 4 columns (c) of rows r0, r0 + rstep, ...
   __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
-  for (int e = tid; e < R * c4n; e += nthr) {
-    const int r = e / c4n, c = (e % c4n) * 4;
+  const int c = (tid % c4n) * 4, rstep = nthr / c4n;
+  for (int r = tid / c4n; r < R; r += rstep) {
     float M = -INFINITY;
     for (int k = 0; k < W.kg; ++k) M = fmaxf(M, mlk[((size_t)k * QR + r) * 2]);
     float Ls = 0.f;
@@ -942,11 +943,12 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   }
   if (nsplit == 1) return;
   cluster_sync_all();
-  // rank `rank` combines rows rank, rank + nsplit, ... over all ranks
-  const int my_rows = (R - rank + nsplit - 1) / nsplit;
-  for (int e = tid; e < my_rows * c4n; e += nthr) {
-    const int r = rank + (e / c4n) * nsplit, c = (e % c4n) * 4, g = r / S, sl = r % S;
+  // rank `rank` combines rows rank, rank + nsplit, ... over all ranks; every
+  // partner's (m, l, O) is requested at once (one round trip)
+  for (int r = rank + (tid / c4n) * nsplit; r < R; r += rstep * nsplit) {
+    const int g = r / S, sl = r % S;
     float mp[MAX_SPLIT], lp[MAX_SPLIT];
+    float4 op[MAX_SPLIT];
     float M = -INFINITY;
 #pragma unroll
     for (int sp = 0; sp < MAX_SPLIT; ++sp) {
@@ -954,16 +956,19 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
         const uint32_t ad = peer_addr(&ml[r * 2], (uint32_t)sp);
         mp[sp] = ld_peer_f(ad);
         lp[sp] = ld_peer_f(ad + 4);
-        M = fmaxf(M, mp[sp]);
+        op[sp] = ld_peer_f4(peer_addr(octa + (size_t)r * OLD + c, (uint32_t)sp));
       }
     }
+#pragma unroll
+    for (int sp = 0; sp < MAX_SPLIT; ++sp)
+      if (sp < nsplit) M = fmaxf(M, mp[sp]);
     float Lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int sp = 0; sp < MAX_SPLIT; ++sp) {
       if (sp < nsplit) {
         const float wt = lp[sp] > 0.f ? exp2f(mp[sp] - M) : 0.f;
-        const float4 ov = ld_peer_f4(peer_addr(octa + (size_t)r * OLD + c, (uint32_t)sp));
+        const float4 ov = op[sp];
         Lsum = fmaf(lp[sp], wt, Lsum);
         acc.x = fmaf(wt, ov.x, acc.x);
         acc.y = fmaf(wt, ov.y, acc.y);
