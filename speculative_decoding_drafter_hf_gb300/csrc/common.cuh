@@ -394,6 +394,17 @@ void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst);
 cudaError_t configure_gemm_sk();
 // Workspace floats a launch of these shapes needs (tiles, slots per tile out).
 size_t gemm_sk_workspace(int M0, int M1, int K, int num_sms, int* tiles, int* nslot);
+// Token-major stream-K variant (gemm_streamk_tm.cu) for products with more
+// than 32 activation rows: X [M, K] activation rows and W [N, K] plain
+// weights through TMA, output row m (token), column n (feature); one or two
+// products (X1 = NULL: one); ws: gemm_tm_workspace(num_sms) floats.
+cudaError_t configure_gemm_tm();
+size_t gemm_tm_workspace(int num_sms);
+cudaError_t launch_gemm_tm(const void* X0, long long ldx0, int M0, const void* W0, long long ldw0,
+                           int N0, const Epi& epi0, const void* X1, long long ldx1, int M1,
+                           const void* W1, long long ldw1, int N1, const Epi& epi1, int K,
+                           int num_sms, float* ws, size_t ws_floats, int* tickets, int n_tickets,
+                           int32_t* err, int late_trigger, cudaStream_t st, int* launches);
 cudaError_t launch_gemm_sk(const void* a_tiles0, int M0, int gm0, const void* B0, long long ldb0,
                            int N0, const Epi& epi0, const void* a_tiles1, int M1, const void* B1,
                            long long ldb1, int N1, const Epi& epi1, int K, int num_sms, float* ws,

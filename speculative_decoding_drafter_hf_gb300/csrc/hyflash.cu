@@ -289,6 +289,11 @@ cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, in
     return hf::launch_gemm_fma(h->cfg.dtype, X, ldx, Wt, ldw, R, C, K, splits, h->part, epi, st,
                                count);
   }
+  // more than 32 rows: token-major (contiguous epilogue runs), split-K
+  // partners in a cluster summing through distributed shared memory
+  if (R > 32)
+    return hf::launch_gemm_tc(X, ldx, R, Wt, ldw, C, K, 0, hf::tc_pick_splits(R, C, K), h->err,
+                              epi, st, count, nullptr, late_trigger);
   // skinny and more weight tiles than SMs: stream-K (no partial last wave);
   // otherwise one CTA or split-K cluster per tile (measured faster there)
   if (tiles && R <= 32 && (C + 127) / 128 > h->num_sms)
@@ -436,6 +441,7 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     size_t need = hf::gemm_sk_workspace(d.Nd, 0, d.D, h->num_sms, &tiles, &nslot);
     need = std::max(need, hf::gemm_sk_workspace(d.D, 0, d.Nz, h->num_sms, &tiles, &nslot));
     need = std::max(need, hf::gemm_sk_workspace(d.L * h->nc_pad, d.Nd, d.D, h->num_sms, &tiles, &nslot));
+    need = std::max(need, hf::gemm_tm_workspace(h->num_sms));
     h->skws_floats = need;
     A((void**)&h->skws, need * 4);
   }
@@ -470,6 +476,7 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc();
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_tc_persistent(h->num_sms);
     if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_gemm_sk();
+    if (e == cudaSuccess && h->cfg.dtype == HF_BF16) e = hf::configure_gemm_tm();
     if (e == cudaSuccess) e = hf::configure_commit_state(h->d);
     if (e != cudaSuccess) s = cuda_fail(h, e, "kernel set-up");
   }
@@ -631,6 +638,14 @@ Epi commit_epi(const hf_handle* h, const int32_t* n_accepted) {
 
 // early: the commit projection signalled its dependents after its wait;
 // late: the next launch reads the ring before its own wait.
+// The commit epilogue over the plain (unpadded) commit weights.
+Epi plain_commit_epi(const hf_handle* h, const int32_t* n_accepted) {
+  Epi ep = commit_epi(h, n_accepted);
+  ep.cols_per_layer = h->d.Nc;
+  ep.cols_valid = 0;
+  return ep;
+}
+
 hf_status commit_state(hf_handle* h, const int32_t* n_accepted, int batch, const float* memC,
                        int early, int late, cudaStream_t st) {
   const Dims& d = h->d;
@@ -692,10 +707,12 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, 
   const Epi ep = commit_epi(h, n_accepted);
   const int rows = batch * (d.S + 1);
   const int late = h->cfg.dtype == HF_BF16 ? 1 : 0;  // the tensor-core GEMM can signal late
-  // the tiled commit weights are one matrix per layer, stacked
+  // the tiled commit weights are one matrix per layer, stacked; wide batches
+  // run token-major over the plain weights
+  const bool tiled = h->wt_commit && rows <= 32;
   s = gemm(h, HF_K_COMMIT_PROJ, feats, d.D, h->w_commit, d.D, rows,
-           d.L * (h->wt_commit ? h->nc_pad : d.Nc), d.D, ep, st, h->wt_commit, late,
-           h->nc_pad / 128);
+           d.L * (tiled ? h->nc_pad : d.Nc), d.D, tiled ? ep : plain_commit_epi(h, n_accepted), st,
+           tiled ? h->wt_commit : nullptr, late, h->nc_pad / 128);
   if (s != HF_OK) return s;
   return commit_state(h, n_accepted, batch, nullptr, late, 0, st);
 }
@@ -726,9 +743,14 @@ hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
     const int splits =
         hf::tc_pick_splits((M0 + 127) / 128 * 128 + d.Nd, std::max(N0, N1), d.D);
     Scope sc(h, HF_K_ROUND_PROJ, st);
-    const bool sk = std::max(N0, N1) <= 32 && (M0 + 127) / 128 + (d.Nd + 127) / 128 > h->num_sms;
+    const bool tm = std::max(N0, N1) > 32;  // wide batch: token-major over the plain weights
+    const bool sk = !tm && (M0 + 127) / 128 + (d.Nd + 127) / 128 > h->num_sms;
     cudaError_t e =
-        sk  ? hf::launch_gemm_sk(h->wt_commit, M0, h->nc_pad / 128, feats, d.D, N0, ec, h->wt_draft,
+        tm  ? hf::launch_gemm_tm(feats, d.D, N0, h->w_commit, d.D, d.L * d.Nc,
+                                 plain_commit_epi(h, n_accepted), slot_emb, d.D, N1, h->w_draft, d.D,
+                                 d.Nd, e1, d.D, h->num_sms, h->skws, h->skws_floats, h->counters,
+                                 h->n_counters, h->err, /*late_trigger=*/1, st, &sc.count)
+        : sk  ? hf::launch_gemm_sk(h->wt_commit, M0, h->nc_pad / 128, feats, d.D, N0, ec, h->wt_draft,
                                  d.Nd, slot_emb, d.D, N1, e1, d.D, h->num_sms, h->skws,
                                  h->skws_floats, h->counters, h->n_counters, h->err,
                                  /*late_trigger=*/1, st, &sc.count)

@@ -377,6 +377,9 @@ def test_round_api_in_cuda_graph():
     ("serving_qwen3_4b_b64", 4, "separate"),  # commit projection alone, 32 rows, 174 tiles
     ("serving_qwen3_4b_b64", 2, "round"),     # grouped with the slot projection, 16 rows
     ("phi4_bf16", 1, "round"),                # Phi-4 widths: 164 tiles
+    ("serving_qwen3_4b_b64", 5, "round"),     # token-major stream-K: 40 and 35 token rows
+    ("serving_qwen3_4b_b64", 33, "round"),    # token-major: three token tiles, ragged last
+    ("serving_qwen3_4b_b64", 5, "separate"),  # token-major cluster split-K, 35 and 40 rows
 ])
 def test_stream_k_products(name, batch, api):
     """Skinny products with more weight tiles than SMs run stream-K (equal
