@@ -518,7 +518,6 @@ __device__ __forceinline__ void mem_cta(const Args& a, uint8_t* sm, int idx) {
 constexpr int KT = 64;         // keys per window tile
 constexpr int KTS = KT + 16;   // rows of a tile buffer: window tile + slot rows
 constexpr int TC_STAGES = 2;   // window tiles in flight per CTA
-constexpr int OW_MAX = 16;     // 16x8 O fragments per warp (head-dim part <= 128)
 
 // Warp roles of the tensor-core attention for a shape.
 struct TcWarps {
@@ -597,6 +596,21 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// 2^x on the special-function unit (ex2.approx.ftz; 2^-inf = 0). The
+// probabilities it makes are rounded to bf16 right after, far coarser than
+// its error.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// A row's running max moves only when a chunk's max exceeds it by more than
+// this (log2 units); otherwise the chunk's exponentials are taken against the
+// older max and stay below 2^kRescaleLog2. (m, l, O) stay consistent either
+// way, so the merges are unchanged and the result differs by rounding only.
+constexpr float kRescaleLog2 = 8.f;
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -609,6 +623,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t& r0, uint32_t& r1
                : "r"(a));
 }
 
+template <int DH>
 __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk,
                                             const CUtensorMap* mv, uint8_t* sm_raw, int idx) {
   const Dims& d = a.d;
@@ -616,7 +631,9 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   const int rank = nsplit > 1 ? (int)cluster_rank() : 0;
   const int pair = idx / nsplit;
   const int kvh = pair % d.Hkv, b = pair / d.Hkv;
-  const int S = d.S, G = d.G, R = G * S, dh = d.dh, dsub = dh / 64;
+  const int S = d.S, G = d.G, R = G * S;
+  constexpr int dh = DH, dsub = DH / 64;
+  constexpr int NTO = (DH > 128 ? 128 : DH) / 8;  // 16x8 O fragments per warp
   const TcLayout L = make_tc_layout(d);
   const TcWarps W = tc_warps(d);
   const int QR = L.qrows;
@@ -663,7 +680,7 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     if (!waited) pdl_wait();
     waited = true;
   };
-  const int c4n = dh / 4;
+  constexpr int c4n = DH / 4;
   auto stage = [&]() {
     // Q rows (pre-scaled) as bf16; rows R..QR-1 zero.
     for (int i = tid; i < QR * c4n; i += nthr) {
@@ -730,95 +747,96 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   const int nact = W.mt * W.kg * W.dp;
   const bool active = warp < nact;
   const int wdp = warp % W.dp, wkg = (warp / W.dp) % W.kg, wmt = warp / (W.dp * W.kg);
-  const int NTO = W.dw / 8;  // O fragments of this warp
-  float o[OW_MAX][4];
+  float o[NTO][4];
 #pragma unroll
-  for (int k = 0; k < OW_MAX; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+  for (int k = 0; k < NTO; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY;  // running max of rows g8, g8 + 8 of the m-tile
   float l0 = 0.f, l1 = 0.f;              // this lane's part of the running sums
-  const uint32_t qb = smem_u32(qt);
   const int qrow = wmt * 16 + (lane & 15);
+  // ldmatrix addresses: a fragment's 16-byte chunk index within its 128-byte
+  // row is (2 * step + half) XOR (row & 7); the half bit and the row phase are
+  // per lane, the step is a compile-time constant
+  const uint32_t qbase = smem_u32(qt) + (uint32_t)qrow * 128;
+  const uint32_t qblk = (uint32_t)QR * 128;                              // one 64-column block of Q
+  const uint32_t qh4 = (uint32_t)(((lane >> 4) ^ (lane & 7)) << 4);       // Q and V rows
+  const uint32_t kh4 = (uint32_t)((((lane >> 3) & 1) ^ (lane & 7)) << 4);  // K rows
+  const uint32_t vcol = (uint32_t)(wdp * (NTO / 8)) * KTS * 128;          // this warp's V columns
 
-  // One online-softmax update over the 16 keys at tile rows kr..kr+15 of
-  // the K/V buffers kb/vb; key row j is valid when j < nvr or KT <= j < KT + nsk.
-  // One online-softmax update over the 16 keys at tile rows kr..kr+15 of
-  // the K/V buffers kb/vb; key row j is valid when j < nvr or KT <= j < KT + nsk.
-  auto update = [&](uint32_t kb, uint32_t vb, int kr, int nvr, int nsk) {
-    float sc[2][4];
+  // One online-softmax update over the 16 keys at tile rows kr..kr+15 of the
+  // K/V buffers kb/vb; key row j is valid when j < lim.
+  auto update = [&](uint32_t kb, uint32_t vb, int kr, int lim) {
+    // [n-fragment][k-step parity][...]: two shorter mma chains per fragment
+    // (one at head dim 256, where the registers are needed for O)
+    constexpr int CH = DH > 128 ? 1 : 2;
+    float sc[2][CH][4];
 #pragma unroll
-    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int h = 0; h < CH; ++h) sc[n][h][0] = sc[n][h][1] = sc[n][h][2] = sc[n][h][3] = 0.f;
     // S = Q K^T: per k-step one Q fragment and one K fragment pair
     const uint32_t krow = kb + (uint32_t)(kr + (lane & 7) + ((lane >> 4) << 3)) * 128;
-    const int kx = lane & 7;  // row phase of the swizzle (kr is a multiple of 8)
-    for (int ks = 0; ks < dh / 16; ++ks) {
+#pragma unroll
+    for (int ks = 0; ks < DH / 16; ++ks) {
       uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-      ldsm_x4(qb + sw_chunk(QR, qrow, ks * 2 + (lane >> 4)), a0, a1, a2, a3);
-      const int c = ks * 2 + ((lane >> 3) & 1);
-      ldsm_x4(krow + (uint32_t)((c >> 3) * KTS * 128 + (((c & 7) ^ kx) << 4)), b0, b1, b2, b3);
-      mma_bf16_16816(sc[0], a0, a1, a2, a3, b0, b1);
-      mma_bf16_16816(sc[1], a0, a1, a2, a3, b2, b3);
+      const uint32_t ph = (uint32_t)((ks & 3) << 5);
+      ldsm_x4(qbase + (uint32_t)(ks >> 2) * qblk + (ph ^ qh4), a0, a1, a2, a3);
+      ldsm_x4(krow + (uint32_t)((ks >> 2) * KTS * 128) + (ph ^ kh4), b0, b1, b2, b3);
+      mma_bf16_16816(sc[0][ks % CH], a0, a1, a2, a3, b0, b1);
+      mma_bf16_16816(sc[1][ks % CH], a0, a1, a2, a3, b2, b3);
     }
-    // masked row maxima over this warp's keys (quad of lanes per row)
-    float x0 = -INFINITY, x1 = -INFINITY;
+    float x0 = -INFINITY, x1 = -INFINITY;  // masked row maxima (quad of lanes per row)
+    float t[2][4];
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
-        const int j = kr + n * 8 + 2 * t4;
-        const bool v0 = j < nvr || (j >= KT && j < KT + nsk);
-        const bool v1 = j + 1 < nvr || (j + 1 >= KT && j + 1 < KT + nsk);
-        if (!v0) sc[n][0] = sc[n][2] = -INFINITY;
-        if (!v1) sc[n][1] = sc[n][3] = -INFINITY;
-        x0 = fmaxf(x0, fmaxf(sc[n][0], sc[n][1]));
-        x1 = fmaxf(x1, fmaxf(sc[n][2], sc[n][3]));
-      }
+      const int j = kr + n * 8 + 2 * t4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) t[n][e] = CH == 2 ? sc[n][0][e] + sc[n][CH - 1][e] : sc[n][0][e];
+      if (j >= lim) t[n][0] = t[n][2] = -INFINITY;
+      if (j + 1 >= lim) t[n][1] = t[n][3] = -INFINITY;
+      x0 = fmaxf(x0, fmaxf(t[n][0], t[n][1]));
+      x1 = fmaxf(x1, fmaxf(t[n][2], t[n][3]));
+    }
     x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
     x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
     x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
     x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
-    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    const float s0 = m0 == -INFINITY ? 0.f : exp2f(m0 - n0);
-    const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - n1);
-    m0 = n0;
-    m1 = n1;
-    l0 *= s0;
-    l1 *= s1;
+    if (__any_sync(0xffffffffu, x0 > m0 + kRescaleLog2 || x1 > m1 + kRescaleLog2)) {
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      const float s0 = n0 == -INFINITY ? 1.f : ex2_fast(m0 - n0);
+      const float s1 = n1 == -INFINITY ? 1.f : ex2_fast(m1 - n1);
+      m0 = n0;
+      m1 = n1;
+      l0 *= s0;
+      l1 *= s1;
 #pragma unroll
-    for (int k = 0; k < OW_MAX; ++k)
-      if (k < NTO) {
+      for (int k = 0; k < NTO; ++k) {
         o[k][0] *= s0;
         o[k][1] *= s0;
         o[k][2] *= s1;
         o[k][3] *= s1;
       }
+    }
     // P = exp2(S - m) rounded to bf16, packed as the A operand of P.V
     uint32_t pa[2][2];
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
-        const float e0 = sc[n][0] == -INFINITY ? 0.f : exp2f(sc[n][0] - n0);
-        const float e1 = sc[n][1] == -INFINITY ? 0.f : exp2f(sc[n][1] - n0);
-        const float e2 = sc[n][2] == -INFINITY ? 0.f : exp2f(sc[n][2] - n1);
-        const float e3 = sc[n][3] == -INFINITY ? 0.f : exp2f(sc[n][3] - n1);
-        pa[n][0] = pack_bf16x2(e0, e1);
-        pa[n][1] = pack_bf16x2(e2, e3);
-        const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[n][0]));
-        const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[n][1]));
-        l0 += r0.x + r0.y;
-        l1 += r1.x + r1.y;
-      }
+      pa[n][0] = pack_bf16x2(ex2_fast(t[n][0] - m0), ex2_fast(t[n][1] - m0));
+      pa[n][1] = pack_bf16x2(ex2_fast(t[n][2] - m1), ex2_fast(t[n][3] - m1));
+      const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[n][0]));
+      const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pa[n][1]));
+      l0 += r0.x + r0.y;
+      l1 += r1.x + r1.y;
+    }
     // O += P V over this warp's head-dim part, two 8-column fragments per load
-    {
-      const int key = kr + (lane & 7) + ((lane >> 3) & 1) * 8;
-      const uint32_t vrow = vb + (uint32_t)key * 128;
-      const int c0 = wdp * (W.dw / 8) + (lane >> 4);
+    const int key = kr + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t vrow = vb + (uint32_t)key * 128 + vcol;
 #pragma unroll
-      for (int k = 0; k < OW_MAX; k += 2)
-        if (k < NTO) {
-          uint32_t b0, b1, b2, b3;
-          const int c = c0 + k;
-          ldsm_x4_t(vrow + (uint32_t)((c >> 3) * KTS * 128 + (((c & 7) ^ (key & 7)) << 4)), b0, b1,
-                    b2, b3);
-          mma_bf16_16816(o[k], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b0, b1);
-          mma_bf16_16816(o[k + 1], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b2, b3);
-        }
+    for (int k = 0; k < NTO; k += 2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vrow + (uint32_t)((k >> 3) * KTS * 128) + ((uint32_t)((k & 7) << 4) ^ qh4), b0,
+                b1, b2, b3);
+      mma_bf16_16816(o[k], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b0, b1);
+      mma_bf16_16816(o[k + 1], pa[0][0], pa[0][1], pa[1][0], pa[1][1], b2, b3);
     }
   };
 
@@ -849,10 +867,10 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     }
     if (active && ring)
       for (int q = 0; q < W.kw; q += 16)
-        if (wkg * W.kw + q < nvr) update(smem_u32(kt), smem_u32(vt), wkg * W.kw + q, nvr, 0);
+        if (wkg * W.kw + q < nvr) update(smem_u32(kt), smem_u32(vt), wkg * W.kw + q, nvr);
     // the slot keys (rows KT..KT+15) go to the last key group
     if (with_slots && active && wkg == W.kg - 1)
-      update(smem_u32(kt), smem_u32(vt), KT, 0, S);
+      update(smem_u32(kt), smem_u32(vt), KT, KT + S);
     if (ring) {
       __syncthreads();  // every warp done with this stage
       if (tid == 0 && i + TC_STAGES < nwt) {
@@ -894,11 +912,10 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     const int r = wmt * 16 + g8;
     float* ob = okg + ((size_t)wkg * QR + r) * OLD + wdp * W.dw + 2 * t4;
 #pragma unroll
-    for (int k = 0; k < OW_MAX; ++k)
-      if (k < NTO) {
-        *reinterpret_cast<float2*>(ob + k * 8) = make_float2(o[k][0], o[k][1]);
-        *reinterpret_cast<float2*>(ob + 8 * OLD + k * 8) = make_float2(o[k][2], o[k][3]);
-      }
+    for (int k = 0; k < NTO; ++k) {
+      *reinterpret_cast<float2*>(ob + k * 8) = make_float2(o[k][0], o[k][1]);
+      *reinterpret_cast<float2*>(ob + 8 * OLD + k * 8) = make_float2(o[k][2], o[k][3]);
+    }
     if (t4 == 0 && wdp == 0) {
       float* mb = mlk + ((size_t)wkg * QR + r) * 2;
       mb[0] = m0;
@@ -909,19 +926,31 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   }
   __syncthreads();
   // merge the key groups per row: M = max m_k, L = sum w_k l_k, O = sum w_k O_k.
-  // Thread tid owns 4 columns (c) of rows r0, r0 + rstep, ...
-  __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
-  const int c = (tid % c4n) * 4, rstep = nthr / c4n;
-  for (int r = tid / c4n; r < R; r += rstep) {
+  // First one thread per row turns each group's max into its weight w_k
+  // (in place) and keeps L (1/L when there is no cluster combine) with M.
+  for (int r = tid; r < R; r += nthr) {
     float M = -INFINITY;
     for (int k = 0; k < W.kg; ++k) M = fmaxf(M, mlk[((size_t)k * QR + r) * 2]);
     float Ls = 0.f;
+    for (int k = 0; k < W.kg; ++k) {
+      float* e = mlk + ((size_t)k * QR + r) * 2;
+      const float lk = e[1];
+      const float wt = lk > 0.f ? ex2_fast(e[0] - M) : 0.f;  // an empty group weighs 0
+      Ls = fmaf(wt, lk, Ls);
+      e[0] = wt;
+    }
+    ml[r * 2] = M;
+    ml[r * 2 + 1] = nsplit == 1 ? 1.f / Ls : Ls;
+  }
+  __syncthreads();
+  // then thread tid sums 4 columns (c) of rows r0, r0 + rstep, ...
+  __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
+  const int c = (tid % c4n) * 4, rstep = nthr / c4n;
+  for (int r = tid / c4n; r < R; r += rstep) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < W.kg; ++k) {
-      const float lk = mlk[((size_t)k * QR + r) * 2 + 1];
-      const float wt = lk > 0.f ? exp2f(mlk[((size_t)k * QR + r) * 2] - M) : 0.f;
+      const float wt = mlk[((size_t)k * QR + r) * 2];
       const float4 ov = *reinterpret_cast<const float4*>(okg + ((size_t)k * QR + r) * OLD + c);
-      Ls = fmaf(wt, lk, Ls);
       acc.x = fmaf(wt, ov.x, acc.x);
       acc.y = fmaf(wt, ov.y, acc.y);
       acc.z = fmaf(wt, ov.z, acc.z);
@@ -929,16 +958,12 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     }
     if (nsplit == 1) {
       const int g = r / S, sl = r % S;
-      const float inv = 1.f / Ls;
+      const float inv = ml[r * 2 + 1];
       __nv_bfloat16* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
       *reinterpret_cast<uint2*>(dst) =
           make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
     } else {
       *reinterpret_cast<float4*>(octa + (size_t)r * OLD + c) = acc;
-      if (c == 0) {
-        ml[r * 2] = M;
-        ml[r * 2 + 1] = Ls;
-      }
     }
   }
   if (nsplit == 1) return;
@@ -1061,13 +1086,14 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
   }
 }
 
+template <int DH>
 __global__ void __launch_bounds__(THREADS, 2)
 attn_tc_kernel(Args a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
   extern __shared__ __align__(128) uint8_t sm[];
   pdl_trigger();
   const int idx = blockIdx.x;
   if (idx < a.n_attn)
-    attn_tc_cta(a, &mk, &mv, sm, idx);
+    attn_tc_cta<DH>(a, &mk, &mv, sm, idx);
   else if (idx < a.n_attn + a.n_mem) {
     if (a.mem_tc)
       mem_tc_cta(a, sm, idx - a.n_attn);
@@ -1134,7 +1160,9 @@ cudaError_t configure_attn_cluster(const Dims&) {
   if (configured) return cudaSuccess;
   cudaError_t e = configure_dtype<float>();
   if (e == cudaSuccess) e = configure_dtype<__nv_bfloat16>();
-  if (e == cudaSuccess) e = configure_kernel(attn_tc_kernel);
+  if (e == cudaSuccess) e = configure_kernel(attn_tc_kernel<64>);
+  if (e == cudaSuccess) e = configure_kernel(attn_tc_kernel<128>);
+  if (e == cudaSuccess) e = configure_kernel(attn_tc_kernel<256>);
   if (e == cudaSuccess) configured = true;
   return e;
 }
@@ -1212,7 +1240,14 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   ++*launches;
-  if (tc) return cudaLaunchKernelEx(&cfg, attn_tc_kernel, a, *mk, *mv);
+  if (tc) {
+    switch (d.dh) {
+      case 64: return cudaLaunchKernelEx(&cfg, attn_tc_kernel<64>, a, *mk, *mv);
+      case 128: return cudaLaunchKernelEx(&cfg, attn_tc_kernel<128>, a, *mk, *mv);
+      case 256: return cudaLaunchKernelEx(&cfg, attn_tc_kernel<256>, a, *mk, *mv);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (dtype == HF_F32) return launch_typed<float>(cfg, a);
   return launch_typed<__nv_bfloat16>(cfg, a);
 }
