@@ -39,6 +39,18 @@ Readings where the pages are silent (each is also listed in the design notes):
   R8 bf16 mode: float64 arithmetic on the bf16-rounded inputs and weights, no
      emulation of intermediate rounding.
 
+Ablation modes (the paper's intervention table "Recurrent history" /
+"Intra-block interactions", and the explainer's paragraph on the ablations),
+off by default, selected by two fields of the shape:
+  R9  cross_slot = False ("Cross-slot off"): attention among the draft slots
+      is switched off -- slot s attends to the window entries and to its own
+      key only; the other slots' keys are masked;
+  R10 mem_horizon = M > 0 ("SSM: Last 512" with M = 512, "SSM: Last feature"
+      with M = 1): the recurrent history is restricted to the last M
+      committed features -- the memory is the fold from h = 0 over the last
+      min(pos, M) committed features, whatever came before them. M = 0 keeps
+      the whole history.
+
 Parity pins (tests/test_oracle_pins.py): the chunked fold equals the
 token-by-token recurrence and the unrolled product closed form; constant decay
 matches scipy.signal.lfilter; A = 0 gives the plain sum, huge decay keeps only
@@ -167,6 +179,7 @@ class Context:
     tag: np.ndarray      # [W] committed position held by each slot, -1 if empty
     pos: int             # committed tokens so far
     h: np.ndarray        # [Hm, P, N]
+    hist: Optional[tuple] = None  # R10: (x, B, dt) of the last M committed features
 
     @staticmethod
     def empty(cfg) -> "Context":
@@ -179,6 +192,16 @@ class Context:
 
     def clone(self) -> "Context":
         return copy.deepcopy(self)
+
+
+def mem_horizon(cfg) -> int:
+    """R10: 0 = whole history, M > 0 = the last M committed features."""
+    return int(getattr(cfg, "mem_horizon", 0) or 0)
+
+
+def cross_slot(cfg) -> bool:
+    """R9: False masks slot-to-slot attention (each slot keeps its own key)."""
+    return bool(getattr(cfg, "cross_slot", True))
 
 
 def ring_slot(position: int, window: int) -> int:
@@ -214,6 +237,10 @@ def prefill_layer(lw: Weights64, cfg, feats: np.ndarray,
     if L == 0:
         return ctx
     x, B, dt = ssm_inputs(lw, cfg, feats)
+    M = mem_horizon(cfg)
+    if M > 0:  # R10: only the last M features are remembered
+        x, B, dt = x[-M:], B[-M:], dt[-M:]
+        ctx.hist = (x, B, dt)
     if method == "recurrent":
         ctx.h = ssm_fold_recurrent(ctx.h, x, B, dt, lw.A)
     else:
@@ -235,7 +262,17 @@ def commit_layer(lw: Weights64, cfg, ctx: Context, feats_rows: np.ndarray,
     k, v = kv_of(lw, cfg, f)
     ring_append(out, cfg, k, v, out.pos)
     x, B, dt = ssm_inputs(lw, cfg, f)
-    out.h = ssm_fold_recurrent(out.h, x, B, dt, lw.A)
+    M = mem_horizon(cfg)
+    if M > 0:
+        # R10: keep the last M committed features and fold them afresh
+        if out.hist is not None:
+            x = np.concatenate([out.hist[0], x])
+            B = np.concatenate([out.hist[1], B])
+            dt = np.concatenate([out.hist[2], dt])
+        out.hist = (x[-M:], B[-M:], dt[-M:])
+        out.h = ssm_fold_recurrent(np.zeros_like(out.h), *out.hist, lw.A)
+    else:
+        out.h = ssm_fold_recurrent(out.h, x, B, dt, lw.A)
     out.pos += n
     return out
 
@@ -252,7 +289,8 @@ def softmax_rows(s: np.ndarray) -> np.ndarray:
 
 def window_block_attention(cfg, ctx: Context, Q, Ks, Vs) -> np.ndarray:
     """Bidirectional attention of the slot queries over the valid window
-    entries plus all slot keys (R4, R5). Q [S,Hq,dh], Ks/Vs [S,Hkv,dh]."""
+    entries plus all slot keys (R4, R5); with cross_slot off (R9) slot s sees
+    the window and its own key only. Q [S,Hq,dh], Ks/Vs [S,Hkv,dh]."""
     S = Q.shape[0]
     G = cfg.n_q_heads // cfg.n_kv_heads
     valid = np.nonzero(ctx.tag >= 0)[0]
@@ -262,7 +300,11 @@ def window_block_attention(cfg, ctx: Context, Q, Ks, Vs) -> np.ndarray:
         g = hq // G
         keys = np.concatenate([ctx.ring_k[g, valid, :], Ks[:, g, :]], axis=0)
         vals = np.concatenate([ctx.ring_v[g, valid, :], Vs[:, g, :]], axis=0)
-        p = softmax_rows((Q[:, hq, :] @ keys.T) * scale)
+        scores = (Q[:, hq, :] @ keys.T) * scale
+        if not cross_slot(cfg):
+            slot_part = scores[:, len(valid):]
+            slot_part[~np.eye(S, dtype=bool)] = -np.inf
+        p = softmax_rows(scores)
         O[:, hq, :] = p @ vals
     return O
 

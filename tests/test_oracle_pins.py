@@ -333,3 +333,115 @@ def test_sizing_matches_printed_figures():
     st = O.state_bytes(s["n_layers"], s["d_inner"], s["d_state"], s["elem_bytes"])
     assert st == s["bytes"] == int(2.5 * 2**20)
     assert kv + st == g["drafter_context_total"]["bytes"]
+
+
+# ---------------------------------------------------------------- ablation modes
+# (paper, intervention table: "Cross-slot off", "SSM: Last 512", "SSM: Last
+# feature"; explainer, paragraph on the ablations)
+
+def test_cross_slot_off_empty_window_returns_own_value():
+    # with no window entries each slot attends to its own key alone: O = V_s
+    cfg = small_cfg(cross_slot=False)
+    ctx = O.Context.empty(cfg)
+    ctx.ring_k[:] = 1e3  # unused slots are never read
+    rng = np.random.default_rng(30)
+    Q = rng.standard_normal((7, cfg.n_q_heads, cfg.head_dim))
+    Ks = rng.standard_normal((7, cfg.n_kv_heads, cfg.head_dim))
+    Vs = rng.standard_normal((7, cfg.n_kv_heads, cfg.head_dim))
+    out = O.window_block_attention(cfg, ctx, Q, Ks, Vs)
+    G = cfg.n_q_heads // cfg.n_kv_heads
+    for hq in range(cfg.n_q_heads):
+        assert np.array_equal(out[:, hq], Vs[:, hq // G])
+
+
+def test_cross_slot_off_matches_sdpa_with_mask():
+    cfg = small_cfg(window=64, cross_slot=False)
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(31)
+    pre = rng.standard_normal((23, cfg.d_model))
+    ctx = O.prefill_layer(lw, cfg, pre)
+    X = rng.standard_normal((7, cfg.d_model))
+    _, parts = O.draft_layer(lw, cfg, ctx, X, return_parts=True)
+    kp, vp = O.kv_of(lw, cfg, pre)
+    keys = np.concatenate([kp, parts["Ks"]], 0)
+    vals = np.concatenate([vp, parts["Vs"]], 0)
+    allowed = torch.ones((7, 23 + 7), dtype=torch.bool)
+    allowed[:, 23:] = torch.eye(7, dtype=torch.bool)   # window + own key
+    q = torch.tensor(parts["Q"]).permute(1, 0, 2)[None]
+    G = cfg.n_q_heads // cfg.n_kv_heads
+    k = torch.tensor(keys).permute(1, 0, 2)[None].repeat_interleave(G, dim=1)
+    v = torch.tensor(vals).permute(1, 0, 2)[None].repeat_interleave(G, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=allowed)
+    assert rel(parts["O"], ref[0].permute(1, 0, 2).numpy()) < 1e-13
+    # and it differs from the default (slots interact)
+    full = O.window_block_attention(small_cfg(window=64), ctx, parts["Q"], parts["Ks"], parts["Vs"])
+    assert rel(full, parts["O"]) > 1e-3
+
+
+def _last_term(lw, cfg, f):
+    """dt x (outer) B of one feature row via torch (softplus and matmuls)."""
+    ft = torch.tensor(f[None])
+    dt = torch.nn.functional.softplus(ft @ torch.tensor(lw.w_dt) + torch.tensor(lw.dt_bias),
+                                      threshold=1e6)[0]
+    x = (ft @ torch.tensor(lw.w_x))[0].reshape(cfg.ssm_heads, cfg.ssm_headdim)
+    B = (ft @ torch.tensor(lw.w_B))[0]
+    return (dt[:, None, None] * x[:, :, None] * B[None, None, :]).numpy()
+
+
+def test_memory_horizon_one_is_last_feature():
+    cfg = small_cfg(mem_horizon=1)
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(32)
+    pre = rng.standard_normal((9, cfg.d_model))
+    ctx = O.prefill_layer(lw, cfg, pre)
+    assert rel(ctx.h, _last_term(lw, cfg, pre[-1])) < 1e-14
+    rows = rng.standard_normal((8, cfg.d_model))
+    c = O.commit_layer(lw, cfg, ctx, rows, 3)
+    assert rel(c.h, _last_term(lw, cfg, rows[2])) < 1e-14
+    z = O.commit_layer(lw, cfg, c, rows, 0)    # n = 0: unchanged
+    assert np.array_equal(z.h, c.h)
+
+
+def test_memory_horizon_without_decay_is_window_sum():
+    # A = 0: the memory is the plain sum of dt x (outer) B over the last M features
+    cfg = small_cfg(mem_horizon=5)
+    w = make_layer_weights(cfg, 0)
+    lw = O.Weights64.from_any(w)
+    lw.A_log[:] = -1e9                          # A = -exp(-1e9) = 0
+    rng = np.random.default_rng(33)
+    feats = rng.standard_normal((9 + 3 + 4, cfg.d_model))
+    ctx = O.prefill_layer(lw, cfg, feats[:9])
+    ctx = O.commit_layer(lw, cfg, ctx, feats[9:17], 3)
+    ctx = O.commit_layer(lw, cfg, ctx, np.concatenate([feats[12:], feats[:4]]), 4)
+    want = sum(_last_term(lw, cfg, feats[t]) for t in range(16 - 5, 16))
+    assert rel(ctx.h, want) < 1e-13
+    # the window moved past the early features: those no longer count at all
+    assert rel(ctx.h, sum(_last_term(lw, cfg, feats[t]) for t in range(16 - 6, 16))) > 1e-3
+
+
+def test_memory_horizon_long_enough_equals_whole_history():
+    cfg_all = small_cfg()
+    cfg_m = small_cfg(mem_horizon=40)
+    lw = O.Weights64.from_any(make_layer_weights(cfg_all, 0))
+    rng = np.random.default_rng(34)
+    pre = rng.standard_normal((11, cfg_all.d_model))
+    rows = rng.standard_normal((8, cfg_all.d_model))
+    a = O.commit_layer(lw, cfg_all, O.prefill_layer(lw, cfg_all, pre), rows, 6)
+    b = O.commit_layer(lw, cfg_m, O.prefill_layer(lw, cfg_m, pre), rows, 6)
+    assert rel(b.h, a.h) < 1e-12
+
+
+def test_memory_horizon_commits_equal_prefill_of_last_m():
+    # whatever the commit pattern, the memory is the fold of the last M features
+    cfg = small_cfg(mem_horizon=6)
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(35)
+    feats = rng.standard_normal((30, cfg.d_model))
+    ctx = O.prefill_layer(lw, cfg, feats[:4])
+    used = 4
+    for n in (3, 0, 8, 1, 5):
+        rows = np.concatenate([feats[used:used + n], rng.standard_normal((8 - n, cfg.d_model))])
+        ctx = O.commit_layer(lw, cfg, ctx, rows, n)
+        used += n
+        ref = O.prefill_layer(lw, small_cfg(), feats[max(0, used - 6):used], method="recurrent")
+        assert rel(ctx.h, ref.h) < 1e-12

@@ -49,6 +49,10 @@ class DrafterShape:
     n_groups: int = 1
     prefix_lo: int = 0     # log-uniform prefix range (serving batch)
     prefix_hi: int = 0
+    # ablation modes (off by default): slot-to-slot attention masked; memory
+    # restricted to the last mem_horizon committed features (0: all of them)
+    cross_slot: bool = True
+    mem_horizon: int = 0
 
     @property
     def d_inner(self) -> int:
