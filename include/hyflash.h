@@ -94,6 +94,19 @@ typedef struct {
   int32_t chunk;        /* prefill scan chunk length: 64, 128 or 256 */
   int32_t dtype;        /* hf_dtype */
   int64_t prefill_tokens_max; /* tokens per internal prefill pass; 0 = 16384 */
+  /* Ablation modes of the paper's intervention table (HyFlash paper, table
+   * "Recurrent history" / "Intra-block interactions"), 0 = off:
+   *   cross_slot_off = 1: attention among the draft slots is switched off --
+   *     slot s attends to the window entries and to its own key only
+   *     ("Cross-slot off");
+   *   mem_horizon = M > 0: the memory holds the fold, from zero, of the last
+   *     M committed features only ("SSM: Last 512" is M = 512, "SSM: Last
+   *     feature" M = 1); M <= window. For M > 1 the handle keeps the x, B
+   *     and dt rows of the last M + block + 1 committed features per request
+   *     and layer, and each commit removes the contribution of the features
+   *     that leave the horizon. */
+  int32_t cross_slot_off;
+  int32_t mem_horizon;
 } hf_config;
 
 /* One layer's weights, HOST pointers, row-major [in, out] in the handle's
@@ -195,8 +208,13 @@ typedef enum {
                          last commit (entries past its batch are stale) */
   HF_T_DRAFT_PROJ = 6,/* fp32 [max_batch*block, Hq*dh + 2*Hkv*dh + N]: last
                          layer's slot projections Q|K_s|V_s|C_s, last draft */
-  HF_T_DRAFT_MIX = 7  /* dtype [max_batch*block, Hq*dh + Hm*P]: last layer's
+  HF_T_DRAFT_MIX = 7, /* dtype [max_batch*block, Hq*dh + Hm*P]: last layer's
                          attention output | memory read y, last draft */
+  /* memory horizon M > 1 only (0 bytes otherwise); R = M + block + 1 ring
+   * rows, committed position t in row t mod R */
+  HF_T_MEM_X = 8,     /* fp32 [L, max_batch, R, Hm*P]: x of the last features */
+  HF_T_MEM_B = 9,     /* fp32 [L, max_batch, R, N]: B of the last features */
+  HF_T_MEM_DT = 10    /* fp32 [L, max_batch, Hm, R]: dt (after softplus) */
 } hf_tensor_id;
 
 /* Size in bytes of an inspectable tensor. */
@@ -206,7 +224,8 @@ hf_status hf_tensor_bytes(const hf_handle* h, int32_t which, size_t* bytes);
  * hf_tensor_bytes). Synchronises the device. */
 hf_status hf_read_tensor(hf_handle* h, int32_t which, void* host_out, size_t bytes);
 
-/* Bytes of the complete drafter context (states, rings, tags, positions):
+/* Bytes of the complete drafter context (states, rings, tags, positions,
+ * and with a memory horizon M > 1 the x/B/dt rows of the last features):
  * the fixed-size draft-side memory of all requests and layers. */
 size_t hf_context_bytes(const hf_handle* h);
 

@@ -42,6 +42,9 @@ class Tensor(enum.IntEnum):
     OFFSETS = 5
     DRAFT_PROJ = 6
     DRAFT_MIX = 7
+    MEM_X = 8
+    MEM_B = 9
+    MEM_DT = 10
 
 
 class Family(enum.IntEnum):
@@ -62,7 +65,9 @@ class HfConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "d_model", "n_q_heads", "n_kv_heads", "head_dim", "window", "block",
         "ssm_heads", "ssm_headdim", "d_state", "n_groups", "n_layers",
-        "max_batch", "chunk", "dtype")] + [("prefill_tokens_max", ctypes.c_int64)]
+        "max_batch", "chunk", "dtype")] + [("prefill_tokens_max", ctypes.c_int64),
+                                           ("cross_slot_off", ctypes.c_int32),
+                                           ("mem_horizon", ctypes.c_int32)]
 
 
 WEIGHT_FIELDS = ("w_q", "w_k", "w_v", "w_o", "w_x", "w_B", "w_C", "w_dt", "w_mo",
@@ -130,7 +135,9 @@ def make_config(shape, max_batch: int, prefill_tokens_max: int = 0) -> HfConfig:
         n_groups=getattr(shape, "n_groups", 1), n_layers=shape.n_layers, max_batch=max_batch,
         chunk=getattr(shape, "chunk", 128),
         dtype=HF_F32 if shape.dtype in ("f32", "fp32", "float32") else HF_BF16,
-        prefill_tokens_max=prefill_tokens_max)
+        prefill_tokens_max=prefill_tokens_max,
+        cross_slot_off=0 if getattr(shape, "cross_slot", True) else 1,
+        mem_horizon=int(getattr(shape, "mem_horizon", 0) or 0))
 
 
 def _stream_ptr(stream) -> Optional[int]:
@@ -265,6 +272,8 @@ class Drafter:
     def read(self, which: int) -> np.ndarray:
         """Whole inspectable tensor as a NumPy array (bf16 returned as float32)."""
         nb = self.tensor_bytes(which)
+        if nb == 0:  # memory-horizon rows of a handle without them
+            return np.zeros((0,), dtype=np.float32)
         buf = np.empty(nb, dtype=np.uint8)
         self._check(hf_read_tensor(self._h, int(which), buf.ctypes.data, nb))
         sh, L, Bm = self.shape, self.shape.n_layers, self.max_batch
@@ -282,6 +291,12 @@ class Drafter:
             return buf.view(np.int32).copy()
         if which == Tensor.DRAFT_PROJ:
             return buf.view(np.float32).reshape(Bm * sh.block, -1)
+        if which in (Tensor.MEM_X, Tensor.MEM_B, Tensor.MEM_DT):
+            R = int(getattr(sh, "mem_horizon", 0)) + sh.block + 1
+            a = buf.view(np.float32)
+            if which == Tensor.MEM_DT:
+                return a.reshape(L, Bm, sh.ssm_heads, R)
+            return a.reshape(L, Bm, R, -1)
         return self._model_to_f32(buf).reshape(Bm * sh.block, -1)
 
     def _model_to_f32(self, buf: np.ndarray) -> np.ndarray:

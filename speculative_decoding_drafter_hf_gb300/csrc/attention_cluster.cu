@@ -275,7 +275,11 @@ __device__ __forceinline__ void attn_cta(const Args& a, uint8_t* sm, int idx) {
         if (hl == 0 && j < nk) {
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr)
-            if (r0 + rr < R) s[(r0 + rr) * JK + j] = acc[rr];
+            if (r0 + rr < R) {
+              // cross-slot off: slot key j - nring counts for its own slot only
+              const bool masked = d.xoff && j >= nring && j - nring != (r0 + rr) % S;
+              s[(r0 + rr) * JK + j] = masked ? -INFINITY : acc[rr];
+            }
         }
       }
     }
@@ -762,9 +766,14 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   const uint32_t kh4 = (uint32_t)((((lane >> 3) & 1) ^ (lane & 7)) << 4);  // K rows
   const uint32_t vcol = (uint32_t)(wdp * (NTO / 8)) * KTS * 128;          // this warp's V columns
 
+  // slots of this lane's two rows (cross-slot off masks the other slots' keys)
+  const int sl0 = (wmt * 16 + g8) % S, sl1 = (wmt * 16 + g8 + 8) % S;
+
   // One online-softmax update over the 16 keys at tile rows kr..kr+15 of the
-  // K/V buffers kb/vb; key row j is valid when j < lim.
+  // K/V buffers kb/vb; key row j is valid when j < lim (and, for the slot
+  // keys with cross-slot attention off, when it is the row's own slot).
   auto update = [&](uint32_t kb, uint32_t vb, int kr, int lim) {
+    const bool own_slot = d.xoff && kr >= KT;
     // [n-fragment][k-step parity][...]: two shorter mma chains per fragment
     // (one at head dim 256, where the registers are needed for O)
     constexpr int CH = DH > 128 ? 1 : 2;
@@ -793,6 +802,13 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
       for (int e = 0; e < 4; ++e) t[n][e] = CH == 2 ? sc[n][0][e] + sc[n][CH - 1][e] : sc[n][0][e];
       if (j >= lim) t[n][0] = t[n][2] = -INFINITY;
       if (j + 1 >= lim) t[n][1] = t[n][3] = -INFINITY;
+      if (own_slot) {  // cross-slot off: a slot key counts for its own slot's rows only
+        const int js = j - KT;
+        if (js != sl0) t[n][0] = -INFINITY;
+        if (js + 1 != sl0) t[n][1] = -INFINITY;
+        if (js != sl1) t[n][2] = -INFINITY;
+        if (js + 1 != sl1) t[n][3] = -INFINITY;
+      }
       x0 = fmaxf(x0, fmaxf(t[n][0], t[n][1]));
       x1 = fmaxf(x1, fmaxf(t[n][2], t[n][3]));
     }

@@ -20,7 +20,7 @@ constexpr int QPT_HEAD = 8;  // float4 elements per thread when one CTA holds a 
 // when the memory read is fused), then the padded copy of the new state and
 // the k-part sums of the memory read.
 struct CsLayout {
-  size_t sx, sb, sd, rows, red, total;  // float offsets
+  size_t sx, sb, sd, sxo, sbo, sdo, wsum, rows, red, total;  // float offsets
 };
 __host__ __device__ inline CsLayout cs_layout(const Dims& d, bool read) {
   CsLayout m{};
@@ -28,7 +28,12 @@ __host__ __device__ inline CsLayout cs_layout(const Dims& d, bool read) {
   m.sx = 0;
   m.sb = m.sx + (size_t)lim * d.P;
   m.sd = m.sb + (size_t)lim * d.N;
-  m.rows = m.sd + ((lim + 3) & ~3);
+  m.sxo = m.sd + ((lim + 3) & ~3);
+  // memory horizon M > 1: the rows leaving the horizon, and a reduction slot
+  m.sbo = m.sxo + (d.Mr > 0 ? (size_t)lim * d.P : 0);
+  m.sdo = m.sbo + (d.Mr > 0 ? (size_t)lim * d.N : 0);
+  m.wsum = m.sdo + (d.Mr > 0 ? (size_t)((lim + 3) & ~3) : 0);
+  m.rows = m.wsum + (d.Mr > 0 ? 32 : 0);
   m.red = m.rows + (read ? (size_t)d.P * (d.N + 8) : 0);
   m.total = m.red + (read ? (size_t)mem_ksplit(d) * d.P * 8 : 0);
   return m;
@@ -55,7 +60,22 @@ __host__ __device__ inline CsLayout cs_layout(const Dims& d, bool read) {
 // the tensor cores from a padded shared-memory copy of the new state, into
 // mix[b*S + s][QD + h*P + p] -- the values the draft-time read would
 // produce, without reading the state a second time.
-template <typename T, int QPT>
+//
+// Memory horizon M (the paper's "SSM: Last feature" / "SSM: Last 512"
+// interventions: the memory is the fold, from zero, of the last M committed
+// features). M = 1: the new state is the last accepted row's term alone (the
+// old state is not read). M > 1: each accepted row at position p adds its
+// term and removes the term of the feature at position q = p - M, which
+// leaves the horizon; in the state after p that feature's weight is
+// dt_q * exp(A * sum_{s=q+1..p} dt_s), so
+//   h <- exp(dt_p A) h + dt_p x_p B_p^T - dt_q exp(A W_p) x_q B_q^T,
+//   W_p = sum of dt over positions q+1..p.
+// x, B and dt of the last Mr = M + S + 1 committed features sit in a ring
+// (row = position mod Mr); a commit reads rows of positions < T (its first
+// position, recorded by the commit projection) and writes rows T..T+n-1,
+// never the same rows (n <= S + 1). W is recomputed from the ring every
+// commit, so no running sum drifts. (RING: compiled in only for M > 1.)
+template <typename T, int QPT, bool RING>
 __global__ void __launch_bounds__(THREADS_CS)
 commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
                     const int32_t* __restrict__ n_acc,
@@ -63,7 +83,7 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
                     const float* __restrict__ A_log, float* __restrict__ state,
                     int64_t* __restrict__ pos, int32_t* __restrict__ offsets,
                     int32_t* __restrict__ tags, int32_t* __restrict__ err,
-                    const float* __restrict__ memC, T* __restrict__ mix) {
+                    const float* __restrict__ memC, T* __restrict__ mix, MemRing mr) {
   extern __shared__ __align__(16) float sm[];
   if (!late) pdl_trigger();
   if (!early) {
@@ -83,13 +103,15 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
   const int nq = P * N / 4;
   const int q0 = qs * QPT * THREADS_CS;
   const bool work = n > 0 || read;
+  const bool last_only = d.Mh == 1;       // memory = the last accepted row's term
+  const bool fresh = last_only && n > 0;  // (then the old state is not needed)
   float4 hv[QPT];
   int pi[QPT], ci[QPT];
 #pragma unroll
   for (int u = 0; u < QPT; ++u) {  // elements past the head: index 0 (in bounds), never stored
     const int q = q0 + threadIdx.x + u * THREADS_CS;
     const bool in = work && q < nq;
-    hv[u] = in ? __ldcg(&h[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    hv[u] = in && !fresh ? __ldcg(&h[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
     pi[u] = in ? (q * 4) / N : 0;
     ci[u] = in ? (q * 4) % N : 0;
   }
@@ -143,9 +165,77 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
     sd[t] = __ldcg(&xb[(size_t)t * d.NS + d.dinner + N + hd]);
   __syncthreads();
   const float A = -expf(__ldg(&A_log[l * d.Hm + hd]));
+  const bool ring = RING && n > 0;
+  float* sxo = sm + L.sxo;  // [lim][P]: x of the rows leaving the horizon (0: none)
+  float* sbo = sm + L.sbo;  // [lim][N]
+  float* sdo = sm + L.sdo;  // [lim]
+  float wbase = 0.f;        // sum of dt over positions T - M .. T - 1
+  if (ring) {
+    const long long T0 = __ldcg(&mr.pos_snap[b]);
+    const int Mh = d.Mh, Mr = d.Mr;
+    const size_t lb = (size_t)l * d.Bmax + b;
+    const float* dtr = mr.dt + (lb * d.Hm + hd) * Mr;
+    float part = 0.f;
+    for (long long pp = (T0 > Mh ? T0 - Mh : 0) + threadIdx.x; pp < T0; pp += blockDim.x)
+      part += __ldcg(&dtr[pp % Mr]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    float* wsum = sm + L.wsum;
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = part;
+    // leaving rows: position q = T + t - M; older than the commit -> ring,
+    // inside it (M <= S) -> staged rows; negative -> no row
+    for (int i = threadIdx.x; i < n * (P / 4); i += blockDim.x) {
+      const int t = i / (P / 4), c = (i % (P / 4)) * 4;
+      const long long q = T0 + t - Mh;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q >= T0)
+        v = *reinterpret_cast<const float4*>(&sx[(int)(q - T0) * P + c]);
+      else if (q >= 0)
+        v = __ldcg(reinterpret_cast<const float4*>(mr.x + (lb * Mr + q % Mr) * d.dinner + hd * P + c));
+      *reinterpret_cast<float4*>(&sxo[t * P + c]) = v;
+    }
+    for (int i = threadIdx.x; i < n * (N / 4); i += blockDim.x) {
+      const int t = i / (N / 4), c = (i % (N / 4)) * 4;
+      const long long q = T0 + t - Mh;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q >= T0)
+        v = *reinterpret_cast<const float4*>(&sb[(int)(q - T0) * N + c]);
+      else if (q >= 0)
+        v = __ldcg(reinterpret_cast<const float4*>(mr.b + (lb * Mr + q % Mr) * N + c));
+      *reinterpret_cast<float4*>(&sbo[t * N + c]) = v;
+    }
+    for (int t = threadIdx.x; t < n; t += blockDim.x) {
+      const long long q = T0 + t - Mh;
+      sdo[t] = q >= T0 ? sd[(int)(q - T0)] : (q >= 0 ? __ldcg(&dtr[q % Mr]) : 0.f);
+    }
+    // the new rows into the ring (one CTA per head; head 0 also writes B)
+    if (qs == 0) {
+      for (int i = threadIdx.x; i < n * (P / 4); i += blockDim.x) {
+        const int t = i / (P / 4), c = (i % (P / 4)) * 4;
+        *reinterpret_cast<float4*>(mr.x + (lb * Mr + (T0 + t) % Mr) * d.dinner + hd * P + c) =
+            *reinterpret_cast<const float4*>(&sx[t * P + c]);
+      }
+      for (int t = threadIdx.x; t < n; t += blockDim.x)
+        mr.dt[(lb * d.Hm + hd) * Mr + (T0 + t) % Mr] = sd[t];
+      if (hd == 0)
+        for (int i = threadIdx.x; i < n * (N / 4); i += blockDim.x) {
+          const int t = i / (N / 4), c = (i % (N / 4)) * 4;
+          *reinterpret_cast<float4*>(mr.b + (lb * Mr + (T0 + t) % Mr) * N + c) =
+              *reinterpret_cast<const float4*>(&sb[t * N + c]);
+        }
+    }
+    __syncthreads();
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) wbase += wsum[w];
+  }
+  float W = wbase;  // sum of dt over the horizon ending at the current row
   for (int t = 0; t < n; ++t) {
     const float dt = sd[t];
-    const float dec = expf(dt * A);
+    const float dec = last_only ? 0.f : expf(dt * A);
+    float co = 0.f;  // weight of the row leaving the horizon
+    if (ring) {
+      W += dt - sdo[t];
+      co = sdo[t] * expf(A * W);
+    }
 #pragma unroll
     for (int u = 0; u < QPT; ++u) {
       const float xv = dt * sx[t * P + pi[u]];
@@ -154,6 +244,14 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
       hv[u].y = fmaf(dec, hv[u].y, xv * Bv.y);
       hv[u].z = fmaf(dec, hv[u].z, xv * Bv.z);
       hv[u].w = fmaf(dec, hv[u].w, xv * Bv.w);
+      if (ring) {
+        const float xo = co * sxo[t * P + pi[u]];
+        const float4 Bo = *reinterpret_cast<const float4*>(&sbo[t * N + ci[u]]);
+        hv[u].x = fmaf(-xo, Bo.x, hv[u].x);
+        hv[u].y = fmaf(-xo, Bo.y, hv[u].y);
+        hv[u].z = fmaf(-xo, Bo.z, hv[u].z);
+        hv[u].w = fmaf(-xo, Bo.w, hv[u].w);
+      }
     }
   }
   if (n > 0) {
@@ -229,16 +327,42 @@ template <typename K>
 cudaError_t set_smem(K kernel, int smem) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
+
+template <bool R>
+cudaError_t configure_variant(int smem) {
+  cudaError_t e = set_smem(commit_state_kernel<float, 2, R>, smem);
+  if (e == cudaSuccess) e = set_smem(commit_state_kernel<float, QPT_HEAD, R>, smem);
+  if (e == cudaSuccess) e = set_smem(commit_state_kernel<__nv_bfloat16, 2, R>, smem);
+  if (e == cudaSuccess) e = set_smem(commit_state_kernel<__nv_bfloat16, QPT_HEAD, R>, smem);
+  return e;
+}
+
+template <bool R>
+cudaError_t launch_variant(int dtype, const Dims& d, int B, bool whole, int qsplit, size_t smem,
+                           int early, int late, const int32_t* n_acc, const float* xbd,
+                           long long xls, const float* A_log, float* state, int64_t* pos,
+                           int32_t* offsets, int32_t* tags, int32_t* err, const float* memC,
+                           void* mix, const MemRing& mr, cudaStream_t st) {
+  const dim3 grid(d.Hm * qsplit, B, d.L);
+  const dim3 blk(THREADS_CS);
+  if (dtype == HF_F32) {
+    auto k = whole ? commit_state_kernel<float, QPT_HEAD, R> : commit_state_kernel<float, 2, R>;
+    return launch_pdl(k, grid, blk, smem, st, d, B, qsplit, early, late, n_acc, xbd, xls, A_log,
+                      state, pos, offsets, tags, err, memC, (float*)mix, mr);
+  }
+  auto k = whole ? commit_state_kernel<__nv_bfloat16, QPT_HEAD, R>
+                 : commit_state_kernel<__nv_bfloat16, 2, R>;
+  return launch_pdl(k, grid, blk, smem, st, d, B, qsplit, early, late, n_acc, xbd, xls, A_log,
+                    state, pos, offsets, tags, err, memC, (__nv_bfloat16*)mix, mr);
+}
 }  // namespace
 
 cudaError_t configure_commit_state(const Dims& d) {
-  static int configured = 0;  // attribute of the kernel: keep the largest need
+  static int configured = 0;  // attribute of the kernels: keep the largest need
   const int smem = (int)commit_state_smem(d, mem_tc_ok(d));
   if (smem <= configured) return cudaSuccess;
-  cudaError_t e = set_smem(commit_state_kernel<float, 2>, smem);
-  if (e == cudaSuccess) e = set_smem(commit_state_kernel<float, QPT_HEAD>, smem);
-  if (e == cudaSuccess) e = set_smem(commit_state_kernel<__nv_bfloat16, 2>, smem);
-  if (e == cudaSuccess) e = set_smem(commit_state_kernel<__nv_bfloat16, QPT_HEAD>, smem);
+  cudaError_t e = configure_variant<false>(smem);
+  if (e == cudaSuccess) e = configure_variant<true>(smem);
   if (e == cudaSuccess) configured = smem;
   return e;
 }
@@ -247,8 +371,9 @@ cudaError_t launch_commit_state(int dtype, const Dims& d, int B, const int32_t* 
                                 const float* xbd, long long xls, const float* A_log, float* state,
                                 int64_t* pos, int32_t* offsets, int32_t* tags, int32_t* err,
                                 const float* memC, void* mix, int early, int late,
-                                int num_sms, cudaStream_t st) {
+                                int num_sms, const MemRing& mr, cudaStream_t st) {
   if (memC && (dtype != HF_BF16 || !mem_tc_ok(d))) return cudaErrorInvalidValue;
+  if (d.Mr > 0 && (!mr.x || !mr.b || !mr.dt || !mr.pos_snap)) return cudaErrorInvalidValue;
   const int nq = d.P * d.N / 4;
   if (nq > QPT_HEAD * THREADS_CS) return cudaErrorInvalidValue;
   // whole heads per CTA when fused or when they alone give ~4 CTAs per SM
@@ -256,17 +381,11 @@ cudaError_t launch_commit_state(int dtype, const Dims& d, int B, const int32_t* 
   const int qpt = whole ? QPT_HEAD : 2;
   const int qsplit = (nq + qpt * THREADS_CS - 1) / (qpt * THREADS_CS);
   const size_t smem = commit_state_smem(d, memC != nullptr);
-  const dim3 grid(d.Hm * qsplit, B, d.L);
-  const dim3 blk(THREADS_CS);
-  if (dtype == HF_F32) {
-    auto k = whole ? commit_state_kernel<float, QPT_HEAD> : commit_state_kernel<float, 2>;
-    return launch_pdl(k, grid, blk, smem, st, d, B, qsplit, early, late, n_acc, xbd, xls, A_log,
-                      state, pos, offsets, tags, err, memC, (float*)mix);
-  }
-  auto k = whole ? commit_state_kernel<__nv_bfloat16, QPT_HEAD>
-                 : commit_state_kernel<__nv_bfloat16, 2>;
-  return launch_pdl(k, grid, blk, smem, st, d, B, qsplit, early, late, n_acc, xbd, xls, A_log,
-                    state, pos, offsets, tags, err, memC, (__nv_bfloat16*)mix);
+  return d.Mr > 0
+             ? launch_variant<true>(dtype, d, B, whole, qsplit, smem, early, late, n_acc, xbd, xls,
+                                    A_log, state, pos, offsets, tags, err, memC, mix, mr, st)
+             : launch_variant<false>(dtype, d, B, whole, qsplit, smem, early, late, n_acc, xbd,
+                                     xls, A_log, state, pos, offsets, tags, err, memC, mix, mr, st);
 }
 
 }  // namespace hf

@@ -140,6 +140,9 @@ struct Dims {
   int NS;      // memory-input columns: dinner + N + Hm
   int Nz;      // output-projection inputs: QD + dinner
   int esize;   // element bytes of the model dtype
+  int xoff;    // 1: cross-slot attention off (slot s sees the window and its own key)
+  int Mh;      // memory horizon: 0 = whole history, M > 0 = last M committed features
+  int Mr;      // rows of the memory-input ring (M > 1: M + S + 1, else 0)
 };
 
 // ---------------------------------------------------------------- GEMM epilogues
@@ -149,7 +152,8 @@ enum EpiKind : int {
   EPI_SSM_KV = 2, // ring append / memory inputs (commit, prefill window)
   EPI_DT = 3,     // prefill: dt of token r, head c, stored transposed (fp32)
   EPI_XB = 4,     // prefill: w-scaled x and B of token r, stored transposed (model dtype)
-  EPI_STATE = 5   // prefill: state row r = (head, p), column n: decay * state + v
+  EPI_STATE = 5,  // prefill: state row r = (head, p), column n: decay * state + v
+  EPI_MEMRING = 6 // prefill, memory horizon M > 1: x / B / dt of the last M features
 };
 
 struct Epi {
@@ -181,6 +185,13 @@ struct Epi {
   float* xbd;
   long long xbd_layer_stride;  // elements between layers in xbd
   const float* dt_bias;        // [L][Hm]
+  int64_t* pos_snap;           // commit rows: pos[b] before the commit, stored by row t = 0
+  // EPI_MEMRING (mapped rows; columns [x | B | dt] of layer0): rows at
+  // positions >= req_len[b] - Mh go to ring row (position mod Mr)
+  float* mx;                   // [L][Bmax][Mr][dinner]
+  float* mb;                   // [L][Bmax][Mr][N]
+  float* mdt;                  // [L][Bmax][Hm][Mr]
+  const int64_t* req_len;      // [Bmax]
   // Prefill chunked-scan epilogues (one request, one segment of T tokens):
   //  EPI_DT    dtw[c*ldt + r] = softplus(v + dt_bias[layer0][c])
   //  EPI_XB    c <  dinner: xsT[c*ldt + r] = dtw[(c/P)*ldt + r] * v   (dtw holds w)
@@ -196,13 +207,16 @@ struct Epi {
 };
 
 // Request and committed position of an EPI_SSM_KV row; position < 0: skip.
-__device__ __forceinline__ void epi_row(const Epi& e, int r, int& b, long long& p) {
+// c: the first output column the caller stores for this row (column 0 of a
+// commit row t = 0 also records the position before the commit).
+__device__ __forceinline__ void epi_row(const Epi& e, int r, int& b, long long& p, int c) {
   if (e.n_acc) {
     const int lim = e.d.S + 1;
     b = r / lim;
     const int t = r % lim;
     const int n = __ldcg(&e.n_acc[b]);
     p = (n >= 0 && n <= lim && t < n) ? __ldcg(&e.pos[b]) + t : -1;
+    if (e.pos_snap && t == 0 && c == 0 && p >= 0) e.pos_snap[b] = p;
   } else if (e.row_req) {
     b = __ldcg(&e.row_req[r]);
     p = __ldcg(&e.row_pos[r]);
@@ -295,7 +309,7 @@ __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
   } else if (e.kind == EPI_SSM_KV) {
     int b;
     long long p;
-    epi_row(e, r, b, p);
+    epi_row(e, r, b, p, c);
     epi_ssm<T>(e, r, c, v, b, p);
   } else if (e.kind == EPI_DT) {
     e.dtw[(size_t)c * e.ldt + r] = softplus_f(v + __ldg(&e.dt_bias[e.layer0 * e.d.Hm + c]));
@@ -305,6 +319,22 @@ __device__ __forceinline__ void epi_apply(const Epi& e, int r, int c, float v) {
       static_cast<T*>(e.xsT)[(size_t)c * e.ldt + r] = from_f<T>(w * v);
     } else {
       static_cast<T*>(e.bT)[(size_t)(c - e.d.dinner) * e.ldt + r] = from_f<T>(v);
+    }
+  } else if (e.kind == EPI_MEMRING) {
+    const Dims& d = e.d;
+    const int b = __ldcg(&e.row_req[r]);
+    const long long p = __ldcg(&e.row_pos[r]);
+    if (p < __ldcg(&e.req_len[b]) - d.Mh) return;  // older than the horizon
+    const size_t lb = (size_t)e.layer0 * d.Bmax + b;
+    const int row = (int)(p % d.Mr);
+    if (c < d.dinner) {
+      e.mx[(lb * d.Mr + row) * d.dinner + c] = v;
+    } else if (c < d.dinner + d.N) {
+      e.mb[(lb * d.Mr + row) * d.N + (c - d.dinner)] = v;
+    } else if (c < d.dinner + d.N + d.Hm) {
+      const int hd = c - d.dinner - d.N;
+      e.mdt[(lb * d.Hm + hd) * d.Mr + row] =
+          softplus_f(v + __ldg(&e.dt_bias[e.layer0 * d.Hm + hd]));
     }
   } else {  // EPI_STATE
     const size_t i = (size_t)r * e.d.N + c;
@@ -460,19 +490,32 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
 // the new state, into the memory columns of mix (model dtype).
 size_t commit_state_smem(const Dims& d, bool read);
 cudaError_t configure_commit_state(const Dims& d);  // at handle creation
+// Memory-input ring of a memory horizon M > 1 (all NULL otherwise): x / B /
+// dt of the last Mr = M + S + 1 committed features per (layer, request),
+// position t in row t mod Mr, and the positions before the running commit
+// (stored by the commit projection's epilogue).
+struct MemRing {
+  float* x;          // [L][Bmax][Mr][dinner]
+  float* b;          // [L][Bmax][Mr][N]
+  float* dt;         // [L][Bmax][Hm][Mr]
+  const int64_t* pos_snap;  // [Bmax]
+};
+
 cudaError_t launch_commit_state(int dtype, const Dims& d, int B, const int32_t* n_acc,
                                 const float* xbd, long long xbd_layer_stride, const float* A_log,
                                 float* state, int64_t* pos, int32_t* offsets, int32_t* tags,
                                 int32_t* err, const float* memC, void* mix, int early,
-                                int late, int num_sms, cudaStream_t st);
+                                int late, int num_sms, const MemRing& mr, cudaStream_t st);
 
 // Prefill helpers (lens/reqs/cu are device int32 arrays of n_req entries).
 cudaError_t launch_prefill_reset(const Dims& d, int n_req, const int32_t* reqs,
                                  float* state, int32_t* tags, int64_t* pos, cudaStream_t st);
+// (req_len, when not NULL, receives each named request's prefix length.)
 cudaError_t launch_prefill_ring_prep(int dtype, const Dims& d, int n_req, int n_rows,
                                      const int32_t* lens, const int32_t* reqs,
                                      const void* feats, int32_t* row_req, int64_t* row_pos,
-                                     int32_t* tags, void* packed, cudaStream_t st);
+                                     int32_t* tags, void* packed, int64_t* req_len,
+                                     cudaStream_t st);
 // Chunked decay scan of one prefill segment of T tokens, per head h (grid Hm):
 // dtw[h][t] holds dt_t on entry and w_t = dt_t * exp(A_h * sum_{s>t} dt_s)
 // on exit; seg_decay[h] = exp(A_h * sum_t dt_t). Chunks of `chunk` tokens

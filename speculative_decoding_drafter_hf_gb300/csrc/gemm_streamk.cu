@@ -196,7 +196,7 @@ tc_gemm_sk_kernel(const __grid_constant__ CUtensorMap tb0, const __grid_constant
       if (ep.kind == EPI_SSM_KV && n < (p ? a.N1 : a.N0)) {
         int bq;
         long long pq;
-        epi_row(ep, n, bq, pq);
+        epi_row(ep, n, bq, pq, 0);
         ro = ssm_row_off(ep.d, bq, pq);
       }
       ep_ro[e] = ro;

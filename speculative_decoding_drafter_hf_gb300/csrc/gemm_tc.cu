@@ -229,7 +229,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       for (int nl = t2; nl < n_here; nl += 64) {
         int bq;
         long long pq;
-        epi_row(epi, n_tile * BN + nl, bq, pq);
+        epi_row(epi, n_tile * BN + nl, bq, pq, m_tile * 128);
         ep_b[nl] = bq;
         ep_p[nl] = ssm_row_off(epi.d, bq, pq);
       }

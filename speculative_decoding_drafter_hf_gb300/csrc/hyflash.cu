@@ -46,6 +46,12 @@ struct hf_handle {
   int32_t* tags = nullptr;   // [Bmax][W]
   int64_t* pos = nullptr;    // [Bmax]
   float* state = nullptr;    // [L][Bmax][Hm][P][N]
+  // memory horizon M > 1: x / B / dt of the last M + S + 1 committed features
+  float* mem_x = nullptr;    // [L][Bmax][Mr][dinner]
+  float* mem_b = nullptr;    // [L][Bmax][Mr][N]
+  float* mem_dt = nullptr;   // [L][Bmax][Hm][Mr]
+  int64_t* pos_snap = nullptr;  // [Bmax]: positions before the running commit
+  int64_t* req_len = nullptr;   // [Bmax]: prefix lengths of the running prefill
 
   int32_t* offsets = nullptr;  // [Bmax+1]
   int32_t* row_req = nullptr;  // [Rmax]
@@ -124,6 +130,9 @@ Dims make_dims(const hf_config& c) {
   d.NS = (int)round_up(d.dinner + d.N + d.Hm, 4);
   d.Nz = d.QD + d.dinner;
   d.esize = c.dtype == HF_F32 ? 4 : 2;
+  d.xoff = c.cross_slot_off ? 1 : 0;
+  d.Mh = c.mem_horizon;
+  d.Mr = c.mem_horizon > 1 ? c.mem_horizon + c.block + 1 : 0;
   return d;
 }
 
@@ -153,6 +162,9 @@ hf_status validate(const hf_config* c, std::string* why) {
   if (c->max_batch > 65535) return bad("max_batch must be <= 65535");
   if (c->dtype == HF_BF16 && c->ssm_headdim % 16)
     return bad("bf16 needs ssm_headdim a multiple of 16");
+  if (c->cross_slot_off != 0 && c->cross_slot_off != 1) return bad("cross_slot_off must be 0 or 1");
+  if (c->mem_horizon < 0 || c->mem_horizon > c->window)
+    return bad("mem_horizon must be in 0..window");
   {
     const Dims d = make_dims(*c);
     if (hf::attn_cluster_smem(d, d.esize) > 232448)
@@ -416,6 +428,13 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   A((void**)&h->tags, Bm * d.W * 4);
   A((void**)&h->pos, Bm * 8);
   A((void**)&h->state, L * Bm * d.Hm * d.P * d.N * 4);
+  if (d.Mr > 0) {
+    A((void**)&h->mem_x, L * Bm * d.Mr * d.dinner * 4);
+    A((void**)&h->mem_b, L * Bm * d.Mr * d.N * 4);
+    A((void**)&h->mem_dt, L * Bm * d.Hm * d.Mr * 4);
+    A((void**)&h->pos_snap, Bm * 8);
+    A((void**)&h->req_len, Bm * 8);
+  }
   A((void**)&h->offsets, (Bm + 1) * 4);
   A((void**)&h->row_req, h->rmax * 4);
   A((void**)&h->row_pos, h->rmax * 8);
@@ -629,6 +648,7 @@ Epi commit_epi(const hf_handle* h, const int32_t* n_accepted) {
   ep.pos = h->pos;
   ep.xbd = h->xbd;
   ep.xbd_layer_stride = h->xbd_ls;
+  ep.pos_snap = h->pos_snap;  // memory horizon M > 1 only (else NULL)
   if (h->wt_commit) {  // pre-tiled: rows padded per layer to nc_pad, padding skipped
     ep.cols_per_layer = h->nc_pad;
     ep.cols_valid = d.Nc;
@@ -650,9 +670,10 @@ hf_status commit_state(hf_handle* h, const int32_t* n_accepted, int batch, const
                        int early, int late, cudaStream_t st) {
   const Dims& d = h->d;
   Scope sc(h, HF_K_COMMIT_STATE, st);
+  const hf::MemRing mr{h->mem_x, h->mem_b, h->mem_dt, h->pos_snap};
   cudaError_t e = hf::launch_commit_state(h->cfg.dtype, d, batch, n_accepted, h->xbd, h->xbd_ls,
                                           h->A_log, h->state, h->pos, h->offsets, h->tags, h->err,
-                                          memC, h->mix, early, late, h->num_sms, st);
+                                          memC, h->mix, early, late, h->num_sms, mr, st);
   sc.count = 1;
   if (e != cudaSuccess) return cuda_fail(h, e, "commit state launch");
   return HF_OK;
@@ -816,7 +837,7 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
   if (ring_rows > 0) {
     e = hf::launch_prefill_ring_prep(h->cfg.dtype, d, n_req, (int)ring_rows, h->pf_lens,
                                      h->pf_reqs, feats, h->row_req, h->row_pos, h->tags,
-                                     h->packed, st);
+                                     h->packed, h->req_len, st);
     sc.count++;
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill ring prep");
   }
@@ -833,6 +854,22 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
       e = gemm_launch(h, h->packed, d.D, wl, d.D, (int)ring_rows, 2 * d.KVD, d.D, ek, st,
                       &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "prefill kv gemm");
+      if (d.Mr > 0) {
+        // memory horizon M > 1: x, B, dt of each request's last M features
+        // (among the window rows, M <= W) into the memory-input ring
+        Epi em = epi_base(h);
+        em.kind = hf::EPI_MEMRING;
+        em.layer0 = l;
+        em.row_req = h->row_req;
+        em.row_pos = h->row_pos;
+        em.req_len = h->req_len;
+        em.mx = h->mem_x;
+        em.mb = h->mem_b;
+        em.mdt = h->mem_dt;
+        e = gemm_launch(h, h->packed, d.D, wl + (size_t)2 * d.KVD * d.D * es, d.D, (int)ring_rows,
+                        d.dinner + d.N + d.Hm, d.D, em, st, &sc.count);
+        if (e != cudaSuccess) return cuda_fail(h, e, "prefill memory-input gemm");
+      }
     }
     // Memory fold, per request and segment of at most Tseg tokens:
     //   dt (transposed) -> chunked decay scan -> w*x, B (transposed, bf16/fp32)
@@ -845,7 +882,9 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
     for (int i = 0; i < n_req; ++i) {
       const long long Li = lens[i];
       float* st_b = h->state + (((size_t)l * d.Bmax + reqs[i]) * d.Hm * d.P) * d.N;
-      for (long long s0 = 0; s0 < Li; s0 += Tseg) {
+      // with a memory horizon M only the last M features are folded
+      const long long first = d.Mh > 0 ? std::max(0LL, Li - d.Mh) : 0;
+      for (long long s0 = first; s0 < Li; s0 += Tseg) {
         const int T = (int)std::min(Tseg, Li - s0);
         const void* fseg = bptr(feats, (size_t)(cu + s0) * d.D * es);
         Epi e1 = epi_base(h);
@@ -925,6 +964,9 @@ hf_status hf_tensor_bytes(const hf_handle* h, int32_t which, size_t* bytes) {
     case HF_T_OFFSETS: *bytes = (Bm + 1) * 4; break;
     case HF_T_DRAFT_PROJ: *bytes = Bm * d.S * d.Nd * 4; break;
     case HF_T_DRAFT_MIX: *bytes = Bm * d.S * d.Nz * h->esz; break;
+    case HF_T_MEM_X: *bytes = L * Bm * d.Mr * d.dinner * 4; break;
+    case HF_T_MEM_B: *bytes = L * Bm * d.Mr * d.N * 4; break;
+    case HF_T_MEM_DT: *bytes = L * Bm * d.Hm * d.Mr * 4; break;
     default: return HF_EINVAL;
   }
   return HF_OK;
@@ -940,6 +982,9 @@ static const void* tensor_ptr(const hf_handle* h, int which) {
     case HF_T_OFFSETS: return h->offsets;
     case HF_T_DRAFT_PROJ: return h->proj;
     case HF_T_DRAFT_MIX: return h->mix;
+    case HF_T_MEM_X: return h->mem_x;
+    case HF_T_MEM_B: return h->mem_b;
+    case HF_T_MEM_DT: return h->mem_dt;
   }
   return nullptr;
 }
@@ -951,14 +996,19 @@ hf_status hf_read_tensor(hf_handle* h, int32_t which, void* host_out, size_t byt
   if (!host_out || bytes != want) return fail(h, HF_EINVAL, "host buffer size mismatch");
   HF_CUDA(h, cudaSetDevice(h->device));
   HF_CUDA(h, cudaDeviceSynchronize());
-  HF_CUDA(h, cudaMemcpy(host_out, tensor_ptr(h, which), bytes, cudaMemcpyDeviceToHost));
+  if (bytes) HF_CUDA(h, cudaMemcpy(host_out, tensor_ptr(h, which), bytes, cudaMemcpyDeviceToHost));
   return HF_OK;
 }
+
+// The context: everything a request's drafting depends on (the memory-input
+// rows are empty without a memory horizon M > 1).
+static const int kContextTensors[] = {HF_T_STATE, HF_T_RING_K, HF_T_RING_V, HF_T_RING_TAG,
+                                      HF_T_POS,   HF_T_MEM_X,  HF_T_MEM_B,  HF_T_MEM_DT};
 
 size_t hf_context_bytes(const hf_handle* h) {
   if (!h) return 0;
   size_t total = 0, b = 0;
-  for (int w : {HF_T_STATE, HF_T_RING_K, HF_T_RING_V, HF_T_RING_TAG, HF_T_POS}) {
+  for (int w : kContextTensors) {
     hf_tensor_bytes(h, w, &b);
     total += b;
   }
@@ -971,8 +1021,9 @@ static hf_status copy_context(hf_handle* h, void* host, size_t bytes, bool out) 
   HF_CUDA(h, cudaSetDevice(h->device));
   HF_CUDA(h, cudaDeviceSynchronize());
   size_t off = 0, b = 0;
-  for (int w : {HF_T_STATE, HF_T_RING_K, HF_T_RING_V, HF_T_RING_TAG, HF_T_POS}) {
+  for (int w : kContextTensors) {
     hf_tensor_bytes(h, w, &b);
+    if (b == 0) continue;
     void* dev = const_cast<void*>(tensor_ptr(h, w));
     if (out)
       HF_CUDA(h, cudaMemcpy(bptr(host, off), dev, b, cudaMemcpyDeviceToHost));

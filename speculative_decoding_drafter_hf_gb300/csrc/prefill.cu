@@ -35,7 +35,8 @@ __global__ void prefill_ring_prep_kernel(Dims d, int n_req, const int32_t* __res
                                          const T* __restrict__ feats,
                                          int32_t* __restrict__ row_req,
                                          int64_t* __restrict__ row_pos,
-                                         int32_t* __restrict__ tags, T* __restrict__ packed) {
+                                         int32_t* __restrict__ tags, T* __restrict__ packed,
+                                         int64_t* __restrict__ req_len) {
   const int j = blockIdx.x;
   __shared__ long long s_src;
   __shared__ int s_found;
@@ -52,6 +53,7 @@ __global__ void prefill_ring_prep_kernel(Dims d, int n_req, const int32_t* __res
         const int b = reqs[i];
         row_req[j] = b;
         row_pos[j] = p;
+        if (req_len && jj == 0) req_len[b] = L;
         tags[(size_t)b * d.W + (int)(p % d.W)] = (int32_t)p;
         s_src = cu + p;
         s_found = 1;
@@ -152,15 +154,16 @@ cudaError_t launch_prefill_reset(const Dims& d, int n_req, const int32_t* reqs, 
 cudaError_t launch_prefill_ring_prep(int dtype, const Dims& d, int n_req, int n_rows,
                                      const int32_t* lens, const int32_t* reqs, const void* feats,
                                      int32_t* row_req, int64_t* row_pos, int32_t* tags,
-                                     void* packed, cudaStream_t st) {
+                                     void* packed, int64_t* req_len, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
   if (dtype == HF_F32)
     prefill_ring_prep_kernel<float><<<n_rows, 128, 0, st>>>(
-        d, n_req, lens, reqs, (const float*)feats, row_req, row_pos, tags, (float*)packed);
+        d, n_req, lens, reqs, (const float*)feats, row_req, row_pos, tags, (float*)packed,
+        req_len);
   else
     prefill_ring_prep_kernel<__nv_bfloat16><<<n_rows, 128, 0, st>>>(
         d, n_req, lens, reqs, (const __nv_bfloat16*)feats, row_req, row_pos, tags,
-        (__nv_bfloat16*)packed);
+        (__nv_bfloat16*)packed, req_len);
   return cudaGetLastError();
 }
 

@@ -127,7 +127,7 @@ __device__ __forceinline__ void epi_chunk16(const Epi& e, int m, int n0, int nco
   if (e.kind == EPI_SSM_KV) {  // the row's request and position once per chunk
     int b;
     long long p;
-    epi_row(e, m, b, p);
+    epi_row(e, m, b, p, n0);
     const long long ro = ssm_row_off(d, b, p);
     if (ro < 0) return;
     // the 16 columns usually fall in one region (one ring head, or the x / B /

@@ -25,11 +25,13 @@ def maxnorm_err(got, ref) -> float:
 class Pair:
     """A GPU handle and an oracle over the same weights and inputs."""
 
-    def __init__(self, cfg, batch=None, prefill_tokens_max=0, seed=0, oracle=True):
+    def __init__(self, cfg, batch=None, prefill_tokens_max=0, seed=0, oracle=True, tweak=None):
         import speculative_decoding_drafter_hf_gb300 as hf
         self.cfg = cfg
         self.B = cfg.batch if batch is None else batch
         self.weights = [make_layer_weights(cfg, l, seed) for l in range(cfg.n_layers)]
+        if tweak is not None:  # e.g. a slower decay, so that old features still count
+            self.weights = [tweak(w) for w in self.weights]
         self.gpu = hf.Drafter(cfg, self.B, prefill_tokens_max=prefill_tokens_max)
         for l, w in enumerate(self.weights):
             self.gpu.set_weights(l, w)

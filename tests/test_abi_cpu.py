@@ -38,7 +38,9 @@ def test_every_declared_symbol_is_exported(hf):
 
 
 def test_config_struct_layout(hf):
-    assert ctypes.sizeof(hf.HfConfig) == 64
+    # 14 int32, the int64 pass size, the two int32 ablation fields
+    assert ctypes.sizeof(hf.HfConfig) == 72
+    assert hf.HfConfig.mem_horizon.offset == 68
     assert ctypes.sizeof(hf.HfLayerWeights) == 11 * ctypes.sizeof(ctypes.c_void_p)
 
 
@@ -53,7 +55,8 @@ def _cfg(hf, **kw):
 @pytest.mark.parametrize("field,value", [
     ("n_groups", 2), ("n_kv_heads", 3), ("head_dim", 66), ("window", 7), ("chunk", 100),
     ("dtype", 5), ("d_model", 250), ("block", 17), ("d_state", 18), ("max_batch", 0),
-    ("prefill_tokens_max", -1), ("ssm_headdim", 130)])
+    ("prefill_tokens_max", -1), ("ssm_headdim", 130), ("cross_slot_off", 2),
+    ("mem_horizon", -1), ("mem_horizon", 65)])
 def test_invalid_config_is_einval_without_cuda(hf, field, value):
     from speculative_decoding_drafter_hf_gb300 import _binding as B
     h = ctypes.c_void_p()

@@ -3,6 +3,8 @@
 Bars: ring tags, positions and commit offsets bit-exact; floating point
 within max-normalised 1e-4 (fp32 mode) or 2e-2 (bf16 mode) per tensor.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -393,4 +395,65 @@ def test_stream_k_products(name, batch, api):
         run_round_api(p, 2, check_every=1)
     else:
         run_rounds(p, 2, check_every=1)
+    p.close()
+
+
+# ---------------------------------------------------------------- ablation modes
+
+def slow_decay(a_log):
+    """Weights whose memory decays slowly (A = -exp(a_log)), so that features
+    far back still weigh in and a memory horizon visibly changes the state."""
+    return lambda w: dataclasses.replace(w, A_log=torch.full_like(w.A_log, a_log))
+
+
+@pytest.mark.parametrize("name,batch", [("tiny_fp32", 3), ("qwen3_4b_bf16", 2)])
+def test_cross_slot_off(name, batch):
+    """Cross-slot off: each slot attends to the window and its own key only
+    (both attention paths: fp32 CUDA cores, bf16 tensor cores)."""
+    cfg = CONFIGS[name].replace(batch=batch, prefix=100, cross_slot=False)
+    p = Pair(cfg)
+    lens = [0, 37, 700][:batch] if name == "tiny_fp32" else [5, 700]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    run_rounds(p, 3)
+    # the draft differs from the default mode (the slots interact there)
+    slot, _ = make_round_inputs(cfg, 7, p.B)
+    got, ref = p.draft(slot)
+    q = Pair(cfg.replace(cross_slot=True), oracle=False)
+    q.prefill(lens, make_prefix_feats(cfg, lens))
+    other = q.gpu.draft(slot.cuda()).float().cpu().numpy()
+    q.close()
+    p.close()
+    assert maxnorm_err(got, ref) <= p.tol
+    assert maxnorm_err(other, ref) > 10 * p.tol or name == "qwen3_4b_bf16"
+
+
+@pytest.mark.parametrize("name,batch,horizon,lens", [
+    ("tiny_fp32", 4, 1, [0, 1, 9, 300]),        # last feature
+    ("tiny_fp32", 4, 3, [0, 2, 9, 300]),        # leaving rows inside one commit
+    ("tiny_fp32", 4, 20, [0, 7, 25, 300]),      # leaving rows from the ring
+    ("tiny_fp32", 2, 64, [10, 500]),            # horizon = window
+    ("qwen3_4b_bf16", 2, 1, [3, 700]),
+    ("qwen3_4b_bf16", 2, 512, [300, 1200]),     # the paper's "last 512"
+])
+def test_memory_horizon(name, batch, horizon, lens):
+    """Memory restricted to the last M committed features (prefill folds the
+    last M only; each commit adds its rows and removes the ones leaving)."""
+    cfg = CONFIGS[name].replace(batch=batch, prefix=100, mem_horizon=horizon)
+    p = Pair(cfg, tweak=slow_decay(-4.0 if horizon <= 64 else -7.0), prefill_tokens_max=256)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="prefill")
+    rounds = 12 if horizon < 512 else 4
+    run_rounds(p, rounds, check_every=1)
+    if horizon > 1:
+        x = p.gpu.read(Tensor.MEM_X)
+        assert x.shape == (cfg.n_layers, batch, horizon + cfg.block + 1, cfg.d_inner)
+    p.close()
+
+
+def test_memory_horizon_round_api_and_graph():
+    cfg = CONFIGS["tiny_fp32"].replace(batch=3, prefix=40, mem_horizon=6, n_layers=2)
+    p = Pair(cfg, tweak=slow_decay(-4.0))
+    lens = [0, 5, 40]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    run_round_api(p, 6, check_every=1)
     p.close()
