@@ -99,7 +99,11 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
     per step; later layers read their state again at draft time (their C
     depends on the layer below, which needs the updated state first).
     step_bytes is the fused figure: the least traffic any schedule of a
-    step needs."""
+    step needs.
+
+    Memory horizon M (ablation): M = 1 writes the state without reading it;
+    M > 1 also reads the leaving rows' and writes the new rows' x, B, dt
+    and reads M dt values per head for the horizon's decay sum."""
     e = cfg.elem_bytes
     D, hq, hkv, dh, W = cfg.d_model, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.window
     din, N, Hm, P, S, L = cfg.d_inner, cfg.d_state, cfg.ssm_heads, cfg.ssm_headdim, cfg.block, cfg.n_layers
@@ -118,12 +122,16 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
     io_mem = 4 * R * N + e * R * din                   # C in, memory read out
     commit_io = e * rows * D + L * rows * (2 * hkv * dh * e + (din + N + Hm) * 4)
     state_io = L * rows * (din + N + Hm) * 4
+    M = int(getattr(cfg, "mem_horizon", 0) or 0)
+    state_rw = 1 if M == 1 else 2                      # M = 1: the old state is not read
+    if M > 1:
+        state_io += L * (rows * 2 * (din + N + Hm) * 4 + batch * Hm * min(M, window_fill) * 4)
 
     def fused_fams():
         return {
             "round_proj": (w_commit + commit_io + w_draft + io_draft, 1),
             "draft_proj": ((L - 1) * (w_draft + io_draft), L - 1),
-            "commit_state": (L * 2 * state + state_io + io_mem, 1),
+            "commit_state": (L * state_rw * state + state_io + io_mem, 1),
             "attn_mem": (L * (window + io_attn) + (L - 1) * (state + io_mem), L),
             "out_proj": (L * (w_out + io_out), L),
         }
@@ -133,11 +141,21 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
         "attn_mem": (L * (window + state + io_attn + io_mem), L),
         "out_proj": (L * (w_out + io_out), L),
         "commit_proj": (w_commit + commit_io, 1),
-        "commit_state": (L * 2 * state + state_io, 1),
+        "commit_state": (L * state_rw * state + state_io, 1),
     }
     step = sum(b for b, _ in fused_fams().values())
     flops = L * 2 * R * D * (Nd + Nz) + 2 * rows * D * L * Nc
     return {"families": fam, "step_bytes": step, "step_flops": flops}
+
+
+def ablation_config(cfg) -> dict:
+    """The ablation modes in force, if any (config keys of the JSON line)."""
+    out = {}
+    if not getattr(cfg, "cross_slot", True):
+        out["cross_slot"] = "off (each slot sees the window and its own key)"
+    if getattr(cfg, "mem_horizon", 0):
+        out["mem_horizon"] = int(cfg.mem_horizon)
+    return {"ablation": out} if out else {}
 
 
 def kernel_sources_digest() -> str:
@@ -311,7 +329,7 @@ def run_reference(args, cfg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "committed_tokens_per_s": tok_rate,
         "config": {"workload": cfg.name, "batch": batch, "prefix": cfg.prefix,
-                   "layers": cfg.n_layers, "l2": "n/a (CPU)"},
+                   "layers": cfg.n_layers, "l2": "n/a (CPU)", **ablation_config(cfg)},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -651,7 +669,8 @@ def run_hyflash(args, cfg):
                        "l2": f"flushed between steps ({2 * l2 >> 20} MiB write, untimed)",
                        "timing": "CUDA graph of one round replayed per step; CUDA events; "
                                  "kernel-family times from a second pass with event nodes",
-                       "parallelism": f"replicas x{ws}"},
+                       "parallelism": f"replicas x{ws}",
+                       **ablation_config(cfg)},
             "committed_tokens_per_s": all_acc / (total_ms_max / 1e3),
             "step_ms_median": statistics.median(step_ms),
             "algorithmic": {"step_bytes": alg["step_bytes"],
@@ -690,11 +709,16 @@ def main(argv=None):
                     help="round configs: cap every request's prefix (0: the workload's own)")
     ap.add_argument("--chunk", type=int, default=128, help="prefill sweep: scan chunk")
     ap.add_argument("--layers", type=int, default=1, help="prefill sweep: drafter depth")
+    ap.add_argument("--cross-slot-off", action="store_true",
+                    help="ablation: mask attention among the draft slots")
+    ap.add_argument("--mem-horizon", type=int, default=0,
+                    help="ablation: memory of the last M committed features (0: all)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from workload import CONFIGS
-    cfg = CONFIGS[args.config]
+    cfg = CONFIGS[args.config].replace(cross_slot=not args.cross_slot_off,
+                                       mem_horizon=args.mem_horizon)
     if args.impl == "reference":
         return run_reference(args, cfg)
     if cfg.rounds == 0:

@@ -173,11 +173,14 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
   if (ring) {
     const long long T0 = __ldcg(&mr.pos_snap[b]);
     const int Mh = d.Mh, Mr = d.Mr;
+    const int r0 = (int)(T0 % Mr);  // ring row of position T0 (one 64-bit modulo)
+    // ring row of position T0 + k, -Mr <= k < Mr
+    auto row_of = [&](int k) { int r = r0 + k; r += r < 0 ? Mr : 0; return r >= Mr ? r - Mr : r; };
     const size_t lb = (size_t)l * d.Bmax + b;
     const float* dtr = mr.dt + (lb * d.Hm + hd) * Mr;
+    const int cnt = (int)(T0 < Mh ? T0 : Mh);  // positions T0 - cnt .. T0 - 1 in the horizon
     float part = 0.f;
-    for (long long pp = (T0 > Mh ? T0 - Mh : 0) + threadIdx.x; pp < T0; pp += blockDim.x)
-      part += __ldcg(&dtr[pp % Mr]);
+    for (int k = (int)threadIdx.x; k < cnt; k += blockDim.x) part += __ldcg(&dtr[row_of(k - cnt)]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     float* wsum = sm + L.wsum;
@@ -191,7 +194,7 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
       if (q >= T0)
         v = *reinterpret_cast<const float4*>(&sx[(int)(q - T0) * P + c]);
       else if (q >= 0)
-        v = __ldcg(reinterpret_cast<const float4*>(mr.x + (lb * Mr + q % Mr) * d.dinner + hd * P + c));
+        v = __ldcg(reinterpret_cast<const float4*>(mr.x + (lb * Mr + row_of(t - Mh)) * d.dinner + hd * P + c));
       *reinterpret_cast<float4*>(&sxo[t * P + c]) = v;
     }
     for (int i = threadIdx.x; i < n * (N / 4); i += blockDim.x) {
@@ -201,26 +204,26 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
       if (q >= T0)
         v = *reinterpret_cast<const float4*>(&sb[(int)(q - T0) * N + c]);
       else if (q >= 0)
-        v = __ldcg(reinterpret_cast<const float4*>(mr.b + (lb * Mr + q % Mr) * N + c));
+        v = __ldcg(reinterpret_cast<const float4*>(mr.b + (lb * Mr + row_of(t - Mh)) * N + c));
       *reinterpret_cast<float4*>(&sbo[t * N + c]) = v;
     }
     for (int t = threadIdx.x; t < n; t += blockDim.x) {
       const long long q = T0 + t - Mh;
-      sdo[t] = q >= T0 ? sd[(int)(q - T0)] : (q >= 0 ? __ldcg(&dtr[q % Mr]) : 0.f);
+      sdo[t] = q >= T0 ? sd[(int)(q - T0)] : (q >= 0 ? __ldcg(&dtr[row_of(t - Mh)]) : 0.f);
     }
     // the new rows into the ring (one CTA per head; head 0 also writes B)
     if (qs == 0) {
       for (int i = threadIdx.x; i < n * (P / 4); i += blockDim.x) {
         const int t = i / (P / 4), c = (i % (P / 4)) * 4;
-        *reinterpret_cast<float4*>(mr.x + (lb * Mr + (T0 + t) % Mr) * d.dinner + hd * P + c) =
+        *reinterpret_cast<float4*>(mr.x + (lb * Mr + row_of(t)) * d.dinner + hd * P + c) =
             *reinterpret_cast<const float4*>(&sx[t * P + c]);
       }
       for (int t = threadIdx.x; t < n; t += blockDim.x)
-        mr.dt[(lb * d.Hm + hd) * Mr + (T0 + t) % Mr] = sd[t];
+        mr.dt[(lb * d.Hm + hd) * Mr + row_of(t)] = sd[t];
       if (hd == 0)
         for (int i = threadIdx.x; i < n * (N / 4); i += blockDim.x) {
           const int t = i / (N / 4), c = (i % (N / 4)) * 4;
-          *reinterpret_cast<float4*>(mr.b + (lb * Mr + (T0 + t) % Mr) * N + c) =
+          *reinterpret_cast<float4*>(mr.b + (lb * Mr + row_of(t)) * N + c) =
               *reinterpret_cast<const float4*>(&sb[t * N + c]);
         }
     }

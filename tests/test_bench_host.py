@@ -71,6 +71,23 @@ def test_algorithmic_bytes_qwen_shape():
     assert all(n == 1 for k, (_, n) in fused["families"].items() if k != "draft_proj")
 
 
+def test_algorithmic_bytes_memory_horizon():
+    from workload import CONFIGS
+    cfg = CONFIGS["qwen3_4b_bf16"]
+    base = bench.algorithmic(cfg, 1, 512, 4.5, True)["families"]["commit_state"][0]
+    last = bench.algorithmic(cfg.replace(mem_horizon=1), 1, 512, 4.5, True)["families"]
+    ring = bench.algorithmic(cfg.replace(mem_horizon=512), 1, 512, 4.5, True)["families"]
+    state = 80 * 64 * 128 * 4
+    # last feature: the state is written, never read
+    assert base - last["commit_state"][0] == pytest.approx(state)
+    # horizon 512: leaving and new rows of x, B, dt, and 512 dt per head
+    extra = 4.5 * 2 * (5120 + 128 + 80) * 4 + 80 * 512 * 4
+    assert ring["commit_state"][0] - base == pytest.approx(extra)
+    assert bench.ablation_config(cfg) == {}
+    assert bench.ablation_config(cfg.replace(cross_slot=False, mem_horizon=1))["ablation"][
+        "mem_horizon"] == 1
+
+
 def test_clock_summary_parses_samples(tmp_path):
     c = bench.ClockSampler(0)
     c.path = str(tmp_path / "clk.csv")
