@@ -51,6 +51,21 @@ off by default, selected by two fields of the shape:
       min(pos, M) committed features, whatever came before them. M = 0 keeps
       the whole history.
 
+Gated-delta memory (the paper's memory-swap table "Mamba-2 / GDN-2", and the
+explainer's last paragraph: swapping Mamba-2 for Gated DeltaNet-2 gives
+comparable results). The pages do not define the variant; the gated delta
+rule is taken from its published paper (Yang, Kautz, Hatamizadeh, "Gated
+Delta Networks: Improving Mamba2 with Delta Rule"):
+      S_t = S_{t-1} (alpha_t (I - beta_t k_t k_t^T)) + beta_t v_t k_t^T,
+      o = S q,
+with S [P x N] per head (value x key). Readings:
+  R11 memory = "gdn": k_t = B_t / |B_t| (one group: shared by the heads),
+      v_t = x_t (the head's P values), alpha_t = exp(dt_t A) with dt and A
+      exactly as in the Mamba-2 memory (the paper's gate has this form),
+      beta_t = sigmoid(f_t W_beta) per head (a new projection), and the read
+      uses q = C_s / |C_s|; no memory horizon with this kind. Prefill is the
+      same rule applied token by token (committing the whole prefix).
+
 Parity pins (tests/test_oracle_pins.py): the chunked fold equals the
 token-by-token recurrence and the unrolled product closed form; constant decay
 matches scipy.signal.lfilter; A = 0 gives the plain sum, huge decay keeps only
@@ -105,11 +120,13 @@ class Weights64:
     w_mo: np.ndarray
     dt_bias: np.ndarray
     A_log: np.ndarray
+    w_beta: Optional[np.ndarray] = None   # gated-delta memory only
 
     @staticmethod
     def from_any(w) -> "Weights64":
         names = [f.name for f in dataclasses.fields(Weights64)]
-        return Weights64(**{n: to64(getattr(w, n)) for n in names})
+        vals = {n: getattr(w, n, None) for n in names}
+        return Weights64(**{n: (None if v is None else to64(v)) for n, v in vals.items()})
 
     @property
     def A(self) -> np.ndarray:
@@ -166,6 +183,47 @@ def ssm_fold_chunked(h: np.ndarray, x, B, dt, A, chunk: int) -> np.ndarray:
 def ssm_read(h: np.ndarray, C: np.ndarray) -> np.ndarray:
     """y[s, hd, p] = sum_n h[hd, p, n] C[s, n] (draft-time read, state untouched)."""
     return np.einsum("hpn,sn->shp", h, C)
+
+
+# --------------------------------------------------------------------------
+# gated-delta memory (R11)
+
+
+def memory_kind(cfg) -> str:
+    return str(getattr(cfg, "memory", "mamba2") or "mamba2")
+
+
+def sigmoid(x):
+    x = np.asarray(x, dtype=np.float64)
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def gdn_inputs(lw: Weights64, cfg, feats: np.ndarray):
+    """v = x [T,Hm,P], unit keys k [T,N], alpha [T,Hm], beta [T,Hm] (R11)."""
+    x, B, dt = ssm_inputs(lw, cfg, feats)
+    k = B / np.linalg.norm(B, axis=1, keepdims=True)
+    alpha = np.exp(dt * lw.A[None, :])
+    beta = sigmoid(feats @ lw.w_beta)
+    return x, k, alpha, beta
+
+
+def gdn_fold_recurrent(S: np.ndarray, v, k, alpha, beta) -> np.ndarray:
+    """Token by token, per head: S <- S (alpha (I - beta k k^T)) + beta v k^T."""
+    S = np.array(S, dtype=np.float64, copy=True)
+    N = S.shape[2]
+    eye = np.eye(N)
+    for t in range(v.shape[0]):
+        for hd in range(S.shape[0]):
+            kk = k[t][:, None]
+            S[hd] = S[hd] @ (alpha[t, hd] * (eye - beta[t, hd] * (kk @ kk.T))) \
+                + beta[t, hd] * np.outer(v[t, hd], k[t])
+    return S
+
+
+def gdn_read(S: np.ndarray, C: np.ndarray) -> np.ndarray:
+    """y[s, hd, p] = (S_hd q_s)[p] with q_s = C_s / |C_s| (R11)."""
+    q = C / np.linalg.norm(C, axis=1, keepdims=True)
+    return np.einsum("hpn,sn->shp", S, q)
 
 
 # --------------------------------------------------------------------------
@@ -236,6 +294,13 @@ def prefill_layer(lw: Weights64, cfg, feats: np.ndarray,
     L = feats.shape[0]
     if L == 0:
         return ctx
+    if memory_kind(cfg) == "gdn":  # R11: the delta rule over the whole prefix
+        ctx.h = gdn_fold_recurrent(ctx.h, *gdn_inputs(lw, cfg, feats))
+        first = max(0, L - cfg.window)
+        k, v = kv_of(lw, cfg, feats[first:])
+        ring_append(ctx, cfg, k, v, first)
+        ctx.pos = L
+        return ctx
     x, B, dt = ssm_inputs(lw, cfg, feats)
     M = mem_horizon(cfg)
     if M > 0:  # R10: only the last M features are remembered
@@ -261,6 +326,10 @@ def commit_layer(lw: Weights64, cfg, ctx: Context, feats_rows: np.ndarray,
     f = feats_rows[:n]
     k, v = kv_of(lw, cfg, f)
     ring_append(out, cfg, k, v, out.pos)
+    if memory_kind(cfg) == "gdn":  # R11
+        out.h = gdn_fold_recurrent(out.h, *gdn_inputs(lw, cfg, f))
+        out.pos += n
+        return out
     x, B, dt = ssm_inputs(lw, cfg, f)
     M = mem_horizon(cfg)
     if M > 0:
@@ -318,7 +387,7 @@ def draft_layer(lw: Weights64, cfg, ctx: Context, X: np.ndarray,
     Vs = (X @ lw.w_v).reshape(S, cfg.n_kv_heads, cfg.head_dim)
     Cs = X @ lw.w_C
     O = window_block_attention(cfg, ctx, Q, Ks, Vs)
-    y = ssm_read(ctx.h, Cs)
+    y = gdn_read(ctx.h, Cs) if memory_kind(cfg) == "gdn" else ssm_read(ctx.h, Cs)
     out = X + O.reshape(S, -1) @ lw.w_o + y.reshape(S, -1) @ lw.w_mo
     if return_parts:
         return out, dict(Q=Q, Ks=Ks, Vs=Vs, Cs=Cs, O=O, y=y)

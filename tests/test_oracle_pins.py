@@ -445,3 +445,96 @@ def test_memory_horizon_commits_equal_prefill_of_last_m():
         used += n
         ref = O.prefill_layer(lw, small_cfg(), feats[max(0, used - 6):used], method="recurrent")
         assert rel(ctx.h, ref.h) < 1e-12
+
+
+# ---------------------------------------------------------------- gated-delta memory
+# (gated delta rule of "Gated Delta Networks: Improving Mamba2 with Delta Rule";
+# the paper's memory-swap table)
+
+def test_gdn_delta_rule_retrieves_last_write_per_key():
+    # alpha = 1, beta = 1 and orthonormal keys: S e_i is the last value
+    # written at key i, and unwritten keys read zero
+    Hm, P, N, T = 2, 3, 5, 9
+    rng = np.random.default_rng(40)
+    keys = rng.integers(0, 4, size=T)            # key 4 never written
+    k = np.eye(N)[keys]
+    v = rng.standard_normal((T, Hm, P))
+    S = O.gdn_fold_recurrent(np.zeros((Hm, P, N)), v, k, np.ones((T, Hm)), np.ones((T, Hm)))
+    for i in range(N):
+        last = [t for t in range(T) if keys[t] == i]
+        want = v[last[-1]] if last else np.zeros((Hm, P))
+        assert np.allclose(S[:, :, i], want, rtol=0, atol=1e-14)
+
+
+def test_gdn_zero_gate_keeps_only_the_last_token():
+    Hm, P, N, T = 2, 3, 4, 6
+    rng = np.random.default_rng(41)
+    k = rng.standard_normal((T, N))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    v = rng.standard_normal((T, Hm, P))
+    beta = rng.uniform(0.1, 0.9, (T, Hm))
+    S = O.gdn_fold_recurrent(rng.standard_normal((Hm, P, N)), v, k, np.zeros((T, Hm)), beta)
+    want = beta[-1][:, None, None] * v[-1][:, :, None] * k[-1][None, None, :]
+    assert rel(S, want) < 1e-15
+
+
+def test_gdn_zero_beta_is_pure_decay():
+    Hm, P, N, T = 2, 3, 4, 5
+    rng = np.random.default_rng(42)
+    k = rng.standard_normal((T, N))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    alpha = rng.uniform(0.5, 1.0, (T, Hm))
+    S0 = rng.standard_normal((Hm, P, N))
+    S = O.gdn_fold_recurrent(S0, rng.standard_normal((T, Hm, P)), k, alpha, np.zeros((T, Hm)))
+    assert rel(S, np.prod(alpha, axis=0)[:, None, None] * S0) < 1e-14
+
+
+def test_gdn_rank_one_scalar_loops():
+    # the update written element by element: S[p,n] <- a (S[p,n] - b (S k)[p] k[n]) + b v[p] k[n]
+    Hm, P, N, T = 1, 2, 3, 4
+    rng = np.random.default_rng(43)
+    k = rng.standard_normal((T, N))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    v = rng.standard_normal((T, Hm, P))
+    a = rng.uniform(0.3, 1.0, (T, Hm))
+    b = rng.uniform(0.0, 1.0, (T, Hm))
+    S0 = rng.standard_normal((Hm, P, N))
+    want = S0[0].tolist()
+    for t in range(T):
+        sk = [sum(want[p][m] * k[t, m] for m in range(N)) for p in range(P)]
+        want = [[a[t, 0] * (want[p][n] - b[t, 0] * sk[p] * k[t, n]) + b[t, 0] * v[t, 0, p] * k[t, n]
+                 for n in range(N)] for p in range(P)]
+    got = O.gdn_fold_recurrent(S0, v, k, a, b)
+    assert rel(got[0], np.array(want)) < 1e-13
+
+
+def test_gdn_inputs_and_read():
+    cfg = small_cfg(memory="gdn")
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(44)
+    f = rng.standard_normal((5, cfg.d_model))
+    v, k, alpha, beta = O.gdn_inputs(lw, cfg, f)
+    assert np.allclose(np.linalg.norm(k, axis=1), 1.0, rtol=0, atol=1e-14)
+    ref_beta = torch.sigmoid(torch.tensor(f) @ torch.tensor(lw.w_beta)).numpy()
+    assert rel(beta, ref_beta) < 1e-14
+    assert np.all(alpha > 0) and np.all(alpha < 1)
+    S = rng.standard_normal((cfg.ssm_heads, cfg.ssm_headdim, cfg.d_state))
+    C = rng.standard_normal((7, cfg.d_state))
+    y = O.gdn_read(S, C)
+    assert rel(O.gdn_read(S, 3.5 * C), y) < 1e-15          # scale of the query drops out
+    qt = torch.nn.functional.normalize(torch.tensor(C), dim=1)
+    assert rel(y, torch.einsum("hpn,sn->shp", torch.tensor(S), qt).numpy()) < 1e-14
+
+
+def test_gdn_prefill_equals_commits():
+    cfg = small_cfg(memory="gdn")
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    rng = np.random.default_rng(45)
+    pre = rng.standard_normal((9, cfg.d_model))
+    rows = rng.standard_normal((8, cfg.d_model))
+    a = O.commit_layer(lw, cfg, O.commit_layer(lw, cfg, O.prefill_layer(lw, cfg, pre), rows, 3),
+                       rows[3:], 5)
+    b = O.prefill_layer(lw, cfg, np.concatenate([pre, rows]))
+    assert rel(a.h, b.h) < 1e-12 and np.array_equal(a.tag, b.tag)
+    z = O.commit_layer(lw, cfg, a, rows, 0)
+    assert np.array_equal(z.h, a.h)

@@ -53,6 +53,9 @@ class DrafterShape:
     # restricted to the last mem_horizon committed features (0: all of them)
     cross_slot: bool = True
     mem_horizon: int = 0
+    # memory kind: "mamba2" (the pages' memory) or "gdn" (gated delta rule,
+    # the paper's Gated DeltaNet-2 swap)
+    memory: str = "mamba2"
 
     @property
     def d_inner(self) -> int:
@@ -124,9 +127,10 @@ class LayerWeightsT:
     w_mo: torch.Tensor
     dt_bias: torch.Tensor
     A_log: torch.Tensor
+    w_beta: torch.Tensor = None   # gated-delta memory only: writing strength projection [D, Hm]
 
     FIELDS = ("w_q", "w_k", "w_v", "w_o", "w_x", "w_B", "w_C", "w_dt", "w_mo",
-              "dt_bias", "A_log")
+              "dt_bias", "A_log", "w_beta")
 
 
 def make_layer_weights(cfg: DrafterShape, layer: int, seed: int = 0) -> LayerWeightsT:
@@ -149,6 +153,7 @@ def make_layer_weights(cfg: DrafterShape, layer: int, seed: int = 0) -> LayerWei
         w_mo=n((din, D), 0.02),
         dt_bias=torch.full((Hm,), -2.0, dtype=torch.float32),
         A_log=torch.rand((Hm,), generator=g, dtype=torch.float32),
+        w_beta=n((D, Hm), 1.0 / math.sqrt(D)),   # drawn last: earlier draws unchanged
     )
 
 
