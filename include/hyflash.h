@@ -107,12 +107,23 @@ typedef struct {
    *     that leave the horizon. */
   int32_t cross_slot_off;
   int32_t mem_horizon;
+  /* Memory kind: HF_MEM_MAMBA2 (the pages' Mamba-2 memory) or
+   * HF_MEM_GATED_DELTA (the paper's swap to Gated DeltaNet-2, memory-swap
+   * table): per head S <- S (alpha (I - beta k k^T)) + beta v k^T with unit
+   * keys k = B/|B|, values x, alpha = exp(dt A) as in Mamba-2, beta =
+   * sigmoid(f W_beta), and the draft-time read y = S C/|C| (the gated delta
+   * rule of "Gated Delta Networks: Improving Mamba2 with Delta Rule").
+   * Needs w_beta; no memory horizon. */
+  int32_t memory_kind;
 } hf_config;
+
+enum { HF_MEM_MAMBA2 = 0, HF_MEM_GATED_DELTA = 1 };
 
 /* One layer's weights, HOST pointers, row-major [in, out] in the handle's
  * dtype (dt_bias, A_log: fp32 [ssm_heads]). Shapes:
  *   w_q [D, Hq*dh]  w_k, w_v [D, Hkv*dh]  w_o [Hq*dh, D]
- *   w_x [D, Hm*P]   w_B, w_C [D, N]       w_dt [D, Hm]   w_mo [Hm*P, D] */
+ *   w_x [D, Hm*P]   w_B, w_C [D, N]       w_dt [D, Hm]   w_mo [Hm*P, D]
+ *   w_beta [D, Hm] (gated-delta memory only) */
 typedef struct {
   const void* w_q;
   const void* w_k;
@@ -125,6 +136,7 @@ typedef struct {
   const void* w_mo;
   const float* dt_bias;
   const float* A_log;
+  const void* w_beta;  /* [D, Hm]: gated-delta writing strength (NULL otherwise) */
 } hf_layer_weights;
 
 /* Create a handle on CUDA device `device`: validates cfg (HF_EINVAL before

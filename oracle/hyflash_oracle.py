@@ -213,10 +213,9 @@ def gdn_fold_recurrent(S: np.ndarray, v, k, alpha, beta) -> np.ndarray:
     N = S.shape[2]
     eye = np.eye(N)
     for t in range(v.shape[0]):
-        for hd in range(S.shape[0]):
-            kk = k[t][:, None]
-            S[hd] = S[hd] @ (alpha[t, hd] * (eye - beta[t, hd] * (kk @ kk.T))) \
-                + beta[t, hd] * np.outer(v[t, hd], k[t])
+        kk = np.outer(k[t], k[t])                                   # k k^T
+        trans = alpha[t][:, None, None] * (eye[None] - beta[t][:, None, None] * kk[None])
+        S = S @ trans + beta[t][:, None, None] * (v[t][:, :, None] * k[t][None, None, :])
     return S
 
 

@@ -67,11 +67,13 @@ class HfConfig(ctypes.Structure):
         "ssm_heads", "ssm_headdim", "d_state", "n_groups", "n_layers",
         "max_batch", "chunk", "dtype")] + [("prefill_tokens_max", ctypes.c_int64),
                                            ("cross_slot_off", ctypes.c_int32),
-                                           ("mem_horizon", ctypes.c_int32)]
+                                           ("mem_horizon", ctypes.c_int32),
+                                           ("memory_kind", ctypes.c_int32)]
 
 
 WEIGHT_FIELDS = ("w_q", "w_k", "w_v", "w_o", "w_x", "w_B", "w_C", "w_dt", "w_mo",
-                 "dt_bias", "A_log")
+                 "dt_bias", "A_log", "w_beta")
+MEMORY_KINDS = {"mamba2": 0, "gdn": 1}
 
 
 class HfLayerWeights(ctypes.Structure):
@@ -137,7 +139,8 @@ def make_config(shape, max_batch: int, prefill_tokens_max: int = 0) -> HfConfig:
         dtype=HF_F32 if shape.dtype in ("f32", "fp32", "float32") else HF_BF16,
         prefill_tokens_max=prefill_tokens_max,
         cross_slot_off=0 if getattr(shape, "cross_slot", True) else 1,
-        mem_horizon=int(getattr(shape, "mem_horizon", 0) or 0))
+        mem_horizon=int(getattr(shape, "mem_horizon", 0) or 0),
+        memory_kind=MEMORY_KINDS[getattr(shape, "memory", "mamba2") or "mamba2"])
 
 
 def _stream_ptr(stream) -> Optional[int]:
@@ -202,7 +205,9 @@ class Drafter:
         keep = []
         lw = HfLayerWeights()
         for name in WEIGHT_FIELDS:
-            t = getattr(w, name)
+            t = getattr(w, name, None)
+            if t is None:  # optional (w_beta outside the gated-delta memory)
+                continue
             want = torch.float32 if name in ("dt_bias", "A_log") else self.torch_dtype
             t = t.detach().to("cpu", want).contiguous()
             keep.append(t)

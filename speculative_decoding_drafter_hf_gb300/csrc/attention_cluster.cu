@@ -92,7 +92,7 @@ __host__ __device__ inline Layout make_layout(const Dims& d, const Plan& p, int 
   m.ml = off;
   off += (size_t)R * 2 * 4;
   off = (off + 15) & ~(size_t)15;
-  const size_t mem_need = (size_t)d.S * d.N * 4;
+  const size_t mem_need = (size_t)d.S * d.N * 4 + 16 * 4;  // C rows, 1/|C_s| (gated delta)
   m.total = off > mem_need ? off : mem_need;
   return m;
 }
@@ -420,6 +420,12 @@ __device__ __forceinline__ void mem_head(const Args& a, uint8_t* sm, int b, int 
   const float* hb = a.state + (((size_t)b * d.Hm + hd) * P) * N;
   T* mix = static_cast<T*>(a.mix);
   const int cC = d.QD + 2 * d.KVD;
+  float* qn = cs + (size_t)S * N;  // gated delta: 1/|C_s|
+  if (d.gdn) {
+    __syncthreads();  // qn of the previous head fully consumed
+    slot_inv_norms(a.proj + (size_t)b * S * d.Nd + cC, d.Nd, S, N, qn);
+    __syncthreads();
+  }
   if (N == 128 && S <= 8) {
     // lane l owns state columns 4l..4l+3; a warp takes 4 state rows at a time
     // and all slots: 4 x 8 partial dots per lane, one reduce-scatter.
@@ -445,7 +451,8 @@ __device__ __forceinline__ void mem_head(const Args& a, uint8_t* sm, int b, int 
       const float tot = reduce_scatter32(v, lane);
       const int rr = lane / 8, sl = lane % 8, pr = p0 + rr;
       if (sl < S && pr < P)
-        mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)hd * P + pr] = from_f<T>(tot);
+        mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)hd * P + pr] =
+            from_f<T>(d.gdn ? tot * qn[sl] : tot);
     }
     return;
   }
@@ -478,7 +485,8 @@ __device__ __forceinline__ void mem_head(const Args& a, uint8_t* sm, int b, int 
       float acc = hv[u].x * c.x + hv[u].y * c.y + hv[u].z * c.z + hv[u].w * c.w;
       for (int o = gsz / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if ((qi & (gsz - 1)) == 0 && qi < nq)
-        mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)hd * P + pr] = from_f<T>(acc);
+        mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)hd * P + pr] =
+            from_f<T>(d.gdn ? acc * qn[sl] : acc);
     }
   }
 }
@@ -571,7 +579,7 @@ __host__ __device__ inline TcLayout make_tc_layout(const Dims& d) {
   off = (off + 7) & ~(size_t)7;
   m.bar = off;
   off += TC_STAGES * 8;
-  size_t mem_need = (size_t)d.S * d.N * 4;
+  size_t mem_need = (size_t)d.S * d.N * 4 + 16 * 4;  // C rows, 1/|C_s| (gated delta)
   if (mem_tc_ok(d)) {
     const size_t t = mem_tc_bytes(d);
     if (t > mem_need) mem_need = t;
@@ -1073,6 +1081,8 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
       bf[j][3] = to_tf32(c.w);
     }
   }
+  float* qn = red + (size_t)KSPL * P * 8;  // gated delta: 1/|C_s|
+  if (d.gdn) slot_inv_norms(a.proj + (size_t)b * S * d.Nd + d.QD + 2 * d.KVD, d.Nd, S, N, qn);
   __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
   for (int i = 0; i < nh; ++i) {
     if (active) {
@@ -1096,6 +1106,7 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
       const int sl = e / P, p = e % P;
       float y = 0.f;
       for (int q = 0; q < KSPL; ++q) y += red[((size_t)q * P + p) * 8 + sl];
+      if (d.gdn) y *= qn[sl];
       mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)(hd0 + i) * P + p] = __float2bfloat16_rn(y);
     }
     __syncthreads();  // partial sums read before the next head overwrites them

@@ -20,7 +20,7 @@ constexpr int QPT_HEAD = 8;  // float4 elements per thread when one CTA holds a 
 // when the memory read is fused), then the padded copy of the new state and
 // the k-part sums of the memory read.
 struct CsLayout {
-  size_t sx, sb, sd, sxo, sbo, sdo, wsum, rows, red, total;  // float offsets
+  size_t sx, sb, sd, sbeta, sxo, sbo, sdo, wsum, rows, red, qn, total;  // float offsets
 };
 __host__ __device__ inline CsLayout cs_layout(const Dims& d, bool read) {
   CsLayout m{};
@@ -28,15 +28,103 @@ __host__ __device__ inline CsLayout cs_layout(const Dims& d, bool read) {
   m.sx = 0;
   m.sb = m.sx + (size_t)lim * d.P;
   m.sd = m.sb + (size_t)lim * d.N;
-  m.sxo = m.sd + ((lim + 3) & ~3);
+  m.sbeta = m.sd + ((lim + 3) & ~3);  // gated delta: writing strengths
+  m.sxo = m.sbeta + (d.gdn ? (size_t)((lim + 3) & ~3) : 0);
   // memory horizon M > 1: the rows leaving the horizon, and a reduction slot
   m.sbo = m.sxo + (d.Mr > 0 ? (size_t)lim * d.P : 0);
   m.sdo = m.sbo + (d.Mr > 0 ? (size_t)lim * d.N : 0);
   m.wsum = m.sdo + (d.Mr > 0 ? (size_t)((lim + 3) & ~3) : 0);
   m.rows = m.wsum + (d.Mr > 0 ? 32 : 0);
   m.red = m.rows + (read ? (size_t)d.P * (d.N + 8) : 0);
-  m.total = m.red + (read ? (size_t)mem_ksplit(d) * d.P * 8 : 0);
+  m.qn = m.red + (read ? (size_t)mem_ksplit(d) * d.P * 8 : 0);
+  m.total = m.qn + (read ? 16 : 0);  // gated delta: 1/|C_s| of the slots
   return m;
+}
+
+// One gated-delta row applied to a thread's QPT float4 of a head's state
+// (state rows of gsz consecutive lanes; k4: this lane's 4 columns of B, not
+// yet normalised): S <- al (S - be (S k) k^T) + be x k^T, k = B/|B|, written
+// as S <- al S + be (x - al (S k)) k^T.
+template <int QPT>
+__device__ __forceinline__ void gdn_token(float4 (&hv)[QPT], const float (&xv)[QPT], float4 k4,
+                                          float al, float be, int gsz) {
+  float ss = k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w;
+  for (int o = 1; o < gsz; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float kn = 1.f / sqrtf(ss);
+  k4 = make_float4(k4.x * kn, k4.y * kn, k4.z * kn, k4.w * kn);
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {
+    float dot = hv[u].x * k4.x + hv[u].y * k4.y + hv[u].z * k4.z + hv[u].w * k4.w;
+    for (int o = 1; o < gsz; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    const float cf = be * (xv[u] - al * dot);
+    hv[u].x = fmaf(al, hv[u].x, cf * k4.x);
+    hv[u].y = fmaf(al, hv[u].y, cf * k4.y);
+    hv[u].z = fmaf(al, hv[u].z, cf * k4.z);
+    hv[u].w = fmaf(al, hv[u].w, cf * k4.w);
+  }
+}
+
+constexpr int QPT_SCAN = 2;
+
+// Gated-delta prefill of one request and layer over T tokens, whose x | B |
+// dt | beta rows (stride NS) the projection left in xs: grid (Hm * qsplit),
+// CTA (h * qsplit + q) keeps its slice of head h's state in registers and
+// applies the tokens in order; the next token's inputs are loaded while the
+// current one is applied.
+__global__ void __launch_bounds__(THREADS_CS)
+gdn_prefill_kernel(Dims d, int l, int b, int T, int qsplit, const float* __restrict__ xs,
+                   const float* __restrict__ A_log, float* __restrict__ state) {
+  const int hd = blockIdx.x / qsplit, qs = blockIdx.x % qsplit;
+  const int P = d.P, N = d.N, nq = P * N / 4;
+  float4* h = reinterpret_cast<float4*>(state + ((((size_t)l * d.Bmax + b) * d.Hm + hd) * P) * N);
+  const int q0 = qs * QPT_SCAN * THREADS_CS;
+  float4 hv[QPT_SCAN];
+  int pi[QPT_SCAN];
+  int ci = 0;
+#pragma unroll
+  for (int u = 0; u < QPT_SCAN; ++u) {  // elements past the head: index 0, never stored
+    const int q = q0 + threadIdx.x + u * THREADS_CS;
+    const bool in = q < nq;
+    hv[u] = in ? __ldcg(&h[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    pi[u] = in ? (q * 4) / N : 0;
+    if (u == 0) ci = in ? (q * 4) % N : 0;
+  }
+  const float A = -expf(__ldg(&A_log[l * d.Hm + hd]));
+  const int gsz = N / 4;
+  const size_t cx = (size_t)hd * P, cb = d.dinner, cd = (size_t)d.dinner + N + hd,
+               cbe = (size_t)d.dinner + N + d.Hm + hd;
+  float xv[QPT_SCAN], dt = 0.f, be = 0.f;
+  float4 kb = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (T > 0) {
+#pragma unroll
+    for (int u = 0; u < QPT_SCAN; ++u) xv[u] = __ldcg(&xs[cx + pi[u]]);
+    kb = __ldcg(reinterpret_cast<const float4*>(xs + cb + ci));
+    dt = __ldcg(&xs[cd]);
+    be = __ldcg(&xs[cbe]);
+  }
+  for (int t = 0; t < T; ++t) {
+    float xn[QPT_SCAN], dn = 0.f, bn = 0.f;
+    float4 kn = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t + 1 < T) {
+      const float* row = xs + (size_t)(t + 1) * d.NS;
+#pragma unroll
+      for (int u = 0; u < QPT_SCAN; ++u) xn[u] = __ldcg(&row[cx + pi[u]]);
+      kn = __ldcg(reinterpret_cast<const float4*>(row + cb + ci));
+      dn = __ldcg(&row[cd]);
+      bn = __ldcg(&row[cbe]);
+    }
+    gdn_token<QPT_SCAN>(hv, xv, kb, expf(dt * A), be, gsz);
+#pragma unroll
+    for (int u = 0; u < QPT_SCAN; ++u) xv[u] = xn[u];
+    kb = kn;
+    dt = dn;
+    be = bn;
+  }
+#pragma unroll
+  for (int u = 0; u < QPT_SCAN; ++u) {
+    const int q = q0 + threadIdx.x + u * THREADS_CS;
+    if (q < nq) h[q] = hv[u];
+  }
 }
 
 // grid (Hm * qsplit, B, L): CTA (h * qsplit + q, b, l) takes the q-th of
@@ -74,8 +162,15 @@ __host__ __device__ inline CsLayout cs_layout(const Dims& d, bool read) {
 // (row = position mod Mr); a commit reads rows of positions < T (its first
 // position, recorded by the commit projection) and writes rows T..T+n-1,
 // never the same rows (n <= S + 1). W is recomputed from the ring every
-// commit, so no running sum drifts. (RING: compiled in only for M > 1.)
-template <typename T, int QPT, bool RING>
+// commit, so no running sum drifts.
+//
+// Gated-delta memory (gdn_token; MODE 2): per accepted row, with the unit
+// key k = B/|B| (|B| summed over the lanes that hold one state row),
+// alpha = exp(dt A) and beta the row's writing strength,
+//   S <- alpha (S - beta (S k) k^T) + beta x k^T,
+// where (S k) of a state row is a sum over the lanes holding that row.
+// MODE: 0 Mamba-2, 1 Mamba-2 with a horizon ring (M > 1), 2 gated delta.
+template <typename T, int QPT, int MODE>
 __global__ void __launch_bounds__(THREADS_CS)
 commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
                     const int32_t* __restrict__ n_acc,
@@ -165,7 +260,14 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
     sd[t] = __ldcg(&xb[(size_t)t * d.NS + d.dinner + N + hd]);
   __syncthreads();
   const float A = -expf(__ldg(&A_log[l * d.Hm + hd]));
-  const bool ring = RING && n > 0;
+  const bool ring = MODE == 1 && n > 0;
+  constexpr bool GDN = MODE == 2;
+  float* sbeta = sm + L.sbeta;
+  if (GDN) {
+    for (int t = threadIdx.x; t < n; t += blockDim.x)
+      sbeta[t] = __ldcg(&xb[(size_t)t * d.NS + d.dinner + N + d.Hm + hd]);
+    __syncthreads();
+  }
   float* sxo = sm + L.sxo;  // [lim][P]: x of the rows leaving the horizon (0: none)
   float* sbo = sm + L.sbo;  // [lim][N]
   float* sdo = sm + L.sdo;  // [lim]
@@ -231,7 +333,17 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) wbase += wsum[w];
   }
   float W = wbase;  // sum of dt over the horizon ending at the current row
-  for (int t = 0; t < n; ++t) {
+  if (GDN) {
+    const int gsz = N / 4;  // lanes holding one state row
+    for (int t = 0; t < n; ++t) {
+      float xv[QPT];
+#pragma unroll
+      for (int u = 0; u < QPT; ++u) xv[u] = sx[t * P + pi[u]];
+      gdn_token<QPT>(hv, xv, *reinterpret_cast<const float4*>(&sb[t * N + ci[0]]),
+                     expf(sd[t] * A), sbeta[t], gsz);
+    }
+  }
+  for (int t = 0; t < (GDN ? 0 : n); ++t) {
     const float dt = sd[t];
     const float dec = last_only ? 0.f : expf(dt * A);
     float co = 0.f;  // weight of the row leaving the horizon
@@ -295,6 +407,20 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
       bf[j][3] = to_tf32(c.w);
     }
   }
+  float* qn = sm + L.qn;
+  if (GDN) {  // read with q = C_s / |C_s|
+    const int nw = blockDim.x >> 5;
+    for (int s2 = warp; s2 < d.S; s2 += nw) {
+      float acc = 0.f;
+      for (int c = lane; c < N; c += 32) {
+        const float v = __ldcg(&memC[((size_t)b * d.S + s2) * d.Nd + c]);
+        acc = fmaf(v, v, acc);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) qn[s2] = 1.f / sqrtf(acc);
+    }
+  }
   __syncthreads();  // the new state is in shared memory
   if (active) {
     float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -317,6 +443,7 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
     const int sl = e / P, p = e % P;
     float y = 0.f;
     for (int q = 0; q < KSPL; ++q) y += red[((size_t)q * P + p) * 8 + sl];
+    if (GDN) y *= qn[sl];
     mix[((size_t)b * d.S + sl) * d.Nz + d.QD + (size_t)hd * P + p] = from_f<T>(y);
   }
 }
@@ -331,7 +458,7 @@ cudaError_t set_smem(K kernel, int smem) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-template <bool R>
+template <int R>
 cudaError_t configure_variant(int smem) {
   cudaError_t e = set_smem(commit_state_kernel<float, 2, R>, smem);
   if (e == cudaSuccess) e = set_smem(commit_state_kernel<float, QPT_HEAD, R>, smem);
@@ -340,7 +467,7 @@ cudaError_t configure_variant(int smem) {
   return e;
 }
 
-template <bool R>
+template <int R>
 cudaError_t launch_variant(int dtype, const Dims& d, int B, bool whole, int qsplit, size_t smem,
                            int early, int late, const int32_t* n_acc, const float* xbd,
                            long long xls, const float* A_log, float* state, int64_t* pos,
@@ -364,8 +491,9 @@ cudaError_t configure_commit_state(const Dims& d) {
   static int configured = 0;  // attribute of the kernels: keep the largest need
   const int smem = (int)commit_state_smem(d, mem_tc_ok(d));
   if (smem <= configured) return cudaSuccess;
-  cudaError_t e = configure_variant<false>(smem);
-  if (e == cudaSuccess) e = configure_variant<true>(smem);
+  cudaError_t e = configure_variant<0>(smem);
+  if (e == cudaSuccess) e = configure_variant<1>(smem);
+  if (e == cudaSuccess) e = configure_variant<2>(smem);
   if (e == cudaSuccess) configured = smem;
   return e;
 }
@@ -384,11 +512,24 @@ cudaError_t launch_commit_state(int dtype, const Dims& d, int B, const int32_t* 
   const int qpt = whole ? QPT_HEAD : 2;
   const int qsplit = (nq + qpt * THREADS_CS - 1) / (qpt * THREADS_CS);
   const size_t smem = commit_state_smem(d, memC != nullptr);
-  return d.Mr > 0
-             ? launch_variant<true>(dtype, d, B, whole, qsplit, smem, early, late, n_acc, xbd, xls,
-                                    A_log, state, pos, offsets, tags, err, memC, mix, mr, st)
-             : launch_variant<false>(dtype, d, B, whole, qsplit, smem, early, late, n_acc, xbd,
-                                     xls, A_log, state, pos, offsets, tags, err, memC, mix, mr, st);
+  if (d.gdn)
+    return launch_variant<2>(dtype, d, B, whole, qsplit, smem, early, late, n_acc, xbd, xls, A_log,
+                             state, pos, offsets, tags, err, memC, mix, mr, st);
+  if (d.Mr > 0)
+    return launch_variant<1>(dtype, d, B, whole, qsplit, smem, early, late, n_acc, xbd, xls, A_log,
+                             state, pos, offsets, tags, err, memC, mix, mr, st);
+  return launch_variant<0>(dtype, d, B, whole, qsplit, smem, early, late, n_acc, xbd, xls, A_log,
+                           state, pos, offsets, tags, err, memC, mix, mr, st);
+}
+
+cudaError_t launch_gdn_prefill(const Dims& d, int layer, int b, int T, const float* xs,
+                               const float* A_log, float* state, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int nq = d.P * d.N / 4;
+  const int qsplit = (nq + QPT_SCAN * THREADS_CS - 1) / (QPT_SCAN * THREADS_CS);
+  gdn_prefill_kernel<<<d.Hm * qsplit, THREADS_CS, 0, st>>>(d, layer, b, T, qsplit, xs, A_log,
+                                                            state);
+  return cudaGetLastError();
 }
 
 }  // namespace hf

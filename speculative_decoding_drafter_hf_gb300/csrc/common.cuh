@@ -38,6 +38,9 @@ __device__ __forceinline__ float softplus_f(float x) {
   return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
 }
 
+// Logistic function (gated-delta writing strength).
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+
 // ---------------------------------------------------------------- PDL
 // Programmatic dependent launch: every kernel of a round lets the next one
 // start as soon as all of its CTAs are running (launch_dependents), and waits
@@ -143,6 +146,7 @@ struct Dims {
   int xoff;    // 1: cross-slot attention off (slot s sees the window and its own key)
   int Mh;      // memory horizon: 0 = whole history, M > 0 = last M committed features
   int Mr;      // rows of the memory-input ring (M > 1: M + S + 1, else 0)
+  int gdn;     // 1: gated-delta memory (commit columns gain beta: Nc, NS + Hm)
 };
 
 // ---------------------------------------------------------------- GEMM epilogues
@@ -243,7 +247,10 @@ __device__ __forceinline__ void epi_ssm(const Epi& e, int r, int c, float v, int
   } else {
     const int j = cl - 2 * d.KVD;
     float o = v;
-    if (j >= d.dinner + d.N) o = softplus_f(v + __ldg(&e.dt_bias[layer * d.Hm + (j - d.dinner - d.N)]));
+    if (j >= d.dinner + d.N + d.Hm)
+      o = sigmoid_f(v);
+    else if (j >= d.dinner + d.N)
+      o = softplus_f(v + __ldg(&e.dt_bias[layer * d.Hm + (j - d.dinner - d.N)]));
     e.xbd[(size_t)layer * e.xbd_layer_stride + (size_t)r * d.NS + j] = o;
   }
 }
@@ -253,7 +260,7 @@ __device__ __forceinline__ void epi_ssm(const Epi& e, int r, int c, float v, int
 // committed row, -1 when the row is skipped), so that a tile's inner loop is
 // one store per element.
 struct SsmCol {
-  int kind;      // 0: skip, 1: ring K/V, 2: x or B, 3: dt (softplus with bias)
+  int kind;      // 0: skip, 1: ring K/V, 2: x or B, 3: dt (softplus with bias), 4: beta (sigmoid)
   void* ring;    // ring_k or ring_v (kind 1)
   size_t base;   // element offset of (layer, head, dim) in the ring, or of (layer, column) in xbd
   float bias;    // dt bias (kind 3)
@@ -275,7 +282,9 @@ __device__ __forceinline__ SsmCol ssm_col(const Epi& e, int c) {
     const int j = cl - 2 * d.KVD;
     k.base = (size_t)layer * e.xbd_layer_stride + j;
     k.kind = 2;
-    if (j >= d.dinner + d.N) {
+    if (j >= d.dinner + d.N + d.Hm) {
+      k.kind = 4;
+    } else if (j >= d.dinner + d.N) {
       k.kind = 3;
       k.bias = __ldg(&e.dt_bias[layer * d.Hm + (j - d.dinner - d.N)]);
     }
@@ -295,7 +304,8 @@ __device__ __forceinline__ void ssm_store(const Epi& e, const SsmCol& k, int r, 
   if (k.kind == 1)
     static_cast<T*>(k.ring)[k.base + ro] = from_f<T>(v);
   else
-    e.xbd[k.base + (size_t)r * e.d.NS] = k.kind == 3 ? softplus_f(v + k.bias) : v;
+    e.xbd[k.base + (size_t)r * e.d.NS] =
+        k.kind == 3 ? softplus_f(v + k.bias) : (k.kind == 4 ? sigmoid_f(v) : v);
 }
 
 template <typename T>
@@ -363,7 +373,23 @@ __host__ __device__ inline int mem_ksplit(const Dims& d) {
   return ks;
 }
 __host__ __device__ inline size_t mem_tc_bytes(const Dims& d) {
-  return (size_t)mem_ksplit(d) * d.P * 8 * 4;
+  return (size_t)mem_ksplit(d) * d.P * 8 * 4 + 16 * 4;  // partial sums, 1/|C_s| (gated delta)
+}
+
+// Gated-delta read (q = C_s / |C_s|): 1/|C_s| of the S slot rows c0 + s*ld
+// into qn[0..S), one warp per row; the caller synchronises before use.
+__device__ __forceinline__ void slot_inv_norms(const float* c0, int ld, int S, int N, float* qn) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int s = warp; s < S; s += nw) {
+    float acc = 0.f;
+    for (int c = lane; c < N; c += 32) {
+      const float v = __ldcg(&c0[(size_t)s * ld + c]);
+      acc = fmaf(v, v, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) qn[s] = 1.f / sqrtf(acc);
+  }
 }
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
@@ -510,6 +536,12 @@ cudaError_t launch_commit_state(int dtype, const Dims& d, int B, const int32_t* 
 // Prefill helpers (lens/reqs/cu are device int32 arrays of n_req entries).
 cudaError_t launch_prefill_reset(const Dims& d, int n_req, const int32_t* reqs,
                                  float* state, int32_t* tags, int64_t* pos, cudaStream_t st);
+// Gated-delta prefill of request b, layer `layer`: the T rows of xs (x | B |
+// dt | beta, stride NS, as the commit projection writes them) applied in
+// order to the state.
+cudaError_t launch_gdn_prefill(const Dims& d, int layer, int b, int T, const float* xs,
+                               const float* A_log, float* state, cudaStream_t st);
+
 // (req_len, when not NULL, receives each named request's prefix length.)
 cudaError_t launch_prefill_ring_prep(int dtype, const Dims& d, int n_req, int n_rows,
                                      const int32_t* lens, const int32_t* reqs,

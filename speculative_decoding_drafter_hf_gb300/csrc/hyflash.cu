@@ -52,6 +52,7 @@ struct hf_handle {
   float* mem_dt = nullptr;   // [L][Bmax][Hm][Mr]
   int64_t* pos_snap = nullptr;  // [Bmax]: positions before the running commit
   int64_t* req_len = nullptr;   // [Bmax]: prefix lengths of the running prefill
+  float* gdn_xs = nullptr;      // gated delta: x | B | dt | beta of a prefill pass [Tseg][NS]
 
   int32_t* offsets = nullptr;  // [Bmax+1]
   int32_t* row_req = nullptr;  // [Rmax]
@@ -126,8 +127,9 @@ Dims make_dims(const hf_config& c) {
   d.KVD = d.Hkv * d.dh;
   d.dinner = d.Hm * d.P;
   d.Nd = d.QD + 2 * d.KVD + d.N;
-  d.Nc = 2 * d.KVD + d.dinner + d.N + d.Hm;
-  d.NS = (int)round_up(d.dinner + d.N + d.Hm, 4);
+  d.gdn = c.memory_kind == HF_MEM_GATED_DELTA ? 1 : 0;
+  d.Nc = 2 * d.KVD + d.dinner + d.N + d.Hm * (1 + d.gdn);  // [K | V | x | B | dt (| beta)]
+  d.NS = (int)round_up(d.dinner + d.N + d.Hm * (1 + d.gdn), 4);
   d.Nz = d.QD + d.dinner;
   d.esize = c.dtype == HF_F32 ? 4 : 2;
   d.xoff = c.cross_slot_off ? 1 : 0;
@@ -165,6 +167,10 @@ hf_status validate(const hf_config* c, std::string* why) {
   if (c->cross_slot_off != 0 && c->cross_slot_off != 1) return bad("cross_slot_off must be 0 or 1");
   if (c->mem_horizon < 0 || c->mem_horizon > c->window)
     return bad("mem_horizon must be in 0..window");
+  if (c->memory_kind != HF_MEM_MAMBA2 && c->memory_kind != HF_MEM_GATED_DELTA)
+    return bad("memory_kind must be HF_MEM_MAMBA2 or HF_MEM_GATED_DELTA");
+  if (c->memory_kind == HF_MEM_GATED_DELTA && c->mem_horizon != 0)
+    return bad("the gated-delta memory takes no memory horizon");
   {
     const Dims d = make_dims(*c);
     if (hf::attn_cluster_smem(d, d.esize) > 232448)
@@ -464,6 +470,7 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     h->skws_floats = need;
     A((void**)&h->skws, need * 4);
   }
+  if (d.gdn) A((void**)&h->gdn_xs, (size_t)h->pf_tokens * d.NS * 4);
   A((void**)&h->pf_dtw, (size_t)d.Hm * h->pf_tokens * 4);
   A((void**)&h->pf_decay, (size_t)d.Hm * 4);
   A(&h->pf_xsT, (size_t)d.dinner * h->pf_tokens * es);
@@ -528,6 +535,7 @@ hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w)
                         w->dt_bias, w->A_log};
   for (const void* p : ptrs)
     if (!p) return fail(h, HF_EINVAL, "a weight pointer is NULL");
+  if (h->d.gdn && !w->w_beta) return fail(h, HF_EINVAL, "the gated-delta memory needs w_beta");
   HF_CUDA(h, cudaSetDevice(h->device));
   const Dims& d = h->d;
   const size_t es = h->esz, D = d.D;
@@ -549,6 +557,7 @@ hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w)
   put_t(wc, 2 * d.KVD, D, w->w_x, D, d.dinner);
   put_t(wc, 2 * d.KVD + d.dinner, D, w->w_B, D, d.N);
   put_t(wc, 2 * d.KVD + d.dinner + d.N, D, w->w_dt, D, d.Hm);
+  if (d.gdn) put_t(wc, 2 * d.KVD + d.dinner + d.N + d.Hm, D, w->w_beta, D, d.Hm);
   // W_out^T: row c = [W_o[:, c] | W_mo[:, c]]
   {
     const char* so = static_cast<const char*>(w->w_o);
@@ -871,10 +880,39 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
         if (e != cudaSuccess) return cuda_fail(h, e, "prefill memory-input gemm");
       }
     }
+    const long long Tseg = h->pf_tokens;
+    if (d.gdn) {
+      // Gated delta: per request and pass of at most Tseg tokens, x | B | dt |
+      // beta of every token (the commit projection's columns and epilogue),
+      // then the rule applied token by token (no chunked form here)
+      const char* w_mem = wl + (size_t)2 * d.KVD * d.D * es;
+      const int ncol = d.dinner + d.N + 2 * d.Hm;
+      long long cu = 0;
+      for (int i = 0; i < n_req; ++i) {
+        const long long Li = lens[i];
+        for (long long s0 = 0; s0 < Li; s0 += Tseg) {
+          const int T = (int)std::min(Tseg, Li - s0);
+          Epi eg = epi_base(h);
+          eg.kind = hf::EPI_SSM_KV;  // rows of no request: every row kept, no ring columns
+          eg.layer0 = l;
+          eg.cols_per_layer = ncol;
+          eg.col_off = 2 * d.KVD;
+          eg.xbd = h->gdn_xs;
+          eg.xbd_layer_stride = 0;
+          e = tokens_gemm(h, bptr(feats, (size_t)(cu + s0) * d.D * es), T, w_mem, ncol, eg, st,
+                          &sc.count);
+          if (e != cudaSuccess) return cuda_fail(h, e, "prefill gated-delta projection");
+          e = hf::launch_gdn_prefill(d, l, reqs[i], T, h->gdn_xs, h->A_log, h->state, st);
+          sc.count++;
+          if (e != cudaSuccess) return cuda_fail(h, e, "prefill gated-delta scan");
+        }
+        cu += Li;
+      }
+      continue;
+    }
     // Memory fold, per request and segment of at most Tseg tokens:
     //   dt (transposed) -> chunked decay scan -> w*x, B (transposed, bf16/fp32)
     //   -> state = decay_seg * state + (w*x)^T B   (contraction over tokens)
-    const long long Tseg = h->pf_tokens;
     const int nx = d.dinner + d.N;
     const char* w_xb = wl + (size_t)2 * d.KVD * d.D * es;
     const char* w_dt = wl + (size_t)(2 * d.KVD + d.dinner + d.N) * d.D * es;

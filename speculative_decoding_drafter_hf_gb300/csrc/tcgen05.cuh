@@ -157,6 +157,9 @@ __device__ __forceinline__ void epi_chunk16(const Epi& e, int m, int n0, int nco
             const int h0 = (n0 % e.cols_per_layer + e.col_off) - 2 * d.KVD - d.dinner - d.N;
 #pragma unroll
             for (int q = 0; q < 16; ++q) x[q] = softplus_f(v[q] + __ldg(&e.dt_bias[layer * d.Hm + h0 + q]));
+          } else if (k0.kind == 4) {  // gated-delta writing strength
+#pragma unroll
+            for (int q = 0; q < 16; ++q) x[q] = sigmoid_f(v[q]);
           }
           float4* o4 = reinterpret_cast<float4*>(o);
 #pragma unroll

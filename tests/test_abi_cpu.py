@@ -38,10 +38,11 @@ def test_every_declared_symbol_is_exported(hf):
 
 
 def test_config_struct_layout(hf):
-    # 14 int32, the int64 pass size, the two int32 ablation fields
-    assert ctypes.sizeof(hf.HfConfig) == 72
-    assert hf.HfConfig.mem_horizon.offset == 68
-    assert ctypes.sizeof(hf.HfLayerWeights) == 11 * ctypes.sizeof(ctypes.c_void_p)
+    # 14 int32, the int64 pass size, two int32 ablation fields, the memory
+    # kind, padding to the int64 alignment
+    assert ctypes.sizeof(hf.HfConfig) == 80
+    assert hf.HfConfig.mem_horizon.offset == 68 and hf.HfConfig.memory_kind.offset == 72
+    assert ctypes.sizeof(hf.HfLayerWeights) == 12 * ctypes.sizeof(ctypes.c_void_p)
 
 
 def _cfg(hf, **kw):
@@ -56,7 +57,7 @@ def _cfg(hf, **kw):
     ("n_groups", 2), ("n_kv_heads", 3), ("head_dim", 66), ("window", 7), ("chunk", 100),
     ("dtype", 5), ("d_model", 250), ("block", 17), ("d_state", 18), ("max_batch", 0),
     ("prefill_tokens_max", -1), ("ssm_headdim", 130), ("cross_slot_off", 2),
-    ("mem_horizon", -1), ("mem_horizon", 65)])
+    ("mem_horizon", -1), ("mem_horizon", 65), ("memory_kind", 2)])
 def test_invalid_config_is_einval_without_cuda(hf, field, value):
     from speculative_decoding_drafter_hf_gb300 import _binding as B
     h = ctypes.c_void_p()
@@ -84,3 +85,10 @@ def test_valid_config_without_gpu_is_ecuda(hf):
     h = ctypes.c_void_p()
     s = B.hf_create(ctypes.byref(_cfg(hf)), 0, ctypes.byref(h))
     assert s == hf.Status.ECUDA and not h.value
+
+
+def test_gated_delta_with_horizon_is_einval(hf):
+    from speculative_decoding_drafter_hf_gb300 import _binding as B
+    h = ctypes.c_void_p()
+    s = B.hf_create(ctypes.byref(_cfg(hf, memory_kind=1, mem_horizon=4)), 0, ctypes.byref(h))
+    assert s == hf.Status.EINVAL and not h.value

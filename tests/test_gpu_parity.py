@@ -457,3 +457,25 @@ def test_memory_horizon_round_api_and_graph():
     p.prefill(lens, make_prefix_feats(cfg, lens))
     run_round_api(p, 6, check_every=1)
     p.close()
+
+
+# ---------------------------------------------------------------- gated-delta memory
+
+@pytest.mark.parametrize("name,batch,lens,api", [
+    ("tiny_fp32", 3, [0, 9, 300], "separate"),   # several prefill passes (128 tokens)
+    ("qwen3_4b_bf16", 2, [5, 60], "separate"),
+    ("qwen3_4b_bf16", 2, [5, 60], "round"),
+    ("qwen3_4b_bf16", 8, [3, 7, 12, 20, 25, 30, 33, 40], "round"),  # fused memory read
+])
+def test_gated_delta_memory(name, batch, lens, api):
+    """The gated delta rule as the memory: prefill (token-by-token scan),
+    commits (the state kernel's gated-delta update) and the normalised read."""
+    cfg = CONFIGS[name].replace(batch=batch, prefix=100, memory="gdn")
+    p = Pair(cfg, prefill_tokens_max=128)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="prefill")
+    if api == "round":
+        run_round_api(p, 3, check_every=1)
+    else:
+        run_rounds(p, 4 if name == "tiny_fp32" else 3, check_every=1)
+    p.close()
