@@ -110,7 +110,8 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
     QD = hq * dh
     Nd = QD + 2 * hkv * dh + N
     Nz = QD + din
-    Nc = 2 * hkv * dh + din + N + Hm
+    gdn = getattr(cfg, "memory", "mamba2") == "gdn"
+    Nc = 2 * hkv * dh + din + N + Hm * (2 if gdn else 1)   # gated delta: + beta columns
     R = batch * S
     rows = batch * mean_accept
     w_draft, w_out, w_commit = e * Nd * D, e * D * Nz, e * L * Nc * D
@@ -120,8 +121,9 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
     state = batch * Hm * P * N * 4                     # one layer's states, read once
     io_attn = 4 * R * Nd + e * R * QD                  # projections in, attention out
     io_mem = 4 * R * N + e * R * din                   # C in, memory read out
-    commit_io = e * rows * D + L * rows * (2 * hkv * dh * e + (din + N + Hm) * 4)
-    state_io = L * rows * (din + N + Hm) * 4
+    ns = din + N + Hm * (2 if gdn else 1)              # memory-input columns per row
+    commit_io = e * rows * D + L * rows * (2 * hkv * dh * e + ns * 4)
+    state_io = L * rows * ns * 4
     M = int(getattr(cfg, "mem_horizon", 0) or 0)
     state_rw = 1 if M == 1 else 2                      # M = 1: the old state is not read
     if M > 1:
@@ -155,7 +157,10 @@ def ablation_config(cfg) -> dict:
         out["cross_slot"] = "off (each slot sees the window and its own key)"
     if getattr(cfg, "mem_horizon", 0):
         out["mem_horizon"] = int(cfg.mem_horizon)
-    return {"ablation": out} if out else {}
+    res = {"ablation": out} if out else {}
+    if getattr(cfg, "memory", "mamba2") == "gdn":
+        res["memory"] = "gated delta rule (GDN)"
+    return res
 
 
 def kernel_sources_digest() -> str:
@@ -713,12 +718,14 @@ def main(argv=None):
                     help="ablation: mask attention among the draft slots")
     ap.add_argument("--mem-horizon", type=int, default=0,
                     help="ablation: memory of the last M committed features (0: all)")
+    ap.add_argument("--memory", default="mamba2", choices=["mamba2", "gdn"],
+                    help="memory kind: Mamba-2 (default) or the gated delta rule")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from workload import CONFIGS
     cfg = CONFIGS[args.config].replace(cross_slot=not args.cross_slot_off,
-                                       mem_horizon=args.mem_horizon)
+                                       mem_horizon=args.mem_horizon, memory=args.memory)
     if args.impl == "reference":
         return run_reference(args, cfg)
     if cfg.rounds == 0:
