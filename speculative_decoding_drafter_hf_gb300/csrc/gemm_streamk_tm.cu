@@ -17,6 +17,12 @@
 // row is one token and its 16-column chunks are 16 consecutive features, so
 // the epilogue moves contiguous runs (epi_chunk16).
 //
+// With at least as many tiles as CTAs the launch is data-parallel instead
+// (dp): CTA g takes whole tiles g, g + G, g + 2G, ...; with tokens innermost
+// the CTAs 4s..4s+3 of a wave then stream the same weight panel at the same
+// time (one DRAM read, the other three from L2), where contiguous stream-K
+// shares would come back to a panel only after a whole tile of every CTA.
+//
 // Warp 0 (one lane) streams W (before the dependency wait: weights do not
 // depend on earlier launches) and X through a ring of STAGES slots; warp 1
 // (one lane) issues tcgen05.mma into one of two TMEM accumulators; warps 2-9
@@ -43,6 +49,8 @@ struct TmArgs {
   float* ws;               // [2G][16 chunks][128][16] partial slots
   int* tickets;            // [tile], zero between launches
   int late_trigger;        // 1: signal dependents only after the dependency wait
+  int dp;                  // 1: whole tiles g, g + G, ... per CTA (no partial tiles)
+  int tiles;               // tiles of both products
   int32_t* err;
 };
 
@@ -78,9 +86,18 @@ tc_gemm_tm_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant
   const int g = blockIdx.x;
   const int kb = a.kblocks;
   const int T0 = a.mt0 * a.nt0;
-  const long long u0 = tm_start(g, a.U, a.G), u1 = tm_start(g + 1, a.U, a.G);
-  const int nu = (int)(u1 - u0);
+  const long long u0 = a.dp ? 0 : tm_start(g, a.U, a.G), u1 = a.dp ? 0 : tm_start(g + 1, a.U, a.G);
+  const int nu = a.dp ? (g < a.tiles ? (a.tiles - 1 - g) / a.G + 1 : 0) * kb : (int)(u1 - u0);
   const int first_tile = (int)(u0 / kb);
+  // global unit of this CTA's i-th unit, and the end (local) of the segment holding it
+  auto gu = [&](int i) -> long long {
+    return a.dp ? (long long)(g + (i / kb) * a.G) * kb + i % kb : u0 + i;
+  };
+  auto seg_end_of = [&](int i) -> int {
+    if (a.dp) return (i / kb + 1) * kb;
+    const long long t = (u0 + i) / kb;
+    return (int)(min(u1, (t + 1) * kb) - u0);
+  };
   // tile t -> product, token tile, feature tile (token tiles innermost)
   auto tile_of = [&](int t, bool& second, int& mt, int& nt) {
     second = t >= T0;
@@ -124,11 +141,11 @@ tc_gemm_tm_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant
     const int pre = nu < TM_STAGES ? nu : TM_STAGES;
     for (int j = 0; j < pre; ++j) {
       mbar_expect_tx(&full[j], STAGE_BYTES);
-      load_w(j, u0 + j);
+      load_w(j, gu(j));
     }
     pdl_wait();
     if (a.late_trigger) pdl_trigger();
-    for (int j = 0; j < pre; ++j) load_x(j, u0 + j);
+    for (int j = 0; j < pre; ++j) load_x(j, gu(j));
     int i = pre;
     for (; i < nu; ++i) {
       const int s = i % TM_STAGES;
@@ -139,8 +156,8 @@ tc_gemm_tm_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant
       }
       if (*(volatile int*)&flags[0]) break;
       mbar_expect_tx(&full[s], STAGE_BYTES);
-      load_w(s, u0 + i);
-      load_x(s, u0 + i);
+      load_w(s, gu(i));
+      load_x(s, gu(i));
     }
     flags[1] = i;
   } else if (warp == 1 && lane == 0) {
@@ -152,9 +169,7 @@ tc_gemm_tm_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant
     int i = 0, j = 0;
     bool ok = true;
     while (i < nu && ok) {
-      const long long u = u0 + i;
-      const int t = (int)(u / kb);
-      const int seg_end = (int)(min(u1, (long long)(t + 1) * kb) - u0);
+      const int seg_end = seg_end_of(i);
       const int buf = j & 1;
       if (!mbar_wait(&tempty[buf], ((uint32_t)(j >> 1) & 1u) ^ 1u)) {
         ok = false;
@@ -195,10 +210,10 @@ tc_gemm_tm_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant
     if (a.late_trigger) pdl_trigger();
     int i = 0, j = 0;
     while (i < nu) {
-      const long long u = u0 + i;
+      const long long u = gu(i);
       const int t = (int)(u / kb);
       const long long t_lo = (long long)t * kb, t_hi = t_lo + kb;
-      i = (int)(min(u1, t_hi) - u0);
+      i = seg_end_of(i);
       const int buf = j & 1;
       if (!mbar_wait(&tfull[buf], (uint32_t)(j >> 1) & 1u)) {
         atomicExch(&flags[0], 1);
@@ -213,7 +228,8 @@ tc_gemm_tm_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant
       const int M = second ? a.M1 : a.M0, N = second ? a.N1 : a.N0;
       const Epi& ep = second ? epi1 : epi0;
       const int m = mt * 128 + ml, n_base = nt * TM_BN;
-      const int gfirst = tm_owner(t_lo, a.U, a.G), glast = tm_owner(t_hi - 1, a.U, a.G);
+      const int gfirst = a.dp ? g : tm_owner(t_lo, a.U, a.G);
+      const int glast = a.dp ? g : tm_owner(t_hi - 1, a.U, a.G);
       const int nseg = glast - gfirst + 1;
       float v[16];
       if (nseg > 1) {
@@ -335,6 +351,8 @@ cudaError_t launch_gemm_tm(const void* X0, long long ldx0, int M0, const void* W
   const long long tiles = (long long)a.mt0 * a.nt0 + (long long)a.mt1 * a.nt1;
   a.U = tiles * a.kblocks;
   a.G = (int)std::min<long long>(num_sms, a.U);
+  a.tiles = (int)tiles;
+  a.dp = tiles >= a.G ? 1 : 0;  // enough whole tiles for every CTA
   if (tiles > n_tickets || gemm_tm_workspace(a.G) > ws_floats) return cudaErrorInvalidValue;
   a.ws = ws;
   a.tickets = tickets;
