@@ -114,7 +114,8 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
     Nc = 2 * hkv * dh + din + N + Hm * (2 if gdn else 1)   # gated delta: + beta columns
     R = batch * S
     rows = batch * mean_accept
-    w_draft, w_out, w_commit = e * Nd * D, e * D * Nz, e * L * Nc * D
+    we = e if getattr(cfg, "weight_bits", 16) != 4 else 0.5 + 4.0 / 128  # 4-bit codes + group params
+    w_draft, w_out, w_commit = we * Nd * D, we * D * Nz, we * L * Nc * D
     io_draft = e * R * D + 4 * R * Nd                 # slot rows in, projections out
     io_out = e * R * Nz + 2 * e * R * D                # mix in, residual in, output out
     window = batch * window_fill * 2 * hkv * dh * e    # one layer's valid K and V
@@ -150,6 +151,18 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
     return {"families": fam, "step_bytes": step, "step_flops": flops}
 
 
+def layer_weights(cfg, layer: int):
+    """The workload's weights of one layer (4-bit codes when weight_bits = 4)."""
+    from workload import make_layer_weights, make_layer_weights_q4
+    return (make_layer_weights_q4 if getattr(cfg, "weight_bits", 16) == 4 else make_layer_weights)(
+        cfg, layer)
+
+
+def set_layer_weights(drafter, cfg, layer: int):
+    w = layer_weights(cfg, layer)
+    (drafter.set_weights_q4 if getattr(cfg, "weight_bits", 16) == 4 else drafter.set_weights)(layer, w)
+
+
 def ablation_config(cfg) -> dict:
     """The ablation modes in force, if any (config keys of the JSON line)."""
     out = {}
@@ -160,6 +173,8 @@ def ablation_config(cfg) -> dict:
     res = {"ablation": out} if out else {}
     if getattr(cfg, "memory", "mamba2") == "gdn":
         res["memory"] = "gated delta rule (GDN)"
+    if getattr(cfg, "weight_bits", 16) == 4:
+        res["weights"] = "4-bit codes, bf16 scale + zero point per 128 inputs (skinny products dequantise on chip)"
     return res
 
 
@@ -281,7 +296,7 @@ def oracle_rounds(cfg, batch: int, steps: int, warmup: int, budget_s: float, see
     from oracle import hyflash_oracle as O
     from workload import (make_accepted, make_layer_weights, make_prefix_feats,
                           make_prefix_lens, make_round_inputs)
-    weights = [make_layer_weights(cfg, l) for l in range(cfg.n_layers)]
+    weights = [layer_weights(cfg, l) for l in range(cfg.n_layers)]
     orc = O.OracleDrafter(cfg, weights, batch)
     lens = [min(L, ORACLE_PREFIX_CAP) for L in make_prefix_lens(cfg)[:batch]]
     orc.prefill(lens, make_prefix_feats(cfg, lens, seed=seed))
@@ -450,7 +465,7 @@ def run_hyflash(args, cfg):
     seed = rank  # each replica drafts for its own requests
     drafter = hf.Drafter(cfg, batch, device=local)
     for l in range(cfg.n_layers):
-        drafter.set_weights(l, make_layer_weights(cfg, l))
+        set_layer_weights(drafter, cfg, l)
     lens = make_prefix_lens(cfg, seed=0)[:batch]
     if args.prefix_max:  # smaller prefill (e.g. for profiling); rounds unchanged once windows fill
         lens = [min(L, args.prefix_max) for L in lens]
@@ -720,12 +735,15 @@ def main(argv=None):
                     help="ablation: memory of the last M committed features (0: all)")
     ap.add_argument("--memory", default="mamba2", choices=["mamba2", "gdn"],
                     help="memory kind: Mamba-2 (default) or the gated delta rule")
+    ap.add_argument("--weight-bits", type=int, default=16, choices=[16, 4],
+                    help="weights in the model dtype (16) or 4-bit codes (4)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from workload import CONFIGS
     cfg = CONFIGS[args.config].replace(cross_slot=not args.cross_slot_off,
-                                       mem_horizon=args.mem_horizon, memory=args.memory)
+                                       mem_horizon=args.mem_horizon, memory=args.memory,
+                                       weight_bits=args.weight_bits)
     if args.impl == "reference":
         return run_reference(args, cfg)
     if cfg.rounds == 0:

@@ -115,6 +115,15 @@ typedef struct {
    * rule of "Gated Delta Networks: Improving Mamba2 with Delta Rule").
    * Needs w_beta; no memory horizon. */
   int32_t memory_kind;
+  /* Weight precision: 16 (the model dtype) or 4 (bf16 handles only; the
+   * paper's INT4 / GPTQ drafter): weights enter through hf_set_weights_q4 as
+   * 4-bit codes with a bf16 scale and an integer zero point per output
+   * column and group of 128 input rows, w = scale * (code - zero). Draft and
+   * commit products of at most 32 activation rows read the 4-bit tiles and
+   * dequantise them on chip; wider products and prefill use the same
+   * weights dequantised once to bf16. d_model, n_q_heads*head_dim and
+   * ssm_heads*ssm_headdim must be multiples of 128. 0 means 16. */
+  int32_t weight_bits;
 } hf_config;
 
 enum { HF_MEM_MAMBA2 = 0, HF_MEM_GATED_DELTA = 1 };
@@ -139,6 +148,25 @@ typedef struct {
   const void* w_beta;  /* [D, Hm]: gated-delta writing strength (NULL otherwise) */
 } hf_layer_weights;
 
+/* One 4-bit matrix of hf_layer_weights_q4, HOST pointers, for a weight of
+ * shape [in, out] (in a multiple of 128): codes uint8 [in, out] with values
+ * 0..15; scales bf16 bits [in/128, out]; zeros uint8 [in/128, out] (0..15).
+ * Element (i, o) is scales[i/128][o] * (codes[i][o] - zeros[i/128][o]). */
+typedef struct {
+  const uint8_t* codes;
+  const uint16_t* scales;
+  const uint8_t* zeros;
+} hf_q4_matrix;
+
+/* A layer's weights in 4 bits (same matrices and shapes as
+ * hf_layer_weights; w_beta only with the gated-delta memory, else codes
+ * NULL). dt_bias and A_log stay fp32 [ssm_heads]. */
+typedef struct {
+  hf_q4_matrix w_q, w_k, w_v, w_o, w_x, w_B, w_C, w_dt, w_mo, w_beta;
+  const float* dt_bias;
+  const float* A_log;
+} hf_layer_weights_q4;
+
 /* Create a handle on CUDA device `device`: validates cfg (HF_EINVAL before
  * touching CUDA), allocates and zeroes rings, states, positions, weights and
  * scratch (HF_ENOMEM on failure, everything freed). Synchronises. */
@@ -151,6 +179,11 @@ void hf_destroy(hf_handle* h);
  * transposed to [out, in] and concatenated per call site). Synchronises;
  * the caller may free its buffers afterwards. */
 hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w);
+
+/* The same for a handle with weight_bits = 4 (HF_EINVAL otherwise, and for
+ * codes or zeros above 15): keeps the 4-bit tiles of the skinny products and
+ * the bf16 dequantisation of the others. Synchronises. */
+hf_status hf_set_weights_q4(hf_handle* h, int32_t layer, const hf_layer_weights_q4* w);
 
 /* Prefill (fold the committed prefix). feats: DEVICE [sum(lens), D] packed
  * in request order; lens: HOST int32 [n_req], each >= 0; requests: HOST int32

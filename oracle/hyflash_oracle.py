@@ -66,6 +66,15 @@ with S [P x N] per head (value x key). Readings:
       uses q = C_s / |C_s|; no memory horizon with this kind. Prefill is the
       same rule applied token by token (committing the whole prefix).
 
+4-bit weights (the paper's INT4 / GPTQ table: the 4-bit drafter keeps
+99.2% of the bf16 acceptance; explainer, "Where it earns its keep"):
+  R12 a 4-bit matrix of shape [in, out] holds codes q in 0..15 and, per
+      group of 128 consecutive inputs and per output, a scale s and a zero
+      point z (GPTQ's asymmetric group format); its value is
+      w[i, o] = s[i // 128, o] * (q[i, o] - z[i // 128, o]). How the codes
+      were chosen (GPTQ's error-compensating rounding) is outside the hot
+      path: the layer computes with these values.
+
 Parity pins (tests/test_oracle_pins.py): the chunked fold equals the
 token-by-token recurrence and the unrolled product closed form; constant decay
 matches scipy.signal.lfilter; A = 0 gives the plain sum, huge decay keeps only
@@ -126,12 +135,23 @@ class Weights64:
     def from_any(w) -> "Weights64":
         names = [f.name for f in dataclasses.fields(Weights64)]
         vals = {n: getattr(w, n, None) for n in names}
-        return Weights64(**{n: (None if v is None else to64(v)) for n, v in vals.items()})
+        return Weights64(**{n: (None if v is None else
+                                (dequantize_q4(v) if hasattr(v, "codes") else to64(v)))
+                            for n, v in vals.items()})
 
     @property
     def A(self) -> np.ndarray:
         """Learned negative decay A = -exp(A_log), one scalar per SSM head."""
         return -np.exp(self.A_log)
+
+
+def dequantize_q4(m) -> np.ndarray:
+    """R12: w[i, o] = s[i // 128, o] * (q[i, o] - z[i // 128, o]), float64."""
+    q = to64(m.codes)
+    s = to64(m.scales)
+    z = to64(m.zeros)
+    g = np.arange(q.shape[0]) // 128
+    return s[g, :] * (q - z[g, :])
 
 
 # --------------------------------------------------------------------------

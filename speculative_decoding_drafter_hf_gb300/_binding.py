@@ -68,7 +68,8 @@ class HfConfig(ctypes.Structure):
         "max_batch", "chunk", "dtype")] + [("prefill_tokens_max", ctypes.c_int64),
                                            ("cross_slot_off", ctypes.c_int32),
                                            ("mem_horizon", ctypes.c_int32),
-                                           ("memory_kind", ctypes.c_int32)]
+                                           ("memory_kind", ctypes.c_int32),
+                                           ("weight_bits", ctypes.c_int32)]
 
 
 WEIGHT_FIELDS = ("w_q", "w_k", "w_v", "w_o", "w_x", "w_B", "w_C", "w_dt", "w_mo",
@@ -78,6 +79,18 @@ MEMORY_KINDS = {"mamba2": 0, "gdn": 1}
 
 class HfLayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class HfQ4Matrix(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("zeros", ctypes.c_void_p)]
+
+
+Q4_MATRICES = ("w_q", "w_k", "w_v", "w_o", "w_x", "w_B", "w_C", "w_dt", "w_mo", "w_beta")
+
+
+class HfLayerWeightsQ4(ctypes.Structure):
+    _fields_ = [(n, HfQ4Matrix) for n in Q4_MATRICES] + [
+        ("dt_bias", ctypes.c_void_p), ("A_log", ctypes.c_void_p)]
 
 
 _h = ctypes.c_void_p
@@ -96,6 +109,7 @@ def _sig(name, res, *args):
 hf_create = _sig("hf_create", _st, ctypes.POINTER(HfConfig), _i32, ctypes.POINTER(_h))
 hf_destroy = _sig("hf_destroy", None, _h)
 hf_set_weights = _sig("hf_set_weights", _st, _h, _i32, ctypes.POINTER(HfLayerWeights))
+hf_set_weights_q4 = _sig("hf_set_weights_q4", _st, _h, _i32, ctypes.POINTER(HfLayerWeightsQ4))
 hf_prefill = _sig("hf_prefill", _st, _h, _vp, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32, _vp)
 hf_commit = _sig("hf_commit", _st, _h, _vp, _vp, _i32, _vp)
 hf_draft = _sig("hf_draft", _st, _h, _vp, _vp, _i32, _vp)
@@ -116,7 +130,7 @@ hf_launch_count = _sig("hf_launch_count", ctypes.c_int64, _h)
 hf_attention_noalloc = _sig("hf_attention_noalloc", _st, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                             _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp)
 
-EXPORTED = ("hf_create", "hf_destroy", "hf_set_weights", "hf_prefill", "hf_commit", "hf_draft",
+EXPORTED = ("hf_create", "hf_destroy", "hf_set_weights", "hf_set_weights_q4", "hf_prefill", "hf_commit", "hf_draft",
             "hf_round", "hf_sync", "hf_last_error", "hf_status_string", "hf_tensor_bytes", "hf_read_tensor",
             "hf_context_bytes", "hf_export_context", "hf_import_context", "hf_profile_enable",
             "hf_profile_collect", "hf_profile_read", "hf_launch_count", "hf_attention_noalloc")
@@ -140,7 +154,8 @@ def make_config(shape, max_batch: int, prefill_tokens_max: int = 0) -> HfConfig:
         prefill_tokens_max=prefill_tokens_max,
         cross_slot_off=0 if getattr(shape, "cross_slot", True) else 1,
         mem_horizon=int(getattr(shape, "mem_horizon", 0) or 0),
-        memory_kind=MEMORY_KINDS[getattr(shape, "memory", "mamba2") or "mamba2"])
+        memory_kind=MEMORY_KINDS[getattr(shape, "memory", "mamba2") or "mamba2"],
+        weight_bits=int(getattr(shape, "weight_bits", 16) or 16))
 
 
 def _stream_ptr(stream) -> Optional[int]:
@@ -213,6 +228,30 @@ class Drafter:
             keep.append(t)
             setattr(lw, name, t.data_ptr())
         self._check(hf_set_weights(self._h, layer, ctypes.byref(lw)))
+
+    def set_weights_q4(self, layer: int, w):
+        """4-bit weights (weight_bits = 4): each matrix as codes uint8 [in, out],
+        scales bf16 [in/128, out], zeros uint8 [in/128, out]."""
+        import torch
+        keep = []
+        lw = HfLayerWeightsQ4()
+
+        def host(t, dtype):
+            t = t.detach().to("cpu", dtype).contiguous()
+            keep.append(t)
+            return t.data_ptr()
+
+        for name in Q4_MATRICES:
+            m = getattr(w, name, None)
+            if m is None:
+                continue
+            q = getattr(lw, name)
+            q.codes = host(m.codes, torch.uint8)
+            q.scales = host(m.scales, torch.bfloat16)
+            q.zeros = host(m.zeros, torch.uint8)
+        lw.dt_bias = host(w.dt_bias, torch.float32)
+        lw.A_log = host(w.A_log, torch.float32)
+        self._check(hf_set_weights_q4(self._h, layer, ctypes.byref(lw)))
 
     # -- the three operations of the method
     def prefill(self, feats, lens: Sequence[int], requests: Optional[Sequence[int]] = None,

@@ -432,14 +432,27 @@ cudaError_t launch_gemm_fma(int dtype, const void* X, int ldx, const void* Wt, i
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb,
                            int N, int K, int swap, int splits, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches, const void* a_tiles = nullptr,
-                           int late_trigger = 0, int a_group_mtiles = 0);
+                           int late_trigger = 0, int a_group_mtiles = 0, int q4 = 0);
 // Two swapped products with the same K in one launch (both A operands
 // pre-tiled): D0 = A0 B0^T with epilogue epi0, D1 = A1 B1^T with epi1.
 cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, int gm0, const void* B0,
                                    long long ldb0, int N0, const Epi& epi0, const void* a_tiles1,
                                    int M1, const void* B1, long long ldb1, int N1, const Epi& epi1,
                                    int K, int splits, int32_t* err, cudaStream_t st, int* launches,
-                                   int late_trigger = 0);
+                                   int late_trigger = 0, int q4 = 0);
+
+// 4-bit weights (GPTQ-style: codes 0..15, per row and 128-column group a bf16
+// scale s and a zero point z, w = s * (code - z)), pre-tiled like
+// tile_weights: per (m_tile, k_block) of 128 rows x 64 columns, 32 bytes of
+// codes per row (one 32-bit word per 8 columns: nibble i holds column 2i for
+// i < 4 and column 2(i-4)+1 otherwise), then per row one word (s's bf16 bits
+// | z << 16). q4 launches read these tiles (skinny products, at most 32
+// activation rows).
+constexpr int Q4_TILE_BYTES = 128 * 32 + 128 * 4;
+size_t q4_tiled_bytes(long long M, long long K);
+// codes [M][K] (0..15), prm [M][K/128] (scale bits | zero << 16) -> tiles
+void tile_weights_q4(const uint8_t* codes, const uint32_t* prm, long long M, long long K,
+                     uint8_t* dst);
 void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst);
 
 // Stream-K variant for the skinny swapped products (gemm_streamk.cu): one or
@@ -475,7 +488,7 @@ cudaError_t launch_gemm_persistent(const void* A, long long lda, int M, const vo
                                    long long ldb, int N, int K, int32_t* err, const Epi& epi,
                                    int num_sms, cudaStream_t st, int* launches);
 size_t tiled_bytes(long long M, long long K);
-int tc_pick_splits(int M, int N, int K);
+int tc_pick_splits(int M, int N, int K, int q4 = 0);
 
 // 2-D bf16 tensor map over rows x K (row stride ld elements), box 64 x
 // box_rows, 128-byte swizzle (gemm_tc.cu).

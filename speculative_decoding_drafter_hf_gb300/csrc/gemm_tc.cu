@@ -23,6 +23,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -85,14 +86,33 @@ struct EpiCache {
   static constexpr size_t bytes = BN * 8 + BN * 4 + RES_ROWS * 128 * 4;
 };
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(128, 1)
+__device__ __forceinline__ __nv_bfloat162 bf2_of(uint32_t u) {
+  __nv_bfloat162 v;
+  memcpy(&v, &u, 4);
+  return v;
+}
+__device__ __forceinline__ uint32_t bits_of(__nv_bfloat162 v) {
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  return u;
+}
+
+// Q4: A is 4-bit weights (pre-tiled, Q4_TILE_BYTES per (m_tile, k_block):
+// codes of 128 rows x 64 columns, then per row the bf16 scale and the zero
+// point of its 128-column group). Warps 4-11 turn each packed tile into the
+// bf16 swizzled tile the tensor core reads (w = scale * (code - zero), one
+// rounding) and release it to the MMA warp through afull; the producer, MMA
+// and epilogue warps are those of the bf16 kernel.
+template <int BN, int STAGES, bool Q4>
+__global__ void __launch_bounds__(Q4 ? 384 : 128, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb0,
                const __grid_constant__ CUtensorMap tb1, TcArgs a, const __grid_constant__ Epi epi0,
                const __grid_constant__ Epi epi1) {
   constexpr int A_BYTES = 128 * 128;
   constexpr int B_BYTES = BN * 128;
-  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr int PK_BYTES = Q4 ? Q4_TILE_BYTES : 0;
+  constexpr int TILE_BYTES = Q4 ? Q4_TILE_BYTES : A_BYTES;  // one stored A tile
+  constexpr uint32_t STAGE_BYTES = TILE_BYTES + B_BYTES;    // bytes the copies of a stage bring
   constexpr uint32_t NCOLS = BN < 32 ? 32 : BN;
   constexpr int RES_ROWS = EpiCache<BN>::RES_ROWS;
 
@@ -101,9 +121,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint8_t* sP = sB + STAGES * B_BYTES;  // Q4: packed tiles
+  uint64_t* full = reinterpret_cast<uint64_t*>(sP + STAGES * PK_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* done = empty + STAGES;
+  uint64_t* afull = empty + STAGES;     // Q4: dequantised A tile ready
+  uint64_t* done = afull + (Q4 ? STAGES : 0);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] issued, [2] consumed, [3] last
   // epilogue cache after the 32 bytes of TMEM slot and flags (8-byte aligned)
@@ -120,6 +142,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   const uint8_t* a_tiles = second ? a.a_tiles1 : a.a_tiles;
   const int a_gm = second ? a.a_gm1 : a.a_gm0;  // m-tiles per stored group
   const size_t a_tile_idx0 = ((size_t)(m_tile / a_gm) * a.kblocks) * a_gm + m_tile % a_gm;
+  const bool epw = !Q4 || warp < 4;  // the warps of the epilogue (TMEM lane quadrants)
   const CUtensorMap* tb = second ? &tb1 : &tb0;
   const Epi& epi = second ? epi1 : epi0;
   if (n_tile * BN >= N) return;  // the other product has more n-tiles (whole cluster)
@@ -132,6 +155,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      if (Q4) mbar_init(&afull[s], 8);  // one arrival per dequantising warp
     }
     mbar_init(done, 1);
     flags[0] = flags[1] = flags[2] = flags[3] = 0;
@@ -155,7 +179,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     const int pre = nkb < STAGES ? nkb : STAGES;
     // A tile of local k-block i into stage st
     auto load_a = [&](int st, int i) {
-      if (a_tiles)
+      if (Q4)
+        bulk_g2s(sP + st * PK_BYTES,
+                 a_tiles + (a_tile_idx0 + (size_t)(kb0 + i) * a_gm) * (size_t)TILE_BYTES,
+                 TILE_BYTES, &full[st]);
+      else if (a_tiles)
         bulk_g2s(sA + st * A_BYTES,
                  a_tiles + (a_tile_idx0 + (size_t)(kb0 + i) * a_gm) * (size_t)A_BYTES, A_BYTES,
                  &full[st]);
@@ -198,14 +226,52 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     pdl_wait();
     pdl_trigger();
   }
+  if (Q4 && warp >= 4) {
+    // dequantisers: thread (r, h) makes columns 32h..32h+31 of tile row r
+    const int dq = tid - 128, r = dq >> 1, h = dq & 1;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % STAGES;
+      if (!mbar_wait(&full[s], (uint32_t)(i / STAGES) & 1u)) {
+        atomicExch(&flags[0], 1);
+        break;
+      }
+      const uint8_t* pk = sP + s * PK_BYTES;
+      const uint4 cw = *reinterpret_cast<const uint4*>(pk + r * 32 + h * 16);
+      const uint32_t prm = *reinterpret_cast<const uint32_t*>(pk + 4096 + r * 4);
+      // bf16 pairs: s in both halves; 128 + z in both halves (0x4300 | z)
+      const uint32_t sb = prm & 0xFFFFu, zb = 0x4300u | ((prm >> 16) & 0xFu);
+      const __nv_bfloat162 s2 = bf2_of(sb | (sb << 16)), c2 = bf2_of(zb | (zb << 16));
+      const uint32_t wds[4] = {cw.x, cw.y, cw.z, cw.w};
+      uint8_t* arow = sA + s * A_BYTES + r * 128;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * h + cc;  // 16-byte chunk: columns 8c..8c+7
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // nibbles j and j + 4 of the word are columns 8c + 2j and 8c + 2j + 1
+          // (the tiles store them so); OR-ing a nibble into 0x4300 makes the
+          // bf16 128 + code, minus 128 + z is code - z exactly, times s rounds once
+          const uint32_t x = ((wds[cc] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+          o[j] = bits_of(__hmul2(__hsub2(bf2_of(x), c2), s2));
+        }
+        *reinterpret_cast<uint4*>(arow + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the tensor core
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&afull[s])) : "memory");
+    }
+  }
   if (warp == 1 && lane == 0) {
     // MMA issuer
     constexpr uint32_t idesc = idesc_bf16(BN < 16 ? 16 : BN);
+    uint64_t* ready = Q4 ? afull : full;
     int i = 0;
     for (; i < nkb; ++i) {
       const int s = i % STAGES;
       const uint32_t ph = (uint32_t)(i / STAGES) & 1u;
-      if (!mbar_wait(&full[s], ph)) {
+      if (!mbar_wait(&ready[s], ph)) {
         atomicExch(&flags[0], 1);
         break;
       }
@@ -223,7 +289,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   __syncwarp();
   pdl_wait();  // the epilogue writes memory earlier kernels may still read
   const int n_here = min(BN, N - n_tile * BN);
-  if (warp >= 2 && a.swap) {  // idle during the main loop: fetch the epilogue inputs
+  if (warp >= 2 && epw && a.swap) {  // idle during the main loop: fetch the epilogue inputs
     const int t2 = tid - 64;
     if (epi.kind == EPI_SSM_KV) {
       for (int nl = t2; nl < n_here; nl += 64) {
@@ -287,7 +353,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   };
   if (a.splits == 1) {
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
+    for (int c0 = 0; c0 < (epw ? BN : 0); c0 += 16) {
       tmem_ld16(trow + c0, v);
       if (m < M && c0 < n_here) {
         if (!a.swap) {
@@ -317,14 +383,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     // them over all partners in rank order (deterministic).
     float* red = reinterpret_cast<float*>(smem);
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
+    for (int c0 = 0; c0 < (epw ? BN : 0); c0 += 16) {
       tmem_ld16(trow + c0, v);
 #pragma unroll
       for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + m_local] = v[j];
     }
     cluster_sync_all();
     const int rank = (int)cluster_rank();
-    for (int c0 = rank * 16; c0 < n_here; c0 += a.splits * 16) {
+    for (int c0 = rank * 16; c0 < (epw ? n_here : 0); c0 += a.splits * 16) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         float part[8];
@@ -345,7 +411,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     // r, r + splits, ... over all partners in rank order (deterministic).
     float* red = reinterpret_cast<float*>(smem);
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
+    for (int c0 = 0; c0 < (epw ? BN : 0); c0 += 16) {
       tmem_ld16(trow + c0, v);
 #pragma unroll
       for (int j = 0; j < 16; ++j)
@@ -353,7 +419,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     }
     cluster_sync_all();
     const int rank = (int)cluster_rank();
-    for (int nl = rank; nl < n_here; nl += a.splits) {
+    for (int nl = rank; nl < (epw ? n_here : 0); nl += a.splits) {
       float part[8];
 #pragma unroll
       for (int sp = 0; sp < 8; ++sp)
@@ -417,31 +483,32 @@ namespace {
 // SM) measured slower at batch 1.
 constexpr int kStages16 = 7, kStages32 = 6;
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool Q4 = false>
 constexpr size_t tc_smem() {
-  // 1 KB alignment slack, stages, barriers, TMEM slot + flags (28 B), epilogue cache
-  return 1024 + (size_t)STAGES * (128 * 128 + BN * 128) + (2 * STAGES + 1) * 8 + 32 +
-         EpiCache<BN>::bytes;
+  // 1 KB alignment slack, stages (+ packed tiles), barriers, TMEM slot + flags
+  // (28 B), epilogue cache
+  return 1024 + (size_t)STAGES * (128 * 128 + BN * 128 + (Q4 ? Q4_TILE_BYTES : 0)) +
+         ((Q4 ? 3 : 2) * STAGES + 1) * 8 + 32 + EpiCache<BN>::bytes;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool Q4 = false>
 cudaError_t configure_one() {
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, Q4>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)tc_smem<BN, STAGES>());
+                                       (int)tc_smem<BN, STAGES, Q4>());
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES>,
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BN, STAGES, Q4>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool Q4 = false>
 cudaLaunchConfig_t tc_config(dim3 grid, int cz, cudaStream_t st, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = tc_smem<BN, STAGES>();
+  cfg.blockDim = dim3(Q4 ? 384 : 128);
+  cfg.dynamicSmemBytes = tc_smem<BN, STAGES, Q4>();
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -454,13 +521,26 @@ cudaLaunchConfig_t tc_config(dim3 grid, int cz, cudaStream_t st, cudaLaunchAttri
   return cfg;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool Q4 = false>
 cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1,
                       const TcArgs& a, const Epi& epi0, const Epi& epi1, dim3 grid,
                       cudaStream_t st) {
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = tc_config<BN, STAGES>(grid, a.splits, st, attr);
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES>, ma, mb0, mb1, a, epi0, epi1);
+  cudaLaunchConfig_t cfg = tc_config<BN, STAGES, Q4>(grid, a.splits, st, attr);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, STAGES, Q4>, ma, mb0, mb1, a, epi0, epi1);
+}
+
+// 4-bit weights: the skinny widths only (16 or 32 activation rows), the
+// bf16 ring depths (one CTA per SM). A 4-stage ring with two CTAs per SM and
+// split-K partners measured faster on the Phi-4 round projection (55 vs
+// 74 us) but slower over the Qwen3-4B round (17.6K vs 18.9K steps/s).
+template <typename... X>
+cudaError_t launch_bn_q4(int bn, X&&... x) {
+  switch (bn) {
+    case 16: return launch_tc<16, kStages16, true>(x...);
+    case 32: return launch_tc<32, kStages32, true>(x...);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <typename... X>
@@ -476,14 +556,14 @@ cudaError_t launch_bn(int bn, X&&... x) {
 
 // How many clusters of cz CTAs of this instantiation are resident at once
 // (the driver's answer for the tcgen05 kernel itself: one CTA per SM).
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool Q4 = false>
 int max_clusters(int cz) {
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = tc_config<BN, STAGES>(dim3(cz, 1, 1), cz, nullptr, attr);
+  cudaLaunchConfig_t cfg = tc_config<BN, STAGES, Q4>(dim3(cz, 1, 1), cz, nullptr, attr);
   cfg.attrs = attr + 1;  // occupancy query: cluster shape only
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, STAGES>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, STAGES, Q4>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -491,6 +571,7 @@ int max_clusters(int cz) {
 }
 
 int g_max_clusters[5][9] = {};  // [log2(BN/16)][cz]
+int g_max_clusters_q4[2][9] = {};  // 4-bit variants, BN 16 and 32
 
 }  // namespace
 
@@ -503,6 +584,8 @@ cudaError_t configure_tc() {
   if (e == cudaSuccess) e = configure_one<64, 5>();
   if (e == cudaSuccess) e = configure_one<128, 4>();
   if (e == cudaSuccess) e = configure_one<256, 4>();
+  if (e == cudaSuccess) e = configure_one<16, kStages16, true>();
+  if (e == cudaSuccess) e = configure_one<32, kStages32, true>();
   if (e != cudaSuccess) return e;
   for (int cz = 1; cz <= 8; ++cz) {
     g_max_clusters[0][cz] = max_clusters<16, kStages16>(cz);
@@ -510,6 +593,8 @@ cudaError_t configure_tc() {
     g_max_clusters[2][cz] = max_clusters<64, 5>(cz);
     g_max_clusters[3][cz] = max_clusters<128, 4>(cz);
     g_max_clusters[4][cz] = max_clusters<256, 4>(cz);
+    g_max_clusters_q4[0][cz] = max_clusters<16, kStages16, true>(cz);
+    g_max_clusters_q4[1][cz] = max_clusters<32, kStages32, true>(cz);
   }
   return cudaSuccess;
 }
@@ -517,7 +602,7 @@ cudaError_t configure_tc() {
 // Split-K factor for an M x N x K product: the largest cluster size (<= 8,
 // <= kblocks / 2) whose clusters, one per output tile, are all resident in a
 // single wave; 1 when the tiles alone fill the GPU.
-int tc_pick_splits(int M, int N, int K) {
+int tc_pick_splits(int M, int N, int K, int q4) {
   int bn = 16, lg = 0;
   while (bn < N && bn < 256) {
     bn *= 2;
@@ -527,15 +612,16 @@ int tc_pick_splits(int M, int N, int K) {
   const int kblocks = (K + 63) / 64;
   int best = 1;
   for (int cz = 2; cz <= 8 && cz <= kblocks / 2; ++cz)
-    if (tiles <= g_max_clusters[lg][cz]) best = cz;
+    if (tiles <= (q4 && lg < 2 ? g_max_clusters_q4[lg][cz] : g_max_clusters[lg][cz])) best = cz;
   return best;
 }
 
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb, int N,
                            int K, int swap, int splits, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches, const void* a_tiles,
-                           int late_trigger, int a_group_mtiles) {
+                           int late_trigger, int a_group_mtiles, int q4) {
   if (M <= 0 || N <= 0) return cudaSuccess;
+  if (q4 && (!a_tiles || !swap || N > 32)) return cudaErrorInvalidValue;
   int bn = 16;
   while (bn < N && bn < 256) bn *= 2;
   const int m_tiles = (M + 127) / 128;
@@ -563,6 +649,7 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   if (m_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
   dim3 grid(a.splits, m_tiles, n_tiles);
   ++*launches;
+  if (q4) return launch_bn_q4(bn, ma, mb, mb, a, epi, epi, grid, st);
   return launch_bn(bn, ma, mb, mb, a, epi, epi, grid, st);
 }
 
@@ -570,9 +657,10 @@ cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, int gm0, const 
                                    long long ldb0, int N0, const Epi& epi0, const void* a_tiles1,
                                    int M1, const void* B1, long long ldb1, int N1, const Epi& epi1,
                                    int K, int splits, int32_t* err, cudaStream_t st, int* launches,
-                                   int late_trigger) {
+                                   int late_trigger, int q4) {
   if (M0 <= 0 || N0 <= 0 || M1 <= 0 || N1 <= 0 || !a_tiles0 || !a_tiles1)
     return cudaErrorInvalidValue;
+  if (q4 && std::max(N0, N1) > 32) return cudaErrorInvalidValue;
   const int nmax = N0 > N1 ? N0 : N1;
   int bn = 16;
   while (bn < nmax && bn < 256) bn *= 2;
@@ -602,6 +690,7 @@ cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, int gm0, const 
   if (mt0 + mt1 > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
   dim3 grid(a.splits, mt0 + mt1, n_tiles);
   ++*launches;
+  if (q4) return launch_bn_q4(bn, mb0, mb0, mb1, a, epi0, epi1, grid, st);
   return launch_bn(bn, mb0, mb0, mb1, a, epi0, epi1, grid, st);
 }
 
@@ -627,6 +716,36 @@ void tile_weights(const uint16_t* src, long long M, long long K, uint16_t* dst) 
 
 size_t tiled_bytes(long long M, long long K) {
   return (size_t)((M + 127) / 128) * ((K + 63) / 64) * 128 * 64 * 2;
+}
+
+size_t q4_tiled_bytes(long long M, long long K) {
+  return (size_t)((M + 127) / 128) * ((K + 63) / 64) * Q4_TILE_BYTES;
+}
+
+void tile_weights_q4(const uint8_t* codes, const uint32_t* prm, long long M, long long K,
+                     uint8_t* dst) {
+  const long long mt = (M + 127) / 128, kb = (K + 63) / 64, ng = (K + 127) / 128;
+  for (long long t = 0; t < mt; ++t)
+    for (long long b = 0; b < kb; ++b) {
+      uint8_t* tile = dst + (size_t)(b * mt + t) * Q4_TILE_BYTES;
+      for (int r = 0; r < 128; ++r) {
+        const long long gr = t * 128 + r;
+        // per 8 columns one 32-bit word; nibble i holds column 2i (i < 4) or
+        // 2(i - 4) + 1, so that the kernel's pair j = nibbles (j, j + 4)
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w = 0;
+          for (int i = 0; i < 8; ++i) {
+            const int e = i < 4 ? 2 * i : 2 * (i - 4) + 1;
+            const long long gc = b * 64 + 8 * c + e;
+            const uint32_t q = (gr < M && gc < K) ? codes[gr * K + gc] & 15u : 0u;
+            w |= q << (4 * i);
+          }
+          std::memcpy(tile + r * 32 + 4 * c, &w, 4);
+        }
+        const uint32_t w = gr < M ? prm[gr * ng + (b * 64) / 128] : 0u;
+        std::memcpy(tile + 4096 + r * 4, &w, 4);
+      }
+    }
 }
 
 }  // namespace hf

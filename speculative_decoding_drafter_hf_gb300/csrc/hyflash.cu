@@ -36,6 +36,7 @@ struct hf_handle {
   void* wt_draft = nullptr;
   void* wt_commit = nullptr;
   void* wt_out = nullptr;
+  int q4 = 0;  // weight_bits = 4: the wt_* tiles hold 4-bit tiles (tile_weights_q4)
   size_t wt_draft_l = 0, wt_commit_l = 0, wt_out_l = 0;  // bytes per layer
   int nc_pad = 0;                                         // padded commit rows per layer
   float* dt_bias = nullptr;  // [L][Hm]
@@ -171,6 +172,14 @@ hf_status validate(const hf_config* c, std::string* why) {
     return bad("memory_kind must be HF_MEM_MAMBA2 or HF_MEM_GATED_DELTA");
   if (c->memory_kind == HF_MEM_GATED_DELTA && c->mem_horizon != 0)
     return bad("the gated-delta memory takes no memory horizon");
+  if (c->weight_bits != 0 && c->weight_bits != 16 && c->weight_bits != 4)
+    return bad("weight_bits must be 16 or 4");
+  if (c->weight_bits == 4) {
+    if (c->dtype != HF_BF16) return bad("4-bit weights need a bf16 handle");
+    if (c->d_model % 128 || ((long long)c->n_q_heads * c->head_dim) % 128 ||
+        ((long long)c->ssm_heads * c->ssm_headdim) % 128)
+      return bad("4-bit weights need d_model, n_q_heads*head_dim, ssm_heads*ssm_headdim multiples of 128");
+  }
   {
     const Dims d = make_dims(*c);
     if (hf::attn_cluster_smem(d, d.esize) > 232448)
@@ -314,13 +323,13 @@ cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, in
                               epi, st, count, nullptr, late_trigger);
   // skinny and more weight tiles than SMs: stream-K (no partial last wave);
   // otherwise one CTA or split-K cluster per tile (measured faster there)
-  if (tiles && R <= 32 && (C + 127) / 128 > h->num_sms)
+  if (tiles && R <= 32 && (C + 127) / 128 > h->num_sms && !h->q4)
     return hf::launch_gemm_sk(tiles, C, tile_group, X, ldx, R, epi, nullptr, 0, nullptr, 0, 0, epi,
                               K, h->num_sms, h->skws, h->skws_floats, h->counters, h->n_counters,
                               h->err, late_trigger, st, count);
-  const int splits = hf::tc_pick_splits(C, R, K);
+  const int splits = hf::tc_pick_splits(C, R, K, tiles && h->q4 ? 1 : 0);
   return hf::launch_gemm_tc(Wt, ldw, C, X, ldx, R, K, 1, splits, h->err, epi, st, count, tiles,
-                            late_trigger, tile_group);
+                            late_trigger, tile_group, tiles && h->q4 ? 1 : 0);
 }
 
 hf_status gemm(hf_handle* h, int fam, const void* X, int ldx, const void* Wt, int ldw, int R,
@@ -420,9 +429,10 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
   A(&h->w_out, L * d.D * d.Nz * es);
   if (h->cfg.dtype == HF_BF16) {
     h->nc_pad = (d.Nc + 127) / 128 * 128;
-    h->wt_draft_l = hf::tiled_bytes(d.Nd, d.D);
-    h->wt_commit_l = hf::tiled_bytes(h->nc_pad, d.D);
-    h->wt_out_l = hf::tiled_bytes(d.D, d.Nz);
+    h->q4 = h->cfg.weight_bits == 4 ? 1 : 0;
+    h->wt_draft_l = h->q4 ? hf::q4_tiled_bytes(d.Nd, d.D) : hf::tiled_bytes(d.Nd, d.D);
+    h->wt_commit_l = h->q4 ? hf::q4_tiled_bytes(h->nc_pad, d.D) : hf::tiled_bytes(h->nc_pad, d.D);
+    h->wt_out_l = h->q4 ? hf::q4_tiled_bytes(d.D, d.Nz) : hf::tiled_bytes(d.D, d.Nz);
     A(&h->wt_draft, L * h->wt_draft_l);
     A(&h->wt_commit, L * h->wt_commit_l);
     A(&h->wt_out, L * h->wt_out_l);
@@ -528,8 +538,98 @@ void hf_destroy(hf_handle* h) {
   delete h;
 }
 
+// The 4-bit side of a layer upload: codes / parameters in the per-call-site
+// row order of the bf16 weights (rows = output features, K = inputs).
+struct Q4Site {
+  std::vector<uint8_t> codes;  // [M][K]
+  std::vector<uint32_t> prm;   // [M][K/128]: scale bits | zero << 16
+  long long M = 0, K = 0;
+  void init(long long m, long long k) {
+    M = m;
+    K = k;
+    codes.assign((size_t)m * k, 0);
+    prm.assign((size_t)m * (k / 128), 0);
+  }
+  // matrix [in, outn] (q4 form) into rows row0.. and input columns col0..
+  void put(const hf_q4_matrix& q, size_t row0, size_t col0, size_t in, size_t outn) {
+    for (size_t i = 0; i < in; ++i)
+      for (size_t o = 0; o < outn; ++o) codes[(row0 + o) * K + col0 + i] = q.codes[i * outn + o];
+    for (size_t g = 0; g < in / 128; ++g)
+      for (size_t o = 0; o < outn; ++o)
+        prm[(row0 + o) * (K / 128) + col0 / 128 + g] =
+            (uint32_t)q.scales[g * outn + o] | ((uint32_t)q.zeros[g * outn + o] << 16);
+  }
+};
+struct Q4Layer {
+  Q4Site draft, commit, out;
+};
+
+static hf_status upload_layer(hf_handle* h, int32_t layer, const hf_layer_weights* w,
+                              const hf_layer_weights_q4* q);
+
 hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w) {
   if (!h) return HF_EINVAL;
+  if (h->q4) return fail(h, HF_EINVAL, "weight_bits = 4: set the weights with hf_set_weights_q4");
+  return upload_layer(h, layer, w, nullptr);
+}
+
+// bf16 bits, round to nearest even (finite inputs)
+static uint16_t to_bf16_bits(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+hf_status hf_set_weights_q4(hf_handle* h, int32_t layer, const hf_layer_weights_q4* q) {
+  if (!h) return HF_EINVAL;
+  if (!h->q4) return fail(h, HF_EINVAL, "hf_set_weights_q4 needs a handle with weight_bits = 4");
+  if (!q || layer < 0 || layer >= h->d.L) return fail(h, HF_EINVAL, "bad layer or weights");
+  const Dims& d = h->d;
+  const hf_q4_matrix* mats[] = {&q->w_q, &q->w_k, &q->w_v, &q->w_o, &q->w_x, &q->w_B,
+                                &q->w_C, &q->w_dt, &q->w_mo, &q->w_beta};
+  const size_t ins[] = {(size_t)d.D, (size_t)d.D, (size_t)d.D, (size_t)d.QD, (size_t)d.D,
+                        (size_t)d.D, (size_t)d.D, (size_t)d.D, (size_t)d.dinner, (size_t)d.D};
+  const size_t outs[] = {(size_t)d.QD, (size_t)d.KVD, (size_t)d.KVD, (size_t)d.D, (size_t)d.dinner,
+                         (size_t)d.N, (size_t)d.N, (size_t)d.Hm, (size_t)d.D, (size_t)d.Hm};
+  const int nm = d.gdn ? 10 : 9;
+  if (!q->dt_bias || !q->A_log) return fail(h, HF_EINVAL, "a weight pointer is NULL");
+  // dequantise on the host (w = s * (code - zero), one rounding to bf16: the
+  // product of a bf16 scale and a 4-bit integer is exact in fp32)
+  std::vector<std::vector<uint16_t>> deq(nm);
+  for (int m = 0; m < nm; ++m) {
+    const hf_q4_matrix& x = *mats[m];
+    if (!x.codes || !x.scales || !x.zeros) return fail(h, HF_EINVAL, "a weight pointer is NULL");
+    const size_t in = ins[m], on = outs[m];
+    deq[m].resize(in * on);
+    for (size_t i = 0; i < in; ++i)
+      for (size_t o = 0; o < on; ++o) {
+        const uint8_t c = x.codes[i * on + o], z = x.zeros[(i / 128) * on + o];
+        if (c > 15 || z > 15) return fail(h, HF_EINVAL, "4-bit codes and zeros must be 0..15");
+        uint32_t sb = (uint32_t)x.scales[(i / 128) * on + o] << 16;
+        float sc;
+        std::memcpy(&sc, &sb, 4);
+        deq[m][i * on + o] = to_bf16_bits(sc * ((float)c - (float)z));
+      }
+  }
+  hf_layer_weights wb{};
+  wb.w_q = deq[0].data();
+  wb.w_k = deq[1].data();
+  wb.w_v = deq[2].data();
+  wb.w_o = deq[3].data();
+  wb.w_x = deq[4].data();
+  wb.w_B = deq[5].data();
+  wb.w_C = deq[6].data();
+  wb.w_dt = deq[7].data();
+  wb.w_mo = deq[8].data();
+  wb.w_beta = d.gdn ? deq[9].data() : nullptr;
+  wb.dt_bias = q->dt_bias;
+  wb.A_log = q->A_log;
+  return upload_layer(h, layer, &wb, q);
+}
+
+static hf_status upload_layer(hf_handle* h, int32_t layer, const hf_layer_weights* w,
+                              const hf_layer_weights_q4* q) {
   if (!w || layer < 0 || layer >= h->d.L) return fail(h, HF_EINVAL, "bad layer or weights");
   const void* ptrs[] = {w->w_q, w->w_k, w->w_v, w->w_o, w->w_x, w->w_B, w->w_C, w->w_dt, w->w_mo,
                         w->dt_bias, w->A_log};
@@ -571,7 +671,41 @@ hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w)
   HF_CUDA(h, cudaMemcpy(bptr(h->w_draft, (size_t)layer * wd.size()), wd.data(), wd.size(), cudaMemcpyHostToDevice));
   HF_CUDA(h, cudaMemcpy(bptr(h->w_commit, (size_t)layer * wc.size()), wc.data(), wc.size(), cudaMemcpyHostToDevice));
   HF_CUDA(h, cudaMemcpy(bptr(h->w_out, (size_t)layer * wo.size()), wo.data(), wo.size(), cudaMemcpyHostToDevice));
-  if (h->cfg.dtype == HF_BF16) {
+  if (q) {  // 4-bit tiles of the three call sites, rows as in wd / wc / wo
+    Q4Layer ql;
+    ql.draft.init(d.Nd, D);
+    ql.draft.put(q->w_q, 0, 0, D, d.QD);
+    ql.draft.put(q->w_k, d.QD, 0, D, d.KVD);
+    ql.draft.put(q->w_v, d.QD + d.KVD, 0, D, d.KVD);
+    ql.draft.put(q->w_C, d.QD + 2 * d.KVD, 0, D, d.N);
+    ql.commit.init(d.Nc, D);
+    ql.commit.put(q->w_k, 0, 0, D, d.KVD);
+    ql.commit.put(q->w_v, d.KVD, 0, D, d.KVD);
+    ql.commit.put(q->w_x, 2 * d.KVD, 0, D, d.dinner);
+    ql.commit.put(q->w_B, 2 * d.KVD + d.dinner, 0, D, d.N);
+    ql.commit.put(q->w_dt, 2 * d.KVD + d.dinner + d.N, 0, D, d.Hm);
+    if (d.gdn) ql.commit.put(q->w_beta, 2 * d.KVD + d.dinner + d.N + d.Hm, 0, D, d.Hm);
+    ql.out.init(D, d.Nz);
+    ql.out.put(q->w_o, 0, 0, d.QD, D);
+    ql.out.put(q->w_mo, 0, d.QD, d.dinner, D);
+    std::vector<uint8_t> t(std::max({h->wt_draft_l, h->wt_commit_l, h->wt_out_l}));
+    struct {
+      Q4Site* site;
+      long long rows;
+      void* dst;
+      size_t bytes;
+    } jobs[] = {{&ql.draft, d.Nd, h->wt_draft, h->wt_draft_l},
+                {&ql.commit, h->nc_pad, h->wt_commit, h->wt_commit_l},
+                {&ql.out, D, h->wt_out, h->wt_out_l}};
+    for (auto& j : jobs) {
+      // rows past the site's (commit padding) are zero codes and parameters
+      j.site->codes.resize((size_t)j.rows * j.site->K, 0);
+      j.site->prm.resize((size_t)j.rows * (j.site->K / 128), 0);
+      hf::tile_weights_q4(j.site->codes.data(), j.site->prm.data(), j.rows, j.site->K, t.data());
+      HF_CUDA(h, cudaMemcpy(bptr(j.dst, (size_t)layer * j.bytes), t.data(), j.bytes,
+                            cudaMemcpyHostToDevice));
+    }
+  } else if (h->cfg.dtype == HF_BF16) {
     std::vector<uint16_t> t(std::max({h->wt_draft_l, h->wt_commit_l, h->wt_out_l}) / 2);
     hf::tile_weights(reinterpret_cast<const uint16_t*>(wd.data()), d.Nd, D, t.data());
     HF_CUDA(h, cudaMemcpy(bptr(h->wt_draft, (size_t)layer * h->wt_draft_l), t.data(), h->wt_draft_l,
@@ -771,10 +905,10 @@ hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
     e1.ld = d.Nd;
     const int M0 = d.L * h->nc_pad, N0 = batch * (d.S + 1), N1 = batch * d.S;
     const int splits =
-        hf::tc_pick_splits((M0 + 127) / 128 * 128 + d.Nd, std::max(N0, N1), d.D);
+        hf::tc_pick_splits((M0 + 127) / 128 * 128 + d.Nd, std::max(N0, N1), d.D, h->q4);
     Scope sc(h, HF_K_ROUND_PROJ, st);
     const bool tm = std::max(N0, N1) > 32;  // wide batch: token-major over the plain weights
-    const bool sk = !tm && (M0 + 127) / 128 + (d.Nd + 127) / 128 > h->num_sms;
+    const bool sk = !tm && !h->q4 && (M0 + 127) / 128 + (d.Nd + 127) / 128 > h->num_sms;
     cudaError_t e =
         tm  ? hf::launch_gemm_tm(feats, d.D, N0, h->w_commit, d.D, d.L * d.Nc,
                                  plain_commit_epi(h, n_accepted), slot_emb, d.D, N1, h->w_draft, d.D,
@@ -786,7 +920,7 @@ hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
                                  /*late_trigger=*/1, st, &sc.count)
             : hf::launch_gemm_tc_grouped(h->wt_commit, M0, h->nc_pad / 128, feats, d.D, N0, ec,
                                          h->wt_draft, d.Nd, slot_emb, d.D, N1, e1, d.D, splits,
-                                         h->err, st, &sc.count, /*late_trigger=*/1);
+                                         h->err, st, &sc.count, /*late_trigger=*/1, h->q4);
     if (e != cudaSuccess) return cuda_fail(h, e, "grouped projection launch");
   }
   // 2. state update; at large batch also the layer-0 memory read of the new

@@ -6,7 +6,7 @@ import numpy as np
 import torch
 
 from oracle import hyflash_oracle as O
-from workload import make_layer_weights
+from workload import make_layer_weights, make_layer_weights_q4
 
 # Tolerances: max-normalised error |g - r|_inf / |r|_inf per compared tensor.
 TOL = {"f32": 1e-4, "bf16": 2e-2}
@@ -29,12 +29,14 @@ class Pair:
         import speculative_decoding_drafter_hf_gb300 as hf
         self.cfg = cfg
         self.B = cfg.batch if batch is None else batch
-        self.weights = [make_layer_weights(cfg, l, seed) for l in range(cfg.n_layers)]
+        q4 = getattr(cfg, "weight_bits", 16) == 4
+        make = make_layer_weights_q4 if q4 else make_layer_weights
+        self.weights = [make(cfg, l, seed) for l in range(cfg.n_layers)]
         if tweak is not None:  # e.g. a slower decay, so that old features still count
             self.weights = [tweak(w) for w in self.weights]
         self.gpu = hf.Drafter(cfg, self.B, prefill_tokens_max=prefill_tokens_max)
         for l, w in enumerate(self.weights):
-            self.gpu.set_weights(l, w)
+            (self.gpu.set_weights_q4 if q4 else self.gpu.set_weights)(l, w)
         self.orc = O.OracleDrafter(cfg, self.weights, self.B) if oracle else None
         self.tol = TOL[cfg.dtype]
 

@@ -25,7 +25,7 @@ def hf():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(hf_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(hf_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(hf):
@@ -42,6 +42,7 @@ def test_config_struct_layout(hf):
     # kind, padding to the int64 alignment
     assert ctypes.sizeof(hf.HfConfig) == 80
     assert hf.HfConfig.mem_horizon.offset == 68 and hf.HfConfig.memory_kind.offset == 72
+    assert hf.HfConfig.weight_bits.offset == 76
     assert ctypes.sizeof(hf.HfLayerWeights) == 12 * ctypes.sizeof(ctypes.c_void_p)
 
 
@@ -57,7 +58,8 @@ def _cfg(hf, **kw):
     ("n_groups", 2), ("n_kv_heads", 3), ("head_dim", 66), ("window", 7), ("chunk", 100),
     ("dtype", 5), ("d_model", 250), ("block", 17), ("d_state", 18), ("max_batch", 0),
     ("prefill_tokens_max", -1), ("ssm_headdim", 130), ("cross_slot_off", 2),
-    ("mem_horizon", -1), ("mem_horizon", 65), ("memory_kind", 2)])
+    ("mem_horizon", -1), ("mem_horizon", 65), ("memory_kind", 2), ("weight_bits", 8),
+    ("weight_bits", 4)])  # (4 bits need a bf16 handle; this one is fp32)
 def test_invalid_config_is_einval_without_cuda(hf, field, value):
     from speculative_decoding_drafter_hf_gb300 import _binding as B
     h = ctypes.c_void_p()

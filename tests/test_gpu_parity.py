@@ -479,3 +479,35 @@ def test_gated_delta_memory(name, batch, lens, api):
     else:
         run_rounds(p, 4 if name == "tiny_fp32" else 3, check_every=1)
     p.close()
+
+
+# ---------------------------------------------------------------- 4-bit weights
+
+@pytest.mark.parametrize("batch,api,lens", [
+    (1, "round", [700]),              # the skinny products read the 4-bit tiles
+    (2, "separate", [5, 700]),
+    (6, "round", [3, 9, 30, 60, 100, 700]),   # wide products: the bf16 dequantisation
+])
+def test_q4_weights(batch, api, lens):
+    """4-bit weights (codes, bf16 group scales, zero points): the on-chip
+    dequantisation of the skinny GEMMs and the host one of the wide paths
+    against the oracle's exact dequantised weights."""
+    cfg = CONFIGS["qwen3_4b_bf16"].replace(batch=batch, prefix=100, weight_bits=4)
+    p = Pair(cfg)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="prefill")
+    if api == "round":
+        run_round_api(p, 3, check_every=1)
+    else:
+        run_rounds(p, 3, check_every=1)
+    p.close()
+
+
+def test_q4_weights_phi4_grouped_and_layers():
+    """Phi-4 widths (164 commit tiles: the grouped 4-bit launch in two waves)
+    and two layers (the later layer's slot projection)."""
+    cfg = CONFIGS["phi4_bf16"].replace(batch=1, prefix=300, weight_bits=4, n_layers=2)
+    p = Pair(cfg)
+    p.prefill([300], make_prefix_feats(cfg, [300]))
+    run_round_api(p, 2, check_every=1)
+    p.close()

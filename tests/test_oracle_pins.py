@@ -538,3 +538,40 @@ def test_gdn_prefill_equals_commits():
     assert rel(a.h, b.h) < 1e-12 and np.array_equal(a.tag, b.tag)
     z = O.commit_layer(lw, cfg, a, rows, 0)
     assert np.array_equal(z.h, a.h)
+
+
+# ---------------------------------------------------------------- 4-bit weights
+
+def test_q4_dequantization_matches_torch_and_bounds():
+    from workload import make_layer_weights_q4
+    cfg = small_cfg(d_model=256, weight_bits=4)
+    wq = make_layer_weights_q4(cfg, 0)
+    m = wq.w_x
+    got = O.dequantize_q4(m)
+    # torch: expand the group parameters over their 128 rows
+    s = m.scales.double().repeat_interleave(128, dim=0)
+    z = m.zeros.double().repeat_interleave(128, dim=0)
+    ref = (s * (m.codes.double() - z)).numpy()
+    assert np.array_equal(got, ref)
+    # values lie on the group's grid and inside [s (0 - z), s (15 - z)]
+    assert np.all(np.abs(got) <= 15 * s.numpy() + 1e-30)
+
+
+def test_q4_round_trip_error_bound():
+    # quantising a matrix to the nearest grid point and dequantising it moves
+    # each entry by at most half a step s/2 (round to nearest)
+    rng = np.random.default_rng(50)
+    w = rng.standard_normal((256, 7)) * 0.02
+    g = np.arange(256) // 128
+    lo = np.stack([w[g == k].min(0) for k in range(2)])
+    hi = np.stack([w[g == k].max(0) for k in range(2)])
+    s = (hi - lo) / 15.0
+    z = np.round(-lo / s)
+    q = np.clip(np.round(w / s[g] + z[g]), 0, 15)
+
+    class M:  # the oracle's input form
+        pass
+    m = M()
+    m.codes, m.scales, m.zeros = q, s, z
+    back = O.dequantize_q4(m)
+    assert np.max(np.abs(back - w) / s[g]) <= 0.5 + 1e-9

@@ -9,6 +9,9 @@ from .synth import (  # noqa: F401
     DrafterShape,
     LayerWeightsT,
     make_layer_weights,
+    make_layer_weights_q4,
+    LayerWeightsQ4,
+    Q4Matrix,
     make_prefix_feats,
     make_round_inputs,
     make_accepted,

@@ -56,6 +56,8 @@ class DrafterShape:
     # memory kind: "mamba2" (the pages' memory) or "gdn" (gated delta rule,
     # the paper's Gated DeltaNet-2 swap)
     memory: str = "mamba2"
+    # weight precision: 16 (model dtype) or 4 (4-bit codes, group 128)
+    weight_bits: int = 16
 
     @property
     def d_inner(self) -> int:
@@ -154,6 +156,67 @@ def make_layer_weights(cfg: DrafterShape, layer: int, seed: int = 0) -> LayerWei
         dt_bias=torch.full((Hm,), -2.0, dtype=torch.float32),
         A_log=torch.rand((Hm,), generator=g, dtype=torch.float32),
         w_beta=n((D, Hm), 1.0 / math.sqrt(D)),   # drawn last: earlier draws unchanged
+    )
+
+
+@dataclasses.dataclass
+class Q4Matrix:
+    """A 4-bit weight of shape [in, out]: codes uint8 [in, out] in 0..15,
+    scales bf16 [in/128, out], zeros uint8 [in/128, out] in 0..15."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    zeros: torch.Tensor
+
+
+@dataclasses.dataclass
+class LayerWeightsQ4:
+    """Per-layer 4-bit weights (the matrices of LayerWeightsT as Q4Matrix);
+    dt_bias and A_log fp32."""
+    w_q: Q4Matrix
+    w_k: Q4Matrix
+    w_v: Q4Matrix
+    w_o: Q4Matrix
+    w_x: Q4Matrix
+    w_B: Q4Matrix
+    w_C: Q4Matrix
+    w_dt: Q4Matrix
+    w_mo: Q4Matrix
+    dt_bias: torch.Tensor
+    A_log: torch.Tensor
+    w_beta: Q4Matrix = None
+
+    MATRICES = ("w_q", "w_k", "w_v", "w_o", "w_x", "w_B", "w_C", "w_dt", "w_mo", "w_beta")
+
+
+def make_layer_weights_q4(cfg: DrafterShape, layer: int, seed: int = 0) -> LayerWeightsQ4:
+    """Random 4-bit weights with the same spread as the bf16 ones: codes
+    uniform in 0..15, zero points 7 or 8, and per (group of 128 inputs,
+    output) a scale drawn around std / 4.6 (the std of code - zero), rounded
+    to bf16."""
+    g = rng("weights_q4", cfg.name, seed, layer)
+    D, hq, hkv, dh = cfg.d_model, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    din, N, Hm = cfg.d_inner, cfg.d_state, cfg.ssm_heads
+
+    def m(shape, std):
+        i, o = shape
+        codes = torch.randint(0, 16, (i, o), generator=g, dtype=torch.uint8)
+        zeros = torch.randint(7, 9, (i // 128, o), generator=g, dtype=torch.uint8)
+        scales = (torch.rand((i // 128, o), generator=g) * 0.4 + 0.8) * (std / 4.6)
+        return Q4Matrix(codes, scales.to(torch.bfloat16).contiguous(), zeros)
+
+    return LayerWeightsQ4(
+        w_q=m((D, hq * dh), 0.02),
+        w_k=m((D, hkv * dh), 0.02),
+        w_v=m((D, hkv * dh), 0.02),
+        w_o=m((hq * dh, D), 0.02),
+        w_x=m((D, din), 0.02),
+        w_B=m((D, N), (1.0 / 16.0) / math.sqrt(D)),
+        w_C=m((D, N), (1.0 / 16.0) / math.sqrt(D)),
+        w_dt=m((D, Hm), 1.0 / math.sqrt(D)),
+        w_mo=m((din, D), 0.02),
+        dt_bias=torch.full((Hm,), -2.0, dtype=torch.float32),
+        A_log=torch.rand((Hm,), generator=g, dtype=torch.float32),
+        w_beta=m((D, Hm), 1.0 / math.sqrt(D)),
     )
 
 
