@@ -91,6 +91,24 @@ class Pair:
                 e = maxnorm_err(state[l, b], c.h)
                 assert e <= self.tol, f"{what}: state err {e:.3e} (layer {l}, request {b})"
                 worst = max(worst, e)
+                M = int(getattr(cfg, "mem_horizon", 0) or 0)
+                if M > 1 and c.hist is not None and len(c.hist[0]):
+                    # memory-input ring: rows of the last M committed positions
+                    hx, hB, hdt = c.hist
+                    mx, mb, mdt = (g.read(hf.Tensor.MEM_X), g.read(hf.Tensor.MEM_B),
+                                   g.read(hf.Tensor.MEM_DT))
+                    Mr = M + cfg.block + 1
+                    first = c.pos - len(hx)
+                    rows = [(q - first, q % Mr) for q in range(first, c.pos)]
+                    for name, gg, rr in (
+                            ("x", np.stack([mx[l, b, r] for _, r in rows]),
+                             np.stack([hx[i].reshape(-1) for i, _ in rows])),
+                            ("B", np.stack([mb[l, b, r] for _, r in rows]),
+                             np.stack([hB[i] for i, _ in rows])),
+                            ("dt", np.stack([mdt[l, b, :, r] for _, r in rows]),
+                             np.stack([hdt[i] for i, _ in rows]))):
+                        e = maxnorm_err(gg, rr)
+                        assert e <= self.tol, f"{what}: memory-input {name} err {e:.3e} (layer {l}, request {b})"
                 valid = c.tag >= 0
                 if valid.any():
                     for name, gr, orr in (("K", rk, c.ring_k), ("V", rv, c.ring_v)):

@@ -315,13 +315,16 @@ def test_round_api(name, batch, rounds):
     p.close()
 
 
-def test_round_api_rejected_and_invalid_counts():
+@pytest.mark.parametrize("variant", [
+    {}, {"memory": "gdn"}, {"mem_horizon": 3}, {"mem_horizon": 512}, {"cross_slot": False},
+    {"weight_bits": 4}])
+def test_round_api_rejected_and_invalid_counts(variant):
     """Zero, full and invalid accepted counts through hf_round: invalid ones
     leave the request untouched, raise EDEVICE, and the draft still reads the
-    (unchanged) state."""
+    (unchanged) state -- for the default layer and every optional mode."""
     import speculative_decoding_drafter_hf_gb300 as hf
-    cfg = CONFIGS["qwen3_4b_bf16"].replace(batch=3)
-    p = Pair(cfg)
+    cfg = CONFIGS["qwen3_4b_bf16"].replace(batch=3, **variant)
+    p = Pair(cfg, tweak=slow_decay(-6.0) if variant.get("mem_horizon") else None)
     lens = [700, 40, 1500]
     p.prefill(lens, make_prefix_feats(cfg, lens))
     slot, feats = make_round_inputs(cfg, 0, p.B)
