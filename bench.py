@@ -202,9 +202,11 @@ def measured_traffic(workload: str, family: str):
             t = _json.load(fh)
     except (OSError, ValueError):
         return None
-    if t.get("kernel_sources_sha256") != kernel_sources_digest():
+    # one capture per workload, keyed by the sources it was taken with
+    w = t.get("workloads", {}).get(workload, {})
+    if w.get("kernel_sources_sha256") != kernel_sources_digest():
         return None
-    return t.get("per_launch_bytes", {}).get(workload, {}).get(family)
+    return w.get("per_launch_bytes", {}).get(family)
 
 
 def prefill_flops(cfg, total_tokens: int, ring_rows: int) -> float:

@@ -347,8 +347,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       const float x = RES_ROWS > 0 ? ep_res[nl * 128 + m_local]
                                    : to_f(__ldcg(&static_cast<const __nv_bfloat16*>(epi.resid)[i]));
       static_cast<__nv_bfloat16*>(epi.out_t)[i] = __float2bfloat16_rn(x + val);
-    } else {
+    } else if (epi.kind == EPI_SSM_KV) {
       ssm_store<__nv_bfloat16>(epi, scol, n, ep_p[nl], val);
+    } else {  // any other epilogue: element (row n, column m)
+      epi_apply<__nv_bfloat16>(epi, n, m, val);
     }
   };
   if (a.splits == 1) {

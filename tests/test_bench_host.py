@@ -106,7 +106,8 @@ def test_traffic_only_for_unchanged_kernels(tmp_path, monkeypatch):
     real = bench.kernel_sources_digest()
     for digest, want in ((real, 123), ("0" * 64, None)):
         (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
-            {"kernel_sources_sha256": digest, "per_launch_bytes": {"w": {"round_proj": 123}}}))
+            {"workloads": {"w": {"kernel_sources_sha256": digest,
+                                 "per_launch_bytes": {"round_proj": 123}}}}))
         monkeypatch.setattr(bench, "ROOT", str(tmp_path))
         monkeypatch.setattr(bench, "kernel_sources_digest", lambda: real)
         assert bench.measured_traffic("w", "round_proj") == want

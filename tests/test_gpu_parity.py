@@ -437,6 +437,7 @@ def test_cross_slot_off(name, batch):
     ("tiny_fp32", 2, 64, [10, 500]),            # horizon = window
     ("qwen3_4b_bf16", 2, 1, [3, 700]),
     ("qwen3_4b_bf16", 2, 512, [300, 1200]),     # the paper's "last 512"
+    ("qwen3_4b_bf16", 2, 20, [5, 20]),          # 25 window rows: the skinny prefill GEMM
 ])
 def test_memory_horizon(name, batch, horizon, lens):
     """Memory restricted to the last M committed features (prefill folds the
