@@ -10,6 +10,10 @@ from .synth import (  # noqa: F401
     LayerWeightsT,
     make_layer_weights,
     make_layer_weights_q4,
+    make_block_weights,
+    make_head_weights,
+    BlockWeightsT,
+    HeadWeightsT,
     LayerWeightsQ4,
     Q4Matrix,
     make_prefix_feats,

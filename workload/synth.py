@@ -58,6 +58,9 @@ class DrafterShape:
     memory: str = "mamba2"
     # weight precision: 16 (model dtype) or 4 (4-bit codes, group 128)
     weight_bits: int = 16
+    # full drafter block around the layer (MLP width, LM-head vocabulary)
+    mlp_dim: int = 0
+    vocab: int = 0
 
     @property
     def d_inner(self) -> int:
@@ -217,6 +220,63 @@ def make_layer_weights_q4(cfg: DrafterShape, layer: int, seed: int = 0) -> Layer
         dt_bias=torch.full((Hm,), -2.0, dtype=torch.float32),
         A_log=torch.rand((Hm,), generator=g, dtype=torch.float32),
         w_beta=m((D, Hm), 1.0 / math.sqrt(D)),
+    )
+
+
+@dataclasses.dataclass
+class BlockWeightsT:
+    """One full drafter block: the layer's weights plus the norms' gains, the
+    memory's gate / skip / convolution and the MLP ([in, out] row-major)."""
+    layer: LayerWeightsT
+    g_mix: torch.Tensor
+    g_mlp: torch.Tensor
+    w_z: torch.Tensor
+    d_skip: torch.Tensor
+    conv_w: torch.Tensor
+    conv_b: torch.Tensor
+    w_gate: torch.Tensor
+    w_up: torch.Tensor
+    w_down: torch.Tensor
+
+
+@dataclasses.dataclass
+class HeadWeightsT:
+    g_final: torch.Tensor
+    w_lm: torch.Tensor
+
+
+def make_block_weights(cfg: DrafterShape, layer: int, seed: int = 0) -> BlockWeightsT:
+    """The layer's weights (the same draws as make_layer_weights) and the
+    block's extra parts: gains ~1 + N(0, 0.1), W_z and the MLP ~N(0, 0.02),
+    D ~U(0, 1), conv taps ~N(0, 1/2) and bias ~N(0, 0.1) (conv width 4)."""
+    g = rng("block", cfg.name, seed, layer)
+    D, din, N, Hm, F = cfg.d_model, cfg.d_inner, cfg.d_state, cfg.ssm_heads, cfg.mlp_dim
+
+    def n(shape, std):
+        return _round(torch.randn(shape, generator=g) * std, cfg)
+
+    def f32(t):
+        return t.to(torch.float32).contiguous()
+
+    return BlockWeightsT(
+        layer=make_layer_weights(cfg, layer, seed),
+        g_mix=f32(1.0 + 0.1 * torch.randn((D,), generator=g)),
+        g_mlp=f32(1.0 + 0.1 * torch.randn((D,), generator=g)),
+        w_z=n((D, din), 0.02),
+        d_skip=f32(torch.rand((Hm,), generator=g)),
+        conv_w=f32(torch.randn((din + N, 4), generator=g) * 0.5),
+        conv_b=f32(torch.randn((din + N,), generator=g) * 0.1),
+        w_gate=n((D, F), 0.02),
+        w_up=n((D, F), 0.02),
+        w_down=n((F, D), 0.02),
+    )
+
+
+def make_head_weights(cfg: DrafterShape, seed: int = 0) -> HeadWeightsT:
+    g = rng("head", cfg.name, seed)
+    return HeadWeightsT(
+        g_final=(1.0 + 0.1 * torch.randn((cfg.d_model,), generator=g)).to(torch.float32),
+        w_lm=_round(torch.randn((cfg.d_model, cfg.vocab), generator=g) * 0.02, cfg),
     )
 
 
