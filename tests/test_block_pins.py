@@ -160,3 +160,130 @@ def test_block_drafter_runs_rounds():
         assert np.all((tok >= 0) & (tok < cfg.vocab))
         d.commit(feats, make_accepted(cfg, r, 2))
     assert [c.pos for c in d.ctx[1]] == [d.ctx[1][0].pos] * 2
+
+
+def _torch_rms(x, g):
+    t = torch.tensor(x)
+    return torch.nn.functional.rms_norm(t, (t.shape[-1],), torch.tensor(g), eps=FB.EPS)
+
+
+def test_skip_and_gate_with_empty_memory():
+    """B4 with h = 0 (nothing committed): the memory branch is
+    (D[head] * x_s) * silu(z_s) per channel, taken through W_mo. Checked
+    against torch (rms_norm, silu, matmuls) with distinct D per head and a
+    random W_mo, so that a gate on the other side of W_mo, D per channel, or
+    silu on x instead of z all fail."""
+    cfg = TINY
+    bw = _block(cfg)
+    rng = np.random.default_rng(67)
+    lw = bw.layer
+    lw.w_o = np.zeros_like(lw.w_o)        # attention branch off
+    bw.w_down = np.zeros_like(bw.w_down)  # MLP off
+    bw.d_skip = np.array([0.3, -1.2, 2.0, 0.7])
+    assert bw.d_skip.shape == (cfg.ssm_heads,)
+    ctx = FB.BlockContext.empty(cfg)      # h = 0: C h vanishes
+    X = rng.standard_normal((7, cfg.d_model))
+    got = FB.block_draft(bw, cfg, ctx, X) - X
+    a = _torch_rms(X, bw.g_mix)
+    xs = a @ torch.tensor(lw.w_x)
+    z = a @ torch.tensor(bw.w_z)
+    D = torch.tensor(bw.d_skip).repeat_interleave(cfg.ssm_headdim)
+    want = ((D * xs) * torch.nn.functional.silu(z)) @ torch.tensor(lw.w_mo)
+    assert rel(got, want.numpy()) < 1e-12
+    # a gate applied after W_mo, or D per channel index mod heads, differs
+    wrong = (D * xs) @ torch.tensor(lw.w_mo) * torch.nn.functional.silu(z[:, :cfg.d_model])
+    assert rel(got, wrong.numpy()) > 1e-2
+    Dw = torch.tensor(bw.d_skip)[torch.arange(cfg.d_inner) % cfg.ssm_heads]
+    wrong2 = ((Dw * xs) * torch.nn.functional.silu(z)) @ torch.tensor(lw.w_mo)
+    assert rel(got, wrong2.numpy()) > 1e-2
+
+
+def test_gated_read_with_state_and_no_skip():
+    """B4 with a folded memory and D = 0: the branch is (C_s h) * silu(z_s)
+    per channel, with C_s h written out as torch einsum over the state the
+    fold left (the fold itself is pinned against the recurrence)."""
+    cfg = TINY
+    bw = _block(cfg)
+    lw = bw.layer
+    lw.w_o = np.zeros_like(lw.w_o)
+    bw.w_down = np.zeros_like(bw.w_down)
+    bw.d_skip = np.zeros_like(bw.d_skip)
+    rng = np.random.default_rng(68)
+    ctx = FB.block_prefill(bw, cfg, rng.standard_normal((40, cfg.d_model)))
+    assert np.max(np.abs(ctx.h)) > 0
+    X = rng.standard_normal((7, cfg.d_model))
+    got = FB.block_draft(bw, cfg, ctx, X) - X
+    a = _torch_rms(X, bw.g_mix)
+    C = a @ torch.tensor(lw.w_C)                                   # [S, N]
+    y = torch.einsum("hpn,sn->shp", torch.tensor(ctx.h), C).reshape(7, -1)
+    want = (y * torch.nn.functional.silu(a @ torch.tensor(bw.w_z))) @ torch.tensor(lw.w_mo)
+    assert rel(got, want.numpy()) < 1e-12
+
+
+def test_swiglu_mlp_matches_torch():
+    """B5: with both mixer branches off, out = X + W_down(silu(n W_gate) *
+    (n W_up)) with n = rms_norm(X, g_mlp); torch silu / rms_norm / matmuls.
+    Swapping gate and up, or leaving out the norm, fails."""
+    cfg = TINY
+    bw = _block(cfg)
+    lw = bw.layer
+    lw.w_o = np.zeros_like(lw.w_o)
+    lw.w_mo = np.zeros_like(lw.w_mo)
+    rng = np.random.default_rng(69)
+    ctx = FB.block_prefill(bw, cfg, rng.standard_normal((10, cfg.d_model)))
+    X = 3.0 * rng.standard_normal((7, cfg.d_model))
+    got = FB.block_draft(bw, cfg, ctx, X)
+    n = _torch_rms(X, bw.g_mlp)
+    silu = torch.nn.functional.silu
+    G, U, Dn = (torch.tensor(bw.w_gate), torch.tensor(bw.w_up), torch.tensor(bw.w_down))
+    want = torch.tensor(X) + (silu(n @ G) * (n @ U)) @ Dn
+    assert rel(got, want.numpy()) < 1e-12
+    swapped = torch.tensor(X) + (silu(n @ U) * (n @ G)) @ Dn
+    assert rel(got - X, (swapped - torch.tensor(X)).numpy()) > 1e-2
+    no_norm = torch.tensor(X) + (silu(torch.tensor(X) @ G) * (torch.tensor(X) @ U)) @ Dn
+    assert rel(got - X, (no_norm - torch.tensor(X)).numpy()) > 1e-2
+
+
+def test_swiglu_closed_form_identity_weights():
+    """B5 closed form: D = F, W_gate = W_up = W_down = I and unit gains give
+    out = X + silu(n) * n elementwise."""
+    cfg = TINY.replace(mlp_dim=TINY.d_model)
+    bw = _block(cfg)
+    lw = bw.layer
+    lw.w_o = np.zeros_like(lw.w_o)
+    lw.w_mo = np.zeros_like(lw.w_mo)
+    I = np.eye(cfg.d_model)
+    bw.w_gate, bw.w_up, bw.w_down = I.copy(), I.copy(), I.copy()
+    bw.g_mlp = np.ones(cfg.d_model)
+    X = np.random.default_rng(70).standard_normal((7, cfg.d_model))
+    n = X / np.sqrt(np.mean(X * X, axis=-1, keepdims=True) + FB.EPS)
+    got = FB.block_draft(bw, cfg, FB.BlockContext.empty(cfg), X)
+    assert rel(got, X + n * n / (1.0 + np.exp(-n))) < 1e-13
+
+
+def test_block_fold_with_newest_tap_is_fold_of_silu_inputs():
+    """B3 inside the fold: with conv taps (0, 0, 0, 1) and zero bias the
+    convolution is silu of the newest row, so the memory equals the layer's
+    recurrence over silu(x), silu(B) (torch silu); with a memory that
+    forgets at once (A -> -inf) it is dt_last * silu(x_last) (x) silu(B_last)."""
+    cfg = TINY
+    bw = _block(cfg)
+    lw = bw.layer
+    bw.conv_w = np.zeros_like(bw.conv_w)
+    bw.conv_w[:, 3] = 1.0
+    bw.conv_b = np.zeros_like(bw.conv_b)
+    rng = np.random.default_rng(71)
+    f = rng.standard_normal((25, cfg.d_model))
+    ctx = FB.block_prefill(bw, cfg, f)
+    silu = lambda a: torch.nn.functional.silu(torch.tensor(a)).numpy()
+    x = silu(f @ lw.w_x).reshape(25, cfg.ssm_heads, cfg.ssm_headdim)
+    B = silu(f @ lw.w_B)
+    dt = torch.nn.functional.softplus(torch.tensor(f @ lw.w_dt + lw.dt_bias)).numpy()
+    h = np.zeros_like(ctx.h)
+    for t in range(25):   # h <- exp(dt A) h + dt x (x) B, written out per token
+        h = np.exp(dt[t] * lw.A)[:, None, None] * h + dt[t][:, None, None] * x[t][:, :, None] * B[t][None, None, :]
+    assert rel(ctx.h, h) < 1e-12
+    lw.A_log = np.full_like(lw.A_log, 50.0)     # exp(dt A) underflows to 0
+    ctx = FB.block_prefill(bw, cfg, f)
+    want = dt[-1][:, None, None] * x[-1][:, :, None] * B[-1][None, None, :]
+    assert rel(ctx.h, want) < 1e-12
