@@ -38,7 +38,7 @@ if ROOT not in sys.path:
 
 METRIC = "drafter draft-steps/s and committed tokens/s at 1 GB300; % of HBM/tensor roofline"
 UNIT = "draft-steps/s"
-DEFAULT_CONFIG = "qwen3_4b_bf16"
+DEFAULT_CONFIG = "serving_qwen3_4b_b64"
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -329,7 +329,8 @@ def cpu_sample(cfg, steps: int, warmup: int, budget: float):
     v = done / t * scale if t > 0 else 0.0
     sample = (f"{done} rounds (draft+commit) of {cfg.name} for {sb} of {cfg.batch} requests "
               f"(rate scaled by {sb}/{cfg.batch}), prefixes capped at {ORACLE_PREFIX_CAP} tokens, "
-              f"float64 NumPy, after an untimed oracle prefill and {warmup} warm-up rounds")
+              f"the float64 NumPy oracle as it stands (no fp32 instantiation), after an untimed "
+              f"oracle prefill and {warmup} warm-up rounds")
     return v, acc / t * (1 / scale) if t > 0 else 0.0, done, t, sample
 
 
@@ -602,6 +603,25 @@ def run_hyflash(args, cfg):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
 
+    # ---- the same K steps four more times (L2 flushed), for the median of
+    # five runs, and once with the L2 left warm between steps (steady state)
+    def timed_run(flush_l2: bool) -> float:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            stage(args.warmup + i)
+            if flush_l2:
+                flush.zero_()
+            evs[i][0].record(stream)
+            graph.replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs)
+
+    run_ms = [total_ms] + [timed_run(True) for _ in range(4)]
+    warm_ms = timed_run(False)
+
     # ---- per-family device times: the same rounds through the profiled graph
     for i in range(args.steps):
         stage(args.warmup + i)
@@ -703,6 +723,14 @@ def run_hyflash(args, cfg):
                        **ablation_config(cfg)},
             "committed_tokens_per_s": all_acc / (total_ms_max / 1e3),
             "step_ms_median": statistics.median(step_ms),
+            "runs_l2_flushed": {"runs": len(run_ms),
+                                "median_value": args.steps / (statistics.median(run_ms) / 1e3),
+                                "min_value": args.steps / (max(run_ms) / 1e3),
+                                "max_value": args.steps / (min(run_ms) / 1e3),
+                                "unit": UNIT, "note": "this rank; run 1 is the value's"},
+            "steady_state": {"value": args.steps / (warm_ms / 1e3), "unit": UNIT,
+                             "ms_per_step": warm_ms / args.steps,
+                             "note": "same graph, L2 not flushed between steps (this rank)"},
             "algorithmic": {"step_bytes": alg["step_bytes"],
                             "families": {k: {"bytes_per_step": b, "launches_per_step": n}
                                          for k, (b, n) in fams.items()},

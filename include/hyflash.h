@@ -316,29 +316,63 @@ hf_status hf_profile_read(hf_handle* h, int32_t family, double* total_ms,
 /* Number of kernels this handle has launched since creation. */
 int64_t hf_launch_count(const hf_handle* h);
 
+/* ---- failure detection (tests) ---------------------------------------
+ *
+ * Hooks that let tests drive the error paths without faulting a GPU. */
+
+/* Limit, in clock cycles, of the ring-tile wait of the CUDA-core attention
+ * kernel (the fp32 path of hf_draft / hf_round) of handle h; with h NULL,
+ * of hf_attention_noalloc's ring-tile wait. cycles < 0 restores the default
+ * (about 2 s); 0 makes that wait give up at once, so the kernel takes its
+ * expiry path: it raises the timeout bit, lets its copies land (default
+ * limit), drops its ring tile (the window is left out of that draft) and
+ * returns; hf_sync then reports HF_ETIMEOUT and clears the word. Never
+ * fails. */
+hf_status hf_debug_set_wait_limit(hf_handle* h, int64_t cycles);
+
+/* Make the k-th device allocation made by the library from now on fail as
+ * if the device were out of memory (k >= 1; 0 switches it off). hf_create
+ * then returns HF_ENOMEM and frees whatever it had allocated. Process-wide. */
+hf_status hf_debug_fail_alloc(int64_t k);
+
+/* Every device buffer of a handle sits between two 256-byte guard regions
+ * filled with 0xA5. Synchronises the device and reads them all back:
+ * HF_OK if intact, HF_EDEVICE naming the first overwritten one. */
+hf_status hf_debug_check_guards(hf_handle* h);
+
 /* ---- allocation-free window attention --------------------------------
  *
- * The pages have no counterpart to this call. It runs the same window+block
- * attention kernels as hf_draft (split over the window, then combined), but
- * it keeps the split partials in one fixed array compiled into the
- * library's device image instead of in memory a handle allocated. It is for
- * callers that cannot allocate device memory when they run the op: a host
- * that gives all of the GPU's memory to its own arena, a serving loop whose
- * memory was sized once at start-up, or code that must not cause the
- * device-wide synchronisation cudaMalloc/cudaFree can bring. This call
- * makes no cudaMalloc, cudaFree or other allocating call.
+ * The pages have no counterpart to this call. It computes the window+block
+ * attention of hf_draft (every slot query of a request over the valid ring
+ * entries and the block's slot keys) with a separate split-combine kernel:
+ * the window is cut into 32-key splits, one CTA each, whose partial results
+ * go to one fixed array compiled into the library's device image (not to
+ * memory a handle allocated), and the last split of each (request, KV head)
+ * to finish combines them in split order. hf_draft itself runs a cluster
+ * kernel that combines on chip; the two agree to rounding.
+ *
+ * It is for callers that cannot allocate device memory when they run the
+ * op: a host that hands all of the GPU's memory to its own arena, a serving
+ * loop whose memory was sized once at start-up, or code that must not
+ * cause the device-wide synchronisation cudaMalloc/cudaFree can bring. This
+ * call makes no cudaMalloc, cudaFree or other allocating call.
  *
  * The fixed array holds 4,194,304 floats (16 MiB) and exists on every GPU
  * that loads the library until the process exits. A call needs
  *   batch * n_kv_heads * ceil(window / 32) * (n_q_heads / n_kv_heads)
  *         * block * (head_dim + 2)
- * floats of it; a larger call returns HF_EINVAL and launches nothing.
+ * floats of it, and batch * n_kv_heads <= 16384; a larger call returns
+ * HF_EINVAL and launches nothing. So does a call whose CTA would need more
+ * shared memory than the device allows per block: about
+ *   (n_q_heads/n_kv_heads) * block * (4 (head_dim + 4) + 4 (32 + block)
+ *     + 4 ceil(window/32)) + 8 (32 + block)(head_dim + 4) + 64 head_dim e
+ * bytes (e = 4 for HF_F32, 2 for HF_BF16) against 232,448 on GB300.
  * All calls share the one array: calls that can overlap on the GPU (other
  * streams, other host threads) race and must be ordered by the caller. Each
  * call rewrites every partial it later reads, so nothing needs clearing.
- * The first call on each device looks up the array's device address (once,
- * with that device current); make that first call before any stream
- * capture.
+ * The first call on each device looks up the array's device address and the
+ * device's shared-memory limit (once, with that device current); make that
+ * first call before any stream capture.
  *
  * Arguments (all buffers DEVICE memory on the current device, caller-owned):
  *   dtype     HF_F32 or HF_BF16: element type of ring_k, ring_v and out.
@@ -351,13 +385,18 @@ int64_t hf_launch_count(const hf_handle* h);
  *   pos       int64 [batch]: committed tokens per request.
  *   out       [batch*block, out_ld]: attention output of head h written to
  *             columns [h*dh, (h+1)*dh) (out_ld >= Hq*dh); other columns kept.
+ *   status    int32, optional (NULL: not reported): if a ring-tile copy does
+ *             not land within the wait limit (about 2 s), the CTA records
+ *             HF_ETIMEOUT's device bit (2) here with an atomic OR, waits once
+ *             more (bounded) for its copies, and leaves its split out of the
+ *             result. The caller zeroes it and reads it when it likes.
  * Errors: HF_EINVAL for bad sizes or pointers (message in
  * hf_last_error(NULL)), HF_ECUDA for a failed launch. */
 hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t n_q_heads,
                                int32_t n_kv_heads, int32_t head_dim, int32_t window,
                                int32_t block, const float* proj, int32_t proj_ld,
                                const void* ring_k, const void* ring_v, const int64_t* pos,
-                               void* out, int32_t out_ld, void* stream);
+                               void* out, int32_t out_ld, int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -128,12 +128,16 @@ hf_profile_read = _sig("hf_profile_read", _st, _h, _i32, ctypes.POINTER(ctypes.c
                        ctypes.POINTER(ctypes.c_int64), _i32)
 hf_launch_count = _sig("hf_launch_count", ctypes.c_int64, _h)
 hf_attention_noalloc = _sig("hf_attention_noalloc", _st, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
-                            _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp)
+                            _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp)
+hf_debug_set_wait_limit = _sig("hf_debug_set_wait_limit", _st, _h, ctypes.c_int64)
+hf_debug_fail_alloc = _sig("hf_debug_fail_alloc", _st, ctypes.c_int64)
+hf_debug_check_guards = _sig("hf_debug_check_guards", _st, _h)
 
 EXPORTED = ("hf_create", "hf_destroy", "hf_set_weights", "hf_set_weights_q4", "hf_prefill", "hf_commit", "hf_draft",
             "hf_round", "hf_sync", "hf_last_error", "hf_status_string", "hf_tensor_bytes", "hf_read_tensor",
             "hf_context_bytes", "hf_export_context", "hf_import_context", "hf_profile_enable",
-            "hf_profile_collect", "hf_profile_read", "hf_launch_count", "hf_attention_noalloc")
+            "hf_profile_collect", "hf_profile_read", "hf_launch_count", "hf_attention_noalloc",
+            "hf_debug_set_wait_limit", "hf_debug_fail_alloc", "hf_debug_check_guards")
 
 
 class HyflashError(RuntimeError):
@@ -379,3 +383,12 @@ class Drafter:
 
     def launch_count(self) -> int:
         return int(hf_launch_count(self._h))
+
+    # -- failure detection (tests)
+    def set_wait_limit(self, cycles: int):
+        """Limit of the CUDA-core attention's ring-tile wait (-1: default)."""
+        self._check(hf_debug_set_wait_limit(self._h, int(cycles)))
+
+    def check_guards(self):
+        """Raise if a guard region around one of the handle's buffers changed."""
+        self._check(hf_debug_check_guards(self._h))

@@ -13,6 +13,7 @@
 // order (deterministic) and writes O. The scratch and tickets live in fixed
 // device arrays (see the end of this file). hf_draft uses the cluster
 // variant in attention_cluster.cu, which keeps the partials on chip.
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -39,7 +40,8 @@ struct AttnArgs {
   float* part_o;        // [B*Hkv*nsplit][R][dh]
   float* part_ml;       // [B*Hkv*nsplit][R][2]
   int* tickets;         // [B*Hkv], left at zero
-  int32_t* err;
+  int32_t* err;         // ERR_TIMEOUT is ORed in here on a wait that gave up
+  long long wait;       // limit (clock cycles) of the ring-tile wait
 };
 
 struct AttnSmem {
@@ -96,9 +98,8 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, uint8_t* sm, int idx
   const long long p = __ldcg(&a.pos[b]);
   const int nv = (int)(p < (long long)d.W ? p : (long long)d.W);
   const int j0 = split * JT;
-  const int nring = max(0, min(nv, j0 + JT) - j0);
+  int nring = max(0, min(nv, j0 + JT) - j0);
   const int nslot = split == 0 ? S : 0;
-  int nk = nring + nslot;
   const size_t rowbase = (size_t)b * S;
   const size_t rb = ((size_t)b * d.Hkv + kvh) * d.W * dh;
 
@@ -113,7 +114,7 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, uint8_t* sm, int idx
       bulk_g2s(stv, static_cast<const T*>(a.ring_v) + rb + (size_t)j0 * dh, bytes, bar);
     }
   }
-  // Query rows (pre-scaled) and the slot keys/values, 16-byte loads.
+  // Query rows (pre-scaled), 16-byte loads.
   const int c4n = dh / 4;
   for (int i = tid; i < R * c4n; i += nthr) {
     const int r = i / c4n, c = (i % c4n) * 4, g = r / S, sl = r % S;
@@ -125,23 +126,17 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, uint8_t* sm, int idx
     x.w *= a.qscale;
     *reinterpret_cast<float4*>(&q[r * dhp + c]) = x;
   }
-  for (int i = tid; i < nslot * c4n; i += nthr) {
-    const int j = i / c4n, c = (i % c4n) * 4;
-    const float* row = a.proj + (rowbase + j) * d.Nd;
-    *reinterpret_cast<float4*>(&k[(nring + j) * dhp + c]) =
-        __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
-    *reinterpret_cast<float4*>(&v[(nring + j) * dhp + c]) =
-        __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
-  }
   __syncthreads();  // barrier initialised before anyone waits on it
   bool ok = true;
-  if (nring > 0) ok = mbar_wait(bar, 0);
+  if (nring > 0) ok = mbar_wait_for(bar, 0, a.wait);
   if (!__syncthreads_and(ok)) {
     if (tid == 0) {
-      atomicOr(a.err, ERR_TIMEOUT);
-      mbar_wait(bar, 0);  // bounded: let the copies land before leaving
+      if (a.err) atomicOr(a.err, ERR_TIMEOUT);
+      // bounded, default limit: let the copies land before the stage buffers
+      // are released (they are not read again on this path)
+      mbar_wait(bar, 0);
     }
-    nk = 0;  // contribute an empty split, keep the ticket count consistent
+    nring = 0;  // the window tile is left out; the slot keys (split 0) stay
   } else if (nring > 0) {
     constexpr int VE = 16 / (int)sizeof(T);
     for (int i = tid; i < nring * dh / VE; i += nthr) {
@@ -157,6 +152,16 @@ __device__ __forceinline__ void attn_cta(const AttnArgs& a, uint8_t* sm, int idx
       }
     }
   }
+  // slot keys/values after the ring rows (split 0 only)
+  for (int i = tid; i < nslot * c4n; i += nthr) {
+    const int j = i / c4n, c = (i % c4n) * 4;
+    const float* row = a.proj + (rowbase + j) * d.Nd;
+    *reinterpret_cast<float4*>(&k[(nring + j) * dhp + c]) =
+        __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
+    *reinterpret_cast<float4*>(&v[(nring + j) * dhp + c]) =
+        __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
+  }
+  const int nk = nring + nslot;
   __syncthreads();
 
   for (int i = tid; i < R * nk; i += nthr) {
@@ -259,18 +264,21 @@ __global__ void __launch_bounds__(THREADS) attn_mem_kernel(AttnArgs a) {
   attn_cta<T>(a, sm, blockIdx.x);
 }
 
-int g_configured_smem = 0;
+constexpr int kMaxDevices = 64;
+// Dynamic shared memory the kernels were opened up to, per device (the
+// attribute is a per-device setting of the function).
+int g_configured_smem[kMaxDevices] = {};
 std::mutex g_config_mu;
 
-cudaError_t ensure_smem(size_t smem) {
+cudaError_t ensure_smem(int dev, size_t smem) {
   std::lock_guard<std::mutex> lock(g_config_mu);
-  if ((int)smem <= g_configured_smem) return cudaSuccess;
+  if ((int)smem <= g_configured_smem[dev]) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(attn_mem_kernel<float>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(attn_mem_kernel<__nv_bfloat16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess) g_configured_smem = (int)smem;
+  if (e == cudaSuccess) g_configured_smem[dev] = (int)smem;
   return e;
 }
 
@@ -301,33 +309,36 @@ constexpr size_t kNoAllocFloats = (size_t)4 << 20;  // 16 MiB of fp32 partials
 constexpr int kNoAllocTickets = 1 << 14;            // (request, KV head) pairs
 static __device__ __align__(256) float g_noalloc_attn_scratch[kNoAllocFloats];
 static __device__ __align__(256) int g_noalloc_attn_tickets[kNoAllocTickets];
-static __device__ int g_noalloc_attn_err;  // bounded-wait expiries (not reported)
 
-constexpr int kMaxDevices = 64;
 struct NoAllocPtrs {
   float* scratch;
   int* tickets;
-  int* err;
+  int smem_optin;  // the device's opt-in shared memory per block
 };
 NoAllocPtrs g_noalloc[kMaxDevices] = {};
 std::mutex g_noalloc_mu;
+// limit of the ring-tile waits (hf_debug_set_wait_limit with no handle)
+std::atomic<long long> g_noalloc_wait{kWaitCycles};
 
 // The arrays' device addresses on the current device, looked up once per
 // device (host code must not use the arrays' names as device pointers).
-cudaError_t noalloc_scratch(NoAllocPtrs* out) {
+cudaError_t noalloc_scratch(int* dev_out, NoAllocPtrs* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc[dev].scratch) {
-    void *p = nullptr, *t = nullptr, *r = nullptr;
+    void *p = nullptr, *t = nullptr;
+    int optin = 0;
     e = cudaGetSymbolAddress(&p, g_noalloc_attn_scratch);
     if (e == cudaSuccess) e = cudaGetSymbolAddress(&t, g_noalloc_attn_tickets);
-    if (e == cudaSuccess) e = cudaGetSymbolAddress(&r, g_noalloc_attn_err);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    g_noalloc[dev] = {static_cast<float*>(p), static_cast<int*>(t), static_cast<int*>(r)};
+    g_noalloc[dev] = {static_cast<float*>(p), static_cast<int*>(t), optin};
   }
+  *dev_out = dev;
   *out = g_noalloc[dev];
   return cudaSuccess;
 }
@@ -340,7 +351,7 @@ extern "C" hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t 
                                           int32_t block, const float* proj, int32_t proj_ld,
                                           const void* ring_k, const void* ring_v,
                                           const int64_t* pos, void* out, int32_t out_ld,
-                                          void* stream) {
+                                          int32_t* status, void* stream) {
   using namespace hf;
   auto bad = [](const char* m) {
     set_thread_error(m);
@@ -362,6 +373,7 @@ extern "C" hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t 
   if (reinterpret_cast<uintptr_t>(proj) % 16 || reinterpret_cast<uintptr_t>(ring_k) % 16 ||
       reinterpret_cast<uintptr_t>(ring_v) % 16)
     return bad("proj, ring_k and ring_v must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(status) % 4) return bad("status must be 4-byte aligned");
   const int nsplit = (window + JT - 1) / JT;
   const long long R = (long long)(n_q_heads / n_kv_heads) * block;
   const long long need = (long long)batch * n_kv_heads * nsplit * R * (head_dim + 2);
@@ -375,44 +387,53 @@ extern "C" hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t 
     set_thread_error(m);
     return HF_EINVAL;
   }
+  Dims d{};
+  d.Hq = n_q_heads;
+  d.Hkv = n_kv_heads;
+  d.dh = head_dim;
+  d.W = window;
+  d.S = block;
+  d.G = n_q_heads / n_kv_heads;
+  d.QD = (int)qd;
+  d.KVD = (int)kvd;
+  d.Nd = proj_ld;
+  d.Nz = out_ld;
+  d.Hm = 1;
+  d.P = 4;
+  d.N = 4;
+  d.esize = dtype == HF_F32 ? 4 : 2;
+  const AttnSmem L = attn_smem(d, d.esize, nsplit);
+  int dev = 0;
   NoAllocPtrs ptrs{};
-  cudaError_t e = noalloc_scratch(&ptrs);
+  cudaError_t e = noalloc_scratch(&dev, &ptrs);
+  if (e == cudaSuccess && L.total > (size_t)ptrs.smem_optin) {
+    char m[240];
+    snprintf(m, sizeof m,
+             "hf_attention_noalloc: a CTA needs %zu bytes of shared memory, the device allows %d "
+             "(it grows with (Hq/Hkv)*block*head_dim and with window/32)",
+             L.total, ptrs.smem_optin);
+    set_thread_error(m);
+    return HF_EINVAL;
+  }
+  if (e == cudaSuccess) e = ensure_smem(dev, L.total);
   if (e == cudaSuccess) {
-    Dims d{};
-    d.Hq = n_q_heads;
-    d.Hkv = n_kv_heads;
-    d.dh = head_dim;
-    d.W = window;
-    d.S = block;
-    d.G = n_q_heads / n_kv_heads;
-    d.QD = (int)qd;
-    d.KVD = (int)kvd;
-    d.Nd = proj_ld;
-    d.Nz = out_ld;
-    d.Hm = 1;
-    d.P = 4;
-    d.N = 4;
-    d.esize = dtype == HF_F32 ? 4 : 2;
-    const AttnSmem L = attn_smem(d, d.esize, nsplit);
-    e = ensure_smem(L.total);
-    if (e == cudaSuccess) {
-      AttnArgs a{};
-      a.d = d;
-      a.B = batch;
-      a.nsplit = nsplit;
-      a.n_attn = batch * n_kv_heads * nsplit;
-      a.qscale = 1.4426950408889634f / sqrtf((float)head_dim);
-      a.proj = proj;
-      a.ring_k = ring_k;
-      a.ring_v = ring_v;
-      a.pos = pos;
-      a.mix = out;
-      a.part_o = ptrs.scratch;
-      a.part_ml = ptrs.scratch + (size_t)a.n_attn * R * head_dim;
-      a.tickets = ptrs.tickets;
-      a.err = ptrs.err;
-      e = launch(dtype, a, (cudaStream_t)stream);
-    }
+    AttnArgs a{};
+    a.d = d;
+    a.B = batch;
+    a.nsplit = nsplit;
+    a.n_attn = batch * n_kv_heads * nsplit;
+    a.qscale = 1.4426950408889634f / sqrtf((float)head_dim);
+    a.proj = proj;
+    a.ring_k = ring_k;
+    a.ring_v = ring_v;
+    a.pos = pos;
+    a.mix = out;
+    a.part_o = ptrs.scratch;
+    a.part_ml = ptrs.scratch + (size_t)a.n_attn * R * head_dim;
+    a.tickets = ptrs.tickets;
+    a.err = status;
+    a.wait = g_noalloc_wait.load();
+    e = launch(dtype, a, (cudaStream_t)stream);
   }
   if (e != cudaSuccess) {
     set_thread_error(cudaGetErrorString(e));
@@ -420,3 +441,7 @@ extern "C" hf_status hf_attention_noalloc(int32_t dtype, int32_t batch, int32_t 
   }
   return HF_OK;
 }
+
+namespace hf {
+void set_noalloc_wait_limit(long long cycles) { g_noalloc_wait.store(cycles); }
+}  // namespace hf

@@ -207,7 +207,7 @@ __device__ __forceinline__ void attn_cta(const Args& a, uint8_t* sm, int idx) {
   }
   __syncthreads();  // barrier initialised before anyone waits on it
   bool ok = true;
-  if (nring > 0) ok = mbar_wait(bar, 0);
+  if (nring > 0) ok = mbar_wait_for(bar, 0, d.wait);
   if (!__syncthreads_and(ok)) {
     if (tid == 0) {
       atomicOr(a.err, ERR_TIMEOUT);

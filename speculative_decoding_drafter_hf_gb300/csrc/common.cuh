@@ -98,13 +98,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase of `parity` to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait for the phase of `parity` to complete within `limit` clock
+// cycles; false on timeout. A limit of 0 gives up before the first poll (its
+// deadline has already passed): the hook the failure-detection tests use to
+// run a kernel's expiry path without any copy going missing.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, long long limit) {
+  if (limit <= 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
+}
+
+// Bounded wait with the default limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitCycles);
 }
 
 // 1-D bulk copy global -> shared (addresses 16-byte aligned, bytes % 16 == 0),
@@ -147,6 +156,8 @@ struct Dims {
   int Mh;      // memory horizon: 0 = whole history, M > 0 = last M committed features
   int Mr;      // rows of the memory-input ring (M > 1: M + S + 1, else 0)
   int gdn;     // 1: gated-delta memory (commit columns gain beta: Nc, NS + Hm)
+  long long wait;  // limit (clock cycles) of the CUDA-core attention's ring-tile
+                   // wait: kWaitCycles unless a test shortened it
 };
 
 // ---------------------------------------------------------------- GEMM epilogues
@@ -570,6 +581,9 @@ cudaError_t launch_prefill_decay(const Dims& d, int layer, int T, int ldt, int c
                                  const float* A_log, float* seg_decay, cudaStream_t st);
 // Message reported by hf_last_error(NULL) for calls that have no handle.
 void set_thread_error(const char* msg);
+// limit of hf_attention_noalloc's ring-tile waits (clock cycles; 0 = give up
+// at once, the failure-detection tests' hook)
+void set_noalloc_wait_limit(long long cycles);
 
 cudaError_t launch_prefill_finish(int n_req, const int32_t* lens, const int32_t* reqs,
                                   int64_t* pos, cudaStream_t st);

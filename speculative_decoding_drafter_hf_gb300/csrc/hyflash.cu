@@ -5,6 +5,7 @@
 // call enqueues kernels on the caller's stream; host work is argument
 // checking, pointer arithmetic and grid sizing only.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -26,7 +27,8 @@ struct hf_handle {
   int device = 0;
   Dims d{};
   size_t esz = 4;
-  std::vector<void*> allocs;
+  std::vector<void*> allocs;   // what cudaMalloc returned (guard region first)
+  std::vector<size_t> alloc_bytes;  // usable bytes of each, between its guards
 
   void* w_draft = nullptr;   // [L][Nd][D]
   void* w_commit = nullptr;  // [L][Nc][D]
@@ -136,6 +138,7 @@ Dims make_dims(const hf_config& c) {
   d.xoff = c.cross_slot_off ? 1 : 0;
   d.Mh = c.mem_horizon;
   d.Mr = c.mem_horizon > 1 ? c.mem_horizon + c.block + 1 : 0;
+  d.wait = hf::kWaitCycles;
   return d;
 }
 
@@ -188,18 +191,36 @@ hf_status validate(const hf_config* c, std::string* why) {
   return HF_OK;
 }
 
+// Test hook: the k-th device allocation from now on fails as if the device
+// were out of memory (0: off).
+std::atomic<long long> g_fail_alloc_in{0};
+
+// Every buffer sits between two guard regions of kGuardBytes filled with
+// kGuardByte; hf_debug_check_guards reads them back. The usable part starts
+// kGuardBytes after cudaMalloc's (256-byte aligned) address.
+constexpr size_t kGuardBytes = 256;
+constexpr int kGuardByte = 0xA5;
+
 hf_status dev_alloc(hf_handle* h, void** p, size_t bytes) {
   *p = nullptr;
   if (bytes == 0) bytes = 16;
-  cudaError_t e = cudaMalloc(p, bytes);
+  bytes = (bytes + 255) / 256 * 256;
+  long long k = g_fail_alloc_in.load();
+  while (k > 0 && !g_fail_alloc_in.compare_exchange_weak(k, k - 1)) {
+  }
+  void* base = nullptr;
+  cudaError_t e = k == 1 ? cudaErrorMemoryAllocation : cudaMalloc(&base, bytes + 2 * kGuardBytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    *p = nullptr;
     return fail(h, HF_ENOMEM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed: " +
                                   cudaGetErrorString(e));
   }
-  h->allocs.push_back(*p);
-  e = cudaMemset(*p, 0, bytes);
+  h->allocs.push_back(base);
+  h->alloc_bytes.push_back(bytes);
+  *p = static_cast<char*>(base) + kGuardBytes;
+  e = cudaMemset(base, kGuardByte, kGuardBytes);
+  if (e == cudaSuccess) e = cudaMemset(*p, 0, bytes);
+  if (e == cudaSuccess) e = cudaMemset(static_cast<char*>(*p) + bytes, kGuardByte, kGuardBytes);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemset");
   return HF_OK;
 }
@@ -216,6 +237,7 @@ void free_all(hf_handle* h) {
   h->pool.clear();
   for (void* p : h->allocs) cudaFree(p);
   h->allocs.clear();
+  h->alloc_bytes.clear();
 }
 
 // ---- profiling: events around launches of one family
@@ -1256,5 +1278,42 @@ hf_status hf_profile_read(hf_handle* h, int32_t family, double* total_ms, int64_
 }
 
 int64_t hf_launch_count(const hf_handle* h) { return h ? h->launches : 0; }
+
+hf_status hf_debug_set_wait_limit(hf_handle* h, int64_t cycles) {
+  const long long lim = cycles < 0 ? hf::kWaitCycles : (long long)cycles;
+  if (!h) {
+    hf::set_noalloc_wait_limit(lim);
+    return HF_OK;
+  }
+  h->d.wait = lim;
+  return HF_OK;
+}
+
+hf_status hf_debug_fail_alloc(int64_t k) {
+  if (k < 0) return fail(nullptr, HF_EINVAL, "k must be >= 0");
+  g_fail_alloc_in.store(k);
+  return HF_OK;
+}
+
+hf_status hf_debug_check_guards(hf_handle* h) {
+  if (!h) return HF_EINVAL;
+  HF_CUDA(h, cudaSetDevice(h->device));
+  HF_CUDA(h, cudaDeviceSynchronize());
+  std::vector<unsigned char> g(kGuardBytes);
+  for (size_t i = 0; i < h->allocs.size(); ++i) {
+    const char* base = static_cast<const char*>(h->allocs[i]);
+    for (int side = 0; side < 2; ++side) {
+      const char* at = side == 0 ? base : base + kGuardBytes + h->alloc_bytes[i];
+      HF_CUDA(h, cudaMemcpy(g.data(), at, kGuardBytes, cudaMemcpyDeviceToHost));
+      for (unsigned char c : g)
+        if (c != kGuardByte)
+          return fail(h, HF_EDEVICE,
+                      "guard region " + std::string(side ? "after" : "before") + " buffer " +
+                          std::to_string(i) + " (" + std::to_string(h->alloc_bytes[i]) +
+                          " bytes) was overwritten");
+    }
+  }
+  return HF_OK;
+}
 
 }  // extern "C"

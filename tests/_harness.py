@@ -41,6 +41,7 @@ class Pair:
         self.tol = TOL[cfg.dtype]
 
     def close(self):
+        self.gpu.check_guards()  # no kernel wrote outside its buffers
         self.gpu.close()
 
     def prefill(self, lens, feats, requests=None):

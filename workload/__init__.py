@@ -19,6 +19,7 @@ from .synth import (  # noqa: F401
     make_prefix_feats,
     make_round_inputs,
     make_accepted,
+    make_attention_inputs,
     make_prefix_lens,
     make_ssm_core_inputs,
     rng,

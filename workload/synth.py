@@ -320,6 +320,20 @@ def make_round_inputs(cfg: DrafterShape, rnd: int, batch: Optional[int] = None,
     return _round(slot, cfg), _round(feats, cfg)
 
 
+def make_attention_inputs(cfg: DrafterShape, batch: int, seed: int = 0):
+    """Inputs of the window+block attention on its own: slot projections
+    [batch*block, Hq*dh + 2*Hkv*dh] fp32 (queries | slot keys | slot values,
+    ~N(0,1), the spread of the workloads' projections), window rings
+    [batch, Hkv, W, dh] ~N(0,1) rounded once to the model dtype."""
+    g = rng("attention", cfg.name, seed, batch, cfg.window, cfg.head_dim)
+    qd, kvd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    proj = torch.randn((batch * cfg.block, qd + 2 * kvd), generator=g)
+    shape = (batch, cfg.n_kv_heads, cfg.window, cfg.head_dim)
+    ring_k = _round(torch.randn(shape, generator=g), cfg)
+    ring_v = _round(torch.randn(shape, generator=g), cfg)
+    return proj, ring_k, ring_v
+
+
 def make_accepted(cfg: DrafterShape, rnd: int, batch: Optional[int] = None,
                   seed: int = 0) -> torch.Tensor:
     """Accepted counts per request, uniform integers in 1..block+1 (int32)."""
