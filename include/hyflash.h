@@ -124,7 +124,30 @@ typedef struct {
    * weights dequantised once to bf16. d_model, n_q_heads*head_dim and
    * ssm_heads*ssm_headdim must be multiples of 128. 0 means 16. */
   int32_t weight_bits;
+  /* Full drafter block around the layer (0: the layer alone, as above; 1:
+   * the block). The pages describe each drafter layer's two branches and
+   * name none of the parts around them; the block takes the plainest
+   * reading of the model families they use (Qwen3 targets, Mamba-2):
+   *   a = RMSNorm(X; g_mix)                       (eps 1e-6, one norm for both branches)
+   *   Q, K_s at positions pos + s by rotate-half RoPE (base 1e6); committed
+   *     keys are rotated at their positions when they enter the ring
+   *   the memory's x and B pass Mamba-2's causal depthwise conv1d (width 4,
+   *     bias, SiLU) with the last 3 pre-conv committed rows carried across
+   *     commits; dt is not convolved; the draft-time C is not either
+   *   y_s = (C_s h + D[head] x_s) * silu(z_s), x_s = a W_x, z_s = a W_z
+   *   X1 = X + O W_o + y W_mo;  out = X1 + W_down(silu(n W_gate) * (n W_up)),
+   *     n = RMSNorm(X1; g_mlp)
+   *   hf_draft_tokens: logits = RMSNorm(out; g_final) W_lm and the argmax
+   *     token of every slot (ties to the lowest id).
+   * Weights through hf_set_block_weights and hf_set_head_weights. Needs the
+   * Mamba-2 memory, no memory horizon, weight_bits 16, mlp_dim a multiple
+   * of 8, vocab >= 2. */
+  int32_t block_kind;
+  int32_t mlp_dim;      /* F: SwiGLU width (block only) */
+  int32_t vocab;        /* V: LM-head rows (block only) */
 } hf_config;
+
+enum { HF_LAYER = 0, HF_FULL_BLOCK = 1 };
 
 enum { HF_MEM_MAMBA2 = 0, HF_MEM_GATED_DELTA = 1 };
 
@@ -147,6 +170,23 @@ typedef struct {
   const float* A_log;
   const void* w_beta;  /* [D, Hm]: gated-delta writing strength (NULL otherwise) */
 } hf_layer_weights;
+
+/* The block's parts around one layer (block_kind = HF_FULL_BLOCK), HOST
+ * pointers, row-major [in, out]: gains g_mix, g_mlp fp32 [D]; w_z [D, Hm*P]
+ * (model dtype); d_skip fp32 [Hm]; conv_w fp32 [Hm*P + N, 4] (tap 3 on the
+ * newest row) and conv_b fp32 [Hm*P + N] over the x | B channels; w_gate,
+ * w_up [D, F], w_down [F, D] (model dtype). */
+typedef struct {
+  const float* g_mix;
+  const float* g_mlp;
+  const void* w_z;
+  const float* d_skip;
+  const float* conv_w;
+  const float* conv_b;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+} hf_block_weights;
 
 /* One 4-bit matrix of hf_layer_weights_q4, HOST pointers, for a weight of
  * shape [in, out] (in a multiple of 128): codes uint8 [in, out] with values
@@ -185,6 +225,16 @@ hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w)
  * the bf16 dequantisation of the others. Synchronises. */
 hf_status hf_set_weights_q4(hf_handle* h, int32_t layer, const hf_layer_weights_q4* w);
 
+/* A block handle's weights of one layer: the layer's (as hf_set_weights)
+ * and the block's parts around it. HOST pointers; synchronises. HF_EINVAL on
+ * a handle without the block (and hf_set_weights is refused on one with it). */
+hf_status hf_set_block_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w,
+                               const hf_block_weights* bw);
+
+/* The LM head of a block handle: g_final fp32 [D], w_lm [D, vocab] in the
+ * model dtype, HOST pointers. Synchronises. */
+hf_status hf_set_head_weights(hf_handle* h, const float* g_final, const void* w_lm);
+
 /* Prefill (fold the committed prefix). feats: DEVICE [sum(lens), D] packed
  * in request order; lens: HOST int32 [n_req], each >= 0; requests: HOST int32
  * [n_req] distinct request slots in 0..max_batch-1, or NULL for 0..n_req-1.
@@ -212,6 +262,13 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted,
  * positions. */
 hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
                    void* stream);
+
+/* hf_draft followed by the LM head (block handles with head weights):
+ * out DEVICE [batch, block, D] as hf_draft, and tokens DEVICE int32
+ * [batch, block]: the argmax of each slot's logits (ties to the lowest
+ * token id); the logits stay readable as HF_T_LOGITS. */
+hf_status hf_draft_tokens(hf_handle* h, const void* slot_emb, void* out, int32_t* tokens,
+                          int32_t batch, void* stream);
 
 /* One serving iteration: commit the verified round (feats, n_accepted as in
  * hf_commit), then draft the next block (slot_emb, out as in hf_draft). The
@@ -252,14 +309,21 @@ typedef enum {
   HF_T_OFFSETS = 5,   /* int32 [max_batch + 1]: packed row offsets of the
                          last commit (entries past its batch are stale) */
   HF_T_DRAFT_PROJ = 6,/* fp32 [max_batch*block, Hq*dh + 2*Hkv*dh + N]: last
-                         layer's slot projections Q|K_s|V_s|C_s, last draft */
+                         layer's slot projections Q|K_s|V_s|C_s, last draft
+                         (full block: + x_s | z_s, Hm*P each; Q and K_s
+                         rotated) */
   HF_T_DRAFT_MIX = 7, /* dtype [max_batch*block, Hq*dh + Hm*P]: last layer's
-                         attention output | memory read y, last draft */
+                         attention output | memory read y, last draft (full
+                         block: y after the skip and the gate) */
   /* memory horizon M > 1 only (0 bytes otherwise); R = M + block + 1 ring
    * rows, committed position t in row t mod R */
   HF_T_MEM_X = 8,     /* fp32 [L, max_batch, R, Hm*P]: x of the last features */
   HF_T_MEM_B = 9,     /* fp32 [L, max_batch, R, N]: B of the last features */
-  HF_T_MEM_DT = 10    /* fp32 [L, max_batch, Hm, R]: dt (after softplus) */
+  HF_T_MEM_DT = 10,   /* fp32 [L, max_batch, Hm, R]: dt (after softplus) */
+  /* full block only (0 bytes otherwise) */
+  HF_T_CONV = 11,     /* fp32 [L, max_batch, 3, Hm*P + N]: last 3 pre-conv
+                         committed x | B rows, oldest first */
+  HF_T_LOGITS = 12    /* fp32 [max_batch*block, vocab]: last hf_draft_tokens */
 } hf_tensor_id;
 
 /* Size in bytes of an inspectable tensor. */
@@ -270,7 +334,8 @@ hf_status hf_tensor_bytes(const hf_handle* h, int32_t which, size_t* bytes);
 hf_status hf_read_tensor(hf_handle* h, int32_t which, void* host_out, size_t bytes);
 
 /* Bytes of the complete drafter context (states, rings, tags, positions,
- * and with a memory horizon M > 1 the x/B/dt rows of the last features):
+ * with a memory horizon M > 1 the x/B/dt rows of the last features, and in
+ * a full block the convolution's carried rows):
  * the fixed-size draft-side memory of all requests and layers. */
 size_t hf_context_bytes(const hf_handle* h);
 
@@ -290,8 +355,11 @@ typedef enum {
   HF_K_COMMIT_PROJ = 4,  /* commit projections + ring append */
   HF_K_COMMIT_STATE = 5, /* sequential memory update */
   HF_K_PREFILL = 6,      /* every prefill kernel */
-  HF_K_OTHER = 7,        /* split-K combine and helpers */
-  HF_K_COUNT = 8
+  HF_K_OTHER = 7,        /* split-K combine and helpers; full block: norms,
+                            RoPE, gate/skip */
+  HF_K_MLP = 8,          /* full block: SwiGLU MLP */
+  HF_K_HEAD = 9,         /* full block: LM head and argmax */
+  HF_K_COUNT = 10
 } hf_kernel_family;
 
 /* Per-kernel-family timing with CUDA events recorded on the launch stream

@@ -6,7 +6,7 @@ only marshals arguments to it. Build the library with
 below load on first use, so the build module stays importable before the
 library exists; using any of them without the library raises ImportError.
 """
-_BINDING_NAMES = ("EXPORTED", "Drafter", "Family", "HfConfig", "HfLayerWeights", "HyflashError",
+_BINDING_NAMES = ("EXPORTED", "Drafter", "Family", "HfBlockWeights", "HfConfig", "HfLayerWeights", "HyflashError",
                   "LIB_PATH", "Status", "Tensor", "make_config")
 
 __all__ = list(_BINDING_NAMES)

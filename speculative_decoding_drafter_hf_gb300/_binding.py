@@ -45,6 +45,8 @@ class Tensor(enum.IntEnum):
     MEM_X = 8
     MEM_B = 9
     MEM_DT = 10
+    CONV = 11
+    LOGITS = 12
 
 
 class Family(enum.IntEnum):
@@ -56,6 +58,8 @@ class Family(enum.IntEnum):
     COMMIT_STATE = 5
     PREFILL = 6
     OTHER = 7
+    MLP = 8
+    HEAD = 9
 
 
 HF_F32, HF_BF16 = 0, 1
@@ -69,7 +73,10 @@ class HfConfig(ctypes.Structure):
                                            ("cross_slot_off", ctypes.c_int32),
                                            ("mem_horizon", ctypes.c_int32),
                                            ("memory_kind", ctypes.c_int32),
-                                           ("weight_bits", ctypes.c_int32)]
+                                           ("weight_bits", ctypes.c_int32),
+                                           ("block_kind", ctypes.c_int32),
+                                           ("mlp_dim", ctypes.c_int32),
+                                           ("vocab", ctypes.c_int32)]
 
 
 WEIGHT_FIELDS = ("w_q", "w_k", "w_v", "w_o", "w_x", "w_B", "w_C", "w_dt", "w_mo",
@@ -79,6 +86,14 @@ MEMORY_KINDS = {"mamba2": 0, "gdn": 1}
 
 class HfLayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_FIELDS]
+
+
+BLOCK_FIELDS = ("g_mix", "g_mlp", "w_z", "d_skip", "conv_w", "conv_b", "w_gate", "w_up", "w_down")
+BLOCK_F32 = ("g_mix", "g_mlp", "d_skip", "conv_w", "conv_b")
+
+
+class HfBlockWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in BLOCK_FIELDS]
 
 
 class HfQ4Matrix(ctypes.Structure):
@@ -129,6 +144,10 @@ hf_profile_read = _sig("hf_profile_read", _st, _h, _i32, ctypes.POINTER(ctypes.c
 hf_launch_count = _sig("hf_launch_count", ctypes.c_int64, _h)
 hf_attention_noalloc = _sig("hf_attention_noalloc", _st, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                             _vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp)
+hf_set_block_weights = _sig("hf_set_block_weights", _st, _h, _i32, ctypes.POINTER(HfLayerWeights),
+                            ctypes.POINTER(HfBlockWeights))
+hf_set_head_weights = _sig("hf_set_head_weights", _st, _h, _vp, _vp)
+hf_draft_tokens = _sig("hf_draft_tokens", _st, _h, _vp, _vp, _vp, _i32, _vp)
 hf_debug_set_wait_limit = _sig("hf_debug_set_wait_limit", _st, _h, ctypes.c_int64)
 hf_debug_fail_alloc = _sig("hf_debug_fail_alloc", _st, ctypes.c_int64)
 hf_debug_check_guards = _sig("hf_debug_check_guards", _st, _h)
@@ -137,7 +156,8 @@ EXPORTED = ("hf_create", "hf_destroy", "hf_set_weights", "hf_set_weights_q4", "h
             "hf_round", "hf_sync", "hf_last_error", "hf_status_string", "hf_tensor_bytes", "hf_read_tensor",
             "hf_context_bytes", "hf_export_context", "hf_import_context", "hf_profile_enable",
             "hf_profile_collect", "hf_profile_read", "hf_launch_count", "hf_attention_noalloc",
-            "hf_debug_set_wait_limit", "hf_debug_fail_alloc", "hf_debug_check_guards")
+            "hf_debug_set_wait_limit", "hf_debug_fail_alloc", "hf_debug_check_guards",
+            "hf_set_block_weights", "hf_set_head_weights", "hf_draft_tokens")
 
 
 class HyflashError(RuntimeError):
@@ -159,7 +179,10 @@ def make_config(shape, max_batch: int, prefill_tokens_max: int = 0) -> HfConfig:
         cross_slot_off=0 if getattr(shape, "cross_slot", True) else 1,
         mem_horizon=int(getattr(shape, "mem_horizon", 0) or 0),
         memory_kind=MEMORY_KINDS[getattr(shape, "memory", "mamba2") or "mamba2"],
-        weight_bits=int(getattr(shape, "weight_bits", 16) or 16))
+        weight_bits=int(getattr(shape, "weight_bits", 16) or 16),
+        block_kind=1 if getattr(shape, "full_block", False) else 0,
+        mlp_dim=int(getattr(shape, "mlp_dim", 0) or 0) if getattr(shape, "full_block", False) else 0,
+        vocab=int(getattr(shape, "vocab", 0) or 0) if getattr(shape, "full_block", False) else 0)
 
 
 def _stream_ptr(stream) -> Optional[int]:
@@ -232,6 +255,53 @@ class Drafter:
             keep.append(t)
             setattr(lw, name, t.data_ptr())
         self._check(hf_set_weights(self._h, layer, ctypes.byref(lw)))
+
+    def _layer_struct(self, w, keep):
+        import torch
+        lw = HfLayerWeights()
+        for name in WEIGHT_FIELDS:
+            t = getattr(w, name, None)
+            if t is None:  # optional (w_beta outside the gated-delta memory)
+                continue
+            want = torch.float32 if name in ("dt_bias", "A_log") else self.torch_dtype
+            t = t.detach().to("cpu", want).contiguous()
+            keep.append(t)
+            setattr(lw, name, t.data_ptr())
+        return lw
+
+    def set_block_weights(self, layer: int, bw):
+        """Full block: the layer's weights (bw.layer) and the parts around it."""
+        import torch
+        keep = []
+        lw = self._layer_struct(bw.layer, keep)
+        b = HfBlockWeights()
+        for name in BLOCK_FIELDS:
+            want = torch.float32 if name in BLOCK_F32 else self.torch_dtype
+            t = getattr(bw, name).detach().to("cpu", want).contiguous()
+            keep.append(t)
+            setattr(b, name, t.data_ptr())
+        self._check(hf_set_block_weights(self._h, layer, ctypes.byref(lw), ctypes.byref(b)))
+
+    def set_head_weights(self, hw):
+        import torch
+        g = hw.g_final.detach().to("cpu", torch.float32).contiguous()
+        w = hw.w_lm.detach().to("cpu", self.torch_dtype).contiguous()
+        self._check(hf_set_head_weights(self._h, g.data_ptr(), w.data_ptr()))
+
+    def draft_tokens(self, slot_emb, out=None, tokens=None, stream=None):
+        """hf_draft_tokens: (hidden out [B, S, D], tokens int32 [B, S])."""
+        import torch
+        B = int(slot_emb.shape[0])
+        shp = (B, self.shape.block, self.shape.d_model)
+        sp = _dev_ptr(slot_emb, self.torch_dtype, shp, "slot_emb")
+        if out is None:
+            out = torch.empty(shp, dtype=self.torch_dtype, device=slot_emb.device)
+        if tokens is None:
+            tokens = torch.empty((B, self.shape.block), dtype=torch.int32, device=slot_emb.device)
+        op = _dev_ptr(out, self.torch_dtype, shp, "out")
+        tp = _dev_ptr(tokens, torch.int32, (B, self.shape.block), "tokens")
+        self._check(hf_draft_tokens(self._h, sp, op, tp, B, _stream_ptr(stream)))
+        return out, tokens
 
     def set_weights_q4(self, layer: int, w):
         """4-bit weights (weight_bits = 4): each matrix as codes uint8 [in, out],
@@ -338,6 +408,10 @@ class Drafter:
         if which == Tensor.OFFSETS:
             return buf.view(np.int32).copy()
         if which == Tensor.DRAFT_PROJ:
+            return buf.view(np.float32).reshape(Bm * sh.block, -1)
+        if which == Tensor.CONV:
+            return buf.view(np.float32).reshape(L, Bm, 3, -1)
+        if which == Tensor.LOGITS:
             return buf.view(np.float32).reshape(Bm * sh.block, -1)
         if which in (Tensor.MEM_X, Tensor.MEM_B, Tensor.MEM_DT):
             R = int(getattr(sh, "mem_horizon", 0)) + sh.block + 1

@@ -158,6 +158,9 @@ struct Dims {
   int gdn;     // 1: gated-delta memory (commit columns gain beta: Nc, NS + Hm)
   long long wait;  // limit (clock cycles) of the CUDA-core attention's ring-tile
                    // wait: kWaitCycles unless a test shortened it
+  int blk;     // 1: full drafter block (norms, RoPE, conv, gate/skip, MLP, head)
+  int F;       // block: MLP width
+  int V;       // block: LM-head vocabulary
 };
 
 // ---------------------------------------------------------------- GEMM epilogues
@@ -581,6 +584,28 @@ cudaError_t launch_prefill_decay(const Dims& d, int layer, int T, int ldt, int c
                                  const float* A_log, float* seg_decay, cudaStream_t st);
 // Message reported by hf_last_error(NULL) for calls that have no handle.
 void set_thread_error(const char* msg);
+
+// full drafter block (block.cu)
+cudaError_t launch_rms_norm(int dtype, const void* x, const float* g, void* y, int rows, int D,
+                            cudaStream_t st);
+cudaError_t launch_rope_slots(const Dims& d, int rows, float* proj, const int64_t* pos,
+                              const double* inv, cudaStream_t st);
+cudaError_t launch_gate_skip(int dtype, const Dims& d, int rows, void* mix, const float* proj,
+                             const float* d_skip, cudaStream_t st);
+cudaError_t launch_swiglu(int dtype, int rows, int F, const float* h, void* act, cudaStream_t st);
+cudaError_t launch_argmax(int rows, int V, const float* logits, int32_t* tokens, cudaStream_t st);
+cudaError_t launch_commit_prep(int dtype, const Dims& d, int B, const int32_t* n_acc,
+                               const int64_t* pos, void* ring_k, float* xbd, long long xls,
+                               float* conv_state, const float* conv_w, const float* conv_b,
+                               const double* inv, cudaStream_t st);
+cudaError_t launch_ring_rope(int dtype, const Dims& d, int layer, int rows, const int32_t* row_req,
+                             const int64_t* row_pos, void* ring_k, const double* inv,
+                             cudaStream_t st);
+cudaError_t launch_conv_prefill(int dtype, const Dims& d, int Tn, int ldt, const float* U,
+                                float* hist, const float* dtw, const float* conv_w,
+                                const float* conv_b, void* xsT, void* bT, cudaStream_t st);
+cudaError_t launch_conv_reset(const Dims& d, int n_req, const int32_t* reqs, float* conv_state,
+                              cudaStream_t st);
 // limit of hf_attention_noalloc's ring-tile waits (clock cycles; 0 = give up
 // at once, the failure-detection tests' hook)
 void set_noalloc_wait_limit(long long cycles);

@@ -6,6 +6,7 @@
 // checking, pointer arithmetic and grid sizing only.
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -88,6 +89,30 @@ struct hf_handle {
 
   int32_t* err = nullptr;
 
+  // full drafter block (block_kind = 1)
+  float* g_mix = nullptr;      // [L][D]
+  float* g_mlp = nullptr;      // [L][D]
+  float* d_skip = nullptr;     // [L][Hm]
+  float* conv_w = nullptr;     // [L][C][4], C = dinner + N
+  float* conv_b = nullptr;     // [L][C]
+  float* conv_state = nullptr; // [L][Bmax][3][C]: last 3 pre-conv committed rows
+  void* w_up = nullptr;        // [L][2F][D]: W_gate^T rows, then W_up^T rows
+  void* w_down = nullptr;      // [L][D][F]
+  void* wt_up = nullptr;       // bf16 tiles of the same
+  void* wt_down = nullptr;
+  size_t wt_up_l = 0, wt_down_l = 0;
+  float* g_final = nullptr;    // [D]
+  void* w_lm = nullptr;        // [V][D]
+  void* wt_lm = nullptr;
+  int head_set = 0;
+  void* anorm = nullptr;       // [Bmax*S][D]: normed rows (model dtype)
+  void* x1 = nullptr;          // [Bmax*S][D]: X + mixer branches
+  float* mlp_h = nullptr;      // [Bmax*S][2F]: gate | up
+  void* act = nullptr;         // [Bmax*S][F]
+  float* logits = nullptr;     // [Bmax*S][V]
+  float* pf_u = nullptr;       // [Tseg][C]: pre-conv x | B rows of a prefill pass
+  double* rope_inv = nullptr;  // [dh/2]: theta^(-2i/dh)
+
   int prof = 0;                 // 0 off, 1 records read once, 2 records kept (graphs)
   std::vector<ProfRec> pending;  // mode 1
   std::vector<ProfRec> kept;     // mode 2
@@ -139,6 +164,10 @@ Dims make_dims(const hf_config& c) {
   d.Mh = c.mem_horizon;
   d.Mr = c.mem_horizon > 1 ? c.mem_horizon + c.block + 1 : 0;
   d.wait = hf::kWaitCycles;
+  d.blk = c.block_kind == HF_FULL_BLOCK ? 1 : 0;
+  d.F = d.blk ? c.mlp_dim : 0;
+  d.V = d.blk ? c.vocab : 0;
+  if (d.blk) d.Nd += 2 * d.dinner;  // + x_s | z_s (skip and gate of the memory read)
   return d;
 }
 
@@ -182,6 +211,16 @@ hf_status validate(const hf_config* c, std::string* why) {
     if (c->d_model % 128 || ((long long)c->n_q_heads * c->head_dim) % 128 ||
         ((long long)c->ssm_heads * c->ssm_headdim) % 128)
       return bad("4-bit weights need d_model, n_q_heads*head_dim, ssm_heads*ssm_headdim multiples of 128");
+  }
+  if (c->block_kind != HF_LAYER && c->block_kind != HF_FULL_BLOCK)
+    return bad("block_kind must be HF_LAYER or HF_FULL_BLOCK");
+  if (c->block_kind == HF_FULL_BLOCK) {
+    if (c->memory_kind != HF_MEM_MAMBA2 || c->mem_horizon != 0)
+      return bad("the full block takes the Mamba-2 memory without a horizon");
+    if (c->weight_bits == 4) return bad("the full block takes weight_bits 16");
+    if (c->mlp_dim < 8 || c->mlp_dim % 8) return bad("mlp_dim must be a positive multiple of 8");
+    if (c->vocab < 2) return bad("vocab must be >= 2");
+    if (c->head_dim % 2) return bad("head_dim must be even (RoPE pairs)");
   }
   {
     const Dims d = make_dims(*c);
@@ -499,10 +538,48 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
     need = std::max(need, hf::gemm_sk_workspace(d.D, 0, d.Nz, h->num_sms, &tiles, &nslot));
     need = std::max(need, hf::gemm_sk_workspace(d.L * h->nc_pad, d.Nd, d.D, h->num_sms, &tiles, &nslot));
     need = std::max(need, hf::gemm_tm_workspace(h->num_sms));
+    if (d.blk) {
+      need = std::max(need, hf::gemm_sk_workspace(2 * d.F, 0, d.D, h->num_sms, &tiles, &nslot));
+      need = std::max(need, hf::gemm_sk_workspace(d.D, 0, d.F, h->num_sms, &tiles, &nslot));
+      need = std::max(need, hf::gemm_sk_workspace(d.V, 0, d.D, h->num_sms, &tiles, &nslot));
+    }
     h->skws_floats = need;
     A((void**)&h->skws, need * 4);
   }
   if (d.gdn) A((void**)&h->gdn_xs, (size_t)h->pf_tokens * d.NS * 4);
+  if (d.blk) {
+    const size_t C = d.dinner + d.N, rows = Bm * d.S;
+    A((void**)&h->g_mix, L * d.D * 4);
+    A((void**)&h->g_mlp, L * d.D * 4);
+    A((void**)&h->d_skip, L * d.Hm * 4);
+    A((void**)&h->conv_w, L * C * 4 * 4);
+    A((void**)&h->conv_b, L * C * 4);
+    A((void**)&h->conv_state, L * Bm * 3 * C * 4);
+    A(&h->w_up, L * 2 * d.F * d.D * es);
+    A(&h->w_down, L * d.D * d.F * es);
+    A((void**)&h->g_final, d.D * 4);
+    A(&h->w_lm, (size_t)d.V * d.D * es);
+    if (h->cfg.dtype == HF_BF16) {
+      h->wt_up_l = hf::tiled_bytes(2LL * d.F, d.D);
+      h->wt_down_l = hf::tiled_bytes(d.D, d.F);
+      A(&h->wt_up, L * h->wt_up_l);
+      A(&h->wt_down, L * h->wt_down_l);
+      A(&h->wt_lm, hf::tiled_bytes(d.V, d.D));
+    }
+    A(&h->anorm, rows * d.D * es);
+    A(&h->x1, rows * d.D * es);
+    A((void**)&h->mlp_h, rows * 2 * d.F * 4);
+    A(&h->act, rows * d.F * es);
+    A((void**)&h->logits, rows * d.V * 4);
+    A((void**)&h->pf_u, (size_t)h->pf_tokens * C * 4);
+    A((void**)&h->rope_inv, (size_t)(d.dh / 2) * 8);
+    if (s == HF_OK) {
+      std::vector<double> inv(d.dh / 2);
+      for (int i = 0; i < d.dh / 2; ++i) inv[i] = std::pow(1e6, -2.0 * i / d.dh);
+      e = cudaMemcpy(h->rope_inv, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) s = cuda_fail(h, e, "cudaMemcpy(rope table)");
+    }
+  }
   A((void**)&h->pf_dtw, (size_t)d.Hm * h->pf_tokens * 4);
   A((void**)&h->pf_decay, (size_t)d.Hm * 4);
   A(&h->pf_xsT, (size_t)d.dinner * h->pf_tokens * es);
@@ -587,12 +664,82 @@ struct Q4Layer {
 };
 
 static hf_status upload_layer(hf_handle* h, int32_t layer, const hf_layer_weights* w,
-                              const hf_layer_weights_q4* q);
+                              const hf_layer_weights_q4* q, const void* w_z = nullptr);
 
 hf_status hf_set_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w) {
   if (!h) return HF_EINVAL;
   if (h->q4) return fail(h, HF_EINVAL, "weight_bits = 4: set the weights with hf_set_weights_q4");
+  if (h->d.blk) return fail(h, HF_EINVAL, "full block: set the weights with hf_set_block_weights");
   return upload_layer(h, layer, w, nullptr);
+}
+
+// Transpose a host [in, out] matrix (element size es) into [out][in] rows.
+static std::vector<char> transposed(const void* src, size_t in, size_t outn, size_t es) {
+  std::vector<char> t(in * outn * es);
+  const char* s = static_cast<const char*>(src);
+  for (size_t i = 0; i < in; ++i)
+    for (size_t o = 0; o < outn; ++o) std::memcpy(&t[(o * in + i) * es], s + (i * outn + o) * es, es);
+  return t;
+}
+
+// Copy a [rows][K] weight (model dtype) and, for bf16 handles, its tiles.
+static hf_status put_weight(hf_handle* h, const std::vector<char>& w, long long rows, long long K,
+                            void* dst, void* tiles) {
+  HF_CUDA(h, cudaMemcpy(dst, w.data(), w.size(), cudaMemcpyHostToDevice));
+  if (tiles) {
+    std::vector<uint16_t> t(hf::tiled_bytes(rows, K) / 2);
+    hf::tile_weights(reinterpret_cast<const uint16_t*>(w.data()), rows, K, t.data());
+    HF_CUDA(h, cudaMemcpy(tiles, t.data(), t.size() * 2, cudaMemcpyHostToDevice));
+  }
+  return HF_OK;
+}
+
+hf_status hf_set_block_weights(hf_handle* h, int32_t layer, const hf_layer_weights* w,
+                               const hf_block_weights* bw) {
+  if (!h) return HF_EINVAL;
+  const Dims& d = h->d;
+  if (!d.blk) return fail(h, HF_EINVAL, "hf_set_block_weights needs a full-block handle");
+  if (!w || !bw || layer < 0 || layer >= d.L) return fail(h, HF_EINVAL, "bad layer or weights");
+  const void* ptrs[] = {bw->g_mix, bw->g_mlp, bw->w_z, bw->d_skip, bw->conv_w,
+                        bw->conv_b, bw->w_gate, bw->w_up, bw->w_down};
+  for (const void* p : ptrs)
+    if (!p) return fail(h, HF_EINVAL, "a block weight pointer is NULL");
+  hf_status s = upload_layer(h, layer, w, nullptr, bw->w_z);
+  if (s != HF_OK) return s;
+  const size_t es = h->esz, D = d.D, F = d.F, C = d.dinner + d.N;
+  HF_CUDA(h, cudaMemcpy(h->g_mix + (size_t)layer * D, bw->g_mix, D * 4, cudaMemcpyHostToDevice));
+  HF_CUDA(h, cudaMemcpy(h->g_mlp + (size_t)layer * D, bw->g_mlp, D * 4, cudaMemcpyHostToDevice));
+  HF_CUDA(h, cudaMemcpy(h->d_skip + (size_t)layer * d.Hm, bw->d_skip, d.Hm * 4, cudaMemcpyHostToDevice));
+  HF_CUDA(h, cudaMemcpy(h->conv_w + (size_t)layer * C * 4, bw->conv_w, C * 4 * 4, cudaMemcpyHostToDevice));
+  HF_CUDA(h, cudaMemcpy(h->conv_b + (size_t)layer * C, bw->conv_b, C * 4, cudaMemcpyHostToDevice));
+  // [W_gate^T ; W_up^T] rows, and W_down^T
+  std::vector<char> up = transposed(bw->w_gate, D, F, es);
+  const std::vector<char> u2 = transposed(bw->w_up, D, F, es);
+  up.insert(up.end(), u2.begin(), u2.end());
+  const std::vector<char> down = transposed(bw->w_down, F, D, es);
+  if ((s = put_weight(h, up, 2 * F, D, bptr(h->w_up, layer * up.size()),
+                      h->wt_up ? bptr(h->wt_up, layer * h->wt_up_l) : nullptr)) != HF_OK)
+    return s;
+  if ((s = put_weight(h, down, D, F, bptr(h->w_down, layer * down.size()),
+                      h->wt_down ? bptr(h->wt_down, layer * h->wt_down_l) : nullptr)) != HF_OK)
+    return s;
+  HF_CUDA(h, cudaDeviceSynchronize());
+  return HF_OK;
+}
+
+hf_status hf_set_head_weights(hf_handle* h, const float* g_final, const void* w_lm) {
+  if (!h) return HF_EINVAL;
+  const Dims& d = h->d;
+  if (!d.blk) return fail(h, HF_EINVAL, "hf_set_head_weights needs a full-block handle");
+  if (!g_final || !w_lm) return fail(h, HF_EINVAL, "a head weight pointer is NULL");
+  HF_CUDA(h, cudaSetDevice(h->device));
+  HF_CUDA(h, cudaMemcpy(h->g_final, g_final, (size_t)d.D * 4, cudaMemcpyHostToDevice));
+  const std::vector<char> lm = transposed(w_lm, d.D, d.V, h->esz);
+  hf_status s = put_weight(h, lm, d.V, d.D, h->w_lm, h->wt_lm);
+  if (s != HF_OK) return s;
+  HF_CUDA(h, cudaDeviceSynchronize());
+  h->head_set = 1;
+  return HF_OK;
 }
 
 // bf16 bits, round to nearest even (finite inputs)
@@ -651,7 +798,7 @@ hf_status hf_set_weights_q4(hf_handle* h, int32_t layer, const hf_layer_weights_
 }
 
 static hf_status upload_layer(hf_handle* h, int32_t layer, const hf_layer_weights* w,
-                              const hf_layer_weights_q4* q) {
+                              const hf_layer_weights_q4* q, const void* w_z) {
   if (!w || layer < 0 || layer >= h->d.L) return fail(h, HF_EINVAL, "bad layer or weights");
   const void* ptrs[] = {w->w_q, w->w_k, w->w_v, w->w_o, w->w_x, w->w_B, w->w_C, w->w_dt, w->w_mo,
                         w->dt_bias, w->A_log};
@@ -674,6 +821,10 @@ static hf_status upload_layer(hf_handle* h, int32_t layer, const hf_layer_weight
   put_t(wd, d.QD, D, w->w_k, D, d.KVD);
   put_t(wd, d.QD + d.KVD, D, w->w_v, D, d.KVD);
   put_t(wd, d.QD + 2 * d.KVD, D, w->w_C, D, d.N);
+  if (d.blk) {  // full block: x_s and z_s of the memory read's skip and gate
+    put_t(wd, d.QD + 2 * d.KVD + d.N, D, w->w_x, D, d.dinner);
+    put_t(wd, d.QD + 2 * d.KVD + d.N + d.dinner, D, w_z, D, d.dinner);
+  }
   put_t(wc, 0, D, w->w_k, D, d.KVD);
   put_t(wc, d.KVD, D, w->w_v, D, d.KVD);
   put_t(wc, 2 * d.KVD, D, w->w_x, D, d.dinner);
@@ -800,6 +951,110 @@ hf_status draft_rest(hf_handle* h, int l, const void* X, void* Y, int batch, int
               h->wt_out ? bptr(h->wt_out, (size_t)l * h->wt_out_l) : nullptr);
 }
 
+// One layer of the full drafter block: X -> Y (rows batch*S).
+//   a = RMSNorm(X; g_mix) -> [Q | K_s | V_s | C_s | x_s | z_s] = a W (fp32)
+//   -> RoPE of Q, K_s at pos + s -> attention O and memory read y
+//   -> y <- (y + D x_s) silu(z_s) -> X1 = X + [O | y] W_out
+//   -> n = RMSNorm(X1; g_mlp) -> [g | u] = n [W_gate | W_up] -> act = silu(g) u
+//   -> Y = X1 + act W_down
+hf_status draft_block_layer(hf_handle* h, int l, const void* X, void* Y, int batch,
+                            cudaStream_t st) {
+  const Dims& d = h->d;
+  const size_t es = h->esz;
+  const int rows = batch * d.S, dt = h->cfg.dtype;
+  cudaError_t e;
+  {
+    Scope sc(h, HF_K_OTHER, st);
+    e = hf::launch_rms_norm(dt, X, h->g_mix + (size_t)l * d.D, h->anorm, rows, d.D, st);
+    sc.count = 1;
+    if (e != cudaSuccess) return cuda_fail(h, e, "rms_norm launch");
+  }
+  hf_status s = draft_proj(h, l, h->anorm, batch, 0, st);
+  if (s != HF_OK) return s;
+  {
+    Scope sc(h, HF_K_OTHER, st);
+    e = hf::launch_rope_slots(d, rows, h->proj, h->pos, h->rope_inv, st);
+    sc.count = 1;
+    if (e != cudaSuccess) return cuda_fail(h, e, "rope launch");
+  }
+  const size_t ring_ls = (size_t)d.Bmax * d.Hkv * d.W * d.dh * es;
+  const size_t state_ls = (size_t)d.Bmax * d.Hm * d.P * d.N;
+  {
+    Scope sc(h, HF_K_ATTN_MEM, st);
+    const CUtensorMap* mk = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l];
+    const CUtensorMap* mv = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l + 1];
+    e = hf::launch_attn_cluster(dt, d, batch, h->proj, bptr(h->ring_k, l * ring_ls),
+                                bptr(h->ring_v, l * ring_ls), h->pos, h->state + l * state_ls,
+                                h->mix, mk, mv, h->err, h->num_sms, 0, 1, st, &sc.count);
+    if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
+  }
+  {
+    Scope sc(h, HF_K_OTHER, st);
+    e = hf::launch_gate_skip(dt, d, rows, h->mix, h->proj, h->d_skip + (size_t)l * d.Hm, st);
+    sc.count = 1;
+    if (e != cudaSuccess) return cuda_fail(h, e, "gate launch");
+  }
+  Epi e2 = epi_base(h);
+  e2.kind = hf::EPI_RESID;
+  e2.resid = X;
+  e2.out_t = h->x1;
+  e2.ld = d.D;
+  s = gemm(h, HF_K_OUT_PROJ, h->mix, d.Nz, bptr(h->w_out, (size_t)l * d.D * d.Nz * es), d.Nz,
+           rows, d.D, d.Nz, e2, st, h->wt_out ? bptr(h->wt_out, (size_t)l * h->wt_out_l) : nullptr);
+  if (s != HF_OK) return s;
+  {
+    Scope sc(h, HF_K_OTHER, st);
+    e = hf::launch_rms_norm(dt, h->x1, h->g_mlp + (size_t)l * d.D, h->anorm, rows, d.D, st);
+    sc.count = 1;
+    if (e != cudaSuccess) return cuda_fail(h, e, "rms_norm launch");
+  }
+  Epi eu = epi_base(h);
+  eu.kind = hf::EPI_F32;
+  eu.out = h->mlp_h;
+  eu.ld = 2 * d.F;
+  s = gemm(h, HF_K_MLP, h->anorm, d.D, bptr(h->w_up, (size_t)l * 2 * d.F * d.D * es), d.D, rows,
+           2 * d.F, d.D, eu, st, h->wt_up ? bptr(h->wt_up, (size_t)l * h->wt_up_l) : nullptr);
+  if (s != HF_OK) return s;
+  {
+    Scope sc(h, HF_K_MLP, st);
+    e = hf::launch_swiglu(dt, rows, d.F, h->mlp_h, h->act, st);
+    sc.count = 1;
+    if (e != cudaSuccess) return cuda_fail(h, e, "swiglu launch");
+  }
+  Epi ed = epi_base(h);
+  ed.kind = hf::EPI_RESID;
+  ed.resid = h->x1;
+  ed.out_t = Y;
+  ed.ld = d.D;
+  return gemm(h, HF_K_MLP, h->act, d.F, bptr(h->w_down, (size_t)l * d.D * d.F * es), d.F, rows,
+              d.D, d.F, ed, st, h->wt_down ? bptr(h->wt_down, (size_t)l * h->wt_down_l) : nullptr);
+}
+
+// The LM head of a block handle: logits = RMSNorm(X; g_final) W_lm, tokens =
+// row argmax (ties to the lowest id).
+hf_status draft_head(hf_handle* h, const void* X, int32_t* tokens, int batch, cudaStream_t st) {
+  const Dims& d = h->d;
+  const int rows = batch * d.S;
+  cudaError_t e;
+  {
+    Scope sc(h, HF_K_OTHER, st);
+    e = hf::launch_rms_norm(h->cfg.dtype, X, h->g_final, h->anorm, rows, d.D, st);
+    sc.count = 1;
+    if (e != cudaSuccess) return cuda_fail(h, e, "rms_norm launch");
+  }
+  Epi el = epi_base(h);
+  el.kind = hf::EPI_F32;
+  el.out = h->logits;
+  el.ld = d.V;
+  hf_status s = gemm(h, HF_K_HEAD, h->anorm, d.D, h->w_lm, d.D, rows, d.V, d.D, el, st, h->wt_lm);
+  if (s != HF_OK) return s;
+  Scope sc(h, HF_K_HEAD, st);
+  e = hf::launch_argmax(rows, d.V, h->logits, tokens, st);
+  sc.count = 1;
+  if (e != cudaSuccess) return cuda_fail(h, e, "argmax launch");
+  return HF_OK;
+}
+
 // Commit-projection epilogue: of the batch*(S+1) rows of every layer only
 // rows t < n_b are kept (ring append at pos_b + t; x, B, dt into xbd).
 Epi commit_epi(const hf_handle* h, const int32_t* n_accepted) {
@@ -874,11 +1129,26 @@ hf_status hf_draft(hf_handle* h, const void* slot_emb, void* out, int32_t batch,
   for (int l = 0; l < d.L; ++l) {
     const void* X = l == 0 ? slot_emb : h->xbuf[(l - 1) % 2];
     void* Y = l == d.L - 1 ? out : h->xbuf[l % 2];
+    if (d.blk) {
+      if ((s = draft_block_layer(h, l, X, Y, batch, st)) != HF_OK) return s;
+      continue;
+    }
     if ((s = draft_proj(h, l, X, batch, tc, st)) != HF_OK) return s;
     if ((s = draft_rest(h, l, X, Y, batch, tc ? kEarlyRing | kEarlyState : 0, 1, st)) != HF_OK)
       return s;
   }
   return HF_OK;
+}
+
+hf_status hf_draft_tokens(hf_handle* h, const void* slot_emb, void* out, int32_t* tokens,
+                          int32_t batch, void* stream) {
+  if (!h) return HF_EINVAL;
+  if (!h->d.blk) return fail(h, HF_EINVAL, "hf_draft_tokens needs a full-block handle");
+  if (!h->head_set) return fail(h, HF_EINVAL, "hf_draft_tokens: set the head weights first");
+  if (!tokens) return fail(h, HF_EINVAL, "NULL buffer");
+  hf_status s = hf_draft(h, slot_emb, out, batch, stream);
+  if (s != HF_OK || batch == 0) return s;
+  return draft_head(h, out, tokens, batch, (cudaStream_t)stream);
 }
 
 hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, int32_t batch,
@@ -900,6 +1170,18 @@ hf_status hf_commit(hf_handle* h, const void* feats, const int32_t* n_accepted, 
            d.L * (tiled ? h->nc_pad : d.Nc), d.D, tiled ? ep : plain_commit_epi(h, n_accepted), st,
            tiled ? h->wt_commit : nullptr, late, h->nc_pad / 128);
   if (s != HF_OK) return s;
+  if (d.blk) {
+    // full block: rotate the appended keys at their positions, convolve the
+    // accepted rows' x | B with the carried rows (in place, before the
+    // state update reads them); signals its dependents after its own wait
+    Scope sc(h, HF_K_COMMIT_STATE, st);
+    cudaError_t e = hf::launch_commit_prep(h->cfg.dtype, d, batch, n_accepted, h->pos, h->ring_k,
+                                           h->xbd, h->xbd_ls, h->conv_state, h->conv_w,
+                                           h->conv_b, h->rope_inv, st);
+    sc.count = 1;
+    if (e != cudaSuccess) return cuda_fail(h, e, "commit prep launch");
+    return commit_state(h, n_accepted, batch, nullptr, 1, 0, st);
+  }
   return commit_state(h, n_accepted, batch, nullptr, late, 0, st);
 }
 
@@ -909,7 +1191,8 @@ hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
   hf_status s = check_commit_args(h, feats, n_accepted, batch);
   if (s == HF_OK) s = check_draft_args(h, slot_emb, out, batch);
   if (s != HF_OK || batch == 0) return s;
-  const bool fused = h->cfg.dtype == HF_BF16 && h->wt_commit && h->wt_draft && !h->ring_maps.empty();
+  const bool fused = h->cfg.dtype == HF_BF16 && h->wt_commit && h->wt_draft &&
+                     !h->ring_maps.empty() && !h->d.blk;
   if (!fused) {
     s = hf_commit(h, feats, n_accepted, batch, stream);
     return s != HF_OK ? s : hf_draft(h, slot_emb, out, batch, stream);
@@ -999,6 +1282,11 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
   cudaError_t e = hf::launch_prefill_reset(d, n_req, h->pf_reqs, h->state, h->tags, h->pos, st);
   sc.count++;
   if (e != cudaSuccess) return cuda_fail(h, e, "prefill reset");
+  if (d.blk) {  // the convolution starts from zero rows
+    e = hf::launch_conv_reset(d, n_req, h->pf_reqs, h->conv_state, st);
+    sc.count++;
+    if (e != cudaSuccess) return cuda_fail(h, e, "prefill conv reset");
+  }
   if (ring_rows > 0) {
     e = hf::launch_prefill_ring_prep(h->cfg.dtype, d, n_req, (int)ring_rows, h->pf_lens,
                                      h->pf_reqs, feats, h->row_req, h->row_pos, h->tags,
@@ -1019,6 +1307,12 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
       e = gemm_launch(h, h->packed, d.D, wl, d.D, (int)ring_rows, 2 * d.KVD, d.D, ek, st,
                       &sc.count);
       if (e != cudaSuccess) return cuda_fail(h, e, "prefill kv gemm");
+      if (d.blk) {  // keys rotated at their positions as they enter the window
+        e = hf::launch_ring_rope(h->cfg.dtype, d, l, (int)ring_rows, h->row_req, h->row_pos,
+                                 h->ring_k, h->rope_inv, st);
+        sc.count++;
+        if (e != cudaSuccess) return cuda_fail(h, e, "prefill ring rope");
+      }
       if (d.Mr > 0) {
         // memory horizon M > 1: x, B, dt of each request's last M features
         // (among the window rows, M <= W) into the memory-input ring
@@ -1092,14 +1386,32 @@ hf_status hf_prefill(hf_handle* h, const void* feats, const int32_t* lens, const
                                      h->pf_decay, st);
         sc.count++;
         if (e != cudaSuccess) return cuda_fail(h, e, "prefill decay scan");
-        Epi e2 = epi_base(h);
-        e2.kind = hf::EPI_XB;
-        e2.dtw = h->pf_dtw;
-        e2.ldt = (int)Tseg;
-        e2.xsT = h->pf_xsT;
-        e2.bT = h->pf_bT;
-        e = tokens_gemm(h, fseg, T, w_xb, nx, e2, st, &sc.count);
-        if (e != cudaSuccess) return cuda_fail(h, e, "prefill x/B gemm");
+        if (d.blk) {
+          // full block: pre-conv x | B rows, then the causal conv1d over the
+          // pass (rows before it from the carried ones) writes w * x and B
+          Epi eu = epi_base(h);
+          eu.kind = hf::EPI_F32;
+          eu.out = h->pf_u;
+          eu.ld = nx;
+          e = tokens_gemm(h, fseg, T, w_xb, nx, eu, st, &sc.count);
+          if (e != cudaSuccess) return cuda_fail(h, e, "prefill x/B gemm");
+          const size_t C = nx;
+          float* hist = h->conv_state + ((size_t)l * d.Bmax + reqs[i]) * 3 * C;
+          e = hf::launch_conv_prefill(h->cfg.dtype, d, T, (int)Tseg, h->pf_u, hist, h->pf_dtw,
+                                      h->conv_w + (size_t)l * C * 4, h->conv_b + (size_t)l * C,
+                                      h->pf_xsT, h->pf_bT, st);
+          sc.count += 2;
+          if (e != cudaSuccess) return cuda_fail(h, e, "prefill conv");
+        } else {
+          Epi e2 = epi_base(h);
+          e2.kind = hf::EPI_XB;
+          e2.dtw = h->pf_dtw;
+          e2.ldt = (int)Tseg;
+          e2.xsT = h->pf_xsT;
+          e2.bT = h->pf_bT;
+          e = tokens_gemm(h, fseg, T, w_xb, nx, e2, st, &sc.count);
+          if (e != cudaSuccess) return cuda_fail(h, e, "prefill x/B gemm");
+        }
         Epi e3 = epi_base(h);
         e3.kind = hf::EPI_STATE;
         e3.st = st_b;
@@ -1161,6 +1473,8 @@ hf_status hf_tensor_bytes(const hf_handle* h, int32_t which, size_t* bytes) {
     case HF_T_MEM_X: *bytes = L * Bm * d.Mr * d.dinner * 4; break;
     case HF_T_MEM_B: *bytes = L * Bm * d.Mr * d.N * 4; break;
     case HF_T_MEM_DT: *bytes = L * Bm * d.Hm * d.Mr * 4; break;
+    case HF_T_CONV: *bytes = d.blk ? L * Bm * 3 * (d.dinner + d.N) * 4 : 0; break;
+    case HF_T_LOGITS: *bytes = d.blk ? Bm * d.S * d.V * 4 : 0; break;
     default: return HF_EINVAL;
   }
   return HF_OK;
@@ -1179,6 +1493,8 @@ static const void* tensor_ptr(const hf_handle* h, int which) {
     case HF_T_MEM_X: return h->mem_x;
     case HF_T_MEM_B: return h->mem_b;
     case HF_T_MEM_DT: return h->mem_dt;
+    case HF_T_CONV: return h->conv_state;
+    case HF_T_LOGITS: return h->logits;
   }
   return nullptr;
 }
@@ -1195,9 +1511,11 @@ hf_status hf_read_tensor(hf_handle* h, int32_t which, void* host_out, size_t byt
 }
 
 // The context: everything a request's drafting depends on (the memory-input
-// rows are empty without a memory horizon M > 1).
+// rows are empty without a memory horizon M > 1, the carried convolution rows
+// outside the full block).
 static const int kContextTensors[] = {HF_T_STATE, HF_T_RING_K, HF_T_RING_V, HF_T_RING_TAG,
-                                      HF_T_POS,   HF_T_MEM_X,  HF_T_MEM_B,  HF_T_MEM_DT};
+                                      HF_T_POS,   HF_T_MEM_X,  HF_T_MEM_B,  HF_T_MEM_DT,
+                                      HF_T_CONV};
 
 size_t hf_context_bytes(const hf_handle* h) {
   if (!h) return 0;

@@ -39,10 +39,13 @@ def test_every_declared_symbol_is_exported(hf):
 
 def test_config_struct_layout(hf):
     # 14 int32, the int64 pass size, two int32 ablation fields, the memory
-    # kind, padding to the int64 alignment
-    assert ctypes.sizeof(hf.HfConfig) == 80
+    # kind, the weight bits, the three block fields, padding to the int64
+    # alignment
+    assert ctypes.sizeof(hf.HfConfig) == 96
     assert hf.HfConfig.mem_horizon.offset == 68 and hf.HfConfig.memory_kind.offset == 72
     assert hf.HfConfig.weight_bits.offset == 76
+    assert hf.HfConfig.block_kind.offset == 80 and hf.HfConfig.vocab.offset == 88
+    assert ctypes.sizeof(hf.HfBlockWeights) == 9 * ctypes.sizeof(ctypes.c_void_p)
     assert ctypes.sizeof(hf.HfLayerWeights) == 12 * ctypes.sizeof(ctypes.c_void_p)
 
 
@@ -94,3 +97,27 @@ def test_gated_delta_with_horizon_is_einval(hf):
     h = ctypes.c_void_p()
     s = B.hf_create(ctypes.byref(_cfg(hf, memory_kind=1, mem_horizon=4)), 0, ctypes.byref(h))
     assert s == hf.Status.EINVAL and not h.value
+
+
+@pytest.mark.parametrize("kw", [
+    dict(block_kind=2),
+    dict(block_kind=1, mlp_dim=0, vocab=10),          # no MLP width
+    dict(block_kind=1, mlp_dim=100, vocab=10),        # not a multiple of 8
+    dict(block_kind=1, mlp_dim=64, vocab=1),          # one-token vocabulary
+    dict(block_kind=1, mlp_dim=64, vocab=10, memory_kind=1),
+    dict(block_kind=1, mlp_dim=64, vocab=10, mem_horizon=3),
+])
+def test_invalid_block_config_is_einval_without_cuda(hf, kw):
+    from speculative_decoding_drafter_hf_gb300 import _binding as B
+    h = ctypes.c_void_p()
+    s = B.hf_create(ctypes.byref(_cfg(hf, **kw)), 0, ctypes.byref(h))
+    assert s == hf.Status.EINVAL and not h.value
+
+
+def test_block_calls_on_null_handle_are_einval(hf):
+    from speculative_decoding_drafter_hf_gb300 import _binding as B
+    assert B.hf_set_block_weights(None, 0, None, None) == hf.Status.EINVAL
+    assert B.hf_set_head_weights(None, None, None) == hf.Status.EINVAL
+    assert B.hf_draft_tokens(None, None, None, None, 1, None) == hf.Status.EINVAL
+    assert B.hf_debug_check_guards(None) == hf.Status.EINVAL
+    assert B.hf_debug_fail_alloc(-1) == hf.Status.EINVAL

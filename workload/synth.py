@@ -58,9 +58,10 @@ class DrafterShape:
     memory: str = "mamba2"
     # weight precision: 16 (model dtype) or 4 (4-bit codes, group 128)
     weight_bits: int = 16
-    # full drafter block around the layer (MLP width, LM-head vocabulary)
+    # full drafter block around the layer (on/off, MLP width, LM-head vocabulary)
     mlp_dim: int = 0
     vocab: int = 0
+    full_block: bool = False
 
     @property
     def d_inner(self) -> int:
