@@ -146,8 +146,29 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
         "commit_proj": (w_commit + commit_io, 1),
         "commit_state": (L * state_rw * state + state_io, 1),
     }
-    step = sum(b for b, _ in fused_fams().values())
     flops = L * 2 * R * D * (Nd + Nz) + 2 * rows * D * L * Nc
+    if getattr(cfg, "full_block", False):
+        # the full block runs hf_commit then hf_draft_tokens: the layer's
+        # products plus x_s | z_s in the slot projection, the norms, the
+        # commit's conv / RoPE pass, the SwiGLU MLP and the LM head
+        F, V = cfg.mlp_dim, cfg.vocab
+        xz = 2 * din
+        fam = {
+            "draft_proj": (L * (we * (Nd + xz) * D + io_draft + 4 * R * xz), L),
+            "attn_mem": (L * (window + state + io_attn + io_mem), L),
+            "out_proj": (L * (w_out + io_out), L),
+            "commit_proj": (w_commit + commit_io, 1),
+            "commit_state": (L * 2 * state + state_io + L * (batch * 6 * (din + N) * 4
+                                                             + rows * 2 * (din + N) * 4), 2),
+            "mlp": (L * (3 * we * D * F + e * R * D + 4 * R * 2 * F * 2 + e * R * F * 2
+                         + 2 * e * R * D), 3 * L),
+            "head": (we * V * D + e * R * D + 4 * R * V * 2 + 4 * R, 2),
+            "other": (L * (2 * 2 * e * R * D + 4 * R * (QD + 2 * hkv * dh) * 2
+                           + 2 * e * R * din + 4 * R * 2 * din) + 2 * e * R * D, 4 * L + 1),
+        }
+        flops += L * 2 * R * D * (xz + 3 * F) + 2 * R * D * V
+        return {"families": fam, "step_bytes": sum(b for b, _ in fam.values()), "step_flops": flops}
+    step = sum(b for b, _ in fused_fams().values())
     return {"families": fam, "step_bytes": step, "step_flops": flops}
 
 
@@ -159,6 +180,10 @@ def layer_weights(cfg, layer: int):
 
 
 def set_layer_weights(drafter, cfg, layer: int):
+    if getattr(cfg, "full_block", False):
+        from workload import make_block_weights
+        drafter.set_block_weights(layer, make_block_weights(cfg, layer))
+        return
     w = layer_weights(cfg, layer)
     (drafter.set_weights_q4 if getattr(cfg, "weight_bits", 16) == 4 else drafter.set_weights)(layer, w)
 
@@ -175,6 +200,10 @@ def ablation_config(cfg) -> dict:
         res["memory"] = "gated delta rule (GDN)"
     if getattr(cfg, "weight_bits", 16) == 4:
         res["weights"] = "4-bit codes, bf16 scale + zero point per 128 inputs (skinny products dequantise on chip)"
+    if getattr(cfg, "full_block", False):
+        res["block"] = {"kind": "full drafter block (pre-norms, RoPE, conv1d, skip/gate, SwiGLU, LM head + argmax)",
+                        "mlp_dim": cfg.mlp_dim, "vocab": cfg.vocab,
+                        "step": "hf_commit then hf_draft_tokens"}
     return res
 
 
@@ -298,8 +327,14 @@ def oracle_rounds(cfg, batch: int, steps: int, warmup: int, budget_s: float, see
     from oracle import hyflash_oracle as O
     from workload import (make_accepted, make_layer_weights, make_prefix_feats,
                           make_prefix_lens, make_round_inputs)
-    weights = [layer_weights(cfg, l) for l in range(cfg.n_layers)]
-    orc = O.OracleDrafter(cfg, weights, batch)
+    if getattr(cfg, "full_block", False):  # the block oracle with its LM head
+        from oracle import full_block as FB
+        from workload import make_block_weights, make_head_weights
+        orc = FB.OracleBlockDrafter(cfg, [make_block_weights(cfg, l) for l in range(cfg.n_layers)],
+                                    make_head_weights(cfg), batch)
+    else:
+        weights = [layer_weights(cfg, l) for l in range(cfg.n_layers)]
+        orc = O.OracleDrafter(cfg, weights, batch)
     lens = [min(L, ORACLE_PREFIX_CAP) for L in make_prefix_lens(cfg)[:batch]]
     orc.prefill(lens, make_prefix_feats(cfg, lens, seed=seed))
     for r in range(warmup):
@@ -469,6 +504,10 @@ def run_hyflash(args, cfg):
     drafter = hf.Drafter(cfg, batch, device=local)
     for l in range(cfg.n_layers):
         set_layer_weights(drafter, cfg, l)
+    block = getattr(cfg, "full_block", False)
+    if block:
+        from workload import make_head_weights
+        drafter.set_head_weights(make_head_weights(cfg))
     lens = make_prefix_lens(cfg, seed=0)[:batch]
     if args.prefix_max:  # smaller prefill (e.g. for profiling); rounds unchanged once windows fill
         lens = [min(L, args.prefix_max) for L in lens]
@@ -505,6 +544,7 @@ def run_hyflash(args, cfg):
     d_feat = torch.stack(commits).to(dev)
     d_cnt = torch.stack(counts).to(dev)
     out = torch.empty((batch, cfg.block, cfg.d_model), dtype=drafter.torch_dtype, device=dev)
+    tokens = torch.empty((batch, cfg.block), dtype=torch.int32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
 
@@ -529,10 +569,13 @@ def run_hyflash(args, cfg):
         st_feat.copy_(d_feat[r])
         st_cnt.copy_(d_cnt[r])
 
-    fused = args.api == "round"
+    fused = args.api == "round" and not block
 
     def round_calls():
-        if fused:  # one serving iteration: commit the verified round, draft the next
+        if block:  # the full block: commit the verified round, draft the next with tokens
+            drafter.commit(st_feat, st_cnt)
+            drafter.draft_tokens(st_slot, out, tokens)
+        elif fused:  # one serving iteration: commit the verified round, draft the next
             drafter.round(st_feat, st_cnt, st_slot, out)
         else:
             drafter.draft(st_slot, out)
@@ -543,7 +586,9 @@ def run_hyflash(args, cfg):
     nvtx = torch.cuda.nvtx
     for r in range(args.warmup):
         stage(r)
-        if fused:
+        if block:
+            round_calls()
+        elif fused:
             nvtx.range_push("round")
             drafter.round(st_feat, st_cnt, st_slot, out)
             nvtx.range_pop()
@@ -646,6 +691,7 @@ def run_hyflash(args, cfg):
         for of, (nb, _, _), src in zip(offs, parts, (d_slot[r], d_feat[r], d_cnt[r])):
             h_blob[r, of:of + nb].copy_(src.cpu().contiguous().view(-1).view(torch.uint8))
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_tok = torch.empty(tokens.shape, dtype=tokens.dtype).pin_memory()
     e2e_ev = []
     barrier()
     torch.cuda.synchronize()
@@ -657,6 +703,8 @@ def run_hyflash(args, cfg):
         st_blob.copy_(h_blob[r], non_blocking=True)  # the step's inputs, one copy
         graph.replay()
         h_out.copy_(out, non_blocking=True)
+        if block:
+            h_tok.copy_(tokens, non_blocking=True)
         b.record(stream)
         e2e_ev.append((a, b))
     torch.cuda.synchronize()
@@ -668,7 +716,7 @@ def run_hyflash(args, cfg):
     e2e_value = all_steps / (e2e_ms / 1e3)
     es = drafter.np_elem
     h2d = sum(nb for nb, _, _ in parts)
-    d2h = h_out.numel() * es
+    d2h = h_out.numel() * es + (h_tok.numel() * 4 if block else 0)
 
     # ---- roofline of the dominant kernel family
     import json as _json
@@ -775,6 +823,13 @@ def main(argv=None):
                     help="memory kind: Mamba-2 (default) or the gated delta rule")
     ap.add_argument("--weight-bits", type=int, default=16, choices=[16, 4],
                     help="weights in the model dtype (16) or 4-bit codes (4)")
+    ap.add_argument("--block", default="layer", choices=["layer", "full"],
+                    help="layer: the HyFlash layer alone; full: the drafter block around it "
+                         "(norms, RoPE, conv1d, skip/gate, SwiGLU MLP, LM head + argmax)")
+    ap.add_argument("--mlp-dim", type=int, default=0,
+                    help="full block: MLP width (0: the target family's, 9728 Qwen3-4B, 17920 Phi-4)")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="full block: LM-head rows (0: the target family's, 151936 / 100352)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -782,6 +837,11 @@ def main(argv=None):
     cfg = CONFIGS[args.config].replace(cross_slot=not args.cross_slot_off,
                                        mem_horizon=args.mem_horizon, memory=args.memory,
                                        weight_bits=args.weight_bits)
+    if args.block == "full":
+        # the target families' MLP widths and vocabularies (Qwen3-4B, Phi-4)
+        fam_mlp, fam_vocab = (17920, 100352) if cfg.d_model == 5120 else (9728, 151936)
+        cfg = cfg.replace(full_block=True, mlp_dim=args.mlp_dim or fam_mlp,
+                          vocab=args.vocab or fam_vocab)
     if args.impl == "reference":
         return run_reference(args, cfg)
     if cfg.rounds == 0:
