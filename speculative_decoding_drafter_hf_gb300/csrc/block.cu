@@ -38,9 +38,9 @@ __device__ __forceinline__ float silu_f(float x) { return x / (1.f + expf(-x)); 
 // and more, where a float angle would be off by ~1e-2 -- then sincosf.
 __device__ __forceinline__ void rope_cs(long long p, int i, const double* inv, float* c,
                                         float* s) {
-  const double two_pi = 6.283185307179586;
+  const double two_pi = 6.283185307179586, inv_two_pi = 0.15915494309189535;
   const double a = (double)p * __ldg(&inv[i]);
-  const float r = (float)(a - two_pi * rint(a / two_pi));
+  const float r = (float)fma(-rint(a * inv_two_pi), two_pi, a);  // no fp64 division
   sincosf(r, s, c);
 }
 
@@ -205,16 +205,19 @@ __global__ void commit_prep_kernel(Dims d, const int32_t* __restrict__ n_acc,
     float* cs = conv_state + (((size_t)l * d.Bmax + b) * (kConvK - 1)) * C + u;
     const float* w = conv_w + ((size_t)l * C + u) * kConvK;
     const float bias = __ldg(&conv_b[(size_t)l * C + u]);
-    float seq[kConvK - 1 + 17];  // block + 1 <= 17 rows
-    for (int k = 0; k < kConvK - 1; ++k) seq[k] = cs[(size_t)k * C];
-    for (int t = 0; t < n; ++t) seq[kConvK - 1 + t] = xb[(size_t)t * d.NS];
+    // rolling window of the last 3 pre-conv rows (h0 oldest), in registers
+    float h0 = cs[0], h1 = cs[(size_t)C], h2 = cs[(size_t)2 * C];
+    const float w0 = __ldg(&w[0]), w1 = __ldg(&w[1]), w2 = __ldg(&w[2]), w3 = __ldg(&w[3]);
     for (int t = 0; t < n; ++t) {
-      float acc = bias;
-#pragma unroll
-      for (int k = 0; k < kConvK; ++k) acc = fmaf(__ldg(&w[k]), seq[t + k], acc);
-      xb[(size_t)t * d.NS] = silu_f(acc);
+      const float x = xb[(size_t)t * d.NS];
+      xb[(size_t)t * d.NS] = silu_f(fmaf(w3, x, fmaf(w2, h2, fmaf(w1, h1, fmaf(w0, h0, bias)))));
+      h0 = h1;
+      h1 = h2;
+      h2 = x;
     }
-    for (int k = 0; k < kConvK - 1; ++k) cs[(size_t)k * C] = seq[n + k];
+    cs[0] = h0;
+    cs[(size_t)C] = h1;
+    cs[(size_t)2 * C] = h2;
     return;
   }
   const int half = d.dh / 2;

@@ -448,6 +448,342 @@ commit_state_kernel(Dims d, int B, int qsplit, int early, int late,
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Pipelined state update for large batches (Mamba-2 memory without a
+// horizon). The per-head kernel above loads a head, updates it and stores it
+// with nothing else in flight, so at 64 requests the SMs wait on load latency
+// (three CTAs per SM, ~3.5 TB/s). Here a persistent grid of one CTA per SM
+// walks the (layer, request, head) items i = blockIdx.x + k * gridDim.x,
+// warp-specialised:
+//   producer warp: per item, one bulk copy of the head's state (P*N fp32)
+//     into a shared-memory stage, and 16-byte async copies of the accepted
+//     rows' x, B (and for a layer-0 read the draft's C rows), dt and A_log,
+//     all completing on the stage's "full" barrier; PIPE_ST stages ahead;
+//   16 consumer warps: wait on "full", fold the rows into the state in
+//     registers in order (the update of the per-head kernel), store the
+//     new state, and release the stage on its "empty" barrier. Layer-0
+//     items also make the next draft's memory read when memC is set (the
+//     consumers synchronise among themselves only there).
+// Items with n = 0 and no read are skipped; the producer warp also does the
+// bookkeeping (count check, offsets, tags, pos) of the requests whose
+// (layer 0, head 0) item its CTA owns.
+constexpr int PIPE_CWARPS = 16;                  // consumer warps
+constexpr int PIPE_CT = PIPE_CWARPS * 32;        // consumer threads
+constexpr int PIPE_THREADS = PIPE_CT + 32;       // + the producer warp
+constexpr int PIPE_QPT = 4;    // float4 of the state per consumer thread (P*N <= 8192)
+constexpr int PIPE_ST = 4;     // stages
+constexpr int PIPE_MAXB = 4096;  // accepted counts cached in shared memory
+
+struct PipeLayout {
+  size_t bar, nacc, stages, stage, off_x, off_b, off_c, off_dt, rows, red, total;  // bytes
+};
+__host__ __device__ inline PipeLayout pipe_layout(const Dims& d, bool read) {
+  PipeLayout m{};
+  const int lim = d.S + 1;
+  m.bar = 0;                                        // full[PIPE_ST], empty[PIPE_ST]
+  m.nacc = 128;                                     // [PIPE_MAXB] counts
+  m.stages = (m.nacc + (size_t)PIPE_MAXB * 4 + 127) / 128 * 128;
+  m.off_x = (size_t)d.P * d.N * 4;                  // a stage: state | x rows | B rows | C rows | dt, A_log
+  m.off_b = m.off_x + (size_t)lim * d.P * 4;
+  m.off_c = m.off_b + (size_t)lim * d.N * 4;
+  m.off_dt = m.off_c + (read ? (size_t)d.S * d.N * 4 : 0);
+  m.stage = (m.off_dt + (size_t)(lim + 1) * 4 + 127) / 128 * 128;
+  m.rows = m.stages + PIPE_ST * m.stage;
+  m.red = m.rows + (read ? (size_t)d.P * (d.N + 8) * 4 : 0);
+  m.total = m.red + (read ? (size_t)mem_ksplit(d) * d.P * 8 * 4 : 0);
+  return m;
+}
+
+// A CTA's walk over items i = blockIdx.x + k * gridDim.x, kept as
+// (layer, request, head) and advanced by the grid stride without divisions.
+struct PipeCursor {
+  int l, b, h;
+  __device__ void init(int i, int Hm, int B) {
+    h = i % Hm;
+    b = (i / Hm) % B;
+    l = i / (Hm * B);
+  }
+  __device__ void step(int gl, int gb, int gh, int Hm, int B) {
+    h += gh;
+    int cb = 0;
+    if (h >= Hm) {
+      h -= Hm;
+      cb = 1;
+    }
+    b += gb + cb;
+    int cl = 0;
+    if (b >= B) {
+      b -= B;
+      cl = 1;
+    }
+    l += gl + cl;
+  }
+};
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// The barrier completes one of its expected arrivals once every cp.async
+// this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(PIPE_THREADS)
+commit_state_pipe_kernel(Dims d, int B, int early, int late, const int32_t* __restrict__ n_acc,
+                         const float* __restrict__ xbd, long long xls,
+                         const float* __restrict__ A_log, float* __restrict__ state,
+                         int64_t* __restrict__ pos, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ tags, int32_t* __restrict__ err,
+                         const float* __restrict__ memC, T* __restrict__ mix) {
+  extern __shared__ __align__(128) uint8_t psm[];
+  const bool rd = memC != nullptr;
+  const PipeLayout L = pipe_layout(d, rd);
+  uint64_t* full = reinterpret_cast<uint64_t*>(psm + L.bar);
+  uint64_t* empty = full + PIPE_ST;
+  int* snacc = reinterpret_cast<int*>(psm + L.nacc);
+  __shared__ int s_abort;
+  const int lim = d.S + 1, P = d.P, N = d.N, nq = P * N / 4;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int G = gridDim.x, gh = G % d.Hm, gb = (G / d.Hm) % B, gl = G / (d.Hm * B);
+  if (!late) pdl_trigger();
+
+  // accepted counts (the caller's input, final at launch), invalid -> 0
+  for (int i = tid; i < B; i += PIPE_THREADS) {
+    const int m = __ldcg(&n_acc[i]);
+    snacc[i] = (m >= 0 && m <= lim) ? m : 0;
+  }
+  if (tid == 0) {
+    for (int k = 0; k < PIPE_ST; ++k) {
+      mbar_init(&full[k], 1 + 32);  // the state copy's expect_tx + the producer lanes' rows
+      mbar_init(&empty[k], PIPE_CWARPS);
+    }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto next_work = [&](PipeCursor c) {  // the first item at or after c with work
+    while (c.l < d.L && !(snacc[c.b] > 0 || (rd && c.l == 0))) c.step(gl, gb, gh, d.Hm, B);
+    return c;
+  };
+  auto advance = [&](PipeCursor c) {
+    c.step(gl, gb, gh, d.Hm, B);
+    return next_work(c);
+  };
+  PipeCursor first;
+  first.init(blockIdx.x, d.Hm, B);
+  first = next_work(first);
+
+  if (warp == PIPE_CWARPS) {
+    // ------------------------------------------------------------ producer
+    auto issue_state = [&](const PipeCursor& c, int st) {  // lane 0
+      uint8_t* sg = psm + L.stages + (size_t)st * L.stage;
+      const uint32_t sbytes = (uint32_t)(P * N * 4);
+      mbar_expect_tx(&full[st], sbytes);
+      bulk_g2s(sg, state + (((size_t)c.l * d.Bmax + c.b) * d.Hm + c.h) * (size_t)P * N, sbytes,
+               &full[st]);
+    };
+    auto issue_rows = [&](const PipeCursor& c, int st) {  // all lanes
+      const int n = snacc[c.b];
+      uint8_t* sg = psm + L.stages + (size_t)st * L.stage;
+      const float* xb = xbd + (size_t)c.l * xls + (size_t)c.b * lim * d.NS;
+      const int px = P / 4, pb = N / 4;
+      for (int e = lane; e < n * px; e += 32) {
+        const int t = e / px, c4 = (e % px) * 4;
+        cp_async16(sg + L.off_x + ((size_t)t * P + c4) * 4, xb + (size_t)t * d.NS + (size_t)c.h * P + c4);
+      }
+      for (int e = lane; e < n * pb; e += 32) {
+        const int t = e / pb, c4 = (e % pb) * 4;
+        cp_async16(sg + L.off_b + ((size_t)t * N + c4) * 4, xb + (size_t)t * d.NS + d.dinner + c4);
+      }
+      if (rd && c.l == 0)
+        for (int e = lane; e < d.S * pb; e += 32) {
+          const int s2 = e / pb, c4 = (e % pb) * 4;
+          cp_async16(sg + L.off_c + ((size_t)s2 * N + c4) * 4, memC + ((size_t)c.b * d.S + s2) * d.Nd + c4);
+        }
+      if (lane < n) cp_async4(sg + L.off_dt + (size_t)lane * 4, xb + (size_t)lane * d.NS + d.dinner + N + c.h);
+      if (lane == 31) cp_async4(sg + L.off_dt + (size_t)lim * 4, A_log + c.l * d.Hm + c.h);
+      cp_async_arrive(&full[st]);
+    };
+    PipeCursor pend[PIPE_ST];
+    PipeCursor cur = first;
+    int npro = 0;
+    for (; npro < PIPE_ST && cur.l < d.L; ++npro) {
+      pend[npro] = cur;
+      if (lane == 0 && early) issue_state(cur, npro);
+      cur = advance(cur);
+    }
+    pdl_wait();
+    if (late) pdl_trigger();
+    for (int k = 0; k < npro; ++k) {
+      if (lane == 0 && !early) issue_state(pend[k], k);
+      issue_rows(pend[k], k);
+    }
+    // bookkeeping of the requests whose (layer 0, head 0) item this CTA owns
+    for (int b = 0; b < B; ++b) {
+      if ((b * d.Hm) % G != (int)blockIdx.x) continue;  // B * Hm < 2^30 (launch check)
+      int part = 0;
+      for (int j = lane; j < b; j += 32) part += snacc[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      const int m = __ldcg(&n_acc[b]);
+      const int n = snacc[b];
+      const long long p0 = __ldcg(&pos[b]);
+      if (lane == 0) {
+        if (!(m >= 0 && m <= lim)) atomicOr(err, ERR_BAD_ACCEPTED);
+        offsets[b] = part;
+        if (b == B - 1) offsets[B] = part + n;
+      }
+      for (int t = lane; t < n; t += 32) tags[(size_t)b * d.W + (int)((p0 + t) % d.W)] = (int32_t)(p0 + t);
+      __syncwarp();
+      if (lane == 0) pos[b] = p0 + n;
+    }
+    // the rest: item j into stage j % PIPE_ST once its previous occupant
+    // (item j - PIPE_ST) is released
+    long long j = npro;
+    long long issued = npro;
+    bool ok = true;
+    for (; cur.l < d.L; ++j) {
+      const int st = (int)(j % PIPE_ST);
+      ok = mbar_wait(&empty[st], (uint32_t)((j / PIPE_ST) & 1) ^ 1u) &&
+           !*reinterpret_cast<volatile int*>(&s_abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_state(cur, st);
+      }
+      __syncwarp();
+      issue_rows(cur, st);
+      ++issued;
+      cur = advance(cur);
+    }
+    if (!ok) {
+      // a consumer gave up, or a stage was never released: report, stop
+      // issuing, and let the copies of the items that may still be in
+      // flight (the last PIPE_ST issued) land (bounded) before leaving
+      if (lane == 0) atomicOr(err, ERR_TIMEOUT);
+      for (long long q = j - PIPE_ST > 0 ? j - PIPE_ST : 0; q < issued; ++q)
+        mbar_wait(&full[q % PIPE_ST], (uint32_t)(q / PIPE_ST) & 1u);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // this lane's row copies have landed
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  pdl_wait();
+  if (late) pdl_trigger();
+  // this thread's float4 q = tid + u * PIPE_CT of a head: row pr[u], column
+  // c4 (the same for every u: N / 4 divides PIPE_CT)
+  const int cpr = N / 4;
+  const int c4 = (tid % cpr) * 4;
+  int pr[PIPE_QPT];
+#pragma unroll
+  for (int u = 0; u < PIPE_QPT; ++u) {
+    const int q = tid + u * PIPE_CT;
+    pr[u] = q < nq ? q / cpr : 0;  // elements past the head: row 0, never stored
+  }
+  PipeCursor it = first;
+  bool live = true;  // false after a wait gave up: the walk continues without work
+  for (long long k = 0; it.l < d.L; ++k) {
+    const int st = (int)(k % PIPE_ST);
+    const int l = it.l, b = it.b, h = it.h, n = live ? snacc[b] : 0;
+    if (live && (*reinterpret_cast<volatile int*>(&s_abort) ||
+                 !mbar_wait(&full[st], (uint32_t)(k / PIPE_ST) & 1u))) {
+      live = false;  // the producer stops issuing and drains; the named
+      s_abort = 1;   // barriers below stay matched
+    }
+    const uint8_t* sg = psm + L.stages + (size_t)st * L.stage;
+    const float4* s4 = reinterpret_cast<const float4*>(sg);
+    const float* sx = reinterpret_cast<const float*>(sg + L.off_x);
+    const float* sb = reinterpret_cast<const float*>(sg + L.off_b);
+    const float* sdt = reinterpret_cast<const float*>(sg + L.off_dt);
+    float4 hv[PIPE_QPT];
+#pragma unroll
+    for (int u = 0; u < PIPE_QPT; ++u) {
+      const int q = tid + u * PIPE_CT;
+      hv[u] = live && q < nq ? s4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float A = live ? -expf(sdt[lim]) : 0.f;
+    for (int t = 0; t < n; ++t) {
+      const float dt = sdt[t];
+      const float dec = expf(dt * A);
+      const float4 Bv = *reinterpret_cast<const float4*>(&sb[t * N + c4]);
+#pragma unroll
+      for (int u = 0; u < PIPE_QPT; ++u) {
+        const float xv = dt * sx[t * P + pr[u]];
+        hv[u].x = fmaf(dec, hv[u].x, xv * Bv.x);
+        hv[u].y = fmaf(dec, hv[u].y, xv * Bv.y);
+        hv[u].z = fmaf(dec, hv[u].z, xv * Bv.z);
+        hv[u].w = fmaf(dec, hv[u].w, xv * Bv.w);
+      }
+    }
+    if (live && n > 0) {
+      float4* hg = reinterpret_cast<float4*>(state + (((size_t)l * d.Bmax + b) * d.Hm + h) * (size_t)P * N);
+#pragma unroll
+      for (int u = 0; u < PIPE_QPT; ++u) {
+        const int q = tid + u * PIPE_CT;
+        if (q < nq) __stcs(&hg[q], hv[u]);
+      }
+    }
+    if (rd && l == 0) {
+      // memory read of the new state (tensor cores, as the per-head kernel);
+      // the consumers synchronise among themselves (named barrier 1)
+      const int RS = N + 8;
+      float* rows = reinterpret_cast<float*>(psm + L.rows);
+      float* red = reinterpret_cast<float*>(psm + L.red);
+      const float* sc = reinterpret_cast<const float*>(sg + L.off_c);
+#pragma unroll
+      for (int u = 0; u < PIPE_QPT; ++u) {
+        const int q = tid + u * PIPE_CT;
+        if (live && q < nq) *reinterpret_cast<float4*>(&rows[pr[u] * RS + c4]) = hv[u];
+      }
+      const int g8 = lane >> 2, t4 = lane & 3;
+      const int MT = P / 16, KSPL = mem_ksplit(d), G16 = N / 16 / KSPL;
+      const int mt = warp % MT, kp = warp / MT;
+      const bool active = live && kp < KSPL;
+      const int r0 = mt * 16 + g8;
+      const int col0 = kp * G16 * 16 + 4 * t4;
+      asm volatile("bar.sync 1, %0;" ::"r"(PIPE_CT) : "memory");  // the new state is in rows
+      if (active) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < MEM_G16; ++j)
+          if (j < G16) {
+            float4 cc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (g8 < d.S) cc = *reinterpret_cast<const float4*>(&sc[g8 * N + col0 + j * 16]);
+            const float4 x0 = *reinterpret_cast<const float4*>(&rows[r0 * RS + col0 + j * 16]);
+            const float4 x1 = *reinterpret_cast<const float4*>(&rows[(r0 + 8) * RS + col0 + j * 16]);
+            mma_tf32_1688(c, to_tf32(x0.x), to_tf32(x1.x), to_tf32(x0.y), to_tf32(x1.y),
+                          to_tf32(cc.x), to_tf32(cc.y));
+            mma_tf32_1688(c, to_tf32(x0.z), to_tf32(x1.z), to_tf32(x0.w), to_tf32(x1.w),
+                          to_tf32(cc.z), to_tf32(cc.w));
+          }
+        float* rp = red + ((size_t)kp * P + r0) * 8 + 2 * t4;
+        *reinterpret_cast<float2*>(rp) = make_float2(c[0], c[1]);
+        *reinterpret_cast<float2*>(rp + 64) = make_float2(c[2], c[3]);
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(PIPE_CT) : "memory");  // partial sums in red
+      for (int e = live ? tid : d.S * P; e < d.S * P; e += PIPE_CT) {
+        const int sl = e / P, p = e % P;
+        float y = 0.f;
+        for (int q = 0; q < KSPL; ++q) y += red[((size_t)q * P + p) * 8 + sl];
+        mix[((size_t)b * d.S + sl) * d.Nz + d.QD + (size_t)h * P + p] = from_f<T>(y);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with stage st
+    it = advance(it);
+  }
+}
 }  // namespace
 
 size_t commit_state_smem(const Dims& d, bool read) { return cs_layout(d, read).total * sizeof(float); }
@@ -489,12 +825,21 @@ cudaError_t launch_variant(int dtype, const Dims& d, int B, bool whole, int qspl
 
 cudaError_t configure_commit_state(const Dims& d) {
   static int configured = 0;  // attribute of the kernels: keep the largest need
+  static int configured_pipe = 0;
   const int smem = (int)commit_state_smem(d, mem_tc_ok(d));
-  if (smem <= configured) return cudaSuccess;
-  cudaError_t e = configure_variant<0>(smem);
-  if (e == cudaSuccess) e = configure_variant<1>(smem);
-  if (e == cudaSuccess) e = configure_variant<2>(smem);
-  if (e == cudaSuccess) configured = smem;
+  cudaError_t e = cudaSuccess;
+  if (smem > configured) {
+    e = configure_variant<0>(smem);
+    if (e == cudaSuccess) e = configure_variant<1>(smem);
+    if (e == cudaSuccess) e = configure_variant<2>(smem);
+    if (e == cudaSuccess) configured = smem;
+  }
+  const int psmem = (int)pipe_layout(d, mem_tc_ok(d)).total;
+  if (e == cudaSuccess && psmem > configured_pipe && psmem <= 232448) {
+    e = set_smem(commit_state_pipe_kernel<float>, psmem);
+    if (e == cudaSuccess) e = set_smem(commit_state_pipe_kernel<__nv_bfloat16>, psmem);
+    if (e == cudaSuccess) configured_pipe = psmem;
+  }
   return e;
 }
 
@@ -512,6 +857,21 @@ cudaError_t launch_commit_state(int dtype, const Dims& d, int B, const int32_t* 
   const int qpt = whole ? QPT_HEAD : 2;
   const int qsplit = (nq + qpt * THREADS_CS - 1) / (qpt * THREADS_CS);
   const size_t smem = commit_state_smem(d, memC != nullptr);
+  // large batches of the plain Mamba-2 memory: the pipelined persistent walk
+  const PipeLayout pl = pipe_layout(d, memC != nullptr);
+  if (!d.gdn && d.Mr == 0 && d.Mh == 0 && whole && pl.total <= 232448 &&
+      nq <= PIPE_QPT * PIPE_THREADS && B <= PIPE_MAXB &&
+      (long long)B * d.Hm * d.L >= 8LL * num_sms && (long long)B * d.Hm * d.L < (1LL << 30)) {
+    const long long items = (long long)B * d.Hm * d.L;
+    const dim3 grid((unsigned)std::min<long long>(num_sms, items));
+    if (dtype == HF_F32)
+      return launch_pdl(commit_state_pipe_kernel<float>, grid, dim3(PIPE_THREADS), pl.total, st, d,
+                        B, early, late, n_acc, xbd, xls, A_log, state, pos, offsets, tags, err,
+                        memC, (float*)mix);
+    return launch_pdl(commit_state_pipe_kernel<__nv_bfloat16>, grid, dim3(PIPE_THREADS), pl.total,
+                      st, d, B, early, late, n_acc, xbd, xls, A_log, state, pos, offsets, tags,
+                      err, memC, (__nv_bfloat16*)mix);
+  }
   if (d.gdn)
     return launch_variant<2>(dtype, d, B, whole, qsplit, smem, early, late, n_acc, xbd, xls, A_log,
                              state, pos, offsets, tags, err, memC, mix, mr, st);

@@ -552,3 +552,47 @@ def test_q4_weights_phi4_grouped_and_layers():
     p.prefill([300], make_prefix_feats(cfg, [300]))
     run_round_api(p, 2, check_every=1)
     p.close()
+
+
+# ---------------------------------------------------------------- pipelined state update
+
+@pytest.mark.parametrize("name,batch,layers,api", [
+    ("serving_qwen3_4b_b64", 16, 1, "round"),     # 1280 heads: fused memory read in the walk
+    ("serving_qwen3_4b_b64", 16, 1, "separate"),  # the walk without the read
+    ("serving_qwen3_4b_b64", 9, 2, "round"),      # layer 1 items never read
+    ("tiny_fp32", 320, 1, "separate"),            # small heads (P*N = 1024), fp32
+])
+def test_pipelined_state_walk(name, batch, layers, api):
+    """Large batches run the persistent state-update walk (bulk copies of
+    each head's state and rows, several heads in flight per SM): state, ring,
+    offsets and both draft branches against the oracle, with zero, full and
+    invalid accepted counts among the requests."""
+    import speculative_decoding_drafter_hf_gb300 as hf
+    cfg = CONFIGS[name].replace(batch=batch, n_layers=layers, prefix=60, prefix_lo=0, prefix_hi=0)
+    p = Pair(cfg)
+    lens = [(37 * i) % 700 for i in range(batch)] if name != "tiny_fp32" else \
+        [(13 * i) % 90 for i in range(batch)]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    for r in range(3):
+        slot, feats = make_round_inputs(cfg, r, batch)
+        n = make_accepted(cfg, r, batch)
+        n[0], n[1] = 0, cfg.block + 1
+        if r == 1:
+            n[2] = -3  # invalid: request 2 untouched, EDEVICE at sync
+        if api == "round":
+            out = p.gpu.round(feats.cuda(), n.cuda(), slot.cuda())
+            torch.cuda.synchronize()
+            offs, _ = p.orc.commit(feats, n.numpy())
+            ref = p.orc.draft(slot)
+            assert maxnorm_err(out.float().cpu().numpy(), ref) <= p.tol, f"round {r}"
+            check_mix(p, slot, f"round {r}")
+        else:
+            offs, _ = p.commit(feats, n)
+            got, ref = p.draft(slot)
+            assert maxnorm_err(got, ref) <= p.tol, f"round {r}"
+            check_mix(p, slot, f"round {r}")
+        assert np.array_equal(p.gpu.read(Tensor.OFFSETS)[:batch + 1], offs.astype(np.int32))
+        st = p.gpu.sync_status()[0]
+        assert st == (hf.Status.EDEVICE if r == 1 else hf.Status.OK)
+        p.check_context(what=f"round {r}")
+    p.close()
