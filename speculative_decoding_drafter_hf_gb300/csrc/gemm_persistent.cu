@@ -2,8 +2,11 @@
 // of the prefill (tokens x features): D[m, n] = sum_k A[m, k] * B[n, k].
 //
 // One CTA per SM walks the output tiles t = blockIdx.x, + gridDim.x, ...
-// (tile = 128 tokens x BN features; consecutive tiles share the token rows,
-// the weight panel stays in L2). Warp 0 (one lane) feeds a ring of STAGES
+// (tile = 128 tokens x BN features) in grouped order: the token tiles come
+// in groups whose rows fit well inside L2 (~48 MB), and within a group the
+// tiles run feature-panel by feature-panel, so a wave of CTAs shares one or
+// two weight panels and the group's token rows stay resident: every weight
+// panel is read from DRAM once per group instead of once per wave. Warp 0 (one lane) feeds a ring of STAGES
 // shared-memory slots with TMA, warp 1 (one lane) issues tcgen05.mma into
 // one of two TMEM accumulators, and warps 2-5 drain the other accumulator
 // through the epilogue, so a tile's epilogue overlaps the next tile's main
@@ -22,8 +25,19 @@ constexpr int PTHREADS = 192;
 
 struct PArgs {
   int M, N, K, kblocks, m_tiles, n_tiles;
+  int group_m;  // token tiles per group of the tile order
   int32_t* err;
 };
+
+// Tile t of the grouped order -> (token tile mt, feature tile nt).
+__device__ __forceinline__ void p_tile(const PArgs& a, int t, int& mt, int& nt) {
+  const int per_group = a.group_m * a.n_tiles;
+  const int g = t / per_group, local = t - g * per_group;
+  const int g0 = g * a.group_m;
+  const int gsz = a.m_tiles - g0 < a.group_m ? a.m_tiles - g0 : a.group_m;
+  nt = local / gsz;
+  mt = g0 + local % gsz;
+}
 
 constexpr size_t p_smem() {
   return 1024 + (size_t)PSTAGES * (128 * 128 + PBN * 128) + (2 * PSTAGES + 4) * 8 + 32;
@@ -73,7 +87,8 @@ tc_gemm_persistent_kernel(const __grid_constant__ CUtensorMap ta,
     pdl_wait();
     int g = 0;
     for (int t = blockIdx.x; t < ntiles && !*(volatile int*)&flags[0]; t += gridDim.x) {
-      const int mt = t / a.n_tiles, nt = t % a.n_tiles;
+      int mt, nt;
+      p_tile(a, t, mt, nt);
       for (int kb = 0; kb < a.kblocks; ++kb, ++g) {
         const int s = g % PSTAGES;
         const uint32_t ph = (uint32_t)(g / PSTAGES) & 1u;
@@ -135,7 +150,8 @@ tc_gemm_persistent_kernel(const __grid_constant__ CUtensorMap ta,
         break;
       }
       tc_fence_after();
-      const int mt = t / a.n_tiles, nt = t % a.n_tiles;
+      int mt, nt;
+      p_tile(a, t, mt, nt);
       const int m = mt * 128 + quad * 32 + lane;
       float v[16];
 #pragma unroll 1
@@ -188,6 +204,8 @@ cudaError_t launch_gemm_persistent(const void* A, long long lda, int M, const vo
   a.kblocks = (K + 63) / 64;
   a.m_tiles = (M + 127) / 128;
   a.n_tiles = (N + PBN - 1) / PBN;
+  // token tiles per group: their rows (128 x K bf16 each) within ~48 MB of L2
+  a.group_m = (int)std::max<long long>(1, std::min<long long>(a.m_tiles, (48ll << 20) / (256ll * K)));
   a.err = err;
   CUtensorMap ma, mb;
   cudaError_t e = make_map(&ma, A, M, K, lda, 128);

@@ -115,6 +115,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   constexpr uint32_t STAGE_BYTES = TILE_BYTES + B_BYTES;    // bytes the copies of a stage bring
   constexpr uint32_t NCOLS = BN < 32 ? 32 : BN;
   constexpr int RES_ROWS = EpiCache<BN>::RES_ROWS;
+  // Split-K partial tiles are summed through the drained stage buffers, 128
+  // floats per tile column (token-major) or row (swap); when BN of them do
+  // not fit (two-stage rings) the sum runs in passes of RED_COLS.
+  constexpr int RED_FLOATS = STAGES * (A_BYTES + B_BYTES + PK_BYTES) / 4;
+  constexpr int RED_COLS = (RED_FLOATS / 128 / 16) * 16 < BN ? (RED_FLOATS / 128 / 16) * 16 : BN;
+  constexpr int RED_PASSES = (BN + RED_COLS - 1) / RED_COLS;
+  static_assert(RED_COLS >= 16, "stage buffers too small for the split-K sum");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -318,10 +325,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     }
     tc_fence_before();
     __syncthreads();
-    if (a.splits > 1) {  // keep the cluster's barrier sequence matched
-      cluster_sync_all();
-      cluster_sync_all();
-    }
+    if (a.splits > 1)  // keep the cluster's barrier sequence matched (two per pass)
+      for (int p = 0; p < RED_PASSES; ++p) {
+        cluster_sync_all();
+        cluster_sync_all();
+      }
     if (warp == 1)
       asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOLS));
     return;
@@ -384,54 +392,65 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     // rank r owns the 16-column chunks r, r + splits, ... of the tile and sums
     // them over all partners in rank order (deterministic).
     float* red = reinterpret_cast<float*>(smem);
-#pragma unroll 1
-    for (int c0 = 0; c0 < (epw ? BN : 0); c0 += 16) {
-      tmem_ld16(trow + c0, v);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + m_local] = v[j];
-    }
-    cluster_sync_all();
     const int rank = (int)cluster_rank();
-    for (int c0 = rank * 16; c0 < (epw ? n_here : 0); c0 += a.splits * 16) {
+#pragma unroll 1
+    for (int p0 = 0; p0 < BN; p0 += RED_COLS) {  // columns [p0, p0 + RED_COLS) per pass
+      const int p1 = p0 + RED_COLS < BN ? p0 + RED_COLS : BN;
+#pragma unroll 1
+      for (int c0 = p0; c0 < (epw ? p1 : p0); c0 += 16) {
+        tmem_ld16(trow + c0, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float part[8];
-#pragma unroll
-        for (int sp = 0; sp < 8; ++sp)
-          part[sp] = sp < a.splits ? ld_peer(&red[(c0 + j) * 128 + m_local], (uint32_t)sp) : 0.f;
-        float sum = 0.f;
-#pragma unroll
-        for (int sp = 0; sp < 8; ++sp) sum += part[sp];
-        v[j] = sum;
+        for (int j = 0; j < 16; ++j) red[(c0 - p0 + j) * 128 + m_local] = v[j];
       }
-      if (m < M) epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
+      cluster_sync_all();
+      const int pe = p1 < n_here ? p1 : n_here;
+      for (int c0 = p0 + rank * 16; c0 < (epw ? pe : p0); c0 += a.splits * 16) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float part[8];
+#pragma unroll
+          for (int sp = 0; sp < 8; ++sp)
+            part[sp] = sp < a.splits ? ld_peer(&red[(c0 - p0 + j) * 128 + m_local], (uint32_t)sp)
+                                     : 0.f;
+          float sum = 0.f;
+#pragma unroll
+          for (int sp = 0; sp < 8; ++sp) sum += part[sp];
+          v[j] = sum;
+        }
+        if (m < M) epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
+      }
+      cluster_sync_all();  // partners keep their shared memory until all reads are done
     }
-    cluster_sync_all();  // partners keep their shared memory until all reads are done
   } else {
     // Split-K: this CTA's partial tile goes to its own shared memory (the
     // drained stage buffers); after a cluster barrier, rank r sums rows
     // r, r + splits, ... over all partners in rank order (deterministic).
     float* red = reinterpret_cast<float*>(smem);
-#pragma unroll 1
-    for (int c0 = 0; c0 < (epw ? BN : 0); c0 += 16) {
-      tmem_ld16(trow + c0, v);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (c0 + j < n_here) red[(c0 + j) * 128 + m_local] = v[j];
-    }
-    cluster_sync_all();
     const int rank = (int)cluster_rank();
-    for (int nl = rank; nl < (epw ? n_here : 0); nl += a.splits) {
-      float part[8];
+#pragma unroll 1
+    for (int p0 = 0; p0 < BN; p0 += RED_COLS) {  // tile rows [p0, p0 + RED_COLS) per pass
+      const int p1 = p0 + RED_COLS < BN ? p0 + RED_COLS : BN;
+#pragma unroll 1
+      for (int c0 = p0; c0 < (epw ? p1 : p0); c0 += 16) {
+        tmem_ld16(trow + c0, v);
 #pragma unroll
-      for (int sp = 0; sp < 8; ++sp)
-        part[sp] = sp < a.splits ? ld_peer(&red[nl * 128 + m_local], (uint32_t)sp) : 0.f;
-      float sum = 0.f;
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < n_here) red[(c0 - p0 + j) * 128 + m_local] = v[j];
+      }
+      cluster_sync_all();
+      const int pe = p1 < n_here ? p1 : n_here;
+      for (int nl = p0 + rank; nl < (epw ? pe : p0); nl += a.splits) {
+        float part[8];
 #pragma unroll
-      for (int sp = 0; sp < 8; ++sp) sum += part[sp];
-      if (m < M) emit(nl, sum);
+        for (int sp = 0; sp < 8; ++sp)
+          part[sp] = sp < a.splits ? ld_peer(&red[(nl - p0) * 128 + m_local], (uint32_t)sp) : 0.f;
+        float sum = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < 8; ++sp) sum += part[sp];
+        if (m < M) emit(nl, sum);
+      }
+      cluster_sync_all();  // partners keep their shared memory until all reads are done
     }
-    cluster_sync_all();  // partners keep their shared memory until all reads are done
   }
   tc_fence_before();
   __syncthreads();

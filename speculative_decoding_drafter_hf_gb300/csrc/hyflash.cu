@@ -377,8 +377,13 @@ cudaError_t gemm_launch(hf_handle* h, const void* X, int ldx, const void* Wt, in
     return hf::launch_gemm_fma(h->cfg.dtype, X, ldx, Wt, ldw, R, C, K, splits, h->part, epi, st,
                                count);
   }
-  // more than 32 rows: token-major (contiguous epilogue runs), split-K
+  // more than 32 rows: token-major (contiguous epilogue runs); products with
+  // at least a tile per SM run on the persistent kernel (two accumulators,
+  // epilogue overlapped, grouped tile order), smaller ones as split-K
   // partners in a cluster summing through distributed shared memory
+  if (R > 32 && C >= 256 && (long long)((R + 127) / 128) * ((C + 255) / 256) >= h->num_sms &&
+      !late_trigger)
+    return hf::launch_gemm_persistent(X, ldx, R, Wt, ldw, C, K, h->err, epi, h->num_sms, st, count);
   if (R > 32)
     return hf::launch_gemm_tc(X, ldx, R, Wt, ldw, C, K, 0, hf::tc_pick_splits(R, C, K), h->err,
                               epi, st, count, nullptr, late_trigger);
