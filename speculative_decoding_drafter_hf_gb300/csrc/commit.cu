@@ -784,6 +784,7 @@ commit_state_pipe_kernel(Dims d, int B, int early, int late, const int32_t* __re
     it = advance(it);
   }
 }
+
 }  // namespace
 
 size_t commit_state_smem(const Dims& d, bool read) { return cs_layout(d, read).total * sizeof(float); }

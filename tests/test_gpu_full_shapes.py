@@ -146,3 +146,21 @@ def test_serving_batch64_three_layers_subset():
                 e = maxnorm_err(state[l, b], orc.ctx[i][l].h)
                 assert e <= tol, f"round {r} request {b} layer {l}: state err {e:.3e}"
     d.close()
+
+
+def test_prefill_sweep_128k_sampled_heads():
+    """The sweep's longest prefix (128K tokens) on one request: every window
+    entry, tags, position, and two memory heads against the oracle's fold."""
+    cfg = CONFIGS["prefill_phi4_sweep"].replace(batch=1)
+    check_long_prefill(cfg, [131072], heads=[7, 120])
+
+
+def test_prefill_depth5_bf16_all_layers():
+    """Five drafter layers at the sweep's Phi-4 widths (bf16), prefixes folded
+    in several passes: every layer's state, ring and tags against the oracle."""
+    cfg = CONFIGS["prefill_phi4_sweep"].replace(batch=2, n_layers=5, chunk=64)
+    p = Pair(cfg, prefill_tokens_max=512)
+    lens = [1200, 300]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="depth-5 prefill")
+    p.close()
