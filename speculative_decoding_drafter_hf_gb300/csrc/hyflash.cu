@@ -1219,8 +1219,23 @@ hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
     Scope sc(h, HF_K_ROUND_PROJ, st);
     const bool tm = std::max(N0, N1) > 32;  // wide batch: token-major over the plain weights
     const bool sk = !tm && !h->q4 && (M0 + 127) / 128 + (d.Nd + 127) / 128 > h->num_sms;
+    // wide batch with a tile per SM in the commit product alone: the commit
+    // projection on the persistent GEMM, then the slot projection (split-K
+    // clusters), which signals its dependents after its own wait
+    const bool two_launch = tm && (long long)((N0 + 127) / 128) * ((d.L * d.Nc + 255) / 256) >= h->num_sms;
+    if (two_launch) {
+      cudaError_t e = hf::launch_gemm_persistent(feats, d.D, N0, h->w_commit, d.D, d.L * d.Nc, d.D,
+                                                 h->err, plain_commit_epi(h, n_accepted),
+                                                 h->num_sms, st, &sc.count);
+      if (e == cudaSuccess)
+        e = hf::launch_gemm_tc(slot_emb, d.D, N1, h->w_draft, d.D, d.Nd, d.D, 0,
+                               hf::tc_pick_splits(N1, d.Nd, d.D), h->err, e1, st, &sc.count, nullptr,
+                               /*late_trigger=*/1);
+      if (e != cudaSuccess) return cuda_fail(h, e, "round projection launches");
+    }
     cudaError_t e =
-        tm  ? hf::launch_gemm_tm(feats, d.D, N0, h->w_commit, d.D, d.L * d.Nc,
+        two_launch ? cudaSuccess
+        : tm  ? hf::launch_gemm_tm(feats, d.D, N0, h->w_commit, d.D, d.L * d.Nc,
                                  plain_commit_epi(h, n_accepted), slot_emb, d.D, N1, h->w_draft, d.D,
                                  d.Nd, e1, d.D, h->num_sms, h->skws, h->skws_floats, h->counters,
                                  h->n_counters, h->err, /*late_trigger=*/1, st, &sc.count)
