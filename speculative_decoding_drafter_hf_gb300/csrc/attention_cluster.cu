@@ -22,6 +22,8 @@
 // y[s, h, p] = sum_n state[h, p, n] * C_s[s, n]. The state block of (b, h)
 // is read with 16-byte loads, all in flight at once, and reduced across the
 // lanes that share a state row. The state is never written here.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace hf {
@@ -1182,15 +1184,23 @@ cudaError_t configure_dtype() {
 
 // Every variant may use up to the opt-in maximum; the launch passes the
 // layout's own size, which sets the occupancy.
+// (The attributes are per-device settings: configured once per device.)
 cudaError_t configure_attn_cluster(const Dims&) {
-  static bool configured = false;
-  if (configured) return cudaSuccess;
-  cudaError_t e = configure_dtype<float>();
+  constexpr int kMaxDevices = 64;
+  static bool configured[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (configured[dev]) return cudaSuccess;
+  e = configure_dtype<float>();
   if (e == cudaSuccess) e = configure_dtype<__nv_bfloat16>();
   if (e == cudaSuccess) e = configure_kernel(attn_tc_kernel<64>);
   if (e == cudaSuccess) e = configure_kernel(attn_tc_kernel<128>);
   if (e == cudaSuccess) e = configure_kernel(attn_tc_kernel<256>);
-  if (e == cudaSuccess) configured = true;
+  if (e == cudaSuccess) configured[dev] = true;
   return e;
 }
 

@@ -8,6 +8,8 @@
 // "Sliding-window attention"): the window keeps the most recent W committed
 // positions, position t in slot t mod W. The K/V ring append itself happens
 // in the commit projection's epilogue (common.cuh, EPI_SSM_KV).
+#include <mutex>
+
 #include "common.cuh"
 
 namespace hf {
@@ -824,22 +826,30 @@ cudaError_t launch_variant(int dtype, const Dims& d, int B, bool whole, int qspl
 }
 }  // namespace
 
+// The kernels' shared-memory attribute is a per-device setting: keep, per
+// device, the largest need configured so far.
+constexpr int kMaxDevices = 64;
+std::mutex g_cs_mu;
+int g_cs_configured[kMaxDevices] = {}, g_cs_configured_pipe[kMaxDevices] = {};
+
 cudaError_t configure_commit_state(const Dims& d) {
-  static int configured = 0;  // attribute of the kernels: keep the largest need
-  static int configured_pipe = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_cs_mu);
   const int smem = (int)commit_state_smem(d, mem_tc_ok(d));
-  cudaError_t e = cudaSuccess;
-  if (smem > configured) {
+  if (smem > g_cs_configured[dev]) {
     e = configure_variant<0>(smem);
     if (e == cudaSuccess) e = configure_variant<1>(smem);
     if (e == cudaSuccess) e = configure_variant<2>(smem);
-    if (e == cudaSuccess) configured = smem;
+    if (e == cudaSuccess) g_cs_configured[dev] = smem;
   }
   const int psmem = (int)pipe_layout(d, mem_tc_ok(d)).total;
-  if (e == cudaSuccess && psmem > configured_pipe && psmem <= 232448) {
+  if (e == cudaSuccess && psmem > g_cs_configured_pipe[dev] && psmem <= 232448) {
     e = set_smem(commit_state_pipe_kernel<float>, psmem);
     if (e == cudaSuccess) e = set_smem(commit_state_pipe_kernel<__nv_bfloat16>, psmem);
-    if (e == cudaSuccess) configured_pipe = psmem;
+    if (e == cudaSuccess) g_cs_configured_pipe[dev] = psmem;
   }
   return e;
 }
