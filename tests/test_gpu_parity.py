@@ -596,3 +596,18 @@ def test_pipelined_state_walk(name, batch, layers, api):
         assert st == (hf.Status.EDEVICE if r == 1 else hf.Status.OK)
         p.check_context(what=f"round {r}")
     p.close()
+
+
+@pytest.mark.parametrize("name,lens,tokens_max", [
+    ("tiny_fp32", [700, 130, 1], 512),     # two passes, a one-token prefix
+    ("qwen3_4b_bf16", [260, 64], 100),      # 100-token passes
+])
+def test_gated_delta_long_prefill_passes(name, lens, tokens_max):
+    """The gated-delta prefill over long prefixes cut into several passes:
+    the state after prefill and after rounds against the oracle's rule."""
+    cfg = CONFIGS[name].replace(batch=len(lens), prefix=100, memory="gdn")
+    p = Pair(cfg, prefill_tokens_max=tokens_max)
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    p.check_context(what="gated-delta prefill in passes")
+    run_rounds(p, 2, check_every=1)
+    p.close()
