@@ -145,20 +145,29 @@ tc_gemm_persistent_kernel(const __grid_constant__ CUtensorMap ta,
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int buf = i & 1;
       const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+      int mt, nt;
+      p_tile(a, t, mt, nt);
+      const int m = mt * 128 + quad * 32 + lane;
+      // the commit epilogue's per-row part (request, position: dependent
+      // global loads) once per tile row, issued before the accumulator wait
+      const bool kv = epi.kind == EPI_SSM_KV;
+      const long long ro = kv && m < a.M ? ssm_kv_row(epi, m, nt * PBN) : -1;
       if (!mbar_wait(&tfull[buf], aph)) {
         atomicExch(&flags[0], 1);
         break;
       }
       tc_fence_after();
-      int mt, nt;
-      p_tile(a, t, mt, nt);
-      const int m = mt * 128 + quad * 32 + lane;
       float v[16];
 #pragma unroll 1
       for (int c0 = 0; c0 < PBN; c0 += 16) {
         tmem_ld16(tmem + lane_base + (uint32_t)(buf * PBN + c0), v);
         const int n0 = nt * PBN + c0;
-        if (m < a.M && n0 < a.N) epi_chunk16(epi, m, n0, min(16, a.N - n0), v);
+        if (m < a.M && n0 < a.N) {
+          if (kv)
+            epi_ssm_chunk16(epi, m, n0, min(16, a.N - n0), v, ro);
+          else
+            epi_chunk16(epi, m, n0, min(16, a.N - n0), v);
+        }
       }
       tc_fence_before();
       __syncwarp();

@@ -53,6 +53,24 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
   return v;
 }
 
+// Remote shared-memory store of four floats into partner `rank`'s copy of
+// the local address (a cluster-window address; no reply is awaited).
+__device__ __forceinline__ void st_peer4(const float* local, uint32_t rank, float4 v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+// Receive slots of the token-major split-K sum: for (sending partner's slot,
+// owned chunk k, tile row m) the row's 16 partial sums, its four float4 in
+// an order rotated by row pair (conflict-free stores and loads by a warp of
+// 32 consecutive rows). Returns the float offset of float4 q.
+__device__ __forceinline__ int recv_off(int slot, int k, int kmax, int m, int q) {
+  return (((slot * kmax + k) * 128 + m) << 4) + ((q ^ ((m >> 1) & 3)) << 2);
+}
+
 struct TcArgs {
   int M, N, K;        // D is M x N
   int kblocks;        // ceil(K / 64)
@@ -122,6 +140,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   constexpr int RED_COLS = (RED_FLOATS / 128 / 16) * 16 < BN ? (RED_FLOATS / 128 / 16) * 16 : BN;
   constexpr int RED_PASSES = (BN + RED_COLS - 1) / RED_COLS;
   static_assert(RED_COLS >= 16, "stage buffers too small for the split-K sum");
+  // token-major split-K: (splits - 1) receive slots of ceil(chunks / splits)
+  // 16-column chunks x 128 rows, for every cluster size up to 8
+  constexpr int NCH = BN / 16 > 0 ? BN / 16 : 1;
+  static_assert(7 * ((NCH + 6) / 7) * 8192 <= STAGES * (A_BYTES + B_BYTES + PK_BYTES) &&
+                    6 * ((NCH + 5) / 6) * 8192 <= STAGES * (A_BYTES + B_BYTES + PK_BYTES) &&
+                    5 * ((NCH + 4) / 5) * 8192 <= STAGES * (A_BYTES + B_BYTES + PK_BYTES) &&
+                    4 * ((NCH + 3) / 4) * 8192 <= STAGES * (A_BYTES + B_BYTES + PK_BYTES) &&
+                    3 * ((NCH + 2) / 3) * 8192 <= STAGES * (A_BYTES + B_BYTES + PK_BYTES) &&
+                    2 * ((NCH + 1) / 2) * 8192 <= STAGES * (A_BYTES + B_BYTES + PK_BYTES) &&
+                    NCH * 8192 <= STAGES * (A_BYTES + B_BYTES + PK_BYTES),
+                "stage buffers too small for the split-K receive slots");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -315,6 +344,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     }
   }
 
+  // token-major commit epilogue: the row's ring offset once per row (its
+  // dependent loads overlap the main loop)
+  const bool kv_tm = !a.swap && epi.kind == EPI_SSM_KV;
+  const int m_row = m_tile * 128 + warp * 32 + lane;
+  const long long ro_tm = kv_tm && epw && m_row < M ? ssm_kv_row(epi, m_row, n_tile * BN) : -1;
+
   const bool ok = mbar_wait(done, 0);
   if (__syncthreads_or(!ok || flags[0])) {
     // Timed out somewhere: report, drain issued copies (bounded), free TMEM.
@@ -325,8 +360,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     }
     tc_fence_before();
     __syncthreads();
-    if (a.splits > 1)  // keep the cluster's barrier sequence matched (two per pass)
-      for (int p = 0; p < RED_PASSES; ++p) {
+    if (a.splits > 1)  // keep the cluster's barrier sequence matched (token-major:
+                       // two; swap: two per pass)
+      for (int p = 0; p < (a.swap ? RED_PASSES : 1); ++p) {
         cluster_sync_all();
         cluster_sync_all();
       }
@@ -366,7 +402,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
     for (int c0 = 0; c0 < (epw ? BN : 0); c0 += 16) {
       tmem_ld16(trow + c0, v);
       if (m < M && c0 < n_here) {
-        if (!a.swap) {
+        if (kv_tm) {
+          epi_ssm_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v, ro_tm);
+        } else if (!a.swap) {
           epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
         } else if (epi.kind == EPI_RESID && RES_ROWS == 0) {
           // 16 independent residual loads in flight, then the stores
@@ -388,38 +426,89 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       }
     }
   } else if (!a.swap) {
-    // Split-K, token-major: partial tiles meet in distributed shared memory;
-    // rank r owns the 16-column chunks r, r + splits, ... of the tile and sums
-    // them over all partners in rank order (deterministic).
-    float* red = reinterpret_cast<float*>(smem);
-    const int rank = (int)cluster_rank();
-#pragma unroll 1
-    for (int p0 = 0; p0 < BN; p0 += RED_COLS) {  // columns [p0, p0 + RED_COLS) per pass
-      const int p1 = p0 + RED_COLS < BN ? p0 + RED_COLS : BN;
-#pragma unroll 1
-      for (int c0 = p0; c0 < (epw ? p1 : p0); c0 += 16) {
-        tmem_ld16(trow + c0, v);
+    // Split-K, token-major: 16-column chunk u of the tile belongs to rank
+    // u % splits. Once every partner's main loop has drained (first cluster
+    // barrier: the stage buffers are free), each partner pushes its partial
+    // of the chunks it does not own into the owner's receive slots with
+    // remote stores; after the second barrier the owner adds the partials in
+    // rank order (its own straight from tensor memory; deterministic) and
+    // runs the epilogue. The residual rows of the owned chunks are loaded
+    // while the pushes are in flight.
+    float* recv = reinterpret_cast<float*>(smem);
+    const int rank = (int)cluster_rank(), S = a.splits;
+    const int nch = (n_here + 15) / 16, kmax = (NCH + S - 1) / S;
+    const bool resid = epi.kind == EPI_RESID && epi.ld % 8 == 0;
+    constexpr int KPRE = (NCH + 1) / 2;  // owned chunks per rank, at most (S >= 2)
+    uint4 rpre[2 * KPRE];
+    if (epw && resid && m < M) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) red[(c0 - p0 + j) * 128 + m_local] = v[j];
-      }
-      cluster_sync_all();
-      const int pe = p1 < n_here ? p1 : n_here;
-      for (int c0 = p0 + rank * 16; c0 < (epw ? pe : p0); c0 += a.splits * 16) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float part[8];
-#pragma unroll
-          for (int sp = 0; sp < 8; ++sp)
-            part[sp] = sp < a.splits ? ld_peer(&red[(c0 - p0 + j) * 128 + m_local], (uint32_t)sp)
-                                     : 0.f;
-          float sum = 0.f;
-#pragma unroll
-          for (int sp = 0; sp < 8; ++sp) sum += part[sp];
-          v[j] = sum;
+      for (int k = 0; k < KPRE; ++k) {
+        const int u = rank + k * S;
+        if (u < nch && u * 16 + 16 <= n_here) {
+          const uint4* r = reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(epi.resid) + (size_t)m * epi.ld + n_tile * BN + u * 16);
+          rpre[2 * k] = __ldcg(r);
+          rpre[2 * k + 1] = __ldcg(r + 1);
         }
-        if (m < M) epi_chunk16(epi, m, n_tile * BN + c0, min(16, n_here - c0), v);
       }
-      cluster_sync_all();  // partners keep their shared memory until all reads are done
+    }
+    cluster_sync_all();
+    if (epw) {
+#pragma unroll 1
+      for (int u = 0; u < nch; ++u) {
+        const int owner = u % S;
+        if (owner == rank) continue;
+        tmem_ld16(trow + u * 16, v);
+        if (m < M) {
+          const int slot = rank < owner ? rank : rank - 1, k = u / S;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_peer4(recv + recv_off(slot, k, kmax, m_local, q), (uint32_t)owner,
+                     make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        }
+      }
+    }
+    cluster_sync_all();  // the pushed partials are visible to their owners
+    if (epw) {
+#pragma unroll 1
+      for (int k = 0; k < kmax; ++k) {
+        const int u = rank + k * S;
+        if (u >= nch) break;
+        float own[16];
+        tmem_ld16(trow + u * 16, own);
+        if (m < M) {  // a structured branch: the warp reconverges before the next tcgen05.ld
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.f;
+          for (int sp = 0; sp < S; ++sp) {
+            if (sp == rank) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += own[j];
+            } else {
+              const int slot = sp < rank ? sp : sp - 1;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float4 p = *reinterpret_cast<const float4*>(recv + recv_off(slot, k, kmax, m_local, q));
+                v[4 * q] += p.x;
+                v[4 * q + 1] += p.y;
+                v[4 * q + 2] += p.z;
+                v[4 * q + 3] += p.w;
+              }
+            }
+          }
+          const int n0 = n_tile * BN + u * 16, nc = min(16, n_here - u * 16);
+          bool pre = false;
+#pragma unroll
+          for (int kk = 0; kk < KPRE; ++kk)
+            if (kk == k && resid && nc == 16) {
+              epi_resid16(epi, m, n0, v, rpre[2 * kk], rpre[2 * kk + 1]);
+              pre = true;
+            }
+          if (kv_tm)
+            epi_ssm_chunk16(epi, m, n0, nc, v, ro_tm);
+          else if (!pre)
+            epi_chunk16(epi, m, n0, nc, v);
+        }
+      }
     }
   } else {
     // Split-K: this CTA's partial tile goes to its own shared memory (the

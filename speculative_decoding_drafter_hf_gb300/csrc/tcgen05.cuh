@@ -72,6 +72,84 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
 }
 
+// Residual epilogue of 16 columns of row m (ld % 8 == 0) whose residual
+// bf16 values r0 | r1 the caller has loaded: out = bf16(resid + v).
+__device__ __forceinline__ void epi_resid16(const Epi& e, int m, int n0, const float* v, uint4 r0,
+                                            uint4 r1) {
+  uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(e.out_t) + (size_t)m * e.ld + n0);
+  const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&r0);
+  const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&r1);
+  uint4 w0, w1;
+  __nv_bfloat162* c2 = reinterpret_cast<__nv_bfloat162*>(&w0);
+  __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(&w1);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 fa = __bfloat1622float2(a2[q]), fb = __bfloat1622float2(b2[q]);
+    c2[q] = __floats2bfloat162_rn(fa.x + v[2 * q], fa.y + v[2 * q + 1]);
+    d2[q] = __floats2bfloat162_rn(fb.x + v[8 + 2 * q], fb.y + v[8 + 2 * q + 1]);
+  }
+  o[0] = w0;
+  o[1] = w1;
+}
+
+// Commit-projection epilogue (EPI_SSM_KV) of 16 columns of row m whose
+// ring-row offset ro the caller has computed (ssm_kv_row; -1: the row is
+// skipped).
+__device__ __forceinline__ void epi_ssm_chunk16(const Epi& e, int m, int n0, int ncols,
+                                                const float* v, long long ro) {
+  const Dims& d = e.d;
+  if (ro < 0) return;
+  // the 16 columns usually fall in one region (one ring head, or the x / B /
+  // dt block): one column look-up and 16-byte stores then
+  const SsmCol k0 = ssm_col(e, n0);
+  if (ncols == 16) {
+    const SsmCol k15 = ssm_col(e, n0 + 15);
+    if (k0.kind == 1 && k15.kind == 1 && k15.ring == k0.ring && k15.base == k0.base + 15) {
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(k0.ring) + k0.base + ro;
+      if ((reinterpret_cast<uintptr_t>(o) & 15) == 0) {
+        uint4 w[2];
+        __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(w);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w2[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+        reinterpret_cast<uint4*>(o)[0] = w[0];
+        reinterpret_cast<uint4*>(o)[1] = w[1];
+        return;
+      }
+    } else if (k0.kind >= 2 && k15.kind == k0.kind && k15.base == k0.base + 15) {
+      float* o = e.xbd + k0.base + (size_t)m * d.NS;
+      if ((reinterpret_cast<uintptr_t>(o) & 15) == 0) {
+        float x[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) x[q] = v[q];
+        if (k0.kind == 3) {  // dt columns: softplus with each head's bias
+          const int layer = e.layer0 + n0 / e.cols_per_layer;
+          const int h0 = (n0 % e.cols_per_layer + e.col_off) - 2 * d.KVD - d.dinner - d.N;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) x[q] = softplus_f(v[q] + __ldg(&e.dt_bias[layer * d.Hm + h0 + q]));
+        } else if (k0.kind == 4) {  // gated-delta writing strength
+#pragma unroll
+          for (int q = 0; q < 16; ++q) x[q] = sigmoid_f(v[q]);
+        }
+        float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o4[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        return;
+      }
+    }
+  }
+  for (int j = 0; j < ncols; ++j) ssm_store<__nv_bfloat16>(e, ssm_col(e, n0 + j), m, ro, v[j]);
+}
+
+// The committed-row part of the commit epilogue for row m: its ring-row
+// offset (-1: not a committed row). n0 is the first column the caller will
+// store for the row (column 0 also records the row's position snapshot).
+__device__ __forceinline__ long long ssm_kv_row(const Epi& e, int m, int n0) {
+  int b;
+  long long p;
+  epi_row(e, m, b, p, n0);
+  return ssm_row_off(e.d, b, p);
+}
+
 // Token-major epilogue (swap = 0: output row m = this thread's accumulator
 // lane, 16 consecutive output columns n0..n0+15): loads that depend only on
 // the row (decay weight of the column's head, segment decay of the row's
@@ -105,70 +183,13 @@ __device__ __forceinline__ void epi_chunk16(const Epi& e, int m, int n0, int nco
     return;
   }
   if (e.kind == EPI_RESID && ncols == 16 && e.ld % 8 == 0) {
-    const size_t i = (size_t)m * e.ld + n0;
-    const uint4* r = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(e.resid) + i);
-    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(e.out_t) + i);
-    const uint4 r0 = __ldcg(r), r1 = __ldcg(r + 1);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&r0);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&r1);
-    uint4 w0, w1;
-    __nv_bfloat162* c2 = reinterpret_cast<__nv_bfloat162*>(&w0);
-    __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(&w1);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 fa = __bfloat1622float2(a2[q]), fb = __bfloat1622float2(b2[q]);
-      c2[q] = __floats2bfloat162_rn(fa.x + v[2 * q], fa.y + v[2 * q + 1]);
-      d2[q] = __floats2bfloat162_rn(fb.x + v[8 + 2 * q], fb.y + v[8 + 2 * q + 1]);
-    }
-    o[0] = w0;
-    o[1] = w1;
+    const uint4* r = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(e.resid) +
+                                                    (size_t)m * e.ld + n0);
+    epi_resid16(e, m, n0, v, __ldcg(r), __ldcg(r + 1));
     return;
   }
-  if (e.kind == EPI_SSM_KV) {  // the row's request and position once per chunk
-    int b;
-    long long p;
-    epi_row(e, m, b, p, n0);
-    const long long ro = ssm_row_off(d, b, p);
-    if (ro < 0) return;
-    // the 16 columns usually fall in one region (one ring head, or the x / B /
-    // dt block): one column look-up and 16-byte stores then
-    const SsmCol k0 = ssm_col(e, n0);
-    if (ncols == 16) {
-      const SsmCol k15 = ssm_col(e, n0 + 15);
-      if (k0.kind == 1 && k15.kind == 1 && k15.ring == k0.ring && k15.base == k0.base + 15) {
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(k0.ring) + k0.base + ro;
-        if ((reinterpret_cast<uintptr_t>(o) & 15) == 0) {
-          uint4 w[2];
-          __nv_bfloat162* w2 = reinterpret_cast<__nv_bfloat162*>(w);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) w2[q] = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
-          reinterpret_cast<uint4*>(o)[0] = w[0];
-          reinterpret_cast<uint4*>(o)[1] = w[1];
-          return;
-        }
-      } else if (k0.kind >= 2 && k15.kind == k0.kind && k15.base == k0.base + 15) {
-        float* o = e.xbd + k0.base + (size_t)m * d.NS;
-        if ((reinterpret_cast<uintptr_t>(o) & 15) == 0) {
-          float x[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) x[q] = v[q];
-          if (k0.kind == 3) {  // dt columns: softplus with each head's bias
-            const int layer = e.layer0 + n0 / e.cols_per_layer;
-            const int h0 = (n0 % e.cols_per_layer + e.col_off) - 2 * d.KVD - d.dinner - d.N;
-#pragma unroll
-            for (int q = 0; q < 16; ++q) x[q] = softplus_f(v[q] + __ldg(&e.dt_bias[layer * d.Hm + h0 + q]));
-          } else if (k0.kind == 4) {  // gated-delta writing strength
-#pragma unroll
-            for (int q = 0; q < 16; ++q) x[q] = sigmoid_f(v[q]);
-          }
-          float4* o4 = reinterpret_cast<float4*>(o);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) o4[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-          return;
-        }
-      }
-    }
-    for (int j = 0; j < ncols; ++j) ssm_store<__nv_bfloat16>(e, ssm_col(e, n0 + j), m, ro, v[j]);
+  if (e.kind == EPI_SSM_KV) {
+    epi_ssm_chunk16(e, m, n0, ncols, v, ssm_kv_row(e, m, n0));
     return;
   }
   for (int j = 0; j < ncols; ++j) epi_apply<__nv_bfloat16>(e, m, n0 + j, v[j]);
