@@ -446,7 +446,8 @@ cudaError_t launch_gemm_fma(int dtype, const void* X, int ldx, const void* Wt, i
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb,
                            int N, int K, int swap, int splits, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches, const void* a_tiles = nullptr,
-                           int late_trigger = 0, int a_group_mtiles = 0, int q4 = 0);
+                           int late_trigger = 0, int a_group_mtiles = 0, int q4 = 0,
+                           int independent = 0);
 // Two swapped products with the same K in one launch (both A operands
 // pre-tiled): D0 = A0 B0^T with epilogue epi0, D1 = A1 B1^T with epi1.
 cudaError_t launch_gemm_tc_grouped(const void* a_tiles0, int M0, int gm0, const void* B0,

@@ -83,6 +83,9 @@ struct TcArgs {
                            // one bulk copy; NULL: A read through the tensor map
   int32_t* err;       // device error word
   int late_trigger;   // 1: signal dependents only after the dependency wait
+  int independent;    // 1: neither operand depends on earlier kernels (both are inputs
+                      //    of the call): the main loop runs without the dependency
+                      //    wait; only the epilogue waits
   // Grouped launch: m-tiles [mt0, ...) belong to a second product with the
   // same K (its own A tiles, B map, N and epilogue). mt0 = all m-tiles when
   // there is one product.
@@ -226,7 +229,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       else
         tma_load_2d(sA + st * A_BYTES, &ta, &full[st], (kb0 + i) * 64, m_tile * 128);
     };
-    if (a.prefetch_a) {
+    if (a.independent) {
+      for (int j = 0; j < pre; ++j) {
+        mbar_expect_tx(&full[j], STAGE_BYTES);
+        load_a(j, j);
+        tma_load_2d(sB + j * B_BYTES, tb, &full[j], (kb0 + j) * 64, n_tile * BN);
+      }
+    } else if (a.prefetch_a) {
       for (int j = 0; j < pre; ++j) {
         mbar_expect_tx(&full[j], STAGE_BYTES);
         load_a(j, j);
@@ -258,7 +267,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       tma_load_2d(sB + s * B_BYTES, tb, &full[s], (kb0 + i) * 64, n_tile * BN);
     }
     flags[1] = i;
-  } else if (a.late_trigger) {
+  } else if (a.late_trigger && !a.independent) {
     pdl_wait();
     pdl_trigger();
   }
@@ -324,6 +333,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
   }
   __syncwarp();
   pdl_wait();  // the epilogue writes memory earlier kernels may still read
+  if (a.independent && a.late_trigger) pdl_trigger();
   const int n_here = min(BN, N - n_tile * BN);
   if (warp >= 2 && epw && a.swap) {  // idle during the main loop: fetch the epilogue inputs
     const int t2 = tid - 64;
@@ -397,7 +407,35 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ C
       epi_apply<__nv_bfloat16>(epi, n, m, val);
     }
   };
-  if (a.splits == 1) {
+  // token-major fp32 output: each warp stages its 32 rows in the drained
+  // stage buffers and stores them a row at a time (the warp's 16-byte pieces
+  // contiguous) instead of 32 rows' pieces per store instruction
+  constexpr int FRS = BN + 4;  // staged row stride (floats): conflict-free
+  static_assert(4 * 32 * FRS * 4 <= STAGES * (A_BYTES + B_BYTES + PK_BYTES),
+                "stage buffers too small for the staged fp32 epilogue");
+  const bool f32_rows = !a.swap && epi.kind == EPI_F32 && epi.ld % 4 == 0 && n_here % 4 == 0;
+  if (a.splits == 1 && f32_rows) {
+    if (epw) {
+      float* stg = reinterpret_cast<float*>(smem) + (size_t)warp * 32 * FRS;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        tmem_ld16(trow + c0, v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<float4*>(&stg[lane * FRS + c0 + 4 * q]) =
+              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+      __syncwarp();
+      const int nv = n_here / 4;
+#pragma unroll 1
+      for (int r = 0; r < 32; ++r) {
+        const int mr = m_tile * 128 + warp * 32 + r;
+        if (mr >= M) break;
+        float4* o = reinterpret_cast<float4*>(epi.out + (size_t)mr * epi.ld + n_tile * BN);
+        for (int q = lane; q < nv; q += 32) o[q] = *reinterpret_cast<const float4*>(&stg[r * FRS + 4 * q]);
+      }
+    }
+  } else if (a.splits == 1) {
 #pragma unroll 1
     for (int c0 = 0; c0 < (epw ? BN : 0); c0 += 16) {
       tmem_ld16(trow + c0, v);
@@ -729,7 +767,7 @@ int tc_pick_splits(int M, int N, int K, int q4) {
 cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, long long ldb, int N,
                            int K, int swap, int splits, int32_t* err, const Epi& epi,
                            cudaStream_t st, int* launches, const void* a_tiles,
-                           int late_trigger, int a_group_mtiles, int q4) {
+                           int late_trigger, int a_group_mtiles, int q4, int independent) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   if (q4 && (!a_tiles || !swap || N > 32)) return cudaErrorInvalidValue;
   int bn = 16;
@@ -747,6 +785,7 @@ cudaError_t launch_gemm_tc(const void* A, long long lda, int M, const void* B, l
   a.splits = std::max(1, std::min(std::min(splits, 8), a.kblocks));
   a.a_tiles = static_cast<const uint8_t*>(a_tiles);
   a.late_trigger = late_trigger;
+  a.independent = independent;
   a.mt0 = m_tiles;
   a.a_gm0 = a.a_gm1 = a_group_mtiles > 0 ? a_group_mtiles : m_tiles;
   CUtensorMap ma, mb;

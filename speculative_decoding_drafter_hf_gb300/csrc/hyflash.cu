@@ -1228,9 +1228,11 @@ hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
                                                  h->err, plain_commit_epi(h, n_accepted),
                                                  h->num_sms, st, &sc.count);
       if (e == cudaSuccess)
+        // (slot embeddings and weights are inputs of the call: the slot
+        // projection's main loop overlaps the commit projection's last tiles)
         e = hf::launch_gemm_tc(slot_emb, d.D, N1, h->w_draft, d.D, d.Nd, d.D, 0,
                                hf::tc_pick_splits(N1, d.Nd, d.D), h->err, e1, st, &sc.count, nullptr,
-                               /*late_trigger=*/1);
+                               /*late_trigger=*/1, 0, 0, /*independent=*/1);
       if (e != cudaSuccess) return cuda_fail(h, e, "round projection launches");
     }
     cudaError_t e =
