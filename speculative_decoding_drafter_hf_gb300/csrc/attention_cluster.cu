@@ -1035,19 +1035,36 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   cluster_sync_all();  // partners keep their shared memory until every read is done
 }
 
-// Memory read CTA (tensor-core form, see common.cuh): warp (m-tile, k-part)
-// loads its 16 state rows x (N / parts) columns straight into registers as
-// 16-byte loads (every 32-byte sector fully used), the whole head in flight
-// at once; the next head's loads are issued as soon as the current head's
-// fragments are consumed.
+// 16-byte asynchronous copy global -> shared, and its group bookkeeping
+// (per thread: a group completes once every copy the thread committed to it
+// has landed).
+__device__ __forceinline__ void ca_copy16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void ca_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int NPEND>
+__device__ __forceinline__ void ca_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(NPEND) : "memory");
+}
+
+// Memory read CTA (tensor-core form, see common.cuh) over its heads: each
+// head's state (P x N fp32, contiguous) is copied into one of MEM_NBUF
+// shared-memory buffers by 16-byte asynchronous copies of the whole CTA (a
+// warp moves one 512-byte row), MEM_NBUF - 1 heads ahead of the one being
+// read, rows padded to N + 4 floats so that the fragment loads below are
+// conflict-free. Warp (m-tile, k-part) reads its 16 rows x (N / parts)
+// columns from the buffer and multiplies them with the C rows on mma.sync
+// (tf32); the k-parts are summed through shared memory.
 __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int idx) {
   const Dims& d = a.d;
   const int nhb = (d.Hm + a.hpc - 1) / a.hpc;
   const int b = idx / nhb, hd0 = (idx % nhb) * a.hpc;
   const int nh = min(d.Hm, hd0 + a.hpc) - hd0;
-  const int P = d.P, N = d.N, S = d.S;
+  const int P = d.P, N = d.N, S = d.S, RS = N + 4;
   const int MT = P / 16, KSPL = mem_ksplit(d), G16 = N / 16 / KSPL;
-  float* red = reinterpret_cast<float*>(sm_raw);  // [KSPL][P][8]
+  float* sbuf = reinterpret_cast<float*>(sm_raw);             // [MEM_NBUF][P][RS]
+  float* red = sbuf + (size_t)MEM_NBUF * P * RS;              // [KSPL][P][8]
+  float* qn = red + (size_t)KSPL * P * 8;                     // gated delta: 1/|C_s|
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g8 = lane >> 2, t4 = lane & 3;
   const int mt = warp % MT, kp = warp / MT;
@@ -1055,19 +1072,23 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
   const int r0 = mt * 16 + g8;
   const int col0 = kp * G16 * 16 + 4 * t4;  // this lane's first column
   const bool state_early = (a.early & EARLY_STATE) != 0;
-  if (!state_early) pdl_wait();
   const float* hb0 = a.state + ((size_t)b * d.Hm + hd0) * P * N;
-  float4 hv[2][MEM_G16];
-  auto load = [&](int i) {
-    const float* hb = hb0 + (size_t)i * P * N;
-#pragma unroll
-    for (int j = 0; j < MEM_G16; ++j)
-      if (j < G16) {
-        hv[0][j] = __ldcg(reinterpret_cast<const float4*>(hb + (size_t)r0 * N + col0 + j * 16));
-        hv[1][j] = __ldcg(reinterpret_cast<const float4*>(hb + (size_t)(r0 + 8) * N + col0 + j * 16));
+  const int nq = P * N / 4, qpr = N / 4;
+  // head i into buffer i % MEM_NBUF (one commit group per call, also when
+  // there is no head i, so that every thread's group count stays in step)
+  auto issue = [&](int i) {
+    if (i < nh) {
+      const float* hb = hb0 + (size_t)i * P * N;
+      float* dst = sbuf + (size_t)(i % MEM_NBUF) * P * RS;
+      for (int q = tid; q < nq; q += blockDim.x) {
+        const int r = q / qpr, c4 = (q - r * qpr) * 4;
+        ca_copy16(dst + r * RS + c4, hb + (size_t)r * N + c4);
       }
+    }
+    ca_commit();
   };
-  if (active && nh > 0) load(0);
+  if (!state_early) pdl_wait();
+  for (int i = 0; i < MEM_NBUF - 1; ++i) issue(i);
   if (state_early) pdl_wait();  // C comes from the previous launch
   // B fragments (C of this request, slot g8), held for all heads
   uint32_t bf[MEM_G16][4];
@@ -1083,21 +1104,27 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
       bf[j][3] = to_tf32(c.w);
     }
   }
-  float* qn = red + (size_t)KSPL * P * 8;  // gated delta: 1/|C_s|
   if (d.gdn) slot_inv_norms(a.proj + (size_t)b * S * d.Nd + d.QD + 2 * d.KVD, d.Nd, S, N, qn);
   __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
   for (int i = 0; i < nh; ++i) {
+    // the buffer of head i + MEM_NBUF - 1 held head i - 1, read by every warp
+    // before the barrier after its partial sums
+    issue(i + MEM_NBUF - 1);
+    ca_wait<MEM_NBUF - 1>();  // this thread's copies of head i have landed
+    __syncthreads();          // and everyone's; the previous head's sums are read
     if (active) {
+      const float* hs = sbuf + (size_t)(i % MEM_NBUF) * P * RS;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < MEM_G16; ++j)
         if (j < G16) {
-          mma_tf32_1688(c, to_tf32(hv[0][j].x), to_tf32(hv[1][j].x), to_tf32(hv[0][j].y),
-                        to_tf32(hv[1][j].y), bf[j][0], bf[j][1]);
-          mma_tf32_1688(c, to_tf32(hv[0][j].z), to_tf32(hv[1][j].z), to_tf32(hv[0][j].w),
-                        to_tf32(hv[1][j].w), bf[j][2], bf[j][3]);
+          const float4 h0 = *reinterpret_cast<const float4*>(hs + r0 * RS + col0 + j * 16);
+          const float4 h1 = *reinterpret_cast<const float4*>(hs + (r0 + 8) * RS + col0 + j * 16);
+          mma_tf32_1688(c, to_tf32(h0.x), to_tf32(h1.x), to_tf32(h0.y), to_tf32(h1.y), bf[j][0],
+                        bf[j][1]);
+          mma_tf32_1688(c, to_tf32(h0.z), to_tf32(h1.z), to_tf32(h0.w), to_tf32(h1.w), bf[j][2],
+                        bf[j][3]);
         }
-      if (i + 1 < nh) load(i + 1);  // next head in flight during the reduction
       // c: (row r0, slots 2t4, 2t4+1), (row r0 + 8, same slots)
       float* rp = red + ((size_t)kp * P + r0) * 8 + 2 * t4;
       *reinterpret_cast<float2*>(rp) = make_float2(c[0], c[1]);
@@ -1111,8 +1138,8 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
       if (d.gdn) y *= qn[sl];
       mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)(hd0 + i) * P + p] = __float2bfloat16_rn(y);
     }
-    __syncthreads();  // partial sums read before the next head overwrites them
   }
+  ca_wait<0>();  // no copy outlives the CTA (the trailing groups are empty)
 }
 
 template <int DH>

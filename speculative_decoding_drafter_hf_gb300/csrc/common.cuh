@@ -386,8 +386,11 @@ __host__ __device__ inline int mem_ksplit(const Dims& d) {
   while (ks > 1 && (d.N / 16) % ks) --ks;
   return ks;
 }
+// Staged heads in flight per memory-read CTA of the attention launch (rows
+// padded to N + 4 floats), then the partial sums and 1/|C_s| (gated delta).
+constexpr int MEM_NBUF = 3;
 __host__ __device__ inline size_t mem_tc_bytes(const Dims& d) {
-  return (size_t)mem_ksplit(d) * d.P * 8 * 4 + 16 * 4;  // partial sums, 1/|C_s| (gated delta)
+  return (size_t)MEM_NBUF * d.P * (d.N + 4) * 4 + (size_t)mem_ksplit(d) * d.P * 8 * 4 + 16 * 4;
 }
 
 // Gated-delta read (q = C_s / |C_s|): 1/|C_s| of the S slot rows c0 + s*ld
