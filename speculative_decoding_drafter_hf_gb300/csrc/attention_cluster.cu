@@ -395,22 +395,6 @@ __device__ __forceinline__ void attn_cta(const Args& a, uint8_t* sm, int idx) {
   cluster_sync_all();  // partners keep their shared memory until every read is done
 }
 
-// Sum over the 32 lanes of each of 32 values: after the butterfly each lane
-// l holds the total of value l (31 shuffles instead of 32 x 5).
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool upper = (lane & half) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
-    }
-  }
-  return v[0];
-}
-
 template <typename T>
 __device__ __forceinline__ void mem_head(const Args& a, uint8_t* sm, int b, int hd) {
   const Dims& d = a.d;

@@ -693,6 +693,9 @@ commit_state_pipe_kernel(Dims d, int B, int early, int late, const int32_t* __re
     const int q = tid + u * PIPE_CT;
     pr[u] = q < nq ? q / cpr : 0;  // elements past the head: row 0, never stored
   }
+  // the fused memory read straight from the registers when every warp holds
+  // whole rows (N = 128) and the head fills the threads exactly
+  const bool reg_read = N == 128 && nq == PIPE_QPT * PIPE_CT && d.S <= 8 && PIPE_QPT * 8 <= 32;
   PipeCursor it = first;
   bool live = true;  // false after a wait gave up: the walk continues without work
   for (long long k = 0; it.l < d.L; ++k) {
@@ -714,18 +717,42 @@ commit_state_pipe_kernel(Dims d, int B, int early, int late, const int32_t* __re
       const int q = tid + u * PIPE_CT;
       hv[u] = live && q < nq ? s4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // h after rows 0..n-1 of h_t = e^{dt_t A} h_{t-1} + dt_t x_t B_t^T, unrolled:
+    // h_n = D h_0 + sum_t (c_t dt_t) x_t B_t^T with c_t the product of the
+    // decays of the rows after t (<= 1) and D that of all n. Lane t of each
+    // warp forms row t's decay; a suffix-product scan by shuffles gives c_t
+    // and D, so the per-element work per row is one FMA.
     const float A = live ? -expf(sdt[lim]) : 0.f;
+    float dt_l = 0.f, suf = 1.f;
+    if (lane < n) {
+      dt_l = sdt[lane];
+      suf = expf(dt_l * A);
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {  // suf = prod over rows >= lane
+      const float v = __shfl_down_sync(0xffffffffu, suf, o);
+      if (lane + o < 32) suf *= v;
+    }
+    const float after = __shfl_down_sync(0xffffffffu, suf, 1);
+    const float wdt = (lane < 31 ? after : 1.f) * dt_l;  // c_t dt_t at lane t
+    const float D = __shfl_sync(0xffffffffu, suf, 0);
+#pragma unroll
+    for (int u = 0; u < PIPE_QPT; ++u) {
+      hv[u].x *= D;
+      hv[u].y *= D;
+      hv[u].z *= D;
+      hv[u].w *= D;
+    }
     for (int t = 0; t < n; ++t) {
-      const float dt = sdt[t];
-      const float dec = expf(dt * A);
+      const float w = __shfl_sync(0xffffffffu, wdt, t);
       const float4 Bv = *reinterpret_cast<const float4*>(&sb[t * N + c4]);
 #pragma unroll
       for (int u = 0; u < PIPE_QPT; ++u) {
-        const float xv = dt * sx[t * P + pr[u]];
-        hv[u].x = fmaf(dec, hv[u].x, xv * Bv.x);
-        hv[u].y = fmaf(dec, hv[u].y, xv * Bv.y);
-        hv[u].z = fmaf(dec, hv[u].z, xv * Bv.z);
-        hv[u].w = fmaf(dec, hv[u].w, xv * Bv.w);
+        const float xv = w * sx[t * P + pr[u]];
+        hv[u].x = fmaf(xv, Bv.x, hv[u].x);
+        hv[u].y = fmaf(xv, Bv.y, hv[u].y);
+        hv[u].z = fmaf(xv, Bv.z, hv[u].z);
+        hv[u].w = fmaf(xv, Bv.w, hv[u].w);
       }
     }
     if (live && n > 0) {
@@ -736,7 +763,29 @@ commit_state_pipe_kernel(Dims d, int B, int early, int late, const int32_t* __re
         if (q < nq) __stcs(&hg[q], hv[u]);
       }
     }
-    if (rd && l == 0) {
+    if (rd && l == 0 && reg_read) {
+      // memory read of the new state from the registers: warp w holds rows
+      // w + 16u (u < 4) whole, 4 columns per lane; per (row, slot) a partial
+      // dot product over the lane's columns, then one butterfly over the
+      // warp leaves lane 8u + s with y[s][row u]
+      const float* sc = reinterpret_cast<const float*>(sg + L.off_c);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2)
+        if (s2 < d.S) {
+          const float4 c = *reinterpret_cast<const float4*>(&sc[s2 * N + c4]);
+#pragma unroll
+          for (int u = 0; u < PIPE_QPT; ++u)
+            v[u * 8 + s2] = hv[u].x * c.x + hv[u].y * c.y + hv[u].z * c.z + hv[u].w * c.w;
+        }
+      const float y = reduce_scatter32(v, lane);
+      const int u = lane >> 3, sl = lane & 7;
+      const int row = (tid + u * PIPE_CT) / cpr;  // pr[u], without indexing it at run time
+      if (live && sl < d.S)
+        mix[((size_t)b * d.S + sl) * d.Nz + d.QD + (size_t)h * P + row] = from_f<T>(y);
+    } else if (rd && l == 0) {
       // memory read of the new state (tensor cores, as the per-head kernel);
       // the consumers synchronise among themselves (named barrier 1)
       const int RS = N + 8;
@@ -870,7 +919,7 @@ cudaError_t launch_commit_state(int dtype, const Dims& d, int B, const int32_t* 
   const size_t smem = commit_state_smem(d, memC != nullptr);
   // large batches of the plain Mamba-2 memory: the pipelined persistent walk
   const PipeLayout pl = pipe_layout(d, memC != nullptr);
-  if (!d.gdn && d.Mr == 0 && d.Mh == 0 && whole && pl.total <= 232448 &&
+  if (!d.gdn && d.Mr == 0 && d.Mh == 0 && whole && pl.total <= 232448 && d.S + 1 <= 32 &&
       nq <= PIPE_QPT * PIPE_THREADS && B <= PIPE_MAXB &&
       (long long)B * d.Hm * d.L >= 8LL * num_sms && (long long)B * d.Hm * d.L < (1LL << 30)) {
     const long long items = (long long)B * d.Hm * d.L;

@@ -386,6 +386,22 @@ __host__ __device__ inline int mem_ksplit(const Dims& d) {
   while (ks > 1 && (d.N / 16) % ks) --ks;
   return ks;
 }
+// Sum over the 32 lanes of each of 32 values: after the butterfly each lane
+// l holds the total of value l (31 shuffles instead of 32 x 5).
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool upper = (lane & half) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+    }
+  }
+  return v[0];
+}
+
 // Staged heads in flight per memory-read CTA of the attention launch (rows
 // padded to N + 4 floats), then the partial sums and 1/|C_s| (gated delta).
 constexpr int MEM_NBUF = 3;
