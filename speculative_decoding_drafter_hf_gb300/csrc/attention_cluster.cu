@@ -55,6 +55,8 @@ struct Args {
   int n_attn;     // attention CTAs = B * Hkv * nsplit
   int n_mem;      // memory-read CTAs = B * ceil(Hm / hpc)
   int hpc;        // memory heads per memory-read CTA
+  int mem0;       // tensor-core launch: CTAs before the attention CTAs (the
+                  // memory-read CTAs, padded to whole clusters)
   int mem_tc;     // 1: memory read on the tensor cores (tf32 mma.sync)
   int ntile;      // tensor-core path: 64-key window tiles per CTA
   float qscale;   // log2(e) / sqrt(dh)
@@ -1019,36 +1021,30 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
   cluster_sync_all();  // partners keep their shared memory until every read is done
 }
 
-// 16-byte asynchronous copy global -> shared, and its group bookkeeping
-// (per thread: a group completes once every copy the thread committed to it
-// has landed).
-__device__ __forceinline__ void ca_copy16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void ca_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int NPEND>
-__device__ __forceinline__ void ca_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(NPEND) : "memory");
-}
-
 // Memory read CTA (tensor-core form, see common.cuh) over its heads: each
-// head's state (P x N fp32, contiguous) is copied into one of MEM_NBUF
-// shared-memory buffers by 16-byte asynchronous copies of the whole CTA (a
-// warp moves one 512-byte row), MEM_NBUF - 1 heads ahead of the one being
-// read, rows padded to N + 4 floats so that the fragment loads below are
-// conflict-free. Warp (m-tile, k-part) reads its 16 rows x (N / parts)
-// columns from the buffer and multiplies them with the C rows on mma.sync
-// (tf32); the k-parts are summed through shared memory.
-__device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int idx) {
+// head's state (P x N fp32) arrives by TMA in one of MEM_NBUF shared-memory
+// buffers, MEM_NBUF - 1 heads ahead of the one being read, as 128-byte
+// column groups of P rows in the 128-byte swizzle (16-byte chunk c of row r
+// at chunk c ^ (r & 7)), so that the fragment loads below are conflict-free.
+// Warp (m-tile, k-part) reads its 16 rows x (N / parts) columns from the
+// buffer and multiplies them with the C rows on mma.sync (tf32); the k-parts
+// are summed through shared memory. Every wait is bounded; on expiry the CTA
+// raises ERR_TIMEOUT, lets the copies it issued land (bounded) and returns.
+__device__ __forceinline__ void mem_tc_cta(const Args& a, const CUtensorMap* ms, uint8_t* sm_raw,
+                                           int idx) {
   const Dims& d = a.d;
   const int nhb = (d.Hm + a.hpc - 1) / a.hpc;
   const int b = idx / nhb, hd0 = (idx % nhb) * a.hpc;
   const int nh = min(d.Hm, hd0 + a.hpc) - hd0;
-  const int P = d.P, N = d.N, S = d.S, RS = N + 4;
+  const int P = d.P, N = d.N, S = d.S;
   const int MT = P / 16, KSPL = mem_ksplit(d), G16 = N / 16 / KSPL;
-  float* sbuf = reinterpret_cast<float*>(sm_raw);             // [MEM_NBUF][P][RS]
-  float* red = sbuf + (size_t)MEM_NBUF * P * RS;              // [KSPL][P][8]
-  float* qn = red + (size_t)KSPL * P * 8;                     // gated delta: 1/|C_s|
+  const size_t SB = mem_stage_bytes(d);
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sbuf = sm;                                                   // [MEM_NBUF][groups][P][128 B]
+  float* red = reinterpret_cast<float*>(sm + MEM_NBUF * SB);          // [KSPL][P][8]
+  float* qn = red + (size_t)KSPL * P * 8;                              // gated delta: 1/|C_s|
+  uint64_t* bar = reinterpret_cast<uint64_t*>(qn + 16);               // [MEM_NBUF]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int g8 = lane >> 2, t4 = lane & 3;
   const int mt = warp % MT, kp = warp / MT;
@@ -1056,23 +1052,25 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
   const int r0 = mt * 16 + g8;
   const int col0 = kp * G16 * 16 + 4 * t4;  // this lane's first column
   const bool state_early = (a.early & EARLY_STATE) != 0;
-  const float* hb0 = a.state + ((size_t)b * d.Hm + hd0) * P * N;
-  const int nq = P * N / 4, qpr = N / 4;
-  // head i into buffer i % MEM_NBUF (one commit group per call, also when
-  // there is no head i, so that every thread's group count stays in step)
-  auto issue = [&](int i) {
-    if (i < nh) {
-      const float* hb = hb0 + (size_t)i * P * N;
-      float* dst = sbuf + (size_t)(i % MEM_NBUF) * P * RS;
-      for (int q = tid; q < nq; q += blockDim.x) {
-        const int r = q / qpr, c4 = (q - r * qpr) * 4;
-        ca_copy16(dst + r * RS + c4, hb + (size_t)r * N + c4);
-      }
-    }
-    ca_commit();
+  const int ngroups = (N + 31) / 32;
+  const int y0 = (b * d.Hm + hd0) * P;  // first state row of this CTA's heads
+  auto issue = [&](int i) {  // head i into buffer i % MEM_NBUF (thread 0)
+    uint8_t* dst = sbuf + (size_t)(i % MEM_NBUF) * SB;
+    uint64_t* br = &bar[i % MEM_NBUF];
+    mbar_expect_tx(br, (uint32_t)SB);
+    for (int g = 0; g < ngroups; ++g)
+      tma_load_2d(dst + (size_t)g * P * 128, ms, br, g * 32, y0 + i * P);
   };
+  const int pre = nh < MEM_NBUF - 1 ? nh : MEM_NBUF - 1;
+  if (tid == 0) {
+    for (int k = 0; k < MEM_NBUF; ++k) mbar_init(&bar[k], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
   if (!state_early) pdl_wait();
-  for (int i = 0; i < MEM_NBUF - 1; ++i) issue(i);
+  if (tid == 0)
+    for (int i = 0; i < pre; ++i) issue(i);
   if (state_early) pdl_wait();  // C comes from the previous launch
   // B fragments (C of this request, slot g8), held for all heads
   uint32_t bf[MEM_G16][4];
@@ -1090,20 +1088,30 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
   }
   if (d.gdn) slot_inv_norms(a.proj + (size_t)b * S * d.Nd + d.QD + 2 * d.KVD, d.Nd, S, N, qn);
   __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
+  int issued = pre, done = 0;
+  bool ok = true;
   for (int i = 0; i < nh; ++i) {
     // the buffer of head i + MEM_NBUF - 1 held head i - 1, read by every warp
     // before the barrier after its partial sums
-    issue(i + MEM_NBUF - 1);
-    ca_wait<MEM_NBUF - 1>();  // this thread's copies of head i have landed
-    __syncthreads();          // and everyone's; the previous head's sums are read
+    if (tid == 0 && issued < nh && issued == i + MEM_NBUF - 1) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(issued++);
+    }
+    ok = mbar_wait(&bar[i % MEM_NBUF], (uint32_t)((i / MEM_NBUF) & 1));
+    if (!__syncthreads_and(ok)) break;  // and the previous head's sums are read
+    done = i + 1;
     if (active) {
-      const float* hs = sbuf + (size_t)(i % MEM_NBUF) * P * RS;
+      const uint8_t* hs = sbuf + (size_t)(i % MEM_NBUF) * SB;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < MEM_G16; ++j)
         if (j < G16) {
-          const float4 h0 = *reinterpret_cast<const float4*>(hs + r0 * RS + col0 + j * 16);
-          const float4 h1 = *reinterpret_cast<const float4*>(hs + (r0 + 8) * RS + col0 + j * 16);
+          const int col = col0 + j * 16;  // 4 columns: one 16-byte chunk of a 128-byte group
+          const uint8_t* gb = hs + (size_t)(col >> 5) * P * 128;
+          const int ch = (col & 31) >> 2;
+          const float4 h0 = *reinterpret_cast<const float4*>(gb + r0 * 128 + ((ch ^ (r0 & 7)) << 4));
+          const float4 h1 =
+              *reinterpret_cast<const float4*>(gb + (r0 + 8) * 128 + ((ch ^ ((r0 + 8) & 7)) << 4));
           mma_tf32_1688(c, to_tf32(h0.x), to_tf32(h1.x), to_tf32(h0.y), to_tf32(h1.y), bf[j][0],
                         bf[j][1]);
           mma_tf32_1688(c, to_tf32(h0.z), to_tf32(h1.z), to_tf32(h0.w), to_tf32(h1.w), bf[j][2],
@@ -1123,25 +1131,33 @@ __device__ __forceinline__ void mem_tc_cta(const Args& a, uint8_t* sm_raw, int i
       mix[((size_t)b * S + sl) * d.Nz + d.QD + (size_t)(hd0 + i) * P + p] = __float2bfloat16_rn(y);
     }
   }
-  ca_wait<0>();  // no copy outlives the CTA (the trailing groups are empty)
+  if (!ok && tid == 0) {
+    // a copy never completed: report, and let the copies in flight land
+    // (bounded) before the shared memory is released
+    atomicOr(a.err, ERR_TIMEOUT);
+    for (int i = done; i < issued; ++i) mbar_wait(&bar[i % MEM_NBUF], (uint32_t)((i / MEM_NBUF) & 1));
+  }
 }
 
 template <int DH>
 __global__ void __launch_bounds__(THREADS, 2)
-attn_tc_kernel(Args a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv) {
+attn_tc_kernel(Args a, const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+               const __grid_constant__ CUtensorMap ms) {
   extern __shared__ __align__(128) uint8_t sm[];
   pdl_trigger();
+  // the memory-read CTAs first (few, long-lived), then the attention CTAs
+  // (many, short: they pack the launch's tail)
   const int idx = blockIdx.x;
-  if (idx < a.n_attn)
-    attn_tc_cta<DH>(a, &mk, &mv, sm, idx);
-  else if (idx < a.n_attn + a.n_mem) {
+  if (idx < a.n_mem) {
     if (a.mem_tc)
-      mem_tc_cta(a, sm, idx - a.n_attn);
+      mem_tc_cta(a, &ms, sm, idx);
     else
-      mem_cta<__nv_bfloat16>(a, sm, idx - a.n_attn);
-  }
-  else
+      mem_cta<__nv_bfloat16>(a, sm, idx);
+  } else if (idx >= a.mem0 && idx - a.mem0 < a.n_attn) {
+    attn_tc_cta<DH>(a, &mk, &mv, sm, idx - a.mem0);
+  } else {
     pdl_wait();  // cluster padding
+  }
 }
 
 // E = head_dim / 16: the slice of a key each lane of a half-warp holds.
@@ -1245,8 +1261,9 @@ static Plan make_tc_plan(const Dims& d, int B, int num_sms, int* ntile) {
 cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
                                 const float* state, void* mix, const CUtensorMap* mk,
-                                const CUtensorMap* mv, int32_t* err, int num_sms, int early,
-                                int with_mem, cudaStream_t st, int* launches) {
+                                const CUtensorMap* mv, const CUtensorMap* ms, int32_t* err,
+                                int num_sms, int early, int with_mem, cudaStream_t st,
+                                int* launches) {
   if (B <= 0) return cudaSuccess;
   const bool tc = attn_uses_tc(d, dtype) && mk && mv;
   Args a{};
@@ -1256,11 +1273,18 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   else
     a.plan = make_plan(d.W);
   a.n_attn = B * d.Hkv * a.plan.nsplit;
-  // memory-read CTAs: one head each up to ~8 CTAs per SM, then several
-  a.hpc = (B * d.Hm + 8 * num_sms - 1) / (8 * num_sms);
+  a.mem_tc = tc && mem_tc_ok(d) && ms ? 1 : 0;
+  if (a.mem_tc) {
+    // staged memory reads (their copies pipelined over the CTA's heads): about
+    // two long-lived CTAs per SM in all
+    const int per_req = std::max(1, 2 * num_sms / B);
+    a.hpc = (d.Hm + per_req - 1) / per_req;
+  } else {
+    // memory-read CTAs: one head each up to ~8 CTAs per SM, then several
+    a.hpc = (B * d.Hm + 8 * num_sms - 1) / (8 * num_sms);
+  }
   if (a.hpc < 1) a.hpc = 1;
   a.n_mem = with_mem ? B * ((d.Hm + a.hpc - 1) / a.hpc) : 0;
-  a.mem_tc = tc && mem_tc_ok(d) ? 1 : 0;
   a.qscale = 1.4426950408889634f / sqrtf((float)d.dh);
   a.proj = proj;
   a.ring_k = ring_k;
@@ -1271,7 +1295,9 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   a.err = err;
   a.early = tc ? early : 0;
   const int cz = a.plan.nsplit;
-  const int total = (a.n_attn + a.n_mem + cz - 1) / cz * cz;
+  a.mem0 = tc ? (a.n_mem + cz - 1) / cz * cz : 0;
+  const int total = tc ? a.mem0 + (a.n_attn + cz - 1) / cz * cz
+                       : (a.n_attn + a.n_mem + cz - 1) / cz * cz;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(total);
   cfg.blockDim = dim3(THREADS);
@@ -1290,9 +1316,11 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   ++*launches;
   if (tc) {
     switch (d.dh) {
-      case 64: return cudaLaunchKernelEx(&cfg, attn_tc_kernel<64>, a, *mk, *mv);
-      case 128: return cudaLaunchKernelEx(&cfg, attn_tc_kernel<128>, a, *mk, *mv);
-      case 256: return cudaLaunchKernelEx(&cfg, attn_tc_kernel<256>, a, *mk, *mv);
+      // (without a state map the memory-read CTAs take the CUDA-core form and
+      // the map argument is not read)
+      case 64: return cudaLaunchKernelEx(&cfg, attn_tc_kernel<64>, a, *mk, *mv, ms ? *ms : *mk);
+      case 128: return cudaLaunchKernelEx(&cfg, attn_tc_kernel<128>, a, *mk, *mv, ms ? *ms : *mk);
+      case 256: return cudaLaunchKernelEx(&cfg, attn_tc_kernel<256>, a, *mk, *mv, ms ? *ms : *mk);
     }
     return cudaErrorInvalidValue;
   }

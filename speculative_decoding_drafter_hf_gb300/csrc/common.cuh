@@ -402,11 +402,16 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
   return v[0];
 }
 
-// Staged heads in flight per memory-read CTA of the attention launch (rows
-// padded to N + 4 floats), then the partial sums and 1/|C_s| (gated delta).
+// Staged heads per memory-read CTA of the attention launch (each as
+// ceil(N / 32) swizzled 128-byte column groups of P rows), then the partial
+// sums, 1/|C_s| (gated delta) and one barrier per buffer.
 constexpr int MEM_NBUF = 3;
+__host__ __device__ inline size_t mem_stage_bytes(const Dims& d) {
+  return (size_t)((d.N + 31) / 32) * d.P * 128;
+}
 __host__ __device__ inline size_t mem_tc_bytes(const Dims& d) {
-  return (size_t)MEM_NBUF * d.P * (d.N + 4) * 4 + (size_t)mem_ksplit(d) * d.P * 8 * 4 + 16 * 4;
+  return (size_t)MEM_NBUF * mem_stage_bytes(d) + (size_t)mem_ksplit(d) * d.P * 8 * 4 + 16 * 4 +
+         MEM_NBUF * 8;
 }
 
 // Gated-delta read (q = C_s / |C_s|): 1/|C_s| of the S slot rows c0 + s*ld
@@ -528,6 +533,11 @@ int tc_pick_splits(int M, int N, int K, int q4 = 0);
 // box_rows, 128-byte swizzle (gemm_tc.cu).
 cudaError_t make_map(CUtensorMap* map, const void* base, long long rows, long long K, long long ld,
                      int box_rows);
+// 2-D fp32 tensor map over rows x cols (row stride cols), box 32 columns x
+// box_rows, 128-byte swizzle (gemm_tc.cu): the memory states of a layer,
+// one box column group of a head per copy.
+cudaError_t make_map_f32(CUtensorMap* map, const void* base, long long rows, long long cols,
+                         int box_rows);
 
 // One-time kernel attribute set-up (dynamic shared memory limits, driver
 // entry points, cluster occupancy), done at handle creation.
@@ -539,7 +549,9 @@ cudaError_t configure_attn_cluster(const Dims& d);
 // state of this layer; pos [Bmax]; mix [B*S, Nz] model dtype (O | y).
 // bf16 handles with head_dim % 64 == 0 run the tensor-core variant, which
 // loads ring tiles through the per-layer tensor maps mk / mv (rows =
-// Bmax*Hkv*W, box attn_tile_rows(d) rows); other handles pass NULL maps.
+// Bmax*Hkv*W, box attn_tile_rows(d) rows) and, when its memory read runs on
+// the tensor cores (mem_tc_ok), the layer's states through ms (make_map_f32
+// over rows Bmax*Hm*P, N columns, box P rows); other handles pass NULL maps.
 // early: what the previous launch (which signalled its dependents after its
 // own wait) leaves final at launch, read before this launch's wait:
 // bit 0 the ring K/V, bit 1 the positions and states, bit 2 the slot
@@ -551,8 +563,9 @@ bool attn_uses_tc(const Dims& d, int dtype);
 cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* proj,
                                 const void* ring_k, const void* ring_v, const int64_t* pos,
                                 const float* state, void* mix, const CUtensorMap* mk,
-                                const CUtensorMap* mv, int32_t* err, int num_sms, int early,
-                                int with_mem, cudaStream_t st, int* launches);
+                                const CUtensorMap* mv, const CUtensorMap* ms, int32_t* err,
+                                int num_sms, int early, int with_mem, cudaStream_t st,
+                                int* launches);
 
 // Commit state step, all layers: validates the accepted counts (error word),
 // writes the packed offsets (exclusive scan of the valid counts) and the ring

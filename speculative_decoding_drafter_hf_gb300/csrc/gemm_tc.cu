@@ -624,6 +624,23 @@ cudaError_t make_map(CUtensorMap* map, const void* base, long long rows, long lo
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 2-D fp32 tensor map over rows x cols (row stride cols elements, a multiple
+// of 4), box 32 columns (128 bytes) x box_rows, 128-byte swizzle.
+cudaError_t make_map_f32(CUtensorMap* map, const void* base, long long rows, long long cols,
+                         int box_rows) {
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * 4)};
+  cuuint32_t box[2] = {32u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 namespace {
 
 // Pipeline depth of the narrow tiles (skinny products at small batch): a

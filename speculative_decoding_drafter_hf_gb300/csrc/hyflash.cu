@@ -72,6 +72,7 @@ struct hf_handle {
   float* part = nullptr;
   size_t part_elems = 0;
   std::vector<CUtensorMap> ring_maps;  // per layer: K, V tile maps (tensor-core attention)
+  std::vector<CUtensorMap> state_maps; // per layer: the memory states (its memory-read CTAs)
   int* counters = nullptr;     // tile tickets of the stream-K GEMM (zero between launches)
   int n_counters = 0;
   float* skws = nullptr;       // stream-K partial tiles
@@ -610,6 +611,15 @@ hf_status hf_create(const hf_config* cfg, int32_t device, hf_handle** out) {
                          d.dh, hf::attn_tile_rows(d));
       if (e != cudaSuccess) s = cuda_fail(h, e, "ring tensor maps");
     }
+    if (s == HF_OK && hf::mem_tc_ok(d)) {
+      h->state_maps.resize(L);
+      const size_t sl_bytes = Bm * d.Hm * d.P * d.N * 4;
+      for (size_t l = 0; l < L && s == HF_OK; ++l) {
+        e = hf::make_map_f32(&h->state_maps[l], bptr(h->state, l * sl_bytes),
+                             (long long)Bm * d.Hm * d.P, d.N, d.P);
+        if (e != cudaSuccess) s = cuda_fail(h, e, "state tensor maps");
+      }
+    }
   }
   if (s == HF_OK) {
     e = hf::configure_attn_cluster(h->d);
@@ -939,10 +949,11 @@ hf_status draft_rest(hf_handle* h, int l, const void* X, void* Y, int batch, int
     Scope sc(h, HF_K_ATTN_MEM, st);
     const CUtensorMap* mk = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l];
     const CUtensorMap* mv = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l + 1];
+    const CUtensorMap* ms = h->state_maps.empty() ? nullptr : &h->state_maps[l];
     cudaError_t e = hf::launch_attn_cluster(h->cfg.dtype, d, batch, h->proj,
                                             bptr(h->ring_k, l * ring_ls),
                                             bptr(h->ring_v, l * ring_ls), h->pos,
-                                            h->state + l * state_ls, h->mix, mk, mv, h->err,
+                                            h->state + l * state_ls, h->mix, mk, mv, ms, h->err,
                                             h->num_sms, early, with_mem, st, &sc.count);
     if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
   }
@@ -988,9 +999,10 @@ hf_status draft_block_layer(hf_handle* h, int l, const void* X, void* Y, int bat
     Scope sc(h, HF_K_ATTN_MEM, st);
     const CUtensorMap* mk = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l];
     const CUtensorMap* mv = h->ring_maps.empty() ? nullptr : &h->ring_maps[2 * l + 1];
+    const CUtensorMap* ms = h->state_maps.empty() ? nullptr : &h->state_maps[l];
     e = hf::launch_attn_cluster(dt, d, batch, h->proj, bptr(h->ring_k, l * ring_ls),
                                 bptr(h->ring_v, l * ring_ls), h->pos, h->state + l * state_ls,
-                                h->mix, mk, mv, h->err, h->num_sms, 0, 1, st, &sc.count);
+                                h->mix, mk, mv, ms, h->err, h->num_sms, 0, 1, st, &sc.count);
     if (e != cudaSuccess) return cuda_fail(h, e, "attention launch");
   }
   {
