@@ -55,8 +55,8 @@ struct Args {
   int n_attn;     // attention CTAs = B * Hkv * nsplit
   int n_mem;      // memory-read CTAs = B * ceil(Hm / hpc)
   int hpc;        // memory heads per memory-read CTA
-  int mem0;       // tensor-core launch: CTAs before the attention CTAs (the
-                  // memory-read CTAs, padded to whole clusters)
+  int mem_first;  // tensor-core launch: 1 = memory-read CTAs before the attention CTAs
+  int mem0;       // tensor-core launch: CTAs of the first kind, padded to whole clusters
   int mem_tc;     // 1: memory read on the tensor cores (tf32 mma.sync)
   int ntile;      // tensor-core path: 64-key window tiles per CTA
   float qscale;   // log2(e) / sqrt(dh)
@@ -1145,16 +1145,20 @@ attn_tc_kernel(Args a, const __grid_constant__ CUtensorMap mk, const __grid_cons
                const __grid_constant__ CUtensorMap ms) {
   extern __shared__ __align__(128) uint8_t sm[];
   pdl_trigger();
-  // the memory-read CTAs first (few, long-lived), then the attention CTAs
-  // (many, short: they pack the launch's tail)
+  // launches of more than one wave: the memory-read CTAs first (few,
+  // long-lived), then the attention CTAs (many, short: they pack the
+  // launch's tail); a single wave: the attention CTAs (the critical path)
+  // first. Each kind starts on a whole cluster.
   const int idx = blockIdx.x;
-  if (idx < a.n_mem) {
+  const int att0 = a.mem_first ? a.mem0 : 0;  // first attention CTA
+  const int mem0 = a.mem_first ? 0 : a.mem0;  // first memory-read CTA
+  if (idx >= att0 && idx - att0 < a.n_attn) {
+    attn_tc_cta<DH>(a, &mk, &mv, sm, idx - att0);
+  } else if (idx >= mem0 && idx - mem0 < a.n_mem) {
     if (a.mem_tc)
-      mem_tc_cta(a, &ms, sm, idx);
+      mem_tc_cta(a, &ms, sm, idx - mem0);
     else
-      mem_cta<__nv_bfloat16>(a, sm, idx);
-  } else if (idx >= a.mem0 && idx - a.mem0 < a.n_attn) {
-    attn_tc_cta<DH>(a, &mk, &mv, sm, idx - a.mem0);
+      mem_cta<__nv_bfloat16>(a, sm, idx - mem0);
   } else {
     pdl_wait();  // cluster padding
   }
@@ -1295,9 +1299,10 @@ cudaError_t launch_attn_cluster(int dtype, const Dims& d, int B, const float* pr
   a.err = err;
   a.early = tc ? early : 0;
   const int cz = a.plan.nsplit;
-  a.mem0 = tc ? (a.n_mem + cz - 1) / cz * cz : 0;
-  const int total = tc ? a.mem0 + (a.n_attn + cz - 1) / cz * cz
-                       : (a.n_attn + a.n_mem + cz - 1) / cz * cz;
+  const int mem_pad = (a.n_mem + cz - 1) / cz * cz, attn_pad = (a.n_attn + cz - 1) / cz * cz;
+  a.mem_first = tc && a.n_attn + a.n_mem > 2 * num_sms ? 1 : 0;
+  a.mem0 = a.mem_first ? mem_pad : attn_pad;
+  const int total = tc ? mem_pad + attn_pad : (a.n_attn + a.n_mem + cz - 1) / cz * cz;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(total);
   cfg.blockDim = dim3(THREADS);
