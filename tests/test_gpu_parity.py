@@ -239,6 +239,16 @@ ATTN_SHAPES = {
     "w300_b80_one_cta": (dict(d_model=256, n_q_heads=8, n_kv_heads=4, head_dim=64, window=300,
                               ssm_heads=4, ssm_headdim=32, d_state=32),
                          [(37 * i) % 420 for i in range(80)]),
+    # one CTA per (request, KV head) at the serving shape's head dim (128) and
+    # query rows (28): partial and wrapped windows, and with cross-slot
+    # attention off
+    "w300_dh128_b80_one_cta": (dict(d_model=512, n_q_heads=16, n_kv_heads=4, head_dim=128,
+                                    window=300, ssm_heads=4, ssm_headdim=32, d_state=32),
+                               [(37 * i) % 420 for i in range(80)]),
+    "w300_dh128_b80_one_cta_xoff": (dict(d_model=512, n_q_heads=16, n_kv_heads=4, head_dim=128,
+                                         window=300, ssm_heads=4, ssm_headdim=32, d_state=32,
+                                         cross_slot=False),
+                                    [(53 * i) % 400 for i in range(80)]),
 }
 
 
