@@ -88,7 +88,8 @@ def sum_over_ranks(x: float, device=None) -> float:
 
 # ------------------------------------------------------------------ algorithmic sizes
 
-def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: bool):
+def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: bool,
+                num_sms: int = 0):
     """Bytes each step must move at minimum (weights, window, state and the
     slot / feature I/O read or written once), per kernel family of the path
     that runs: {family: (bytes per step, launches per step)}.
@@ -99,7 +100,9 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
     per step; later layers read their state again at draft time (their C
     depends on the layer below, which needs the updated state first).
     step_bytes is the fused figure: the least traffic any schedule of a
-    step needs.
+    step needs. With num_sms given, a wide batch whose commit product alone
+    has a 128 x 256 tile per SM counts two round-projection launches (the
+    commit projection on the persistent GEMM, then the slot projection).
 
     Memory horizon M (ablation): M = 1 writes the state without reading it;
     M > 1 also reads the leaving rows' and writes the new rows' x, B, dt
@@ -130,9 +133,12 @@ def algorithmic(cfg, batch: int, window_fill: float, mean_accept: float, fused: 
     if M > 1:
         state_io += L * (rows * 2 * (din + N + Hm) * 4 + batch * Hm * min(M, window_fill) * 4)
 
+    n0 = batch * (S + 1)
+    two = bool(num_sms) and n0 > 32 and (-(-n0 // 128)) * (-(-(L * Nc) // 256)) >= num_sms
+
     def fused_fams():
         return {
-            "round_proj": (w_commit + commit_io + w_draft + io_draft, 1),
+            "round_proj": (w_commit + commit_io + w_draft + io_draft, 2 if two else 1),
             "draft_proj": ((L - 1) * (w_draft + io_draft), L - 1),
             "commit_state": (L * state_rw * state + state_io + io_mem, 1),
             "attn_mem": (L * (window + io_attn) + (L - 1) * (state + io_mem), L),
@@ -728,7 +734,8 @@ def run_hyflash(args, cfg):
     tc_peak = float(peaks.get("bf16_tflops", 1900.0))
     peak_src = "measured" if peaks else "fallback"
     fill = sum(min(L, cfg.window) for L in lens) / max(len(lens), 1)  # valid window rows
-    alg = algorithmic(cfg, batch, fill, (cfg.block + 2) / 2.0, fused)
+    alg = algorithmic(cfg, batch, fill, (cfg.block + 2) / 2.0, fused,
+                      torch.cuda.get_device_properties(dev).multi_processor_count)
     fams = {k: v for k, v in alg["families"].items() if v[1] > 0}
     top = max(fams, key=lambda k: fam_ms.get(k, (0, 0))[0])
     ms_top, _ = fam_ms[top]
