@@ -277,8 +277,11 @@ hf_status hf_draft_tokens(hf_handle* h, const void* slot_emb, void* out, int32_t
  * window take the newly committed features, then the parallel block is
  * drafted against them). bf16 handles run it as one pipeline: the commit
  * projection and the first layer's slot projection stream their weights in
- * one grouped launch, and the first layer's memory read is computed on the
- * updated state inside the state update (the state is read once per
+ * one grouped launch (at a batch whose commit product alone has a 128 x 256
+ * tile per SM: the commit projection on the persistent GEMM, then the slot
+ * projection, whose main loop runs beside the commit projection's last
+ * tiles), and at large batch the first layer's memory read is computed on
+ * the updated state inside the state update (the state is read once per
  * round). Other handles call the two entry points in turn. */
 hf_status hf_round(hf_handle* h, const void* feats, const int32_t* n_accepted,
                    const void* slot_emb, void* out, int32_t batch, void* stream);
@@ -351,7 +354,7 @@ typedef enum {
   HF_K_DRAFT_PROJ = 0,   /* draft input projections (Q|K_s|V_s|C_s) */
   HF_K_ATTN_MEM = 1,     /* window+block attention and memory read */
   HF_K_OUT_PROJ = 2,     /* output projections + residual */
-  HF_K_ROUND_PROJ = 3,   /* hf_round: grouped commit + first slot projection */
+  HF_K_ROUND_PROJ = 3,   /* hf_round: commit + first slot projection (one or two launches) */
   HF_K_COMMIT_PROJ = 4,  /* commit projections + ring append */
   HF_K_COMMIT_STATE = 5, /* sequential memory update */
   HF_K_PREFILL = 6,      /* every prefill kernel */
