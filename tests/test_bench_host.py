@@ -88,6 +88,26 @@ def test_algorithmic_bytes_memory_horizon():
         "mem_horizon"] == 1
 
 
+def test_round_projection_launch_count():
+    """The serving batch's commit product (512 rows x 3 layers' columns) has
+    more 128 x 256 tiles than SMs: the round projection is two launches (the
+    commit projection, then the slot projection); one request's is one
+    grouped launch, and without an SM count the model keeps one."""
+    from workload import CONFIGS
+    serving = CONFIGS["serving_qwen3_4b_b64"]
+    Nc = 2 * 8 * 128 + 80 * 64 + 128 + 80
+    tiles = (64 * 8 // 128) * -(-(3 * Nc) // 256)
+    assert tiles >= 152
+    fam = bench.algorithmic(serving, 64, 512, 4.5, True, 152)["families"]
+    assert fam["round_proj"][1] == 2
+    assert bench.algorithmic(serving, 64, 512, 4.5, True)["families"]["round_proj"][1] == 1
+    c1 = CONFIGS["qwen3_4b_bf16"]
+    assert bench.algorithmic(c1, 1, 512, 4.5, True, 152)["families"]["round_proj"][1] == 1
+    # the bytes do not depend on how the projection is launched
+    assert fam["round_proj"][0] == bench.algorithmic(serving, 64, 512, 4.5, True)["families"][
+        "round_proj"][0]
+
+
 def test_clock_summary_parses_samples(tmp_path):
     c = bench.ClockSampler(0)
     c.path = str(tmp_path / "clk.csv")
