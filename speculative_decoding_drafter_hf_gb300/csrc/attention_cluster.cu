@@ -937,9 +937,45 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     }
   }
   __syncthreads();
-  // merge the key groups per row: M = max m_k, L = sum w_k l_k, O = sum w_k O_k.
-  // First one thread per row turns each group's max into its weight w_k
-  // (in place) and keeps L (1/L when there is no cluster combine) with M.
+  __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
+  const int c = (tid % c4n) * 4, rstep = nthr / c4n;
+  if (nsplit == 1) {
+    // merge the key groups per row and write O: every thread of a row forms
+    // the groups' weights w_k = 2^(m_k - M) itself (M = max m_k), then sums
+    // its 4 columns: O = sum w_k O_k / sum w_k l_k
+    for (int r = tid / c4n; r < R; r += rstep) {
+      float mk[4], lk[4];
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        mk[k] = k < W.kg ? mlk[((size_t)k * QR + r) * 2] : -INFINITY;
+        lk[k] = k < W.kg ? mlk[((size_t)k * QR + r) * 2 + 1] : 0.f;
+        M = fmaxf(M, mk[k]);
+      }
+      float Ls = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (k >= W.kg) break;
+        const float wt = lk[k] > 0.f ? ex2_fast(mk[k] - M) : 0.f;  // an empty group weighs 0
+        Ls = fmaf(wt, lk[k], Ls);
+        const float4 ov = *reinterpret_cast<const float4*>(okg + ((size_t)k * QR + r) * OLD + c);
+        acc.x = fmaf(wt, ov.x, acc.x);
+        acc.y = fmaf(wt, ov.y, acc.y);
+        acc.z = fmaf(wt, ov.z, acc.z);
+        acc.w = fmaf(wt, ov.w, acc.w);
+      }
+      const float inv = 1.f / Ls;
+      const int g = r / S, sl = r % S;
+      __nv_bfloat16* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    }
+    return;
+  }
+  // several ranks: merge the key groups per row: M = max m_k, L = sum w_k l_k,
+  // O = sum w_k O_k. First one thread per row turns each group's max into its
+  // weight w_k (in place) and keeps L with M.
   for (int r = tid; r < R; r += nthr) {
     float M = -INFINITY;
     for (int k = 0; k < W.kg; ++k) M = fmaxf(M, mlk[((size_t)k * QR + r) * 2]);
@@ -952,12 +988,10 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
       e[0] = wt;
     }
     ml[r * 2] = M;
-    ml[r * 2 + 1] = nsplit == 1 ? 1.f / Ls : Ls;
+    ml[r * 2 + 1] = Ls;
   }
   __syncthreads();
   // then thread tid sums 4 columns (c) of rows r0, r0 + rstep, ...
-  __nv_bfloat16* mix = static_cast<__nv_bfloat16*>(a.mix);
-  const int c = (tid % c4n) * 4, rstep = nthr / c4n;
   for (int r = tid / c4n; r < R; r += rstep) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < W.kg; ++k) {
@@ -968,17 +1002,8 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
       acc.z = fmaf(wt, ov.z, acc.z);
       acc.w = fmaf(wt, ov.w, acc.w);
     }
-    if (nsplit == 1) {
-      const int g = r / S, sl = r % S;
-      const float inv = ml[r * 2 + 1];
-      __nv_bfloat16* dst = mix + (rowbase + sl) * d.Nz + (size_t)(kvh * G + g) * dh + c;
-      *reinterpret_cast<uint2*>(dst) =
-          make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-    } else {
-      *reinterpret_cast<float4*>(octa + (size_t)r * OLD + c) = acc;
-    }
+    *reinterpret_cast<float4*>(octa + (size_t)r * OLD + c) = acc;
   }
-  if (nsplit == 1) return;
   cluster_sync_all();
   // rank `rank` combines rows rank, rank + nsplit, ... over all ranks; every
   // partner's (m, l, O) is requested at once (one round trip)
