@@ -18,10 +18,12 @@
 // all partners' partials through distributed shared memory in rank order
 // (deterministic, no global round trip, no atomics).
 //
-// Memory read (same launch, the CTAs after the attention clusters):
-// y[s, h, p] = sum_n state[h, p, n] * C_s[s, n]. The state block of (b, h)
-// is read with 16-byte loads, all in flight at once, and reduced across the
-// lanes that share a state row. The state is never written here.
+// Memory read (same launch, CTAs of their own):
+// y[s, h, p] = sum_n state[h, p, n] * C_s[s, n]. On the CUDA cores (fp32
+// handles, other shapes) the state block of (b, h) is read with 16-byte
+// loads, all in flight at once, and reduced across the lanes that share a
+// state row; the bf16 form stages the heads by TMA and multiplies on the
+// tensor cores (mem_tc_cta below). The state is never written here.
 #include <mutex>
 
 #include "common.cuh"

@@ -11,11 +11,14 @@
 //  * skinny (draft / commit): A = weights [out features, K], B = the few
 //    activation rows (7 slots per request, or the accepted rows), so the
 //    weights stream through the tensor core exactly once; the epilogue maps
-//    D[m, n] to output row n, column m ("swap"). Split-K over CTAs keeps
-//    every SM streaming; partial tiles are summed by the last CTA to finish
-//    a tile, in split order (deterministic, no atomics on data, no waiting).
-//  * prefill: A = the prefix features [tokens, K], B = weight rows; output
-//    row m, column n.
+//    D[m, n] to output row n, column m ("swap").
+//  * token-major (more than 32 activation rows, prefill): A = the rows
+//    [tokens, K], B = weight rows; output row m, column n.
+// Split-K partners of one output tile form a thread-block cluster (along
+// grid x) and sum their partial tiles through distributed shared memory in
+// rank order (deterministic, no atomics on data): swap tiles by remote
+// reads of the partners' partials, token-major tiles by pushing each
+// partial chunk to the rank that owns it (remote stores, one exchange).
 //
 // Every mbarrier wait is bounded (clock-based); on expiry the CTA raises
 // ERR_TIMEOUT in the device error word, drains the copies it issued (again
