@@ -148,6 +148,116 @@ def test_serving_batch64_three_layers_subset():
     d.close()
 
 
+def subset_branches(orc, cfg, slot64, mix, subset):
+    """The last layer's attention output O and memory read y for the requests
+    the oracle follows (oracle index i = request subset[i]), against the rows
+    of those requests in the handle's DRAFT_MIX."""
+    S, QD = cfg.block, cfg.n_q_heads * cfg.head_dim
+    got_o, got_y, ref_o, ref_y = [], [], [], []
+    for i, b in enumerate(subset):
+        cur = slot64[i]
+        for lw, c in zip(orc.layers[:-1], orc.ctx[i][:-1]):
+            cur = O.draft_layer(lw, cfg, c, cur)
+        _, parts = O.draft_layer(orc.layers[-1], cfg, orc.ctx[i][-1], cur, return_parts=True)
+        rows = slice(b * S, (b + 1) * S)
+        got_o.append(mix[rows, :QD])
+        got_y.append(mix[rows, QD:])
+        ref_o.append(parts["O"].reshape(S, -1))
+        ref_y.append(parts["y"].reshape(S, -1))
+    return ((maxnorm_err(np.concatenate(got_o), np.concatenate(ref_o)),
+             maxnorm_err(np.concatenate(got_y), np.concatenate(ref_y))))
+
+
+def test_serving_batch64_round_graph_subset():
+    """hf_round at the full serving batch (64 requests, 3 layers), captured in
+    a CUDA graph over fixed staging buffers and replayed per round, as the
+    throughput measurement runs it: the commit projection grouped with the
+    first slot projection, the layer-0 memory read fused into the state walk,
+    and attention launches whose memory-read CTAs come first. The oracle
+    follows requests 0, 31 and 63 (requests are independent): their drafts,
+    the last layer's two branches, and after each round their state, ring,
+    tags and position. Prefixes are 520-1500 tokens, so every window is full,
+    as at the workload's 2K-32K prefixes (a round's work does not depend on
+    the prefix once the window is full)."""
+    import speculative_decoding_drafter_hf_gb300 as hf
+    cfg = CONFIGS["serving_qwen3_4b_b64"].replace(prefix_lo=520, prefix_hi=1500)
+    B = cfg.batch
+    weights = [make_layer_weights(cfg, l) for l in range(cfg.n_layers)]
+    d = hf.Drafter(cfg, B)
+    for l, w in enumerate(weights):
+        d.set_weights(l, w)
+    lens = make_prefix_lens(cfg)
+    assert min(lens) > cfg.window
+    feats = make_prefix_feats(cfg, lens)
+    d.prefill(feats.cuda(), lens)
+    subset = [0, 31, 63]
+    orc = O.OracleDrafter(cfg, weights, len(subset))
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    sub_feats = torch.cat([feats[starts[b]:starts[b + 1]] for b in subset])
+    orc.prefill([lens[b] for b in subset], sub_feats)
+    tol = TOL[cfg.dtype]
+
+    dt = d.torch_dtype
+    st_slot = torch.empty((B, cfg.block, cfg.d_model), dtype=dt, device="cuda")
+    st_feat = torch.empty((B, cfg.block + 1, cfg.d_model), dtype=dt, device="cuda")
+    st_cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    out = torch.empty_like(st_slot)
+
+    def stage(r):
+        slot, cf = make_round_inputs(cfg, r, B)
+        n = make_accepted(cfg, r, B)
+        st_slot.copy_(slot)
+        st_feat.copy_(cf)
+        st_cnt.copy_(n.to(torch.int32))
+        return slot, cf, n
+
+    # round 0 eagerly (as the warm-up rounds), then capture and replay
+    slot, cf, n = stage(0)
+    d.round(st_feat, st_cnt, st_slot, out)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+        d.round(st_feat, st_cnt, st_slot, out)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for r in range(3):
+        if r > 0:
+            slot, cf, n = stage(r)
+            g.replay()
+            torch.cuda.synchronize()
+        orc.commit(cf[subset], n[subset].numpy())
+        ref = orc.draft(slot[subset])
+        got = out.float().cpu().numpy()
+        for i, b in enumerate(subset):
+            e = maxnorm_err(got[b], ref[i])
+            assert e <= tol, f"round {r} request {b}: draft err {e:.3e}"
+        e_o, e_y = subset_branches(orc, cfg, O.to64(slot[subset]), d.read(Tensor.DRAFT_MIX), subset)
+        assert e_o <= tol, f"round {r}: attention branch err {e_o:.3e}"
+        assert e_y <= tol, f"round {r}: memory read branch err {e_y:.3e}"
+        offs = d.read(Tensor.OFFSETS)
+        want = np.concatenate([[0], np.cumsum(n.numpy())]).astype(np.int32)
+        assert np.array_equal(offs[:B + 1], want), f"round {r}: offsets"
+        state = d.read(Tensor.STATE)
+        pos = d.read(Tensor.POS)
+        tags = d.read(Tensor.RING_TAG)
+        rk = d.read(Tensor.RING_K)
+        for i, b in enumerate(subset):
+            c0 = orc.ctx[i][0]
+            assert pos[b] == c0.pos, f"round {r} request {b}: position"
+            assert np.array_equal(tags[b], c0.tag.astype(np.int32)), f"round {r} request {b}: tags"
+            for l in range(cfg.n_layers):
+                c = orc.ctx[i][l]
+                valid = c.tag >= 0
+                e = maxnorm_err(state[l, b], c.h)
+                assert e <= tol, f"round {r} request {b} layer {l}: state err {e:.3e}"
+                e = maxnorm_err(rk[l, b][:, valid, :], c.ring_k[:, valid, :])
+                assert e <= tol, f"round {r} request {b} layer {l}: ring K err {e:.3e}"
+    d.check_guards()
+    d.close()
+
+
 def test_prefill_sweep_128k_sampled_heads():
     """The sweep's longest prefix (128K tokens) on one request: every window
     entry, tags, position, and two memory heads against the oracle's fold."""

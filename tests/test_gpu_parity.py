@@ -501,6 +501,36 @@ def test_memory_horizon(name, batch, horizon, lens):
     p.close()
 
 
+@pytest.mark.parametrize("name,horizon,rounds,check_every", [
+    ("tiny_fp32", 20, 300, 50),        # leaving rows from the ring, ~1,300 removals per request
+    ("tiny_fp32", 3, 300, 50),         # leaving rows inside the commit, every round
+    ("qwen3_4b_bf16", 20, 120, 40),
+])
+def test_memory_horizon_no_drift_over_many_rounds(name, horizon, rounds, check_every):
+    """The GPU removes each feature leaving the horizon by subtracting its
+    decayed term from the state, while the oracle refolds the last M features
+    from zero at every commit (the plain definition): the rounding of the
+    subtractions must not build up over hundreds of rounds. Drafts, both
+    branches of the draft and the whole context are compared every
+    `check_every` rounds, with the tolerance of a single round."""
+    cfg = CONFIGS[name].replace(batch=2, prefix=100, mem_horizon=horizon)
+    p = Pair(cfg, tweak=slow_decay(-4.0), prefill_tokens_max=256)
+    lens = [5, 700]
+    p.prefill(lens, make_prefix_feats(cfg, lens))
+    for r in range(rounds):
+        slot, feats = make_round_inputs(cfg, r, p.B)
+        if (r + 1) % check_every == 0:
+            got, ref = p.draft(slot)
+            e = maxnorm_err(got, ref)
+            assert e <= p.tol, f"round {r}: draft err {e:.3e}"
+            check_mix(p, slot, f"round {r}")
+        p.commit(feats, make_accepted(cfg, r, p.B))
+        if (r + 1) % check_every == 0:
+            p.check_context(what=f"round {r}")
+    assert all(p.orc.ctx[b][0].pos >= lens[b] + rounds for b in range(p.B))
+    p.close()
+
+
 def test_memory_horizon_round_api_and_graph():
     cfg = CONFIGS["tiny_fp32"].replace(batch=3, prefix=40, mem_horizon=6, n_layers=2)
     p = Pair(cfg, tweak=slow_decay(-4.0))
