@@ -683,39 +683,66 @@ __device__ __forceinline__ void attn_tc_cta(const Args& a, const CUtensorMap* mk
     waited = true;
   };
   constexpr int c4n = DH / 4;
+  // Q rows (pre-scaled) as bf16, rows R..QR-1 zero; slot keys / values (rank
+  // 0) into rows KT..KT+15 of every tile buffer (the copies write rows
+  // 0..KT-1 only), rows past S zero (finite V for P.V). Each pass loads a
+  // thread's QU Q pieces and SU slot pieces before it converts and stores any
+  // of them, so a pass costs one L2 round trip (two passes at the serving
+  // shape instead of a round trip per piece); a slot row is loaded once
+  // for all tile buffers.
+  constexpr int QU = 2, SU = 2;
   auto stage = [&]() {
-    // Q rows (pre-scaled) as bf16; rows R..QR-1 zero.
-    for (int i = tid; i < QR * c4n; i += nthr) {
-      const int r = i / c4n, c = (i % c4n) * 4;
-      uint2 w = make_uint2(0u, 0u);
-      if (r < R) {
-        const int g = r / S, sl = r % S;
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(
-            a.proj + (rowbase + sl) * d.Nd + (size_t)(kvh * G + g) * dh + c));
-        w = make_uint2(pack_bf16x2(x.x * a.qscale, x.y * a.qscale),
-                       pack_bf16x2(x.z * a.qscale, x.w * a.qscale));
+    const int nq = QR * c4n, ns = slots ? 16 * c4n : 0;
+    for (int pass = 0; pass * nthr * QU < nq || pass * nthr * SU < ns; ++pass) {
+      float4 qx[QU], kx[SU], vx[SU];
+#pragma unroll
+      for (int u = 0; u < QU; ++u) {
+        const int i = (pass * QU + u) * nthr + tid;
+        const int r = i / c4n, c = (i % c4n) * 4;
+        qx[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < nq && r < R)
+          qx[u] = __ldcg(reinterpret_cast<const float4*>(
+              a.proj + (rowbase + r % S) * d.Nd + (size_t)(kvh * G + r / S) * dh + c));
       }
-      *reinterpret_cast<uint2*>(qt + sw_chunk(QR, r, c >> 3) + (c & 7) * 2) = w;
-    }
-    // slot keys / values (rank 0) into rows KT..KT+15 of every tile buffer
-    // (the copies write rows 0..KT-1 only); rows past S zero (finite V for P.V)
-    if (slots)
-      for (int i = tid; i < TC_STAGES * 16 * c4n; i += nthr) {
-        const int stg = i / (16 * c4n), j = (i / c4n) % 16, c = (i % c4n) * 4;
-        uint2 kw = make_uint2(0u, 0u), vw = make_uint2(0u, 0u);
-        if (j < S) {
+#pragma unroll
+      for (int u = 0; u < SU; ++u) {
+        const int i = (pass * SU + u) * nthr + tid;
+        const int j = i / c4n, c = (i % c4n) * 4;
+        kx[u] = vx[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < ns && j < S) {
           const float* row = a.proj + (rowbase + j) * d.Nd;
-          const float4 kx = __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
-          const float4 vx =
-              __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
-          kw = make_uint2(pack_bf16x2(kx.x, kx.y), pack_bf16x2(kx.z, kx.w));
-          vw = make_uint2(pack_bf16x2(vx.x, vx.y), pack_bf16x2(vx.z, vx.w));
+          kx[u] = __ldcg(reinterpret_cast<const float4*>(row + d.QD + kvh * dh + c));
+          vx[u] = __ldcg(reinterpret_cast<const float4*>(row + d.QD + d.KVD + kvh * dh + c));
         }
-        uint8_t* kd = kv + (size_t)stg * 2 * L.stage;
-        const uint32_t off = sw_chunk(KTS, KT + j, c >> 3) + (c & 7) * 2;
-        *reinterpret_cast<uint2*>(kd + off) = kw;
-        *reinterpret_cast<uint2*>(kd + L.stage + off) = vw;
       }
+#pragma unroll
+      for (int u = 0; u < QU; ++u) {
+        const int i = (pass * QU + u) * nthr + tid;
+        if (i < nq) {
+          const int r = i / c4n, c = (i % c4n) * 4;
+          const float4 x = qx[u];
+          *reinterpret_cast<uint2*>(qt + sw_chunk(QR, r, c >> 3) + (c & 7) * 2) =
+              make_uint2(pack_bf16x2(x.x * a.qscale, x.y * a.qscale),
+                         pack_bf16x2(x.z * a.qscale, x.w * a.qscale));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < SU; ++u) {
+        const int i = (pass * SU + u) * nthr + tid;
+        if (i < ns) {
+          const int j = i / c4n, c = (i % c4n) * 4;
+          const uint2 kw = make_uint2(pack_bf16x2(kx[u].x, kx[u].y), pack_bf16x2(kx[u].z, kx[u].w));
+          const uint2 vw = make_uint2(pack_bf16x2(vx[u].x, vx[u].y), pack_bf16x2(vx[u].z, vx[u].w));
+          const uint32_t off = sw_chunk(KTS, KT + j, c >> 3) + (c & 7) * 2;
+#pragma unroll
+          for (int stg = 0; stg < TC_STAGES; ++stg) {
+            uint8_t* kd = kv + (size_t)stg * 2 * L.stage;
+            *reinterpret_cast<uint2*>(kd + off) = kw;
+            *reinterpret_cast<uint2*>(kd + L.stage + off) = vw;
+          }
+        }
+      }
+    }
   };
   int nissue = 0;
   if (blind) {
