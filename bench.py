@@ -392,8 +392,13 @@ def run_reference(args, cfg):
         "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * t / max(done, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "committed_tokens_per_s": tok_rate,
-        "config": {"workload": cfg.name, "batch": batch, "prefix": cfg.prefix,
-                   "layers": cfg.n_layers, "l2": "n/a (CPU)", **ablation_config(cfg)},
+        "config": {"workload": cfg.name, "batch_per_gpu": batch,
+                   "prefix": (f"log-uniform [{cfg.prefix_lo}, {cfg.prefix_hi}]"
+                              if cfg.prefix_lo else cfg.prefix),
+                   "prefix_cap": ORACLE_PREFIX_CAP,
+                   "api": "the oracle's draft, then its commit of the round",
+                   "layers": cfg.n_layers, "window": cfg.window, "block": cfg.block,
+                   "l2": "n/a (CPU)", **ablation_config(cfg)},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
