@@ -132,3 +132,25 @@ def test_traffic_only_for_unchanged_kernels(tmp_path, monkeypatch):
         monkeypatch.setattr(bench, "kernel_sources_digest", lambda: real)
         assert bench.measured_traffic("w", "round_proj") == want
         assert bench.measured_traffic("w", "out_proj") is None
+
+
+def test_reference_arm_line(capsys):
+    """The reference arm (the float64 oracle on the host cores) prints one
+    JSON line with the GPU arm's metric, unit and workload keys, its sample
+    described as the oracle's, and an e2e entry that moves no bytes."""
+    import json
+    assert bench.main(["--impl", "reference", "--config", "tiny_fp32",
+                       "--steps", "3", "--warmup", "3"]) in (0, None)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    c = d["config"]
+    assert c["workload"] == "tiny_fp32"
+    for k in ("batch_per_gpu", "prefix", "prefix_cap", "layers", "window", "block"):
+        assert k in c
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
