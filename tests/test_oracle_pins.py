@@ -575,3 +575,73 @@ def test_q4_round_trip_error_bound():
     m.codes, m.scales, m.zeros = q, s, z
     back = O.dequantize_q4(m)
     assert np.max(np.abs(back - w) / s[g]) <= 0.5 + 1e-9
+
+
+# ---------------------------------------------------------------- brute force
+
+def _bf_project(f, W, ncol):
+    """Row f times the [len(f), ncol] matrix W, one scalar product per column."""
+    return [sum(f[i] * W[i][c] for i in range(len(f))) for c in range(ncol)]
+
+
+def test_bruteforce_sequence_on_tiny_shapes():
+    """A prefill, two commits with rejected rows and a draft on tiny shapes
+    (4 query heads over 2 KV heads, a window of 4 that the sequence wraps),
+    recomputed from the definitions with scalar Python loops — the memory
+    folded token by token (h <- exp(dt A) h + dt x B^T, dt = softplus(f W_dt
+    + bias), A = -exp(A_log)), each slot attending with scale 1/sqrt(dh)
+    over the last W committed keys and the 7 slot keys of its query head's
+    KV head, y = C h, out = X + O W_o + y W_mo — against the oracle."""
+    D, Hq, Hkv, dh, Wn, Hm, P, N, S = 8, 4, 2, 2, 4, 2, 2, 2, 7
+    cfg = small_cfg(d_model=D, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=dh, window=Wn,
+                    ssm_heads=Hm, ssm_headdim=P, d_state=N, chunk=2)
+    lw = O.Weights64.from_any(make_layer_weights(cfg, 0))
+    Wt = {k: getattr(lw, k).tolist() for k in
+          ("w_q", "w_k", "w_v", "w_o", "w_x", "w_B", "w_C", "w_dt", "w_mo")}
+    bias = lw.dt_bias.tolist()
+    A = [-math.exp(v) for v in lw.A_log.tolist()]
+    rng = np.random.default_rng(23)
+    prefix = rng.standard_normal((6, D))
+    commits = [(rng.standard_normal((8, D)), 3), (rng.standard_normal((8, D)), 1)]
+    X = rng.standard_normal((S, D))
+
+    ctx = O.prefill_layer(lw, cfg, prefix)
+    for f, n in commits:
+        ctx = O.commit_layer(lw, cfg, ctx, f, n)
+    out = O.draft_layer(lw, cfg, ctx, X)
+
+    committed = [list(r) for r in prefix] + [list(r) for f, n in commits for r in f[:n]]
+    h = [[[0.0] * N for _ in range(P)] for _ in range(Hm)]
+    for f in committed:
+        x, B = _bf_project(f, Wt["w_x"], Hm * P), _bf_project(f, Wt["w_B"], N)
+        dtr = _bf_project(f, Wt["w_dt"], Hm)
+        for m in range(Hm):
+            v = dtr[m] + bias[m]
+            dt = max(v, 0.0) + math.log1p(math.exp(-abs(v)))
+            decay = math.exp(dt * A[m])
+            for p in range(P):
+                for n in range(N):
+                    h[m][p][n] = decay * h[m][p][n] + dt * x[m * P + p] * B[n]
+    keys_from = committed[-Wn:] + [list(r) for r in X]
+    K = [_bf_project(f, Wt["w_k"], Hkv * dh) for f in keys_from]
+    V = [_bf_project(f, Wt["w_v"], Hkv * dh) for f in keys_from]
+    want = []
+    for s in range(S):
+        xs = list(X[s])
+        q = _bf_project(xs, Wt["w_q"], Hq * dh)
+        C = _bf_project(xs, Wt["w_C"], N)
+        o = [0.0] * (Hq * dh)
+        for hq in range(Hq):
+            g = hq // (Hq // Hkv)
+            sc = [sum(q[hq * dh + c] * K[j][g * dh + c] for c in range(dh)) / math.sqrt(dh)
+                  for j in range(len(K))]
+            mx = max(sc)
+            e = [math.exp(v - mx) for v in sc]
+            for c in range(dh):
+                o[hq * dh + c] = sum(e[j] * V[j][g * dh + c] for j in range(len(K))) / sum(e)
+        y = [sum(h[m][p][n] * C[n] for n in range(N)) for m in range(Hm) for p in range(P)]
+        want.append([xs[d] + sum(o[i] * Wt["w_o"][i][d] for i in range(Hq * dh))
+                     + sum(y[i] * Wt["w_mo"][i][d] for i in range(Hm * P)) for d in range(D)])
+    assert ctx.pos == len(committed) == 10
+    assert rel(ctx.h, np.array(h)) < 1e-12
+    assert rel(out, np.array(want)) < 1e-12
