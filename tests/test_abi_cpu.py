@@ -121,3 +121,50 @@ def test_block_calls_on_null_handle_are_einval(hf):
     assert B.hf_draft_tokens(None, None, None, None, 1, None) == hf.Status.EINVAL
     assert B.hf_debug_check_guards(None) == hf.Status.EINVAL
     assert B.hf_debug_fail_alloc(-1) == hf.Status.EINVAL
+
+
+# hf_attention_noalloc: a valid call (bf16, 2 requests, 4 query heads over 2
+# KV heads, head dim 64, window 64, 7 slots) and one argument changed at a
+# time; every refusal comes from the host-side checks, before any CUDA call
+# (the pointers are never dereferenced).
+_NOALLOC_OK = dict(dtype=1, batch=2, hq=4, hkv=2, dh=64, window=64, block=7, proj=16,
+                   proj_ld=512, ring_k=16, ring_v=16, pos=16, out=16, out_ld=256, status=None)
+
+
+@pytest.mark.parametrize("change,msg", [
+    (dict(dtype=5), "dtype"),
+    (dict(batch=-1), "positive"),
+    (dict(window=0), "positive"),
+    (dict(hkv=3), "divide"),
+    (dict(dh=12), "multiple of 8"),
+    (dict(dh=264, proj_ld=2112, out_ld=1056), "<= 256"),
+    (dict(block=17), "block"),
+    (dict(hq=32, hkv=1, proj_ld=4352, out_ld=2048), "block"),   # 32 heads x 7 slots > 64 rows
+    (dict(proj_ld=510), "proj_ld"),
+    (dict(proj_ld=508), "proj_ld"),
+    (dict(out_ld=255), "out_ld"),
+    (dict(proj=None), "NULL"),
+    (dict(out=None), "NULL"),
+    (dict(ring_k=8), "16-byte"),
+    (dict(proj=20), "16-byte"),
+    (dict(status=2), "4-byte"),
+    (dict(batch=4096, hq=32, hkv=8, dh=128, window=512, proj_ld=6272, out_ld=4096), "scratch"),
+])
+def test_noalloc_argument_checks_without_cuda(hf, change, msg):
+    from speculative_decoding_drafter_hf_gb300 import _binding as B
+    a = {**_NOALLOC_OK, **change}
+    s = B.hf_attention_noalloc(a["dtype"], a["batch"], a["hq"], a["hkv"], a["dh"], a["window"],
+                               a["block"], a["proj"], a["proj_ld"], a["ring_k"], a["ring_v"],
+                               a["pos"], a["out"], a["out_ld"], a["status"], None)
+    assert s == hf.Status.EINVAL
+    assert msg in B.hf_last_error(None).decode()
+
+
+def test_noalloc_empty_batch_is_ok_without_buffers(hf):
+    from speculative_decoding_drafter_hf_gb300 import _binding as B
+    a = {**_NOALLOC_OK, "batch": 0, "proj": None, "ring_k": None, "ring_v": None, "pos": None,
+         "out": None}
+    s = B.hf_attention_noalloc(a["dtype"], a["batch"], a["hq"], a["hkv"], a["dh"], a["window"],
+                               a["block"], a["proj"], a["proj_ld"], a["ring_k"], a["ring_v"],
+                               a["pos"], a["out"], a["out_ld"], a["status"], None)
+    assert s == hf.Status.OK
