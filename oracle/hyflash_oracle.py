@@ -83,9 +83,11 @@ torch's scaled_dot_product_attention when the window covers the prefix; all
 keys equal gives the mean of V; rejected rows never matter; splitting a commit
 equals one commit; ring slots match a brute-force list of the last W tokens;
 softplus matches closed values and torch; context sizing matches the pages'
-printed byte figures (tests/golden/sizing.json). No function here is "parity
-unpinned", but the layer's full output values have no printed worked example:
-they are pinned only through the pieces above.
+printed byte figures (tests/golden/sizing.json); a prefill, two commits and a
+draft on tiny shapes equal a recomputation from the definitions in scalar
+loops. No function here is "parity unpinned"; the layer's full output values
+have no printed worked example, so they are pinned by that brute force and
+through the pieces above.
 """
 from __future__ import annotations
 
